@@ -1,0 +1,175 @@
+/*
+ * mxfp4.h — C ABI of the GB300 (sm_103a) MXFP4 block-quantization library
+ * (libmxfp4_gb300.so).
+ *
+ * Format (OCP MX, MXFP4): a tensor of BF16 values is cut, along its last
+ * dimension K, into blocks of 32 consecutive elements.  Each block gets one
+ * E8M0 scale byte s (value 2^(s-127)) and 32 E2M1 codes (4 bits each:
+ * sign bit 3, magnitude index bits 2..0 over {0,0.5,1,1.5,2,3,4,6}).
+ *
+ * Sources (vLLM pull-request summary pages):
+ *   [PR43557] "Fix the E8M0 scale computation in the MXFP4 MoE CUTLASS kernel"
+ *             (vllm-project/vllm PR #43557): sections "Motivation",
+ *             "Implementation breakdown" items 1-3, "Key source snippets"
+ *             (compute_reference_e8m0_scale, untile_cutlass_scale and the
+ *             cvt_warp_fp16_to_fp4 excerpt), "Risks and impact".
+ *   [PR51038] "[Bugfix][Quantization] Fix MXFP4 conversion for FlashInfer
+ *             CUTLASS" (PR #51038): "Implementation breakdown" item 2 and the
+ *             convert_weight_to_mxfp4_moe_kernel_format / test excerpts.
+ *   [PR46915] "Fix the SM90 MXFP4 MoE test weight/scale interleave"
+ *             (PR #46915): "Motivation" (packed FP4 weights read through a
+ *             FP4->BF16 table).
+ *
+ * Common conventions of every entry point below
+ *   - Every data pointer is DEVICE memory owned by the caller.  The library
+ *     never allocates, never frees and never synchronises the host; work is
+ *     enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy
+ *     default stream) and the call returns as soon as it is enqueued.
+ *   - Host-checkable errors (shapes, NULL or misaligned pointers, overlapping
+ *     input/output ranges) are reported synchronously through the return
+ *     value, before anything is enqueued; outputs are then untouched.
+ *   - A failed kernel launch returns MXFP4_ECUDA.
+ *   - Errors only the device can see (malformed expert offsets) are written
+ *     to a caller-provided device status word.
+ *   - Size 0 (M == 0, K == 0, E == 0 with no rows) is a valid no-op.
+ *   - No kernel of this library waits on another CTA or on the host.
+ */
+#ifndef MXFP4_GB300_H
+#define MXFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes.  MXFP4_EOFFSETS is only ever written to a device status word. */
+typedef enum {
+  MXFP4_OK = 0,
+  MXFP4_EINVAL = -1,   /* NULL pointer, negative size, bad flag value            */
+  MXFP4_EALIGN = -2,   /* pointer or row stride breaks the 16-byte rule            */
+  MXFP4_ESHAPE = -3,   /* K % 32 != 0, ldx < K, odd two_n, size overflow          */
+  MXFP4_EALIAS = -4,   /* an output byte range overlaps an input or another output */
+  MXFP4_ECUDA = -5,    /* the CUDA runtime refused a launch                        */
+  MXFP4_EOFFSETS = -6  /* device-detected: expert offsets not 0 = o[0] <= ... <= o[E] = rows */
+} mxfp4_status;
+
+/* Bytes of the 128x4-tiled scale buffer of an [M, K] matrix:
+ * ceil(M/128)*128 * ceil((K/32)/4)*4.  Every byte of that range is written by
+ * the quantizers (pad bytes as 0x00).  Returns 0 when M <= 0, K <= 0 or
+ * K % 32 != 0.  [PR43557] untile_cutlass_scale (padded_M x padded_sK). */
+size_t mxfp4_scale_bytes(int64_t M, int64_t K);
+
+/* Upper bound of the grouped scale buffer for `total_rows` rows split into E
+ * segments, each padded to a multiple of 128 rows on its own:
+ * floor((total_rows + 127*E)/128) * 128 * ceil((K/32)/4)*4.
+ * Returns 0 on invalid arguments. */
+size_t mxfp4_grouped_scale_bytes_bound(int64_t total_rows, int32_t E, int64_t K);
+
+/* mxfp4_quantize — BF16 [M, K] -> packed E2M1 codes + tiled E8M0 scales.
+ *
+ * Defined by [PR43557] "Implementation breakdown" item 1 and the
+ * cvt_warp_fp16_to_fp4 excerpt (UE8M0 branch), plus the plain OCP-MX reading
+ * of the element step the pages leave implicit:
+ *   vecMax = max |x| over the 32-element block;
+ *   s = ((bits(vecMax) + 2^21) & 0xFF800000) >> 23 & 0xFF, minus 2 if that
+ *       exponent is > 2 else 0, clamped to 254; s = 0 when vecMax <= 0;
+ *   code = E2M1 round-to-nearest-even of x * 2^(127-s), saturating at +-6;
+ *   every code of a block with s == 0 is 0x0.
+ *
+ * x       BF16 bits, row r starts at x + r*ldx elements.  16-byte aligned,
+ *         ldx % 8 == 0, ldx >= K.  Read only.
+ * M, K    rows and columns; K % 32 == 0.
+ * codes   [M, K/2] bytes, row stride K/2; byte j of a row holds element 2j
+ *         in bits 0..3 and element 2j+1 in bits 4..7.  16-byte aligned.
+ * scales  mxfp4_scale_bytes(M, K) bytes, 16-byte aligned, CUTLASS 128x4
+ *         tiled layout [ceil(M/128), ceil(K/128), 32, 4, 4]: the scale of row
+ *         r, block column c sits at byte
+ *           ((r/128)*ceil(K/128) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4
+ *         ([PR43557] untile_cutlass_scale).  Rows >= M and columns >= K/32
+ *         of the padded tile are written as 0x00.
+ * Inputs containing Inf or NaN give unspecified codes (but no fault).
+ */
+int mxfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ldx,
+                   uint8_t* codes, uint8_t* scales, void* stream);
+
+/* mxfp4_quantize_grouped — per-expert ("experts quant") activation quantize.
+ *
+ * [PR43557] "Implementation breakdown" item 3 (the experts-quant tests) and
+ * item 1.  Rows [o[e], o[e+1]) of x form segment e; each segment is quantized
+ * exactly as mxfp4_quantize would quantize it alone.  Codes keep the input
+ * row order ([total_rows, K/2]).  Segment e's scales form its own tiled,
+ * zero-padded buffer of ceil(n_e/128)*128 rows, stored at byte
+ * P[e]*ceil(K/128)*4 of `scales`, where P[e] = sum_{e'<e} ceil(n_e'/128)*128.
+ *
+ * x                  BF16 [total_rows, K], contiguous (row stride K), 16-byte aligned.
+ * expert_offsets     DEVICE int32 [E+1]; must satisfy 0 = o[0] <= o[1] <= ...
+ *                    <= o[E] = total_rows (checked on the device).
+ * codes              [total_rows, K/2], 16-byte aligned.
+ * scales             >= mxfp4_grouped_scale_bytes_bound(total_rows, E, K)
+ *                    bytes, 16-byte aligned.  Bytes past P[E]*ceil(K/128)*4
+ *                    are not touched.
+ * scale_row_offsets  DEVICE int32 [E+1], output: P[0..E] (padded row starts).
+ * status             DEVICE int32, output, may be NULL: MXFP4_OK, or
+ *                    MXFP4_EOFFSETS when the offsets break the rule above;
+ *                    in that case scale_row_offsets is filled with -1 and
+ *                    codes/scales are left untouched.
+ */
+int mxfp4_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
+                           const int32_t* expert_offsets, int32_t E,
+                           uint8_t* codes, uint8_t* scales,
+                           int32_t* scale_row_offsets, int32_t* status,
+                           void* stream);
+
+/* mxfp4_dequantize — packed codes + tiled scales -> BF16 [M, K].
+ *
+ * The inverse mapping of the format ([PR46915] "Motivation": FP4 -> BF16
+ * table; [PR43557] cvt_warp_fp16_to_fp4 excerpt: scale value 2^(s-127)):
+ *   y = BF16_RNE(e2m1(code) * 2^(s-127)); overflow gives +-Inf, code 0x8
+ *   gives -0.0, s == 255 (E8M0 NaN) gives 0x7FC0 for the whole block.
+ *
+ * codes   [M, K/2], layout as written by mxfp4_quantize, 16-byte aligned.
+ * scales  mxfp4_scale_bytes(M, K) bytes, tiled layout, 16-byte aligned.
+ * y       BF16 [M, K], contiguous, 16-byte aligned, written.
+ */
+int mxfp4_dequantize(const uint8_t* codes, const uint8_t* scales,
+                     int64_t M, int64_t K, void* y, void* stream);
+
+/* mxfp4_swap_w13 — fused gate/up weights [w1; w3] -> [w3; w1].
+ *
+ * [PR51038] "Implementation breakdown" item 2 and the
+ * convert_weight_to_mxfp4_moe_kernel_format branch / its test: per expert,
+ * rows [0, N) and [N, 2N) of the w13 codes and scales change places
+ * (out row r = in row (r + N) mod 2N); the w13 bias halves change places the
+ * same way and are cast FP32 -> BF16 (RNE); the w2 bias is only cast.
+ *
+ * codes_in/out   [E, two_n, K/2] bytes, 16-byte aligned.
+ * scales_in/out  scales_tiled == 0: flat [E, two_n, K/32] bytes;
+ *                scales_tiled == 1: E consecutive tiled buffers of
+ *                mxfp4_scale_bytes(two_n, K) bytes each (rows are swapped by
+ *                logical row; pad bytes are written 0x00).  16-byte aligned.
+ * w13_bias_in    FP32 [E, two_n] or NULL (then w13_bias_out is ignored).
+ * w13_bias_out   BF16 [E, two_n].
+ * w2_bias_in     FP32 [w2_bias_numel] or NULL (then w2_bias_out is ignored).
+ * w2_bias_out    BF16 [w2_bias_numel].
+ * two_n must be even, K % 32 == 0.  Out-of-place only (MXFP4_EALIAS if any
+ * output range overlaps an input range).
+ */
+int mxfp4_swap_w13(const uint8_t* codes_in, const uint8_t* scales_in,
+                   const float* w13_bias_in, int32_t E, int64_t two_n, int64_t K,
+                   int32_t scales_tiled, uint8_t* codes_out, uint8_t* scales_out,
+                   void* w13_bias_out, const float* w2_bias_in,
+                   int64_t w2_bias_numel, void* w2_bias_out, void* stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char* mxfp4_status_string(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int mxfp4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_GB300_H */

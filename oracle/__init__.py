@@ -1,0 +1,271 @@
+"""CPU oracle of MXFP4 block quantization — TEST INFRASTRUCTURE ONLY.
+
+Plain, slow, single-threaded C (``mxfp4_oracle.c``) behind numpy wrappers.
+Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package; the GPU library never does, and the two
+share no code.  Each wrapper names the step of the method it runs; the C file
+cites the pages for every step.
+
+Pins: see the CPU tests (``tests/test_oracle_*.py``).  The relative-L2 and
+saturation reports computed from oracle outputs have no independent pin
+(parity unpinned).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_i64 = ctypes.c_int64
+
+
+def lib():
+    """Load (building first if needed) the oracle shared library."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        L.orc_bf16_to_double.restype = ctypes.c_double
+        L.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+        L.orc_double_to_bf16_rne.restype = ctypes.c_uint16
+        L.orc_double_to_bf16_rne.argtypes = [ctypes.c_double]
+        L.orc_block_absmax.restype = ctypes.c_float
+        L.orc_block_absmax.argtypes = [_u16p, _i64]
+        L.orc_e8m0_scale.restype = ctypes.c_uint8
+        L.orc_e8m0_scale.argtypes = [ctypes.c_float]
+        L.orc_e2m1_encode.restype = ctypes.c_uint8
+        L.orc_e2m1_encode.argtypes = [ctypes.c_uint16, ctypes.c_uint8]
+        L.orc_e2m1_decode.restype = ctypes.c_double
+        L.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+        L.orc_e8m0_scale_many.restype = None
+        L.orc_e8m0_scale_many.argtypes = [_u16p, _i64, _u8p]
+        L.orc_e2m1_encode_many.restype = None
+        L.orc_e2m1_encode_many.argtypes = [_u16p, _i64, ctypes.c_uint8, _u8p]
+        L.orc_dequant_value_many.restype = None
+        L.orc_dequant_value_many.argtypes = [_u8p, _u8p, _i64, _u16p]
+        L.orc_scale_bytes.restype = ctypes.c_size_t
+        L.orc_scale_bytes.argtypes = [_i64, _i64]
+        L.orc_quantize_flat.restype = None
+        L.orc_quantize_flat.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p]
+        L.orc_tile_scales.restype = None
+        L.orc_tile_scales.argtypes = [_u8p, _i64, _i64, _u8p]
+        L.orc_untile_scales.restype = None
+        L.orc_untile_scales.argtypes = [_u8p, _i64, _i64, _u8p]
+        L.orc_quantize.restype = None
+        L.orc_quantize.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p]
+        L.orc_quantize_grouped.restype = ctypes.c_int
+        L.orc_quantize_grouped.argtypes = [_u16p, _i64, _i64, _i32p, ctypes.c_int32,
+                                           _u8p, _u8p, _i32p]
+        L.orc_dequantize.restype = None
+        L.orc_dequantize.argtypes = [_u8p, _u8p, _i64, _i64, _u16p]
+        L.orc_swap_halves.restype = None
+        L.orc_swap_halves.argtypes = [_u8p, _u8p, _i64, _i64, _i64]
+        L.orc_swap_bias_bf16.restype = None
+        L.orc_swap_bias_bf16.argtypes = [_f32p, _u16p, _i64, _i64]
+        L.orc_cast_bf16.restype = None
+        L.orc_cast_bf16.argtypes = [_f32p, _u16p, _i64]
+        L.orc_swap_w13.restype = None
+        L.orc_swap_w13.argtypes = [_u8p, _u8p, _f32p, ctypes.c_int32, _i64, _i64,
+                                   ctypes.c_int32, _u8p, _u8p, _u16p, _f32p, _i64, _u16p]
+        _lib = L
+    return _lib
+
+
+def _p(a, t):
+    return a.ctypes.data_as(t) if a is not None else None
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ----------------------------------------------------------------- scalars
+def bf16_to_double(b: int) -> float:
+    return lib().orc_bf16_to_double(int(b))
+
+
+def double_to_bf16(d: float) -> int:
+    """Round a double to the nearest BF16 (ties to even); returns the bits."""
+    return int(lib().orc_double_to_bf16_rne(float(d)))
+
+
+def e8m0_scale(vecmax: float) -> int:
+    """Step 2: scale exponent of a block whose absmax is ``vecmax`` (float32)."""
+    return int(lib().orc_e8m0_scale(float(np.float32(vecmax))))
+
+
+def e2m1_encode(xbits: int, s: int) -> int:
+    """Step 3: nibble of one BF16 element under scale exponent ``s``."""
+    return int(lib().orc_e2m1_encode(int(xbits), int(s)))
+
+
+def e2m1_decode(nib: int) -> float:
+    return lib().orc_e2m1_decode(int(nib))
+
+
+def scale_bytes(M: int, K: int) -> int:
+    return int(lib().orc_scale_bytes(int(M), int(K)))
+
+
+# ----------------------------------------------------------------- vectors
+def e8m0_scale_many(vbits: np.ndarray) -> np.ndarray:
+    """Step 2 over BF16 bit patterns taken as vecMax."""
+    v = _c(vbits, np.uint16).ravel()
+    s = np.empty(v.size, np.uint8)
+    lib().orc_e8m0_scale_many(_p(v, _u16p), v.size, _p(s, _u8p))
+    return s
+
+
+def e2m1_encode_many(xbits: np.ndarray, s: int) -> np.ndarray:
+    """Step 3 over many BF16 elements sharing scale exponent ``s``."""
+    x = _c(xbits, np.uint16).ravel()
+    out = np.empty(x.size, np.uint8)
+    lib().orc_e2m1_encode_many(_p(x, _u16p), x.size, int(s), _p(out, _u8p))
+    return out
+
+
+def dequant_value_many(nib: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """Step 7 per element: BF16 bits of e2m1(nib) * 2^(s-127)."""
+    n = _c(nib, np.uint8).ravel()
+    sc = _c(np.broadcast_to(s, n.shape), np.uint8).ravel()
+    y = np.empty(n.size, np.uint16)
+    lib().orc_dequant_value_many(_p(n, _u8p), _p(sc, _u8p), n.size, _p(y, _u16p))
+    return y
+
+
+# ---------------------------------------------------------------- matrices
+def quantize_flat(xbits: np.ndarray):
+    """Steps 1-4: (codes [M, K/2], flat scales [M, K/32]) of a BF16 [M, K]."""
+    x = _c(xbits, np.uint16)
+    M, K = x.shape
+    codes = np.zeros((M, K // 2), np.uint8)
+    flat = np.zeros((M, K // 32), np.uint8)
+    if M and K:
+        lib().orc_quantize_flat(_p(x, _u16p), M, K, K, _p(codes, _u8p), _p(flat, _u8p))
+    return codes, flat
+
+
+def tile(flat: np.ndarray) -> np.ndarray:
+    """Step 5: flat [M, sK] scales -> tiled bytes (zero padding)."""
+    f = _c(flat, np.uint8)
+    M, sK = f.shape
+    out = np.zeros(scale_bytes(M, sK * 32), np.uint8)
+    if out.size:
+        lib().orc_tile_scales(_p(f, _u8p), M, sK, _p(out, _u8p))
+    return out
+
+
+def untile(tiled: np.ndarray, M: int, sK: int) -> np.ndarray:
+    """Inverse of step 5: tiled bytes -> flat [M, sK]."""
+    t = _c(tiled, np.uint8).ravel()
+    out = np.zeros((M, sK), np.uint8)
+    if M and sK:
+        lib().orc_untile_scales(_p(t, _u8p), M, sK, _p(out, _u8p))
+    return out
+
+
+def quantize(xbits: np.ndarray):
+    """Steps 1-5: (codes [M, K/2], tiled scales) of a BF16 [M, K] (bits)."""
+    x = _c(xbits, np.uint16)
+    M, K = x.shape
+    codes = np.zeros((M, K // 2), np.uint8)
+    scales = np.zeros(scale_bytes(M, K), np.uint8)
+    if M and K:
+        lib().orc_quantize(_p(x, _u16p), M, K, K, _p(codes, _u8p), _p(scales, _u8p))
+    return codes, scales
+
+
+def grouped_scale_bytes_bound(total_rows: int, E: int, K: int) -> int:
+    tiles = (total_rows + 127 * E) // 128
+    return tiles * 128 * ((K // 32 + 3) // 4 * 4)
+
+
+def quantize_grouped(xbits: np.ndarray, offsets: np.ndarray):
+    """Step 6: (rc, codes, scales, scale_row_offsets); rc is 0 or -6."""
+    x = _c(xbits, np.uint16)
+    off = _c(offsets, np.int32)
+    total, K = x.shape
+    E = off.size - 1
+    codes = np.zeros((total, K // 2), np.uint8)
+    scales = np.zeros(max(grouped_scale_bytes_bound(total, E, K), 1), np.uint8)
+    sro = np.zeros(E + 1, np.int32)
+    rc = lib().orc_quantize_grouped(_p(x, _u16p), total, K, _p(off, _i32p), E,
+                                    _p(codes, _u8p), _p(scales, _u8p), _p(sro, _i32p))
+    return rc, codes, scales, sro
+
+
+def dequantize(codes: np.ndarray, tiled: np.ndarray, M: int, K: int) -> np.ndarray:
+    """Step 7: BF16 bits [M, K] from codes and tiled scales."""
+    c = _c(codes, np.uint8)
+    t = _c(tiled, np.uint8).ravel()
+    y = np.zeros((M, K), np.uint16)
+    if M and K:
+        lib().orc_dequantize(_p(c, _u8p), _p(t, _u8p), M, K, _p(y, _u16p))
+    return y
+
+
+def swap_halves(a: np.ndarray) -> np.ndarray:
+    """Step 8 on bytes: a [E, 2N, row_bytes] uint8 -> rows (r + N) mod 2N."""
+    x = _c(a, np.uint8)
+    E, two_n, rb = x.shape
+    out = np.zeros_like(x)
+    lib().orc_swap_halves(_p(x, _u8p), _p(out, _u8p), E, two_n, rb)
+    return out
+
+
+def swap_bias_bf16(b: np.ndarray) -> np.ndarray:
+    """Step 8 on a w13 bias [E, 2N] FP32 -> [b3, b1] as BF16 bits."""
+    x = _c(b, np.float32)
+    E, two_n = x.shape
+    out = np.zeros(x.shape, np.uint16)
+    lib().orc_swap_bias_bf16(_p(x, _f32p), _p(out, _u16p), E, two_n)
+    return out
+
+
+def cast_bf16(b: np.ndarray) -> np.ndarray:
+    """FP32 -> BF16 bits (round to nearest, ties to even)."""
+    x = _c(b, np.float32)
+    out = np.zeros(x.shape, np.uint16)
+    lib().orc_cast_bf16(_p(x, _f32p), _p(out, _u16p), x.size)
+    return out
+
+
+def swap_w13(codes, scales, w13_bias, E, two_n, K, scales_tiled, w2_bias=None):
+    """Step 8: (codes_out, scales_out, w13_bias_bf16 | None, w2_bias_bf16 | None)."""
+    c = _c(codes, np.uint8)
+    s = _c(scales, np.uint8)
+    b13 = _c(w13_bias, np.float32) if w13_bias is not None else None
+    b2 = _c(w2_bias, np.float32) if w2_bias is not None else None
+    c_out = np.zeros_like(c)
+    s_out = np.zeros_like(s)
+    b13_out = np.zeros(b13.shape, np.uint16) if b13 is not None else None
+    b2_out = np.zeros(b2.shape, np.uint16) if b2 is not None else None
+    lib().orc_swap_w13(_p(c, _u8p), _p(s, _u8p), _p(b13, _f32p), E, two_n, K,
+                       int(scales_tiled), _p(c_out, _u8p), _p(s_out, _u8p),
+                       _p(b13_out, _u16p), _p(b2, _f32p),
+                       b2.size if b2 is not None else 0, _p(b2_out, _u16p))
+    return c_out, s_out, b13_out, b2_out
+
+
+def quantize_rows_into(xbits: np.ndarray, row0: int, row1: int, codes: np.ndarray,
+                       scales: np.ndarray) -> None:
+    """Step 1-5 over rows [row0, row1) of a full matrix, writing into the full
+    outputs (row0 must be a multiple of 128).  Lets the CPU baseline spread the
+    unchanged single-threaded routine over several host threads."""
+    x = xbits
+    M, K = x.shape
+    assert row0 % 128 == 0 and x.flags.c_contiguous
+    n_k_tiles = (K // 32 + 3) // 4
+    xs = x[row0:row1]
+    cs = codes[row0:row1]
+    off = (row0 // 128) * n_k_tiles * 512
+    lib().orc_quantize(xs.ctypes.data_as(_u16p), row1 - row0, K, K,
+                       cs.ctypes.data_as(_u8p),
+                       scales[off:].ctypes.data_as(_u8p))

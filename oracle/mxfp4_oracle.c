@@ -1,0 +1,305 @@
+/*
+ * mxfp4_oracle.c — plain single-threaded CPU oracle of MXFP4 block
+ * quantization.  TEST INFRASTRUCTURE ONLY (tests, smoke check, the CPU
+ * baseline of the benchmark); the GPU library never uses it.  Written for a
+ * reader checking it against the pages by eye: no blocking, no fusion, one
+ * step per function, doubles wherever the value is exact.
+ *
+ * Sources: see mxfp4_oracle.h ([PR43557], [PR51038], [PR46915]).
+ */
+#include "mxfp4_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------------- */
+/* BF16 helpers (IEEE binary32 with the low 16 mantissa bits dropped).     */
+
+double orc_bf16_to_double(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+uint16_t orc_double_to_bf16_rne(double d) {
+  uint16_t sign = signbit(d) ? 0x8000u : 0u;
+  double a = fabs(d);
+  if (isnan(d)) return (uint16_t)(sign | 0x7FC0u);
+  if (a == 0.0) return sign;
+  if (isinf(d)) return (uint16_t)(sign | 0x7F80u);
+  /* Quantum (spacing of BF16 values) around a: 2^-133 in the subnormal
+   * range, else 2^(e-7) with e = floor(log2 a). */
+  int e;
+  frexp(a, &e); /* a = f * 2^e, f in [0.5, 1)  ->  floor(log2 a) = e - 1 */
+  int exp2 = e - 1;
+  int qexp = (exp2 < -126) ? -133 : exp2 - 7;
+  double n = nearbyint(ldexp(a, -qexp)); /* ties to even (default mode) */
+  double r = ldexp(n, qexp);
+  if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80u);
+  if (r < ldexp(1.0, -126)) return (uint16_t)(sign | (uint16_t)n); /* subnormal */
+  frexp(r, &e);
+  int rexp = e - 1;                                  /* r in [2^rexp, 2^(rexp+1)) */
+  uint32_t mant = (uint32_t)(ldexp(r, -rexp) * 128.0 - 128.0);
+  return (uint16_t)(sign | ((uint32_t)(rexp + 127) << 7) | mant);
+}
+
+static float bf16_to_float(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Step 1 — block absmax.  [PR43557] cvt_warp_fp16_to_fp4 excerpt: vecMax is
+ * the block's largest magnitude, taken as a float.  |x| clears the sign bit;
+ * a max involves no rounding. */
+float orc_block_absmax(const uint16_t* x, int64_t n) {
+  float v = 0.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    float a = bf16_to_float((uint16_t)(x[i] & 0x7FFFu));
+    if (a > v) v = a;
+  }
+  return v;
+}
+
+/* Step 2 — E8M0 scale.  [PR43557] "Implementation breakdown" item 1 and the
+ * UE8M0 branch of the cvt_warp_fp16_to_fp4 excerpt (also its Python form,
+ * compute_reference_e8m0_scale): round the mantissa of vecMax up when it is
+ * >= 0.75 by adding 2^21 to its IEEE-754 bits, keep the sign+exponent field,
+ * take the biased exponent, subtract 2 (never below 0), cap at 254.  A block
+ * whose max is <= 0 gets 0. */
+uint8_t orc_e8m0_scale(float vecmax) {
+  if (vecmax <= 0.0f) return 0;
+  uint32_t bits;
+  memcpy(&bits, &vecmax, sizeof bits);
+  uint32_t rounded = (bits + (1u << 21)) & 0xFF800000u; /* 32-bit wraparound */
+  uint32_t biased_exp = (rounded >> 23) & 0xFFu;
+  uint32_t s = (biased_exp > 2u) ? biased_exp - 2u : 0u;
+  if (s > 254u) s = 254u;
+  return (uint8_t)s;
+}
+
+/* Step 3 — one element.  The pages fix only the E2M1 range (largest
+ * magnitude 6.0, [PR43557] "Motivation") and the scale value 2^(s-127)
+ * (the SFValue line of the excerpt).  Plain OCP-MX reading: divide by the
+ * scale (an exact power of two), round the magnitude to the nearest of
+ * {0, 0.5, 1, 1.5, 2, 3, 4, 6}, ties to the value with an even mantissa bit
+ * (the even index), anything above 6 stays 6 (saturation); keep the sign
+ * (so -0.0 and small negatives give 0x8).  Blocks with s == 0 emit 0x0 for
+ * every element (the convention fixed for this library). */
+uint8_t orc_e2m1_encode(uint16_t xbits, uint8_t s) {
+  if (s == 0) return 0;
+  double x = orc_bf16_to_double(xbits);
+  double y = ldexp(x, 127 - (int)s); /* x / 2^(s-127), exact */
+  double m = fabs(y);
+  uint8_t sign = (uint8_t)((xbits >> 15) & 1u);
+  uint8_t idx;
+  /* midpoints 0.25 0.75 1.25 1.75 2.5 3.5 5; at a tie the even index wins */
+  if (m <= 0.25) idx = 0;        /* 0.25 ties 0 (idx 0) / 0.5 (idx 1)   */
+  else if (m < 0.75) idx = 1;    /* 0.75 ties 0.5 (1) / 1.0 (2)         */
+  else if (m <= 1.25) idx = 2;   /* 1.25 ties 1.0 (2) / 1.5 (3)         */
+  else if (m < 1.75) idx = 3;    /* 1.75 ties 1.5 (3) / 2.0 (4)         */
+  else if (m <= 2.5) idx = 4;    /* 2.5  ties 2.0 (4) / 3.0 (5)         */
+  else if (m < 3.5) idx = 5;     /* 3.5  ties 3.0 (5) / 4.0 (6)         */
+  else if (m <= 5.0) idx = 6;    /* 5.0  ties 4.0 (6) / 6.0 (7)         */
+  else idx = 7;                  /* (5, inf): 6.0, saturating           */
+  return (uint8_t)((sign << 3) | idx);
+}
+
+/* E2M1 decode (OCP MX): bit 3 sign, bits 2..1 exponent (bias 1), bit 0
+ * mantissa; exponent 0 is subnormal (0.5 * mantissa). */
+double orc_e2m1_decode(uint8_t nib) {
+  int sign = (nib >> 3) & 1;
+  int e = (nib >> 1) & 3;
+  int m = nib & 1;
+  double mag = (e == 0) ? 0.5 * m : (1.0 + 0.5 * m) * ldexp(1.0, e - 1);
+  return sign ? -mag : mag;
+}
+
+void orc_e8m0_scale_many(const uint16_t* vbits, int64_t n, uint8_t* s) {
+  for (int64_t i = 0; i < n; ++i) s[i] = orc_e8m0_scale(bf16_to_float(vbits[i]));
+}
+
+void orc_e2m1_encode_many(const uint16_t* x, int64_t n, uint8_t s, uint8_t* nib) {
+  for (int64_t i = 0; i < n; ++i) nib[i] = orc_e2m1_encode(x[i], s);
+}
+
+/* Step 7 for one element: E2M1 value times the E8M0 value 2^(s-127), rounded
+ * once to BF16; s == 255 is the E8M0 NaN. */
+static uint16_t dequant_value(uint8_t nib, uint8_t s) {
+  if (s == 255) return 0x7FC0u;
+  double v = orc_e2m1_decode(nib) * ldexp(1.0, (int)s - 127);
+  return orc_double_to_bf16_rne(v);
+}
+
+void orc_dequant_value_many(const uint8_t* nib, const uint8_t* s, int64_t n, uint16_t* y) {
+  for (int64_t i = 0; i < n; ++i) y[i] = dequant_value(nib[i], s[i]);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Matrices.                                                               */
+
+size_t orc_scale_bytes(int64_t M, int64_t K) {
+  if (M <= 0 || K <= 0 || K % 32 != 0) return 0;
+  int64_t sK = K / 32;
+  int64_t padded_M = (M + 127) / 128 * 128;
+  int64_t padded_sK = (sK + 3) / 4 * 4;
+  return (size_t)(padded_M * padded_sK);
+}
+
+/* Steps 1-4 row by row, block by block: absmax, scale, 32 nibbles, then two
+ * nibbles per byte with element 2j in the low half. */
+void orc_quantize_flat(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                       uint8_t* codes, uint8_t* flat_scales) {
+  int64_t sK = K / 32;
+  for (int64_t r = 0; r < M; ++r) {
+    const uint16_t* row = x + r * ldx;
+    for (int64_t b = 0; b < sK; ++b) {
+      const uint16_t* blk = row + b * 32;
+      uint8_t s = orc_e8m0_scale(orc_block_absmax(blk, 32));
+      flat_scales[r * sK + b] = s;
+      uint8_t nib[32];
+      for (int i = 0; i < 32; ++i) nib[i] = orc_e2m1_encode(blk[i], s);
+      for (int j = 0; j < 16; ++j)
+        codes[r * (K / 2) + b * 16 + j] = (uint8_t)(nib[2 * j] | (nib[2 * j + 1] << 4));
+    }
+  }
+}
+
+/* Step 5 — CUTLASS 128x4 tiled scale layout.  [PR43557] untile_cutlass_scale:
+ * the tiled bytes are viewed as [numMTiles, numKTiles, 32, 4, 4] and
+ * permuted (0,3,2,1,4) back to [padded_M, padded_sK]; hence flat element
+ * (r, c) lives at tiled index [r/128, c/4, r%32, (r%128)/32, c%4].  Bytes
+ * outside [M, sK] but inside the padded extent are 0 (padding value: the
+ * pages show the extent only; zero is this library's convention). */
+static int64_t tiled_index(int64_t r, int64_t c, int64_t num_k_tiles) {
+  int64_t m_tile = r / 128, k_tile = c / 4;
+  int64_t outer_m = r % 32, inner_m = (r % 128) / 32, inner_k = c % 4;
+  return (((m_tile * num_k_tiles + k_tile) * 32 + outer_m) * 4 + inner_m) * 4 + inner_k;
+}
+
+void orc_tile_scales(const uint8_t* flat, int64_t M, int64_t sK, uint8_t* tiled) {
+  int64_t padded_M = (M + 127) / 128 * 128;
+  int64_t num_k_tiles = (sK + 3) / 4;
+  int64_t padded_sK = num_k_tiles * 4;
+  for (int64_t r = 0; r < padded_M; ++r)
+    for (int64_t c = 0; c < padded_sK; ++c)
+      tiled[tiled_index(r, c, num_k_tiles)] = (r < M && c < sK) ? flat[r * sK + c] : 0;
+}
+
+void orc_untile_scales(const uint8_t* tiled, int64_t M, int64_t sK, uint8_t* flat) {
+  int64_t num_k_tiles = (sK + 3) / 4;
+  for (int64_t r = 0; r < M; ++r)
+    for (int64_t c = 0; c < sK; ++c) flat[r * sK + c] = tiled[tiled_index(r, c, num_k_tiles)];
+}
+
+void orc_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                  uint8_t* codes, uint8_t* tiled_scales) {
+  int64_t sK = K / 32;
+  if (M <= 0 || sK <= 0) return;
+  uint8_t* flat = (uint8_t*)calloc((size_t)(M * sK), 1);
+  orc_quantize_flat(x, M, K, ldx, codes, flat);
+  orc_tile_scales(flat, M, sK, tiled_scales);
+  free(flat);
+}
+
+/* Step 6 — per-expert ("experts quant") segments.  [PR43557] "Implementation
+ * breakdown" item 3 tests the experts-quant kernel per block after untiling;
+ * this library's reading: every segment [o[e], o[e+1]) is quantized as its
+ * own matrix, codes keep the row order, and segment e's tiled scales (padded
+ * to a multiple of 128 rows by itself) start at padded row P[e]. */
+int orc_quantize_grouped(const uint16_t* x, int64_t total_rows, int64_t K,
+                         const int32_t* offsets, int32_t E, uint8_t* codes,
+                         uint8_t* scales, int32_t* scale_row_offsets) {
+  int ok = (E >= 0) && offsets[0] == 0 && (int64_t)offsets[E] == total_rows;
+  for (int32_t e = 0; ok && e < E; ++e) ok = offsets[e] <= offsets[e + 1];
+  if (!ok) {
+    for (int32_t e = 0; e <= E; ++e) scale_row_offsets[e] = -1;
+    return -6;
+  }
+  int64_t sK = K / 32;
+  int64_t padded_sK = (sK + 3) / 4 * 4;
+  int64_t P = 0;
+  for (int32_t e = 0; e < E; ++e) {
+    int64_t n = (int64_t)offsets[e + 1] - offsets[e];
+    scale_row_offsets[e] = (int32_t)P;
+    orc_quantize(x + (int64_t)offsets[e] * K, n, K, K, codes + (int64_t)offsets[e] * (K / 2),
+                 scales + P * padded_sK);
+    P += (n + 127) / 128 * 128;
+  }
+  scale_row_offsets[E] = (int32_t)P;
+  return 0;
+}
+
+/* Step 7 — dequantize: for each element, its nibble and its block's scale
+ * byte (read back through the tiled layout) give E2M1 value * 2^(s-127),
+ * rounded once to BF16.  [PR46915] "Motivation" (FP4 -> BF16 table);
+ * [PR43557] excerpt (scale value from the exponent bits). */
+void orc_dequantize(const uint8_t* codes, const uint8_t* tiled_scales,
+                    int64_t M, int64_t K, uint16_t* y) {
+  int64_t sK = K / 32;
+  if (M <= 0 || sK <= 0) return;
+  uint8_t* flat = (uint8_t*)calloc((size_t)(M * sK), 1);
+  orc_untile_scales(tiled_scales, M, sK, flat);
+  for (int64_t r = 0; r < M; ++r)
+    for (int64_t k = 0; k < K; ++k) {
+      uint8_t byte = codes[r * (K / 2) + k / 2];
+      uint8_t nib = (k % 2 == 0) ? (byte & 0xFu) : (byte >> 4);
+      y[r * K + k] = dequant_value(nib, flat[r * sK + k / 32]);
+    }
+  free(flat);
+}
+
+/* Step 8 — [w1; w3] -> [w3; w1].  [PR51038] "Implementation breakdown"
+ * item 2 and the convert_weight_to_mxfp4_moe_kernel_format branch: the two
+ * halves of dim 1 (2N rows per expert) of the w13 codes and scales change
+ * places; the w13 bias is cut in two along its last dim, re-joined as
+ * [b3, b1] and cast to BF16; the w2 bias is only cast to BF16.  Tiled scales
+ * are swapped by logical row: untile, swap, tile. */
+void orc_swap_halves(const uint8_t* in, uint8_t* out, int64_t E, int64_t two_n,
+                     int64_t row_bytes) {
+  int64_t n = two_n / 2;
+  for (int64_t e = 0; e < E; ++e)
+    for (int64_t r = 0; r < two_n; ++r)
+      memcpy(out + (e * two_n + r) * row_bytes, in + (e * two_n + (r + n) % two_n) * row_bytes,
+             (size_t)row_bytes);
+}
+
+void orc_swap_bias_bf16(const float* in, uint16_t* out, int64_t E, int64_t two_n) {
+  int64_t n = two_n / 2;
+  for (int64_t e = 0; e < E; ++e)
+    for (int64_t j = 0; j < two_n; ++j) /* [b1, b3] -> [b3, b1], then BF16 */
+      out[e * two_n + j] = orc_double_to_bf16_rne((double)in[e * two_n + (j + n) % two_n]);
+}
+
+void orc_cast_bf16(const float* in, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_double_to_bf16_rne((double)in[i]);
+}
+
+void orc_swap_w13(const uint8_t* codes_in, const uint8_t* scales_in,
+                  const float* w13_bias_in, int32_t E, int64_t two_n, int64_t K,
+                  int32_t scales_tiled, uint8_t* codes_out, uint8_t* scales_out,
+                  uint16_t* w13_bias_out, const float* w2_bias_in,
+                  int64_t w2_bias_numel, uint16_t* w2_bias_out) {
+  int64_t sK = K / 32;
+  size_t tiled_bytes = orc_scale_bytes(two_n, K);
+  orc_swap_halves(codes_in, codes_out, E, two_n, K / 2);
+  if (scales_tiled) {
+    uint8_t* flat_in = (uint8_t*)calloc((size_t)(two_n * sK) + 1, 1);
+    uint8_t* flat_out = (uint8_t*)calloc((size_t)(two_n * sK) + 1, 1);
+    for (int32_t e = 0; e < E; ++e) {
+      orc_untile_scales(scales_in + e * tiled_bytes, two_n, sK, flat_in);
+      orc_swap_halves(flat_in, flat_out, 1, two_n, sK);
+      orc_tile_scales(flat_out, two_n, sK, scales_out + e * tiled_bytes);
+    }
+    free(flat_in);
+    free(flat_out);
+  } else {
+    orc_swap_halves(scales_in, scales_out, E, two_n, sK);
+  }
+  if (w13_bias_in) orc_swap_bias_bf16(w13_bias_in, w13_bias_out, E, two_n);
+  if (w2_bias_in) orc_cast_bf16(w2_bias_in, w2_bias_out, w2_bias_numel);
+}
