@@ -1,0 +1,231 @@
+"""GB300 (sm_103a) MXFP4 block quantization.
+
+Thin Python binding of ``libmxfp4_gb300.so`` (C ABI declared in
+``include/mxfp4.h``).  The functions named ``mxfp4_*`` mirror the C entry
+points one to one and only marshal arguments (device pointers, sizes, the
+current CUDA stream); every step of the computation runs in the library's
+CUDA kernels.  ``quantize``, ``quantize_grouped``, ``dequantize`` and
+``swap_w13`` are conveniences that allocate the outputs with torch and call
+the matching entry point.  PyTorch supplies device memory and streams only.
+
+There is no CPU path: importing this package fails when the library has not
+been built (``python -m mxfp4_block_quantization_gb300._build``), and every
+call rejects tensors that are not on a CUDA device.
+
+Method sources (vLLM pull-request summary pages): PR #43557 "Fix the E8M0
+scale computation in the MXFP4 MoE CUTLASS kernel" (scale rule, tiled scale
+layout, experts quant); PR #51038 "[Bugfix][Quantization] Fix MXFP4
+conversion for FlashInfer CUTLASS" ([w1; w3] -> [w3; w1] swap, BF16 bias);
+PR #46915 "Fix the SM90 MXFP4 MoE test weight/scale interleave" (FP4 -> BF16
+table read back).
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MXFP4Error", "LIB_PATH", "mxfp4_scale_bytes", "mxfp4_grouped_scale_bytes_bound",
+    "mxfp4_quantize", "mxfp4_quantize_grouped", "mxfp4_dequantize", "mxfp4_swap_w13",
+    "mxfp4_status_string", "mxfp4_version", "quantize", "quantize_grouped", "dequantize",
+    "swap_w13", "MXFP4_OK", "MXFP4_EINVAL", "MXFP4_EALIGN", "MXFP4_ESHAPE", "MXFP4_EALIAS",
+    "MXFP4_ECUDA", "MXFP4_EOFFSETS",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300.so")
+
+MXFP4_OK = 0
+MXFP4_EINVAL = -1
+MXFP4_EALIGN = -2
+MXFP4_ESHAPE = -3
+MXFP4_EALIAS = -4
+MXFP4_ECUDA = -5
+MXFP4_EOFFSETS = -6
+
+
+class MXFP4Error(RuntimeError):
+    """A non-zero status returned by the library."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {mxfp4_status_string(code)} ({code})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m mxfp4_block_quantization_gb300._build` (nvcc, sm_103a)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    L.mxfp4_scale_bytes.restype = ctypes.c_size_t
+    L.mxfp4_scale_bytes.argtypes = [i64, i64]
+    L.mxfp4_grouped_scale_bytes_bound.restype = ctypes.c_size_t
+    L.mxfp4_grouped_scale_bytes_bound.argtypes = [i64, i32, i64]
+    L.mxfp4_quantize.restype = ctypes.c_int
+    L.mxfp4_quantize.argtypes = [vp, i64, i64, i64, vp, vp, vp]
+    L.mxfp4_quantize_grouped.restype = ctypes.c_int
+    L.mxfp4_quantize_grouped.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp]
+    L.mxfp4_dequantize.restype = ctypes.c_int
+    L.mxfp4_dequantize.argtypes = [vp, vp, i64, i64, vp, vp]
+    L.mxfp4_swap_w13.restype = ctypes.c_int
+    L.mxfp4_swap_w13.argtypes = [vp, vp, vp, i32, i64, i64, i32, vp, vp, vp, vp, i64, vp, vp]
+    L.mxfp4_status_string.restype = ctypes.c_char_p
+    L.mxfp4_status_string.argtypes = [ctypes.c_int]
+    L.mxfp4_version.restype = ctypes.c_int
+    L.mxfp4_version.argtypes = []
+    return L
+
+
+_lib = _load()
+
+
+# ------------------------------------------------------------------ helpers
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need_cuda(name, t, dtype=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _check(rc, where):
+    if rc != MXFP4_OK:
+        raise MXFP4Error(rc, where)
+
+
+# ------------------------------------------------------- C entry points
+def mxfp4_scale_bytes(M: int, K: int) -> int:
+    return int(_lib.mxfp4_scale_bytes(int(M), int(K)))
+
+
+def mxfp4_grouped_scale_bytes_bound(total_rows: int, E: int, K: int) -> int:
+    return int(_lib.mxfp4_grouped_scale_bytes_bound(int(total_rows), int(E), int(K)))
+
+
+def mxfp4_status_string(code: int) -> str:
+    return _lib.mxfp4_status_string(int(code)).decode()
+
+
+def mxfp4_version() -> int:
+    return int(_lib.mxfp4_version())
+
+
+def mxfp4_quantize(x, codes, scales, stream=None) -> None:
+    """BF16 ``x`` [M, K] (row stride may exceed K) -> ``codes`` uint8 [M, K/2]
+    and ``scales`` uint8 [mxfp4_scale_bytes(M, K)] (128x4 tiled)."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    M, K = x.shape
+    _check(_lib.mxfp4_quantize(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales),
+                               _stream(stream, x.device)), "mxfp4_quantize")
+
+
+def mxfp4_quantize_grouped(x, expert_offsets, codes, scales, scale_row_offsets, status=None,
+                           stream=None) -> None:
+    """Per-expert quantize of contiguous BF16 rows ``x`` [total_rows, K]
+    delimited by int32 ``expert_offsets`` [E+1] (device)."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("expert_offsets", expert_offsets, torch.int32)
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    _need_cuda("scale_row_offsets", scale_row_offsets, torch.int32)
+    _need_cuda("status", status, torch.int32)
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D tensor")
+    total, K = x.shape
+    E = expert_offsets.numel() - 1
+    _check(_lib.mxfp4_quantize_grouped(_ptr(x), total, K, _ptr(expert_offsets), E, _ptr(codes),
+                                       _ptr(scales), _ptr(scale_row_offsets), _ptr(status),
+                                       _stream(stream, x.device)), "mxfp4_quantize_grouped")
+
+
+def mxfp4_dequantize(codes, scales, M: int, K: int, y, stream=None) -> None:
+    """``codes`` [M, K/2] + tiled ``scales`` -> BF16 ``y`` [M, K] (contiguous)."""
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    _need_cuda("y", y, torch.bfloat16)
+    if not y.is_contiguous():
+        raise ValueError("y must be contiguous")
+    _check(_lib.mxfp4_dequantize(_ptr(codes), _ptr(scales), int(M), int(K), _ptr(y),
+                                 _stream(stream, y.device)), "mxfp4_dequantize")
+
+
+def mxfp4_swap_w13(codes_in, scales_in, w13_bias_in, E: int, two_n: int, K: int,
+                   scales_tiled: int, codes_out, scales_out, w13_bias_out=None,
+                   w2_bias_in=None, w2_bias_out=None, stream=None) -> None:
+    """[w1; w3] -> [w3; w1] of codes, scales (flat or tiled per expert) and
+    FP32 biases (cast to BF16); the w2 bias is cast only."""
+    for n, t, d in (("codes_in", codes_in, torch.uint8), ("scales_in", scales_in, torch.uint8),
+                    ("codes_out", codes_out, torch.uint8), ("scales_out", scales_out, torch.uint8),
+                    ("w13_bias_in", w13_bias_in, torch.float32),
+                    ("w13_bias_out", w13_bias_out, torch.bfloat16),
+                    ("w2_bias_in", w2_bias_in, torch.float32),
+                    ("w2_bias_out", w2_bias_out, torch.bfloat16)):
+        _need_cuda(n, t, d)
+    dev = next(t.device for t in (codes_in, w13_bias_in, w2_bias_in) if t is not None)
+    n2 = w2_bias_in.numel() if w2_bias_in is not None else 0
+    _check(_lib.mxfp4_swap_w13(_ptr(codes_in), _ptr(scales_in), _ptr(w13_bias_in), int(E),
+                               int(two_n), int(K), int(scales_tiled), _ptr(codes_out),
+                               _ptr(scales_out), _ptr(w13_bias_out), _ptr(w2_bias_in), n2,
+                               _ptr(w2_bias_out), _stream(stream, dev)), "mxfp4_swap_w13")
+
+
+# --------------------------------------------------- allocating wrappers
+def quantize(x, stream=None):
+    """Returns (codes uint8 [M, K/2], scales uint8 [scale_bytes])."""
+    M, K = x.shape
+    codes = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
+    scales = torch.empty(mxfp4_scale_bytes(M, K), dtype=torch.uint8, device=x.device)
+    mxfp4_quantize(x, codes, scales, stream)
+    return codes, scales
+
+
+def quantize_grouped(x, expert_offsets, stream=None):
+    """Returns (codes, scales, scale_row_offsets int32 [E+1], status int32 [1])."""
+    total, K = x.shape
+    E = expert_offsets.numel() - 1
+    dev = x.device
+    codes = torch.empty((total, K // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty(max(mxfp4_grouped_scale_bytes_bound(total, E, K), 16), dtype=torch.uint8,
+                         device=dev)
+    sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    status = torch.empty(1, dtype=torch.int32, device=dev)
+    mxfp4_quantize_grouped(x, expert_offsets, codes, scales, sro, status, stream)
+    return codes, scales, sro, status
+
+
+def dequantize(codes, scales, M: int, K: int, stream=None):
+    y = torch.empty((M, K), dtype=torch.bfloat16, device=codes.device)
+    mxfp4_dequantize(codes, scales, M, K, y, stream)
+    return y
+
+
+def swap_w13(codes, scales, w13_bias=None, w2_bias=None, scales_tiled=True, stream=None):
+    """codes uint8 [E, 2N, K/2]; scales tiled (E x scale_bytes(2N, K)) or flat
+    [E, 2N, K/32].  Returns (codes, scales, w13_bias_bf16, w2_bias_bf16)."""
+    E, two_n, half_k = codes.shape
+    K = half_k * 2
+    codes_out = torch.empty_like(codes)
+    scales_out = torch.empty_like(scales)
+    b13 = torch.empty(w13_bias.shape, dtype=torch.bfloat16, device=codes.device) \
+        if w13_bias is not None else None
+    b2 = torch.empty(w2_bias.shape, dtype=torch.bfloat16, device=codes.device) \
+        if w2_bias is not None else None
+    mxfp4_swap_w13(codes, scales, w13_bias, E, two_n, K, 1 if scales_tiled else 0, codes_out,
+                   scales_out, b13, w2_bias, b2, stream)
+    return codes_out, scales_out, b13, b2

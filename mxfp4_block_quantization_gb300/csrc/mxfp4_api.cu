@@ -1,0 +1,223 @@
+// mxfp4_api.cu — the extern "C" entry points of libmxfp4_gb300.so.
+//
+// Each entry point validates its arguments on the host (no device access,
+// no allocation, no synchronisation), then enqueues the kernels on the
+// caller's stream.  See include/mxfp4.h for the contract of every call.
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "mxfp4_internal.h"
+#include "../../include/mxfp4.h"
+
+namespace mxfp4 {
+
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace mxfp4
+
+namespace {
+
+constexpr int64_t kMaxGrid = INT_MAX;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range range_of(const void* p, int64_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + static_cast<uintptr_t>(bytes > 0 ? bytes : 0)};
+}
+
+bool overlap(Range a, Range b) {
+  if (a.lo == a.hi || b.lo == b.hi) return false;
+  return a.lo < b.hi && b.lo < a.hi;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? MXFP4_OK : MXFP4_ECUDA; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t padded_scale_cols(int64_t K) { return ceil_div(K / 32, 4) * 4; }
+
+}  // namespace
+
+extern "C" {
+
+size_t mxfp4_scale_bytes(int64_t M, int64_t K) {
+  if (M <= 0 || K <= 0 || K % 32 != 0) return 0;
+  return static_cast<size_t>(ceil_div(M, 128) * 128 * padded_scale_cols(K));
+}
+
+size_t mxfp4_grouped_scale_bytes_bound(int64_t total_rows, int32_t E, int64_t K) {
+  if (total_rows < 0 || E < 0 || K <= 0 || K % 32 != 0) return 0;
+  const int64_t tiles = (total_rows + 127 * static_cast<int64_t>(E)) / 128;
+  return static_cast<size_t>(tiles * 128 * padded_scale_cols(K));
+}
+
+int mxfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
+                   uint8_t* scales, void* stream) {
+  if (M < 0 || K < 0) return MXFP4_EINVAL;
+  if (K % 32 != 0 || ldx < K) return MXFP4_ESHAPE;
+  if (M == 0 || K == 0) return MXFP4_OK;
+  if (!x || !codes || !scales) return MXFP4_EINVAL;
+  if (!aligned16(x) || ldx % 8 != 0 || !aligned16(codes) || !aligned16(scales))
+    return MXFP4_EALIGN;
+  const int64_t tiles = ceil_div(M, 128) * ceil_div(K / 32, 4);
+  if (M > (INT64_MAX / 4) / ldx || tiles > kMaxGrid) return MXFP4_ESHAPE;
+  const Range rx = range_of(x, ((M - 1) * ldx + K) * 2);
+  const Range rc = range_of(codes, M * (K / 2));
+  const Range rs = range_of(scales, static_cast<int64_t>(mxfp4_scale_bytes(M, K)));
+  if (overlap(rx, rc) || overlap(rx, rs) || overlap(rc, rs)) return MXFP4_EALIAS;
+  return from_cuda(mxfp4::launch_quantize(x, M, K, ldx, codes, scales,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int mxfp4_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
+                           const int32_t* expert_offsets, int32_t E, uint8_t* codes,
+                           uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
+                           void* stream) {
+  if (total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
+  if (K % 32 != 0) return MXFP4_ESHAPE;
+  if (!expert_offsets || !scale_row_offsets) return MXFP4_EINVAL;
+  if (total_rows > 0 && K > 0 && (!x || !codes || !scales)) return MXFP4_EINVAL;
+  if (E == 0 && total_rows > 0) return MXFP4_EINVAL;
+  // padded rows must fit int32 (scale_row_offsets) and the grid must fit
+  const int64_t bound_tiles = (total_rows + 127 * static_cast<int64_t>(E)) / 128;
+  if (total_rows + 127 * static_cast<int64_t>(E) > INT32_MAX) return MXFP4_ESHAPE;
+  const int64_t grid = bound_tiles * ceil_div(K / 32, 4);
+  if (grid > kMaxGrid) return MXFP4_ESHAPE;
+  if ((x && !aligned16(x)) || (codes && !aligned16(codes)) || (scales && !aligned16(scales)) ||
+      (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) ||
+      (reinterpret_cast<uintptr_t>(scale_row_offsets) & 3u) ||
+      (reinterpret_cast<uintptr_t>(status) & 3u))
+    return MXFP4_EALIGN;
+  const Range rx = range_of(x, total_rows * K * 2);
+  const Range ro = range_of(expert_offsets, (static_cast<int64_t>(E) + 1) * 4);
+  const Range rc = range_of(codes, total_rows * (K / 2));
+  const Range rs =
+      range_of(scales, static_cast<int64_t>(mxfp4_grouped_scale_bytes_bound(total_rows, E, K)));
+  const Range rp = range_of(scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
+  const Range rt = range_of(status, status ? 4 : 0);
+  const Range outs[4] = {rc, rs, rp, rt};
+  for (int i = 0; i < 4; ++i) {
+    if (overlap(outs[i], rx) || overlap(outs[i], ro)) return MXFP4_EALIAS;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(outs[i], outs[j])) return MXFP4_EALIAS;
+  }
+  const int64_t tiles = (K == 0) ? 0 : bound_tiles;
+  return from_cuda(mxfp4::launch_quantize_grouped(x, total_rows, K, expert_offsets, E, codes,
+                                                  scales, scale_row_offsets, status, tiles,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+int mxfp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int64_t K, void* y,
+                     void* stream) {
+  if (M < 0 || K < 0) return MXFP4_EINVAL;
+  if (K % 32 != 0) return MXFP4_ESHAPE;
+  if (M == 0 || K == 0) return MXFP4_OK;
+  if (!codes || !scales || !y) return MXFP4_EINVAL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(y)) return MXFP4_EALIGN;
+  const int64_t tiles = ceil_div(M, 128) * ceil_div(K / 32, 4);
+  if (M > (INT64_MAX / 4) / K || tiles > kMaxGrid) return MXFP4_ESHAPE;
+  const Range rc = range_of(codes, M * (K / 2));
+  const Range rs = range_of(scales, static_cast<int64_t>(mxfp4_scale_bytes(M, K)));
+  const Range ry = range_of(y, M * K * 2);
+  if (overlap(ry, rc) || overlap(ry, rs)) return MXFP4_EALIAS;
+  return from_cuda(
+      mxfp4::launch_dequantize(codes, scales, M, K, y, static_cast<cudaStream_t>(stream)));
+}
+
+int mxfp4_swap_w13(const uint8_t* codes_in, const uint8_t* scales_in, const float* w13_bias_in,
+                   int32_t E, int64_t two_n, int64_t K, int32_t scales_tiled, uint8_t* codes_out,
+                   uint8_t* scales_out, void* w13_bias_out, const float* w2_bias_in,
+                   int64_t w2_bias_numel, void* w2_bias_out, void* stream) {
+  if (E < 0 || two_n < 0 || K < 0 || w2_bias_numel < 0) return MXFP4_EINVAL;
+  if (scales_tiled != 0 && scales_tiled != 1) return MXFP4_EINVAL;
+  if (two_n % 2 != 0 || K % 32 != 0) return MXFP4_ESHAPE;
+  const bool w13_work = E > 0 && two_n > 0 && K > 0;
+  if (w13_work && (!codes_in || !scales_in || !codes_out || !scales_out)) return MXFP4_EINVAL;
+  if (w13_bias_in && E > 0 && two_n > 0 && !w13_bias_out) return MXFP4_EINVAL;
+  if (w2_bias_in && w2_bias_numel > 0 && !w2_bias_out) return MXFP4_EINVAL;
+  if (static_cast<int64_t>(E) * two_n > INT64_MAX / (K > 0 ? K : 1) / 4) return MXFP4_ESHAPE;
+  if ((codes_in && !aligned16(codes_in)) || (codes_out && !aligned16(codes_out)) ||
+      (scales_in && !aligned16(scales_in)) || (scales_out && !aligned16(scales_out)) ||
+      (w13_bias_in && (reinterpret_cast<uintptr_t>(w13_bias_in) & 3u)) ||
+      (w13_bias_out && (reinterpret_cast<uintptr_t>(w13_bias_out) & 1u)) ||
+      (w2_bias_in && (reinterpret_cast<uintptr_t>(w2_bias_in) & 3u)) ||
+      (w2_bias_out && (reinterpret_cast<uintptr_t>(w2_bias_out) & 1u)))
+    return MXFP4_EALIGN;
+  const int64_t rows = static_cast<int64_t>(E) * two_n;
+  const int64_t scale_bytes =
+      scales_tiled ? static_cast<int64_t>(E) * static_cast<int64_t>(mxfp4_scale_bytes(two_n, K))
+                   : rows * (K / 32);
+  const int64_t n13 = w13_bias_in ? rows : 0;
+  const int64_t n2 = w2_bias_in ? w2_bias_numel : 0;
+  const Range ins[4] = {range_of(codes_in, w13_work ? rows * (K / 2) : 0),
+                        range_of(scales_in, w13_work ? scale_bytes : 0),
+                        range_of(w13_bias_in, n13 * 4), range_of(w2_bias_in, n2 * 4)};
+  const Range outs[4] = {range_of(codes_out, w13_work ? rows * (K / 2) : 0),
+                         range_of(scales_out, w13_work ? scale_bytes : 0),
+                         range_of(w13_bias_out, n13 * 2), range_of(w2_bias_out, n2 * 2)};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 4; ++j)
+      if (overlap(outs[i], ins[j])) return MXFP4_EALIAS;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(outs[i], outs[j])) return MXFP4_EALIAS;
+  }
+  mxfp4::SwapArgs a{};
+  a.codes_in = codes_in;
+  a.scales_in = scales_in;
+  a.w13_bias_in = (E > 0 && two_n > 0) ? w13_bias_in : nullptr;
+  a.E = w13_work ? E : 0;
+  a.two_n = two_n > 0 ? two_n : 2;
+  a.K = K;
+  a.scales_tiled = scales_tiled;
+  a.codes_out = codes_out;
+  a.scales_out = scales_out;
+  a.w13_bias_out = w13_bias_out;
+  a.w2_bias_in = n2 > 0 ? w2_bias_in : nullptr;
+  a.w2_bias_numel = n2;
+  a.w2_bias_out = w2_bias_out;
+  if (!w13_work) {
+    // bias-only work (e.g. K == 0): keep the bias part, skip codes/scales
+    a.E = (E > 0 && two_n > 0) ? E : 0;
+    a.K = 0;
+  }
+  if (a.E == 0 && n2 == 0) return MXFP4_OK;
+  return from_cuda(mxfp4::launch_swap_w13(a, static_cast<cudaStream_t>(stream)));
+}
+
+const char* mxfp4_status_string(int status) {
+  switch (status) {
+    case MXFP4_OK: return "MXFP4_OK: success";
+    case MXFP4_EINVAL: return "MXFP4_EINVAL: NULL pointer, negative size or bad flag";
+    case MXFP4_EALIGN: return "MXFP4_EALIGN: pointer or row stride breaks the 16-byte rule";
+    case MXFP4_ESHAPE: return "MXFP4_ESHAPE: K % 32 != 0, ldx < K, odd two_n or size overflow";
+    case MXFP4_EALIAS: return "MXFP4_EALIAS: an output overlaps an input or another output";
+    case MXFP4_ECUDA: return "MXFP4_ECUDA: kernel launch failed";
+    case MXFP4_EOFFSETS: return "MXFP4_EOFFSETS: expert offsets are not 0 <= ... <= total_rows";
+    default: return "unknown mxfp4 status";
+  }
+}
+
+int mxfp4_version(void) { return 100; }
+
+}  // extern "C"

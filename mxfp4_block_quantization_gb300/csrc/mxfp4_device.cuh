@@ -1,0 +1,137 @@
+// mxfp4_device.cuh — device-side building blocks of the sm_103a MXFP4 kernels.
+//
+// Format sources (vLLM pull-request summary pages):
+//   [PR43557] "Fix the E8M0 scale computation in the MXFP4 MoE CUTLASS kernel":
+//             "Implementation breakdown" item 1 and the cvt_warp_fp16_to_fp4
+//             excerpt (E8M0 scale rule, scale value 2^(s-127)); the
+//             untile_cutlass_scale snippet (128x4 tiled scale layout).
+//   OCP MX v1.0 for the E2M1 element encoding the pages leave implicit.
+#pragma once
+
+#include <cstdint>
+
+namespace mxfp4 {
+
+// ---------------------------------------------------------------- geometry
+constexpr int kBlock = 32;          // elements per scale block
+constexpr int kTileRows = 128;      // rows of one tiled scale chunk
+constexpr int kTileBlocks = 4;      // scale columns of one tiled scale chunk
+constexpr int kTileCols = kTileBlocks * kBlock;   // 128 BF16 columns
+constexpr int kChunkBytes = kTileRows * kTileBlocks;  // 512 B of scales per tile
+
+// Byte offset of (local row lr in [0,128), block b in [0,4)) inside one 512 B
+// tiled chunk: [32 outerM][4 innerM][4 innerK] with outerM = lr % 32,
+// innerM = lr / 32 ([PR43557] untile_cutlass_scale permutation).
+__device__ __forceinline__ int chunk_offset(int lr, int b) {
+  return (lr & 31) * 16 + (lr >> 5) * 4 + b;
+}
+
+// ------------------------------------------------------------ E8M0 scale
+// [PR43557] UE8M0 branch: add 2^21 to the float bits of vecMax (rounds the
+// exponent up when the mantissa is >= 0.75), take the exponent field,
+// subtract 2 when it is > 2 (else 0), cap at 254.  vecMax arrives as the
+// BF16 bit pattern of a non-negative value (sign already cleared), i.e. the
+// float bits are m << 16, so the add is (m + 0x20) on the BF16 pattern and
+// the 8-bit exponent field is bits 7..14 of that sum (bit 15 set only by the
+// NaN patterns >= 0x7FE0, where the 32-bit form wraps the same way).
+__device__ __forceinline__ uint32_t e8m0_from_absmax_bf16(uint32_t m) {
+  uint32_t e = ((m + 0x20u) >> 7) & 0xFFu;
+  uint32_t s = e > 2u ? e - 2u : 0u;
+  return s < 254u ? s : 254u;
+}
+
+// 2^(127 - s) as float bits for s in [1, 253]: biased exponent 254 - s.
+__device__ __forceinline__ float inv_scale_from_e8m0(uint32_t s) {
+  return __uint_as_float((254u - s) << 23);
+}
+
+// 2^(s - 127) as a float, every s in [0, 254]: s == 0 is the subnormal
+// 2^-127 (mantissa bit 22).  s == 255 (E8M0 NaN) is handled by the caller.
+__device__ __forceinline__ float scale_from_e8m0(uint32_t s) {
+  return __uint_as_float(s ? (s << 23) : 0x00400000u);
+}
+
+// ------------------------------------------------- E2M1 conversion (PTX)
+// Two float32 -> one byte of two E2M1 codes, round to nearest even with
+// saturation to +-6 (sm_100-family instruction).  `lo` lands in bits 0..3,
+// `hi` in bits 4..7.  Four such bytes are packed into one 32-bit word,
+// element 2j in the low nibble of byte j.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float a0, float a1, float a2, float a3,
+                                               float a4, float a5, float a6, float a7) {
+  uint32_t r;
+  asm("{\n\t"
+      ".reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t"
+      "}"
+      : "=r"(r)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7));
+  return r;
+}
+
+// One byte of two E2M1 codes -> two halves (f16x2), low nibble in the low half.
+__device__ __forceinline__ uint32_t cvt_e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
+  uint32_t r;
+  uint16_t v = static_cast<uint16_t>(byte_in_low_bits);
+  asm("{\n\t"
+      ".reg .b8 lo, hi;\n\t"
+      "mov.b16 {lo, hi}, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, lo;\n\t"
+      "}"
+      : "=r"(r)
+      : "h"(v));
+  return r;
+}
+
+// Two float32 -> BF16x2 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float half_lo_to_f32(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+__device__ __forceinline__ float half_hi_to_f32(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+
+// -------------------------------------------------------- memory access
+// Streaming 16-byte load of data read exactly once: read-only path, no L1
+// allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// Streaming stores (evict-first: outputs are not re-read by this kernel).
+__device__ __forceinline__ void st_stream_u32(void* p, uint32_t v) {
+  asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Unsigned max of the two 16-bit halves of a and b.
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
+
+}  // namespace mxfp4

@@ -1,0 +1,48 @@
+// mxfp4_internal.h — launchers shared between the kernel translation units
+// and the C ABI (mxfp4_api.cu).  Arguments are already validated by the
+// caller; each launcher only enqueues work and returns the launch status.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace mxfp4 {
+
+// Dense quantize of a [M, K] BF16 matrix (row stride ldx elements).
+cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
+                            uint8_t* scales, cudaStream_t stream);
+
+// Grouped quantize: validates offsets and writes padded row starts, then
+// quantizes every segment.  `bound_tiles` is the host-side upper bound of
+// padded 128-row tiles.
+cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
+                                    const int32_t* offsets, int32_t E, uint8_t* codes,
+                                    uint8_t* scales, int32_t* scale_row_offsets,
+                                    int32_t* status, int64_t bound_tiles, cudaStream_t stream);
+
+cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int64_t K,
+                              void* y, cudaStream_t stream);
+
+struct SwapArgs {
+  const uint8_t* codes_in;
+  const uint8_t* scales_in;
+  const float* w13_bias_in;
+  int32_t E;
+  int64_t two_n;
+  int64_t K;
+  int32_t scales_tiled;
+  uint8_t* codes_out;
+  uint8_t* scales_out;
+  void* w13_bias_out;
+  const float* w2_bias_in;
+  int64_t w2_bias_numel;
+  void* w2_bias_out;
+};
+
+cudaError_t launch_swap_w13(const SwapArgs& a, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace mxfp4

@@ -1,0 +1,130 @@
+"""Host-side checks of the C-ABI library: it loads, it exports every entry
+point its header declares, and argument validation returns the documented
+status codes before anything reaches the GPU (no compute call here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "mxfp4.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxfp4_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mxfp4_block_quantization_gb300 import _build
+    _build.build()
+    import mxfp4_block_quantization_gb300 as m
+    return m
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("mxfp4_quantize", "mxfp4_quantize_grouped", "mxfp4_dequantize", "mxfp4_swap_w13",
+              "mxfp4_scale_bytes", "mxfp4_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    L = ctypes.CDLL(lib.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_size_helpers(lib):
+    assert lib.mxfp4_scale_bytes(128, 256) == 1024
+    assert lib.mxfp4_scale_bytes(4096, 7168) == 917504
+    assert lib.mxfp4_scale_bytes(1000, 2880) == 94208
+    assert lib.mxfp4_scale_bytes(1, 32) == 512
+    assert lib.mxfp4_scale_bytes(0, 32) == 0 and lib.mxfp4_scale_bytes(4, 48) == 0
+    # 131072 rows over 384 experts, K = 7168: floor((131072 + 127*384)/128) tiles
+    assert lib.mxfp4_grouped_scale_bytes_bound(131072, 384, 7168) == 1405 * 128 * 224
+    assert lib.mxfp4_version() >= 100
+    assert "OFFSETS" in lib.mxfp4_status_string(lib.MXFP4_EOFFSETS)
+
+
+A = 1 << 32   # fake, 16-byte aligned addresses: validation fails before any use
+
+
+def q(lib, x, M, K, ldx, c, s):
+    return lib._lib.mxfp4_quantize(x, M, K, ldx, c, s, None)
+
+
+def test_quantize_validation(lib):
+    assert q(lib, A, -1, 32, 32, 2 * A, 3 * A) == lib.MXFP4_EINVAL
+    assert q(lib, A, 4, 48, 48, 2 * A, 3 * A) == lib.MXFP4_ESHAPE
+    assert q(lib, A, 4, 64, 32, 2 * A, 3 * A) == lib.MXFP4_ESHAPE
+    assert q(lib, None, 4, 64, 64, 2 * A, 3 * A) == lib.MXFP4_EINVAL
+    assert q(lib, A + 8, 4, 64, 64, 2 * A, 3 * A) == lib.MXFP4_EALIGN
+    assert q(lib, A, 4, 64, 68, 2 * A, 3 * A) == lib.MXFP4_EALIGN
+    assert q(lib, A, 4, 64, 64, 2 * A, 3 * A + 4) == lib.MXFP4_EALIGN
+    # codes overlapping x, scales overlapping codes
+    assert q(lib, A, 4, 64, 64, A + 256, 3 * A) == lib.MXFP4_EALIAS
+    assert q(lib, A, 4, 64, 64, 2 * A, 2 * A + 64) == lib.MXFP4_EALIAS
+    # empty work is a no-op, even with NULL pointers
+    assert q(lib, None, 0, 64, 64, None, None) == lib.MXFP4_OK
+    assert q(lib, None, 5, 0, 0, None, None) == lib.MXFP4_OK
+
+
+def test_grouped_validation(lib):
+    g = lib._lib.mxfp4_quantize_grouped
+    assert g(A, 10, 64, 2 * A, -1, 3 * A, 4 * A, 5 * A, None, None) == lib.MXFP4_EINVAL
+    assert g(A, 10, 48, 2 * A, 2, 3 * A, 4 * A, 5 * A, None, None) == lib.MXFP4_ESHAPE
+    assert g(A, 10, 64, None, 2, 3 * A, 4 * A, 5 * A, None, None) == lib.MXFP4_EINVAL
+    assert g(A, 10, 64, 2 * A, 0, 3 * A, 4 * A, 5 * A, None, None) == lib.MXFP4_EINVAL
+    assert g(A, 10, 64, 2 * A, 2, 3 * A + 4, 4 * A, 5 * A, None, None) == lib.MXFP4_EALIGN
+    assert g(A, 10, 64, 2 * A + 2, 2, 3 * A, 4 * A, 5 * A, None, None) == lib.MXFP4_EALIGN
+    # scale_row_offsets overlapping the offsets input
+    assert g(A, 10, 64, 2 * A, 2, 3 * A, 4 * A, 2 * A + 4, None, None) == lib.MXFP4_EALIAS
+    # status overlapping codes
+    assert g(A, 10, 64, 2 * A, 2, 3 * A, 4 * A, 5 * A, 3 * A + 16, None) == lib.MXFP4_EALIAS
+    # padded rows must fit int32
+    assert g(A, 2 ** 31 - 10, 32, 2 * A, 2, 3 * A, 4 * A, 5 * A, None, None) == lib.MXFP4_ESHAPE
+
+
+def test_dequantize_validation(lib):
+    d = lib._lib.mxfp4_dequantize
+    assert d(A, 2 * A, 4, 40, 3 * A, None) == lib.MXFP4_ESHAPE
+    assert d(A, 2 * A, -4, 64, 3 * A, None) == lib.MXFP4_EINVAL
+    assert d(A, None, 4, 64, 3 * A, None) == lib.MXFP4_EINVAL
+    assert d(A, 2 * A, 4, 64, 3 * A + 2, None) == lib.MXFP4_EALIGN
+    assert d(A, 2 * A, 4, 64, A + 64, None) == lib.MXFP4_EALIAS
+    assert d(None, None, 0, 64, None, None) == lib.MXFP4_OK
+
+
+def test_swap_validation(lib):
+    s = lib._lib.mxfp4_swap_w13
+    ok_args = [A, 2 * A, None, 2, 8, 64, 0, 3 * A, 4 * A, None, None, 0, None, None]
+
+    def call(**kw):
+        names = ["ci", "si", "b13", "E", "two_n", "K", "tiled", "co", "so", "b13o", "b2", "n2",
+                 "b2o", "st"]
+        a = dict(zip(names, ok_args))
+        a.update(kw)
+        return s(*[a[n] for n in names])
+
+    assert call(two_n=7) == lib.MXFP4_ESHAPE
+    assert call(K=48) == lib.MXFP4_ESHAPE
+    assert call(tiled=2) == lib.MXFP4_EINVAL
+    assert call(E=-1) == lib.MXFP4_EINVAL
+    assert call(co=None) == lib.MXFP4_EINVAL
+    assert call(b13=5 * A) == lib.MXFP4_EINVAL              # bias without output
+    assert call(co=3 * A + 8) == lib.MXFP4_EALIGN
+    assert call(co=A + 64) == lib.MXFP4_EALIAS               # out overlaps codes_in
+    assert call(so=3 * A + 128) == lib.MXFP4_EALIAS          # scales_out overlaps codes_out
+    assert call(E=0) == lib.MXFP4_OK                          # nothing to do
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        lib.quantize(x)

@@ -1,0 +1,321 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle,
+element by element, bit-exact for codes, every tiled scale byte (pad
+included) and dequantized BF16.  Output buffers carry 0xA5 guard bands that
+must survive every call."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp4_block_quantization_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 256  # bytes of 0xA5 on each side of every output
+
+
+@pytest.fixture(scope="module")
+def mx():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import mxfp4_block_quantization_gb300 as m
+    return m
+
+
+class Guarded:
+    """A uint8 (or other dtype) device buffer framed by 0xA5 guard bands."""
+
+    def __init__(self, nbytes, dtype=torch.uint8, shape=None):
+        self.raw = torch.full((nbytes + 2 * GUARD,), 0xA5, dtype=torch.uint8, device="cuda")
+        self.nbytes = nbytes
+        inner = self.raw[GUARD:GUARD + nbytes]
+        self.t = inner.view(dtype)
+        if shape is not None:
+            self.t = self.t.view(shape)
+
+    def check(self):
+        head = self.raw[:GUARD].cpu().numpy()
+        tail = self.raw[GUARD + self.nbytes:].cpu().numpy()
+        assert (head == 0xA5).all() and (tail == 0xA5).all(), "guard band overwritten"
+
+
+def bits(t):
+    return W.bf16_bits(t)
+
+
+def run_quantize(mx, x):
+    M, K = x.shape
+    codes = Guarded(M * (K // 2), shape=(M, K // 2))
+    sb = mx.mxfp4_scale_bytes(M, K)
+    scales = Guarded(sb)
+    mx.mxfp4_quantize(x, codes.t, scales.t)
+    torch.cuda.synchronize()
+    codes.check()
+    scales.check()
+    return codes.t.cpu().numpy(), scales.t.cpu().numpy()
+
+
+def run_dequantize(mx, codes, scales, M, K):
+    y = Guarded(M * K * 2, torch.bfloat16, (M, K))
+    mx.mxfp4_dequantize(torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda(), M, K, y.t)
+    torch.cuda.synchronize()
+    y.check()
+    return bits(y.t)
+
+
+def assert_quant_parity(mx, x_dev):
+    xb = bits(x_dev)
+    M, K = xb.shape
+    c_gpu, s_gpu = run_quantize(mx, x_dev)
+    c_orc, s_orc = oracle.quantize(xb)
+    assert np.array_equal(c_gpu, c_orc), _first_diff(c_gpu, c_orc)
+    assert np.array_equal(s_gpu, s_orc), _first_diff(s_gpu, s_orc)
+    y_gpu = run_dequantize(mx, c_gpu, s_gpu, M, K)
+    y_orc = oracle.dequantize(c_orc, s_orc, M, K)
+    assert np.array_equal(y_gpu, y_orc), _first_diff(y_gpu, y_orc)
+    return c_orc, s_orc, y_orc
+
+
+def _first_diff(a, b):
+    idx = np.argwhere(a != b)
+    if idx.size == 0:
+        return "equal"
+    i = tuple(idx[0])
+    return f"{idx.shape[0]} mismatches, first at {i}: got {a[i]:#x} want {b[i]:#x}"
+
+
+def rel_l2(xb, yb):
+    x = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    y = (yb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return float(np.linalg.norm(y - x) / np.linalg.norm(x))
+
+
+# ------------------------------------------------------------------ dense
+def test_small_matrix_128x256(mx):
+    x = W.small_matrix(0).cuda()
+    assert_quant_parity(mx, x)
+
+
+def test_edge_cases_1000x2880(mx):
+    x = W.edge_cases(4).cuda()
+    c, s, y = assert_quant_parity(mx, x)
+    print("edge-case rel-L2", rel_l2(bits(x), y))
+
+
+def test_dense_activation_4096x7168(mx):
+    x = W.dense_activation(1, device="cuda")
+    c, s, y = assert_quant_parity(mx, x)
+    print("dense rel-L2", rel_l2(bits(x), y))
+
+
+@pytest.mark.parametrize("M", [1, 31, 127, 128, 129, 300])
+@pytest.mark.parametrize("K", [32, 96, 160, 2880])
+def test_ragged_shapes(mx, M, K):
+    x = W.normal_bf16((M, K), seed=M * 1000 + K, device="cuda")
+    assert_quant_parity(mx, x)
+
+
+def test_strided_input(mx):
+    """Row stride larger than K (a column slice of a wider matrix)."""
+    wide = W.dense_activation(5, 300, 1024, device="cuda")
+    x = wide[:, 128:128 + 640]
+    assert x.stride(0) == 1024
+    c_gpu, s_gpu = run_quantize(mx, x)
+    c_orc, s_orc = oracle.quantize(bits(x.contiguous()))
+    assert np.array_equal(c_gpu, c_orc) and np.array_equal(s_gpu, s_orc)
+
+
+def test_empty(mx):
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    codes, scales = mx.quantize(x)
+    assert codes.numel() == 0 and scales.numel() == 0
+
+
+def test_element_map_exhaustive(mx):
+    """Every finite BF16 value under every reachable scale exponent: block b
+    holds a max that fixes s (2^(s-125), or 0x7F7F for s = 253) followed by
+    31 values of magnitude <= that max, enumerating all such BF16 patterns."""
+    finite = np.arange(0x0000, 0x7F80, dtype=np.uint16)           # positive finite
+    rows = []
+    for s in range(1, 254):
+        vmax = (s + 2) << 7 if s <= 252 else 0x7F7F                # bits of 2^(s-125)
+        vals = finite[finite <= vmax]
+        vals = np.concatenate([vals, vals | 0x8000])               # both signs
+        pad = (-vals.size) % 31
+        vals = np.concatenate([vals, np.zeros(pad, np.uint16)]).reshape(-1, 31)
+        blocks = np.concatenate([np.full((vals.shape[0], 1), vmax, np.uint16), vals], axis=1)
+        rows.append(blocks)
+    blocks = np.concatenate(rows)
+    pad = (-blocks.shape[0]) % 32
+    blocks = np.concatenate([blocks, np.zeros((pad, 32), np.uint16)])
+    xb = blocks.reshape(-1, 32 * 32)                               # K = 1024
+    x = W.from_bits(xb, "cuda")
+    c_gpu, s_gpu = run_quantize(mx, x)
+    c_orc, s_orc = oracle.quantize(xb)
+    assert np.array_equal(s_gpu, s_orc), _first_diff(s_gpu, s_orc)
+    assert np.array_equal(c_gpu, c_orc), _first_diff(c_gpu, c_orc)
+
+
+def test_dequant_all_codes_all_scales(mx):
+    """All 16 codes x all 256 scale bytes (including 0 and the NaN 255)."""
+    M, K = 256, 256                       # 2048 blocks: 8 per row
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 256, (M, K // 2), dtype=np.uint16).astype(np.uint8)
+    codes[:16, :] = np.arange(256, dtype=np.uint16).astype(np.uint8)[None, :128]
+    flat = (np.arange(M * (K // 32)) % 256).astype(np.uint8).reshape(M, K // 32)
+    tiled = oracle.tile(flat)
+    y_gpu = run_dequantize(mx, codes, tiled, M, K)
+    y_orc = oracle.dequantize(codes, tiled, M, K)
+    assert np.array_equal(y_gpu, y_orc), _first_diff(y_gpu, y_orc)
+
+
+# ---------------------------------------------------------------- grouped
+def run_grouped(mx, x, offsets):
+    total, K = x.shape
+    E = offsets.numel() - 1
+    codes = Guarded(total * (K // 2), shape=(total, K // 2))
+    bound = mx.mxfp4_grouped_scale_bytes_bound(total, E, K)
+    scales = Guarded(bound)
+    sro = Guarded(4 * (E + 1), torch.int32)
+    status = Guarded(4, torch.int32)
+    mx.mxfp4_quantize_grouped(x, offsets, codes.t, scales.t, sro.t, status.t)
+    torch.cuda.synchronize()
+    for g in (codes, scales, sro, status):
+        g.check()
+    return (codes.t.cpu().numpy(), scales.t.cpu().numpy(), sro.t.cpu().numpy(),
+            int(status.t.cpu()[0]))
+
+
+def test_grouped_small(mx):
+    g = W.moe_grouped(seed=2, tokens=200, top_k=4, num_experts=12, K=288, device="cuda")
+    c, s, sro, st = run_grouped(mx, g.x, g.offsets)
+    rc, c_o, s_o, sro_o = oracle.quantize_grouped(bits(g.x), g.offsets.cpu().numpy())
+    assert st == 0 and rc == 0
+    assert np.array_equal(sro, sro_o)
+    assert np.array_equal(c, c_o)
+    pk = (288 // 32 + 3) // 4 * 4
+    used = int(sro_o[-1]) * pk
+    assert np.array_equal(s[:used], s_o[:used])
+    assert (s[used:] == 0xA5).all(), "slack past P[E] must be untouched"
+
+
+def test_grouped_empty_and_uniform_segments(mx):
+    x = W.small_matrix(3, 512, 256).cuda()
+    for off in ([0, 0, 130, 130, 130, 512, 512], [0, 128, 256, 384, 512], [0, 512]):
+        o = torch.tensor(off, dtype=torch.int32, device="cuda")
+        c, s, sro, st = run_grouped(mx, x, o)
+        rc, c_o, s_o, sro_o = oracle.quantize_grouped(bits(x), np.array(off, np.int32))
+        assert st == 0 and np.array_equal(sro, sro_o) and np.array_equal(c, c_o)
+        used = int(sro_o[-1]) * 8
+        assert np.array_equal(s[:used], s_o[:used])
+
+
+@pytest.mark.parametrize("off", [[1, 10, 20], [0, 12, 8, 20], [0, 10, 19], [0, 10, 21]])
+def test_grouped_bad_offsets(mx, off):
+    x = W.small_matrix(3, 20, 64).cuda()
+    o = torch.tensor(off, dtype=torch.int32, device="cuda")
+    c, s, sro, st = run_grouped(mx, x, o)
+    assert st == mx.MXFP4_EOFFSETS
+    assert (sro == -1).all()
+    assert (c == 0xA5).all() and (s == 0xA5).all(), "outputs must stay untouched"
+
+
+def test_grouped_moe_full_size_sampled(mx):
+    """131072 rows (16384 tokens x top-8 over 384 experts), K = 7168: every
+    padded offset checked; codes and scale chunks of 12 random experts (and
+    the first and last) compared with the oracle segment by segment."""
+    g = W.moe_grouped(seed=2, device="cuda")
+    x, off = g.x, g.offsets
+    total, K = x.shape
+    E = off.numel() - 1
+    codes, scales, sro, st = mx.quantize_grouped(x, off)
+    torch.cuda.synchronize()
+    assert int(st.cpu()[0]) == 0
+    off_h = off.cpu().numpy().astype(np.int64)
+    n = np.diff(off_h)
+    want_sro = np.concatenate([[0], np.cumsum((n + 127) // 128 * 128)])
+    assert np.array_equal(sro.cpu().numpy(), want_sro)
+    pk = K // 32
+    rng = np.random.default_rng(0)
+    for e in sorted(set(rng.choice(E, 12, replace=False).tolist()) | {0, E - 1}):
+        a, b = int(off_h[e]), int(off_h[e + 1])
+        xb = bits(x[a:b])
+        c_o, s_o = oracle.quantize(xb)
+        assert np.array_equal(codes[a:b].cpu().numpy(), c_o), e
+        p0 = int(want_sro[e]) * pk
+        assert np.array_equal(scales[p0:p0 + s_o.size].cpu().numpy(), s_o), e
+
+
+# ------------------------------------------------------------------- swap
+def run_swap(mx, codes, scales, b13, b2, E, two_n, K, tiled):
+    c_in = torch.from_numpy(codes).cuda()
+    s_in = torch.from_numpy(scales).cuda()
+    b13_in = torch.from_numpy(b13).cuda() if b13 is not None else None
+    b2_in = torch.from_numpy(b2).cuda() if b2 is not None else None
+    c_out = Guarded(codes.size, shape=codes.shape)
+    s_out = Guarded(scales.size, shape=scales.shape)
+    b13_out = Guarded(b13.size * 2, torch.bfloat16, b13.shape) if b13 is not None else None
+    b2_out = Guarded(b2.size * 2, torch.bfloat16, b2.shape) if b2 is not None else None
+    mx.mxfp4_swap_w13(c_in, s_in, b13_in, E, two_n, K, tiled, c_out.t, s_out.t,
+                      b13_out.t if b13_out else None, b2_in, b2_out.t if b2_out else None)
+    torch.cuda.synchronize()
+    for g in (c_out, s_out, b13_out, b2_out):
+        if g is not None:
+            g.check()
+    return (c_out.t.cpu().numpy(), s_out.t.cpu().numpy(),
+            bits(b13_out.t) if b13_out else None, bits(b2_out.t) if b2_out else None)
+
+
+@pytest.mark.parametrize("tiled", [0, 1])
+@pytest.mark.parametrize("E,two_n,K", [(3, 200, 160), (2, 256, 2048), (1, 4, 64), (5, 130, 2880)])
+def test_swap_matches_oracle(mx, tiled, E, two_n, K):
+    rng = np.random.default_rng(E * 100 + two_n + K)
+    codes = rng.integers(0, 256, (E, two_n, K // 2), dtype=np.uint16).astype(np.uint8)
+    flat = rng.integers(0, 256, (E, two_n, K // 32), dtype=np.uint16).astype(np.uint8)
+    scales = np.concatenate([oracle.tile(flat[e]) for e in range(E)]) if tiled else flat
+    b13 = rng.standard_normal((E, two_n)).astype(np.float32)
+    b2 = rng.standard_normal((E, 37)).astype(np.float32)
+    got = run_swap(mx, codes, scales, b13, b2, E, two_n, K, tiled)
+    want = oracle.swap_w13(codes, scales, b13, E, two_n, K, tiled, b2)
+    for g, w in zip(got, want):
+        assert np.array_equal(g, w), _first_diff(g, w)
+
+
+def test_swap_page_arange_layout(mx):
+    """The PR #51038 test tensors in this library's layout: E = 1, 2N = 4,
+    K = 64 (flat scales [1, 4, 2] = arange(8)); rows become (2, 3, 0, 1)."""
+    codes = np.arange(128, dtype=np.uint8).reshape(1, 4, 32)
+    scales = np.arange(8, dtype=np.uint8).reshape(1, 4, 2)
+    b = np.arange(4, dtype=np.float32).reshape(1, 4)
+    c, s, b13, b2 = run_swap(mx, codes, scales, b, b.copy(), 1, 4, 64, 0)
+    assert np.array_equal(c[0], codes[0][[2, 3, 0, 1]])
+    assert s.tolist() == [[[4, 5], [6, 7], [0, 1], [2, 3]]]
+    assert b13.tolist() == [[0x4000, 0x4040, 0x0000, 0x3F80]]
+    assert b2.tolist() == [[0x0000, 0x3F80, 0x4000, 0x4040]]
+
+
+def test_expert_weights_full_size_sampled(mx):
+    """128 experts: w13 [128, 1536, 2048] and w2 [128, 2048, 768] quantized
+    as dense [E*rows, K] matrices (each expert a whole number of 128-row
+    tiles), then the w13 swap; 3 experts of each compared with the oracle."""
+    w = W.expert_weights(3, device="cuda")
+    E, two_n, H = w.w13.shape
+    codes13, scales13 = mx.quantize(w.w13.view(E * two_n, H))
+    codes2, scales2 = mx.quantize(w.w2.view(-1, w.w2.shape[2]))
+    per13 = mx.mxfp4_scale_bytes(two_n, H)
+    c_sw, s_sw, b13_sw, b2_sw = mx.swap_w13(codes13.view(E, two_n, H // 2), scales13,
+                                            w.w13_bias, w.w2_bias, scales_tiled=True)
+    torch.cuda.synchronize()
+    N2 = w.w2.shape[1]
+    per2 = mx.mxfp4_scale_bytes(N2, w.w2.shape[2])
+    for e in (0, 57, E - 1):
+        c_o, s_o = oracle.quantize(bits(w.w13[e]))
+        assert np.array_equal(codes13[e * two_n:(e + 1) * two_n].cpu().numpy(), c_o)
+        assert np.array_equal(scales13[e * per13:(e + 1) * per13].cpu().numpy(), s_o)
+        sw = oracle.swap_w13(c_o[None], s_o, w.w13_bias[e:e + 1].cpu().numpy(), 1, two_n, H, 1)
+        assert np.array_equal(c_sw[e].cpu().numpy(), sw[0][0])
+        assert np.array_equal(s_sw[e * per13:(e + 1) * per13].cpu().numpy(), sw[1])
+        assert np.array_equal(bits(b13_sw[e:e + 1]), sw[2])
+        c2_o, s2_o = oracle.quantize(bits(w.w2[e]))
+        assert np.array_equal(codes2[e * N2:(e + 1) * N2].cpu().numpy(), c2_o)
+        assert np.array_equal(scales2[e * per2:(e + 1) * per2].cpu().numpy(), s2_o)
+    assert np.array_equal(bits(b2_sw), oracle.cast_bf16(w.w2_bias.cpu().numpy()))
