@@ -9,7 +9,7 @@ CUDA kernels.  ``quantize``, ``quantize_grouped``, ``dequantize`` and
 the matching entry point.  PyTorch supplies device memory and streams only.
 
 There is no CPU path: importing this package fails when the library has not
-been built (``python -m mxfp4_block_quantization_gb300._build``), and every
+been built (``python mxfp4_block_quantization_gb300/_build.py``), and every
 call rejects tensors that are not on a CUDA device.
 
 Method sources (vLLM pull-request summary pages): PR #43557 "Fix the E8M0
@@ -55,7 +55,7 @@ def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"{LIB_PATH} is missing: build it with "
-            "`python -m mxfp4_block_quantization_gb300._build` (nvcc, sm_103a)")
+            "`python mxfp4_block_quantization_gb300/_build.py` (nvcc, sm_103a)")
     L = ctypes.CDLL(LIB_PATH)
     vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
     L.mxfp4_scale_bytes.restype = ctypes.c_size_t

@@ -20,8 +20,6 @@ def declared_functions():
 
 @pytest.fixture(scope="module")
 def lib():
-    from mxfp4_block_quantization_gb300 import _build
-    _build.build()
     import mxfp4_block_quantization_gb300 as m
     return m
 
