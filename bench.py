@@ -423,7 +423,7 @@ def run_ours(args):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
-    t_end = time.time() + 1.0
+    t_end = time.time() + args.settle
     i = 0
     while time.time() < t_end:
         for _ in range(200):
@@ -532,6 +532,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--settle", type=float, default=1.0,
+                    help="seconds of untimed launches after the warm-up steps (clock settling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
