@@ -11,9 +11,10 @@
 // The product has at most two significant bits, so the only rounding is
 // overflow to +-Inf (s >= 253) — no double rounding through float32.
 //
-// Same tile decomposition as the quantizer: one CTA per 128x128 tile, lane l
-// handles 8 elements of one row per pass (a 4-byte code load, one scale
-// byte from the tile's 512-byte chunk, a 16-byte BF16 store).
+// Same tiles as the quantizer (128 rows x 128 columns = one 512-byte scale
+// chunk), persistent grid, loads pipelined one tile ahead.  Per tile a thread
+// reads 8 code words (one per pass) and the two 16-byte rows of the chunk
+// that hold its 8 scale bytes, and writes 8 x 16 bytes of BF16.
 #include <cuda_runtime.h>
 
 #include "mxfp4_device.cuh"
@@ -34,6 +35,7 @@ struct DequantizeParams {
   int64_t y_ld;     // 2K bytes
   int32_t sK;
   int32_t nKT;
+  int32_t n_units;
 };
 
 // Four code bytes (8 elements, element 2j in the low nibble of byte j) and a
@@ -52,45 +54,83 @@ __device__ __forceinline__ uint4 decode8(uint32_t c, float sc) {
   return o;
 }
 
+struct Tile {
+  const uint8_t* c;     // code word of this thread's pass-0 row
+  const uint8_t* s;     // 16-byte chunk row of pass 0 (pass 1 is +256 bytes)
+  uint8_t* y;           // output of this thread's pass-0 row
+  int lim;
+  bool col_ok;
+};
+
 __global__ void __launch_bounds__(kThreads) dequantize_tiles_kernel(const DequantizeParams p) {
-  const int kt = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.nKT));
-  const int64_t tile = blockIdx.x / static_cast<uint32_t>(p.nKT);
-  const int64_t row0 = tile * kTileRows;
+  pdl_wait();
+  pdl_release();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int seg = lane & 15;
-  const int blk = seg >> 2;
-  const bool col_ok = kt * kTileBlocks + blk < p.sK;
-  const uint8_t* chunk = p.scales + (tile * p.nKT + kt) * kChunkBytes;
+  const int seg16 = lane & 15;
+  const int blk = seg16 >> 2;
+  const int lr0 = warp * 2 + (lane >> 4);  // row in pass 0; passes add 16 rows
+  const int64_t cld16 = p.code_ld * 16;
+  const int64_t yld16 = p.y_ld * 16;
 
+  int unit = blockIdx.x;
+  if (unit >= p.n_units) return;
+
+  auto make_tile = [&](int u) {
+    Tile t;
+    const int mt = u / p.nKT;
+    const int kt = u - mt * p.nKT;
+    const int64_t row0 = static_cast<int64_t>(mt) * kTileRows;
+    const int64_t avail = p.M - row0;
+    t.lim = static_cast<int>((avail < kTileRows ? avail : kTileRows) - lr0);
+    t.col_ok = kt * kTileBlocks + blk < p.sK;
+    t.c = p.codes + (row0 + lr0) * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) +
+          seg16 * 4;
+    // pass i sits in chunk row (lr0 + 16*(i&1)) % 32, word (i >> 1)
+    t.s = p.scales + static_cast<int64_t>(u) * kChunkBytes + lr0 * 16;
+    t.y = p.y + (row0 + lr0) * p.y_ld + static_cast<int64_t>(kt) * (kTileCols * 2) + seg16 * 16;
+    return t;
+  };
+
+  Tile cur = make_tile(unit);
   uint32_t c[kPasses];
-  uint32_t s[kPasses];
+  uint4 srow[2];
 #pragma unroll
-  for (int i = 0; i < kPasses; ++i) {
-    const int lr = i * 16 + warp * 2 + (lane >> 4);
-    const int64_t r = row0 + lr;
-    c[i] = 0u;
-    s[i] = 0u;
-    if (col_ok && r < p.M) {
-      c[i] = ld_stream_u32(p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) +
-                           seg * 4);
-      s[i] = __ldg(chunk + chunk_offset(lr, blk));
+  for (int i = 0; i < kPasses; ++i) c[i] = (cur.col_ok && 16 * i < cur.lim) ? ld_stream_u32(cur.c + i * cld16) : 0u;
+  srow[0] = ld_stream_v4(cur.s);
+  srow[1] = ld_stream_v4(cur.s + 256);
+
+  for (;;) {
+    const int next_unit = unit + static_cast<int>(gridDim.x);
+    const bool has_next = next_unit < p.n_units;
+    Tile nxt = cur;
+    if (has_next) nxt = make_tile(next_unit);
+    const uint4 sr0 = srow[0], sr1 = srow[1];
+    if (has_next) {
+      srow[0] = ld_stream_v4(nxt.s);
+      srow[1] = ld_stream_v4(nxt.s + 256);
     }
-  }
 #pragma unroll
-  for (int i = 0; i < kPasses; ++i) {
-    const int lr = i * 16 + warp * 2 + (lane >> 4);
-    const int64_t r = row0 + lr;
-    uint4 o;
-    if (s[i] == 255u) {
-      o = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
-    } else {
-      o = decode8(c[i], scale_from_e8m0(s[i]));
+    for (int i = 0; i < kPasses; ++i) {
+      const uint4 sr = (i & 1) ? sr1 : sr0;
+      const uint32_t word = (i >> 1) == 0 ? sr.x : (i >> 1) == 1 ? sr.y : (i >> 1) == 2 ? sr.z : sr.w;
+      const uint32_t s = (word >> (8 * blk)) & 0xFFu;
+      uint4 o;
+      if (s == 255u) {
+        o = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+      } else {
+        o = decode8(c[i], scale_from_e8m0(s));
+      }
+      if (cur.col_ok && 16 * i < cur.lim) st_stream_v4(cur.y + i * yld16, o);
+      if (has_next) c[i] = (nxt.col_ok && 16 * i < nxt.lim) ? ld_stream_u32(nxt.c + i * cld16) : 0u;
     }
-    if (col_ok && r < p.M)
-      st_stream_v4(p.y + r * p.y_ld + static_cast<int64_t>(kt) * (kTileCols * 2) + seg * 16, o);
+    if (!has_next) break;
+    cur = nxt;
+    unit = next_unit;
   }
 }
+
+int g_occ[64];
 
 }  // namespace
 
@@ -106,9 +146,11 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64
   p.sK = static_cast<int32_t>(K / kBlock);
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
-  const unsigned grid = static_cast<unsigned>(tiles * p.nKT);
-  dequantize_tiles_kernel<<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  p.n_units = static_cast<int32_t>(tiles * p.nKT);
+  const int64_t resident = static_cast<int64_t>(sm_count()) *
+                           resident_ctas(dequantize_tiles_kernel, kThreads, 0, g_occ);
+  const int64_t grid = p.n_units < resident ? p.n_units : resident;
+  return launch_pdl(dequantize_tiles_kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
 }  // namespace mxfp4

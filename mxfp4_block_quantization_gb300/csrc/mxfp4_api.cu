@@ -33,7 +33,7 @@ int sm_count() {
 
 namespace {
 
-constexpr int64_t kMaxGrid = INT_MAX;
+constexpr int64_t kMaxGrid = INT_MAX / 2;  // tile counts stay far from int overflow
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

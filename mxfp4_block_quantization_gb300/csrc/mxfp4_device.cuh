@@ -131,7 +131,20 @@ __device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
                : "memory");
 }
 
-// Unsigned max of the two 16-bit halves of a and b.
-__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
+// Per-half max of |a| and |b| for BF16x2 (the sign bit of each half becomes
+// the xor of the input signs and is cleared by the caller).
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Programmatic dependent launch: wait until the preceding grid of the stream
+// has completed and its writes are visible (no-op without a predecessor),
+// and allow the next grid of the stream to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 }  // namespace mxfp4

@@ -7,14 +7,18 @@
 // snippet (tiled layout).  Element rounding: OCP MX E2M1, round to nearest
 // even, saturating at +-6; blocks whose scale exponent is 0 emit zero codes.
 //
-// Work decomposition.  One CTA (256 threads) owns one 128-row x 128-column
-// tile: exactly the rows and scale columns of one 512-byte chunk of the tiled
-// scale layout, so the chunk is assembled in shared memory and leaves the SM
-// as 32 coalesced 16-byte stores.  Lane l of a warp covers 8 BF16 elements
-// (one 16-byte load) of row (2*warp + l/16) of a 16-row pass; four lanes form
-// one 32-element block, reduced with two xor-shuffles.  All eight passes'
-// loads are issued before any compute (32 KB in flight per CTA).
-// Each 16-lane half-warp writes 64 contiguous code bytes per row.
+// Work decomposition.  The unit of work is one 128-row x 128-column tile:
+// exactly the rows and scale columns of one 512-byte chunk of the tiled scale
+// layout, so the chunk is assembled in shared memory and leaves the SM as 32
+// coalesced 16-byte stores.  Lane l of a warp covers 8 BF16 elements (one
+// 16-byte load) of row (2*warp + l/16) of a 16-row pass; four lanes form one
+// 32-element block, reduced with two xor-shuffles.
+//
+// The grid is persistent (resident CTAs x SMs) and walks the tiles
+// round-robin.  Loads are software-pipelined across tiles: as soon as pass i
+// of the current tile has been consumed, its register slot is refilled with
+// pass i of the CTA's next tile, so every thread keeps eight 16-byte loads in
+// flight from start to finish and all CTAs end within one tile of each other.
 #include <cuda_runtime.h>
 
 #include "mxfp4_device.cuh"
@@ -26,6 +30,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kPasses = kTileRows / (2 * (kThreads / 32));  // 8 passes of 16 rows
+constexpr int kSegSmemMaxEntries = 2048;                   // E+1 staged in shared memory
 
 struct QuantizeParams {
   const uint8_t* __restrict__ x;  // BF16 bytes
@@ -36,94 +41,160 @@ struct QuantizeParams {
   uint8_t* __restrict__ scales;
   int32_t sK;                     // scale columns K/32
   int32_t nKT;                    // k tiles ceil(sK/4)
+  int32_t n_units;                // dense: tiles * nKT
   const int32_t* __restrict__ offsets;  // grouped: input row offsets [E+1]
   const int32_t* __restrict__ padded;   // grouped: padded row offsets [E+1]
   int32_t E;
+  int32_t seg_in_smem;            // grouped: offsets staged in dynamic shared memory
+};
+
+// Where one thread reads and writes for one tile.
+struct Tile {
+  const uint8_t* x;  // element 0 of this thread's pass-0 row
+  uint8_t* c;        // code word of this thread's pass-0 row
+  int lim;           // pass i is a real row when 16*i < lim
+  bool col_ok;       // this thread's block is a real scale column
+  int unit;          // tile index = scale chunk index
 };
 
 // Segment holding padded row `prow`: the last e in [0, E) with P[e] <= prow
 // (empty segments share their start with the next one, so the last such e
 // is never empty when prow < P[E]).
-__device__ __forceinline__ int find_segment(const int32_t* __restrict__ P, int E, int64_t prow) {
+template <typename Load>
+__device__ __forceinline__ int find_segment(Load P, int E, int prow) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (static_cast<int64_t>(__ldg(P + mid)) <= prow) lo = mid; else hi = mid - 1;
+    const int mid = (lo + hi + 1) >> 1;
+    if (P(mid) <= prow) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
 
 template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const QuantizeParams p) {
-  const int kt = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.nKT));
-  const int64_t tile = blockIdx.x / static_cast<uint32_t>(p.nKT);
+  __shared__ __align__(16) uint8_t chunk[2][kChunkBytes];
+  extern __shared__ int32_t seg[];  // grouped: [0, E] offsets, [E+1, 2E+1] padded
 
-  int64_t row0, row_end;
-  if constexpr (kGrouped) {
-    const int64_t total_padded = __ldg(p.padded + p.E);
-    const int64_t prow = tile * kTileRows;
-    if (total_padded < 0 || prow >= total_padded) return;  // bad offsets / past the end
-    const int e = find_segment(p.padded, p.E, prow);
-    row0 = __ldg(p.offsets + e) + (prow - __ldg(p.padded + e));
-    row_end = __ldg(p.offsets + e + 1);
-  } else {
-    row0 = tile * kTileRows;
-    row_end = p.M;
-  }
-
-  __shared__ __align__(16) uint8_t chunk[kChunkBytes];
+  pdl_wait();
+  pdl_release();
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int seg = lane & 15;        // 8-element segment inside the 128 columns
-  const int blk = seg >> 2;         // scale column inside the tile (0..3)
-  const bool col_ok = kt * kTileBlocks + blk < p.sK;
-  const int64_t col_byte = static_cast<int64_t>(kt) * (kTileCols * 2) + seg * 16;
+  const int seg16 = lane & 15;      // 8-element segment inside the 128 columns
+  const int blk = seg16 >> 2;       // scale column inside the tile (0..3)
+  const int lr0 = warp * 2 + (lane >> 4);  // this thread's row in pass 0
+  const int64_t ldx16 = p.ldx_bytes * 16;
+  const int64_t cld16 = p.code_ld * 16;
 
+  int n_units = p.n_units;
+  if constexpr (kGrouped) {
+    const int total_padded = __ldg(p.padded + p.E);
+    if (total_padded < 0) return;  // offsets rejected by the offsets kernel
+    n_units = (total_padded / kTileRows) * p.nKT;
+    if (p.seg_in_smem) {
+      for (int i = threadIdx.x; i <= p.E; i += kThreads) {
+        seg[i] = __ldg(p.offsets + i);
+        seg[p.E + 1 + i] = __ldg(p.padded + i);
+      }
+      __syncthreads();
+    }
+  }
+  int unit = blockIdx.x;
+  if (unit >= n_units) return;
+
+  auto make_tile = [&](int u) {
+    Tile t;
+    const int mt = u / p.nKT;
+    const int kt = u - mt * p.nKT;
+    int64_t row0, row_end;
+    if constexpr (kGrouped) {
+      const int prow = mt * kTileRows;
+      int e, seg_start, pad_start, seg_end;
+      if (p.seg_in_smem) {
+        const int32_t* P = seg + p.E + 1;
+        e = find_segment([&](int i) { return P[i]; }, p.E, prow);
+        seg_start = seg[e];
+        seg_end = seg[e + 1];
+        pad_start = P[e];
+      } else {
+        e = find_segment([&](int i) { return __ldg(p.padded + i); }, p.E, prow);
+        seg_start = __ldg(p.offsets + e);
+        seg_end = __ldg(p.offsets + e + 1);
+        pad_start = __ldg(p.padded + e);
+      }
+      row0 = static_cast<int64_t>(seg_start) + (prow - pad_start);
+      row_end = seg_end;
+    } else {
+      row0 = static_cast<int64_t>(mt) * kTileRows;
+      row_end = p.M;
+    }
+    const int64_t r = row0 + lr0;
+    const int64_t avail = row_end - row0;
+    t.lim = static_cast<int>((avail < kTileRows ? avail : kTileRows) - lr0);
+    t.col_ok = kt * kTileBlocks + blk < p.sK;
+    t.x = p.x + r * p.ldx_bytes + static_cast<int64_t>(kt) * (kTileCols * 2) + seg16 * 16;
+    t.c = p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) + seg16 * 4;
+    t.unit = u;
+    return t;
+  };
+
+  Tile cur = make_tile(unit);
   uint4 v[kPasses];
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
-    const int lr = i * 16 + warp * 2 + (lane >> 4);
-    const int64_t r = row0 + lr;
     v[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (col_ok && r < row_end) v[i] = ld_stream_v4(p.x + r * p.ldx_bytes + col_byte);
+    if (cur.col_ok && 16 * i < cur.lim) v[i] = ld_stream_v4(cur.x + i * ldx16);
   }
+
+  int buf = 0;
+  for (;;) {
+    const int next_unit = unit + static_cast<int>(gridDim.x);
+    const bool has_next = next_unit < n_units;
+    Tile nxt = cur;
+    if (has_next) nxt = make_tile(next_unit);
 
 #pragma unroll
-  for (int i = 0; i < kPasses; ++i) {
-    const int lr = i * 16 + warp * 2 + (lane >> 4);
-    const int64_t r = row0 + lr;
-    // block absmax on BF16 bit patterns: with the sign cleared, the unsigned
-    // order of the patterns is the order of the magnitudes.
-    const uint32_t m2 = vmax_u16x2(vmax_u16x2(v[i].x & 0x7FFF7FFFu, v[i].y & 0x7FFF7FFFu),
-                                   vmax_u16x2(v[i].z & 0x7FFF7FFFu, v[i].w & 0x7FFF7FFFu));
-    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-    const uint32_t s = e8m0_from_absmax_bf16(m);
-    if ((lane & 3) == 0) chunk[chunk_offset(lr, blk)] = static_cast<uint8_t>(s);
+    for (int i = 0; i < kPasses; ++i) {
+      // block absmax: |x| per half with max.xorsign.abs, sign bits cleared,
+      // then the larger half (unsigned order of non-negative BF16 patterns
+      // is the order of their magnitudes)
+      const uint32_t h = max_abs_bf16x2(max_abs_bf16x2(v[i].x, v[i].y),
+                                        max_abs_bf16x2(v[i].z, v[i].w)) & 0x7FFF7FFFu;
+      uint32_t m = max(h & 0xFFFFu, h >> 16);
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      const uint32_t s = e8m0_from_absmax_bf16(m);
+      if ((lane & 3) == 0) chunk[buf][chunk_offset(lr0 + 16 * i, blk)] = static_cast<uint8_t>(s);
 
-    // x * 2^(127-s): exact power-of-two scaling of BF16 values in float32.
-    const float inv = inv_scale_from_e8m0(s);
-    uint32_t code = cvt_e2m1x8(__uint_as_float(v[i].x << 16) * inv,
-                               __uint_as_float(v[i].x & 0xFFFF0000u) * inv,
-                               __uint_as_float(v[i].y << 16) * inv,
-                               __uint_as_float(v[i].y & 0xFFFF0000u) * inv,
-                               __uint_as_float(v[i].z << 16) * inv,
-                               __uint_as_float(v[i].z & 0xFFFF0000u) * inv,
-                               __uint_as_float(v[i].w << 16) * inv,
-                               __uint_as_float(v[i].w & 0xFFFF0000u) * inv);
-    if (s == 0u) code = 0u;
-    if (col_ok && r < row_end)
-      st_stream_u32(p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) + seg * 4,
-                    code);
-  }
+      // x * 2^(127-s): exact power-of-two scaling of BF16 values in float32
+      const float inv = inv_scale_from_e8m0(s);
+      uint32_t code = cvt_e2m1x8(__uint_as_float(v[i].x << 16) * inv,
+                                 __uint_as_float(v[i].x & 0xFFFF0000u) * inv,
+                                 __uint_as_float(v[i].y << 16) * inv,
+                                 __uint_as_float(v[i].y & 0xFFFF0000u) * inv,
+                                 __uint_as_float(v[i].z << 16) * inv,
+                                 __uint_as_float(v[i].z & 0xFFFF0000u) * inv,
+                                 __uint_as_float(v[i].w << 16) * inv,
+                                 __uint_as_float(v[i].w & 0xFFFF0000u) * inv);
+      if (s == 0u) code = 0u;
+      if (cur.col_ok && 16 * i < cur.lim) st_stream_u32(cur.c + i * cld16, code);
 
-  __syncthreads();
-  if (threadIdx.x < kChunkBytes / 16) {
-    const int64_t c = tile * p.nKT + kt;
-    const uint4 w = reinterpret_cast<const uint4*>(chunk)[threadIdx.x];
-    st_stream_v4(p.scales + c * kChunkBytes + threadIdx.x * 16, w);
+      // refill this slot with the same pass of the next tile
+      if (has_next) {
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (nxt.col_ok && 16 * i < nxt.lim) v[i] = ld_stream_v4(nxt.x + i * ldx16);
+      }
+    }
+
+    __syncthreads();
+    if (threadIdx.x < kChunkBytes / 16) {
+      const uint4 w = reinterpret_cast<const uint4*>(chunk[buf])[threadIdx.x];
+      st_stream_v4(p.scales + static_cast<int64_t>(cur.unit) * kChunkBytes + threadIdx.x * 16, w);
+    }
+    if (!has_next) break;
+    cur = nxt;
+    unit = next_unit;
+    buf ^= 1;
   }
 }
 
@@ -138,6 +209,8 @@ grouped_offsets_kernel(const int32_t* __restrict__ off, int32_t E, int64_t total
   __shared__ int s_bad;
   __shared__ int64_t s_warp[kScanThreads / 32];
   __shared__ int64_t s_carry;
+  pdl_wait();
+  pdl_release();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_bad = (off[0] != 0) || (static_cast<int64_t>(off[E]) != total_rows);
@@ -184,6 +257,10 @@ grouped_offsets_kernel(const int32_t* __restrict__ off, int32_t E, int64_t total
   if (tid == 0 && status != nullptr) *status = s_bad ? MXFP4_EOFFSETS : MXFP4_OK;
 }
 
+int g_occ_dense[64];
+int g_occ_grouped[64];
+int g_occ_grouped_smem[64];
+
 }  // namespace
 
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
@@ -198,18 +275,21 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
   p.sK = static_cast<int32_t>(K / kBlock);
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
-  const unsigned grid = static_cast<unsigned>(tiles * p.nKT);
-  quantize_tiles_kernel<false><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  p.n_units = static_cast<int32_t>(tiles * p.nKT);
+  const int64_t resident =
+      static_cast<int64_t>(sm_count()) *
+      resident_ctas(quantize_tiles_kernel<false>, kThreads, 0, g_occ_dense);
+  const int64_t grid = p.n_units < resident ? p.n_units : resident;
+  return launch_pdl(quantize_tiles_kernel<false>, static_cast<unsigned>(grid), kThreads, 0, stream,
+                    p);
 }
 
 cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
                                     const int32_t* offsets, int32_t E, uint8_t* codes,
                                     uint8_t* scales, int32_t* scale_row_offsets,
                                     int32_t* status, int64_t bound_tiles, cudaStream_t stream) {
-  grouped_offsets_kernel<<<1, kScanThreads, 0, stream>>>(offsets, E, total_rows,
-                                                         scale_row_offsets, status);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(grouped_offsets_kernel, 1, kScanThreads, 0, stream, offsets, E,
+                               total_rows, scale_row_offsets, status);
   if (err != cudaSuccess || E == 0 || bound_tiles == 0) return err;
   QuantizeParams p{};
   p.x = static_cast<const uint8_t*>(x);
@@ -223,9 +303,17 @@ cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K
   p.offsets = offsets;
   p.padded = scale_row_offsets;
   p.E = E;
-  const unsigned grid = static_cast<unsigned>(bound_tiles * p.nKT);
-  quantize_tiles_kernel<true><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  p.seg_in_smem = (E + 1 <= kSegSmemMaxEntries) ? 1 : 0;
+  const size_t smem = p.seg_in_smem ? static_cast<size_t>(E + 1) * 2 * sizeof(int32_t) : 0;
+  const int occ = p.seg_in_smem
+                      ? resident_ctas(quantize_tiles_kernel<true>, kThreads,
+                                      kSegSmemMaxEntries * 2 * sizeof(int32_t), g_occ_grouped_smem)
+                      : resident_ctas(quantize_tiles_kernel<true>, kThreads, 0, g_occ_grouped);
+  const int64_t bound_units = bound_tiles * p.nKT;
+  const int64_t resident = static_cast<int64_t>(sm_count()) * occ;
+  const int64_t grid = bound_units < resident ? bound_units : resident;
+  return launch_pdl(quantize_tiles_kernel<true>, static_cast<unsigned>(grid), kThreads, smem,
+                    stream, p);
 }
 
 }  // namespace mxfp4

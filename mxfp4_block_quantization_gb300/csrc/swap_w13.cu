@@ -6,13 +6,20 @@
 // convert_weight_to_mxfp4_moe_kernel_format branch: per expert, output row r
 // of the 2N fused rows is input row (r + N) mod 2N, for codes and scales;
 // the w13 bias halves change places and are cast FP32 -> BF16 (RNE); the w2
-// bias is cast only.  Tiled scales are swapped by logical row (each output
-// 4-byte word of a chunk is one row's 4 scale columns, gathered from the
-// source row's word), pad rows and pad columns written as zero.
+// bias is cast only.  Tiled scales are swapped by logical row, pad rows and
+// pad columns written as zero.
 //
-// One launch covers all three parts: the grid is split into a code range
-// (one warp per row, 16-byte vector copies), a scale range and a bias range.
+// Rows of one expert are contiguous, so for codes the swap is two contiguous
+// copies of N*K/2 bytes per expert ("half copies").  The same holds for flat
+// scales (N*K/32 bytes) and for tiled scales when N is a multiple of 128
+// (whole 128-row tiles).  Otherwise tiled scales are gathered word by word:
+// each 4-byte word of a chunk is one row's 4 scale columns.
+//
+// One launch covers all parts: the grid is split into a code range, a scale
+// range and a bias range.  A half-copy CTA moves 32 KB with eight 16-byte
+// loads in flight per thread.
 #include <algorithm>
+#include <climits>
 
 #include <cuda_runtime.h>
 
@@ -23,23 +30,35 @@ namespace mxfp4 {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kVecPerThread = 8;
+constexpr int kVecPerCta = kThreads * kVecPerThread;  // 2048 x 16 B = 32 KB
+
+enum ScaleMode : int32_t { kScaleHalfCopy = 0, kScaleTiledGather = 1, kScaleFlatGather = 2 };
+
+// E experts, each two contiguous halves of `half_vecs` 16-byte vectors;
+// out half h of expert e <- in half (1 - h).
+struct HalfCopy {
+  const uint4* __restrict__ in;
+  uint4* __restrict__ out;
+  int64_t half_vecs;
+  int32_t ctas_per_half;
+  int32_t ctas;  // 2 * E * ctas_per_half
+};
 
 struct SwapParams {
-  const uint4* __restrict__ codes_in;
-  uint4* __restrict__ codes_out;
-  int64_t rows;       // E * 2N
-  int64_t two_n;
-  int64_t half;       // N
-  int32_t row_vecs;   // 16-byte vectors per code row = K/32
-  // scales
+  HalfCopy codes;
+  int32_t scale_mode;
+  HalfCopy scales;  // kScaleHalfCopy
+  // gather modes
   const uint8_t* __restrict__ scales_in;
   uint8_t* __restrict__ scales_out;
-  int32_t tiled;
+  int64_t two_n;
+  int64_t half;       // N
   int32_t sK;
   int32_t nKT;
   int64_t chunk_words;  // tiled: 4-byte words per expert buffer
-  int64_t scale_items;  // tiled: E * chunk_words; flat: E * 2N * sK bytes
+  int64_t scale_items;  // gather: tiled words or flat bytes
+  int32_t scale_ctas;
   // biases
   const float* __restrict__ b13_in;
   uint16_t* __restrict__ b13_out;
@@ -47,9 +66,6 @@ struct SwapParams {
   const float* __restrict__ b2_in;
   uint16_t* __restrict__ b2_out;
   int64_t b2_numel;
-  // grid split
-  uint32_t code_blocks;
-  uint32_t scale_blocks;
 };
 
 __device__ __forceinline__ int64_t partner_row(int64_t r, int64_t half) {
@@ -60,39 +76,45 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   return static_cast<uint16_t>(cvt_bf16x2(f, 0.0f) & 0xFFFFu);
 }
 
+__device__ __forceinline__ void half_copy_cta(const HalfCopy& hc, int b) {
+  const int hi = b / hc.ctas_per_half;
+  const int part = b - hi * hc.ctas_per_half;
+  const int64_t e = hi >> 1;
+  const int h = hi & 1;
+  const uint4* src = hc.in + (2 * e + (1 - h)) * hc.half_vecs;
+  uint4* dst = hc.out + (2 * e + h) * hc.half_vecs;
+  const int64_t base = static_cast<int64_t>(part) * kVecPerCta + threadIdx.x;
+  uint4 v[kVecPerThread];
+#pragma unroll
+  for (int k = 0; k < kVecPerThread; ++k) {
+    const int64_t j = base + k * kThreads;
+    if (j < hc.half_vecs) v[k] = ld_stream_v4(src + j);
+  }
+#pragma unroll
+  for (int k = 0; k < kVecPerThread; ++k) {
+    const int64_t j = base + k * kThreads;
+    if (j < hc.half_vecs) st_stream_v4(dst + j, v[k]);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads) swap_w13_kernel(const SwapParams p) {
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  if (blockIdx.x < p.code_blocks) {
-    // ---- codes: one warp per row, 16-byte vectors, two rows in flight
-    const int64_t stride = static_cast<int64_t>(p.code_blocks) * kWarps;
-    for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp; row < p.rows;
-         row += stride) {
-      const int64_t e = row / p.two_n;
-      const int64_t r = row - e * p.two_n;
-      const int64_t src = e * p.two_n + partner_row(r, p.half);
-      const uint4* in = p.codes_in + src * p.row_vecs;
-      uint4* out = p.codes_out + row * p.row_vecs;
-      int v = lane;
-      for (; v + 96 < p.row_vecs; v += 128) {
-        const uint4 a = ld_stream_v4(in + v), b = ld_stream_v4(in + v + 32);
-        const uint4 c = ld_stream_v4(in + v + 64), d = ld_stream_v4(in + v + 96);
-        st_stream_v4(out + v, a);
-        st_stream_v4(out + v + 32, b);
-        st_stream_v4(out + v + 64, c);
-        st_stream_v4(out + v + 96, d);
-      }
-      for (; v < p.row_vecs; v += 32) st_stream_v4(out + v, ld_stream_v4(in + v));
-    }
+  pdl_wait();
+  pdl_release();
+  int b = static_cast<int>(blockIdx.x);
+  if (b < p.codes.ctas) {
+    half_copy_cta(p.codes, b);
     return;
   }
-  const uint32_t bid = blockIdx.x - p.code_blocks;
-  if (bid < p.scale_blocks) {
-    // ---- scales
-    const int64_t stride = static_cast<int64_t>(p.scale_blocks) * kThreads;
-    for (int64_t i = static_cast<int64_t>(bid) * kThreads + threadIdx.x; i < p.scale_items;
+  b -= p.codes.ctas;
+  if (b < p.scale_ctas) {
+    if (p.scale_mode == kScaleHalfCopy) {
+      half_copy_cta(p.scales, b);
+      return;
+    }
+    const int64_t stride = static_cast<int64_t>(p.scale_ctas) * kThreads;
+    for (int64_t i = static_cast<int64_t>(b) * kThreads + threadIdx.x; i < p.scale_items;
          i += stride) {
-      if (p.tiled) {
+      if (p.scale_mode == kScaleTiledGather) {
         // word i of the tiled output: expert e, chunk t (= m-tile * nKT + k-tile),
         // word w inside the 512-byte chunk = outerM * 4 + innerM.
         const int64_t e = i / p.chunk_words;
@@ -123,9 +145,10 @@ __global__ void __launch_bounds__(kThreads) swap_w13_kernel(const SwapParams p) 
     return;
   }
   // ---- biases (FP32 -> BF16, round to nearest even)
-  const uint32_t bb = bid - p.scale_blocks;
-  const int64_t stride = static_cast<int64_t>(gridDim.x - p.code_blocks - p.scale_blocks) * kThreads;
-  for (int64_t i = static_cast<int64_t>(bb) * kThreads + threadIdx.x; i < p.b13_numel + p.b2_numel;
+  b -= p.scale_ctas;
+  const int64_t bias_ctas = static_cast<int64_t>(gridDim.x) - p.codes.ctas - p.scale_ctas;
+  const int64_t stride = bias_ctas * kThreads;
+  for (int64_t i = static_cast<int64_t>(b) * kThreads + threadIdx.x; i < p.b13_numel + p.b2_numel;
        i += stride) {
     if (i < p.b13_numel) {
       const int64_t e = i / p.two_n;
@@ -138,49 +161,71 @@ __global__ void __launch_bounds__(kThreads) swap_w13_kernel(const SwapParams p) 
   }
 }
 
+HalfCopy make_half_copy(const uint8_t* in, uint8_t* out, int64_t E, int64_t half_bytes,
+                        int64_t* ctas) {
+  HalfCopy h{};
+  h.in = reinterpret_cast<const uint4*>(in);
+  h.out = reinterpret_cast<uint4*>(out);
+  h.half_vecs = half_bytes / 16;
+  const int64_t per = (h.half_vecs + kVecPerCta - 1) / kVecPerCta;
+  *ctas = 2 * E * per;
+  h.ctas_per_half = static_cast<int32_t>(per < INT_MAX ? per : INT_MAX);
+  h.ctas = static_cast<int32_t>(*ctas < INT_MAX ? *ctas : INT_MAX);
+  return h;
+}
+
 }  // namespace
 
 cudaError_t launch_swap_w13(const SwapArgs& a, cudaStream_t stream) {
   SwapParams p{};
-  p.codes_in = reinterpret_cast<const uint4*>(a.codes_in);
-  p.codes_out = reinterpret_cast<uint4*>(a.codes_out);
-  p.rows = static_cast<int64_t>(a.E) * a.two_n;
+  const int64_t N = a.two_n / 2;
+  const int64_t sK = a.K / kBlock;
   p.two_n = a.two_n;
-  p.half = a.two_n / 2;
-  p.row_vecs = static_cast<int32_t>(a.K / 32);
+  p.half = N;
+  p.sK = static_cast<int32_t>(sK);
+  p.nKT = static_cast<int32_t>((sK + kTileBlocks - 1) / kTileBlocks);
+  // codes: two contiguous halves of N*K/2 bytes per expert (K/2 is a multiple of 16)
+  int64_t code_ctas = 0;
+  p.codes = make_half_copy(a.codes_in, a.codes_out, a.E, N * (a.K / 2), &code_ctas);
+
+  const int64_t sms = sm_count();
+  int64_t scale_ctas = 0;
   p.scales_in = a.scales_in;
   p.scales_out = a.scales_out;
-  p.tiled = a.scales_tiled;
-  p.sK = static_cast<int32_t>(a.K / kBlock);
-  p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
-  if (a.scales_tiled) {
-    const int64_t tiles = (a.two_n + kTileRows - 1) / kTileRows;
-    p.chunk_words = tiles * p.nKT * (kChunkBytes / 4);
-    p.scale_items = static_cast<int64_t>(a.E) * p.chunk_words;
-  } else {
-    p.chunk_words = 0;
-    p.scale_items = static_cast<int64_t>(a.E) * a.two_n * p.sK;
+  if (a.E > 0 && sK > 0) {
+    const int64_t flat_half = N * sK;
+    if (a.scales_tiled && N % kTileRows == 0) {
+      p.scale_mode = kScaleHalfCopy;
+      p.scales = make_half_copy(a.scales_in, a.scales_out, a.E,
+                                (N / kTileRows) * p.nKT * kChunkBytes, &scale_ctas);
+    } else if (!a.scales_tiled && flat_half % 16 == 0) {
+      p.scale_mode = kScaleHalfCopy;
+      p.scales = make_half_copy(a.scales_in, a.scales_out, a.E, flat_half, &scale_ctas);
+    } else if (a.scales_tiled) {
+      p.scale_mode = kScaleTiledGather;
+      const int64_t tiles = (a.two_n + kTileRows - 1) / kTileRows;
+      p.chunk_words = tiles * p.nKT * (kChunkBytes / 4);
+      p.scale_items = static_cast<int64_t>(a.E) * p.chunk_words;
+      scale_ctas = std::min<int64_t>((p.scale_items + kThreads - 1) / kThreads, sms * 8);
+    } else {
+      p.scale_mode = kScaleFlatGather;
+      p.scale_items = static_cast<int64_t>(a.E) * a.two_n * sK;
+      scale_ctas = std::min<int64_t>((p.scale_items + kThreads - 1) / kThreads, sms * 8);
+    }
   }
+  p.scale_ctas = static_cast<int32_t>(scale_ctas);
   p.b13_in = a.w13_bias_in;
   p.b13_out = static_cast<uint16_t*>(a.w13_bias_out);
   p.b13_numel = a.w13_bias_in ? static_cast<int64_t>(a.E) * a.two_n : 0;
   p.b2_in = a.w2_bias_in;
   p.b2_out = static_cast<uint16_t*>(a.w2_bias_out);
   p.b2_numel = a.w2_bias_in ? a.w2_bias_numel : 0;
-
-  // Code rows: one warp each, enough CTAs to fill every SM several times over.
-  const int64_t sms = sm_count();
-  const int64_t cap = sms * 16;
-  const int64_t code_blocks = std::min<int64_t>((p.rows + kWarps - 1) / kWarps, cap);
-  const int64_t scale_blocks = std::min<int64_t>((p.scale_items + kThreads - 1) / kThreads, sms * 4);
   const int64_t bias_items = p.b13_numel + p.b2_numel;
-  const int64_t bias_blocks = std::min<int64_t>((bias_items + kThreads - 1) / kThreads, sms * 2);
-  p.code_blocks = static_cast<uint32_t>(code_blocks);
-  p.scale_blocks = static_cast<uint32_t>(scale_blocks);
-  const int64_t grid = code_blocks + scale_blocks + bias_blocks;
+  const int64_t bias_ctas = std::min<int64_t>((bias_items + kThreads - 1) / kThreads, sms * 2);
+  const int64_t grid = code_ctas + scale_ctas + bias_ctas;
   if (grid == 0) return cudaSuccess;
-  swap_w13_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  if (grid > INT_MAX / 2) return cudaErrorInvalidConfiguration;
+  return launch_pdl(swap_w13_kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
 }  // namespace mxfp4
