@@ -24,7 +24,10 @@ namespace mxfp4 {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kPasses = kTileRows / (2 * (kThreads / 32));
+constexpr int kElems = 16;                                  // elements per lane per pass
+constexpr int kLanesPerRow = kTileCols / kElems;            // 8
+constexpr int kRowsPerPass = (kThreads / 32) * (32 / kLanesPerRow);  // 32
+constexpr int kPasses = kTileRows / kRowsPerPass;           // 4
 
 struct DequantizeParams {
   const uint8_t* __restrict__ codes;
@@ -55,23 +58,27 @@ __device__ __forceinline__ uint4 decode8(uint32_t c, float sc) {
 }
 
 struct Tile {
-  const uint8_t* c;     // code word of this thread's pass-0 row
-  const uint8_t* s;     // 16-byte chunk row of pass 0 (pass 1 is +256 bytes)
+  const uint8_t* c;     // code bytes of this thread's pass-0 row
+  const uint8_t* s;     // the 16-byte chunk row holding this thread's 4 scale bytes
   uint8_t* y;           // output of this thread's pass-0 row
   int lim;
   bool col_ok;
 };
 
+// Lane l of warp w covers elements [16*(l%8), 16*(l%8)+16) of row
+// 4*w + l/8 (+32 per pass).  Pass i of that row sits in chunk row
+// (4*w + l/8), word i, byte (l%8)/2.
+template <bool kPersistent>
 __global__ void __launch_bounds__(kThreads) dequantize_tiles_kernel(const DequantizeParams p) {
   pdl_wait();
   pdl_release();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int seg16 = lane & 15;
-  const int blk = seg16 >> 2;
-  const int lr0 = warp * 2 + (lane >> 4);  // row in pass 0; passes add 16 rows
-  const int64_t cld16 = p.code_ld * 16;
-  const int64_t yld16 = p.y_ld * 16;
+  const int sub = lane & (kLanesPerRow - 1);
+  const int blk = sub >> 1;
+  const int lr0 = warp * (32 / kLanesPerRow) + (lane >> 3);
+  const int64_t cld_pass = p.code_ld * kRowsPerPass;
+  const int64_t yld_pass = p.y_ld * kRowsPerPass;
 
   int unit = blockIdx.x;
   if (unit >= p.n_units) return;
@@ -85,50 +92,63 @@ __global__ void __launch_bounds__(kThreads) dequantize_tiles_kernel(const Dequan
     t.lim = static_cast<int>((avail < kTileRows ? avail : kTileRows) - lr0);
     t.col_ok = kt * kTileBlocks + blk < p.sK;
     t.c = p.codes + (row0 + lr0) * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) +
-          seg16 * 4;
-    // pass i sits in chunk row (lr0 + 16*(i&1)) % 32, word (i >> 1)
+          sub * (kElems / 2);
     t.s = p.scales + static_cast<int64_t>(u) * kChunkBytes + lr0 * 16;
-    t.y = p.y + (row0 + lr0) * p.y_ld + static_cast<int64_t>(kt) * (kTileCols * 2) + seg16 * 16;
+    t.y = p.y + (row0 + lr0) * p.y_ld + static_cast<int64_t>(kt) * (kTileCols * 2) +
+          sub * (kElems * 2);
     return t;
   };
 
   Tile cur = make_tile(unit);
-  uint32_t c[kPasses];
-  uint4 srow[2];
+  uint2 c[kPasses];
 #pragma unroll
-  for (int i = 0; i < kPasses; ++i) c[i] = (cur.col_ok && 16 * i < cur.lim) ? ld_stream_u32(cur.c + i * cld16) : 0u;
-  srow[0] = ld_stream_v4(cur.s);
-  srow[1] = ld_stream_v4(cur.s + 256);
+  for (int i = 0; i < kPasses; ++i)
+    c[i] = (cur.col_ok && kRowsPerPass * i < cur.lim) ? ld_stream_v2(cur.c + i * cld_pass)
+                                                      : make_uint2(0u, 0u);
+  uint4 srow = ld_stream_v4(cur.s);
 
   for (;;) {
-    const int next_unit = unit + static_cast<int>(gridDim.x);
-    const bool has_next = next_unit < p.n_units;
+    int next_unit = 0;
+    bool has_next = false;
     Tile nxt = cur;
-    if (has_next) nxt = make_tile(next_unit);
-    const uint4 sr0 = srow[0], sr1 = srow[1];
-    if (has_next) {
-      srow[0] = ld_stream_v4(nxt.s);
-      srow[1] = ld_stream_v4(nxt.s + 256);
+    const uint4 sr = srow;
+    if constexpr (kPersistent) {
+      next_unit = unit + static_cast<int>(gridDim.x);
+      has_next = next_unit < p.n_units;
+      if (has_next) {
+        nxt = make_tile(next_unit);
+        srow = ld_stream_v4(nxt.s);
+      }
     }
 #pragma unroll
     for (int i = 0; i < kPasses; ++i) {
-      const uint4 sr = (i & 1) ? sr1 : sr0;
-      const uint32_t word = (i >> 1) == 0 ? sr.x : (i >> 1) == 1 ? sr.y : (i >> 1) == 2 ? sr.z : sr.w;
+      const uint32_t word = i == 0 ? sr.x : i == 1 ? sr.y : i == 2 ? sr.z : sr.w;
       const uint32_t s = (word >> (8 * blk)) & 0xFFu;
-      uint4 o;
+      uint4 o0, o1;
       if (s == 255u) {
-        o = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+        o0 = o1 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
       } else {
-        o = decode8(c[i], scale_from_e8m0(s));
+        const float sc = scale_from_e8m0(s);
+        o0 = decode8(c[i].x, sc);
+        o1 = decode8(c[i].y, sc);
       }
-      if (cur.col_ok && 16 * i < cur.lim) st_stream_v4(cur.y + i * yld16, o);
-      if (has_next) c[i] = (nxt.col_ok && 16 * i < nxt.lim) ? ld_stream_u32(nxt.c + i * cld16) : 0u;
+      if (cur.col_ok && kRowsPerPass * i < cur.lim) {
+        st_stream_v4(cur.y + i * yld_pass, o0);
+        st_stream_v4(cur.y + i * yld_pass + 16, o1);
+      }
+      if constexpr (kPersistent) {
+        if (has_next)
+          c[i] = (nxt.col_ok && kRowsPerPass * i < nxt.lim) ? ld_stream_v2(nxt.c + i * cld_pass)
+                                                            : make_uint2(0u, 0u);
+      }
     }
     if (!has_next) break;
     cur = nxt;
     unit = next_unit;
   }
 }
+
+constexpr bool kPersistentDequant = false;
 
 int g_occ[64];
 
@@ -147,10 +167,14 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
   p.n_units = static_cast<int32_t>(tiles * p.nKT);
-  const int64_t resident = static_cast<int64_t>(sm_count()) *
-                           resident_ctas(dequantize_tiles_kernel, kThreads, 0, g_occ);
-  const int64_t grid = p.n_units < resident ? p.n_units : resident;
-  return launch_pdl(dequantize_tiles_kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
+  auto kernel = dequantize_tiles_kernel<kPersistentDequant>;
+  int64_t grid = p.n_units;
+  if (kPersistentDequant) {
+    const int64_t resident =
+        static_cast<int64_t>(sm_count()) * resident_ctas(kernel, kThreads, 0, g_occ);
+    grid = p.n_units < resident ? p.n_units : resident;
+  }
+  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
 }  // namespace mxfp4

@@ -72,6 +72,50 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(float a0, float a1, float a2, flo
   return r;
 }
 
+// Four packed BF16x2 words (elements 0..7, element 0 in the low half of w0)
+// times a power of two `f` -> one 32-bit word of eight E2M1 codes (element
+// 2j in the low nibble of byte j), via float32 pairs and the packed f32x2
+// multiply.  Exact: a BF16 value times 2^k stays representable in float32
+// (results below 2^-126 may round, towards +-0, far below the first E2M1
+// rounding threshold 0.25).
+__device__ __forceinline__ uint32_t scale_cvt_e2m1x8(uint4 w, float f) {
+  uint32_t r;
+  asm("{\n\t"
+      ".reg .b64 p0, p1, p2, p3, fs;\n\t"
+      ".reg .b32 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+      ".reg .b8 q0, q1, q2, q3;\n\t"
+      "shl.b32 l0, %1, 16;\n\t"
+      "and.b32 h0, %1, 0xFFFF0000;\n\t"
+      "shl.b32 l1, %2, 16;\n\t"
+      "and.b32 h1, %2, 0xFFFF0000;\n\t"
+      "shl.b32 l2, %3, 16;\n\t"
+      "and.b32 h2, %3, 0xFFFF0000;\n\t"
+      "shl.b32 l3, %4, 16;\n\t"
+      "and.b32 h3, %4, 0xFFFF0000;\n\t"
+      "mov.b64 fs, {%5, %5};\n\t"
+      "mov.b64 p0, {l0, h0};\n\t"
+      "mov.b64 p1, {l1, h1};\n\t"
+      "mov.b64 p2, {l2, h2};\n\t"
+      "mov.b64 p3, {l3, h3};\n\t"
+      "mul.rn.f32x2 p0, p0, fs;\n\t"
+      "mul.rn.f32x2 p1, p1, fs;\n\t"
+      "mul.rn.f32x2 p2, p2, fs;\n\t"
+      "mul.rn.f32x2 p3, p3, fs;\n\t"
+      "mov.b64 {l0, h0}, p0;\n\t"
+      "mov.b64 {l1, h1}, p1;\n\t"
+      "mov.b64 {l2, h2}, p2;\n\t"
+      "mov.b64 {l3, h3}, p3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, h0, l0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, h1, l1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, h2, l2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, h3, l3;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t"
+      "}"
+      : "=r"(r)
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "f"(f));
+  return r;
+}
+
 // One byte of two E2M1 codes -> two halves (f16x2), low nibble in the low half.
 __device__ __forceinline__ uint32_t cvt_e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
   uint32_t r;
@@ -115,6 +159,12 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return v;
 }
 
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
   uint32_t v;
   asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
@@ -124,6 +174,9 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
 // Streaming stores (evict-first: outputs are not re-read by this kernel).
 __device__ __forceinline__ void st_stream_u32(void* p, uint32_t v) {
   asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_stream_v2(void* p, uint2 v) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 __device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),

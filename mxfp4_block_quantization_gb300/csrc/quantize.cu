@@ -29,8 +29,11 @@ namespace mxfp4 {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kPasses = kTileRows / (2 * (kThreads / 32));  // 8 passes of 16 rows
-constexpr int kSegSmemMaxEntries = 2048;                   // E+1 staged in shared memory
+constexpr int kElems = 16;                                  // elements per lane per pass
+constexpr int kLanesPerRow = kTileCols / kElems;            // 8 lanes cover 128 columns
+constexpr int kRowsPerPass = (kThreads / 32) * (32 / kLanesPerRow);  // 32 rows
+constexpr int kPasses = kTileRows / kRowsPerPass;           // 4 passes
+constexpr int kSegSmemMaxEntries = 2048;                    // E+1 staged in shared memory
 
 struct QuantizeParams {
   const uint8_t* __restrict__ x;  // BF16 bytes
@@ -51,8 +54,8 @@ struct QuantizeParams {
 // Where one thread reads and writes for one tile.
 struct Tile {
   const uint8_t* x;  // element 0 of this thread's pass-0 row
-  uint8_t* c;        // code word of this thread's pass-0 row
-  int lim;           // pass i is a real row when 16*i < lim
+  uint8_t* c;        // code bytes of this thread's pass-0 row
+  int lim;           // pass i is a real row when 32*i < lim
   bool col_ok;       // this thread's block is a real scale column
   int unit;          // tile index = scale chunk index
 };
@@ -70,7 +73,9 @@ __device__ __forceinline__ int find_segment(Load P, int E, int prow) {
   return lo;
 }
 
-template <bool kGrouped>
+// Lane l of warp w covers elements [16*(l%8), 16*(l%8)+16) of row
+// 4*w + l/8 (+32 per pass): two lanes per 32-element block.
+template <bool kGrouped, bool kPersistent>
 __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const QuantizeParams p) {
   __shared__ __align__(16) uint8_t chunk[2][kChunkBytes];
   extern __shared__ int32_t seg[];  // grouped: [0, E] offsets, [E+1, 2E+1] padded
@@ -80,18 +85,19 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int seg16 = lane & 15;      // 8-element segment inside the 128 columns
-  const int blk = seg16 >> 2;       // scale column inside the tile (0..3)
-  const int lr0 = warp * 2 + (lane >> 4);  // this thread's row in pass 0
-  const int64_t ldx16 = p.ldx_bytes * 16;
-  const int64_t cld16 = p.code_ld * 16;
+  const int sub = lane & (kLanesPerRow - 1);  // 16-element segment inside the 128 columns
+  const int blk = sub >> 1;                   // scale column inside the tile (0..3)
+  const int lr0 = warp * (32 / kLanesPerRow) + (lane >> 3);  // row in pass 0 (0..31)
+  const int sbyte = lr0 * 16 + blk;           // chunk byte of pass 0; pass i adds 4*i
+  const int64_t ldx_pass = p.ldx_bytes * kRowsPerPass;
+  const int64_t cld_pass = p.code_ld * kRowsPerPass;
 
   int n_units = p.n_units;
   if constexpr (kGrouped) {
     const int total_padded = __ldg(p.padded + p.E);
     if (total_padded < 0) return;  // offsets rejected by the offsets kernel
     n_units = (total_padded / kTileRows) * p.nKT;
-    if (p.seg_in_smem) {
+    if (kPersistent && p.seg_in_smem) {
       for (int i = threadIdx.x; i <= p.E; i += kThreads) {
         seg[i] = __ldg(p.offsets + i);
         seg[p.E + 1 + i] = __ldg(p.padded + i);
@@ -110,7 +116,7 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
     if constexpr (kGrouped) {
       const int prow = mt * kTileRows;
       int e, seg_start, pad_start, seg_end;
-      if (p.seg_in_smem) {
+      if (kPersistent && p.seg_in_smem) {
         const int32_t* P = seg + p.E + 1;
         e = find_segment([&](int i) { return P[i]; }, p.E, prow);
         seg_start = seg[e];
@@ -132,57 +138,67 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
     const int64_t avail = row_end - row0;
     t.lim = static_cast<int>((avail < kTileRows ? avail : kTileRows) - lr0);
     t.col_ok = kt * kTileBlocks + blk < p.sK;
-    t.x = p.x + r * p.ldx_bytes + static_cast<int64_t>(kt) * (kTileCols * 2) + seg16 * 16;
-    t.c = p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) + seg16 * 4;
+    t.x = p.x + r * p.ldx_bytes + static_cast<int64_t>(kt) * (kTileCols * 2) + sub * (kElems * 2);
+    t.c = p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) + sub * (kElems / 2);
     t.unit = u;
     return t;
   };
 
   Tile cur = make_tile(unit);
-  uint4 v[kPasses];
+  uint4 v[kPasses][2];
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
-    v[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (cur.col_ok && 16 * i < cur.lim) v[i] = ld_stream_v4(cur.x + i * ldx16);
+    v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
+    if (cur.col_ok && kRowsPerPass * i < cur.lim) {
+      v[i][0] = ld_stream_v4(cur.x + i * ldx_pass);
+      v[i][1] = ld_stream_v4(cur.x + i * ldx_pass + 16);
+    }
   }
 
   int buf = 0;
   for (;;) {
-    const int next_unit = unit + static_cast<int>(gridDim.x);
-    const bool has_next = next_unit < n_units;
+    int next_unit = 0;
+    bool has_next = false;
     Tile nxt = cur;
-    if (has_next) nxt = make_tile(next_unit);
+    if constexpr (kPersistent) {
+      next_unit = unit + static_cast<int>(gridDim.x);
+      has_next = next_unit < n_units;
+      if (has_next) nxt = make_tile(next_unit);
+    }
 
 #pragma unroll
     for (int i = 0; i < kPasses; ++i) {
       // block absmax: |x| per half with max.xorsign.abs, sign bits cleared,
       // then the larger half (unsigned order of non-negative BF16 patterns
-      // is the order of their magnitudes)
-      const uint32_t h = max_abs_bf16x2(max_abs_bf16x2(v[i].x, v[i].y),
-                                        max_abs_bf16x2(v[i].z, v[i].w)) & 0x7FFF7FFFu;
+      // is the order of their magnitudes), then the partner lane's half block
+      const uint32_t h =
+          max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(v[i][0].x, v[i][0].y),
+                                        max_abs_bf16x2(v[i][0].z, v[i][0].w)),
+                         max_abs_bf16x2(max_abs_bf16x2(v[i][1].x, v[i][1].y),
+                                        max_abs_bf16x2(v[i][1].z, v[i][1].w))) &
+          0x7FFF7FFFu;
       uint32_t m = max(h & 0xFFFFu, h >> 16);
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
       const uint32_t s = e8m0_from_absmax_bf16(m);
-      if ((lane & 3) == 0) chunk[buf][chunk_offset(lr0 + 16 * i, blk)] = static_cast<uint8_t>(s);
+      if ((lane & 1) == 0) chunk[buf][sbyte + 4 * i] = static_cast<uint8_t>(s);
 
-      // x * 2^(127-s): exact power-of-two scaling of BF16 values in float32
+      // x * 2^(127-s), then round to E2M1; blocks with s == 0 emit zeros
       const float inv = inv_scale_from_e8m0(s);
-      uint32_t code = cvt_e2m1x8(__uint_as_float(v[i].x << 16) * inv,
-                                 __uint_as_float(v[i].x & 0xFFFF0000u) * inv,
-                                 __uint_as_float(v[i].y << 16) * inv,
-                                 __uint_as_float(v[i].y & 0xFFFF0000u) * inv,
-                                 __uint_as_float(v[i].z << 16) * inv,
-                                 __uint_as_float(v[i].z & 0xFFFF0000u) * inv,
-                                 __uint_as_float(v[i].w << 16) * inv,
-                                 __uint_as_float(v[i].w & 0xFFFF0000u) * inv);
-      if (s == 0u) code = 0u;
-      if (cur.col_ok && 16 * i < cur.lim) st_stream_u32(cur.c + i * cld16, code);
+      uint2 code;
+      code.x = scale_cvt_e2m1x8(v[i][0], inv);
+      code.y = scale_cvt_e2m1x8(v[i][1], inv);
+      if (s == 0u) code = make_uint2(0u, 0u);
+      if (cur.col_ok && kRowsPerPass * i < cur.lim) st_stream_v2(cur.c + i * cld_pass, code);
 
-      // refill this slot with the same pass of the next tile
-      if (has_next) {
-        v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (nxt.col_ok && 16 * i < nxt.lim) v[i] = ld_stream_v4(nxt.x + i * ldx16);
+      if constexpr (kPersistent) {
+        // refill this slot with the same pass of the next tile
+        if (has_next) {
+          v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
+          if (nxt.col_ok && kRowsPerPass * i < nxt.lim) {
+            v[i][0] = ld_stream_v4(nxt.x + i * ldx_pass);
+            v[i][1] = ld_stream_v4(nxt.x + i * ldx_pass + 16);
+          }
+        }
       }
     }
 
@@ -257,6 +273,11 @@ grouped_offsets_kernel(const int32_t* __restrict__ off, int32_t E, int64_t total
   if (tid == 0 && status != nullptr) *status = s_bad ? MXFP4_EOFFSETS : MXFP4_OK;
 }
 
+// One tile per CTA (the hardware scheduler balances the tiles) or a
+// persistent grid walking the tiles with loads pipelined one tile ahead.
+constexpr bool kPersistentDense = false;
+constexpr bool kPersistentGrouped = true;
+
 int g_occ_dense[64];
 int g_occ_grouped[64];
 int g_occ_grouped_smem[64];
@@ -276,12 +297,14 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
   p.n_units = static_cast<int32_t>(tiles * p.nKT);
-  const int64_t resident =
-      static_cast<int64_t>(sm_count()) *
-      resident_ctas(quantize_tiles_kernel<false>, kThreads, 0, g_occ_dense);
-  const int64_t grid = p.n_units < resident ? p.n_units : resident;
-  return launch_pdl(quantize_tiles_kernel<false>, static_cast<unsigned>(grid), kThreads, 0, stream,
-                    p);
+  auto kernel = quantize_tiles_kernel<false, kPersistentDense>;
+  int64_t grid = p.n_units;
+  if (kPersistentDense) {
+    const int64_t resident = static_cast<int64_t>(sm_count()) *
+                             resident_ctas(kernel, kThreads, 0, g_occ_dense);
+    grid = p.n_units < resident ? p.n_units : resident;
+  }
+  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
 cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
@@ -303,17 +326,20 @@ cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K
   p.offsets = offsets;
   p.padded = scale_row_offsets;
   p.E = E;
-  p.seg_in_smem = (E + 1 <= kSegSmemMaxEntries) ? 1 : 0;
+  auto kernel = quantize_tiles_kernel<true, kPersistentGrouped>;
+  p.seg_in_smem = (kPersistentGrouped && E + 1 <= kSegSmemMaxEntries) ? 1 : 0;
   const size_t smem = p.seg_in_smem ? static_cast<size_t>(E + 1) * 2 * sizeof(int32_t) : 0;
-  const int occ = p.seg_in_smem
-                      ? resident_ctas(quantize_tiles_kernel<true>, kThreads,
-                                      kSegSmemMaxEntries * 2 * sizeof(int32_t), g_occ_grouped_smem)
-                      : resident_ctas(quantize_tiles_kernel<true>, kThreads, 0, g_occ_grouped);
   const int64_t bound_units = bound_tiles * p.nKT;
-  const int64_t resident = static_cast<int64_t>(sm_count()) * occ;
-  const int64_t grid = bound_units < resident ? bound_units : resident;
-  return launch_pdl(quantize_tiles_kernel<true>, static_cast<unsigned>(grid), kThreads, smem,
-                    stream, p);
+  int64_t grid = bound_units;
+  if (kPersistentGrouped) {
+    const int occ = p.seg_in_smem
+                        ? resident_ctas(kernel, kThreads, kSegSmemMaxEntries * 2 * sizeof(int32_t),
+                                        g_occ_grouped_smem)
+                        : resident_ctas(kernel, kThreads, 0, g_occ_grouped);
+    const int64_t resident = static_cast<int64_t>(sm_count()) * occ;
+    grid = bound_units < resident ? bound_units : resident;
+  }
+  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, smem, stream, p);
 }
 
 }  // namespace mxfp4
