@@ -46,23 +46,6 @@ cudaError_t launch_swap_w13(const SwapArgs& a, cudaStream_t stream);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
-// Resident CTAs per SM of `kernel` at `threads` threads and `smem` dynamic
-// shared bytes on the current device (cached per device by the caller's
-// static `cache`; at least 1).
-template <typename Kernel>
-int resident_ctas(Kernel kernel, int threads, size_t smem, int (&cache)[64]) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (cache[dev] == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess ||
-        n <= 0)
-      n = 1;
-    cache[dev] = n;
-  }
-  return cache[dev];
-}
-
 // Launch with programmatic dependent launch allowed: the grid may be
 // scheduled while the previous kernel of the stream drains; every kernel of
 // this library executes griddepcontrol.wait before touching global memory,

@@ -7,18 +7,15 @@
 // snippet (tiled layout).  Element rounding: OCP MX E2M1, round to nearest
 // even, saturating at +-6; blocks whose scale exponent is 0 emit zero codes.
 //
-// Work decomposition.  The unit of work is one 128-row x 128-column tile:
-// exactly the rows and scale columns of one 512-byte chunk of the tiled scale
-// layout, so the chunk is assembled in shared memory and leaves the SM as 32
-// coalesced 16-byte stores.  Lane l of a warp covers 8 BF16 elements (one
-// 16-byte load) of row (2*warp + l/16) of a 16-row pass; four lanes form one
-// 32-element block, reduced with two xor-shuffles.
-//
-// The grid is persistent (resident CTAs x SMs) and walks the tiles
-// round-robin.  Loads are software-pipelined across tiles: as soon as pass i
-// of the current tile has been consumed, its register slot is refilled with
-// pass i of the CTA's next tile, so every thread keeps eight 16-byte loads in
-// flight from start to finish and all CTAs end within one tile of each other.
+// Work decomposition.  One CTA (256 threads) owns one 128-row x 128-column
+// tile: exactly the rows and scale columns of one 512-byte chunk of the
+// tiled scale layout, so the chunk is assembled in shared memory and leaves
+// the SM as 32 coalesced 16-byte stores.  Lane l of warp w covers 16 BF16
+// elements (two 16-byte loads) of row 4*w + l/8 in each of 4 passes of 32
+// rows; two lanes form one 32-element block, reduced with one xor-shuffle.
+// All four passes' loads are issued before any compute (32 KB in flight per
+// CTA, five CTAs per SM).  Launches use programmatic dependent launch, so a
+// grid is already resident when its predecessor in the stream drains.
 #include <cuda_runtime.h>
 
 #include "mxfp4_device.cuh"
@@ -33,7 +30,6 @@ constexpr int kElems = 16;                                  // elements per lane
 constexpr int kLanesPerRow = kTileCols / kElems;            // 8 lanes cover 128 columns
 constexpr int kRowsPerPass = (kThreads / 32) * (32 / kLanesPerRow);  // 32 rows
 constexpr int kPasses = kTileRows / kRowsPerPass;           // 4 passes
-constexpr int kSegSmemMaxEntries = 2048;                    // E+1 staged in shared memory
 
 struct QuantizeParams {
   const uint8_t* __restrict__ x;  // BF16 bytes
@@ -44,173 +40,106 @@ struct QuantizeParams {
   uint8_t* __restrict__ scales;
   int32_t sK;                     // scale columns K/32
   int32_t nKT;                    // k tiles ceil(sK/4)
-  int32_t n_units;                // dense: tiles * nKT
+  int32_t n_units;                // dense: tiles * nKT (= grid)
   const int32_t* __restrict__ offsets;  // grouped: input row offsets [E+1]
   const int32_t* __restrict__ padded;   // grouped: padded row offsets [E+1]
   int32_t E;
-  int32_t seg_in_smem;            // grouped: offsets staged in dynamic shared memory
-};
-
-// Where one thread reads and writes for one tile.
-struct Tile {
-  const uint8_t* x;  // element 0 of this thread's pass-0 row
-  uint8_t* c;        // code bytes of this thread's pass-0 row
-  int lim;           // pass i is a real row when 32*i < lim
-  bool col_ok;       // this thread's block is a real scale column
-  int unit;          // tile index = scale chunk index
 };
 
 // Segment holding padded row `prow`: the last e in [0, E) with P[e] <= prow
 // (empty segments share their start with the next one, so the last such e
-// is never empty when prow < P[E]).
-template <typename Load>
-__device__ __forceinline__ int find_segment(Load P, int E, int prow) {
+// is never empty when prow < P[E]).  P is small and read by every CTA, so
+// the probes hit L1/L2.
+__device__ __forceinline__ int find_segment(const int32_t* __restrict__ P, int E, int prow) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (P(mid) <= prow) lo = mid; else hi = mid - 1;
+    if (__ldg(P + mid) <= prow) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
 
 // Lane l of warp w covers elements [16*(l%8), 16*(l%8)+16) of row
 // 4*w + l/8 (+32 per pass): two lanes per 32-element block.
-template <bool kGrouped, bool kPersistent>
+template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const QuantizeParams p) {
-  __shared__ __align__(16) uint8_t chunk[2][kChunkBytes];
-  extern __shared__ int32_t seg[];  // grouped: [0, E] offsets, [E+1, 2E+1] padded
+  __shared__ __align__(16) uint8_t chunk[kChunkBytes];
 
   pdl_wait();
   pdl_release();
+
+  const int unit = blockIdx.x;
+  const int mt = unit / p.nKT;
+  const int kt = unit - mt * p.nKT;
+  int64_t row0, row_end;
+  if constexpr (kGrouped) {
+    const int total_padded = __ldg(p.padded + p.E);
+    const int prow = mt * kTileRows;
+    if (total_padded < 0 || prow >= total_padded) return;  // rejected offsets / past the end
+    const int e = find_segment(p.padded, p.E, prow);
+    row0 = static_cast<int64_t>(__ldg(p.offsets + e)) + (prow - __ldg(p.padded + e));
+    row_end = __ldg(p.offsets + e + 1);
+  } else {
+    row0 = static_cast<int64_t>(mt) * kTileRows;
+    row_end = p.M;
+  }
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int sub = lane & (kLanesPerRow - 1);  // 16-element segment inside the 128 columns
   const int blk = sub >> 1;                   // scale column inside the tile (0..3)
   const int lr0 = warp * (32 / kLanesPerRow) + (lane >> 3);  // row in pass 0 (0..31)
-  const int sbyte = lr0 * 16 + blk;           // chunk byte of pass 0; pass i adds 4*i
+  const int64_t avail = row_end - row0;
+  const int lim = static_cast<int>((avail < kTileRows ? avail : kTileRows) - lr0);
+  const bool col_ok = kt * kTileBlocks + blk < p.sK;
+  const int64_t r = row0 + lr0;
+  const uint8_t* xp =
+      p.x + r * p.ldx_bytes + static_cast<int64_t>(kt) * (kTileCols * 2) + sub * (kElems * 2);
+  uint8_t* cp =
+      p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) + sub * (kElems / 2);
   const int64_t ldx_pass = p.ldx_bytes * kRowsPerPass;
   const int64_t cld_pass = p.code_ld * kRowsPerPass;
 
-  int n_units = p.n_units;
-  if constexpr (kGrouped) {
-    const int total_padded = __ldg(p.padded + p.E);
-    if (total_padded < 0) return;  // offsets rejected by the offsets kernel
-    n_units = (total_padded / kTileRows) * p.nKT;
-    if (kPersistent && p.seg_in_smem) {
-      for (int i = threadIdx.x; i <= p.E; i += kThreads) {
-        seg[i] = __ldg(p.offsets + i);
-        seg[p.E + 1 + i] = __ldg(p.padded + i);
-      }
-      __syncthreads();
-    }
-  }
-  int unit = blockIdx.x;
-  if (unit >= n_units) return;
-
-  auto make_tile = [&](int u) {
-    Tile t;
-    const int mt = u / p.nKT;
-    const int kt = u - mt * p.nKT;
-    int64_t row0, row_end;
-    if constexpr (kGrouped) {
-      const int prow = mt * kTileRows;
-      int e, seg_start, pad_start, seg_end;
-      if (kPersistent && p.seg_in_smem) {
-        const int32_t* P = seg + p.E + 1;
-        e = find_segment([&](int i) { return P[i]; }, p.E, prow);
-        seg_start = seg[e];
-        seg_end = seg[e + 1];
-        pad_start = P[e];
-      } else {
-        e = find_segment([&](int i) { return __ldg(p.padded + i); }, p.E, prow);
-        seg_start = __ldg(p.offsets + e);
-        seg_end = __ldg(p.offsets + e + 1);
-        pad_start = __ldg(p.padded + e);
-      }
-      row0 = static_cast<int64_t>(seg_start) + (prow - pad_start);
-      row_end = seg_end;
-    } else {
-      row0 = static_cast<int64_t>(mt) * kTileRows;
-      row_end = p.M;
-    }
-    const int64_t r = row0 + lr0;
-    const int64_t avail = row_end - row0;
-    t.lim = static_cast<int>((avail < kTileRows ? avail : kTileRows) - lr0);
-    t.col_ok = kt * kTileBlocks + blk < p.sK;
-    t.x = p.x + r * p.ldx_bytes + static_cast<int64_t>(kt) * (kTileCols * 2) + sub * (kElems * 2);
-    t.c = p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) + sub * (kElems / 2);
-    t.unit = u;
-    return t;
-  };
-
-  Tile cur = make_tile(unit);
   uint4 v[kPasses][2];
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
     v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
-    if (cur.col_ok && kRowsPerPass * i < cur.lim) {
-      v[i][0] = ld_stream_v4(cur.x + i * ldx_pass);
-      v[i][1] = ld_stream_v4(cur.x + i * ldx_pass + 16);
+    if (col_ok && kRowsPerPass * i < lim) {
+      v[i][0] = ld_stream_v4(xp + i * ldx_pass);
+      v[i][1] = ld_stream_v4(xp + i * ldx_pass + 16);
     }
   }
 
-  int buf = 0;
-  for (;;) {
-    int next_unit = 0;
-    bool has_next = false;
-    Tile nxt = cur;
-    if constexpr (kPersistent) {
-      next_unit = unit + static_cast<int>(gridDim.x);
-      has_next = next_unit < n_units;
-      if (has_next) nxt = make_tile(next_unit);
-    }
-
 #pragma unroll
-    for (int i = 0; i < kPasses; ++i) {
-      // block absmax: |x| per half with max.xorsign.abs, sign bits cleared,
-      // then the larger half (unsigned order of non-negative BF16 patterns
-      // is the order of their magnitudes), then the partner lane's half block
-      const uint32_t h =
-          max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(v[i][0].x, v[i][0].y),
-                                        max_abs_bf16x2(v[i][0].z, v[i][0].w)),
-                         max_abs_bf16x2(max_abs_bf16x2(v[i][1].x, v[i][1].y),
-                                        max_abs_bf16x2(v[i][1].z, v[i][1].w))) &
-          0x7FFF7FFFu;
-      uint32_t m = max(h & 0xFFFFu, h >> 16);
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      const uint32_t s = e8m0_from_absmax_bf16(m);
-      if ((lane & 1) == 0) chunk[buf][sbyte + 4 * i] = static_cast<uint8_t>(s);
+  for (int i = 0; i < kPasses; ++i) {
+    // block absmax: |x| per half with max.xorsign.abs, sign bits cleared,
+    // then the larger half (unsigned order of non-negative BF16 patterns is
+    // the order of their magnitudes), then the partner lane's half block
+    const uint32_t h =
+        max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(v[i][0].x, v[i][0].y),
+                                      max_abs_bf16x2(v[i][0].z, v[i][0].w)),
+                       max_abs_bf16x2(max_abs_bf16x2(v[i][1].x, v[i][1].y),
+                                      max_abs_bf16x2(v[i][1].z, v[i][1].w))) &
+        0x7FFF7FFFu;
+    uint32_t m = max(h & 0xFFFFu, h >> 16);
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    const uint32_t s = e8m0_from_absmax_bf16(m);
+    // rows of pass i sit in chunk row lr0 (outerM), word i (innerM)
+    if ((lane & 1) == 0) chunk[chunk_offset(lr0 + kRowsPerPass * i, blk)] = static_cast<uint8_t>(s);
 
-      // x * 2^(127-s), then round to E2M1; blocks with s == 0 emit zeros
-      const float inv = inv_scale_from_e8m0(s);
-      uint2 code;
-      code.x = scale_cvt_e2m1x8(v[i][0], inv);
-      code.y = scale_cvt_e2m1x8(v[i][1], inv);
-      if (s == 0u) code = make_uint2(0u, 0u);
-      if (cur.col_ok && kRowsPerPass * i < cur.lim) st_stream_v2(cur.c + i * cld_pass, code);
+    // x * 2^(127-s), then round to E2M1; blocks with s == 0 emit zeros
+    const float inv = inv_scale_from_e8m0(s);
+    uint2 code;
+    code.x = scale_cvt_e2m1x8(v[i][0], inv);
+    code.y = scale_cvt_e2m1x8(v[i][1], inv);
+    if (s == 0u) code = make_uint2(0u, 0u);
+    if (col_ok && kRowsPerPass * i < lim) st_stream_v2(cp + i * cld_pass, code);
+  }
 
-      if constexpr (kPersistent) {
-        // refill this slot with the same pass of the next tile
-        if (has_next) {
-          v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
-          if (nxt.col_ok && kRowsPerPass * i < nxt.lim) {
-            v[i][0] = ld_stream_v4(nxt.x + i * ldx_pass);
-            v[i][1] = ld_stream_v4(nxt.x + i * ldx_pass + 16);
-          }
-        }
-      }
-    }
-
-    __syncthreads();
-    if (threadIdx.x < kChunkBytes / 16) {
-      const uint4 w = reinterpret_cast<const uint4*>(chunk[buf])[threadIdx.x];
-      st_stream_v4(p.scales + static_cast<int64_t>(cur.unit) * kChunkBytes + threadIdx.x * 16, w);
-    }
-    if (!has_next) break;
-    cur = nxt;
-    unit = next_unit;
-    buf ^= 1;
+  __syncthreads();
+  if (threadIdx.x < kChunkBytes / 16) {
+    const uint4 w = reinterpret_cast<const uint4*>(chunk)[threadIdx.x];
+    st_stream_v4(p.scales + static_cast<int64_t>(unit) * kChunkBytes + threadIdx.x * 16, w);
   }
 }
 
@@ -273,15 +202,6 @@ grouped_offsets_kernel(const int32_t* __restrict__ off, int32_t E, int64_t total
   if (tid == 0 && status != nullptr) *status = s_bad ? MXFP4_EOFFSETS : MXFP4_OK;
 }
 
-// One tile per CTA (the hardware scheduler balances the tiles) or a
-// persistent grid walking the tiles with loads pipelined one tile ahead.
-constexpr bool kPersistentDense = false;
-constexpr bool kPersistentGrouped = true;
-
-int g_occ_dense[64];
-int g_occ_grouped[64];
-int g_occ_grouped_smem[64];
-
 }  // namespace
 
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
@@ -297,14 +217,8 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
   p.n_units = static_cast<int32_t>(tiles * p.nKT);
-  auto kernel = quantize_tiles_kernel<false, kPersistentDense>;
-  int64_t grid = p.n_units;
-  if (kPersistentDense) {
-    const int64_t resident = static_cast<int64_t>(sm_count()) *
-                             resident_ctas(kernel, kThreads, 0, g_occ_dense);
-    grid = p.n_units < resident ? p.n_units : resident;
-  }
-  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
+  return launch_pdl(quantize_tiles_kernel<false>, static_cast<unsigned>(p.n_units), kThreads, 0,
+                    stream, p);
 }
 
 cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
@@ -326,20 +240,9 @@ cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K
   p.offsets = offsets;
   p.padded = scale_row_offsets;
   p.E = E;
-  auto kernel = quantize_tiles_kernel<true, kPersistentGrouped>;
-  p.seg_in_smem = (kPersistentGrouped && E + 1 <= kSegSmemMaxEntries) ? 1 : 0;
-  const size_t smem = p.seg_in_smem ? static_cast<size_t>(E + 1) * 2 * sizeof(int32_t) : 0;
-  const int64_t bound_units = bound_tiles * p.nKT;
-  int64_t grid = bound_units;
-  if (kPersistentGrouped) {
-    const int occ = p.seg_in_smem
-                        ? resident_ctas(kernel, kThreads, kSegSmemMaxEntries * 2 * sizeof(int32_t),
-                                        g_occ_grouped_smem)
-                        : resident_ctas(kernel, kThreads, 0, g_occ_grouped);
-    const int64_t resident = static_cast<int64_t>(sm_count()) * occ;
-    grid = bound_units < resident ? bound_units : resident;
-  }
-  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, smem, stream, p);
+  const int64_t grid = bound_tiles * p.nKT;  // CTAs past the real padded total exit at once
+  return launch_pdl(quantize_tiles_kernel<true>, static_cast<unsigned>(grid), kThreads, 0, stream,
+                    p);
 }
 
 }  // namespace mxfp4
