@@ -339,7 +339,27 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     nb = 2 * total * K + total * K // 2 + padded * (K // 32) + 4 * (E + 1)
     out["grouped_moe_131072x7168_E384"] = entry(
         nb, ms, 2, f"{padded} padded scale rows; offsets kernel + quantize kernel")
-    del g, codes, scales
+
+    # the same MoE batch with the dispatch gather fused in: token rows
+    # [16384, 7168] + int32 route->token indices, against the unfused pair
+    # (torch index_select materialising the 1.9 GB permuted matrix, then the
+    # grouped quantize)
+    T = g.x_tokens.shape[0]
+    xg = torch.empty_like(g.x)
+    ms_fused = time_launches(
+        lambda i: mx.mxfp4_quantize_grouped_gather(g.x_tokens, g.row_index, g.offsets, codes,
+                                                   scales, sro, st, stream), 30, stream)
+    ms_unfused = time_launches(
+        lambda i: (torch.index_select(g.x_tokens, 0, g.row_index, out=xg),
+                   mx.mxfp4_quantize_grouped(xg, g.offsets, codes, scales, sro, st, stream)),
+        30, stream)
+    nb = 2 * T * K + 4 * total + total * K // 2 + padded * (K // 32) + 4 * (E + 1)
+    e_ = entry(nb, ms_fused, 2, "bytes = token rows read once + indices + codes + scales; "
+               "every token row is read by its 8 routes (L2 serves the repeats)")
+    e_["unfused_us_per_call"] = round(ms_unfused * 1e3, 2)
+    e_["speedup_vs_unfused"] = round(ms_unfused / ms_fused, 3)
+    out["grouped_gather_moe_16384tok_top8_E384"] = e_
+    del g, codes, scales, xg
 
     # expert weights: w13 [128, 1536, 2048], w2 [128, 2048, 768], then the swap
     w = W.expert_weights(3, device="cuda")

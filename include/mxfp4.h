@@ -29,8 +29,9 @@
  *     input/output ranges) are reported synchronously through the return
  *     value, before anything is enqueued; outputs are then untouched.
  *   - A failed kernel launch returns MXFP4_ECUDA.
- *   - Errors only the device can see (malformed expert offsets) are written
- *     to a caller-provided device status word.
+ *   - Errors only the device can see (malformed expert offsets, gather
+ *     indices out of range) are written to a caller-provided device status
+ *     word.
  *   - Size 0 (M == 0, K == 0, E == 0 with no rows) is a valid no-op.
  *   - No kernel of this library waits on another CTA or on the host.
  */
@@ -44,7 +45,8 @@
 extern "C" {
 #endif
 
-/* Return codes.  MXFP4_EOFFSETS is only ever written to a device status word. */
+/* Return codes.  MXFP4_EOFFSETS and MXFP4_EINDEX are only ever written to a
+ * device status word. */
 typedef enum {
   MXFP4_OK = 0,
   MXFP4_EINVAL = -1,   /* NULL pointer, negative size, bad flag value            */
@@ -52,7 +54,8 @@ typedef enum {
   MXFP4_ESHAPE = -3,   /* K % 32 != 0, ldx < K, odd two_n, size overflow          */
   MXFP4_EALIAS = -4,   /* an output byte range overlaps an input or another output */
   MXFP4_ECUDA = -5,    /* the CUDA runtime refused a launch                        */
-  MXFP4_EOFFSETS = -6  /* device-detected: expert offsets not 0 = o[0] <= ... <= o[E] = rows */
+  MXFP4_EOFFSETS = -6, /* device-detected: expert offsets not 0 = o[0] <= ... <= o[E] = rows */
+  MXFP4_EINDEX = -7    /* device-detected: a gather row index outside [0, num_src_rows) */
 } mxfp4_status;
 
 /* Bytes of the 128x4-tiled scale buffer of an [M, K] matrix:
@@ -121,6 +124,31 @@ int mxfp4_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
                            uint8_t* codes, uint8_t* scales,
                            int32_t* scale_row_offsets, int32_t* status,
                            void* stream);
+
+/* mxfp4_quantize_grouped_gather — MoE dispatch permutation fused into the
+ * grouped quantize: output row r is source row row_index[r] of x.  The result
+ * equals mxfp4_quantize_grouped applied to the gathered matrix
+ * x[row_index[0..total_rows)], without writing or reading that BF16 matrix.
+ * [PR43557] "Implementation breakdown" item 3 (experts quant of the routed,
+ * expert-sorted activations).
+ *
+ * x                  BF16 source rows [num_src_rows, K], row stride ldx
+ *                    elements (ldx >= K, ldx % 8 == 0), 16-byte aligned.
+ * row_index          DEVICE int32 [total_rows]: source row of every output
+ *                    row (e.g. the token of each expert-sorted route).
+ * expert_offsets, E, codes, scales, scale_row_offsets: as in
+ *                    mxfp4_quantize_grouped, over the total_rows output rows.
+ * status             DEVICE int32, output, may be NULL: MXFP4_OK,
+ *                    MXFP4_EOFFSETS (as in mxfp4_quantize_grouped), or
+ *                    MXFP4_EINDEX when some row_index is outside
+ *                    [0, num_src_rows): such rows are quantized as zero rows
+ *                    and no out-of-range memory is read.
+ */
+int mxfp4_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
+                                  const int32_t* row_index, int64_t total_rows,
+                                  const int32_t* expert_offsets, int32_t E, uint8_t* codes,
+                                  uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
+                                  void* stream);
 
 /* mxfp4_dequantize — packed codes + tiled scales -> BF16 [M, K].
  *

@@ -29,7 +29,8 @@ __all__ = [
     "mxfp4_quantize", "mxfp4_quantize_grouped", "mxfp4_dequantize", "mxfp4_swap_w13",
     "mxfp4_status_string", "mxfp4_version", "quantize", "quantize_grouped", "dequantize",
     "swap_w13", "MXFP4_OK", "MXFP4_EINVAL", "MXFP4_EALIGN", "MXFP4_ESHAPE", "MXFP4_EALIAS",
-    "MXFP4_ECUDA", "MXFP4_EOFFSETS",
+    "MXFP4_ECUDA", "MXFP4_EOFFSETS", "MXFP4_EINDEX", "mxfp4_quantize_grouped_gather",
+    "quantize_grouped_gather",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300.so")
@@ -41,6 +42,7 @@ MXFP4_ESHAPE = -3
 MXFP4_EALIAS = -4
 MXFP4_ECUDA = -5
 MXFP4_EOFFSETS = -6
+MXFP4_EINDEX = -7
 
 
 class MXFP4Error(RuntimeError):
@@ -66,6 +68,9 @@ def _load():
     L.mxfp4_quantize.argtypes = [vp, i64, i64, i64, vp, vp, vp]
     L.mxfp4_quantize_grouped.restype = ctypes.c_int
     L.mxfp4_quantize_grouped.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp]
+    L.mxfp4_quantize_grouped_gather.restype = ctypes.c_int
+    L.mxfp4_quantize_grouped_gather.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, vp, vp,
+                                                vp, vp]
     L.mxfp4_dequantize.restype = ctypes.c_int
     L.mxfp4_dequantize.argtypes = [vp, vp, i64, i64, vp, vp]
     L.mxfp4_swap_w13.restype = ctypes.c_int
@@ -154,6 +159,29 @@ def mxfp4_quantize_grouped(x, expert_offsets, codes, scales, scale_row_offsets, 
                                        _stream(stream, x.device)), "mxfp4_quantize_grouped")
 
 
+def mxfp4_quantize_grouped_gather(x, row_index, expert_offsets, codes, scales, scale_row_offsets,
+                                  status=None, stream=None) -> None:
+    """Grouped quantize of the rows ``x[row_index]`` (int32 device indices)
+    without materialising the gathered BF16 matrix."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("row_index", row_index, torch.int32)
+    _need_cuda("expert_offsets", expert_offsets, torch.int32)
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    _need_cuda("scale_row_offsets", scale_row_offsets, torch.int32)
+    _need_cuda("status", status, torch.int32)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    if not row_index.is_contiguous():
+        raise ValueError("row_index must be contiguous")
+    n_src, K = x.shape
+    E = expert_offsets.numel() - 1
+    _check(_lib.mxfp4_quantize_grouped_gather(
+        _ptr(x), n_src, K, x.stride(0), _ptr(row_index), row_index.numel(), _ptr(expert_offsets),
+        E, _ptr(codes), _ptr(scales), _ptr(scale_row_offsets), _ptr(status),
+        _stream(stream, x.device)), "mxfp4_quantize_grouped_gather")
+
+
 def mxfp4_dequantize(codes, scales, M: int, K: int, y, stream=None) -> None:
     """``codes`` [M, K/2] + tiled ``scales`` -> BF16 ``y`` [M, K] (contiguous)."""
     _need_cuda("codes", codes, torch.uint8)
@@ -206,6 +234,21 @@ def quantize_grouped(x, expert_offsets, stream=None):
     sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
     status = torch.empty(1, dtype=torch.int32, device=dev)
     mxfp4_quantize_grouped(x, expert_offsets, codes, scales, sro, status, stream)
+    return codes, scales, sro, status
+
+
+def quantize_grouped_gather(x, row_index, expert_offsets, stream=None):
+    """Returns (codes, scales, scale_row_offsets, status) of x[row_index]."""
+    K = x.shape[1]
+    total = row_index.numel()
+    E = expert_offsets.numel() - 1
+    dev = x.device
+    codes = torch.empty((total, K // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty(max(mxfp4_grouped_scale_bytes_bound(total, E, K), 16), dtype=torch.uint8,
+                         device=dev)
+    sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    status = torch.empty(1, dtype=torch.int32, device=dev)
+    mxfp4_quantize_grouped_gather(x, row_index, expert_offsets, codes, scales, sro, status, stream)
     return codes, scales, sro, status
 
 

@@ -22,6 +22,15 @@ cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K
                                     uint8_t* scales, int32_t* scale_row_offsets,
                                     int32_t* status, int64_t bound_tiles, cudaStream_t stream);
 
+// Grouped quantize of gathered rows: output row r reads source row
+// row_index[r] of x (row stride ldx elements, num_src_rows rows).
+cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K,
+                                           int64_t ldx, const int32_t* row_index,
+                                           int64_t total_rows, const int32_t* offsets, int32_t E,
+                                           uint8_t* codes, uint8_t* scales,
+                                           int32_t* scale_row_offsets, int32_t* status,
+                                           int64_t bound_tiles, cudaStream_t stream);
+
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int64_t K,
                               void* y, cudaStream_t stream);
 

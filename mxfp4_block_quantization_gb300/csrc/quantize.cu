@@ -44,6 +44,9 @@ struct QuantizeParams {
   const int32_t* __restrict__ offsets;  // grouped: input row offsets [E+1]
   const int32_t* __restrict__ padded;   // grouped: padded row offsets [E+1]
   int32_t E;
+  const int32_t* __restrict__ row_index;  // gather: source row of every output row
+  int64_t num_src_rows;                   // gather: rows of x
+  int32_t* status;                        // gather: device status word (may be NULL)
 };
 
 // Segment holding padded row `prow`: the last e in [0, E) with P[e] <= prow
@@ -60,9 +63,12 @@ __device__ __forceinline__ int find_segment(const int32_t* __restrict__ P, int E
 }
 
 // Lane l of warp w covers elements [16*(l%8), 16*(l%8)+16) of row
-// 4*w + l/8 (+32 per pass): two lanes per 32-element block.
-template <bool kGrouped>
+// 4*w + l/8 (+32 per pass): two lanes per 32-element block.  kGather (grouped
+// only): output row r reads source row row_index[r]; the four row indices of
+// a thread are fetched first, then its eight data loads.
+template <bool kGrouped, bool kGather>
 __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const QuantizeParams p) {
+  static_assert(kGrouped || !kGather, "gather is a grouped mode");
   __shared__ __align__(16) uint8_t chunk[kChunkBytes];
 
   pdl_wait();
@@ -94,19 +100,42 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
   const bool col_ok = kt * kTileBlocks + blk < p.sK;
   const int64_t r = row0 + lr0;
   const uint8_t* xp =
-      p.x + r * p.ldx_bytes + static_cast<int64_t>(kt) * (kTileCols * 2) + sub * (kElems * 2);
+      kGather ? p.x
+              : p.x + r * p.ldx_bytes + static_cast<int64_t>(kt) * (kTileCols * 2) + sub * (kElems * 2);
   uint8_t* cp =
       p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) + sub * (kElems / 2);
   const int64_t ldx_pass = p.ldx_bytes * kRowsPerPass;
   const int64_t cld_pass = p.code_ld * kRowsPerPass;
 
   uint4 v[kPasses][2];
+  if constexpr (kGather) {
+    // source rows of this thread's four output rows; an index outside
+    // [0, num_src_rows) reads nothing, quantizes as a zero row and is reported
+    int64_t src[kPasses];
 #pragma unroll
-  for (int i = 0; i < kPasses; ++i) {
-    v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
-    if (col_ok && kRowsPerPass * i < lim) {
-      v[i][0] = ld_stream_v4(xp + i * ldx_pass);
-      v[i][1] = ld_stream_v4(xp + i * ldx_pass + 16);
+    for (int i = 0; i < kPasses; ++i)
+      src[i] = (kRowsPerPass * i < lim) ? __ldg(p.row_index + r + kRowsPerPass * i) : 0;
+    const uint8_t* xcol = p.x + static_cast<int64_t>(kt) * (kTileCols * 2) + sub * (kElems * 2);
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
+      const bool in_range = src[i] >= 0 && src[i] < p.num_src_rows;
+      if (kRowsPerPass * i < lim) bad |= !in_range;
+      if (col_ok && kRowsPerPass * i < lim && in_range) {
+        v[i][0] = ld_stream_v4(xcol + src[i] * p.ldx_bytes);
+        v[i][1] = ld_stream_v4(xcol + src[i] * p.ldx_bytes + 16);
+      }
+    }
+    if (bad && p.status != nullptr) atomicExch(p.status, MXFP4_EINDEX);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
+      if (col_ok && kRowsPerPass * i < lim) {
+        v[i][0] = ld_stream_v4(xp + i * ldx_pass);
+        v[i][1] = ld_stream_v4(xp + i * ldx_pass + 16);
+      }
     }
   }
 
@@ -217,8 +246,8 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
   p.n_units = static_cast<int32_t>(tiles * p.nKT);
-  return launch_pdl(quantize_tiles_kernel<false>, static_cast<unsigned>(p.n_units), kThreads, 0,
-                    stream, p);
+  return launch_pdl(quantize_tiles_kernel<false, false>, static_cast<unsigned>(p.n_units), kThreads,
+                    0, stream, p);
 }
 
 cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
@@ -241,8 +270,37 @@ cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K
   p.padded = scale_row_offsets;
   p.E = E;
   const int64_t grid = bound_tiles * p.nKT;  // CTAs past the real padded total exit at once
-  return launch_pdl(quantize_tiles_kernel<true>, static_cast<unsigned>(grid), kThreads, 0, stream,
-                    p);
+  return launch_pdl(quantize_tiles_kernel<true, false>, static_cast<unsigned>(grid), kThreads, 0,
+                    stream, p);
+}
+
+cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K,
+                                           int64_t ldx, const int32_t* row_index,
+                                           int64_t total_rows, const int32_t* offsets, int32_t E,
+                                           uint8_t* codes, uint8_t* scales,
+                                           int32_t* scale_row_offsets, int32_t* status,
+                                           int64_t bound_tiles, cudaStream_t stream) {
+  cudaError_t err = launch_pdl(grouped_offsets_kernel, 1, kScanThreads, 0, stream, offsets, E,
+                               total_rows, scale_row_offsets, status);
+  if (err != cudaSuccess || E == 0 || bound_tiles == 0) return err;
+  QuantizeParams p{};
+  p.x = static_cast<const uint8_t*>(x);
+  p.ldx_bytes = ldx * 2;
+  p.M = total_rows;
+  p.code_ld = K / 2;
+  p.codes = codes;
+  p.scales = scales;
+  p.sK = static_cast<int32_t>(K / kBlock);
+  p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
+  p.offsets = offsets;
+  p.padded = scale_row_offsets;
+  p.E = E;
+  p.row_index = row_index;
+  p.num_src_rows = num_src_rows;
+  p.status = status;
+  const int64_t grid = bound_tiles * p.nKT;
+  return launch_pdl(quantize_tiles_kernel<true, true>, static_cast<unsigned>(grid), kThreads, 0,
+                    stream, p);
 }
 
 }  // namespace mxfp4

@@ -54,8 +54,10 @@ def dense_activation(seed: int = 1, M: int = 4096, K: int = 7168, device="cpu") 
 class GroupedInput:
     x: torch.Tensor          # BF16 [tokens * top_k, K], rows sorted by expert
     offsets: torch.Tensor    # int32 [E + 1], segment e = rows [o[e], o[e+1])
-    token_of_row: torch.Tensor  # int64 [tokens * top_k], source token of each row
+    token_of_row: torch.Tensor  # int64 [tokens * top_k], source token of each row (CPU)
     num_experts: int
+    x_tokens: torch.Tensor   # BF16 [tokens, K], the token rows before dispatch
+    row_index: torch.Tensor  # int32 [tokens * top_k] on `device`: token of each row
 
 
 def moe_grouped(seed: int = 2, tokens: int = 16384, top_k: int = 8, num_experts: int = 384,
@@ -75,9 +77,11 @@ def moe_grouped(seed: int = 2, tokens: int = 16384, top_k: int = 8, num_experts:
     offsets = torch.zeros(num_experts + 1, dtype=torch.int64)
     offsets[1:] = torch.cumsum(counts, 0)
     x_tok = normal_bf16((tokens, K), seed + 1000, device=device)
+    row_index = token_of_row.to(torch.int32).to(device)
     x = x_tok.index_select(0, token_of_row.to(device))
     return GroupedInput(x=x, offsets=offsets.to(torch.int32).to(device),
-                        token_of_row=token_of_row, num_experts=num_experts)
+                        token_of_row=token_of_row, num_experts=num_experts, x_tokens=x_tok,
+                        row_index=row_index)
 
 
 @dataclass

@@ -63,6 +63,9 @@ def lib():
         L.orc_quantize_grouped.restype = ctypes.c_int
         L.orc_quantize_grouped.argtypes = [_u16p, _i64, _i64, _i32p, ctypes.c_int32,
                                            _u8p, _u8p, _i32p]
+        L.orc_quantize_grouped_gather.restype = ctypes.c_int
+        L.orc_quantize_grouped_gather.argtypes = [_u16p, _i64, _i64, _i64, _i32p, _i64, _i32p,
+                                                  ctypes.c_int32, _u8p, _u8p, _i32p]
         L.orc_dequantize.restype = None
         L.orc_dequantize.argtypes = [_u8p, _u8p, _i64, _i64, _u16p]
         L.orc_swap_halves.restype = None
@@ -198,6 +201,24 @@ def quantize_grouped(xbits: np.ndarray, offsets: np.ndarray):
     sro = np.zeros(E + 1, np.int32)
     rc = lib().orc_quantize_grouped(_p(x, _u16p), total, K, _p(off, _i32p), E,
                                     _p(codes, _u8p), _p(scales, _u8p), _p(sro, _i32p))
+    return rc, codes, scales, sro
+
+
+def quantize_grouped_gather(xbits: np.ndarray, row_index: np.ndarray, offsets: np.ndarray):
+    """Step 6 on rows x[row_index]: (rc, codes, scales, scale_row_offsets);
+    rc is 0, -6 (bad offsets) or -7 (an index out of range, zero row)."""
+    x = _c(xbits, np.uint16)
+    idx = _c(row_index, np.int32)
+    off = _c(offsets, np.int32)
+    n_src, K = x.shape
+    total = idx.size
+    E = off.size - 1
+    codes = np.zeros((total, K // 2), np.uint8)
+    scales = np.zeros(max(grouped_scale_bytes_bound(total, E, K), 1), np.uint8)
+    sro = np.zeros(E + 1, np.int32)
+    rc = lib().orc_quantize_grouped_gather(_p(x, _u16p), n_src, K, K, _p(idx, _i32p), total,
+                                           _p(off, _i32p), E, _p(codes, _u8p), _p(scales, _u8p),
+                                           _p(sro, _i32p))
     return rc, codes, scales, sro
 
 

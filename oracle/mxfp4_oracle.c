@@ -234,6 +234,30 @@ int orc_quantize_grouped(const uint16_t* x, int64_t total_rows, int64_t K,
   return 0;
 }
 
+/* Step 6 with the MoE dispatch gather in front ([PR43557] item 3: the
+ * experts-quant input is the routed, expert-sorted activations): output row r
+ * is source row row_index[r]; out-of-range indices give zero rows and -7.
+ * Plainly: gather the rows, then the grouped quantize above. */
+int orc_quantize_grouped_gather(const uint16_t* x, int64_t num_src_rows, int64_t K, int64_t ldx,
+                                const int32_t* row_index, int64_t total_rows,
+                                const int32_t* offsets, int32_t E, uint8_t* codes,
+                                uint8_t* scales, int32_t* scale_row_offsets) {
+  uint16_t* g = (uint16_t*)calloc((size_t)(total_rows * K) + 1, sizeof(uint16_t));
+  int bad = 0;
+  for (int64_t r = 0; r < total_rows; ++r) {
+    int64_t src = row_index[r];
+    if (src < 0 || src >= num_src_rows) {
+      bad = 1;
+      continue; /* stays a zero row */
+    }
+    memcpy(g + r * K, x + src * ldx, (size_t)K * sizeof(uint16_t));
+  }
+  int rc = orc_quantize_grouped(g, total_rows, K, offsets, E, codes, scales, scale_row_offsets);
+  free(g);
+  if (rc != 0) return rc;
+  return bad ? -7 : 0;
+}
+
 /* Step 7 — dequantize: for each element, its nibble and its block's scale
  * byte (read back through the tiled layout) give E2M1 value * 2^(s-127),
  * rounded once to BF16.  [PR46915] "Motivation" (FP4 -> BF16 table);

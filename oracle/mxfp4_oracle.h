@@ -70,6 +70,13 @@ void orc_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
 int orc_quantize_grouped(const uint16_t* x, int64_t total_rows, int64_t K,
                          const int32_t* offsets, int32_t E, uint8_t* codes,
                          uint8_t* scales, int32_t* scale_row_offsets);
+/* Step 6 on gathered rows: output row r is row row_index[r] of x (row
+ * stride ldx).  Returns 0, -6 (bad offsets, as above) or -7 (some index
+ * outside [0, num_src_rows): that row is quantized as zeros). */
+int orc_quantize_grouped_gather(const uint16_t* x, int64_t num_src_rows, int64_t K, int64_t ldx,
+                                const int32_t* row_index, int64_t total_rows,
+                                const int32_t* offsets, int32_t E, uint8_t* codes,
+                                uint8_t* scales, int32_t* scale_row_offsets);
 /* Step 7: codes + tiled scales -> BF16 [M, K]. */
 void orc_dequantize(const uint8_t* codes, const uint8_t* tiled_scales,
                     int64_t M, int64_t K, uint16_t* y);

@@ -126,3 +126,24 @@ def test_binding_rejects_cpu_tensors(lib):
     x = torch.zeros(4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         lib.quantize(x)
+
+
+def test_grouped_gather_validation(lib):
+    g = lib._lib.mxfp4_quantize_grouped_gather
+    # x, n_src, K, ldx, idx, total, off, E, codes, scales, sro, status, stream
+    ok = [A, 50, 64, 64, 2 * A, 10, 3 * A, 2, 4 * A, 5 * A, 6 * A, None, None]
+
+    def call(**kw):
+        names = ["x", "n", "K", "ldx", "idx", "tot", "off", "E", "c", "s", "sro", "st", "strm"]
+        a = dict(zip(names, ok))
+        a.update(kw)
+        return g(*[a[n] for n in names])
+
+    assert call(K=48, ldx=48) == lib.MXFP4_ESHAPE
+    assert call(ldx=32) == lib.MXFP4_ESHAPE
+    assert call(idx=None) == lib.MXFP4_EINVAL
+    assert call(n=0) == lib.MXFP4_EINVAL
+    assert call(idx=2 * A + 2) == lib.MXFP4_EALIGN
+    assert call(ldx=68) == lib.MXFP4_EALIGN
+    assert call(c=2 * A + 16) == lib.MXFP4_EALIAS            # codes overlap the indices
+    assert call(sro=A + 64) == lib.MXFP4_EALIAS              # offsets out overlap x

@@ -319,3 +319,70 @@ def test_expert_weights_full_size_sampled(mx):
         assert np.array_equal(codes2[e * N2:(e + 1) * N2].cpu().numpy(), c2_o)
         assert np.array_equal(scales2[e * per2:(e + 1) * per2].cpu().numpy(), s2_o)
     assert np.array_equal(bits(b2_sw), oracle.cast_bf16(w.w2_bias.cpu().numpy()))
+
+
+# ------------------------------------------------- fused gather + grouped
+def run_gather(mx, x, row_index, offsets):
+    total = row_index.numel()
+    K = x.shape[1]
+    E = offsets.numel() - 1
+    codes = Guarded(total * (K // 2), shape=(total, K // 2))
+    scales = Guarded(mx.mxfp4_grouped_scale_bytes_bound(total, E, K))
+    sro = Guarded(4 * (E + 1), torch.int32)
+    status = Guarded(4, torch.int32)
+    mx.mxfp4_quantize_grouped_gather(x, row_index, offsets, codes.t, scales.t, sro.t, status.t)
+    torch.cuda.synchronize()
+    for g in (codes, scales, sro, status):
+        g.check()
+    return (codes.t.cpu().numpy(), scales.t.cpu().numpy(), sro.t.cpu().numpy(),
+            int(status.t.cpu()[0]))
+
+
+def test_grouped_gather_small(mx):
+    g = W.moe_grouped(seed=2, tokens=200, top_k=4, num_experts=12, K=288, device="cuda")
+    c, s, sro, st = run_gather(mx, g.x_tokens, g.row_index, g.offsets)
+    rc, c_o, s_o, sro_o = oracle.quantize_grouped_gather(bits(g.x_tokens), g.token_of_row.numpy(),
+                                                         g.offsets.cpu().numpy())
+    assert st == 0 and rc == 0 and np.array_equal(sro, sro_o)
+    assert np.array_equal(c, c_o), _first_diff(c, c_o)
+    used = int(sro_o[-1]) * 12
+    assert np.array_equal(s[:used], s_o[:used])
+
+
+def test_grouped_gather_strided_source(mx):
+    g = W.moe_grouped(seed=5, tokens=150, top_k=2, num_experts=5, K=256, device="cuda")
+    wide = torch.zeros((150, 384), dtype=torch.bfloat16, device="cuda")
+    wide[:, 64:320] = g.x_tokens
+    x = wide[:, 64:320]
+    c, s, sro, st = run_gather(mx, x, g.row_index, g.offsets)
+    rc, c_o, s_o, sro_o = oracle.quantize_grouped_gather(bits(g.x_tokens), g.token_of_row.numpy(),
+                                                         g.offsets.cpu().numpy())
+    assert st == 0 and np.array_equal(c, c_o)
+    used = int(sro_o[-1]) * 8
+    assert np.array_equal(s[:used], s_o[:used])
+
+
+def test_grouped_gather_bad_index(mx):
+    xt = W.small_matrix(3, 16, 64).cuda()
+    idx = torch.tensor([0, 5, 99, 7, -1, 3], dtype=torch.int32, device="cuda")
+    off = torch.tensor([0, 2, 6], dtype=torch.int32, device="cuda")
+    c, s, sro, st = run_gather(mx, xt, idx, off)
+    rc, c_o, s_o, sro_o = oracle.quantize_grouped_gather(bits(xt), idx.cpu().numpy(),
+                                                         off.cpu().numpy())
+    assert st == mx.MXFP4_EINDEX and rc == -7
+    assert np.array_equal(c, c_o) and not c[2].any() and not c[4].any()
+    used = int(sro_o[-1]) * 4
+    assert np.array_equal(s[:used], s_o[:used])
+
+
+def test_grouped_gather_moe_full_size(mx):
+    """16384 tokens x top-8 over 384 experts, K = 7168: the fused gather
+    equals the grouped quantize of the gathered matrix, every byte."""
+    g = W.moe_grouped(seed=2, device="cuda")
+    c1, s1, sro1, st1 = mx.quantize_grouped_gather(g.x_tokens, g.row_index, g.offsets)
+    c2, s2, sro2, st2 = mx.quantize_grouped(g.x, g.offsets)
+    torch.cuda.synchronize()
+    assert int(st1.cpu()[0]) == 0 and int(st2.cpu()[0]) == 0
+    assert torch.equal(sro1, sro2) and torch.equal(c1, c2)
+    used = int(sro1[-1].item()) * 224
+    assert torch.equal(s1[:used], s2[:used])

@@ -122,3 +122,31 @@ def test_grouped_bad_offsets(orc, off):
     assert rc == -6
     assert list(sro) == [-1] * len(off)
     assert not codes.any() and not scales.any()
+
+
+def test_grouped_gather_equals_grouped_of_gathered(orc):
+    """The fused dispatch gather: quantizing rows x[row_index] directly equals
+    the grouped quantize of the explicitly gathered matrix (numpy indexing)."""
+    g = W.moe_grouped(seed=2, tokens=80, top_k=3, num_experts=7, K=192)
+    xt = W.bf16_bits(g.x_tokens)
+    idx = g.token_of_row.numpy().astype(np.int32)
+    off = g.offsets.numpy()
+    rc, c, s, sro = orc.quantize_grouped_gather(xt, idx, off)
+    rc2, c2, s2, sro2 = orc.quantize_grouped(xt[idx], off)
+    assert rc == 0 and rc2 == 0
+    assert np.array_equal(c, c2) and np.array_equal(s, s2) and np.array_equal(sro, sro2)
+    assert np.array_equal(xt[idx], W.bf16_bits(g.x))
+
+
+def test_grouped_gather_bad_index_zero_row(orc):
+    xt = W.bf16_bits(W.small_matrix(3, 16, 64))
+    idx = np.array([0, 5, 99, 7, -1, 3], np.int32)
+    off = np.array([0, 2, 6], np.int32)
+    rc, c, s, sro = orc.quantize_grouped_gather(xt, idx, off)
+    assert rc == -7
+    g = xt[np.clip(idx, 0, 15)].copy()
+    g[2] = 0
+    g[4] = 0
+    rc2, c2, s2, _ = orc.quantize_grouped(g, off)
+    assert np.array_equal(c, c2) and np.array_equal(s, s2)
+    assert not c[2].any() and not c[4].any()
