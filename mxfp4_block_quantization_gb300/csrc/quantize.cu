@@ -47,6 +47,7 @@ struct QuantizeParams {
   const int32_t* __restrict__ row_index;  // gather: source row of every output row
   int64_t num_src_rows;                   // gather: rows of x
   int32_t* status;                        // gather: device status word (may be NULL)
+  int32_t n_mtiles;                       // gather: m-tiles of the grid (k-tile-major order)
 };
 
 // Segment holding padded row `prow`: the last e in [0, E) with P[e] <= prow
@@ -74,9 +75,19 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
   pdl_wait();
   pdl_release();
 
+  // Tile order: m-tile-major (consecutive CTAs read adjacent column slices of
+  // the same rows) or, for the gather, k-tile-major: all resident CTAs then
+  // read the same 256-byte column slice of the source rows, a working set the
+  // L2 keeps while the other routes of each row come by.
   const int unit = blockIdx.x;
-  const int mt = unit / p.nKT;
-  const int kt = unit - mt * p.nKT;
+  int mt, kt;
+  if constexpr (kGather) {
+    kt = unit / p.n_mtiles;
+    mt = unit - kt * p.n_mtiles;
+  } else {
+    mt = unit / p.nKT;
+    kt = unit - mt * p.nKT;
+  }
   int64_t row0, row_end;
   if constexpr (kGrouped) {
     const int total_padded = __ldg(p.padded + p.E);
@@ -168,7 +179,9 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
   __syncthreads();
   if (threadIdx.x < kChunkBytes / 16) {
     const uint4 w = reinterpret_cast<const uint4*>(chunk)[threadIdx.x];
-    st_stream_v4(p.scales + static_cast<int64_t>(unit) * kChunkBytes + threadIdx.x * 16, w);
+    // chunk index = m-tile * nKT + k-tile (= unit in m-tile-major order)
+    const int64_t c = kGather ? static_cast<int64_t>(mt) * p.nKT + kt : unit;
+    st_stream_v4(p.scales + c * kChunkBytes + threadIdx.x * 16, w);
   }
 }
 
@@ -298,6 +311,7 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
   p.row_index = row_index;
   p.num_src_rows = num_src_rows;
   p.status = status;
+  p.n_mtiles = static_cast<int32_t>(bound_tiles);
   const int64_t grid = bound_tiles * p.nKT;
   return launch_pdl(quantize_tiles_kernel<true, true>, static_cast<unsigned>(grid), kThreads, 0,
                     stream, p);
