@@ -16,6 +16,8 @@
 // All four passes' loads are issued before any compute (32 KB in flight per
 // CTA, five CTAs per SM).  Launches use programmatic dependent launch, so a
 // grid is already resident when its predecessor in the stream drains.
+#include <cstdint>
+
 #include <cuda_runtime.h>
 
 #include "mxfp4_device.cuh"
@@ -63,11 +65,26 @@ __device__ __forceinline__ int find_segment(const int32_t* __restrict__ P, int E
   return lo;
 }
 
+// One lane's 16 BF16 elements (32 bytes) of one row.
+template <bool kVec32>
+__device__ __forceinline__ void load32(const uint8_t* src, uint4 (&v)[2]) {
+  if constexpr (kVec32) {
+    ld_stream_v8(src, v[0], v[1]);
+  } else {
+    v[0] = ld_stream_v4(src);
+    v[1] = ld_stream_v4(src + 16);
+  }
+}
+
 // Lane l of warp w covers elements [16*(l%8), 16*(l%8)+16) of row
 // 4*w + l/8 (+32 per pass): two lanes per 32-element block.  kGather (grouped
 // only): output row r reads source row row_index[r]; the four row indices of
 // a thread are fetched first, then its eight data loads.
-template <bool kGrouped, bool kGather>
+//
+// kVec32: every lane's 32 bytes are 32-byte aligned (x and the row stride
+// are), so they arrive in one 256-bit load per pass; otherwise two 16-byte
+// loads (each then touches half of a 32-byte sector).
+template <bool kGrouped, bool kGather, bool kVec32>
 __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const QuantizeParams p) {
   static_assert(kGrouped || !kGather, "gather is a grouped mode");
   __shared__ __align__(16) uint8_t chunk[kChunkBytes];
@@ -133,20 +150,14 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
       v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
       const bool in_range = src[i] >= 0 && src[i] < p.num_src_rows;
       if (kRowsPerPass * i < lim) bad |= !in_range;
-      if (col_ok && kRowsPerPass * i < lim && in_range) {
-        v[i][0] = ld_stream_v4(xcol + src[i] * p.ldx_bytes);
-        v[i][1] = ld_stream_v4(xcol + src[i] * p.ldx_bytes + 16);
-      }
+      if (col_ok && kRowsPerPass * i < lim && in_range) load32<kVec32>(xcol + src[i] * p.ldx_bytes, v[i]);
     }
     if (bad && p.status != nullptr) atomicExch(p.status, MXFP4_EINDEX);
   } else {
 #pragma unroll
     for (int i = 0; i < kPasses; ++i) {
       v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
-      if (col_ok && kRowsPerPass * i < lim) {
-        v[i][0] = ld_stream_v4(xp + i * ldx_pass);
-        v[i][1] = ld_stream_v4(xp + i * ldx_pass + 16);
-      }
+      if (col_ok && kRowsPerPass * i < lim) load32<kVec32>(xp + i * ldx_pass, v[i]);
     }
   }
 
@@ -244,6 +255,12 @@ grouped_offsets_kernel(const int32_t* __restrict__ off, int32_t E, int64_t total
   if (tid == 0 && status != nullptr) *status = s_bad ? MXFP4_EOFFSETS : MXFP4_OK;
 }
 
+// 256-bit loads need every lane address 32-byte aligned: the base and the
+// row stride (the column offsets are multiples of 32 bytes).
+bool vec32_ok(const void* x, int64_t ldx_bytes) {
+  return (reinterpret_cast<uintptr_t>(x) % 32 == 0) && (ldx_bytes % 32 == 0);
+}
+
 }  // namespace
 
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
@@ -259,8 +276,9 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
   p.n_units = static_cast<int32_t>(tiles * p.nKT);
-  return launch_pdl(quantize_tiles_kernel<false, false>, static_cast<unsigned>(p.n_units), kThreads,
-                    0, stream, p);
+  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<false, false, true>
+                                               : quantize_tiles_kernel<false, false, false>;
+  return launch_pdl(kernel, static_cast<unsigned>(p.n_units), kThreads, 0, stream, p);
 }
 
 cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
@@ -283,8 +301,9 @@ cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K
   p.padded = scale_row_offsets;
   p.E = E;
   const int64_t grid = bound_tiles * p.nKT;  // CTAs past the real padded total exit at once
-  return launch_pdl(quantize_tiles_kernel<true, false>, static_cast<unsigned>(grid), kThreads, 0,
-                    stream, p);
+  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<true, false, true>
+                                               : quantize_tiles_kernel<true, false, false>;
+  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
 cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K,
@@ -313,8 +332,9 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
   p.status = status;
   p.n_mtiles = static_cast<int32_t>(bound_tiles);
   const int64_t grid = bound_tiles * p.nKT;
-  return launch_pdl(quantize_tiles_kernel<true, true>, static_cast<unsigned>(grid), kThreads, 0,
-                    stream, p);
+  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<true, true, true>
+                                               : quantize_tiles_kernel<true, true, false>;
+  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
 }  // namespace mxfp4

@@ -386,3 +386,51 @@ def test_grouped_gather_moe_full_size(mx):
     assert torch.equal(sro1, sro2) and torch.equal(c1, c2)
     used = int(sro1[-1].item()) * 224
     assert torch.equal(s1[:used], s2[:used])
+
+
+# ----------------------- inputs aligned to 16 bytes but not to 32 bytes
+def offset16(x):
+    """The same values in a buffer whose base is 16 (not 32) bytes aligned:
+    the kernels then take their two-16-byte-load path."""
+    flat = torch.empty(x.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    y = flat[8:].view(x.shape)
+    y.copy_(x)
+    assert y.data_ptr() % 32 == 16
+    return y
+
+
+def test_dense_16b_aligned_input(mx):
+    x = offset16(W.dense_activation(7, 300, 2880, device="cuda"))
+    c_gpu, s_gpu = run_quantize(mx, x)
+    c_orc, s_orc = oracle.quantize(bits(x))
+    assert np.array_equal(c_gpu, c_orc) and np.array_equal(s_gpu, s_orc)
+
+
+def test_dense_row_stride_16b(mx):
+    """Row stride of 1032 elements (2064 bytes: a multiple of 16, not 32)."""
+    wide = W.dense_activation(8, 200, 1032, device="cuda")
+    x = wide[:, :1024]
+    c_gpu, s_gpu = run_quantize(mx, x)
+    c_orc, s_orc = oracle.quantize(bits(x.contiguous()))
+    assert np.array_equal(c_gpu, c_orc) and np.array_equal(s_gpu, s_orc)
+
+
+def test_grouped_16b_aligned_input(mx):
+    g = W.moe_grouped(seed=6, tokens=120, top_k=3, num_experts=9, K=160, device="cuda")
+    x = offset16(g.x)
+    c, s, sro, st = run_grouped(mx, x, g.offsets)
+    rc, c_o, s_o, sro_o = oracle.quantize_grouped(bits(g.x), g.offsets.cpu().numpy())
+    assert st == 0 and np.array_equal(c, c_o) and np.array_equal(sro, sro_o)
+    used = int(sro_o[-1]) * 8
+    assert np.array_equal(s[:used], s_o[:used])
+
+
+def test_grouped_gather_16b_aligned_input(mx):
+    g = W.moe_grouped(seed=7, tokens=120, top_k=3, num_experts=9, K=160, device="cuda")
+    x = offset16(g.x_tokens)
+    c, s, sro, st = run_gather(mx, x, g.row_index, g.offsets)
+    rc, c_o, s_o, sro_o = oracle.quantize_grouped_gather(bits(g.x_tokens), g.token_of_row.numpy(),
+                                                         g.offsets.cpu().numpy())
+    assert st == 0 and np.array_equal(c, c_o)
+    used = int(sro_o[-1]) * 8
+    assert np.array_equal(s[:used], s_o[:used])
