@@ -186,6 +186,12 @@ __device__ __forceinline__ void st_stream_u32(void* p, uint32_t v) {
 __device__ __forceinline__ void st_stream_v2(void* p, uint2 v) {
   asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
+// 32-byte store (two uint4); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_stream_v8(void* p, uint4 a, uint4 b) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x),
+               "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
 __device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
