@@ -11,12 +11,17 @@
 // The product has at most two significant bits, so the only rounding is
 // overflow to +-Inf (s >= 253) — no double rounding through float32.
 //
-// Same tiles as the quantizer: one CTA per 128x128 tile (one 512-byte scale
-// chunk).  Lane l of warp w handles 8 elements of row 2*w + l/16 in each of
-// 8 passes of 16 rows: a 4-byte code load, one scale byte of the chunk and a
-// 16-byte BF16 store, so each warp store instruction writes two full 256-byte
-// row segments.  All loads of a CTA are issued before any compute.  Launched
-// with programmatic dependent launch.
+// Same tiles as the quantizer: one CTA (256 threads) per 128x128 tile (one
+// 512-byte scale chunk), all loads issued before any compute, launched with
+// programmatic dependent launch.  Two lane mappings:
+//  - wide (output 32-byte aligned): lane = 16 elements of one row per pass,
+//    4 passes; an 8-byte code load, the tile's 4 scale bytes of the lane from
+//    one 16-byte chunk row, one 32-byte store per pass (full sectors);
+//  - narrow (output only 16-byte aligned): lane = 8 elements per pass, 8
+//    passes; a 4-byte code load, one scale byte, one 16-byte store, so each
+//    warp store instruction still writes whole 256-byte row segments.
+#include <cstdint>
+
 #include <cuda_runtime.h>
 
 #include "mxfp4_device.cuh"
@@ -26,7 +31,7 @@ namespace mxfp4 {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kPasses = kTileRows / (2 * (kThreads / 32));  // 8 passes of 16 rows
+constexpr int kPasses = kTileRows / (2 * (kThreads / 32));  // narrow: 8 passes of 16 rows
 
 struct DequantizeParams {
   const uint8_t* __restrict__ codes;
@@ -55,7 +60,54 @@ __device__ __forceinline__ uint4 decode8(uint32_t c, float sc) {
   return o;
 }
 
-__global__ void __launch_bounds__(kThreads) dequantize_tiles_kernel(const DequantizeParams p) {
+// Wide mapping: lane l of warp w covers elements [16*(l%8), 16*(l%8)+16) of
+// row 4*w + l/8 (+32 per pass); pass i of that row has its scale byte in
+// chunk row (4*w + l/8), word i, byte (l%8)/2.
+__global__ void __launch_bounds__(kThreads) dequantize_wide_kernel(const DequantizeParams p) {
+  constexpr int kRowsPerPass = 32;
+  constexpr int kWidePasses = kTileRows / kRowsPerPass;
+  pdl_wait();
+  pdl_release();
+  const int kt = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.nKT));
+  const int64_t tile = blockIdx.x / static_cast<uint32_t>(p.nKT);
+  const int64_t row0 = tile * kTileRows;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;
+  const int blk = sub >> 1;
+  const int lr0 = warp * 4 + (lane >> 3);
+  const int64_t avail = p.M - row0;
+  const int lim = static_cast<int>((avail < kTileRows ? avail : kTileRows) - lr0);
+  const bool col_ok = kt * kTileBlocks + blk < p.sK;
+  const uint8_t* cp = p.codes + (row0 + lr0) * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) + sub * 8;
+  uint8_t* yp = p.y + (row0 + lr0) * p.y_ld + static_cast<int64_t>(kt) * (kTileCols * 2) + sub * 32;
+  const int64_t cld_pass = p.code_ld * kRowsPerPass;
+  const int64_t yld_pass = p.y_ld * kRowsPerPass;
+
+  uint2 c[kWidePasses];
+#pragma unroll
+  for (int i = 0; i < kWidePasses; ++i)
+    c[i] = (col_ok && kRowsPerPass * i < lim) ? ld_stream_v2(cp + i * cld_pass) : make_uint2(0u, 0u);
+  const uint4 sr = ld_stream_v4(p.scales + (tile * p.nKT + kt) * kChunkBytes + lr0 * 16);
+#pragma unroll
+  for (int i = 0; i < kWidePasses; ++i) {
+    const uint32_t word = i == 0 ? sr.x : i == 1 ? sr.y : i == 2 ? sr.z : sr.w;
+    const uint32_t s = (word >> (8 * blk)) & 0xFFu;
+    uint4 o0, o1;
+    if (s == 255u) {
+      o0 = o1 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+    } else {
+      const float sc = scale_from_e8m0(s);
+      o0 = decode8(c[i].x, sc);
+      o1 = decode8(c[i].y, sc);
+    }
+    if (col_ok && kRowsPerPass * i < lim) st_stream_v8(yp + i * yld_pass, o0, o1);
+  }
+}
+
+// Narrow mapping: lane l of warp w covers 8 elements of row 2*w + l/16 in
+// each of 8 passes of 16 rows.
+__global__ void __launch_bounds__(kThreads) dequantize_narrow_kernel(const DequantizeParams p) {
   pdl_wait();
   pdl_release();
   const int kt = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.nKT));
@@ -111,8 +163,9 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64
   p.sK = static_cast<int32_t>(K / kBlock);
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
-  return launch_pdl(dequantize_tiles_kernel, static_cast<unsigned>(tiles * p.nKT), kThreads, 0,
-                    stream, p);
+  const bool wide = reinterpret_cast<uintptr_t>(y) % 32 == 0;  // rows are 2K = 64*(K/32) bytes
+  return launch_pdl(wide ? dequantize_wide_kernel : dequantize_narrow_kernel,
+                    static_cast<unsigned>(tiles * p.nKT), kThreads, 0, stream, p);
 }
 
 }  // namespace mxfp4
