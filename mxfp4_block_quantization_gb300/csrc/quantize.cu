@@ -85,7 +85,7 @@ __device__ __forceinline__ void load32(const uint8_t* src, uint4 (&v)[2]) {
 // are), so they arrive in one 256-bit load per pass; otherwise two 16-byte
 // loads (each then touches half of a 32-byte sector).
 template <bool kGrouped, bool kGather, bool kVec32>
-__device__ __forceinline__ void quantize_tile(const QuantizeParams p) {
+__global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const QuantizeParams p) {
   static_assert(kGrouped || !kGather, "gather is a grouped mode");
   __shared__ __align__(16) uint8_t chunk[kChunkBytes];
 
@@ -196,19 +196,6 @@ __device__ __forceinline__ void quantize_tile(const QuantizeParams p) {
   }
 }
 
-// All variants are held to 5 resident CTAs per SM (48 registers, 40 warps):
-// 160 KB of loads in flight per SM for the streaming variants; the gather,
-// whose loads are mostly served by L2, is latency-bound and needs the CTAs.
-template <bool kGrouped, bool kVec32>
-__global__ void __launch_bounds__(kThreads, 5) quantize_tiles_kernel(const QuantizeParams p) {
-  quantize_tile<kGrouped, false, kVec32>(p);
-}
-
-template <bool kVec32>
-__global__ void __launch_bounds__(kThreads, 5) quantize_gather_kernel(const QuantizeParams p) {
-  quantize_tile<true, true, kVec32>(p);
-}
-
 // Validates 0 = o[0] <= o[1] <= ... <= o[E] = total_rows and writes the
 // padded row starts P[e] = sum_{e'<e} ceil(n_e'/128)*128 (P[E] = total).
 // One CTA of 1024 threads; a block-wide scan per 1024 segments.
@@ -289,8 +276,8 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
   p.n_units = static_cast<int32_t>(tiles * p.nKT);
-  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<false, true>
-                                               : quantize_tiles_kernel<false, false>;
+  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<false, false, true>
+                                               : quantize_tiles_kernel<false, false, false>;
   return launch_pdl(kernel, static_cast<unsigned>(p.n_units), kThreads, 0, stream, p);
 }
 
@@ -314,8 +301,8 @@ cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K
   p.padded = scale_row_offsets;
   p.E = E;
   const int64_t grid = bound_tiles * p.nKT;  // CTAs past the real padded total exit at once
-  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<true, true>
-                                               : quantize_tiles_kernel<true, false>;
+  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<true, false, true>
+                                               : quantize_tiles_kernel<true, false, false>;
   return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
@@ -345,8 +332,8 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
   p.status = status;
   p.n_mtiles = static_cast<int32_t>(bound_tiles);
   const int64_t grid = bound_tiles * p.nKT;
-  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_gather_kernel<true>
-                                               : quantize_gather_kernel<false>;
+  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<true, true, true>
+                                               : quantize_tiles_kernel<true, true, false>;
   return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
