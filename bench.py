@@ -324,6 +324,15 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     out["dequantize_4096x7168"] = entry(nb, ms, 1, f"{R} rotating sets")
     del cs, ss, ys, x, codes, scales
 
+    # the same activation in FP16 (same method, binary16 input)
+    x16s = [W.dense_activation(1, M, K, device="cuda").to(torch.float16) for _ in range(R)]
+    cs16 = [torch.empty((M, K // 2), dtype=torch.uint8, device="cuda") for _ in range(R)]
+    ss16 = [torch.empty(M * 224, dtype=torch.uint8, device="cuda") for _ in range(R)]
+    ms = time_launches(lambda i: mx.mxfp4_quantize_f16(x16s[i % R], cs16[i % R], ss16[i % R], stream),
+                       200, stream)
+    out["quantize_f16_4096x7168"] = entry(quant_bytes(M, K), ms, 1, f"{R} rotating sets")
+    del x16s, cs16, ss16
+
     # grouped MoE activations: 16384 tokens x top-8 over 384 experts, K = 7168
     g = W.moe_grouped(seed=2, device="cuda")
     total, K = g.x.shape

@@ -97,6 +97,15 @@ size_t mxfp4_grouped_scale_bytes_bound(int64_t total_rows, int32_t E, int64_t K)
 int mxfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ldx,
                    uint8_t* codes, uint8_t* scales, void* stream);
 
+/* mxfp4_quantize_f16 — the same method and outputs for IEEE binary16 input.
+ * [PR43557] cvt_warp_fp16_to_fp4 excerpt: the kernel converts 16-bit inputs,
+ * its block max is a packed half2 max.  The block max is widened to float32
+ * exactly and the E8M0 rule applied to its bits; elements are scaled in
+ * float32 and rounded to E2M1 as for BF16.  Arguments, layouts, alignment and
+ * errors exactly as for mxfp4_quantize (x holds FP16 bit patterns). */
+int mxfp4_quantize_f16(const void* x, int64_t M, int64_t K, int64_t ldx,
+                       uint8_t* codes, uint8_t* scales, void* stream);
+
 /* mxfp4_quantize_grouped — per-expert ("experts quant") activation quantize.
  *
  * [PR43557] "Implementation breakdown" item 3 (the experts-quant tests) and

@@ -30,7 +30,7 @@ __all__ = [
     "mxfp4_status_string", "mxfp4_version", "quantize", "quantize_grouped", "dequantize",
     "swap_w13", "MXFP4_OK", "MXFP4_EINVAL", "MXFP4_EALIGN", "MXFP4_ESHAPE", "MXFP4_EALIAS",
     "MXFP4_ECUDA", "MXFP4_EOFFSETS", "MXFP4_EINDEX", "mxfp4_quantize_grouped_gather",
-    "quantize_grouped_gather",
+    "quantize_grouped_gather", "mxfp4_quantize_f16",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300.so")
@@ -66,6 +66,8 @@ def _load():
     L.mxfp4_grouped_scale_bytes_bound.argtypes = [i64, i32, i64]
     L.mxfp4_quantize.restype = ctypes.c_int
     L.mxfp4_quantize.argtypes = [vp, i64, i64, i64, vp, vp, vp]
+    L.mxfp4_quantize_f16.restype = ctypes.c_int
+    L.mxfp4_quantize_f16.argtypes = [vp, i64, i64, i64, vp, vp, vp]
     L.mxfp4_quantize_grouped.restype = ctypes.c_int
     L.mxfp4_quantize_grouped.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp]
     L.mxfp4_quantize_grouped_gather.restype = ctypes.c_int
@@ -138,6 +140,19 @@ def mxfp4_quantize(x, codes, scales, stream=None) -> None:
     M, K = x.shape
     _check(_lib.mxfp4_quantize(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales),
                                _stream(stream, x.device)), "mxfp4_quantize")
+
+
+def mxfp4_quantize_f16(x, codes, scales, stream=None) -> None:
+    """FP16 ``x`` [M, K] (row stride may exceed K) -> the same codes and tiled
+    scales as mxfp4_quantize produces for BF16 input."""
+    _need_cuda("x", x, torch.float16)
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    M, K = x.shape
+    _check(_lib.mxfp4_quantize_f16(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales),
+                                   _stream(stream, x.device)), "mxfp4_quantize_f16")
 
 
 def mxfp4_quantize_grouped(x, expert_offsets, codes, scales, scale_row_offsets, status=None,
@@ -215,11 +230,14 @@ def mxfp4_swap_w13(codes_in, scales_in, w13_bias_in, E: int, two_n: int, K: int,
 
 # --------------------------------------------------- allocating wrappers
 def quantize(x, stream=None):
-    """Returns (codes uint8 [M, K/2], scales uint8 [scale_bytes])."""
+    """BF16 or FP16 ``x`` [M, K] -> (codes uint8 [M, K/2], scales uint8 [scale_bytes])."""
     M, K = x.shape
     codes = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
     scales = torch.empty(mxfp4_scale_bytes(M, K), dtype=torch.uint8, device=x.device)
-    mxfp4_quantize(x, codes, scales, stream)
+    if x.dtype == torch.float16:
+        mxfp4_quantize_f16(x, codes, scales, stream)
+    else:
+        mxfp4_quantize(x, codes, scales, stream)
     return codes, scales
 
 

@@ -72,8 +72,12 @@ size_t mxfp4_grouped_scale_bytes_bound(int64_t total_rows, int32_t E, int64_t K)
   return static_cast<size_t>(tiles * 128 * padded_scale_cols(K));
 }
 
-int mxfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
-                   uint8_t* scales, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int quantize_checked(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
+                     uint8_t* scales, bool f16, void* stream) {
   if (M < 0 || K < 0) return MXFP4_EINVAL;
   if (K % 32 != 0 || ldx < K) return MXFP4_ESHAPE;
   if (M == 0 || K == 0) return MXFP4_OK;
@@ -86,8 +90,22 @@ int mxfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* co
   const Range rc = range_of(codes, M * (K / 2));
   const Range rs = range_of(scales, static_cast<int64_t>(mxfp4_scale_bytes(M, K)));
   if (overlap(rx, rc) || overlap(rx, rs) || overlap(rc, rs)) return MXFP4_EALIAS;
-  return from_cuda(mxfp4::launch_quantize(x, M, K, ldx, codes, scales,
+  return from_cuda(mxfp4::launch_quantize(x, M, K, ldx, codes, scales, f16,
                                           static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
+                   uint8_t* scales, void* stream) {
+  return quantize_checked(x, M, K, ldx, codes, scales, false, stream);
+}
+
+int mxfp4_quantize_f16(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
+                       uint8_t* scales, void* stream) {
+  return quantize_checked(x, M, K, ldx, codes, scales, true, stream);
 }
 
 int mxfp4_quantize_grouped(const void* x, int64_t total_rows, int64_t K,

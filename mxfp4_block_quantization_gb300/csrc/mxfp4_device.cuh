@@ -40,6 +40,14 @@ __device__ __forceinline__ uint32_t e8m0_from_absmax_bf16(uint32_t m) {
   return s < 254u ? s : 254u;
 }
 
+// The same rule on the float32 bits of a non-negative vecMax (used for FP16
+// input, whose block max is first widened to float32 exactly).
+__device__ __forceinline__ uint32_t e8m0_from_absmax_f32bits(uint32_t bits) {
+  uint32_t e = ((bits + (1u << 21)) & 0xFF800000u) >> 23 & 0xFFu;
+  uint32_t s = e > 2u ? e - 2u : 0u;
+  return s < 254u ? s : 254u;
+}
+
 // 2^(127 - s) as float bits for s in [1, 253]: biased exponent 254 - s.
 __device__ __forceinline__ float inv_scale_from_e8m0(uint32_t s) {
   return __uint_as_float((254u - s) << 23);
@@ -92,6 +100,52 @@ __device__ __forceinline__ uint32_t scale_cvt_e2m1x8(uint4 w, float f) {
       "and.b32 h2, %3, 0xFFFF0000;\n\t"
       "shl.b32 l3, %4, 16;\n\t"
       "and.b32 h3, %4, 0xFFFF0000;\n\t"
+      "mov.b64 fs, {%5, %5};\n\t"
+      "mov.b64 p0, {l0, h0};\n\t"
+      "mov.b64 p1, {l1, h1};\n\t"
+      "mov.b64 p2, {l2, h2};\n\t"
+      "mov.b64 p3, {l3, h3};\n\t"
+      "mul.rn.f32x2 p0, p0, fs;\n\t"
+      "mul.rn.f32x2 p1, p1, fs;\n\t"
+      "mul.rn.f32x2 p2, p2, fs;\n\t"
+      "mul.rn.f32x2 p3, p3, fs;\n\t"
+      "mov.b64 {l0, h0}, p0;\n\t"
+      "mov.b64 {l1, h1}, p1;\n\t"
+      "mov.b64 {l2, h2}, p2;\n\t"
+      "mov.b64 {l3, h3}, p3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, h0, l0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, h1, l1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, h2, l2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, h3, l3;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t"
+      "}"
+      : "=r"(r)
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "f"(f));
+  return r;
+}
+
+// The FP16 counterpart: four packed F16x2 words -> one word of eight E2M1
+// codes; each half is widened to float32 exactly (cvt.f32.f16) before the
+// power-of-two scaling.
+__device__ __forceinline__ uint32_t scale_cvt_e2m1x8_f16(uint4 w, float f) {
+  uint32_t r;
+  asm("{\n\t"
+      ".reg .b64 p0, p1, p2, p3, fs;\n\t"
+      ".reg .b16 a0, b0, a1, b1, a2, b2, a3, b3;\n\t"
+      ".reg .f32 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+      ".reg .b8 q0, q1, q2, q3;\n\t"
+      "mov.b32 {a0, b0}, %1;\n\t"
+      "mov.b32 {a1, b1}, %2;\n\t"
+      "mov.b32 {a2, b2}, %3;\n\t"
+      "mov.b32 {a3, b3}, %4;\n\t"
+      "cvt.f32.f16 l0, a0;\n\t"
+      "cvt.f32.f16 h0, b0;\n\t"
+      "cvt.f32.f16 l1, a1;\n\t"
+      "cvt.f32.f16 h1, b1;\n\t"
+      "cvt.f32.f16 l2, a2;\n\t"
+      "cvt.f32.f16 h2, b2;\n\t"
+      "cvt.f32.f16 l3, a3;\n\t"
+      "cvt.f32.f16 h3, b3;\n\t"
       "mov.b64 fs, {%5, %5};\n\t"
       "mov.b64 p0, {l0, h0};\n\t"
       "mov.b64 p1, {l1, h1};\n\t"
@@ -204,6 +258,20 @@ __device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
+}
+
+__device__ __forceinline__ uint32_t max_abs_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// FP16 bit pattern (low 16 bits) -> float32 bits, exact.
+__device__ __forceinline__ uint32_t f16_bits_to_f32_bits(uint32_t h) {
+  float f;
+  const uint16_t v = static_cast<uint16_t>(h);
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(v));
+  return __float_as_uint(f);
 }
 
 // Programmatic dependent launch: wait until the preceding grid of the stream

@@ -10,9 +10,10 @@
 
 namespace mxfp4 {
 
-// Dense quantize of a [M, K] BF16 matrix (row stride ldx elements).
+// Dense quantize of a [M, K] BF16 (or, with f16, IEEE binary16) matrix
+// (row stride ldx elements).
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
-                            uint8_t* scales, cudaStream_t stream);
+                            uint8_t* scales, bool f16, cudaStream_t stream);
 
 // Grouped quantize: validates offsets and writes padded row starts, then
 // quantizes every segment.  `bound_tiles` is the host-side upper bound of

@@ -84,7 +84,10 @@ __device__ __forceinline__ void load32(const uint8_t* src, uint4 (&v)[2]) {
 // kVec32: every lane's 32 bytes are 32-byte aligned (x and the row stride
 // are), so they arrive in one 256-bit load per pass; otherwise two 16-byte
 // loads (each then touches half of a 32-byte sector).
-template <bool kGrouped, bool kGather, bool kVec32>
+//
+// kF16: the input is IEEE binary16 instead of BF16 (same method: the block
+// max is widened to float32 exactly and the E8M0 rule is applied to its bits).
+template <bool kGrouped, bool kGather, bool kVec32, bool kF16 = false>
 __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const QuantizeParams p) {
   static_assert(kGrouped || !kGather, "gather is a grouped mode");
   __shared__ __align__(16) uint8_t chunk[kChunkBytes];
@@ -166,23 +169,36 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
     // block absmax: |x| per half with max.xorsign.abs, sign bits cleared,
     // then the larger half (unsigned order of non-negative BF16 patterns is
     // the order of their magnitudes), then the partner lane's half block
-    const uint32_t h =
-        max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(v[i][0].x, v[i][0].y),
-                                      max_abs_bf16x2(v[i][0].z, v[i][0].w)),
-                       max_abs_bf16x2(max_abs_bf16x2(v[i][1].x, v[i][1].y),
-                                      max_abs_bf16x2(v[i][1].z, v[i][1].w))) &
-        0x7FFF7FFFu;
+    uint32_t h;
+    if constexpr (kF16) {
+      h = max_abs_f16x2(max_abs_f16x2(max_abs_f16x2(v[i][0].x, v[i][0].y),
+                                      max_abs_f16x2(v[i][0].z, v[i][0].w)),
+                        max_abs_f16x2(max_abs_f16x2(v[i][1].x, v[i][1].y),
+                                      max_abs_f16x2(v[i][1].z, v[i][1].w)));
+    } else {
+      h = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(v[i][0].x, v[i][0].y),
+                                        max_abs_bf16x2(v[i][0].z, v[i][0].w)),
+                         max_abs_bf16x2(max_abs_bf16x2(v[i][1].x, v[i][1].y),
+                                        max_abs_bf16x2(v[i][1].z, v[i][1].w)));
+    }
+    h &= 0x7FFF7FFFu;
     uint32_t m = max(h & 0xFFFFu, h >> 16);
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    const uint32_t s = e8m0_from_absmax_bf16(m);
+    const uint32_t s =
+        kF16 ? e8m0_from_absmax_f32bits(f16_bits_to_f32_bits(m)) : e8m0_from_absmax_bf16(m);
     // rows of pass i sit in chunk row lr0 (outerM), word i (innerM)
     if ((lane & 1) == 0) chunk[chunk_offset(lr0 + kRowsPerPass * i, blk)] = static_cast<uint8_t>(s);
 
     // x * 2^(127-s), then round to E2M1; blocks with s == 0 emit zeros
     const float inv = inv_scale_from_e8m0(s);
     uint2 code;
-    code.x = scale_cvt_e2m1x8(v[i][0], inv);
-    code.y = scale_cvt_e2m1x8(v[i][1], inv);
+    if constexpr (kF16) {
+      code.x = scale_cvt_e2m1x8_f16(v[i][0], inv);
+      code.y = scale_cvt_e2m1x8_f16(v[i][1], inv);
+    } else {
+      code.x = scale_cvt_e2m1x8(v[i][0], inv);
+      code.y = scale_cvt_e2m1x8(v[i][1], inv);
+    }
     if (s == 0u) code = make_uint2(0u, 0u);
     if (col_ok && kRowsPerPass * i < lim) st_stream_v2(cp + i * cld_pass, code);
   }
@@ -264,7 +280,7 @@ bool vec32_ok(const void* x, int64_t ldx_bytes) {
 }  // namespace
 
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
-                            uint8_t* scales, cudaStream_t stream) {
+                            uint8_t* scales, bool f16, cudaStream_t stream) {
   QuantizeParams p{};
   p.x = static_cast<const uint8_t*>(x);
   p.ldx_bytes = ldx * 2;
@@ -276,8 +292,11 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
   p.n_units = static_cast<int32_t>(tiles * p.nKT);
-  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<false, false, true>
-                                               : quantize_tiles_kernel<false, false, false>;
+  const bool v32 = vec32_ok(x, p.ldx_bytes);
+  const auto kernel = f16 ? (v32 ? quantize_tiles_kernel<false, false, true, true>
+                                 : quantize_tiles_kernel<false, false, false, true>)
+                          : (v32 ? quantize_tiles_kernel<false, false, true>
+                                 : quantize_tiles_kernel<false, false, false>);
   return launch_pdl(kernel, static_cast<unsigned>(p.n_units), kThreads, 0, stream, p);
 }
 

@@ -63,6 +63,17 @@ def lib():
         L.orc_quantize_grouped.restype = ctypes.c_int
         L.orc_quantize_grouped.argtypes = [_u16p, _i64, _i64, _i32p, ctypes.c_int32,
                                            _u8p, _u8p, _i32p]
+        _f64p = ctypes.POINTER(ctypes.c_double)
+        L.orc_f16_to_double.restype = ctypes.c_double
+        L.orc_f16_to_double.argtypes = [ctypes.c_uint16]
+        L.orc_e2m1_encode_f16_many.restype = None
+        L.orc_e2m1_encode_f16_many.argtypes = [_u16p, _i64, ctypes.c_uint8, _u8p]
+        L.orc_f16_to_double_many.restype = None
+        L.orc_f16_to_double_many.argtypes = [_u16p, _i64, _f64p]
+        L.orc_quantize_f16.restype = None
+        L.orc_quantize_f16.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p]
+        L.orc_quantize_flat_f16.restype = None
+        L.orc_quantize_flat_f16.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p]
         L.orc_quantize_grouped_gather.restype = ctypes.c_int
         L.orc_quantize_grouped_gather.argtypes = [_u16p, _i64, _i64, _i64, _i32p, _i64, _i32p,
                                                   ctypes.c_int32, _u8p, _u8p, _i32p]
@@ -202,6 +213,42 @@ def quantize_grouped(xbits: np.ndarray, offsets: np.ndarray):
     rc = lib().orc_quantize_grouped(_p(x, _u16p), total, K, _p(off, _i32p), E,
                                     _p(codes, _u8p), _p(scales, _u8p), _p(sro, _i32p))
     return rc, codes, scales, sro
+
+
+def f16_to_double_many(hbits: np.ndarray) -> np.ndarray:
+    h = _c(hbits, np.uint16).ravel()
+    out = np.empty(h.size, np.float64)
+    lib().orc_f16_to_double_many(_p(h, _u16p), h.size, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    return out
+
+
+def e2m1_encode_f16_many(hbits: np.ndarray, s: int) -> np.ndarray:
+    """Step 3 over many FP16 elements sharing scale exponent ``s``."""
+    x = _c(hbits, np.uint16).ravel()
+    out = np.empty(x.size, np.uint8)
+    lib().orc_e2m1_encode_f16_many(_p(x, _u16p), x.size, int(s), _p(out, _u8p))
+    return out
+
+
+def quantize_f16(hbits: np.ndarray):
+    """Steps 1-5 on FP16 input [M, K] (bit patterns): (codes, tiled scales)."""
+    x = _c(hbits, np.uint16)
+    M, K = x.shape
+    codes = np.zeros((M, K // 2), np.uint8)
+    scales = np.zeros(scale_bytes(M, K), np.uint8)
+    if M and K:
+        lib().orc_quantize_f16(_p(x, _u16p), M, K, K, _p(codes, _u8p), _p(scales, _u8p))
+    return codes, scales
+
+
+def quantize_flat_f16(hbits: np.ndarray):
+    x = _c(hbits, np.uint16)
+    M, K = x.shape
+    codes = np.zeros((M, K // 2), np.uint8)
+    flat = np.zeros((M, K // 32), np.uint8)
+    if M and K:
+        lib().orc_quantize_flat_f16(_p(x, _u16p), M, K, K, _p(codes, _u8p), _p(flat, _u8p))
+    return codes, flat
 
 
 def quantize_grouped_gather(xbits: np.ndarray, row_index: np.ndarray, offsets: np.ndarray):

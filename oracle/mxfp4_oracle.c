@@ -90,12 +90,10 @@ uint8_t orc_e8m0_scale(float vecmax) {
  * (the even index), anything above 6 stays 6 (saturation); keep the sign
  * (so -0.0 and small negatives give 0x8).  Blocks with s == 0 emit 0x0 for
  * every element (the convention fixed for this library). */
-uint8_t orc_e2m1_encode(uint16_t xbits, uint8_t s) {
+static uint8_t e2m1_of_scaled(double x, int negative, uint8_t s) {
   if (s == 0) return 0;
-  double x = orc_bf16_to_double(xbits);
   double y = ldexp(x, 127 - (int)s); /* x / 2^(s-127), exact */
   double m = fabs(y);
-  uint8_t sign = (uint8_t)((xbits >> 15) & 1u);
   uint8_t idx;
   /* midpoints 0.25 0.75 1.25 1.75 2.5 3.5 5; at a tie the even index wins */
   if (m <= 0.25) idx = 0;        /* 0.25 ties 0 (idx 0) / 0.5 (idx 1)   */
@@ -106,7 +104,30 @@ uint8_t orc_e2m1_encode(uint16_t xbits, uint8_t s) {
   else if (m < 3.5) idx = 5;     /* 3.5  ties 3.0 (5) / 4.0 (6)         */
   else if (m <= 5.0) idx = 6;    /* 5.0  ties 4.0 (6) / 6.0 (7)         */
   else idx = 7;                  /* (5, inf): 6.0, saturating           */
-  return (uint8_t)((sign << 3) | idx);
+  return (uint8_t)(((negative ? 1u : 0u) << 3) | idx);
+}
+
+uint8_t orc_e2m1_encode(uint16_t xbits, uint8_t s) {
+  return e2m1_of_scaled(orc_bf16_to_double(xbits), (xbits >> 15) & 1u, s);
+}
+
+/* FP16 (IEEE binary16) input, the other 16-bit type the pages' kernel name
+ * (cvt_warp_fp16_to_fp4) and its packed half2 max refer to ([PR43557]
+ * excerpt).  Exact value of the bit pattern: sign, 5-bit exponent (bias 15),
+ * 10-bit mantissa; exponent 0 is subnormal (mantissa * 2^-24). */
+double orc_f16_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1F;
+  int m = h & 0x3FF;
+  double v;
+  if (e == 0) v = ldexp((double)m, -24);
+  else if (e == 31) v = m ? NAN : INFINITY;
+  else v = ldexp(1024.0 + m, e - 25);
+  return sign ? -v : v;
+}
+
+uint8_t orc_e2m1_encode_f16(uint16_t hbits, uint8_t s) {
+  return e2m1_of_scaled(orc_f16_to_double(hbits), (hbits >> 15) & 1u, s);
 }
 
 /* E2M1 decode (OCP MX): bit 3 sign, bits 2..1 exponent (bias 1), bit 0
@@ -125,6 +146,14 @@ void orc_e8m0_scale_many(const uint16_t* vbits, int64_t n, uint8_t* s) {
 
 void orc_e2m1_encode_many(const uint16_t* x, int64_t n, uint8_t s, uint8_t* nib) {
   for (int64_t i = 0; i < n; ++i) nib[i] = orc_e2m1_encode(x[i], s);
+}
+
+void orc_e2m1_encode_f16_many(const uint16_t* x, int64_t n, uint8_t s, uint8_t* nib) {
+  for (int64_t i = 0; i < n; ++i) nib[i] = orc_e2m1_encode_f16(x[i], s);
+}
+
+void orc_f16_to_double_many(const uint16_t* x, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_f16_to_double(x[i]);
 }
 
 /* Step 7 for one element: E2M1 value times the E8M0 value 2^(s-127), rounded
@@ -169,6 +198,31 @@ void orc_quantize_flat(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
   }
 }
 
+/* Steps 1-4 for FP16 input: the same block max (as a float: every FP16
+ * value is exact in float32), the same E8M0 rule on its float bits, the same
+ * element rounding. */
+void orc_quantize_flat_f16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                           uint8_t* codes, uint8_t* flat_scales) {
+  int64_t sK = K / 32;
+  for (int64_t r = 0; r < M; ++r) {
+    const uint16_t* row = x + r * ldx;
+    for (int64_t b = 0; b < sK; ++b) {
+      const uint16_t* blk = row + b * 32;
+      float vmax = 0.0f;
+      for (int i = 0; i < 32; ++i) {
+        float a = (float)fabs(orc_f16_to_double(blk[i]));
+        if (a > vmax) vmax = a;
+      }
+      uint8_t s = orc_e8m0_scale(vmax);
+      flat_scales[r * sK + b] = s;
+      uint8_t nib[32];
+      for (int i = 0; i < 32; ++i) nib[i] = orc_e2m1_encode_f16(blk[i], s);
+      for (int j = 0; j < 16; ++j)
+        codes[r * (K / 2) + b * 16 + j] = (uint8_t)(nib[2 * j] | (nib[2 * j + 1] << 4));
+    }
+  }
+}
+
 /* Step 5 — CUTLASS 128x4 tiled scale layout.  [PR43557] untile_cutlass_scale:
  * the tiled bytes are viewed as [numMTiles, numKTiles, 32, 4, 4] and
  * permuted (0,3,2,1,4) back to [padded_M, padded_sK]; hence flat element
@@ -202,6 +256,16 @@ void orc_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
   if (M <= 0 || sK <= 0) return;
   uint8_t* flat = (uint8_t*)calloc((size_t)(M * sK), 1);
   orc_quantize_flat(x, M, K, ldx, codes, flat);
+  orc_tile_scales(flat, M, sK, tiled_scales);
+  free(flat);
+}
+
+void orc_quantize_f16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                      uint8_t* codes, uint8_t* tiled_scales) {
+  int64_t sK = K / 32;
+  if (M <= 0 || sK <= 0) return;
+  uint8_t* flat = (uint8_t*)calloc((size_t)(M * sK), 1);
+  orc_quantize_flat_f16(x, M, K, ldx, codes, flat);
   orc_tile_scales(flat, M, sK, tiled_scales);
   free(flat);
 }

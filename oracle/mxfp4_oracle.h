@@ -44,6 +44,9 @@ float orc_block_absmax(const uint16_t* x, int64_t n);
 uint8_t orc_e8m0_scale(float vecmax);
 /* Steps 3: E2M1 nibble of one BF16 element under scale exponent s. */
 uint8_t orc_e2m1_encode(uint16_t xbits, uint8_t s);
+/* FP16 input: exact value of a binary16 pattern; nibble of one element. */
+double orc_f16_to_double(uint16_t h);
+uint8_t orc_e2m1_encode_f16(uint16_t hbits, uint8_t s);
 /* E2M1 nibble -> exact value (sign kept, code 0x8 is -0.0). */
 double orc_e2m1_decode(uint8_t nib);
 
@@ -51,6 +54,8 @@ double orc_e2m1_decode(uint8_t nib);
 void orc_e8m0_scale_many(const uint16_t* vbits, int64_t n, uint8_t* s);
 void orc_e2m1_encode_many(const uint16_t* x, int64_t n, uint8_t s, uint8_t* nib);
 void orc_dequant_value_many(const uint8_t* nib, const uint8_t* s, int64_t n, uint16_t* y);
+void orc_e2m1_encode_f16_many(const uint16_t* x, int64_t n, uint8_t s, uint8_t* nib);
+void orc_f16_to_double_many(const uint16_t* x, int64_t n, double* out);
 
 /* Tiled scale size: ceil(M/128)*128 * ceil(sK/4)*4 bytes, sK = K/32. */
 size_t orc_scale_bytes(int64_t M, int64_t K);
@@ -64,6 +69,11 @@ void orc_untile_scales(const uint8_t* tiled, int64_t M, int64_t sK, uint8_t* fla
 /* Steps 1-5 together: codes + tiled scales (orc_scale_bytes(M,K) bytes). */
 void orc_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
                   uint8_t* codes, uint8_t* tiled_scales);
+/* Steps 1-5 for FP16 input [M, K] (row stride ldx). */
+void orc_quantize_flat_f16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                           uint8_t* codes, uint8_t* flat_scales);
+void orc_quantize_f16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                      uint8_t* codes, uint8_t* tiled_scales);
 /* Step 6: per-segment quantize.  Returns 0, or -6 when the offsets break
  * 0 = o[0] <= ... <= o[E] = total_rows (then scale_row_offsets = -1 and
  * codes/scales are untouched). */

@@ -147,3 +147,11 @@ def test_grouped_gather_validation(lib):
     assert call(ldx=68) == lib.MXFP4_EALIGN
     assert call(c=2 * A + 16) == lib.MXFP4_EALIAS            # codes overlap the indices
     assert call(sro=A + 64) == lib.MXFP4_EALIAS              # offsets out overlap x
+
+
+def test_quantize_f16_validation(lib):
+    f = lib._lib.mxfp4_quantize_f16
+    assert f(A, 4, 48, 48, 2 * A, 3 * A, None) == lib.MXFP4_ESHAPE
+    assert f(A + 8, 4, 64, 64, 2 * A, 3 * A, None) == lib.MXFP4_EALIGN
+    assert f(A, 4, 64, 64, A + 64, 3 * A, None) == lib.MXFP4_EALIAS
+    assert f(None, 0, 64, 64, None, None, None) == lib.MXFP4_OK

@@ -434,3 +434,68 @@ def test_grouped_gather_16b_aligned_input(mx):
     assert st == 0 and np.array_equal(c, c_o)
     used = int(sro_o[-1]) * 8
     assert np.array_equal(s[:used], s_o[:used])
+
+
+# ------------------------------------------------------------- FP16 input
+def f16_bits(t):
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_quantize_f16(mx, x):
+    M, K = x.shape
+    codes = Guarded(M * (K // 2), shape=(M, K // 2))
+    scales = Guarded(mx.mxfp4_scale_bytes(M, K))
+    mx.mxfp4_quantize_f16(x, codes.t, scales.t)
+    torch.cuda.synchronize()
+    codes.check()
+    scales.check()
+    return codes.t.cpu().numpy(), scales.t.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,K", [(4096, 7168), (1000, 2880), (129, 160)])
+def test_f16_dense(mx, M, K):
+    x = W.dense_activation(13, M, K, device="cuda").float()
+    x[::7, ::5] *= 2.0 ** -12                                    # FP16 subnormals too
+    x = x.to(torch.float16)
+    c, s = run_quantize_f16(mx, x)
+    c_o, s_o = oracle.quantize_f16(f16_bits(x))
+    assert np.array_equal(c, c_o), _first_diff(c, c_o)
+    assert np.array_equal(s, s_o), _first_diff(s, s_o)
+
+
+def test_f16_16b_aligned_input(mx):
+    x = W.dense_activation(14, 200, 1024, device="cuda").to(torch.float16)
+    flat = torch.empty(x.numel() + 8, dtype=torch.float16, device="cuda")
+    y = flat[8:].view(x.shape)
+    y.copy_(x)
+    c, s = run_quantize_f16(mx, y)
+    c_o, s_o = oracle.quantize_f16(f16_bits(x))
+    assert np.array_equal(c, c_o) and np.array_equal(s, s_o)
+
+
+def test_f16_element_map_exhaustive(mx):
+    """Every finite FP16 value under every scale exponent FP16 block maxima
+    reach (s = 101..141)."""
+    finite = np.arange(0x0000, 0x7C00, dtype=np.uint16)
+    rows = []
+    for s in range(101, 142):
+        e = s - 125                                                   # vmax = 2^e
+        if s == 141:
+            vmax = 0x7BFF                                             # 65504
+        elif e >= -14:
+            vmax = (e + 15) << 10
+        else:
+            vmax = 1 << (e + 24)                                      # subnormal power of two
+        vals = finite[finite <= vmax]
+        vals = np.concatenate([vals, vals | 0x8000])
+        pad = (-vals.size) % 31
+        vals = np.concatenate([vals, np.zeros(pad, np.uint16)]).reshape(-1, 31)
+        rows.append(np.concatenate([np.full((vals.shape[0], 1), vmax, np.uint16), vals], axis=1))
+    blocks = np.concatenate(rows)
+    blocks = np.concatenate([blocks, np.zeros(((-blocks.shape[0]) % 32, 32), np.uint16)])
+    hb = blocks.reshape(-1, 1024)
+    x = torch.from_numpy(hb.view(np.int16)).view(torch.float16).cuda()
+    c, s = run_quantize_f16(mx, x)
+    c_o, s_o = oracle.quantize_f16(hb)
+    assert np.array_equal(s, s_o), _first_diff(s, s_o)
+    assert np.array_equal(c, c_o), _first_diff(c, c_o)

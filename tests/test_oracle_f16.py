@@ -1,0 +1,59 @@
+"""Pins of the oracle's FP16-input path (same MX method, binary16 input)."""
+import numpy as np
+
+from mxfp4_block_quantization_gb300 import workloads as W
+
+E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+ALL = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+FIN16 = ALL[(ALL & 0x7C00) != 0x7C00]
+
+
+def test_f16_decode_matches_numpy(orc):
+    got = orc.f16_to_double_many(ALL)
+    want = ALL.view(np.float16).astype(np.float64)
+    fin = np.isfinite(want)
+    assert np.array_equal(got[fin], want[fin])
+    assert np.array_equal(np.isinf(got), np.isinf(want)) and np.array_equal(np.isnan(got), np.isnan(want))
+
+
+def test_f16_element_map_exhaustive(orc):
+    xv = FIN16.view(np.float16).astype(np.float64)
+    sign = ((FIN16 >> 15) & 1).astype(np.uint8)
+    for s in range(1, 255):
+        m = np.minimum(np.abs(np.ldexp(xv, 127 - s)), 7.0)
+        d = np.abs(m[:, None] - E2M1_MAG[None, :])
+        dmin = d.min(axis=1, keepdims=True)
+        w = np.where(np.arange(8) % 2 == 0, 2, 1)[None, :]
+        want = (sign << 3) | np.argmax((d == dmin) * w, axis=1).astype(np.uint8)
+        got = orc.e2m1_encode_f16_many(FIN16, s)
+        assert np.array_equal(got, want), s
+    assert not orc.e2m1_encode_f16_many(FIN16, 0).any()
+
+
+def test_f16_quantize_is_blockwise_steps(orc):
+    x = W.dense_activation(11, 64, 256).to(__import__("torch").float16)
+    h = x.view(__import__("torch").int16).numpy().view(np.uint16)
+    codes, flat = orc.quantize_flat_f16(h)
+    xv = h.view(np.float16).astype(np.float64)
+    nib = np.zeros((64, 256), np.uint8)
+    nib[:, 0::2] = codes & 0xF
+    nib[:, 1::2] = codes >> 4
+    for r in range(0, 64, 5):
+        for b in range(8):
+            vmax = np.abs(xv[r, b * 32:(b + 1) * 32]).max()
+            s = orc.e8m0_scale(vmax)
+            assert flat[r, b] == s
+            assert np.array_equal(nib[r, b * 32:(b + 1) * 32],
+                                  orc.e2m1_encode_f16_many(h[r, b * 32:(b + 1) * 32], s))
+
+
+def test_f16_and_bf16_agree_on_shared_values(orc):
+    """Values exactly representable in both formats quantize identically."""
+    import torch
+    x = W.dense_activation(12, 128, 512).float()
+    x = torch.where(x.abs() < 2.0 ** -14, torch.zeros_like(x), x).to(torch.bfloat16)
+    x16 = x.to(torch.float16)                            # FP16 normals hold any BF16 value exactly
+    assert torch.equal(x16.to(torch.bfloat16), x)        # every value survives the round trip
+    cb, sb = orc.quantize(W.bf16_bits(x))
+    ch, sh = orc.quantize_f16(x16.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(cb, ch) and np.array_equal(sb, sh)
