@@ -23,6 +23,7 @@ _u8p = ctypes.POINTER(ctypes.c_uint8)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
 _i64 = ctypes.c_int64
 
 
@@ -63,7 +64,6 @@ def lib():
         L.orc_quantize_grouped.restype = ctypes.c_int
         L.orc_quantize_grouped.argtypes = [_u16p, _i64, _i64, _i32p, ctypes.c_int32,
                                            _u8p, _u8p, _i32p]
-        _f64p = ctypes.POINTER(ctypes.c_double)
         L.orc_f16_to_double.restype = ctypes.c_double
         L.orc_f16_to_double.argtypes = [ctypes.c_uint16]
         L.orc_e2m1_encode_f16_many.restype = None
@@ -74,6 +74,20 @@ def lib():
         L.orc_quantize_f16.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p]
         L.orc_quantize_flat_f16.restype = None
         L.orc_quantize_flat_f16.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p]
+        L.orc_e4m3_to_double.restype = ctypes.c_double
+        L.orc_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_from_double.restype = ctypes.c_uint8
+        L.orc_e4m3_from_double.argtypes = [ctypes.c_double]
+        L.orc_e4m3_from_double_many.restype = None
+        L.orc_e4m3_from_double_many.argtypes = [_f64p, _i64, _u8p]
+        L.orc_nvfp4_scale_bytes.restype = ctypes.c_size_t
+        L.orc_nvfp4_scale_bytes.argtypes = [_i64, _i64]
+        L.orc_nvfp4_quantize_flat.restype = None
+        L.orc_nvfp4_quantize_flat.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_float, _u8p, _u8p]
+        L.orc_nvfp4_quantize.restype = None
+        L.orc_nvfp4_quantize.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_float, _u8p, _u8p]
+        L.orc_nvfp4_dequantize.restype = None
+        L.orc_nvfp4_dequantize.argtypes = [_u8p, _u8p, _i64, _i64, ctypes.c_float, _u16p]
         L.orc_quantize_grouped_gather.restype = ctypes.c_int
         L.orc_quantize_grouped_gather.argtypes = [_u16p, _i64, _i64, _i64, _i32p, _i64, _i32p,
                                                   ctypes.c_int32, _u8p, _u8p, _i32p]
@@ -337,3 +351,54 @@ def quantize_rows_into(xbits: np.ndarray, row0: int, row1: int, codes: np.ndarra
     lib().orc_quantize(xs.ctypes.data_as(_u16p), row1 - row0, K, K,
                        cs.ctypes.data_as(_u8p),
                        scales[off:].ctypes.data_as(_u8p))
+
+
+# ------------------------------------------------------------------ NVFP4
+def e4m3_to_double(b: int) -> float:
+    return lib().orc_e4m3_to_double(int(b))
+
+
+def e4m3_from_double_many(d: np.ndarray) -> np.ndarray:
+    """Nearest FP8 E4M3 (ties to even, saturating at 448) of float64 values."""
+    x = _c(d, np.float64).ravel()
+    out = np.empty(x.size, np.uint8)
+    lib().orc_e4m3_from_double_many(x.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), x.size,
+                                    _p(out, _u8p))
+    return out
+
+
+def nvfp4_scale_bytes(M: int, K: int) -> int:
+    return int(lib().orc_nvfp4_scale_bytes(int(M), int(K)))
+
+
+def nvfp4_quantize_flat(xbits: np.ndarray, g: float):
+    """NVFP4 steps on BF16 [M, K]: (codes [M, K/2], flat E4M3 scales [M, K/16])."""
+    x = _c(xbits, np.uint16)
+    M, K = x.shape
+    codes = np.zeros((M, K // 2), np.uint8)
+    flat = np.zeros((M, K // 16), np.uint8)
+    if M and K:
+        lib().orc_nvfp4_quantize_flat(_p(x, _u16p), M, K, K, float(np.float32(g)),
+                                      _p(codes, _u8p), _p(flat, _u8p))
+    return codes, flat
+
+
+def nvfp4_quantize(xbits: np.ndarray, g: float):
+    """NVFP4 on BF16 [M, K]: (codes [M, K/2], 128x4-tiled E4M3 scales)."""
+    x = _c(xbits, np.uint16)
+    M, K = x.shape
+    codes = np.zeros((M, K // 2), np.uint8)
+    scales = np.zeros(nvfp4_scale_bytes(M, K), np.uint8)
+    if M and K:
+        lib().orc_nvfp4_quantize(_p(x, _u16p), M, K, K, float(np.float32(g)), _p(codes, _u8p),
+                                 _p(scales, _u8p))
+    return codes, scales
+
+
+def nvfp4_dequantize(codes: np.ndarray, tiled: np.ndarray, M: int, K: int, g: float) -> np.ndarray:
+    c = _c(codes, np.uint8)
+    t = _c(tiled, np.uint8).ravel()
+    y = np.zeros((M, K), np.uint16)
+    if M and K:
+        lib().orc_nvfp4_dequantize(_p(c, _u8p), _p(t, _u8p), M, K, float(np.float32(g)), _p(y, _u16p))
+    return y

@@ -9,9 +9,13 @@
  */
 #include "mxfp4_oracle.h"
 
+#include <float.h>
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* float expressions must round every operation to float (x86-64 SSE, AArch64) */
+_Static_assert(FLT_EVAL_METHOD == 0, "float arithmetic must be evaluated in float");
 
 /* ---------------------------------------------------------------------- */
 /* BF16 helpers (IEEE binary32 with the low 16 mantissa bits dropped).     */
@@ -90,9 +94,7 @@ uint8_t orc_e8m0_scale(float vecmax) {
  * (the even index), anything above 6 stays 6 (saturation); keep the sign
  * (so -0.0 and small negatives give 0x8).  Blocks with s == 0 emit 0x0 for
  * every element (the convention fixed for this library). */
-static uint8_t e2m1_of_scaled(double x, int negative, uint8_t s) {
-  if (s == 0) return 0;
-  double y = ldexp(x, 127 - (int)s); /* x / 2^(s-127), exact */
+static uint8_t e2m1_round(double y, int negative) {
   double m = fabs(y);
   uint8_t idx;
   /* midpoints 0.25 0.75 1.25 1.75 2.5 3.5 5; at a tie the even index wins */
@@ -105,6 +107,11 @@ static uint8_t e2m1_of_scaled(double x, int negative, uint8_t s) {
   else if (m <= 5.0) idx = 6;    /* 5.0  ties 4.0 (6) / 6.0 (7)         */
   else idx = 7;                  /* (5, inf): 6.0, saturating           */
   return (uint8_t)(((negative ? 1u : 0u) << 3) | idx);
+}
+
+static uint8_t e2m1_of_scaled(double x, int negative, uint8_t s) {
+  if (s == 0) return 0;
+  return e2m1_round(ldexp(x, 127 - (int)s), negative); /* x / 2^(s-127), exact */
 }
 
 uint8_t orc_e2m1_encode(uint16_t xbits, uint8_t s) {
@@ -390,4 +397,133 @@ void orc_swap_w13(const uint8_t* codes_in, const uint8_t* scales_in,
   }
   if (w13_bias_in) orc_swap_bias_bf16(w13_bias_in, w13_bias_out, E, two_n);
   if (w2_bias_in) orc_cast_bf16(w2_bias_in, w2_bias_out, w2_bias_numel);
+}
+
+/* ======================================================================
+ * NVFP4 — the other branch of the pages' quantize kernel ([PR43557]
+ * "Implementation breakdown" item 1, the non-UE8M0 branch of the
+ * cvt_warp_fp16_to_fp4 excerpt, and "Review highlights": the block scale is
+ * SFScaleVal * vecMax / 6 stored as FP8 E4M3, and the value used to scale the
+ * elements must be the E4M3-rounded one, SFValue = float(E4M3 byte)).
+ * Readings where the pages are silent: 16-element blocks; the global scale
+ * SFScaleVal (g) is a float supplied by the caller; every step is one IEEE
+ * float32 operation rounded to nearest even, in this order:
+ *   q   = vecMax / 6;  sf = g * q;  byte = E4M3_RNE_satfinite(sf);
+ *   SFValue = float(byte);  inv = g / SFValue;  y = x * inv;
+ *   code = E2M1 RNE (saturating) of y;  blocks with byte == 0 emit 0x0.
+ * Dequantize: t = e2m1(code) * SFValue (exact); y = t * (1/g) with 1/g one
+ * float32 division, as NVFP4 consumers apply one global dequant factor;
+ * BF16 RNE of y.
+ * ====================================================================== */
+
+/* FP8 E4M3 (OCP FP8, "fn" variant): sign, 4-bit exponent (bias 7), 3-bit
+ * mantissa, exponent 0 subnormal (m * 2^-9), largest finite 448 (0x7E), 0x7F
+ * NaN, no infinities. */
+double orc_e4m3_to_double(uint8_t b) {
+  int sign = (b >> 7) & 1;
+  int e = (b >> 3) & 0xF;
+  int m = b & 7;
+  double v;
+  if (e == 15 && m == 7) v = NAN;
+  else if (e == 0) v = ldexp((double)m, -9);
+  else v = ldexp(8.0 + m, e - 10);
+  return sign ? -v : v;
+}
+
+/* Nearest E4M3 value, ties to the even mantissa, magnitudes above 448
+ * saturate to 448 (satfinite); NaN -> 0x7F. */
+uint8_t orc_e4m3_from_double(double d) {
+  uint8_t sign = signbit(d) ? 0x80u : 0u;
+  if (isnan(d)) return (uint8_t)(sign | 0x7Fu);
+  double a = fabs(d);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7Eu);
+  /* quantum: 2^-9 in the subnormal range (a < 2^-6), else 2^(e-3) */
+  int e;
+  frexp(a, &e);
+  int ex = e - 1; /* floor(log2 a) */
+  int qexp = (a < ldexp(1.0, -6)) ? -9 : ex - 3;
+  double n = nearbyint(ldexp(a, -qexp));
+  double r = ldexp(n, qexp);
+  if (r > 448.0) r = 448.0;
+  if (r == 0.0) return sign;
+  if (r < ldexp(1.0, -6)) return (uint8_t)(sign | (uint8_t)n); /* subnormal */
+  frexp(r, &e);
+  int rexp = e - 1;
+  uint32_t mant = (uint32_t)(ldexp(r, -rexp) * 8.0 - 8.0);
+  return (uint8_t)(sign | ((uint32_t)(rexp + 7) << 3) | mant);
+}
+
+static float f32_of_bf16(uint16_t b) { return bf16_to_float(b); }
+
+/* Steps of one 16-element block: its E4M3 scale byte and 16 nibbles. */
+static void nvfp4_block(const uint16_t* x, float g, uint8_t* sf_byte, uint8_t* nib) {
+  float vmax = 0.0f;
+  for (int i = 0; i < 16; ++i) {
+    float a = f32_of_bf16((uint16_t)(x[i] & 0x7FFFu));
+    if (a > vmax) vmax = a;
+  }
+  float q = vmax / 6.0f; /* each float step rounds once (no contraction) */
+  float sf = g * q;
+  uint8_t byte = orc_e4m3_from_double((double)sf);
+  *sf_byte = byte;
+  float sfv = (float)orc_e4m3_to_double(byte);
+  if (byte == 0 || sfv == 0.0f) {
+    for (int i = 0; i < 16; ++i) nib[i] = 0;
+    return;
+  }
+  float inv = g / sfv;
+  for (int i = 0; i < 16; ++i) {
+    float y = f32_of_bf16(x[i]) * inv;
+    nib[i] = e2m1_round((double)y, (x[i] >> 15) & 1u);
+  }
+}
+
+size_t orc_nvfp4_scale_bytes(int64_t M, int64_t K) {
+  if (M <= 0 || K <= 0 || K % 16 != 0) return 0;
+  return (size_t)((M + 127) / 128 * 128 * ((K / 16 + 3) / 4 * 4));
+}
+
+void orc_nvfp4_quantize_flat(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float g,
+                             uint8_t* codes, uint8_t* flat_scales) {
+  int64_t sK = K / 16;
+  for (int64_t r = 0; r < M; ++r)
+    for (int64_t b = 0; b < sK; ++b) {
+      uint8_t nib[16];
+      nvfp4_block(x + r * ldx + b * 16, g, &flat_scales[r * sK + b], nib);
+      for (int j = 0; j < 8; ++j)
+        codes[r * (K / 2) + b * 8 + j] = (uint8_t)(nib[2 * j] | (nib[2 * j + 1] << 4));
+    }
+}
+
+void orc_nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float g,
+                        uint8_t* codes, uint8_t* tiled_scales) {
+  int64_t sK = K / 16;
+  if (M <= 0 || sK <= 0) return;
+  uint8_t* flat = (uint8_t*)calloc((size_t)(M * sK), 1);
+  orc_nvfp4_quantize_flat(x, M, K, ldx, g, codes, flat);
+  orc_tile_scales(flat, M, sK, tiled_scales); /* same 128x4 tiling, 16-element columns */
+  free(flat);
+}
+
+void orc_nvfp4_dequantize(const uint8_t* codes, const uint8_t* tiled_scales, int64_t M, int64_t K,
+                          float g, uint16_t* y) {
+  int64_t sK = K / 16;
+  if (M <= 0 || sK <= 0) return;
+  uint8_t* flat = (uint8_t*)calloc((size_t)(M * sK), 1);
+  orc_untile_scales(tiled_scales, M, sK, flat);
+  float inv_g = 1.0f / g;
+  for (int64_t r = 0; r < M; ++r)
+    for (int64_t k = 0; k < K; ++k) {
+      uint8_t byte = codes[r * (K / 2) + k / 2];
+      uint8_t nib = (k % 2 == 0) ? (byte & 0xFu) : (byte >> 4);
+      float sfv = (float)orc_e4m3_to_double(flat[r * sK + k / 16]);
+      float t = (float)orc_e2m1_decode(nib) * sfv; /* exact */
+      float v = t * inv_g;
+      y[r * K + k] = orc_double_to_bf16_rne((double)v);
+    }
+  free(flat);
+}
+
+void orc_e4m3_from_double_many(const double* d, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_from_double(d[i]);
 }

@@ -104,6 +104,18 @@ void orc_swap_w13(const uint8_t* codes_in, const uint8_t* scales_in,
                   uint16_t* w13_bias_out, const float* w2_bias_in,
                   int64_t w2_bias_numel, uint16_t* w2_bias_out);
 
+/* NVFP4 (16-element blocks, E4M3 block scale, caller's global scale g). */
+double orc_e4m3_to_double(uint8_t b);
+uint8_t orc_e4m3_from_double(double d);
+void orc_e4m3_from_double_many(const double* d, int64_t n, uint8_t* out);
+size_t orc_nvfp4_scale_bytes(int64_t M, int64_t K);
+void orc_nvfp4_quantize_flat(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float g,
+                             uint8_t* codes, uint8_t* flat_scales);
+void orc_nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float g,
+                        uint8_t* codes, uint8_t* tiled_scales);
+void orc_nvfp4_dequantize(const uint8_t* codes, const uint8_t* tiled_scales, int64_t M, int64_t K,
+                          float g, uint16_t* y);
+
 #ifdef __cplusplus
 }
 #endif

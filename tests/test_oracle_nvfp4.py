@@ -1,0 +1,110 @@
+"""Pins of the oracle's NVFP4 path: FP8 E4M3 conversion, the block steps, the
+tiled layout with 16-element scale columns, and dequantize."""
+import numpy as np
+import pytest
+import torch
+
+from conftest import load_golden
+from mxfp4_block_quantization_gb300 import workloads as W
+
+E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def torch_e4m3(vals):
+    t = torch.tensor(np.asarray(vals, np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def test_e4m3_decode_matches_torch(orc):
+    b = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(b.copy()).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    got = np.array([orc.e4m3_to_double(int(v)) for v in b])
+    fin = np.isfinite(want)
+    assert np.array_equal(got[fin], want[fin]) and np.isnan(got[~fin]).all()
+    assert orc.e4m3_to_double(0x7E) == 448.0
+
+
+def test_e4m3_encode_matches_torch_in_range(orc):
+    """Round to nearest even against torch's float32 -> float8_e4m3fn cast:
+    random values, every exact midpoint between neighbours, subnormals."""
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([
+        rng.uniform(-448, 448, 20000),
+        np.exp2(rng.uniform(-12, 8.8, 20000)) * rng.choice([-1, 1], 20000),
+    ])
+    grid = np.unique(np.abs([orc.e4m3_to_double(i) for i in range(0x7F)]))
+    mids = (grid[:-1] + grid[1:]) / 2
+    vals = np.concatenate([vals, mids, -mids, grid]).astype(np.float32)
+    vals = vals[np.abs(vals) <= 448]
+    assert np.array_equal(orc.e4m3_from_double_many(vals.astype(np.float64)), torch_e4m3(vals))
+
+
+def test_e4m3_saturates(orc):
+    big = np.array([448.0, 449.0, 463.99, 464.0, 1e6, -500.0])
+    assert [hex(v) for v in orc.e4m3_from_double_many(big)] == ["0x7e"] * 5 + ["0xfe"]
+
+
+def _nibbles(codes):
+    n = np.zeros((codes.shape[0], codes.shape[1] * 2), np.uint8)
+    n[:, 0::2] = codes & 0xF
+    n[:, 1::2] = codes >> 4
+    return n
+
+
+def test_nvfp4_worked_blocks(orc):
+    g = load_golden("nvfp4_worked_blocks.json")
+    for blk in g["blocks"]:
+        x = np.zeros((1, 16), np.uint16)
+        vals = [int(h, 16) for h in blk["x"]]
+        x[0, :len(vals)] = vals
+        codes, flat = orc.nvfp4_quantize_flat(x, blk["g"])
+        assert int(flat[0, 0]) == int(blk["sf"], 16), blk["name"]
+        want = np.zeros(16, np.uint8)
+        want[:len(blk["codes"])] = [int(c, 16) for c in blk["codes"]]
+        assert list(_nibbles(codes)[0]) == list(want), blk["name"]
+    for c in g["dequant"]:
+        codes = np.zeros((1, 32), np.uint8)
+        codes[0, 0] = int(c["code"], 16)
+        flat = np.zeros((1, 4), np.uint8)
+        flat[0, 0] = int(c["sf"], 16)
+        y = orc.nvfp4_dequantize(codes, orc.tile(flat), 1, 64, c["g"])
+        assert int(y[0, 0]) == int(c["y"], 16), c
+
+
+@pytest.mark.parametrize("g", [1.0, 0.37, 2688.0 / 17.0])
+def test_nvfp4_block_properties(orc, g):
+    """Every block: the scale byte is the nearest E4M3 to g*vecMax/6 (within
+    its half-ulp, or saturated), and every code is the E2M1 value nearest to
+    x*g/SFValue (up to the float32 rounding of g/SFValue)."""
+    x = W.dense_activation(21, 64, 256)
+    xb = W.bf16_bits(x)
+    codes, flat = orc.nvfp4_quantize_flat(xb, g)
+    xv = x.float().numpy().astype(np.float64).reshape(64, 16, 16)
+    vmax = np.abs(xv).max(axis=2)
+    target = g * vmax / 6
+    sfv = np.vectorize(orc.e4m3_to_double)(flat)
+    grid = np.unique(np.abs([orc.e4m3_to_double(i) for i in range(0x7F)]))
+    for t, v in zip(target.ravel(), sfv.ravel()):
+        if t >= 448:
+            assert v == 448
+        else:
+            nearest = grid[np.argmin(np.abs(grid - t))]
+            assert abs(v - t) <= abs(nearest - t) * (1 + 1e-6) + 1e-12
+    nib = _nibbles(codes).reshape(64, 16, 16)
+    mag = E2M1[nib & 7]
+    y = np.abs(xv) * g / np.where(sfv > 0, sfv, 1)[:, :, None]
+    y = np.minimum(y, 6.5)
+    err = np.abs(mag - y)
+    step = np.where(y < 2, 0.25, np.where(y < 4, 0.5, 1.0))
+    live = (sfv > 0)[:, :, None] & np.ones_like(y, bool)
+    assert np.all(err[live] <= step[live] * (1 + 1e-5) + 1e-6)
+    assert not nib[~live].any()
+
+
+def test_nvfp4_tiled_layout_is_the_mx_layout_on_16_element_columns(orc):
+    x = W.bf16_bits(W.dense_activation(22, 200, 480))
+    codes, tiled = orc.nvfp4_quantize(x, 1.0)
+    c2, flat = orc.nvfp4_quantize_flat(x, 1.0)
+    assert np.array_equal(codes, c2)
+    assert tiled.size == orc.nvfp4_scale_bytes(200, 480) == 256 * 32
+    assert np.array_equal(orc.untile(tiled, 200, 30), flat)
