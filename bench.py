@@ -333,6 +333,22 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     out["quantize_f16_4096x7168"] = entry(quant_bytes(M, K), ms, 1, f"{R} rotating sets")
     del x16s, cs16, ss16
 
+    # NVFP4 (16-element blocks, E4M3 scales, global scale 448*6/amax): quantize
+    # and dequantize of the same 4096 x 7168 activation
+    xs_nv = [W.dense_activation(1, M, K, device="cuda") for _ in range(R)]
+    g_nv = torch.tensor([448.0 * 6.0 / float(xs_nv[0].float().abs().max())], device="cuda")
+    sb_nv = mx.mxfp4_nvfp4_scale_bytes(M, K)
+    cs_nv = [torch.empty((M, K // 2), dtype=torch.uint8, device="cuda") for _ in range(R)]
+    ss_nv = [torch.empty(sb_nv, dtype=torch.uint8, device="cuda") for _ in range(R)]
+    ms = time_launches(lambda i: mx.mxfp4_quantize_nvfp4(xs_nv[i % R], g_nv, cs_nv[i % R],
+                                                         ss_nv[i % R], stream), 200, stream)
+    nb_nv = 2 * M * K + M * K // 2 + sb_nv
+    out["nvfp4_quantize_4096x7168"] = entry(nb_nv, ms, 1, f"{R} rotating sets")
+    ms = time_launches(lambda i: mx.mxfp4_dequantize_nvfp4(cs_nv[i % R], ss_nv[i % R], g_nv, M, K,
+                                                           xs_nv[i % R], stream), 200, stream)
+    out["nvfp4_dequantize_4096x7168"] = entry(nb_nv, ms, 1, f"{R} rotating sets")
+    del xs_nv, cs_nv, ss_nv
+
     # grouped MoE activations: 16384 tokens x top-8 over 384 experts, K = 7168
     g = W.moe_grouped(seed=2, device="cuda")
     total, K = g.x.shape

@@ -199,6 +199,33 @@ int mxfp4_swap_w13(const uint8_t* codes_in, const uint8_t* scales_in,
                    void* w13_bias_out, const float* w2_bias_in,
                    int64_t w2_bias_numel, void* w2_bias_out, void* stream);
 
+/* ---------------------------------------------------------------- NVFP4
+ * The other branch of the same quantize kernel on [PR43557] ("Implementation
+ * breakdown" item 1, the non-UE8M0 branch of the cvt_warp_fp16_to_fp4
+ * excerpt, and "Review highlights"): one FP8 E4M3 scale per block,
+ * SFScaleVal * vecMax / 6, and the elements scaled with the E4M3-rounded
+ * value so quantize and dequantize agree.  Readings where the page is
+ * silent: 16-element blocks; every step one IEEE float32 operation rounded
+ * to nearest even:
+ *   q = vecMax / 6; sf = g * q; byte = E4M3_RNE_satfinite(sf);
+ *   inv = g / float(byte); code = E2M1_RNE_saturating(x * inv);
+ *   blocks whose byte is 0 emit zero codes;
+ *   dequantize: y = BF16_RNE((e2m1(code) * float(byte)) * (1 / g)).
+ * g is the per-tensor global scale (SFScaleVal), a positive finite float
+ * read from DEVICE memory (global_scale, 4-byte aligned).
+ * Scales use the 128x4 tiled layout of mxfp4_quantize over K/16 scale
+ * columns: mxfp4_nvfp4_scale_bytes(M, K) = ceil(M/128)*128 * ceil(K/64)*4
+ * bytes, pad bytes 0x00.  Codes: [M, K/2], element 2j in the low nibble.
+ * K % 16 == 0; other arguments, alignment and errors as mxfp4_quantize /
+ * mxfp4_dequantize. */
+size_t mxfp4_nvfp4_scale_bytes(int64_t M, int64_t K);
+int mxfp4_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
+                         const float* global_scale, uint8_t* codes, uint8_t* scales,
+                         void* stream);
+int mxfp4_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales,
+                           const float* global_scale, int64_t M, int64_t K, void* y,
+                           void* stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* mxfp4_status_string(int status);
 

@@ -30,7 +30,8 @@ __all__ = [
     "mxfp4_status_string", "mxfp4_version", "quantize", "quantize_grouped", "dequantize",
     "swap_w13", "MXFP4_OK", "MXFP4_EINVAL", "MXFP4_EALIGN", "MXFP4_ESHAPE", "MXFP4_EALIAS",
     "MXFP4_ECUDA", "MXFP4_EOFFSETS", "MXFP4_EINDEX", "mxfp4_quantize_grouped_gather",
-    "quantize_grouped_gather", "mxfp4_quantize_f16",
+    "quantize_grouped_gather", "mxfp4_quantize_f16", "mxfp4_nvfp4_scale_bytes",
+    "mxfp4_quantize_nvfp4", "mxfp4_dequantize_nvfp4", "quantize_nvfp4", "dequantize_nvfp4",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300.so")
@@ -77,6 +78,12 @@ def _load():
     L.mxfp4_dequantize.argtypes = [vp, vp, i64, i64, vp, vp]
     L.mxfp4_swap_w13.restype = ctypes.c_int
     L.mxfp4_swap_w13.argtypes = [vp, vp, vp, i32, i64, i64, i32, vp, vp, vp, vp, i64, vp, vp]
+    L.mxfp4_nvfp4_scale_bytes.restype = ctypes.c_size_t
+    L.mxfp4_nvfp4_scale_bytes.argtypes = [i64, i64]
+    L.mxfp4_quantize_nvfp4.restype = ctypes.c_int
+    L.mxfp4_quantize_nvfp4.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp]
+    L.mxfp4_dequantize_nvfp4.restype = ctypes.c_int
+    L.mxfp4_dequantize_nvfp4.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     L.mxfp4_status_string.restype = ctypes.c_char_p
     L.mxfp4_status_string.argtypes = [ctypes.c_int]
     L.mxfp4_version.restype = ctypes.c_int
@@ -228,6 +235,37 @@ def mxfp4_swap_w13(codes_in, scales_in, w13_bias_in, E: int, two_n: int, K: int,
                                _ptr(w2_bias_out), _stream(stream, dev)), "mxfp4_swap_w13")
 
 
+def mxfp4_nvfp4_scale_bytes(M: int, K: int) -> int:
+    return int(_lib.mxfp4_nvfp4_scale_bytes(int(M), int(K)))
+
+
+def mxfp4_quantize_nvfp4(x, global_scale, codes, scales, stream=None) -> None:
+    """NVFP4: BF16 ``x`` [M, K] with float32 ``global_scale`` (1 element,
+    device) -> codes [M, K/2] + tiled E4M3 scales."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("global_scale", global_scale, torch.float32)
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    M, K = x.shape
+    _check(_lib.mxfp4_quantize_nvfp4(_ptr(x), M, K, x.stride(0), _ptr(global_scale), _ptr(codes),
+                                     _ptr(scales), _stream(stream, x.device)),
+           "mxfp4_quantize_nvfp4")
+
+
+def mxfp4_dequantize_nvfp4(codes, scales, global_scale, M: int, K: int, y, stream=None) -> None:
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    _need_cuda("global_scale", global_scale, torch.float32)
+    _need_cuda("y", y, torch.bfloat16)
+    if not y.is_contiguous():
+        raise ValueError("y must be contiguous")
+    _check(_lib.mxfp4_dequantize_nvfp4(_ptr(codes), _ptr(scales), _ptr(global_scale), int(M),
+                                       int(K), _ptr(y), _stream(stream, y.device)),
+           "mxfp4_dequantize_nvfp4")
+
+
 # --------------------------------------------------- allocating wrappers
 def quantize(x, stream=None):
     """BF16 or FP16 ``x`` [M, K] -> (codes uint8 [M, K/2], scales uint8 [scale_bytes])."""
@@ -290,3 +328,18 @@ def swap_w13(codes, scales, w13_bias=None, w2_bias=None, scales_tiled=True, stre
     mxfp4_swap_w13(codes, scales, w13_bias, E, two_n, K, 1 if scales_tiled else 0, codes_out,
                    scales_out, b13, w2_bias, b2, stream)
     return codes_out, scales_out, b13, b2
+
+
+def quantize_nvfp4(x, global_scale, stream=None):
+    """Returns (codes uint8 [M, K/2], E4M3 scales uint8 [nvfp4_scale_bytes])."""
+    M, K = x.shape
+    codes = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
+    scales = torch.empty(mxfp4_nvfp4_scale_bytes(M, K), dtype=torch.uint8, device=x.device)
+    mxfp4_quantize_nvfp4(x, global_scale, codes, scales, stream)
+    return codes, scales
+
+
+def dequantize_nvfp4(codes, scales, global_scale, M: int, K: int, stream=None):
+    y = torch.empty((M, K), dtype=torch.bfloat16, device=codes.device)
+    mxfp4_dequantize_nvfp4(codes, scales, global_scale, M, K, y, stream)
+    return y

@@ -265,6 +265,54 @@ int mxfp4_swap_w13(const uint8_t* codes_in, const uint8_t* scales_in, const floa
   return from_cuda(mxfp4::launch_swap_w13(a, static_cast<cudaStream_t>(stream)));
 }
 
+size_t mxfp4_nvfp4_scale_bytes(int64_t M, int64_t K) {
+  if (M <= 0 || K <= 0 || K % 16 != 0) return 0;
+  return static_cast<size_t>(ceil_div(M, 128) * 128 * ceil_div(K / 16, 4) * 4);
+}
+
+int mxfp4_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
+                         const float* global_scale, uint8_t* codes, uint8_t* scales,
+                         void* stream) {
+  if (M < 0 || K < 0) return MXFP4_EINVAL;
+  if (K % 16 != 0 || ldx < K) return MXFP4_ESHAPE;
+  if (M == 0 || K == 0) return MXFP4_OK;
+  if (!x || !global_scale || !codes || !scales) return MXFP4_EINVAL;
+  if (!aligned16(x) || ldx % 8 != 0 || !aligned16(codes) || !aligned16(scales) ||
+      (reinterpret_cast<uintptr_t>(global_scale) & 3u))
+    return MXFP4_EALIGN;
+  const int64_t ctas = ceil_div(M, 128) * ceil_div(ceil_div(K / 16, 4), 2);
+  if (M > (INT64_MAX / 4) / ldx || ctas > kMaxGrid) return MXFP4_ESHAPE;
+  const Range rx = range_of(x, ((M - 1) * ldx + K) * 2);
+  const Range rg = range_of(global_scale, 4);
+  const Range rc = range_of(codes, M * (K / 2));
+  const Range rs = range_of(scales, static_cast<int64_t>(mxfp4_nvfp4_scale_bytes(M, K)));
+  if (overlap(rx, rc) || overlap(rx, rs) || overlap(rc, rs) || overlap(rg, rc) ||
+      overlap(rg, rs))
+    return MXFP4_EALIAS;
+  return from_cuda(mxfp4::launch_quantize_nvfp4(x, M, K, ldx, global_scale, codes, scales,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+int mxfp4_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, const float* global_scale,
+                           int64_t M, int64_t K, void* y, void* stream) {
+  if (M < 0 || K < 0) return MXFP4_EINVAL;
+  if (K % 16 != 0) return MXFP4_ESHAPE;
+  if (M == 0 || K == 0) return MXFP4_OK;
+  if (!codes || !scales || !global_scale || !y) return MXFP4_EINVAL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(y) ||
+      (reinterpret_cast<uintptr_t>(global_scale) & 3u))
+    return MXFP4_EALIGN;
+  const int64_t ctas = ceil_div(M, 128) * ceil_div(ceil_div(K / 16, 4), 2);
+  if (M > (INT64_MAX / 4) / K || ctas > kMaxGrid) return MXFP4_ESHAPE;
+  const Range ry = range_of(y, M * K * 2);
+  if (overlap(ry, range_of(codes, M * (K / 2))) ||
+      overlap(ry, range_of(scales, static_cast<int64_t>(mxfp4_nvfp4_scale_bytes(M, K)))) ||
+      overlap(ry, range_of(global_scale, 4)))
+    return MXFP4_EALIAS;
+  return from_cuda(mxfp4::launch_dequantize_nvfp4(codes, scales, global_scale, M, K, y,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
 const char* mxfp4_status_string(int status) {
   switch (status) {
     case MXFP4_OK: return "MXFP4_OK: success";

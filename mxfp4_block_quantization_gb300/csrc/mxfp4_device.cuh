@@ -202,6 +202,22 @@ __device__ __forceinline__ float half_hi_to_f32(uint32_t h2) {
   return f;
 }
 
+// ------------------------------------------------ FP8 E4M3 (NVFP4 scales)
+// float32 -> E4M3 byte, round to nearest even, saturating at +-448.
+__device__ __forceinline__ uint32_t cvt_e4m3_satfinite(float f) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(f));
+  return r & 0xFFu;
+}
+
+// E4M3 byte -> float32 (exact, through f16).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+  uint32_t h2;
+  const uint16_t v = static_cast<uint16_t>(byte);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  return half_lo_to_f32(h2);
+}
+
 // -------------------------------------------------------- memory access
 // Streaming 16-byte load of data read exactly once: read-only path, no L1
 // allocation.

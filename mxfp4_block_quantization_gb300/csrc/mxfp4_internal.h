@@ -32,6 +32,14 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
                                            int32_t* scale_row_offsets, int32_t* status,
                                            int64_t bound_tiles, cudaStream_t stream);
 
+// NVFP4 (16-element blocks, E4M3 scales, device global scale).
+cudaError_t launch_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                  const float* global_scale, uint8_t* codes, uint8_t* scales,
+                                  cudaStream_t stream);
+cudaError_t launch_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales,
+                                    const float* global_scale, int64_t M, int64_t K, void* y,
+                                    cudaStream_t stream);
+
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int64_t K,
                               void* y, cudaStream_t stream);
 

@@ -1,0 +1,227 @@
+// nvfp4.cu — NVFP4 variant: BF16 -> E2M1 codes with one FP8 E4M3 scale per
+// 16 elements (plus the caller's global scale), and its dequantize, sm_103a.
+//
+// Method: vLLM PR #43557 page ("Fix the E8M0 scale computation in the MXFP4
+// MoE CUTLASS kernel"), "Implementation breakdown" item 1 and the non-UE8M0
+// branch of the cvt_warp_fp16_to_fp4 excerpt: block scale =
+// SFScaleVal * vecMax / 6 stored as E4M3; "Review highlights": the elements
+// are scaled with the E4M3-rounded value (SFValue = float(E4M3 byte)), so
+// quantize and dequantize use the same scale.  Readings where the page is
+// silent: 16-element blocks, float32 steps each rounded to nearest even
+//   q = vecMax / 6; sf = g * q; byte = E4M3(sf); inv = g / float(byte);
+//   code = E2M1(x * inv), blocks with byte 0 -> zero codes;
+//   dequantize: BF16((e2m1 * float(byte)) * (1 / g)).
+// Scales use the same 128x4 tiled layout as MXFP4, on 16-element columns:
+// one 512-byte chunk per 128 rows x 64 elements.
+//
+// Work decomposition: one CTA (256 threads) per 128 rows x 128 columns = two
+// scale chunks; lane l of warp w covers one 16-element block of row
+// 4*w + l/8 in each of 4 passes of 32 rows, so the block max needs no shuffle.
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "mxfp4_device.cuh"
+#include "mxfp4_internal.h"
+
+namespace mxfp4 {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kNvBlock = 16;
+constexpr int kRowsPerPass = 32;
+constexpr int kPasses = kTileRows / kRowsPerPass;  // 4
+constexpr int kCtaCols = 128;                       // two 64-column scale chunks
+
+struct Nvfp4Params {
+  const uint8_t* __restrict__ x;      // BF16 bytes (quantize)
+  uint8_t* __restrict__ codes;
+  uint8_t* __restrict__ scales;
+  uint8_t* __restrict__ y;            // BF16 bytes (dequantize)
+  const float* __restrict__ g;        // device global scale
+  int64_t ldx_bytes;
+  int64_t M;
+  int64_t code_ld;                    // K/2
+  int64_t y_ld;                       // 2K
+  int32_t sK;                         // 16-element scale columns K/16
+  int32_t nKT;                        // chunks per m-tile ceil(sK/4)
+  int32_t nCT;                        // CTAs per m-tile ceil(nKT/2)
+};
+
+template <bool kVec32>
+__device__ __forceinline__ void load32(const uint8_t* src, uint4 (&v)[2]) {
+  if constexpr (kVec32) {
+    ld_stream_v8(src, v[0], v[1]);
+  } else {
+    v[0] = ld_stream_v4(src);
+    v[1] = ld_stream_v4(src + 16);
+  }
+}
+
+template <bool kVec32>
+__global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(const Nvfp4Params p) {
+  __shared__ __align__(16) uint8_t chunk[2][kChunkBytes];
+  pdl_wait();
+  pdl_release();
+  const int ct = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.nCT));
+  const int64_t mt = blockIdx.x / static_cast<uint32_t>(p.nCT);
+  const int64_t row0 = mt * kTileRows;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;                 // 16-element block inside the 128 columns
+  const int half = sub >> 2;                // which of the two chunks
+  const int cc = sub & 3;                   // scale column inside the chunk
+  const int lr0 = warp * 4 + (lane >> 3);   // row in pass 0 (0..31)
+  const int64_t avail = p.M - row0;
+  const int lim = static_cast<int>((avail < kTileRows ? avail : kTileRows) - lr0);
+  const bool col_ok = ct * 8 + sub < p.sK;
+  const uint8_t* xp = p.x + (row0 + lr0) * p.ldx_bytes + static_cast<int64_t>(ct) * (kCtaCols * 2) + sub * 32;
+  uint8_t* cp = p.codes + (row0 + lr0) * p.code_ld + static_cast<int64_t>(ct) * (kCtaCols / 2) + sub * 8;
+  const int64_t ldx_pass = p.ldx_bytes * kRowsPerPass;
+  const int64_t cld_pass = p.code_ld * kRowsPerPass;
+  const float g = __ldg(p.g);
+
+  uint4 v[kPasses][2];
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i) {
+    v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
+    if (col_ok && kRowsPerPass * i < lim) load32<kVec32>(xp + i * ldx_pass, v[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i) {
+    const uint32_t h =
+        max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(v[i][0].x, v[i][0].y),
+                                      max_abs_bf16x2(v[i][0].z, v[i][0].w)),
+                       max_abs_bf16x2(max_abs_bf16x2(v[i][1].x, v[i][1].y),
+                                      max_abs_bf16x2(v[i][1].z, v[i][1].w))) &
+        0x7FFF7FFFu;
+    const uint32_t m = max(h & 0xFFFFu, h >> 16);
+    const float vmax = __uint_as_float(m << 16);
+    const float q = vmax / 6.0f;           // IEEE float32 division (no fast-math)
+    const float sf = g * q;
+    const uint32_t byte = cvt_e4m3_satfinite(sf);
+    chunk[half][lr0 * 16 + i * 4 + cc] = static_cast<uint8_t>(byte);
+    uint2 code = make_uint2(0u, 0u);
+    if (byte != 0u) {
+      const float inv = g / e4m3_to_f32(byte);
+      code.x = scale_cvt_e2m1x8(v[i][0], inv);
+      code.y = scale_cvt_e2m1x8(v[i][1], inv);
+    }
+    if (col_ok && kRowsPerPass * i < lim) st_stream_v2(cp + i * cld_pass, code);
+  }
+  __syncthreads();
+  if (threadIdx.x < 2 * (kChunkBytes / 16)) {
+    const int j = threadIdx.x >> 5;
+    const int w = threadIdx.x & 31;
+    const int kt = ct * 2 + j;
+    if (kt < p.nKT) {
+      const uint4 val = reinterpret_cast<const uint4*>(chunk[j])[w];
+      st_stream_v4(p.scales + (mt * p.nKT + kt) * kChunkBytes + w * 16, val);
+    }
+  }
+}
+
+// 8 codes (element 2j in the low nibble of byte j) times float(E4M3 scale)
+// times 1/g -> 16 bytes of BF16.
+__device__ __forceinline__ uint4 decode8_nv(uint32_t c, float sfv, float inv_g) {
+  uint4 o;
+  uint32_t h;
+  h = cvt_e2m1x2_to_f16x2(c);
+  o.x = cvt_bf16x2((half_lo_to_f32(h) * sfv) * inv_g, (half_hi_to_f32(h) * sfv) * inv_g);
+  h = cvt_e2m1x2_to_f16x2(c >> 8);
+  o.y = cvt_bf16x2((half_lo_to_f32(h) * sfv) * inv_g, (half_hi_to_f32(h) * sfv) * inv_g);
+  h = cvt_e2m1x2_to_f16x2(c >> 16);
+  o.z = cvt_bf16x2((half_lo_to_f32(h) * sfv) * inv_g, (half_hi_to_f32(h) * sfv) * inv_g);
+  h = cvt_e2m1x2_to_f16x2(c >> 24);
+  o.w = cvt_bf16x2((half_lo_to_f32(h) * sfv) * inv_g, (half_hi_to_f32(h) * sfv) * inv_g);
+  return o;
+}
+
+template <bool kVec32>
+__global__ void __launch_bounds__(kThreads) nvfp4_dequantize_kernel(const Nvfp4Params p) {
+  pdl_wait();
+  pdl_release();
+  const int ct = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.nCT));
+  const int64_t mt = blockIdx.x / static_cast<uint32_t>(p.nCT);
+  const int64_t row0 = mt * kTileRows;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;
+  const int half = sub >> 2;
+  const int cc = sub & 3;
+  const int lr0 = warp * 4 + (lane >> 3);
+  const int64_t avail = p.M - row0;
+  const int lim = static_cast<int>((avail < kTileRows ? avail : kTileRows) - lr0);
+  const bool col_ok = ct * 8 + sub < p.sK;
+  const uint8_t* cp = p.codes + (row0 + lr0) * p.code_ld + static_cast<int64_t>(ct) * (kCtaCols / 2) + sub * 8;
+  uint8_t* yp = p.y + (row0 + lr0) * p.y_ld + static_cast<int64_t>(ct) * (kCtaCols * 2) + sub * 32;
+  const int64_t cld_pass = p.code_ld * kRowsPerPass;
+  const int64_t yld_pass = p.y_ld * kRowsPerPass;
+  const float inv_g = 1.0f / __ldg(p.g);    // IEEE float32 division
+
+  uint2 c[kPasses];
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i)
+    c[i] = (col_ok && kRowsPerPass * i < lim) ? ld_stream_v2(cp + i * cld_pass) : make_uint2(0u, 0u);
+  uint4 sr = make_uint4(0u, 0u, 0u, 0u);
+  if (col_ok) sr = ld_stream_v4(p.scales + (mt * p.nKT + ct * 2 + half) * kChunkBytes + lr0 * 16);
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i) {
+    const uint32_t word = i == 0 ? sr.x : i == 1 ? sr.y : i == 2 ? sr.z : sr.w;
+    const float sfv = e4m3_to_f32((word >> (8 * cc)) & 0xFFu);
+    const uint4 o0 = decode8_nv(c[i].x, sfv, inv_g);
+    const uint4 o1 = decode8_nv(c[i].y, sfv, inv_g);
+    if (col_ok && kRowsPerPass * i < lim) {
+      if constexpr (kVec32) {
+        st_stream_v8(yp + i * yld_pass, o0, o1);
+      } else {
+        st_stream_v4(yp + i * yld_pass, o0);
+        st_stream_v4(yp + i * yld_pass + 16, o1);
+      }
+    }
+  }
+}
+
+Nvfp4Params make_params(int64_t M, int64_t K) {
+  Nvfp4Params p{};
+  p.M = M;
+  p.code_ld = K / 2;
+  p.y_ld = K * 2;
+  p.sK = static_cast<int32_t>(K / kNvBlock);
+  p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
+  p.nCT = (p.nKT + 1) / 2;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                  const float* global_scale, uint8_t* codes, uint8_t* scales,
+                                  cudaStream_t stream) {
+  Nvfp4Params p = make_params(M, K);
+  p.x = static_cast<const uint8_t*>(x);
+  p.ldx_bytes = ldx * 2;
+  p.codes = codes;
+  p.scales = scales;
+  p.g = global_scale;
+  const int64_t grid = (M + kTileRows - 1) / kTileRows * p.nCT;
+  const bool v32 = reinterpret_cast<uintptr_t>(x) % 32 == 0 && p.ldx_bytes % 32 == 0;
+  return launch_pdl(v32 ? nvfp4_quantize_kernel<true> : nvfp4_quantize_kernel<false>,
+                    static_cast<unsigned>(grid), kThreads, 0, stream, p);
+}
+
+cudaError_t launch_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales,
+                                    const float* global_scale, int64_t M, int64_t K, void* y,
+                                    cudaStream_t stream) {
+  Nvfp4Params p = make_params(M, K);
+  p.codes = const_cast<uint8_t*>(codes);
+  p.scales = const_cast<uint8_t*>(scales);
+  p.y = static_cast<uint8_t*>(y);
+  p.g = global_scale;
+  const int64_t grid = (M + kTileRows - 1) / kTileRows * p.nCT;
+  const bool v32 = reinterpret_cast<uintptr_t>(y) % 32 == 0;  // rows are 2K = 32*(K/16) bytes
+  return launch_pdl(v32 ? nvfp4_dequantize_kernel<true> : nvfp4_dequantize_kernel<false>,
+                    static_cast<unsigned>(grid), kThreads, 0, stream, p);
+}
+
+}  // namespace mxfp4

@@ -155,3 +155,19 @@ def test_quantize_f16_validation(lib):
     assert f(A + 8, 4, 64, 64, 2 * A, 3 * A, None) == lib.MXFP4_EALIGN
     assert f(A, 4, 64, 64, A + 64, 3 * A, None) == lib.MXFP4_EALIAS
     assert f(None, 0, 64, 64, None, None, None) == lib.MXFP4_OK
+
+
+def test_nvfp4_validation(lib):
+    q = lib._lib.mxfp4_quantize_nvfp4
+    d = lib._lib.mxfp4_dequantize_nvfp4
+    assert lib.mxfp4_nvfp4_scale_bytes(1000, 2880) == 1024 * 180
+    assert lib.mxfp4_nvfp4_scale_bytes(4, 24) == 0
+    assert q(A, 4, 24, 24, 9 * A, 2 * A, 3 * A, None) == lib.MXFP4_ESHAPE
+    assert q(A, 4, 64, 64, None, 2 * A, 3 * A, None) == lib.MXFP4_EINVAL
+    assert q(A, 4, 64, 64, 9 * A + 2, 2 * A, 3 * A, None) == lib.MXFP4_EALIGN
+    assert q(A, 4, 64, 64, 9 * A, A + 64, 3 * A, None) == lib.MXFP4_EALIAS
+    assert q(A, 4, 64, 64, 3 * A + 4, 2 * A, 3 * A, None) == lib.MXFP4_EALIAS
+    assert q(None, 0, 64, 64, None, None, None, None) == lib.MXFP4_OK
+    assert d(A, 2 * A, 9 * A, 4, 24, 3 * A, None) == lib.MXFP4_ESHAPE
+    assert d(A, 2 * A, None, 4, 64, 3 * A, None) == lib.MXFP4_EINVAL
+    assert d(A, 2 * A, 9 * A, 4, 64, A + 32, None) == lib.MXFP4_EALIAS

@@ -499,3 +499,80 @@ def test_f16_element_map_exhaustive(mx):
     c_o, s_o = oracle.quantize_f16(hb)
     assert np.array_equal(s, s_o), _first_diff(s, s_o)
     assert np.array_equal(c, c_o), _first_diff(c, c_o)
+
+
+# ------------------------------------------------------------------ NVFP4
+def run_nvfp4(mx, x, g):
+    M, K = x.shape
+    gs = torch.tensor([g], dtype=torch.float32, device="cuda")
+    codes = Guarded(M * (K // 2), shape=(M, K // 2))
+    scales = Guarded(mx.mxfp4_nvfp4_scale_bytes(M, K))
+    mx.mxfp4_quantize_nvfp4(x, gs, codes.t, scales.t)
+    torch.cuda.synchronize()
+    codes.check()
+    scales.check()
+    c, s = codes.t.cpu().numpy(), scales.t.cpu().numpy()
+    y = Guarded(M * K * 2, torch.bfloat16, (M, K))
+    mx.mxfp4_dequantize_nvfp4(torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda(), gs, M, K, y.t)
+    torch.cuda.synchronize()
+    y.check()
+    return c, s, bits(y.t)
+
+
+def assert_nvfp4_parity(mx, x, g):
+    xb = bits(x)
+    M, K = xb.shape
+    c, s, y = run_nvfp4(mx, x, g)
+    g32 = float(np.float32(g))
+    c_o, s_o = oracle.nvfp4_quantize(xb, g32)
+    assert np.array_equal(s, s_o), _first_diff(s, s_o)
+    assert np.array_equal(c, c_o), _first_diff(c, c_o)
+    y_o = oracle.nvfp4_dequantize(c_o, s_o, M, K, g32)
+    assert np.array_equal(y, y_o), _first_diff(y, y_o)
+
+
+@pytest.mark.parametrize("g", [1.0, 0.37, 2688.0 / 25.0])
+def test_nvfp4_dense(mx, g):
+    x = W.dense_activation(31, 1000, 2880, device="cuda")
+    assert_nvfp4_parity(mx, x, g)
+
+
+def test_nvfp4_full_size(mx):
+    x = W.dense_activation(1, device="cuda")
+    amax = float(x.float().abs().max())
+    assert_nvfp4_parity(mx, x, 448.0 * 6.0 / amax)
+
+
+@pytest.mark.parametrize("M", [1, 127, 129])
+@pytest.mark.parametrize("K", [16, 48, 64, 80, 2880])
+def test_nvfp4_ragged(mx, M, K):
+    x = W.normal_bf16((M, K), seed=M * 7 + K, device="cuda")
+    assert_nvfp4_parity(mx, x, 1.0)
+
+
+def test_nvfp4_edge_cases_and_16b_aligned(mx):
+    x = W.edge_cases(4).cuda()
+    assert_nvfp4_parity(mx, x, 1.0)
+    flat = torch.empty(x.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    y = flat[8:].view(x.shape)
+    y.copy_(x)
+    assert_nvfp4_parity(mx, y, 3.0)
+
+
+def test_nvfp4_scale_sweep_every_bf16_max(mx):
+    """Each 16-element block takes a different block max: every positive finite
+    BF16 value (so g*vecMax/6 sweeps zero, subnormal, normal and saturated
+    E4M3 scales), plus blocks whose scale lands exactly on an E4M3 midpoint."""
+    rng = np.random.default_rng(9)
+    vmax = np.arange(1, 0x7F80, dtype=np.uint16)
+    grid = np.unique(np.abs([oracle.e4m3_to_double(i) for i in range(0x7F)]))
+    mids = ((grid[:-1] + grid[1:]) / 2 * 6).astype(np.float32)
+    mid_bits = (mids.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((mid_bits.astype(np.uint32) << 16).view(np.float32), mids)
+    vmax = np.concatenate([vmax, mid_bits])
+    rest = (rng.integers(0, 0x10000, (vmax.size, 15), dtype=np.uint32)).astype(np.uint16)
+    rest = np.where((rest & 0x7FFF) <= vmax[:, None], rest, rest & 0x8000 | (vmax[:, None] >> 1))
+    blocks = np.concatenate([vmax[:, None], rest], axis=1)
+    blocks = np.concatenate([blocks, np.zeros(((-blocks.shape[0]) % 16, 16), np.uint16)])
+    xb = blocks.reshape(-1, 256)
+    assert_nvfp4_parity(mx, W.from_bits(xb, "cuda"), 1.0)
