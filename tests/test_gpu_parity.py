@@ -576,3 +576,67 @@ def test_nvfp4_scale_sweep_every_bf16_max(mx):
     blocks = np.concatenate([blocks, np.zeros(((-blocks.shape[0]) % 16, 16), np.uint16)])
     xb = blocks.reshape(-1, 256)
     assert_nvfp4_parity(mx, W.from_bits(xb, "cuda"), 1.0)
+
+
+# ------------------------------------------------ streams, graphs, 64-bit
+def test_non_default_stream(mx):
+    x = W.dense_activation(41, 512, 1024, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        codes, scales = mx.quantize(x)
+        y = mx.dequantize(codes, scales, 512, 1024)
+    s.synchronize()
+    c_o, s_o = oracle.quantize(bits(x))
+    assert np.array_equal(codes.cpu().numpy(), c_o) and np.array_equal(scales.cpu().numpy(), s_o)
+    assert np.array_equal(bits(y), oracle.dequantize(c_o, s_o, 512, 1024))
+
+
+def test_cuda_graph_capture_and_replay(mx):
+    """The launches (programmatic dependent launch included) can be captured
+    in a CUDA graph and replayed on new input contents."""
+    M, K = 512, 2048
+    x = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    codes = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(mx.mxfp4_scale_bytes(M, K), dtype=torch.uint8, device="cuda")
+    y = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    x.copy_(W.dense_activation(42, M, K, device="cuda"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):                       # warm-up outside the capture
+        mx.mxfp4_quantize(x, codes, scales)
+        mx.mxfp4_dequantize(codes, scales, M, K, y)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mx.mxfp4_quantize(x, codes, scales)
+        mx.mxfp4_dequantize(codes, scales, M, K, y)
+    for seed in (43, 44):
+        x.copy_(W.dense_activation(seed, M, K, device="cuda"))
+        g.replay()
+        torch.cuda.synchronize()
+        c_o, s_o = oracle.quantize(bits(x))
+        assert np.array_equal(codes.cpu().numpy(), c_o)
+        assert np.array_equal(scales.cpu().numpy(), s_o)
+        assert np.array_equal(bits(y), oracle.dequantize(c_o, s_o, M, K))
+
+
+def test_more_than_4gib_input(mx):
+    """33000 x 65536 BF16 (4.3 GB): byte offsets beyond 2^32; the first and
+    last 128-row tiles (and one in the middle) checked against the oracle."""
+    M, K = 33000, 65536
+    x = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    for r0 in range(0, M, 4096):
+        r1 = min(M, r0 + 4096)
+        x[r0:r1] = W.normal_bf16((r1 - r0, K), seed=r0 + 1, device="cuda")
+    codes, scales = mx.quantize(x)
+    torch.cuda.synchronize()
+    per_tile = mx.mxfp4_scale_bytes(128, K)
+    for t in (0, 128, (M - 1) // 128):
+        r0 = t * 128
+        r1 = min(M, r0 + 128)
+        c_o, s_o = oracle.quantize(bits(x[r0:r1]))
+        assert np.array_equal(codes[r0:r1].cpu().numpy(), c_o), t
+        assert np.array_equal(scales[t * per_tile:(t + 1) * per_tile].cpu().numpy(), s_o), t
+    del x, codes, scales
+    torch.cuda.empty_cache()
