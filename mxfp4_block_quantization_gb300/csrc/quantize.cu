@@ -54,10 +54,19 @@ struct QuantizeParams {
 
 // Segment holding padded row `prow`: the last e in [0, E) with P[e] <= prow
 // (empty segments share their start with the next one, so the last such e
-// is never empty when prow < P[E]).  P is small and read by every CTA, so
-// the probes hit L1/L2.
-__device__ __forceinline__ int find_segment(const int32_t* __restrict__ P, int E, int prow) {
-  int lo = 0, hi = E - 1;
+// is never empty when prow < P[E]).  A proportional estimate is checked
+// first with two independent probes (exact whenever the segments are close to
+// uniform, as with balanced MoE routing); otherwise a binary search over the
+// side the estimate excluded.  P is small and read by every CTA (L1/L2 hits).
+__device__ __forceinline__ int find_segment(const int32_t* __restrict__ P, int E, int prow,
+                                            int total) {
+  int e = static_cast<int>(static_cast<int64_t>(prow) * E / total);
+  e = e < E - 1 ? e : E - 1;
+  const int pe = __ldg(P + e);
+  const int pn = __ldg(P + e + 1);
+  if (pe <= prow && prow < pn) return e;
+  int lo, hi;
+  if (pe <= prow) { lo = e + 1; hi = E - 1; } else { lo = 0; hi = e - 1; }
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (__ldg(P + mid) <= prow) lo = mid; else hi = mid - 1;
@@ -113,7 +122,7 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
     const int total_padded = __ldg(p.padded + p.E);
     const int prow = mt * kTileRows;
     if (total_padded < 0 || prow >= total_padded) return;  // rejected offsets / past the end
-    const int e = find_segment(p.padded, p.E, prow);
+    const int e = find_segment(p.padded, p.E, prow, total_padded);
     row0 = static_cast<int64_t>(__ldg(p.offsets + e)) + (prow - __ldg(p.padded + e));
     row_end = __ldg(p.offsets + e + 1);
   } else {
