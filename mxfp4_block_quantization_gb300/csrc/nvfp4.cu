@@ -32,7 +32,6 @@ constexpr int kNvBlock = 16;
 constexpr int kRowsPerPass = 32;
 constexpr int kPasses = kTileRows / kRowsPerPass;  // 4
 constexpr int kCtaCols = 128;                       // two 64-column scale chunks
-static_assert(kThreads == 256, "one E4M3 byte value per thread for the quotient table");
 
 struct Nvfp4Params {
   const uint8_t* __restrict__ x;      // BF16 bytes (quantize)
@@ -62,13 +61,8 @@ __device__ __forceinline__ void load32(const uint8_t* src, uint4 (&v)[2]) {
 template <bool kVec32>
 __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(const Nvfp4Params p) {
   __shared__ __align__(16) uint8_t chunk[2][kChunkBytes];
-  __shared__ float inv_of_byte[256];  // g / float(E4M3 byte), one IEEE division per thread
   pdl_wait();
   pdl_release();
-  {
-    const float gg = __ldg(p.g);
-    inv_of_byte[threadIdx.x] = gg / e4m3_to_f32(threadIdx.x);
-  }
   const int ct = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.nCT));
   const int64_t mt = blockIdx.x / static_cast<uint32_t>(p.nCT);
   const int64_t row0 = mt * kTileRows;
@@ -107,10 +101,9 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(const Nvfp4Par
     const float sf = g * q;
     const uint32_t byte = cvt_e4m3_satfinite(sf);
     chunk[half][lr0 * 16 + i * 4 + cc] = static_cast<uint8_t>(byte);
-    if (i == 0) __syncthreads();  // inv_of_byte ready (its writes overlap the loads)
     uint2 code = make_uint2(0u, 0u);
     if (byte != 0u) {
-      const float inv = inv_of_byte[byte];
+      const float inv = g / e4m3_to_f32(byte);
       code.x = scale_cvt_e2m1x8(v[i][0], inv);
       code.y = scale_cvt_e2m1x8(v[i][1], inv);
     }
