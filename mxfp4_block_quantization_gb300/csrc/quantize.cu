@@ -27,11 +27,15 @@
 namespace mxfp4 {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;                               // dense and grouped CTAs
+constexpr int kGatherThreads = 128;                         // gather CTAs: 8 passes per thread
 constexpr int kElems = 16;                                  // elements per lane per pass
 constexpr int kLanesPerRow = kTileCols / kElems;            // 8 lanes cover 128 columns
-constexpr int kRowsPerPass = (kThreads / 32) * (32 / kLanesPerRow);  // 32 rows
-constexpr int kPasses = kTileRows / kRowsPerPass;           // 4 passes
+
+// Rows covered by one pass of a CTA of `threads` threads (4 rows per warp),
+// and passes per 128-row tile.
+__host__ __device__ constexpr int rows_per_pass(int threads) { return (threads / 32) * (32 / kLanesPerRow); }
+__host__ __device__ constexpr int passes(int threads) { return kTileRows / rows_per_pass(threads); }
 
 struct QuantizeParams {
   const uint8_t* __restrict__ x;  // BF16 bytes
@@ -96,8 +100,11 @@ __device__ __forceinline__ void load32(const uint8_t* src, uint4 (&v)[2]) {
 //
 // kF16: the input is IEEE binary16 instead of BF16 (same method: the block
 // max is widened to float32 exactly and the E8M0 rule is applied to its bits).
-template <bool kGrouped, bool kGather, bool kVec32, bool kF16 = false>
-__global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const QuantizeParams p) {
+template <bool kGrouped, bool kGather, bool kVec32, bool kF16 = false,
+          int kT = kGather ? kGatherThreads : kThreads>
+__global__ void __launch_bounds__(kT) quantize_tiles_kernel(const QuantizeParams p) {
+  constexpr int kRowsPerPass = rows_per_pass(kT);
+  constexpr int kPasses = passes(kT);
   static_assert(kGrouped || !kGather, "gather is a grouped mode");
   __shared__ __align__(16) uint8_t chunk[kChunkBytes];
 
@@ -134,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
   const int lane = threadIdx.x & 31;
   const int sub = lane & (kLanesPerRow - 1);  // 16-element segment inside the 128 columns
   const int blk = sub >> 1;                   // scale column inside the tile (0..3)
-  const int lr0 = warp * (32 / kLanesPerRow) + (lane >> 3);  // row in pass 0 (0..31)
+  const int lr0 = warp * (32 / kLanesPerRow) + (lane >> 3);  // row in pass 0
   const int64_t avail = row_end - row0;
   const int lim = static_cast<int>((avail < kTileRows ? avail : kTileRows) - lr0);
   const bool col_ok = kt * kTileBlocks + blk < p.sK;
@@ -213,6 +220,7 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
   }
 
   __syncthreads();
+  static_assert(kT >= kChunkBytes / 16, "one 16-byte chunk store per thread");
   if (threadIdx.x < kChunkBytes / 16) {
     const uint4 w = reinterpret_cast<const uint4*>(chunk)[threadIdx.x];
     // chunk index = m-tile * nKT + k-tile (= unit in m-tile-major order)
@@ -362,7 +370,7 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
   const int64_t grid = bound_tiles * p.nKT;
   const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<true, true, true>
                                                : quantize_tiles_kernel<true, true, false>;
-  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
+  return launch_pdl(kernel, static_cast<unsigned>(grid), kGatherThreads, 0, stream, p);
 }
 
 }  // namespace mxfp4
