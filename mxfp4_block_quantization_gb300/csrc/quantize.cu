@@ -89,6 +89,45 @@ __device__ __forceinline__ void load32(const uint8_t* src, uint4 (&v)[2]) {
   }
 }
 
+// One lane's share of one pass: its 16 elements (two lanes per 32-element
+// block) -> the block's E8M0 scale exponent.  |x| per half with
+// max.xorsign.abs, sign bits cleared, then the larger half (the unsigned order
+// of non-negative BF16/FP16 patterns is the order of their magnitudes), then
+// the partner lane's half block.
+template <bool kF16>
+__device__ __forceinline__ uint32_t lane_block_scale(const uint4 (&v)[2]) {
+  uint32_t h;
+  if constexpr (kF16) {
+    h = max_abs_f16x2(max_abs_f16x2(max_abs_f16x2(v[0].x, v[0].y), max_abs_f16x2(v[0].z, v[0].w)),
+                      max_abs_f16x2(max_abs_f16x2(v[1].x, v[1].y), max_abs_f16x2(v[1].z, v[1].w)));
+  } else {
+    h = max_abs_bf16x2(
+        max_abs_bf16x2(max_abs_bf16x2(v[0].x, v[0].y), max_abs_bf16x2(v[0].z, v[0].w)),
+        max_abs_bf16x2(max_abs_bf16x2(v[1].x, v[1].y), max_abs_bf16x2(v[1].z, v[1].w)));
+  }
+  h &= 0x7FFF7FFFu;
+  uint32_t m = max(h & 0xFFFFu, h >> 16);
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  return kF16 ? e8m0_from_absmax_f32bits(f16_bits_to_f32_bits(m)) : e8m0_from_absmax_bf16(m);
+}
+
+// The lane's 16 codes (8 bytes): x * 2^(127-s) rounded to E2M1; s == 0 gives
+// zero codes.
+template <bool kF16>
+__device__ __forceinline__ uint2 lane_codes(const uint4 (&v)[2], uint32_t s) {
+  const float inv = inv_scale_from_e8m0(s);
+  uint2 code;
+  if constexpr (kF16) {
+    code.x = scale_cvt_e2m1x8_f16(v[0], inv);
+    code.y = scale_cvt_e2m1x8_f16(v[1], inv);
+  } else {
+    code.x = scale_cvt_e2m1x8(v[0], inv);
+    code.y = scale_cvt_e2m1x8(v[1], inv);
+  }
+  if (s == 0u) code = make_uint2(0u, 0u);
+  return code;
+}
+
 // Lane l of warp w covers elements [16*(l%8), 16*(l%8)+16) of row
 // 4*w + l/8 (+32 per pass): two lanes per 32-element block.  kGather (grouped
 // only): output row r reads source row row_index[r]; the four row indices of
@@ -182,40 +221,10 @@ __global__ void __launch_bounds__(kT) quantize_tiles_kernel(const QuantizeParams
 
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
-    // block absmax: |x| per half with max.xorsign.abs, sign bits cleared,
-    // then the larger half (unsigned order of non-negative BF16 patterns is
-    // the order of their magnitudes), then the partner lane's half block
-    uint32_t h;
-    if constexpr (kF16) {
-      h = max_abs_f16x2(max_abs_f16x2(max_abs_f16x2(v[i][0].x, v[i][0].y),
-                                      max_abs_f16x2(v[i][0].z, v[i][0].w)),
-                        max_abs_f16x2(max_abs_f16x2(v[i][1].x, v[i][1].y),
-                                      max_abs_f16x2(v[i][1].z, v[i][1].w)));
-    } else {
-      h = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(v[i][0].x, v[i][0].y),
-                                        max_abs_bf16x2(v[i][0].z, v[i][0].w)),
-                         max_abs_bf16x2(max_abs_bf16x2(v[i][1].x, v[i][1].y),
-                                        max_abs_bf16x2(v[i][1].z, v[i][1].w)));
-    }
-    h &= 0x7FFF7FFFu;
-    uint32_t m = max(h & 0xFFFFu, h >> 16);
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    const uint32_t s =
-        kF16 ? e8m0_from_absmax_f32bits(f16_bits_to_f32_bits(m)) : e8m0_from_absmax_bf16(m);
-    // rows of pass i sit in chunk row lr0 (outerM), word i (innerM)
+    const uint32_t s = lane_block_scale<kF16>(v[i]);
+    // rows of pass i sit in chunk row lr0 % 32 (outerM), word (lr0 + rows*i) / 32 (innerM)
     if ((lane & 1) == 0) chunk[chunk_offset(lr0 + kRowsPerPass * i, blk)] = static_cast<uint8_t>(s);
-
-    // x * 2^(127-s), then round to E2M1; blocks with s == 0 emit zeros
-    const float inv = inv_scale_from_e8m0(s);
-    uint2 code;
-    if constexpr (kF16) {
-      code.x = scale_cvt_e2m1x8_f16(v[i][0], inv);
-      code.y = scale_cvt_e2m1x8_f16(v[i][1], inv);
-    } else {
-      code.x = scale_cvt_e2m1x8(v[i][0], inv);
-      code.y = scale_cvt_e2m1x8(v[i][1], inv);
-    }
-    if (s == 0u) code = make_uint2(0u, 0u);
+    const uint2 code = lane_codes<kF16>(v[i], s);
     if (col_ok && kRowsPerPass * i < lim) st_stream_v2(cp + i * cld_pass, code);
   }
 
@@ -226,6 +235,90 @@ __global__ void __launch_bounds__(kT) quantize_tiles_kernel(const QuantizeParams
     // chunk index = m-tile * nKT + k-tile (= unit in m-tile-major order)
     const int64_t c = kGather ? static_cast<int64_t>(mt) * p.nKT + kt : unit;
     st_stream_v4(p.scales + c * kChunkBytes + threadIdx.x * 16, w);
+  }
+}
+
+// Fused dispatch gather, chunked over K: one CTA (128 threads, 8 passes of 16
+// rows) owns one padded 128-row tile and a chunk of kGatherChunkTiles k-tiles
+// (1024 columns).  The tile's segment and its 128 source-row indices are
+// fetched once; the CTA then walks its k-tiles, each a full 128x128 tile with
+// its own 512-byte scale chunk (double-buffered in shared memory, one barrier
+// per k-tile).  CTAs are ordered chunk-major, so the resident CTAs read the
+// same 1024-column slice of the source rows (32 MB for 16384 rows of 7168),
+// which the L2 keeps while the other routes of each row come by.
+constexpr int kGatherChunkTiles = 8;
+
+template <bool kVec32>
+__global__ void __launch_bounds__(kGatherThreads) quantize_gather_kernel(const QuantizeParams p) {
+  constexpr int kRowsPerPass = rows_per_pass(kGatherThreads);
+  constexpr int kPasses = passes(kGatherThreads);
+  __shared__ __align__(16) uint8_t chunk[2][kChunkBytes];
+
+  pdl_wait();
+  pdl_release();
+
+  const int unit = blockIdx.x;
+  const int kc = unit / p.n_mtiles;
+  const int mt = unit - kc * p.n_mtiles;
+  const int total_padded = __ldg(p.padded + p.E);
+  const int prow = mt * kTileRows;
+  if (total_padded < 0 || prow >= total_padded) return;  // rejected offsets / past the end
+  const int e = find_segment(p.padded, p.E, prow, total_padded);
+  const int64_t row0 = static_cast<int64_t>(__ldg(p.offsets + e)) + (prow - __ldg(p.padded + e));
+  const int64_t row_end = __ldg(p.offsets + e + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & (kLanesPerRow - 1);
+  const int blk = sub >> 1;
+  const int lr0 = warp * (32 / kLanesPerRow) + (lane >> 3);
+  const int64_t avail = row_end - row0;
+  const int lim = static_cast<int>((avail < kTileRows ? avail : kTileRows) - lr0);
+  const int64_t r = row0 + lr0;
+
+  // source rows of this thread's eight output rows; an index outside
+  // [0, num_src_rows) reads nothing, quantizes as a zero row and is reported
+  int64_t src[kPasses];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i) {
+    src[i] = (kRowsPerPass * i < lim) ? __ldg(p.row_index + r + kRowsPerPass * i) : 0;
+    const bool in_range = src[i] >= 0 && src[i] < p.num_src_rows;
+    if (kRowsPerPass * i < lim) bad |= !in_range;
+    src[i] = (kRowsPerPass * i < lim && in_range) ? src[i] : -1;
+  }
+  if (bad && p.status != nullptr) atomicExch(p.status, MXFP4_EINDEX);
+
+  const int kt0 = kc * kGatherChunkTiles;
+  const int kt_end = kt0 + kGatherChunkTiles < p.nKT ? kt0 + kGatherChunkTiles : p.nKT;
+  const int64_t cld_pass = p.code_ld * kRowsPerPass;
+  int buf = 0;
+  for (int kt = kt0; kt < kt_end; ++kt) {
+    const bool col_ok = kt * kTileBlocks + blk < p.sK;
+    const uint8_t* xcol = p.x + static_cast<int64_t>(kt) * (kTileCols * 2) + sub * (kElems * 2);
+    uint4 v[kPasses][2];
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
+      if (col_ok && src[i] >= 0) load32<kVec32>(xcol + src[i] * p.ldx_bytes, v[i]);
+    }
+    uint8_t* cp = p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) +
+                  sub * (kElems / 2);
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      const uint32_t s = lane_block_scale<false>(v[i]);
+      if ((lane & 1) == 0)
+        chunk[buf][chunk_offset(lr0 + kRowsPerPass * i, blk)] = static_cast<uint8_t>(s);
+      const uint2 code = lane_codes<false>(v[i], s);
+      if (col_ok && kRowsPerPass * i < lim) st_stream_v2(cp + i * cld_pass, code);
+    }
+    __syncthreads();
+    if (threadIdx.x < kChunkBytes / 16) {
+      const uint4 w = reinterpret_cast<const uint4*>(chunk[buf])[threadIdx.x];
+      const int64_t c = static_cast<int64_t>(mt) * p.nKT + kt;
+      st_stream_v4(p.scales + c * kChunkBytes + threadIdx.x * 16, w);
+    }
+    buf ^= 1;
   }
 }
 
@@ -287,6 +380,8 @@ grouped_offsets_kernel(const int32_t* __restrict__ off, int32_t E, int64_t total
   }
   if (tid == 0 && status != nullptr) *status = s_bad ? MXFP4_EOFFSETS : MXFP4_OK;
 }
+
+constexpr bool kGatherChunked = true;
 
 // 256-bit loads need every lane address 32-byte aligned: the base and the
 // row stride (the column offsets are multiples of 32 bytes).
@@ -367,6 +462,12 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
   p.num_src_rows = num_src_rows;
   p.status = status;
   p.n_mtiles = static_cast<int32_t>(bound_tiles);
+  if (kGatherChunked) {
+    const int64_t grid = bound_tiles * ((p.nKT + kGatherChunkTiles - 1) / kGatherChunkTiles);
+    const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_gather_kernel<true>
+                                                 : quantize_gather_kernel<false>;
+    return launch_pdl(kernel, static_cast<unsigned>(grid), kGatherThreads, 0, stream, p);
+  }
   const int64_t grid = bound_tiles * p.nKT;
   const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<true, true, true>
                                                : quantize_tiles_kernel<true, true, false>;
