@@ -53,7 +53,7 @@ struct QuantizeParams {
   const int32_t* __restrict__ row_index;  // gather: source row of every output row
   int64_t num_src_rows;                   // gather: rows of x
   int32_t* status;                        // gather: device status word (may be NULL)
-  int32_t n_mtiles;                       // gather: m-tiles of the grid (k-tile-major order)
+  int32_t n_mtiles;                       // gather: m-tiles of the grid (chunk-major order)
 };
 
 // Segment holding padded row `prow`: the last e in [0, E) with P[e] <= prow
@@ -129,9 +129,7 @@ __device__ __forceinline__ uint2 lane_codes(const uint4 (&v)[2], uint32_t s) {
 }
 
 // Lane l of warp w covers elements [16*(l%8), 16*(l%8)+16) of row
-// 4*w + l/8 (+32 per pass): two lanes per 32-element block.  kGather (grouped
-// only): output row r reads source row row_index[r]; the four row indices of
-// a thread are fetched first, then its eight data loads.
+// 4*w + l/8 (+32 per pass): two lanes per 32-element block.
 //
 // kVec32: every lane's 32 bytes are 32-byte aligned (x and the row stride
 // are), so they arrive in one 256-bit load per pass; otherwise two 16-byte
@@ -139,30 +137,20 @@ __device__ __forceinline__ uint2 lane_codes(const uint4 (&v)[2], uint32_t s) {
 //
 // kF16: the input is IEEE binary16 instead of BF16 (same method: the block
 // max is widened to float32 exactly and the E8M0 rule is applied to its bits).
-template <bool kGrouped, bool kGather, bool kVec32, bool kF16 = false,
-          int kT = kGather ? kGatherThreads : kThreads>
-__global__ void __launch_bounds__(kT) quantize_tiles_kernel(const QuantizeParams p) {
-  constexpr int kRowsPerPass = rows_per_pass(kT);
-  constexpr int kPasses = passes(kT);
-  static_assert(kGrouped || !kGather, "gather is a grouped mode");
+template <bool kGrouped, bool kVec32, bool kF16 = false>
+__global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const QuantizeParams p) {
+  constexpr int kRowsPerPass = rows_per_pass(kThreads);
+  constexpr int kPasses = passes(kThreads);
   __shared__ __align__(16) uint8_t chunk[kChunkBytes];
 
   pdl_wait();
   pdl_release();
 
-  // Tile order: m-tile-major (consecutive CTAs read adjacent column slices of
-  // the same rows) or, for the gather, k-tile-major: all resident CTAs then
-  // read the same 256-byte column slice of the source rows, a working set the
-  // L2 keeps while the other routes of each row come by.
+  // Tile order: m-tile-major, so consecutive CTAs read adjacent column slices
+  // of the same rows.
   const int unit = blockIdx.x;
-  int mt, kt;
-  if constexpr (kGather) {
-    kt = unit / p.n_mtiles;
-    mt = unit - kt * p.n_mtiles;
-  } else {
-    mt = unit / p.nKT;
-    kt = unit - mt * p.nKT;
-  }
+  const int mt = unit / p.nKT;
+  const int kt = unit - mt * p.nKT;
   int64_t row0, row_end;
   if constexpr (kGrouped) {
     const int total_padded = __ldg(p.padded + p.E);
@@ -186,37 +174,17 @@ __global__ void __launch_bounds__(kT) quantize_tiles_kernel(const QuantizeParams
   const bool col_ok = kt * kTileBlocks + blk < p.sK;
   const int64_t r = row0 + lr0;
   const uint8_t* xp =
-      kGather ? p.x
-              : p.x + r * p.ldx_bytes + static_cast<int64_t>(kt) * (kTileCols * 2) + sub * (kElems * 2);
+      p.x + r * p.ldx_bytes + static_cast<int64_t>(kt) * (kTileCols * 2) + sub * (kElems * 2);
   uint8_t* cp =
       p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) + sub * (kElems / 2);
   const int64_t ldx_pass = p.ldx_bytes * kRowsPerPass;
   const int64_t cld_pass = p.code_ld * kRowsPerPass;
 
   uint4 v[kPasses][2];
-  if constexpr (kGather) {
-    // source rows of this thread's four output rows; an index outside
-    // [0, num_src_rows) reads nothing, quantizes as a zero row and is reported
-    int64_t src[kPasses];
 #pragma unroll
-    for (int i = 0; i < kPasses; ++i)
-      src[i] = (kRowsPerPass * i < lim) ? __ldg(p.row_index + r + kRowsPerPass * i) : 0;
-    const uint8_t* xcol = p.x + static_cast<int64_t>(kt) * (kTileCols * 2) + sub * (kElems * 2);
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < kPasses; ++i) {
-      v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
-      const bool in_range = src[i] >= 0 && src[i] < p.num_src_rows;
-      if (kRowsPerPass * i < lim) bad |= !in_range;
-      if (col_ok && kRowsPerPass * i < lim && in_range) load32<kVec32>(xcol + src[i] * p.ldx_bytes, v[i]);
-    }
-    if (bad && p.status != nullptr) atomicExch(p.status, MXFP4_EINDEX);
-  } else {
-#pragma unroll
-    for (int i = 0; i < kPasses; ++i) {
-      v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
-      if (col_ok && kRowsPerPass * i < lim) load32<kVec32>(xp + i * ldx_pass, v[i]);
-    }
+  for (int i = 0; i < kPasses; ++i) {
+    v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
+    if (col_ok && kRowsPerPass * i < lim) load32<kVec32>(xp + i * ldx_pass, v[i]);
   }
 
 #pragma unroll
@@ -229,12 +197,10 @@ __global__ void __launch_bounds__(kT) quantize_tiles_kernel(const QuantizeParams
   }
 
   __syncthreads();
-  static_assert(kT >= kChunkBytes / 16, "one 16-byte chunk store per thread");
   if (threadIdx.x < kChunkBytes / 16) {
     const uint4 w = reinterpret_cast<const uint4*>(chunk)[threadIdx.x];
-    // chunk index = m-tile * nKT + k-tile (= unit in m-tile-major order)
-    const int64_t c = kGather ? static_cast<int64_t>(mt) * p.nKT + kt : unit;
-    st_stream_v4(p.scales + c * kChunkBytes + threadIdx.x * 16, w);
+    // chunk index = m-tile * nKT + k-tile = unit
+    st_stream_v4(p.scales + static_cast<int64_t>(unit) * kChunkBytes + threadIdx.x * 16, w);
   }
 }
 
@@ -381,8 +347,6 @@ grouped_offsets_kernel(const int32_t* __restrict__ off, int32_t E, int64_t total
   if (tid == 0 && status != nullptr) *status = s_bad ? MXFP4_EOFFSETS : MXFP4_OK;
 }
 
-constexpr bool kGatherChunked = true;
-
 // 256-bit loads need every lane address 32-byte aligned: the base and the
 // row stride (the column offsets are multiples of 32 bytes).
 bool vec32_ok(const void* x, int64_t ldx_bytes) {
@@ -405,10 +369,10 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
   p.n_units = static_cast<int32_t>(tiles * p.nKT);
   const bool v32 = vec32_ok(x, p.ldx_bytes);
-  const auto kernel = f16 ? (v32 ? quantize_tiles_kernel<false, false, true, true>
-                                 : quantize_tiles_kernel<false, false, false, true>)
-                          : (v32 ? quantize_tiles_kernel<false, false, true>
-                                 : quantize_tiles_kernel<false, false, false>);
+  const auto kernel = f16 ? (v32 ? quantize_tiles_kernel<false, true, true>
+                                 : quantize_tiles_kernel<false, false, true>)
+                          : (v32 ? quantize_tiles_kernel<false, true>
+                                 : quantize_tiles_kernel<false, false>);
   return launch_pdl(kernel, static_cast<unsigned>(p.n_units), kThreads, 0, stream, p);
 }
 
@@ -432,8 +396,8 @@ cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K
   p.padded = scale_row_offsets;
   p.E = E;
   const int64_t grid = bound_tiles * p.nKT;  // CTAs past the real padded total exit at once
-  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<true, false, true>
-                                               : quantize_tiles_kernel<true, false, false>;
+  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<true, true>
+                                               : quantize_tiles_kernel<true, false>;
   return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
@@ -462,15 +426,9 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
   p.num_src_rows = num_src_rows;
   p.status = status;
   p.n_mtiles = static_cast<int32_t>(bound_tiles);
-  if (kGatherChunked) {
-    const int64_t grid = bound_tiles * ((p.nKT + kGatherChunkTiles - 1) / kGatherChunkTiles);
-    const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_gather_kernel<true>
-                                                 : quantize_gather_kernel<false>;
-    return launch_pdl(kernel, static_cast<unsigned>(grid), kGatherThreads, 0, stream, p);
-  }
-  const int64_t grid = bound_tiles * p.nKT;
-  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<true, true, true>
-                                               : quantize_tiles_kernel<true, true, false>;
+  const int64_t grid = bound_tiles * ((p.nKT + kGatherChunkTiles - 1) / kGatherChunkTiles);
+  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_gather_kernel<true>
+                                               : quantize_gather_kernel<false>;
   return launch_pdl(kernel, static_cast<unsigned>(grid), kGatherThreads, 0, stream, p);
 }
 
