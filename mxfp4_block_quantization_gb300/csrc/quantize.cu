@@ -11,11 +11,14 @@
 // tile: exactly the rows and scale columns of one 512-byte chunk of the
 // tiled scale layout, so the chunk is assembled in shared memory and leaves
 // the SM as 32 coalesced 16-byte stores.  Lane l of warp w covers 16 BF16
-// elements (two 16-byte loads) of row 4*w + l/8 in each of 4 passes of 32
-// rows; two lanes form one 32-element block, reduced with one xor-shuffle.
-// All four passes' loads are issued before any compute (32 KB in flight per
-// CTA, five CTAs per SM).  Launches use programmatic dependent launch, so a
-// grid is already resident when its predecessor in the stream drains.
+// elements (one 32-byte load, or two 16-byte loads when the input is only
+// 16-byte aligned) of row 4*w + l/8 in each of 4 passes of 32 rows; two lanes
+// form one 32-element block, reduced with one xor-shuffle.  All four passes'
+// loads are issued before any compute (32 KB in flight per CTA, four to five
+// CTAs per SM).  The fused-gather variant (quantize_gather_kernel) keeps one
+// 128-row tile per CTA but walks a chunk of k-tiles.  Launches use
+// programmatic dependent launch, so a grid is already resident when its
+// predecessor in the stream drains.
 #include <cstdint>
 
 #include <cuda_runtime.h>
