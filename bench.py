@@ -581,7 +581,8 @@ def run_ours(args):
                          "unit": "GB/s", "frac": round(kernel_gbs / peak, 4),
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
                          if peak_src == "measured" else "fallback 6.8 TB/s",
-                         "traffic": traffic, "kernel": "quantize_tiles_kernel<false>",
+                         "traffic": traffic,
+                         "kernel": "quantize_tiles_kernel (dense BF16, 32-byte loads)",
                          "algorithmic_bytes_per_launch": nbytes},
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": x_host.numel() * 2,
