@@ -640,3 +640,31 @@ def test_more_than_4gib_input(mx):
         assert np.array_equal(scales[t * per_tile:(t + 1) * per_tile].cpu().numpy(), s_o), t
     del x, codes, scales
     torch.cuda.empty_cache()
+
+
+def test_grouped_many_skewed_experts(mx):
+    """3000 experts (the offsets scan spans three 1024-wide chunks) with
+    Zipf-like segment sizes, many empty: the segment estimate misses and the
+    binary-search fallback runs.  Plain grouped and fused gather both match
+    the oracle."""
+    rng = np.random.default_rng(12)
+    E = 3000
+    sizes = np.minimum((rng.zipf(1.6, E) - 1) * 3, 900).astype(np.int64)
+    sizes[rng.random(E) < 0.3] = 0
+    total = int(sizes.sum())
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    K = 160
+    T = 700
+    x_tok = W.normal_bf16((T, K), seed=13, device="cuda")
+    row_index = torch.from_numpy(rng.integers(0, T, total).astype(np.int32)).cuda()
+    x = x_tok.index_select(0, row_index.long())
+    off_d = torch.from_numpy(off).cuda()
+    c, s, sro, st = run_grouped(mx, x, off_d)
+    rc, c_o, s_o, sro_o = oracle.quantize_grouped(bits(x), off)
+    assert st == 0 and rc == 0 and np.array_equal(sro, sro_o)
+    assert np.array_equal(c, c_o)
+    used = int(sro_o[-1]) * 8
+    assert np.array_equal(s[:used], s_o[:used])
+    c2, s2, sro2, st2 = run_gather(mx, x_tok, row_index, off_d)
+    assert st2 == 0 and np.array_equal(sro2, sro_o) and np.array_equal(c2, c_o)
+    assert np.array_equal(s2[:used], s_o[:used])
