@@ -21,6 +21,8 @@
  *             FP4->BF16 table).
  *
  * Common conventions of every entry point below
+ *   - Kernels run on the calling thread's current CUDA device; every device
+ *     pointer must belong to that device (the stream too).
  *   - Every data pointer is DEVICE memory owned by the caller.  The library
  *     never allocates, never frees and never synchronises the host; work is
  *     enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy

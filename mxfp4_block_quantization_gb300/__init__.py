@@ -119,6 +119,15 @@ def _check(rc, where):
         raise MXFP4Error(rc, where)
 
 
+def _device_of(*tensors):
+    """The one CUDA device all given tensors live on (the library launches on
+    the current device, so every call switches to it)."""
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"all tensors must be on the same CUDA device, got {sorted(map(str, devs))}")
+    return devs.pop()
+
+
 # ------------------------------------------------------- C entry points
 def mxfp4_scale_bytes(M: int, K: int) -> int:
     return int(_lib.mxfp4_scale_bytes(int(M), int(K)))
@@ -145,8 +154,9 @@ def mxfp4_quantize(x, codes, scales, stream=None) -> None:
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with unit column stride")
     M, K = x.shape
-    _check(_lib.mxfp4_quantize(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales),
-                               _stream(stream, x.device)), "mxfp4_quantize")
+    with torch.cuda.device(_device_of(x, codes, scales)):
+        _check(_lib.mxfp4_quantize(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales),
+                                   _stream(stream, x.device)), "mxfp4_quantize")
 
 
 def mxfp4_quantize_f16(x, codes, scales, stream=None) -> None:
@@ -158,8 +168,9 @@ def mxfp4_quantize_f16(x, codes, scales, stream=None) -> None:
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with unit column stride")
     M, K = x.shape
-    _check(_lib.mxfp4_quantize_f16(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales),
-                                   _stream(stream, x.device)), "mxfp4_quantize_f16")
+    with torch.cuda.device(_device_of(x, codes, scales)):
+        _check(_lib.mxfp4_quantize_f16(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales),
+                                       _stream(stream, x.device)), "mxfp4_quantize_f16")
 
 
 def mxfp4_quantize_grouped(x, expert_offsets, codes, scales, scale_row_offsets, status=None,
@@ -176,9 +187,11 @@ def mxfp4_quantize_grouped(x, expert_offsets, codes, scales, scale_row_offsets, 
         raise ValueError("x must be a contiguous 2-D tensor")
     total, K = x.shape
     E = expert_offsets.numel() - 1
-    _check(_lib.mxfp4_quantize_grouped(_ptr(x), total, K, _ptr(expert_offsets), E, _ptr(codes),
-                                       _ptr(scales), _ptr(scale_row_offsets), _ptr(status),
-                                       _stream(stream, x.device)), "mxfp4_quantize_grouped")
+    with torch.cuda.device(_device_of(x, expert_offsets, codes, scales, scale_row_offsets, status)):
+        _check(_lib.mxfp4_quantize_grouped(_ptr(x), total, K, _ptr(expert_offsets), E,
+                                           _ptr(codes), _ptr(scales), _ptr(scale_row_offsets),
+                                           _ptr(status), _stream(stream, x.device)),
+               "mxfp4_quantize_grouped")
 
 
 def mxfp4_quantize_grouped_gather(x, row_index, expert_offsets, codes, scales, scale_row_offsets,
@@ -198,10 +211,12 @@ def mxfp4_quantize_grouped_gather(x, row_index, expert_offsets, codes, scales, s
         raise ValueError("row_index must be contiguous")
     n_src, K = x.shape
     E = expert_offsets.numel() - 1
-    _check(_lib.mxfp4_quantize_grouped_gather(
-        _ptr(x), n_src, K, x.stride(0), _ptr(row_index), row_index.numel(), _ptr(expert_offsets),
-        E, _ptr(codes), _ptr(scales), _ptr(scale_row_offsets), _ptr(status),
-        _stream(stream, x.device)), "mxfp4_quantize_grouped_gather")
+    with torch.cuda.device(_device_of(x, row_index, expert_offsets, codes, scales,
+                                      scale_row_offsets, status)):
+        _check(_lib.mxfp4_quantize_grouped_gather(
+            _ptr(x), n_src, K, x.stride(0), _ptr(row_index), row_index.numel(),
+            _ptr(expert_offsets), E, _ptr(codes), _ptr(scales), _ptr(scale_row_offsets),
+            _ptr(status), _stream(stream, x.device)), "mxfp4_quantize_grouped_gather")
 
 
 def mxfp4_dequantize(codes, scales, M: int, K: int, y, stream=None) -> None:
@@ -211,8 +226,9 @@ def mxfp4_dequantize(codes, scales, M: int, K: int, y, stream=None) -> None:
     _need_cuda("y", y, torch.bfloat16)
     if not y.is_contiguous():
         raise ValueError("y must be contiguous")
-    _check(_lib.mxfp4_dequantize(_ptr(codes), _ptr(scales), int(M), int(K), _ptr(y),
-                                 _stream(stream, y.device)), "mxfp4_dequantize")
+    with torch.cuda.device(_device_of(codes, scales, y)):
+        _check(_lib.mxfp4_dequantize(_ptr(codes), _ptr(scales), int(M), int(K), _ptr(y),
+                                     _stream(stream, y.device)), "mxfp4_dequantize")
 
 
 def mxfp4_swap_w13(codes_in, scales_in, w13_bias_in, E: int, two_n: int, K: int,
@@ -227,12 +243,14 @@ def mxfp4_swap_w13(codes_in, scales_in, w13_bias_in, E: int, two_n: int, K: int,
                     ("w2_bias_in", w2_bias_in, torch.float32),
                     ("w2_bias_out", w2_bias_out, torch.bfloat16)):
         _need_cuda(n, t, d)
-    dev = next(t.device for t in (codes_in, w13_bias_in, w2_bias_in) if t is not None)
+    dev = _device_of(codes_in, scales_in, codes_out, scales_out, w13_bias_in, w13_bias_out,
+                     w2_bias_in, w2_bias_out)
     n2 = w2_bias_in.numel() if w2_bias_in is not None else 0
-    _check(_lib.mxfp4_swap_w13(_ptr(codes_in), _ptr(scales_in), _ptr(w13_bias_in), int(E),
-                               int(two_n), int(K), int(scales_tiled), _ptr(codes_out),
-                               _ptr(scales_out), _ptr(w13_bias_out), _ptr(w2_bias_in), n2,
-                               _ptr(w2_bias_out), _stream(stream, dev)), "mxfp4_swap_w13")
+    with torch.cuda.device(dev):
+        _check(_lib.mxfp4_swap_w13(_ptr(codes_in), _ptr(scales_in), _ptr(w13_bias_in), int(E),
+                                   int(two_n), int(K), int(scales_tiled), _ptr(codes_out),
+                                   _ptr(scales_out), _ptr(w13_bias_out), _ptr(w2_bias_in), n2,
+                                   _ptr(w2_bias_out), _stream(stream, dev)), "mxfp4_swap_w13")
 
 
 def mxfp4_nvfp4_scale_bytes(M: int, K: int) -> int:
@@ -249,9 +267,10 @@ def mxfp4_quantize_nvfp4(x, global_scale, codes, scales, stream=None) -> None:
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with unit column stride")
     M, K = x.shape
-    _check(_lib.mxfp4_quantize_nvfp4(_ptr(x), M, K, x.stride(0), _ptr(global_scale), _ptr(codes),
-                                     _ptr(scales), _stream(stream, x.device)),
-           "mxfp4_quantize_nvfp4")
+    with torch.cuda.device(_device_of(x, global_scale, codes, scales)):
+        _check(_lib.mxfp4_quantize_nvfp4(_ptr(x), M, K, x.stride(0), _ptr(global_scale),
+                                         _ptr(codes), _ptr(scales), _stream(stream, x.device)),
+               "mxfp4_quantize_nvfp4")
 
 
 def mxfp4_dequantize_nvfp4(codes, scales, global_scale, M: int, K: int, y, stream=None) -> None:
@@ -261,9 +280,10 @@ def mxfp4_dequantize_nvfp4(codes, scales, global_scale, M: int, K: int, y, strea
     _need_cuda("y", y, torch.bfloat16)
     if not y.is_contiguous():
         raise ValueError("y must be contiguous")
-    _check(_lib.mxfp4_dequantize_nvfp4(_ptr(codes), _ptr(scales), _ptr(global_scale), int(M),
-                                       int(K), _ptr(y), _stream(stream, y.device)),
-           "mxfp4_dequantize_nvfp4")
+    with torch.cuda.device(_device_of(codes, scales, global_scale, y)):
+        _check(_lib.mxfp4_dequantize_nvfp4(_ptr(codes), _ptr(scales), _ptr(global_scale), int(M),
+                                           int(K), _ptr(y), _stream(stream, y.device)),
+               "mxfp4_dequantize_nvfp4")
 
 
 # --------------------------------------------------- allocating wrappers

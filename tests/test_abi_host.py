@@ -171,3 +171,10 @@ def test_nvfp4_validation(lib):
     assert d(A, 2 * A, 9 * A, 4, 24, 3 * A, None) == lib.MXFP4_ESHAPE
     assert d(A, 2 * A, None, 4, 64, 3 * A, None) == lib.MXFP4_EINVAL
     assert d(A, 2 * A, 9 * A, 4, 64, A + 32, None) == lib.MXFP4_EALIAS
+
+
+def test_binding_rejects_mixed_devices(lib):
+    import torch
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        lib._device_of(x, torch.zeros(1, device="meta"))
