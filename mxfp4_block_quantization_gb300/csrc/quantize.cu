@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
 constexpr int kGatherChunkTiles = 8;
 
 template <bool kVec32>
-__global__ void __launch_bounds__(kGatherThreads, 3) quantize_gather_kernel(const QuantizeParams p) {
+__global__ void __launch_bounds__(kGatherThreads) quantize_gather_kernel(const QuantizeParams p) {
   constexpr int kRowsPerPass = rows_per_pass(kGatherThreads);
   constexpr int kPasses = passes(kGatherThreads);
   __shared__ __align__(16) uint8_t chunk[2][kChunkBytes];
@@ -247,12 +247,12 @@ __global__ void __launch_bounds__(kGatherThreads, 3) quantize_gather_kernel(cons
 
   // source rows of this thread's eight output rows; an index outside
   // [0, num_src_rows) reads nothing, quantizes as a zero row and is reported
-  int32_t src[kPasses];
+  int64_t src[kPasses];
   bool bad = false;
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
     src[i] = (kRowsPerPass * i < lim) ? __ldg(p.row_index + r + kRowsPerPass * i) : 0;
-    const bool in_range = src[i] >= 0 && static_cast<int64_t>(src[i]) < p.num_src_rows;
+    const bool in_range = src[i] >= 0 && src[i] < p.num_src_rows;
     if (kRowsPerPass * i < lim) bad |= !in_range;
     src[i] = (kRowsPerPass * i < lim && in_range) ? src[i] : -1;
   }
@@ -261,28 +261,16 @@ __global__ void __launch_bounds__(kGatherThreads, 3) quantize_gather_kernel(cons
   const int kt0 = kc * kGatherChunkTiles;
   const int kt_end = kt0 + kGatherChunkTiles < p.nKT ? kt0 + kGatherChunkTiles : p.nKT;
   const int64_t cld_pass = p.code_ld * kRowsPerPass;
-  const uint8_t* xsub = p.x + sub * (kElems * 2);
-
-  // Loads are pipelined across the chunk's k-tiles: as soon as pass i of
-  // k-tile kt is consumed, its registers are refilled with pass i of k-tile
-  // kt + 1 (same rows, next 256 bytes), so eight 32-byte loads per thread stay
-  // in flight until the chunk ends.
-  uint4 v[kPasses][2];
-  {
-    const bool col_ok = kt0 * kTileBlocks + blk < p.sK;
-#pragma unroll
-    for (int i = 0; i < kPasses; ++i) {
-      v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
-      if (col_ok && src[i] >= 0)
-        load32<kVec32>(xsub + static_cast<int64_t>(kt0) * (kTileCols * 2) +
-                           static_cast<int64_t>(src[i]) * p.ldx_bytes, v[i]);
-    }
-  }
   int buf = 0;
   for (int kt = kt0; kt < kt_end; ++kt) {
     const bool col_ok = kt * kTileBlocks + blk < p.sK;
-    const bool next_ok = kt + 1 < kt_end && (kt + 1) * kTileBlocks + blk < p.sK;
-    const uint8_t* xnext = xsub + static_cast<int64_t>(kt + 1) * (kTileCols * 2);
+    const uint8_t* xcol = p.x + static_cast<int64_t>(kt) * (kTileCols * 2) + sub * (kElems * 2);
+    uint4 v[kPasses][2];
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
+      if (col_ok && src[i] >= 0) load32<kVec32>(xcol + src[i] * p.ldx_bytes, v[i]);
+    }
     uint8_t* cp = p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) +
                   sub * (kElems / 2);
 #pragma unroll
@@ -292,9 +280,6 @@ __global__ void __launch_bounds__(kGatherThreads, 3) quantize_gather_kernel(cons
         chunk[buf][chunk_offset(lr0 + kRowsPerPass * i, blk)] = static_cast<uint8_t>(s);
       const uint2 code = lane_codes<false>(v[i], s);
       if (col_ok && kRowsPerPass * i < lim) st_stream_v2(cp + i * cld_pass, code);
-      v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
-      if (next_ok && src[i] >= 0)
-        load32<kVec32>(xnext + static_cast<int64_t>(src[i]) * p.ldx_bytes, v[i]);
     }
     __syncthreads();
     if (threadIdx.x < kChunkBytes / 16) {
