@@ -35,6 +35,9 @@ __all__ = [
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300.so")
+# The bounds-checking build (same results; every global access checked and
+# counted when out of range); see _load() and mxfp4_debug_bounds_violations.
+DEBUG_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300_debug.so")
 
 MXFP4_OK = 0
 MXFP4_EINVAL = -1
@@ -54,12 +57,12 @@ class MXFP4Error(RuntimeError):
         super().__init__(f"{where}: {mxfp4_status_string(code)} ({code})")
 
 
-def _load():
-    if not os.path.exists(LIB_PATH):
+def _load(path=LIB_PATH):
+    if not os.path.exists(path):
         raise ImportError(
-            f"{LIB_PATH} is missing: build it with "
+            f"{path} is missing: build it with "
             "`python mxfp4_block_quantization_gb300/_build.py` (nvcc, sm_103a)")
-    L = ctypes.CDLL(LIB_PATH)
+    L = ctypes.CDLL(path)
     vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
     L.mxfp4_scale_bytes.restype = ctypes.c_size_t
     L.mxfp4_scale_bytes.argtypes = [i64, i64]
@@ -88,6 +91,9 @@ def _load():
     L.mxfp4_status_string.argtypes = [ctypes.c_int]
     L.mxfp4_version.restype = ctypes.c_int
     L.mxfp4_version.argtypes = []
+    if hasattr(L, "mxfp4_debug_bounds_violations"):
+        L.mxfp4_debug_bounds_violations.restype = ctypes.c_int64
+        L.mxfp4_debug_bounds_violations.argtypes = []
     return L
 
 

@@ -42,7 +42,12 @@ struct DequantizeParams {
   int64_t y_ld;     // 2K bytes
   int32_t sK;
   int32_t nKT;
+#ifdef MXFP4_DEBUG_BOUNDS
+  DebugRanges dbg;  // byte ranges of codes, scales, y (bounds build)
+#endif
 };
+
+enum : int { kDbgCodes = 0, kDbgScales, kDbgY };
 
 // Four code bytes (8 elements, element 2j in the low nibble of byte j) and a
 // scale value -> 16 bytes of BF16.
@@ -87,8 +92,12 @@ __global__ void __launch_bounds__(kThreads) dequantize_wide_kernel(const Dequant
   uint2 c[kWidePasses];
 #pragma unroll
   for (int i = 0; i < kWidePasses; ++i)
-    c[i] = (col_ok && kRowsPerPass * i < lim) ? ld_stream_v2(cp + i * cld_pass) : make_uint2(0u, 0u);
-  const uint4 sr = ld_stream_v4(p.scales + (tile * p.nKT + kt) * kChunkBytes + lr0 * 16);
+    c[i] = (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgCodes, cp + i * cld_pass, 8))
+               ? ld_stream_v2(cp + i * cld_pass)
+               : make_uint2(0u, 0u);
+  const uint8_t* srp = p.scales + (tile * p.nKT + kt) * kChunkBytes + lr0 * 16;
+  const uint4 sr =
+      MXFP4_IN_BOUNDS(p, kDbgScales, srp, 16) ? ld_stream_v4(srp) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
   for (int i = 0; i < kWidePasses; ++i) {
     const uint32_t word = i == 0 ? sr.x : i == 1 ? sr.y : i == 2 ? sr.z : sr.w;
@@ -101,7 +110,8 @@ __global__ void __launch_bounds__(kThreads) dequantize_wide_kernel(const Dequant
       o0 = decode8(c[i].x, sc);
       o1 = decode8(c[i].y, sc);
     }
-    if (col_ok && kRowsPerPass * i < lim) st_stream_v8(yp + i * yld_pass, o0, o1);
+    if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgY, yp + i * yld_pass, 32))
+      st_stream_v8(yp + i * yld_pass, o0, o1);
   }
 }
 
@@ -128,9 +138,10 @@ __global__ void __launch_bounds__(kThreads) dequantize_narrow_kernel(const Dequa
     const int64_t r = row0 + lr;
     c[i] = 0u;
     s[i] = 0u;
-    if (col_ok && r < p.M) {
-      c[i] = ld_stream_u32(p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) +
-                           seg * 4);
+    const uint8_t* cp = p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) + seg * 4;
+    if (col_ok && r < p.M && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 4) &&
+        MXFP4_IN_BOUNDS(p, kDbgScales, chunk + chunk_offset(lr, blk), 1)) {
+      c[i] = ld_stream_u32(cp);
       s[i] = __ldg(chunk + chunk_offset(lr, blk));
     }
   }
@@ -144,8 +155,8 @@ __global__ void __launch_bounds__(kThreads) dequantize_narrow_kernel(const Dequa
     } else {
       o = decode8(c[i], scale_from_e8m0(s[i]));
     }
-    if (col_ok && r < p.M)
-      st_stream_v4(p.y + r * p.y_ld + static_cast<int64_t>(kt) * (kTileCols * 2) + seg * 16, o);
+    uint8_t* yp = p.y + r * p.y_ld + static_cast<int64_t>(kt) * (kTileCols * 2) + seg * 16;
+    if (col_ok && r < p.M && MXFP4_IN_BOUNDS(p, kDbgY, yp, 16)) st_stream_v4(yp, o);
   }
 }
 
@@ -163,9 +174,23 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64
   p.sK = static_cast<int32_t>(K / kBlock);
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(p.dbg, kDbgCodes, codes, M * (K / 2));
+  debug_range(p.dbg, kDbgScales, scales, tiles * p.nKT * kChunkBytes);
+  debug_range(p.dbg, kDbgY, y, M * K * 2);
+#endif
   const bool wide = reinterpret_cast<uintptr_t>(y) % 32 == 0;  // rows are 2K = 64*(K/32) bytes
   return launch_pdl(wide ? dequantize_wide_kernel : dequantize_narrow_kernel,
                     static_cast<unsigned>(tiles * p.nKT), kThreads, 0, stream, p);
 }
+
+#ifdef MXFP4_DEBUG_BOUNDS
+unsigned int debug_violations_dequantize() {
+  unsigned int v = 0, zero = 0;
+  cudaMemcpyFromSymbol(&v, g_debug_violations, sizeof v);
+  cudaMemcpyToSymbol(g_debug_violations, &zero, sizeof zero);
+  return v;
+}
+#endif
 
 }  // namespace mxfp4

@@ -11,6 +11,9 @@
 
 #include "mxfp4_internal.h"
 #include "../../include/mxfp4.h"
+#ifdef MXFP4_DEBUG_BOUNDS
+#include "../../include/mxfp4_debug.h"
+#endif
 
 namespace mxfp4 {
 
@@ -328,5 +331,14 @@ const char* mxfp4_status_string(int status) {
 }
 
 int mxfp4_version(void) { return 100; }
+
+#ifdef MXFP4_DEBUG_BOUNDS
+int64_t mxfp4_debug_bounds_violations(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  return static_cast<int64_t>(mxfp4::debug_violations_quantize()) +
+         mxfp4::debug_violations_dequantize() + mxfp4::debug_violations_nvfp4() +
+         mxfp4::debug_violations_swap();
+}
+#endif
 
 }  // extern "C"

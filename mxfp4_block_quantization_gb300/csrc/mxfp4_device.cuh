@@ -290,6 +290,39 @@ __device__ __forceinline__ uint32_t f16_bits_to_f32_bits(uint32_t h) {
   return __float_as_uint(f);
 }
 
+// ------------------------------------------------- bounds-checking build
+// Compiled with -DMXFP4_DEBUG_BOUNDS (libmxfp4_gb300_debug.so), every global
+// load and store of every kernel is first checked against the byte range of
+// the buffer it belongs to, as the host derived it from the call's
+// arguments.  An access outside its range is skipped (a skipped load yields
+// zeros) and counted in a per-translation-unit device counter; nothing
+// traps.  In the normal build the checks compile away.
+struct DebugRanges {
+  uintptr_t lo[8];
+  uintptr_t hi[8];
+};
+
+#ifdef MXFP4_DEBUG_BOUNDS
+static __device__ unsigned int g_debug_violations;
+
+__device__ __forceinline__ bool debug_in_bounds(const DebugRanges& r, int slot, const void* p,
+                                                unsigned bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const bool ok = a >= r.lo[slot] && a + bytes <= r.hi[slot];
+  if (!ok) atomicAdd(&g_debug_violations, 1u);
+  return ok;
+}
+#define MXFP4_IN_BOUNDS(params, slot, ptr, bytes) \
+  ::mxfp4::debug_in_bounds((params).dbg, (slot), (ptr), (bytes))
+#else
+#define MXFP4_IN_BOUNDS(params, slot, ptr, bytes) true
+#endif
+
+inline void debug_range(DebugRanges& r, int slot, const void* p, int64_t bytes) {
+  r.lo[slot] = reinterpret_cast<uintptr_t>(p);
+  r.hi[slot] = r.lo[slot] + static_cast<uintptr_t>(bytes > 0 ? bytes : 0);
+}
+
 // Programmatic dependent launch: wait until the preceding grid of the stream
 // has completed and its writes are visible (no-op without a predecessor),
 // and allow the next grid of the stream to be scheduled.

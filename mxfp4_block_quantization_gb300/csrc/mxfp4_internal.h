@@ -64,6 +64,15 @@ cudaError_t launch_swap_w13(const SwapArgs& a, cudaStream_t stream);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+#ifdef MXFP4_DEBUG_BOUNDS
+// Bounds build: out-of-range accesses counted by each translation unit since
+// the last read (reading resets the counter).
+unsigned int debug_violations_quantize();
+unsigned int debug_violations_dequantize();
+unsigned int debug_violations_nvfp4();
+unsigned int debug_violations_swap();
+#endif
+
 // Launch with programmatic dependent launch allowed: the grid may be
 // scheduled while the previous kernel of the stream drains; every kernel of
 // this library executes griddepcontrol.wait before touching global memory,

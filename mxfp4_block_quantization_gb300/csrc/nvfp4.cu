@@ -46,7 +46,12 @@ struct Nvfp4Params {
   int32_t sK;                         // 16-element scale columns K/16
   int32_t nKT;                        // chunks per m-tile ceil(sK/4)
   int32_t nCT;                        // CTAs per m-tile ceil(nKT/2)
+#ifdef MXFP4_DEBUG_BOUNDS
+  DebugRanges dbg;                    // byte ranges of the buffers (bounds build)
+#endif
 };
+
+enum : int { kDbgXY = 0, kDbgCodes, kDbgScales, kDbgG };
 
 template <bool kVec32>
 __device__ __forceinline__ void load32(const uint8_t* src, uint4 (&v)[2]) {
@@ -79,13 +84,14 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(const Nvfp4Par
   uint8_t* cp = p.codes + (row0 + lr0) * p.code_ld + static_cast<int64_t>(ct) * (kCtaCols / 2) + sub * 8;
   const int64_t ldx_pass = p.ldx_bytes * kRowsPerPass;
   const int64_t cld_pass = p.code_ld * kRowsPerPass;
-  const float g = __ldg(p.g);
+  const float g = MXFP4_IN_BOUNDS(p, kDbgG, p.g, 4) ? __ldg(p.g) : 0.0f;
 
   uint4 v[kPasses][2];
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
     v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
-    if (col_ok && kRowsPerPass * i < lim) load32<kVec32>(xp + i * ldx_pass, v[i]);
+    if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgXY, xp + i * ldx_pass, 32))
+      load32<kVec32>(xp + i * ldx_pass, v[i]);
   }
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
@@ -107,16 +113,18 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(const Nvfp4Par
       code.x = scale_cvt_e2m1x8(v[i][0], inv);
       code.y = scale_cvt_e2m1x8(v[i][1], inv);
     }
-    if (col_ok && kRowsPerPass * i < lim) st_stream_v2(cp + i * cld_pass, code);
+    if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgCodes, cp + i * cld_pass, 8))
+      st_stream_v2(cp + i * cld_pass, code);
   }
   __syncthreads();
   if (threadIdx.x < 2 * (kChunkBytes / 16)) {
     const int j = threadIdx.x >> 5;
     const int w = threadIdx.x & 31;
     const int kt = ct * 2 + j;
-    if (kt < p.nKT) {
+    uint8_t* const sp = p.scales + (mt * p.nKT + kt) * kChunkBytes + w * 16;
+    if (kt < p.nKT && MXFP4_IN_BOUNDS(p, kDbgScales, sp, 16)) {
       const uint4 val = reinterpret_cast<const uint4*>(chunk[j])[w];
-      st_stream_v4(p.scales + (mt * p.nKT + kt) * kChunkBytes + w * 16, val);
+      st_stream_v4(sp, val);
     }
   }
 }
@@ -157,21 +165,24 @@ __global__ void __launch_bounds__(kThreads) nvfp4_dequantize_kernel(const Nvfp4P
   uint8_t* yp = p.y + (row0 + lr0) * p.y_ld + static_cast<int64_t>(ct) * (kCtaCols * 2) + sub * 32;
   const int64_t cld_pass = p.code_ld * kRowsPerPass;
   const int64_t yld_pass = p.y_ld * kRowsPerPass;
-  const float inv_g = 1.0f / __ldg(p.g);    // IEEE float32 division
+  const float inv_g = 1.0f / (MXFP4_IN_BOUNDS(p, kDbgG, p.g, 4) ? __ldg(p.g) : 1.0f);  // IEEE division
 
   uint2 c[kPasses];
 #pragma unroll
   for (int i = 0; i < kPasses; ++i)
-    c[i] = (col_ok && kRowsPerPass * i < lim) ? ld_stream_v2(cp + i * cld_pass) : make_uint2(0u, 0u);
+    c[i] = (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgCodes, cp + i * cld_pass, 8))
+               ? ld_stream_v2(cp + i * cld_pass)
+               : make_uint2(0u, 0u);
   uint4 sr = make_uint4(0u, 0u, 0u, 0u);
-  if (col_ok) sr = ld_stream_v4(p.scales + (mt * p.nKT + ct * 2 + half) * kChunkBytes + lr0 * 16);
+  const uint8_t* srp = p.scales + (mt * p.nKT + ct * 2 + half) * kChunkBytes + lr0 * 16;
+  if (col_ok && MXFP4_IN_BOUNDS(p, kDbgScales, srp, 16)) sr = ld_stream_v4(srp);
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
     const uint32_t word = i == 0 ? sr.x : i == 1 ? sr.y : i == 2 ? sr.z : sr.w;
     const float sfv = e4m3_to_f32((word >> (8 * cc)) & 0xFFu);
     const uint4 o0 = decode8_nv(c[i].x, sfv, inv_g);
     const uint4 o1 = decode8_nv(c[i].y, sfv, inv_g);
-    if (col_ok && kRowsPerPass * i < lim) {
+    if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgXY, yp + i * yld_pass, 32)) {
       if constexpr (kVec32) {
         st_stream_v8(yp + i * yld_pass, o0, o1);
       } else {
@@ -205,6 +216,12 @@ cudaError_t launch_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t l
   p.scales = scales;
   p.g = global_scale;
   const int64_t grid = (M + kTileRows - 1) / kTileRows * p.nCT;
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(p.dbg, kDbgXY, x, ((M - 1) * ldx + K) * 2);
+  debug_range(p.dbg, kDbgCodes, codes, M * (K / 2));
+  debug_range(p.dbg, kDbgScales, scales, (M + kTileRows - 1) / kTileRows * p.nKT * kChunkBytes);
+  debug_range(p.dbg, kDbgG, global_scale, 4);
+#endif
   const bool v32 = reinterpret_cast<uintptr_t>(x) % 32 == 0 && p.ldx_bytes % 32 == 0;
   return launch_pdl(v32 ? nvfp4_quantize_kernel<true> : nvfp4_quantize_kernel<false>,
                     static_cast<unsigned>(grid), kThreads, 0, stream, p);
@@ -219,9 +236,24 @@ cudaError_t launch_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales,
   p.y = static_cast<uint8_t*>(y);
   p.g = global_scale;
   const int64_t grid = (M + kTileRows - 1) / kTileRows * p.nCT;
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(p.dbg, kDbgXY, y, M * K * 2);
+  debug_range(p.dbg, kDbgCodes, codes, M * (K / 2));
+  debug_range(p.dbg, kDbgScales, scales, (M + kTileRows - 1) / kTileRows * p.nKT * kChunkBytes);
+  debug_range(p.dbg, kDbgG, global_scale, 4);
+#endif
   const bool v32 = reinterpret_cast<uintptr_t>(y) % 32 == 0;  // rows are 2K = 32*(K/16) bytes
   return launch_pdl(v32 ? nvfp4_dequantize_kernel<true> : nvfp4_dequantize_kernel<false>,
                     static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
+
+#ifdef MXFP4_DEBUG_BOUNDS
+unsigned int debug_violations_nvfp4() {
+  unsigned int v = 0, zero = 0;
+  cudaMemcpyFromSymbol(&v, g_debug_violations, sizeof v);
+  cudaMemcpyToSymbol(g_debug_violations, &zero, sizeof zero);
+  return v;
+}
+#endif
 
 }  // namespace mxfp4

@@ -57,7 +57,13 @@ struct QuantizeParams {
   int64_t num_src_rows;                   // gather: rows of x
   int32_t* status;                        // gather: device status word (may be NULL)
   int32_t n_mtiles;                       // gather: m-tiles of the grid (chunk-major order)
+#ifdef MXFP4_DEBUG_BOUNDS
+  DebugRanges dbg;                        // byte ranges of the buffers below (bounds build)
+#endif
 };
+
+// Buffer slots of QuantizeParams::dbg.
+enum : int { kDbgX = 0, kDbgCodes, kDbgScales, kDbgOffsets, kDbgPadded, kDbgRowIndex, kDbgStatus };
 
 // Segment holding padded row `prow`: the last e in [0, E) with P[e] <= prow
 // (empty segments share their start with the next one, so the last such e
@@ -156,6 +162,10 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
   const int kt = unit - mt * p.nKT;
   int64_t row0, row_end;
   if constexpr (kGrouped) {
+    // every offset index read below lies in [0, E]
+    if (!MXFP4_IN_BOUNDS(p, kDbgPadded, p.padded, (p.E + 1) * 4) ||
+        !MXFP4_IN_BOUNDS(p, kDbgOffsets, p.offsets, (p.E + 1) * 4))
+      return;
     const int total_padded = __ldg(p.padded + p.E);
     const int prow = mt * kTileRows;
     if (total_padded < 0 || prow >= total_padded) return;  // rejected offsets / past the end
@@ -187,7 +197,8 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
     v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
-    if (col_ok && kRowsPerPass * i < lim) load32<kVec32>(xp + i * ldx_pass, v[i]);
+    if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgX, xp + i * ldx_pass, 32))
+      load32<kVec32>(xp + i * ldx_pass, v[i]);
   }
 
 #pragma unroll
@@ -196,14 +207,16 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
     // rows of pass i sit in chunk row lr0 % 32 (outerM), word (lr0 + rows*i) / 32 (innerM)
     if ((lane & 1) == 0) chunk[chunk_offset(lr0 + kRowsPerPass * i, blk)] = static_cast<uint8_t>(s);
     const uint2 code = lane_codes<kF16>(v[i], s);
-    if (col_ok && kRowsPerPass * i < lim) st_stream_v2(cp + i * cld_pass, code);
+    if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgCodes, cp + i * cld_pass, 8))
+      st_stream_v2(cp + i * cld_pass, code);
   }
 
   __syncthreads();
-  if (threadIdx.x < kChunkBytes / 16) {
+  // chunk index = m-tile * nKT + k-tile = unit
+  uint8_t* const sp = p.scales + static_cast<int64_t>(unit) * kChunkBytes + threadIdx.x * 16;
+  if (threadIdx.x < kChunkBytes / 16 && MXFP4_IN_BOUNDS(p, kDbgScales, sp, 16)) {
     const uint4 w = reinterpret_cast<const uint4*>(chunk)[threadIdx.x];
-    // chunk index = m-tile * nKT + k-tile = unit
-    st_stream_v4(p.scales + static_cast<int64_t>(unit) * kChunkBytes + threadIdx.x * 16, w);
+    st_stream_v4(sp, w);
   }
 }
 
@@ -229,6 +242,9 @@ __global__ void __launch_bounds__(kGatherThreads) quantize_gather_kernel(const Q
   const int unit = blockIdx.x;
   const int kc = unit / p.n_mtiles;
   const int mt = unit - kc * p.n_mtiles;
+  if (!MXFP4_IN_BOUNDS(p, kDbgPadded, p.padded, (p.E + 1) * 4) ||
+      !MXFP4_IN_BOUNDS(p, kDbgOffsets, p.offsets, (p.E + 1) * 4))
+    return;
   const int total_padded = __ldg(p.padded + p.E);
   const int prow = mt * kTileRows;
   if (total_padded < 0 || prow >= total_padded) return;  // rejected offsets / past the end
@@ -251,12 +267,16 @@ __global__ void __launch_bounds__(kGatherThreads) quantize_gather_kernel(const Q
   bool bad = false;
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
-    src[i] = (kRowsPerPass * i < lim) ? __ldg(p.row_index + r + kRowsPerPass * i) : 0;
+    src[i] = (kRowsPerPass * i < lim &&
+              MXFP4_IN_BOUNDS(p, kDbgRowIndex, p.row_index + r + kRowsPerPass * i, 4))
+                 ? __ldg(p.row_index + r + kRowsPerPass * i)
+                 : 0;
     const bool in_range = src[i] >= 0 && src[i] < p.num_src_rows;
     if (kRowsPerPass * i < lim) bad |= !in_range;
     src[i] = (kRowsPerPass * i < lim && in_range) ? src[i] : -1;
   }
-  if (bad && p.status != nullptr) atomicExch(p.status, MXFP4_EINDEX);
+  if (bad && p.status != nullptr && MXFP4_IN_BOUNDS(p, kDbgStatus, p.status, 4))
+    atomicExch(p.status, MXFP4_EINDEX);
 
   const int kt0 = kc * kGatherChunkTiles;
   const int kt_end = kt0 + kGatherChunkTiles < p.nKT ? kt0 + kGatherChunkTiles : p.nKT;
@@ -269,7 +289,8 @@ __global__ void __launch_bounds__(kGatherThreads) quantize_gather_kernel(const Q
 #pragma unroll
     for (int i = 0; i < kPasses; ++i) {
       v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
-      if (col_ok && src[i] >= 0) load32<kVec32>(xcol + src[i] * p.ldx_bytes, v[i]);
+      if (col_ok && src[i] >= 0 && MXFP4_IN_BOUNDS(p, kDbgX, xcol + src[i] * p.ldx_bytes, 32))
+        load32<kVec32>(xcol + src[i] * p.ldx_bytes, v[i]);
     }
     uint8_t* cp = p.codes + r * p.code_ld + static_cast<int64_t>(kt) * (kTileCols / 2) +
                   sub * (kElems / 2);
@@ -279,13 +300,15 @@ __global__ void __launch_bounds__(kGatherThreads) quantize_gather_kernel(const Q
       if ((lane & 1) == 0)
         chunk[buf][chunk_offset(lr0 + kRowsPerPass * i, blk)] = static_cast<uint8_t>(s);
       const uint2 code = lane_codes<false>(v[i], s);
-      if (col_ok && kRowsPerPass * i < lim) st_stream_v2(cp + i * cld_pass, code);
+      if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgCodes, cp + i * cld_pass, 8))
+        st_stream_v2(cp + i * cld_pass, code);
     }
     __syncthreads();
-    if (threadIdx.x < kChunkBytes / 16) {
+    const int64_t c = static_cast<int64_t>(mt) * p.nKT + kt;
+    uint8_t* const sp = p.scales + c * kChunkBytes + threadIdx.x * 16;
+    if (threadIdx.x < kChunkBytes / 16 && MXFP4_IN_BOUNDS(p, kDbgScales, sp, 16)) {
       const uint4 w = reinterpret_cast<const uint4*>(chunk[buf])[threadIdx.x];
-      const int64_t c = static_cast<int64_t>(mt) * p.nKT + kt;
-      st_stream_v4(p.scales + c * kChunkBytes + threadIdx.x * 16, w);
+      st_stream_v4(sp, w);
     }
     buf ^= 1;
   }
@@ -296,14 +319,33 @@ __global__ void __launch_bounds__(kGatherThreads) quantize_gather_kernel(const Q
 // One CTA of 1024 threads; a block-wide scan per 1024 segments.
 constexpr int kScanThreads = 1024;
 
-__global__ void __launch_bounds__(kScanThreads)
-grouped_offsets_kernel(const int32_t* __restrict__ off, int32_t E, int64_t total_rows,
-                       int32_t* __restrict__ padded, int32_t* __restrict__ status) {
+struct OffsetsParams {
+  const int32_t* __restrict__ off;
+  int32_t E;
+  int64_t total_rows;
+  int32_t* __restrict__ padded;
+  int32_t* __restrict__ status;
+#ifdef MXFP4_DEBUG_BOUNDS
+  DebugRanges dbg;  // slots kDbgOffsets, kDbgPadded, kDbgStatus
+#endif
+};
+
+__global__ void __launch_bounds__(kScanThreads) grouped_offsets_kernel(const OffsetsParams q) {
+  const int32_t* __restrict__ off = q.off;
+  const int32_t E = q.E;
+  const int64_t total_rows = q.total_rows;
+  int32_t* __restrict__ padded = q.padded;
+  int32_t* __restrict__ status = q.status;
   __shared__ int s_bad;
   __shared__ int64_t s_warp[kScanThreads / 32];
   __shared__ int64_t s_carry;
   pdl_wait();
   pdl_release();
+  // every index below lies in [0, E]
+  if (!MXFP4_IN_BOUNDS(q, kDbgOffsets, off, (E + 1) * 4) ||
+      !MXFP4_IN_BOUNDS(q, kDbgPadded, padded, (E + 1) * 4) ||
+      (status != nullptr && !MXFP4_IN_BOUNDS(q, kDbgStatus, status, 4)))
+    return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_bad = (off[0] != 0) || (static_cast<int64_t>(off[E]) != total_rows);
@@ -356,6 +398,22 @@ bool vec32_ok(const void* x, int64_t ldx_bytes) {
   return (reinterpret_cast<uintptr_t>(x) % 32 == 0) && (ldx_bytes % 32 == 0);
 }
 
+cudaError_t launch_offsets(const int32_t* offsets, int32_t E, int64_t total_rows,
+                           int32_t* scale_row_offsets, int32_t* status, cudaStream_t stream) {
+  OffsetsParams q{};
+  q.off = offsets;
+  q.E = E;
+  q.total_rows = total_rows;
+  q.padded = scale_row_offsets;
+  q.status = status;
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(q.dbg, kDbgOffsets, offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(q.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(q.dbg, kDbgStatus, status, status ? 4 : 0);
+#endif
+  return launch_pdl(grouped_offsets_kernel, 1, kScanThreads, 0, stream, q);
+}
+
 }  // namespace
 
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
@@ -371,6 +429,11 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   const int64_t tiles = (M + kTileRows - 1) / kTileRows;
   p.n_units = static_cast<int32_t>(tiles * p.nKT);
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(p.dbg, kDbgX, x, ((M - 1) * ldx + K) * 2);
+  debug_range(p.dbg, kDbgCodes, codes, M * (K / 2));
+  debug_range(p.dbg, kDbgScales, scales, tiles * p.nKT * kChunkBytes);
+#endif
   const bool v32 = vec32_ok(x, p.ldx_bytes);
   const auto kernel = f16 ? (v32 ? quantize_tiles_kernel<false, true, true>
                                  : quantize_tiles_kernel<false, false, true>)
@@ -383,8 +446,7 @@ cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K
                                     const int32_t* offsets, int32_t E, uint8_t* codes,
                                     uint8_t* scales, int32_t* scale_row_offsets,
                                     int32_t* status, int64_t bound_tiles, cudaStream_t stream) {
-  cudaError_t err = launch_pdl(grouped_offsets_kernel, 1, kScanThreads, 0, stream, offsets, E,
-                               total_rows, scale_row_offsets, status);
+  cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
   if (err != cudaSuccess || E == 0 || bound_tiles == 0) return err;
   QuantizeParams p{};
   p.x = static_cast<const uint8_t*>(x);
@@ -398,6 +460,13 @@ cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K
   p.offsets = offsets;
   p.padded = scale_row_offsets;
   p.E = E;
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(p.dbg, kDbgX, x, total_rows * K * 2);
+  debug_range(p.dbg, kDbgCodes, codes, total_rows * (K / 2));
+  debug_range(p.dbg, kDbgScales, scales, bound_tiles * p.nKT * kChunkBytes);
+  debug_range(p.dbg, kDbgOffsets, offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(p.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
+#endif
   const int64_t grid = bound_tiles * p.nKT;  // CTAs past the real padded total exit at once
   const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<true, true>
                                                : quantize_tiles_kernel<true, false>;
@@ -410,8 +479,7 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
                                            uint8_t* codes, uint8_t* scales,
                                            int32_t* scale_row_offsets, int32_t* status,
                                            int64_t bound_tiles, cudaStream_t stream) {
-  cudaError_t err = launch_pdl(grouped_offsets_kernel, 1, kScanThreads, 0, stream, offsets, E,
-                               total_rows, scale_row_offsets, status);
+  cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
   if (err != cudaSuccess || E == 0 || bound_tiles == 0) return err;
   QuantizeParams p{};
   p.x = static_cast<const uint8_t*>(x);
@@ -429,10 +497,28 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
   p.num_src_rows = num_src_rows;
   p.status = status;
   p.n_mtiles = static_cast<int32_t>(bound_tiles);
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(p.dbg, kDbgX, x, ((num_src_rows - 1) * ldx + K) * 2);
+  debug_range(p.dbg, kDbgCodes, codes, total_rows * (K / 2));
+  debug_range(p.dbg, kDbgScales, scales, bound_tiles * p.nKT * kChunkBytes);
+  debug_range(p.dbg, kDbgOffsets, offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(p.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(p.dbg, kDbgRowIndex, row_index, total_rows * 4);
+  debug_range(p.dbg, kDbgStatus, status, status ? 4 : 0);
+#endif
   const int64_t grid = bound_tiles * ((p.nKT + kGatherChunkTiles - 1) / kGatherChunkTiles);
   const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_gather_kernel<true>
                                                : quantize_gather_kernel<false>;
   return launch_pdl(kernel, static_cast<unsigned>(grid), kGatherThreads, 0, stream, p);
 }
+
+#ifdef MXFP4_DEBUG_BOUNDS
+unsigned int debug_violations_quantize() {
+  unsigned int v = 0, zero = 0;
+  cudaMemcpyFromSymbol(&v, g_debug_violations, sizeof v);
+  cudaMemcpyToSymbol(g_debug_violations, &zero, sizeof zero);
+  return v;
+}
+#endif
 
 }  // namespace mxfp4

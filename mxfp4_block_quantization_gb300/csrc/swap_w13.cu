@@ -66,6 +66,14 @@ struct SwapParams {
   const float* __restrict__ b2_in;
   uint16_t* __restrict__ b2_out;
   int64_t b2_numel;
+#ifdef MXFP4_DEBUG_BOUNDS
+  DebugRanges dbg;      // byte ranges of the eight buffers (bounds build)
+#endif
+};
+
+enum : int {
+  kDbgCodesIn = 0, kDbgCodesOut, kDbgScalesIn, kDbgScalesOut, kDbgB13In, kDbgB13Out, kDbgB2In,
+  kDbgB2Out
 };
 
 __device__ __forceinline__ int64_t partner_row(int64_t r, int64_t half) {
@@ -76,7 +84,8 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   return static_cast<uint16_t>(cvt_bf16x2(f, 0.0f) & 0xFFFFu);
 }
 
-__device__ __forceinline__ void half_copy_cta(const HalfCopy& hc, int b) {
+__device__ __forceinline__ void half_copy_cta(const SwapParams& p, const HalfCopy& hc, int b,
+                                              int slot_in, int slot_out) {
   const int hi = b / hc.ctas_per_half;
   const int part = b - hi * hc.ctas_per_half;
   const int64_t e = hi >> 1;
@@ -88,12 +97,12 @@ __device__ __forceinline__ void half_copy_cta(const HalfCopy& hc, int b) {
 #pragma unroll
   for (int k = 0; k < kVecPerThread; ++k) {
     const int64_t j = base + k * kThreads;
-    if (j < hc.half_vecs) v[k] = ld_stream_v4(src + j);
+    if (j < hc.half_vecs && MXFP4_IN_BOUNDS(p, slot_in, src + j, 16)) v[k] = ld_stream_v4(src + j);
   }
 #pragma unroll
   for (int k = 0; k < kVecPerThread; ++k) {
     const int64_t j = base + k * kThreads;
-    if (j < hc.half_vecs) st_stream_v4(dst + j, v[k]);
+    if (j < hc.half_vecs && MXFP4_IN_BOUNDS(p, slot_out, dst + j, 16)) st_stream_v4(dst + j, v[k]);
   }
 }
 
@@ -102,13 +111,13 @@ __global__ void __launch_bounds__(kThreads) swap_w13_kernel(const SwapParams p) 
   pdl_release();
   int b = static_cast<int>(blockIdx.x);
   if (b < p.codes.ctas) {
-    half_copy_cta(p.codes, b);
+    half_copy_cta(p, p.codes, b, kDbgCodesIn, kDbgCodesOut);
     return;
   }
   b -= p.codes.ctas;
   if (b < p.scale_ctas) {
     if (p.scale_mode == kScaleHalfCopy) {
-      half_copy_cta(p.scales, b);
+      half_copy_cta(p, p.scales, b, kDbgScalesIn, kDbgScalesOut);
       return;
     }
     const int64_t stride = static_cast<int64_t>(p.scale_ctas) * kThreads;
@@ -129,17 +138,21 @@ __global__ void __launch_bounds__(kThreads) swap_w13_kernel(const SwapParams p) 
           const int64_t q = partner_row(r, p.half);
           const int64_t src = e * p.chunk_words + ((q >> 7) * p.nKT + kt) * 128 + (q & 31) * 4 +
                               ((q & 127) >> 5);
-          val = __ldg(reinterpret_cast<const uint32_t*>(p.scales_in) + src);
+          const uint32_t* sp = reinterpret_cast<const uint32_t*>(p.scales_in) + src;
+          val = MXFP4_IN_BOUNDS(p, kDbgScalesIn, sp, 4) ? __ldg(sp) : 0u;
           const int valid = p.sK - kt * kTileBlocks;  // real scale columns in this k-tile
           if (valid < 4) val &= (1u << (8 * valid)) - 1u;
         }
-        reinterpret_cast<uint32_t*>(p.scales_out)[i] = val;
+        uint32_t* dp = reinterpret_cast<uint32_t*>(p.scales_out) + i;
+        if (MXFP4_IN_BOUNDS(p, kDbgScalesOut, dp, 4)) *dp = val;
       } else {
         const int64_t row = i / p.sK;
         const int64_t c = i - row * p.sK;
         const int64_t e = row / p.two_n;
         const int64_t r = row - e * p.two_n;
-        p.scales_out[i] = __ldg(p.scales_in + (e * p.two_n + partner_row(r, p.half)) * p.sK + c);
+        const uint8_t* sp = p.scales_in + (e * p.two_n + partner_row(r, p.half)) * p.sK + c;
+        if (MXFP4_IN_BOUNDS(p, kDbgScalesIn, sp, 1) && MXFP4_IN_BOUNDS(p, kDbgScalesOut, p.scales_out + i, 1))
+          p.scales_out[i] = __ldg(sp);
       }
     }
     return;
@@ -153,10 +166,13 @@ __global__ void __launch_bounds__(kThreads) swap_w13_kernel(const SwapParams p) 
     if (i < p.b13_numel) {
       const int64_t e = i / p.two_n;
       const int64_t j = i - e * p.two_n;
-      p.b13_out[i] = f32_to_bf16(__ldg(p.b13_in + e * p.two_n + partner_row(j, p.half)));
+      const float* bp = p.b13_in + e * p.two_n + partner_row(j, p.half);
+      if (MXFP4_IN_BOUNDS(p, kDbgB13In, bp, 4) && MXFP4_IN_BOUNDS(p, kDbgB13Out, p.b13_out + i, 2))
+        p.b13_out[i] = f32_to_bf16(__ldg(bp));
     } else {
       const int64_t k = i - p.b13_numel;
-      p.b2_out[k] = f32_to_bf16(__ldg(p.b2_in + k));
+      if (MXFP4_IN_BOUNDS(p, kDbgB2In, p.b2_in + k, 4) && MXFP4_IN_BOUNDS(p, kDbgB2Out, p.b2_out + k, 2))
+        p.b2_out[k] = f32_to_bf16(__ldg(p.b2_in + k));
     }
   }
 }
@@ -223,9 +239,35 @@ cudaError_t launch_swap_w13(const SwapArgs& a, cudaStream_t stream) {
   const int64_t bias_items = p.b13_numel + p.b2_numel;
   const int64_t bias_ctas = std::min<int64_t>((bias_items + kThreads - 1) / kThreads, sms * 2);
   const int64_t grid = code_ctas + scale_ctas + bias_ctas;
+#ifdef MXFP4_DEBUG_BOUNDS
+  {
+    const int64_t rows = static_cast<int64_t>(a.E) * a.two_n;
+    const int64_t scale_bytes =
+        a.scales_tiled ? static_cast<int64_t>(a.E) *
+                             ((a.two_n + kTileRows - 1) / kTileRows) * p.nKT * kChunkBytes
+                       : rows * sK;
+    debug_range(p.dbg, kDbgCodesIn, a.codes_in, rows * (a.K / 2));
+    debug_range(p.dbg, kDbgCodesOut, a.codes_out, rows * (a.K / 2));
+    debug_range(p.dbg, kDbgScalesIn, a.scales_in, sK > 0 ? scale_bytes : 0);
+    debug_range(p.dbg, kDbgScalesOut, a.scales_out, sK > 0 ? scale_bytes : 0);
+    debug_range(p.dbg, kDbgB13In, a.w13_bias_in, p.b13_numel * 4);
+    debug_range(p.dbg, kDbgB13Out, a.w13_bias_out, p.b13_numel * 2);
+    debug_range(p.dbg, kDbgB2In, a.w2_bias_in, p.b2_numel * 4);
+    debug_range(p.dbg, kDbgB2Out, a.w2_bias_out, p.b2_numel * 2);
+  }
+#endif
   if (grid == 0) return cudaSuccess;
   if (grid > INT_MAX / 2) return cudaErrorInvalidConfiguration;
   return launch_pdl(swap_w13_kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
+
+#ifdef MXFP4_DEBUG_BOUNDS
+unsigned int debug_violations_swap() {
+  unsigned int v = 0, zero = 0;
+  cudaMemcpyFromSymbol(&v, g_debug_violations, sizeof v);
+  cudaMemcpyToSymbol(g_debug_violations, &zero, sizeof zero);
+  return v;
+}
+#endif
 
 }  // namespace mxfp4

@@ -178,3 +178,14 @@ def test_binding_rejects_mixed_devices(lib):
     x = torch.zeros(4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         lib._device_of(x, torch.zeros(1, device="meta"))
+
+
+def test_debug_library_exports_both_headers(lib):
+    import os
+    L = ctypes.CDLL(lib.DEBUG_LIB_PATH)
+    debug_h = os.path.join(ROOT, "include", "mxfp4_debug.h")
+    text = re.sub(r"/\*.*?\*/", "", open(debug_h).read(), flags=re.S)
+    names = declared_functions() + re.findall(r"\b(mxfp4_\w+)\s*\(", text)
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    assert not hasattr(ctypes.CDLL(lib.LIB_PATH), "mxfp4_debug_bounds_violations")
