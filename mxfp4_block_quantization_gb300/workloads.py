@@ -58,6 +58,7 @@ class GroupedInput:
     num_experts: int
     x_tokens: torch.Tensor   # BF16 [tokens, K], the token rows before dispatch
     row_index: torch.Tensor  # int32 [tokens * top_k] on `device`: token of each row
+    dest_rows: torch.Tensor  # int32 [tokens, top_k] on `device`: row of route j of token t
 
 
 def moe_grouped(seed: int = 2, tokens: int = 16384, top_k: int = 8, num_experts: int = 384,
@@ -66,7 +67,8 @@ def moe_grouped(seed: int = 2, tokens: int = 16384, top_k: int = 8, num_experts:
     distinct experts drawn uniformly (the first ``top_k`` of a random
     ordering); its N(0,1) hidden row is duplicated once per route; rows are
     stable-sorted by expert (then token); int32 offsets delimit the experts'
-    segments."""
+    segments.  ``row_index`` (row -> token) and ``dest_rows`` (token, route ->
+    row) are the two directions of the same dispatch permutation."""
     g_route = _gen(seed, "cpu")
     keys = torch.rand((tokens, num_experts), generator=g_route)
     experts = torch.topk(keys, top_k, dim=1).indices.reshape(-1)          # [T*k]
@@ -78,10 +80,13 @@ def moe_grouped(seed: int = 2, tokens: int = 16384, top_k: int = 8, num_experts:
     offsets[1:] = torch.cumsum(counts, 0)
     x_tok = normal_bf16((tokens, K), seed + 1000, device=device)
     row_index = token_of_row.to(torch.int32).to(device)
+    dest = torch.empty(tokens * top_k, dtype=torch.int64)
+    dest[order] = torch.arange(tokens * top_k)
+    dest_rows = dest.view(tokens, top_k).to(torch.int32).to(device)
     x = x_tok.index_select(0, token_of_row.to(device))
     return GroupedInput(x=x, offsets=offsets.to(torch.int32).to(device),
                         token_of_row=token_of_row, num_experts=num_experts, x_tokens=x_tok,
-                        row_index=row_index)
+                        row_index=row_index, dest_rows=dest_rows)
 
 
 @dataclass

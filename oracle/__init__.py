@@ -88,6 +88,9 @@ def lib():
         L.orc_nvfp4_quantize.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_float, _u8p, _u8p]
         L.orc_nvfp4_dequantize.restype = None
         L.orc_nvfp4_dequantize.argtypes = [_u8p, _u8p, _i64, _i64, ctypes.c_float, _u16p]
+        L.orc_quantize_grouped_scatter.restype = ctypes.c_int
+        L.orc_quantize_grouped_scatter.argtypes = [_u16p, _i64, _i64, _i64, _i32p, ctypes.c_int32,
+                                                   _i64, _i32p, ctypes.c_int32, _u8p, _u8p, _i32p]
         L.orc_quantize_grouped_gather.restype = ctypes.c_int
         L.orc_quantize_grouped_gather.argtypes = [_u16p, _i64, _i64, _i64, _i32p, _i64, _i32p,
                                                   ctypes.c_int32, _u8p, _u8p, _i32p]
@@ -280,6 +283,34 @@ def quantize_grouped_gather(xbits: np.ndarray, row_index: np.ndarray, offsets: n
     rc = lib().orc_quantize_grouped_gather(_p(x, _u16p), n_src, K, K, _p(idx, _i32p), total,
                                            _p(off, _i32p), E, _p(codes, _u8p), _p(scales, _u8p),
                                            _p(sro, _i32p))
+    return rc, codes, scales, sro
+
+
+def quantize_grouped_scatter(xbits: np.ndarray, dest_rows: np.ndarray, offsets: np.ndarray,
+                             total_rows: int, codes=None, scales=None):
+    """Step 6 with the dispatch as a scatter: route j of token t is row
+    dest_rows[t, j] of the expert-sorted batch (-1: not dispatched).
+    Returns (rc, codes, scales, scale_row_offsets); rc is 0, -6 (bad offsets)
+    or -7 (an entry outside [-1, total_rows), skipped).  `codes` / `scales`,
+    when given, are the buffers' previous contents (rows that no route
+    targets keep them); by default they start zeroed."""
+    x = _c(xbits, np.uint16)
+    dst = _c(dest_rows, np.int32)
+    off = _c(offsets, np.int32)
+    T, K = x.shape
+    top_k = dst.shape[1] if dst.ndim == 2 else 1
+    assert dst.size == T * top_k
+    E = off.size - 1
+    codes = (np.zeros((total_rows, K // 2), np.uint8) if codes is None
+             else np.array(codes, np.uint8, copy=True).reshape(total_rows, K // 2))
+    nsb = max(grouped_scale_bytes_bound(total_rows, E, K), 1)
+    scales = (np.zeros(nsb, np.uint8) if scales is None
+              else np.array(scales, np.uint8, copy=True).ravel())
+    assert scales.size >= grouped_scale_bytes_bound(total_rows, E, K)
+    sro = np.zeros(E + 1, np.int32)
+    rc = lib().orc_quantize_grouped_scatter(_p(x, _u16p), T, K, K, _p(dst, _i32p), top_k,
+                                            total_rows, _p(off, _i32p), E, _p(codes, _u8p),
+                                            _p(scales, _u8p), _p(sro, _i32p))
     return rc, codes, scales, sro
 
 

@@ -329,6 +329,65 @@ int orc_quantize_grouped_gather(const uint16_t* x, int64_t num_src_rows, int64_t
   return bad ? -7 : 0;
 }
 
+/* Step 6 with the MoE dispatch as a scatter ([PR43557] item 3: the
+ * experts-quant input is the routed, expert-sorted activations), in the form a
+ * router's sort produces: route j of token t lands on row
+ * dest_rows[t * top_k + j] of the expert-sorted batch, -1 meaning the route is
+ * not dispatched.  Plainly: place every token row on its destination rows,
+ * run the grouped quantize above on that batch, then keep the rows some route
+ * targets (their codes and the scale bytes of their padded rows) and every
+ * segment's pad rows (zero scale bytes); rows no route targets are left as
+ * they were.  An entry outside [-1, total_rows) is skipped and gives -7; bad
+ * offsets give -6 and nothing is written but the -1 scale row offsets. */
+int orc_quantize_grouped_scatter(const uint16_t* x, int64_t num_tokens, int64_t K, int64_t ldx,
+                                 const int32_t* dest_rows, int32_t top_k, int64_t total_rows,
+                                 const int32_t* offsets, int32_t E, uint8_t* codes,
+                                 uint8_t* scales, int32_t* scale_row_offsets) {
+  int bad = 0;
+  uint16_t* g = (uint16_t*)calloc((size_t)(total_rows * K) + 1, sizeof(uint16_t));
+  uint8_t* hit = (uint8_t*)calloc((size_t)total_rows + 1, 1);
+  for (int64_t t = 0; t < num_tokens; ++t)
+    for (int32_t j = 0; j < top_k; ++j) {
+      int64_t d = dest_rows[t * top_k + j];
+      if (d == -1) continue;
+      if (d < -1 || d >= total_rows) {
+        bad = 1;
+        continue;
+      }
+      memcpy(g + d * K, x + t * ldx, (size_t)K * sizeof(uint16_t));
+      hit[d] = 1;
+    }
+  int64_t sK = K / 32;
+  int64_t nkt = (sK + 3) / 4;
+  int64_t padded_sK = nkt * 4;
+  /* the segments' padded rows never exceed total_rows + 127 E */
+  int64_t bound_rows = (total_rows + 127 * (int64_t)(E > 0 ? E : 0)) / 128 * 128 + 128;
+  uint8_t* tc = (uint8_t*)calloc((size_t)(total_rows * (K / 2)) + 1, 1);
+  uint8_t* ts = (uint8_t*)calloc((size_t)(bound_rows * padded_sK) + 1, 1);
+  int rc = orc_quantize_grouped(g, total_rows, K, offsets, E, tc, ts, scale_row_offsets);
+  if (rc == 0) {
+    for (int32_t e = 0; e < E; ++e) {
+      int64_t n = (int64_t)offsets[e + 1] - offsets[e];
+      int64_t base = (int64_t)scale_row_offsets[e] * padded_sK;
+      for (int64_t prow = 0; prow < (n + 127) / 128 * 128; ++prow) {
+        int64_t d = offsets[e] + prow;
+        if (prow < n && !hit[d]) continue; /* untargeted: left as it was */
+        if (prow < n) memcpy(codes + d * (K / 2), tc + d * (K / 2), (size_t)(K / 2));
+        for (int64_t c = 0; c < padded_sK; ++c) {
+          int64_t i = base + tiled_index(prow, c, nkt);
+          scales[i] = ts[i];
+        }
+      }
+    }
+  }
+  free(g);
+  free(hit);
+  free(tc);
+  free(ts);
+  if (rc != 0) return rc;
+  return bad ? -7 : 0;
+}
+
 /* Step 7 — dequantize: for each element, its nibble and its block's scale
  * byte (read back through the tiled layout) give E2M1 value * 2^(s-127),
  * rounded once to BF16.  [PR46915] "Motivation" (FP4 -> BF16 table);

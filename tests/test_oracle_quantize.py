@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 import torch
 
+from conftest import load_golden
 from mxfp4_block_quantization_gb300 import workloads as W
 
 
@@ -150,3 +151,122 @@ def test_grouped_gather_bad_index_zero_row(orc):
     rc2, c2, s2, _ = orc.quantize_grouped(g, off)
     assert np.array_equal(c, c2) and np.array_equal(s, s2)
     assert not c[2].any() and not c[4].any()
+
+
+def test_grouped_scatter_equals_gather_of_inverse(orc):
+    """The dispatch as a scatter (token, route -> row) with every row
+    targeted equals the gather form with the inverse map (row -> token) and
+    the grouped quantize of the explicitly permuted matrix."""
+    g = W.moe_grouped(seed=2, tokens=80, top_k=3, num_experts=7, K=192)
+    xt = W.bf16_bits(g.x_tokens)
+    idx = g.row_index.numpy()
+    dst = g.dest_rows.numpy()
+    off = g.offsets.numpy()
+    assert np.array_equal(idx[dst], np.repeat(np.arange(80), 3).reshape(80, 3))
+    rc, c, s, sro = orc.quantize_grouped_scatter(xt, dst, off, idx.size)
+    rc2, c2, s2, sro2 = orc.quantize_grouped_gather(xt, idx, off)
+    rc3, c3, s3, sro3 = orc.quantize_grouped(xt[idx], off)
+    assert rc == rc2 == rc3 == 0
+    for a, b in ((c, c2), (s, s2), (sro, sro2), (c, c3), (s, s3)):
+        assert np.array_equal(a, b)
+
+
+def _packed(nibbles):
+    n = np.asarray(nibbles, np.uint8)
+    return (n[0::2] | (n[1::2] << 4)).astype(np.uint8)
+
+
+def _golden_block(blk):
+    x = np.zeros(32, np.uint16)
+    x[: len(blk["x"])] = [int(h, 16) for h in blk["x"]]
+    nib = np.zeros(32, np.uint8)
+    nib[: len(blk["codes"])] = [int(c, 16) for c in blk["codes"]]
+    return x, _packed(nib), blk["s"]
+
+
+def test_grouped_scatter_worked_example(orc):
+    """Two tokens (worked blocks A and B), two routes each, two experts of two
+    rows, K = 32.  Token A goes to rows 1 and 2, token B to rows 0 and 3
+    (route 1 of B dropped in the second call).  Expected bytes written out by
+    hand: expert 1's scales start at padded row 128 (byte 512); padded row r
+    of a segment with one k-tile holds its 4 scale bytes at (r % 32) * 16 +
+    ((r % 128) // 32) * 4; codes rows are the blocks' packed codes."""
+    g = load_golden("e8m0_e2m1_worked_blocks.json")["blocks"]
+    xa, pa, sa = _golden_block(g[0])
+    xb, pb, sb = _golden_block(g[1])
+    x = np.stack([xa, xb])
+    off = np.array([0, 2, 4], np.int32)
+    for dropped in (False, True):
+        dst = np.array([[1, 2], [0, -1 if dropped else 3]], np.int32)
+        codes0 = np.full((4, 16), 0xA5, np.uint8)
+        scales0 = np.full(1024, 0xA5, np.uint8)
+        rc, c, s, sro = orc.quantize_grouped_scatter(x, dst, off, 4, codes0, scales0)
+        assert rc == 0 and list(sro) == [0, 128, 256]
+        want_c = np.stack([pb, pa, pa, pb])
+        want_s = np.zeros(1024, np.uint8)
+        want_s[0], want_s[16], want_s[512], want_s[528] = sb, sa, sa, sb
+        if dropped:
+            want_c[3] = 0xA5
+            want_s[528:532] = 0xA5
+        assert np.array_equal(c, want_c)
+        assert np.array_equal(s, want_s), np.nonzero(s != want_s)
+
+
+def test_grouped_scatter_untargeted_rows_untouched(orc):
+    """Dropped routes (-1) leave their rows as they were, codes and scale
+    bytes; every targeted row and every pad row is as in the full result."""
+    g = W.moe_grouped(seed=6, tokens=150, top_k=4, num_experts=9, K=160)
+    xt = W.bf16_bits(g.x_tokens)
+    idx = g.row_index.numpy()
+    dst = g.dest_rows.numpy().copy()
+    off = g.offsets.numpy()
+    total = idx.size
+    rng = np.random.default_rng(0)
+    drop = rng.random(dst.shape) < 0.2
+    dropped_rows = dst[drop]
+    dst[drop] = -1
+    nsb = orc.grouped_scale_bytes_bound(total, 9, 160)
+    codes0 = rng.integers(0, 256, (total, 80), dtype=np.uint8)
+    scales0 = rng.integers(0, 256, nsb, dtype=np.uint8)
+    rc, c, s, sro = orc.quantize_grouped_scatter(xt, dst, off, total, codes0, scales0)
+    rc_f, c_f, s_f, _ = orc.quantize_grouped(xt[idx], off)
+    assert rc == 0 and rc_f == 0
+    kept = np.setdiff1d(np.arange(total), dropped_rows)
+    assert np.array_equal(c[kept], c_f[kept])
+    assert np.array_equal(c[dropped_rows], codes0[dropped_rows])
+    # scale bytes: untile each segment from both buffers and compare per row
+    sK = 5
+    for e in range(9):
+        n = int(off[e + 1] - off[e])
+        pad_n = (n + 127) // 128 * 128
+        seg = slice(int(sro[e]) * 8, (int(sro[e]) + pad_n) * 8)
+        got = orc.untile(s[seg], pad_n, 8)
+        full = orc.untile(s_f[seg], pad_n, 8)
+        before = orc.untile(scales0[seg], pad_n, 8)
+        rows = np.arange(pad_n)
+        untargeted = np.isin(off[e] + rows, dropped_rows) & (rows < n)
+        assert np.array_equal(got[~untargeted], full[~untargeted])
+        assert not full[rows >= n].any() and not full[:, sK:].any()
+        assert np.array_equal(got[untargeted], before[untargeted])
+
+
+def test_grouped_scatter_bad_entries(orc):
+    """An entry outside [-1, total_rows) is skipped (as if -1) and reported."""
+    g = W.moe_grouped(seed=7, tokens=40, top_k=2, num_experts=3, K=64)
+    xt = W.bf16_bits(g.x_tokens)
+    dst = g.dest_rows.numpy().copy()
+    off = g.offsets.numpy()
+    total = g.row_index.numel()
+    bad = dst.copy()
+    bad[3, 1] = total
+    bad[7, 0] = -2
+    ok = dst.copy()
+    ok[3, 1] = -1
+    ok[7, 0] = -1
+    rc, c, s, _ = orc.quantize_grouped_scatter(xt, bad, off, total)
+    rc2, c2, s2, _ = orc.quantize_grouped_scatter(xt, ok, off, total)
+    assert rc == -7 and rc2 == 0
+    assert np.array_equal(c, c2) and np.array_equal(s, s2)
+    rc3, _, _, sro = orc.quantize_grouped_scatter(xt, dst, np.array([0, 50, 40, total], np.int32),
+                                                  total)
+    assert rc3 == -6 and (sro == -1).all()
