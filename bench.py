@@ -384,6 +384,16 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     e_["unfused_us_per_call"] = round(ms_unfused * 1e3, 2)
     e_["speedup_vs_unfused"] = round(ms_unfused / ms_fused, 3)
     out["grouped_gather_moe_16384tok_top8_E384"] = e_
+    # the same dispatch given token -> rows (the router's sort output): each
+    # token row read and quantized once, its codes written to its 8 rows
+    ms_sc = time_launches(
+        lambda i: mx.mxfp4_quantize_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets, total,
+                                                    codes, scales, sro, st, stream), 30, stream)
+    e_ = entry(nb, ms_sc, 2, "bytes = token rows read once + route->row map + codes + scales; "
+               "pad CTAs zero the segments' pad scale rows in the same launch")
+    e_["speedup_vs_unfused"] = round(ms_unfused / ms_sc, 3)
+    e_["speedup_vs_fused_gather"] = round(ms_fused / ms_sc, 3)
+    out["grouped_scatter_moe_16384tok_top8_E384"] = e_
     del g, codes, scales, xg
 
     # expert weights: w13 [128, 1536, 2048], w2 [128, 2048, 768], then the swap

@@ -161,6 +161,39 @@ int mxfp4_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K
                                   uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
                                   void* stream);
 
+/* mxfp4_quantize_grouped_scatter — the same dispatch given in the direction
+ * a router's sort produces it (token, route -> row): each token row of x is
+ * read and quantized once, and its codes and scale bytes are written to every
+ * row its routes land on.  Where every row 0..total_rows-1 is targeted
+ * exactly once, the result equals mxfp4_quantize_grouped_gather with the
+ * inverse map.  [PR43557] "Implementation breakdown" item 3 (experts quant of
+ * the routed, expert-sorted activations).
+ *
+ * x                  BF16 token rows [num_tokens, K], row stride ldx elements
+ *                    (ldx >= K, ldx % 8 == 0), 16-byte aligned.
+ * dest_rows          DEVICE int32 [num_tokens, top_k], row-major: the row of
+ *                    the expert-sorted batch that route j of token t lands
+ *                    on, or -1 for a route that is not dispatched.
+ *                    1 <= top_k <= MXFP4_SCATTER_MAX_TOP_K.  No row may be
+ *                    the target of two different tokens (that row's bytes
+ *                    would be unspecified).
+ * expert_offsets, E, codes, scales, scale_row_offsets: as in
+ *                    mxfp4_quantize_grouped, over the total_rows rows of the
+ *                    expert-sorted batch.  Rows that no route targets are not
+ *                    written (neither their codes nor their scale bytes); the
+ *                    pad rows of every segment get zero scale bytes.
+ * status             DEVICE int32, output, may be NULL: MXFP4_OK,
+ *                    MXFP4_EOFFSETS (as in mxfp4_quantize_grouped, nothing
+ *                    else written), or MXFP4_EINDEX when some entry is
+ *                    outside [-1, total_rows): such entries are skipped.
+ */
+#define MXFP4_SCATTER_MAX_TOP_K 32
+int mxfp4_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K, int64_t ldx,
+                                   const int32_t* dest_rows, int32_t top_k, int64_t total_rows,
+                                   const int32_t* expert_offsets, int32_t E, uint8_t* codes,
+                                   uint8_t* scales, int32_t* scale_row_offsets,
+                                   int32_t* status, void* stream);
+
 /* mxfp4_dequantize — packed codes + tiled scales -> BF16 [M, K].
  *
  * The inverse mapping of the format ([PR46915] "Motivation": FP4 -> BF16

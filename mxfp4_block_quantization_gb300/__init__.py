@@ -30,7 +30,8 @@ __all__ = [
     "mxfp4_status_string", "mxfp4_version", "quantize", "quantize_grouped", "dequantize",
     "swap_w13", "MXFP4_OK", "MXFP4_EINVAL", "MXFP4_EALIGN", "MXFP4_ESHAPE", "MXFP4_EALIAS",
     "MXFP4_ECUDA", "MXFP4_EOFFSETS", "MXFP4_EINDEX", "mxfp4_quantize_grouped_gather",
-    "quantize_grouped_gather", "mxfp4_quantize_f16", "mxfp4_nvfp4_scale_bytes",
+    "quantize_grouped_gather", "mxfp4_quantize_grouped_scatter", "quantize_grouped_scatter",
+    "MXFP4_SCATTER_MAX_TOP_K", "mxfp4_quantize_f16", "mxfp4_nvfp4_scale_bytes",
     "mxfp4_quantize_nvfp4", "mxfp4_dequantize_nvfp4", "quantize_nvfp4", "dequantize_nvfp4",
 ]
 
@@ -39,6 +40,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb
 # counted when out of range); see _load() and mxfp4_debug_bounds_violations.
 DEBUG_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300_debug.so")
 
+MXFP4_SCATTER_MAX_TOP_K = 32
 MXFP4_OK = 0
 MXFP4_EINVAL = -1
 MXFP4_EALIGN = -2
@@ -77,6 +79,9 @@ def _load(path=LIB_PATH):
     L.mxfp4_quantize_grouped_gather.restype = ctypes.c_int
     L.mxfp4_quantize_grouped_gather.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, vp, vp,
                                                 vp, vp]
+    L.mxfp4_quantize_grouped_scatter.restype = ctypes.c_int
+    L.mxfp4_quantize_grouped_scatter.argtypes = [vp, i64, i64, i64, vp, i32, i64, vp, i32, vp,
+                                                 vp, vp, vp, vp]
     L.mxfp4_dequantize.restype = ctypes.c_int
     L.mxfp4_dequantize.argtypes = [vp, vp, i64, i64, vp, vp]
     L.mxfp4_swap_w13.restype = ctypes.c_int
@@ -225,6 +230,33 @@ def mxfp4_quantize_grouped_gather(x, row_index, expert_offsets, codes, scales, s
             _ptr(status), _stream(stream, x.device)), "mxfp4_quantize_grouped_gather")
 
 
+def mxfp4_quantize_grouped_scatter(x, dest_rows, expert_offsets, total_rows: int, codes, scales,
+                                   scale_row_offsets, status=None, stream=None) -> None:
+    """Grouped quantize with the dispatch given token -> rows: route j of
+    token t is row ``dest_rows[t, j]`` (int32 device [T, top_k], -1 = not
+    dispatched) of the ``total_rows``-row expert-sorted batch.  Each token
+    row is read and quantized once; rows no route targets are not written."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("dest_rows", dest_rows, torch.int32)
+    _need_cuda("expert_offsets", expert_offsets, torch.int32)
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    _need_cuda("scale_row_offsets", scale_row_offsets, torch.int32)
+    _need_cuda("status", status, torch.int32)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    if dest_rows.dim() != 2 or dest_rows.shape[0] != x.shape[0] or not dest_rows.is_contiguous():
+        raise ValueError("dest_rows must be a contiguous [num_tokens, top_k] tensor")
+    T, K = x.shape
+    E = expert_offsets.numel() - 1
+    with torch.cuda.device(_device_of(x, dest_rows, expert_offsets, codes, scales,
+                                      scale_row_offsets, status)):
+        _check(_lib.mxfp4_quantize_grouped_scatter(
+            _ptr(x), T, K, x.stride(0), _ptr(dest_rows), dest_rows.shape[1], int(total_rows),
+            _ptr(expert_offsets), E, _ptr(codes), _ptr(scales), _ptr(scale_row_offsets),
+            _ptr(status), _stream(stream, x.device)), "mxfp4_quantize_grouped_scatter")
+
+
 def mxfp4_dequantize(codes, scales, M: int, K: int, y, stream=None) -> None:
     """``codes`` [M, K/2] + tiled ``scales`` -> BF16 ``y`` [M, K] (contiguous)."""
     _need_cuda("codes", codes, torch.uint8)
@@ -331,6 +363,25 @@ def quantize_grouped_gather(x, row_index, expert_offsets, stream=None):
     sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
     status = torch.empty(1, dtype=torch.int32, device=dev)
     mxfp4_quantize_grouped_gather(x, row_index, expert_offsets, codes, scales, sro, status, stream)
+    return codes, scales, sro, status
+
+
+def quantize_grouped_scatter(x, dest_rows, expert_offsets, total_rows=None, stream=None):
+    """Returns (codes, scales, scale_row_offsets, status) of the expert-sorted
+    batch that ``dest_rows`` dispatches ``x`` into.  ``total_rows`` defaults
+    to ``dest_rows.numel()`` (every route dispatched); rows that no route
+    targets come back zero."""
+    K = x.shape[1]
+    total = dest_rows.numel() if total_rows is None else int(total_rows)
+    E = expert_offsets.numel() - 1
+    dev = x.device
+    codes = torch.zeros((total, K // 2), dtype=torch.uint8, device=dev)
+    scales = torch.zeros(max(mxfp4_grouped_scale_bytes_bound(total, E, K), 16), dtype=torch.uint8,
+                         device=dev)
+    sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    status = torch.empty(1, dtype=torch.int32, device=dev)
+    mxfp4_quantize_grouped_scatter(x, dest_rows, expert_offsets, total, codes, scales, sro, status,
+                                   stream)
     return codes, scales, sro, status
 
 

@@ -31,6 +31,12 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
                                            uint8_t* codes, uint8_t* scales,
                                            int32_t* scale_row_offsets, int32_t* status,
                                            int64_t bound_tiles, cudaStream_t stream);
+cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
+                                            int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                            int64_t total_rows, const int32_t* offsets, int32_t E,
+                                            uint8_t* codes, uint8_t* scales,
+                                            int32_t* scale_row_offsets, int32_t* status,
+                                            int64_t bound_tiles, cudaStream_t stream);
 
 // NVFP4 (16-element blocks, E4M3 scales, device global scale).
 cudaError_t launch_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,

@@ -16,7 +16,9 @@
 // form one 32-element block, reduced with one xor-shuffle.  All four passes'
 // loads are issued before any compute (32 KB in flight per CTA, four to five
 // CTAs per SM).  The fused-gather variant (quantize_gather_kernel) keeps one
-// 128-row tile per CTA but walks a chunk of k-tiles.  Launches use
+// 128-row tile per CTA but walks a chunk of k-tiles; the scatter variant
+// (quantize_scatter_kernel) reads 128 token rows once and writes each row's
+// codes and scale words to all the rows its routes land on.  Launches use
 // programmatic dependent launch, so a grid is already resident when its
 // predecessor in the stream drains.
 #include <cstdint>
@@ -314,6 +316,162 @@ __global__ void __launch_bounds__(kGatherThreads) quantize_gather_kernel(const Q
   }
 }
 
+// Fused dispatch scatter: route j of token t lands on row dest_rows[t][j] of
+// the expert-sorted batch.  The first E CTAs zero the scale bytes of expert
+// e's pad rows.  Every other CTA (256 threads, the dense lane mapping) owns
+// 128 token rows and a chunk of kScatterChunkTiles k-tiles: it resolves the
+// tile's 128 x top_k destinations once (code row, and padded scale row from
+// the destination's segment) into shared memory, then per k-tile loads the
+// token rows once, quantizes them once, and stores each lane's 8 code bytes
+// to every destination row; the tile's 128 scale words (4 bytes of a row
+// and k-tile) are staged in shared memory and stored once per destination.
+// DRAM traffic is the algorithmic one: each token row read once, each output
+// byte written once.  CTAs run m-tile-major, so the chunks of one token tile
+// complete the destination rows' 128-byte lines back to back.
+constexpr int kScatterChunkTiles = 4;
+
+struct ScatterParams {
+  const uint8_t* __restrict__ x;          // BF16 token rows
+  int64_t ldx_bytes;                      // token row stride in bytes
+  int64_t num_tokens;
+  const int32_t* __restrict__ dest_rows;  // [num_tokens, top_k] row of every route, -1 = none
+  int32_t top_k;
+  int32_t E;
+  int64_t total_rows;                     // rows of the expert-sorted batch
+  int64_t code_ld;                        // K/2
+  uint8_t* __restrict__ codes;
+  uint8_t* __restrict__ scales;
+  const int32_t* __restrict__ offsets;    // [E+1] row offsets of the segments
+  const int32_t* __restrict__ padded;     // [E+1] padded row starts
+  int32_t* status;                        // may be NULL
+  int32_t sK;
+  int32_t nKT;
+#ifdef MXFP4_DEBUG_BOUNDS
+  DebugRanges dbg;                        // slots as in QuantizeParams (kDbgRowIndex: dest_rows)
+#endif
+};
+
+template <bool kVec32>
+__global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const ScatterParams p) {
+  constexpr int kRowsPerPass = rows_per_pass(kThreads);
+  constexpr int kPasses = passes(kThreads);
+  extern __shared__ int32_t s_route[];                // [top_k][128] code rows, then [top_k][128] padded rows
+  __shared__ __align__(16) uint32_t s_words[2][kTileRows];
+
+  pdl_wait();
+  pdl_release();
+
+  if (!MXFP4_IN_BOUNDS(p, kDbgPadded, p.padded, (p.E + 1) * 4) ||
+      !MXFP4_IN_BOUNDS(p, kDbgOffsets, p.offsets, (p.E + 1) * 4))
+    return;
+  const int total_padded = __ldg(p.padded + p.E);
+  if (total_padded < 0) return;  // rejected offsets
+
+  if (static_cast<int>(blockIdx.x) < p.E) {
+    // pad rows [n, ceil128(n)) of expert e: zero scale words, row-fastest
+    const int e = blockIdx.x;
+    const int n = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+    const int npad = ((n + kTileRows - 1) / kTileRows) * kTileRows - n;
+    const int P0 = __ldg(p.padded + e) + n;
+    for (int i = threadIdx.x; i < npad * p.nKT; i += kThreads) {
+      const int kt = i / npad;
+      const int prow = P0 + (i - kt * npad);
+      uint32_t* wp = reinterpret_cast<uint32_t*>(
+          p.scales + (static_cast<int64_t>(prow >> 7) * p.nKT + kt) * kChunkBytes +
+          (prow & 31) * 16 + ((prow & 127) >> 5) * 4);
+      if (MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4)) *wp = 0u;
+    }
+    return;
+  }
+
+  const int unit = blockIdx.x - p.E;
+  const int n_chunks = (p.nKT + kScatterChunkTiles - 1) / kScatterChunkTiles;
+  const int mt = unit / n_chunks;
+  const int kc = unit - mt * n_chunks;
+  const int64_t t0 = static_cast<int64_t>(mt) * kTileRows;
+  const int64_t left = p.num_tokens - t0;
+  const int ntok = static_cast<int>(left < kTileRows ? left : kTileRows);
+  const int top_k = p.top_k;
+  int32_t* const s_code_row = s_route;
+  int32_t* const s_pad_row = s_route + top_k * kTileRows;
+
+  // destinations of the tile's routes; entry i = (token t0 + i / top_k, route i % top_k)
+  bool bad = false;
+  for (int i = threadIdx.x; i < kTileRows * top_k; i += kThreads) {
+    const int lt = i / top_k;
+    const int j = i - lt * top_k;
+    int32_t d = -1, prow = -1;
+    if (lt < ntok) {
+      const int32_t* dp = p.dest_rows + t0 * top_k + i;
+      const int32_t v = MXFP4_IN_BOUNDS(p, kDbgRowIndex, dp, 4) ? __ldg(dp) : -1;
+      if (v >= 0 && v < p.total_rows) {
+        const int e = find_segment(p.offsets, p.E, v, static_cast<int>(p.total_rows));
+        d = v;
+        prow = __ldg(p.padded + e) + (v - __ldg(p.offsets + e));
+      } else {
+        bad |= v != -1;
+      }
+    }
+    s_code_row[j * kTileRows + lt] = d;
+    s_pad_row[j * kTileRows + lt] = prow;
+  }
+  if (bad && p.status != nullptr && MXFP4_IN_BOUNDS(p, kDbgStatus, p.status, 4))
+    atomicExch(p.status, MXFP4_EINDEX);
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & (kLanesPerRow - 1);
+  const int blk = sub >> 1;
+  const int lr0 = warp * (32 / kLanesPerRow) + (lane >> 3);
+  const int lim = ntok - lr0;
+  const uint8_t* xrow = p.x + (t0 + lr0) * p.ldx_bytes + sub * (kElems * 2);
+  const int64_t ldx_pass = p.ldx_bytes * kRowsPerPass;
+  const int kt0 = kc * kScatterChunkTiles;
+  const int kt_end = kt0 + kScatterChunkTiles < p.nKT ? kt0 + kScatterChunkTiles : p.nKT;
+  int buf = 0;
+  for (int kt = kt0; kt < kt_end; ++kt) {
+    const bool col_ok = kt * kTileBlocks + blk < p.sK;
+    const uint8_t* xp = xrow + static_cast<int64_t>(kt) * (kTileCols * 2);
+    uint4 v[kPasses][2];
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
+      if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgX, xp + i * ldx_pass, 32))
+        load32<kVec32>(xp + i * ldx_pass, v[i]);
+    }
+    uint2 code[kPasses];
+    uint8_t* const words = reinterpret_cast<uint8_t*>(s_words[buf]);
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      const uint32_t s = lane_block_scale<false>(v[i]);
+      if ((lane & 1) == 0) words[(lr0 + kRowsPerPass * i) * 4 + blk] = static_cast<uint8_t>(s);
+      code[i] = lane_codes<false>(v[i], s);
+    }
+    const int64_t col = static_cast<int64_t>(kt) * (kTileCols / 2) + sub * (kElems / 2);
+    if (col_ok) {
+      for (int j = 0; j < top_k; ++j) {
+#pragma unroll
+        for (int i = 0; i < kPasses; ++i) {
+          const int32_t d = s_code_row[j * kTileRows + lr0 + kRowsPerPass * i];
+          uint8_t* const cp = p.codes + static_cast<int64_t>(d) * p.code_ld + col;
+          if (d >= 0 && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 8)) st_stream_v2(cp, code[i]);
+        }
+      }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kTileRows * top_k; i += kThreads) {
+      const int32_t prow = s_pad_row[i];
+      if (prow < 0) continue;
+      uint32_t* const wp = reinterpret_cast<uint32_t*>(
+          p.scales + (static_cast<int64_t>(prow >> 7) * p.nKT + kt) * kChunkBytes +
+          (prow & 31) * 16 + ((prow & 127) >> 5) * 4);
+      if (MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4)) st_stream_u32(wp, s_words[buf][i & (kTileRows - 1)]);
+    }
+    buf ^= 1;
+  }
+}
+
 // Validates 0 = o[0] <= o[1] <= ... <= o[E] = total_rows and writes the
 // padded row starts P[e] = sum_{e'<e} ceil(n_e'/128)*128 (P[E] = total).
 // One CTA of 1024 threads; a block-wide scan per 1024 segments.
@@ -510,6 +668,48 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
   const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_gather_kernel<true>
                                                : quantize_gather_kernel<false>;
   return launch_pdl(kernel, static_cast<unsigned>(grid), kGatherThreads, 0, stream, p);
+}
+
+cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
+                                            int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                            int64_t total_rows, const int32_t* offsets, int32_t E,
+                                            uint8_t* codes, uint8_t* scales,
+                                            int32_t* scale_row_offsets, int32_t* status,
+                                            int64_t bound_tiles, cudaStream_t stream) {
+  cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
+  if (err != cudaSuccess || E == 0 || K == 0) return err;
+  ScatterParams p{};
+  p.x = static_cast<const uint8_t*>(x);
+  p.ldx_bytes = ldx * 2;
+  p.num_tokens = num_tokens;
+  p.code_ld = K / 2;
+  p.codes = codes;
+  p.scales = scales;
+  p.sK = static_cast<int32_t>(K / kBlock);
+  p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
+  p.offsets = offsets;
+  p.padded = scale_row_offsets;
+  p.E = E;
+  p.status = status;
+  p.dest_rows = dest_rows;
+  p.top_k = top_k;
+  p.total_rows = total_rows;
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(p.dbg, kDbgX, x, num_tokens > 0 ? ((num_tokens - 1) * ldx + K) * 2 : 0);
+  debug_range(p.dbg, kDbgCodes, codes, total_rows * (K / 2));
+  debug_range(p.dbg, kDbgScales, scales, bound_tiles * p.nKT * kChunkBytes);
+  debug_range(p.dbg, kDbgOffsets, offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(p.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(p.dbg, kDbgRowIndex, dest_rows, num_tokens * top_k * 4);
+  debug_range(p.dbg, kDbgStatus, status, status ? 4 : 0);
+#endif
+  const int64_t token_tiles = (num_tokens + kTileRows - 1) / kTileRows;
+  const int64_t grid =
+      E + token_tiles * ((p.nKT + kScatterChunkTiles - 1) / kScatterChunkTiles);
+  const size_t smem = static_cast<size_t>(top_k) * kTileRows * 2 * sizeof(int32_t);
+  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_scatter_kernel<true>
+                                               : quantize_scatter_kernel<false>;
+  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, smem, stream, p);
 }
 
 #ifdef MXFP4_DEBUG_BOUNDS

@@ -149,6 +149,34 @@ def test_grouped_gather_validation(lib):
     assert call(sro=A + 64) == lib.MXFP4_EALIAS              # offsets out overlap x
 
 
+def test_grouped_scatter_validation(lib):
+    g = lib._lib.mxfp4_quantize_grouped_scatter
+    # x, T, K, ldx, dest, top_k, total, off, E, codes, scales, sro, status, stream
+    ok = [A, 50, 64, 64, 2 * A, 8, 400, 3 * A, 2, 4 * A, 5 * A, 6 * A, None, None]
+
+    def call(**kw):
+        names = ["x", "T", "K", "ldx", "dst", "k", "tot", "off", "E", "c", "s", "sro", "st",
+                 "strm"]
+        a = dict(zip(names, ok))
+        a.update(kw)
+        return g(*[a[n] for n in names])
+
+    assert call(K=48, ldx=48) == lib.MXFP4_ESHAPE
+    assert call(ldx=32) == lib.MXFP4_ESHAPE
+    assert call(k=0) == lib.MXFP4_EINVAL
+    assert call(k=lib.MXFP4_SCATTER_MAX_TOP_K + 1) == lib.MXFP4_EINVAL
+    assert call(dst=None) == lib.MXFP4_EINVAL
+    assert call(c=None) == lib.MXFP4_EINVAL
+    assert call(E=0) == lib.MXFP4_EINVAL                     # rows but no segments
+    assert call(dst=2 * A + 2) == lib.MXFP4_EALIGN
+    assert call(ldx=68) == lib.MXFP4_EALIGN
+    assert call(c=2 * A + 16) == lib.MXFP4_EALIAS            # codes overlap the routes
+    assert call(sro=A + 64) == lib.MXFP4_EALIAS              # offsets out overlap x
+    assert call(s=4 * A + 64) == lib.MXFP4_EALIAS            # scales overlap codes
+    # no tokens: dest_rows and x may be NULL (pad rows are still written)
+    assert call(T=0, x=None, dst=None, off=None) == lib.MXFP4_EINVAL
+
+
 def test_quantize_f16_validation(lib):
     f = lib._lib.mxfp4_quantize_f16
     assert f(A, 4, 48, 48, 2 * A, 3 * A, None) == lib.MXFP4_ESHAPE

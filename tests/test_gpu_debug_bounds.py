@@ -121,6 +121,21 @@ def test_everything_in_bounds(libs):
     ri = torch.from_numpy(rng.integers(0, 300, int(sizes.sum())).astype(np.int32)).cuda()
     cases.append(lambda: written(mx.quantize_grouped_gather(xt2, ri, off_z), 160))
     cases.append(lambda: written(mx.quantize_grouped(xt2.index_select(0, ri.long()), off_z), 160))
+    # scatter: all routes, dropped routes, bad entries, no tokens, strided
+    cases.append(lambda: written(mx.quantize_grouped_scatter(gsmall.x_tokens, gsmall.dest_rows,
+                                                             gsmall.offsets), 288))
+    dsc = gsmall.dest_rows.clone()
+    dsc[::3, 1] = -1
+    dsc[5, 0] = 1 << 20
+    cases.append(lambda: written(mx.quantize_grouped_scatter(gsmall.x_tokens, dsc,
+                                                             gsmall.offsets), 288))
+    cases.append(lambda: written(mx.quantize_grouped_scatter(gsmall.x_tokens[:0], dsc[:0],
+                                                             gsmall.offsets, dsc.numel()), 288))
+    g3 = W.moe_grouped(seed=9, tokens=130, top_k=3, num_experts=5, K=1056, device="cuda")
+    wide3 = torch.zeros((130, 1064), dtype=torch.bfloat16, device="cuda")
+    wide3[:, :1056] = g3.x_tokens
+    cases.append(lambda: written(mx.quantize_grouped_scatter(wide3[:, :1056], g3.dest_rows,
+                                                             g3.offsets), 1056))
     # swap: tiled with N % 128 == 0 and != 0, flat aligned and not
     for E, two_n, K, tiled in [(2, 256, 2048, True), (3, 200, 160, True), (3, 200, 160, False),
                                (2, 256, 64, False)]:

@@ -388,6 +388,138 @@ def test_grouped_gather_moe_full_size(mx):
     assert torch.equal(s1[:used], s2[:used])
 
 
+# ------------------------------------------------- fused dispatch scatter
+def run_scatter(mx, x, dest, offsets, total, seed=0):
+    """Scatter form through the C ABI into guard-banded buffers whose inner
+    bytes start random (the same bytes go to the oracle, so untouched rows
+    and slack compare equal); returns the GPU and oracle results."""
+    K = x.shape[1]
+    E = offsets.numel() - 1
+    rng = np.random.default_rng(seed)
+    nsb = mx.mxfp4_grouped_scale_bytes_bound(total, E, K)
+    c0 = rng.integers(0, 256, (total, K // 2), dtype=np.uint8)
+    s0 = rng.integers(0, 256, nsb, dtype=np.uint8)
+    codes = Guarded(total * (K // 2), shape=(total, K // 2))
+    scales = Guarded(nsb)
+    codes.t.copy_(torch.from_numpy(c0))
+    scales.t.copy_(torch.from_numpy(s0))
+    sro = Guarded(4 * (E + 1), torch.int32)
+    status = Guarded(4, torch.int32)
+    mx.mxfp4_quantize_grouped_scatter(x, dest, offsets, total, codes.t, scales.t, sro.t, status.t)
+    torch.cuda.synchronize()
+    for g in (codes, scales, sro, status):
+        g.check()
+    gpu = (codes.t.cpu().numpy(), scales.t.cpu().numpy(), sro.t.cpu().numpy(),
+           int(status.t.cpu()[0]))
+    rc, c_o, s_o, sro_o = oracle.quantize_grouped_scatter(
+        bits(x.contiguous()), dest.cpu().numpy(), offsets.cpu().numpy(), total, c0, s0)
+    return gpu, (c_o, s_o, sro_o, rc)
+
+
+def assert_scatter_parity(gpu, orc, want_status=0):
+    c, s, sro, st = gpu
+    c_o, s_o, sro_o, rc = orc
+    assert st == want_status and rc == want_status  # the oracle returns the ABI's codes
+    assert np.array_equal(sro, sro_o)
+    assert np.array_equal(c, c_o), _first_diff(c, c_o)
+    assert np.array_equal(s, s_o), _first_diff(s, s_o)
+
+
+def test_grouped_scatter_small(mx):
+    g = W.moe_grouped(seed=2, tokens=200, top_k=4, num_experts=12, K=288, device="cuda")
+    gpu, orc = run_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, g.row_index.numel())
+    assert_scatter_parity(gpu, orc)
+    c_g, s_g, sro_g, _ = run_gather(mx, g.x_tokens, g.row_index, g.offsets)
+    used = int(sro_g[-1]) * 12
+    assert np.array_equal(gpu[0], c_g) and np.array_equal(gpu[1][:used], s_g[:used])
+
+
+@pytest.mark.parametrize("tokens,top_k,E,K", [
+    (1, 1, 1, 32), (129, 3, 5, 160), (300, 2, 7, 2880), (64, 32, 40, 96), (257, 8, 16, 1056)])
+def test_grouped_scatter_shapes(mx, tokens, top_k, E, K):
+    g = W.moe_grouped(seed=tokens + K, tokens=tokens, top_k=top_k, num_experts=E, K=K,
+                      device="cuda")
+    gpu, orc = run_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, g.row_index.numel(), seed=K)
+    assert_scatter_parity(gpu, orc)
+
+
+def test_grouped_scatter_dropped_routes(mx):
+    """20 % of the routes not dispatched (-1): their rows keep their previous
+    bytes, codes and scale bytes alike; pad rows are zeroed."""
+    g = W.moe_grouped(seed=6, tokens=300, top_k=4, num_experts=9, K=160, device="cuda")
+    dst = g.dest_rows.clone()
+    drop = torch.rand(dst.shape, generator=torch.Generator().manual_seed(1)) < 0.2
+    dst[drop.cuda()] = -1
+    gpu, orc = run_scatter(mx, g.x_tokens, dst, g.offsets, g.row_index.numel(), seed=3)
+    assert_scatter_parity(gpu, orc)
+
+
+def test_grouped_scatter_empty_experts_and_no_tokens(mx):
+    x = W.small_matrix(4, 100, 256).cuda()
+    off = torch.tensor([0, 0, 130, 130, 200, 200], dtype=torch.int32, device="cuda")
+    perm = torch.randperm(200, generator=torch.Generator().manual_seed(2)).to(torch.int32)
+    dst = perm.view(100, 2).cuda()
+    gpu, orc = run_scatter(mx, x, dst, off, 200, seed=4)
+    assert_scatter_parity(gpu, orc)
+    # no tokens at all: every row untargeted, only the pad rows are written
+    gpu, orc = run_scatter(mx, x[:0], dst[:0], off, 200, seed=5)
+    assert_scatter_parity(gpu, orc)
+
+
+def test_grouped_scatter_bad_entries(mx):
+    g = W.moe_grouped(seed=7, tokens=140, top_k=2, num_experts=3, K=64, device="cuda")
+    total = g.row_index.numel()
+    dst = g.dest_rows.clone()
+    dst[3, 1] = total
+    dst[7, 0] = -2
+    dst[139, 1] = 1 << 30
+    gpu, orc = run_scatter(mx, g.x_tokens, dst, g.offsets, total, seed=6)
+    assert orc[3] == -7
+    assert_scatter_parity(gpu, orc, want_status=mx.MXFP4_EINDEX)
+
+
+@pytest.mark.parametrize("off", [[1, 10, 20], [0, 12, 8, 20], [0, 10, 19]])
+def test_grouped_scatter_bad_offsets(mx, off):
+    x = W.small_matrix(3, 10, 64).cuda()
+    dst = torch.arange(20, dtype=torch.int32, device="cuda").view(10, 2)
+    o = torch.tensor(off, dtype=torch.int32, device="cuda")
+    gpu, orc = run_scatter(mx, x, dst, o, 20, seed=7)
+    assert orc[3] == -6 and gpu[3] == mx.MXFP4_EOFFSETS
+    assert (gpu[2] == -1).all()
+    assert np.array_equal(gpu[0], orc[0]) and np.array_equal(gpu[1], orc[1])  # untouched
+
+
+def test_grouped_scatter_strided_and_16b_aligned(mx):
+    g = W.moe_grouped(seed=8, tokens=150, top_k=3, num_experts=6, K=256, device="cuda")
+    wide = torch.zeros((150, 392), dtype=torch.bfloat16, device="cuda")
+    wide[:, 8:264] = g.x_tokens
+    for x in (wide[:, 8:264], offset16(g.x_tokens)):
+        gpu, orc = run_scatter(mx, x, g.dest_rows, g.offsets, g.row_index.numel(), seed=8)
+        assert_scatter_parity(gpu, orc)
+
+
+def test_grouped_scatter_moe_full_size(mx):
+    """16384 tokens x top-8 over 384 experts, K = 7168: every byte equals the
+    fused gather's (itself equal to the grouped quantize of the gathered
+    matrix); four experts' segments also against the oracle directly."""
+    g = W.moe_grouped(seed=2, device="cuda")
+    c1, s1, sro1, st1 = mx.quantize_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets)
+    c2, s2, sro2, st2 = mx.quantize_grouped_gather(g.x_tokens, g.row_index, g.offsets)
+    torch.cuda.synchronize()
+    assert int(st1.cpu()[0]) == 0 and int(st2.cpu()[0]) == 0
+    assert torch.equal(sro1, sro2) and torch.equal(c1, c2)
+    used = int(sro1[-1].item()) * 224
+    assert torch.equal(s1[:used], s2[:used])
+    off_h = g.offsets.cpu().numpy().astype(np.int64)
+    sro_h = sro1.cpu().numpy().astype(np.int64)
+    for e in (0, 17, 200, 383):
+        a, b = int(off_h[e]), int(off_h[e + 1])
+        c_o, s_o = oracle.quantize(bits(g.x[a:b]))
+        assert np.array_equal(c1[a:b].cpu().numpy(), c_o), e
+        p0 = int(sro_h[e]) * 224
+        assert np.array_equal(s1[p0:p0 + s_o.size].cpu().numpy(), s_o), e
+
+
 # ----------------------- inputs aligned to 16 bytes but not to 32 bytes
 def offset16(x):
     """The same values in a buffer whose base is 16 (not 32) bytes aligned:
