@@ -20,9 +20,11 @@ LIBRARY = os.path.join(HERE, "libmxfp4_gb300.so")
 DEBUG_LIBRARY = os.path.join(HERE, "libmxfp4_gb300_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-              "-Xptxas", "-warn-spills", "-Werror", "all-warnings"]
+              "-Werror", "all-warnings"]
+# A register spill in the normal build is an error; the bounds-checking build
+# carries extra live ranges and may spill.
 VARIANTS = {
-    "release": (LIBRARY, BUILD_DIR, []),
+    "release": (LIBRARY, BUILD_DIR, ["-Xptxas", "-warn-spills"]),
     "debug": (DEBUG_LIBRARY, os.path.join(BUILD_DIR, "debug"), ["-DMXFP4_DEBUG_BOUNDS"]),
 }
 

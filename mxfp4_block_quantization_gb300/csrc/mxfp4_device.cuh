@@ -323,6 +323,19 @@ inline void debug_range(DebugRanges& r, int slot, const void* p, int64_t bytes) 
   r.hi[slot] = r.lo[slot] + static_cast<uintptr_t>(bytes > 0 ? bytes : 0);
 }
 
+// L2 policy that keeps lines resident ahead of streaming traffic, and a
+// 4-byte store under such a policy: for small stores that several CTAs
+// complete sector by sector (a sector evicted half written costs a DRAM read
+// to merge it).
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void st_keep_u32(void* p, uint32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
+}
+
 // Programmatic dependent launch: wait until the preceding grid of the stream
 // has completed and its writes are visible (no-op without a predecessor),
 // and allow the next grid of the stream to be scheduled.

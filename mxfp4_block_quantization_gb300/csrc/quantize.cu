@@ -17,8 +17,8 @@
 // loads are issued before any compute (32 KB in flight per CTA, four to five
 // CTAs per SM).  The fused-gather variant (quantize_gather_kernel) keeps one
 // 128-row tile per CTA but walks a chunk of k-tiles; the scatter variant
-// (quantize_scatter_kernel) reads 128 token rows once and writes each row's
-// codes and scale words to all the rows its routes land on.  Launches use
+// (quantize_scatter_kernel) gives each warp one token row, read once, whose
+// codes and scale words go to all the rows its routes land on.  Launches use
 // programmatic dependent launch, so a grid is already resident when its
 // predecessor in the stream drains.
 #include <cstdint>
@@ -318,17 +318,22 @@ __global__ void __launch_bounds__(kGatherThreads) quantize_gather_kernel(const Q
 
 // Fused dispatch scatter: route j of token t lands on row dest_rows[t][j] of
 // the expert-sorted batch.  The first E CTAs zero the scale bytes of expert
-// e's pad rows.  Every other CTA (256 threads, the dense lane mapping) owns
-// 128 token rows and a chunk of kScatterChunkTiles k-tiles: it resolves the
-// tile's 128 x top_k destinations once (code row, and padded scale row from
-// the destination's segment) into shared memory, then per k-tile loads the
-// token rows once, quantizes them once, and stores each lane's 8 code bytes
-// to every destination row; the tile's 128 scale words (4 bytes of a row
-// and k-tile) are staged in shared memory and stored once per destination.
-// DRAM traffic is the algorithmic one: each token row read once, each output
-// byte written once.  CTAs run m-tile-major, so the chunks of one token tile
-// complete the destination rows' 128-byte lines back to back.
-constexpr int kScatterChunkTiles = 4;
+// e's pad rows.  In every other CTA each warp owns one token: lanes 0..top_k-1
+// resolve the token's routes (code row, padded scale row from the route's
+// segment) once, then the warp streams the token row in passes of 512
+// elements (lane = 16 elements, 32 bytes), kScatterBatch passes' loads in
+// flight at a time, quantizes each pass once and stores it to every
+// destination: per route one contiguous 256-byte run of codes (two full
+// lines) and, from lanes 0, 8, 16, 24, the 4-byte scale word of each of the
+// pass's four k-tiles.  Each destination row's codes thus leave the SM as one
+// contiguous stream; DRAM traffic is the algorithmic one (token rows read
+// once, every output byte written once).  The scale words are stored with an
+// L2 evict-last policy: a 16-byte group of the tiled layout holds the words
+// of four rows 32 apart, which different warps write at different times, and
+// the codes stream past them (evict-first) in the meantime.
+constexpr int kScatterWarps = kThreads / 32;  // tokens per CTA
+constexpr int kScatterBatch = 4;              // passes with loads in flight together
+constexpr int kScatterPass = 32 * kElems;     // elements per warp pass (4 k-tiles)
 
 struct ScatterParams {
   const uint8_t* __restrict__ x;          // BF16 token rows
@@ -351,12 +356,17 @@ struct ScatterParams {
 #endif
 };
 
+// Byte offset of the scale word (4 scale columns of one k-tile) of padded row
+// `prow` in k-tile 0; k-tile kt adds kt * 512.
+__device__ __forceinline__ int64_t scale_word_base(int prow, int nKT) {
+  return static_cast<int64_t>(prow >> 7) * nKT * kChunkBytes + (prow & 31) * 16 +
+         ((prow & 127) >> 5) * 4;
+}
+
 template <bool kVec32>
 __global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const ScatterParams p) {
-  constexpr int kRowsPerPass = rows_per_pass(kThreads);
-  constexpr int kPasses = passes(kThreads);
-  extern __shared__ int32_t s_route[];                // [top_k][128] code rows, then [top_k][128] padded rows
-  __shared__ __align__(16) uint32_t s_words[2][kTileRows];
+  __shared__ int64_t s_code[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];   // d * K/2, or -1
+  __shared__ int64_t s_scale[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];  // word base, or -1
 
   pdl_wait();
   pdl_release();
@@ -373,102 +383,84 @@ __global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const Scatte
     const int n = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
     const int npad = ((n + kTileRows - 1) / kTileRows) * kTileRows - n;
     const int P0 = __ldg(p.padded + e) + n;
+    const uint64_t keep = l2_evict_last_policy();
     for (int i = threadIdx.x; i < npad * p.nKT; i += kThreads) {
       const int kt = i / npad;
-      const int prow = P0 + (i - kt * npad);
-      uint32_t* wp = reinterpret_cast<uint32_t*>(
-          p.scales + (static_cast<int64_t>(prow >> 7) * p.nKT + kt) * kChunkBytes +
-          (prow & 31) * 16 + ((prow & 127) >> 5) * 4);
-      if (MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4)) *wp = 0u;
+      uint8_t* wp = p.scales + scale_word_base(P0 + (i - kt * npad), p.nKT) + kt * kChunkBytes;
+      if (MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4)) st_keep_u32(wp, 0u, keep);
     }
     return;
   }
 
-  const int unit = blockIdx.x - p.E;
-  const int n_chunks = (p.nKT + kScatterChunkTiles - 1) / kScatterChunkTiles;
-  const int mt = unit / n_chunks;
-  const int kc = unit - mt * n_chunks;
-  const int64_t t0 = static_cast<int64_t>(mt) * kTileRows;
-  const int64_t left = p.num_tokens - t0;
-  const int ntok = static_cast<int>(left < kTileRows ? left : kTileRows);
-  const int top_k = p.top_k;
-  int32_t* const s_code_row = s_route;
-  int32_t* const s_pad_row = s_route + top_k * kTileRows;
-
-  // destinations of the tile's routes; entry i = (token t0 + i / top_k, route i % top_k)
-  bool bad = false;
-  for (int i = threadIdx.x; i < kTileRows * top_k; i += kThreads) {
-    const int lt = i / top_k;
-    const int j = i - lt * top_k;
-    int32_t d = -1, prow = -1;
-    if (lt < ntok) {
-      const int32_t* dp = p.dest_rows + t0 * top_k + i;
-      const int32_t v = MXFP4_IN_BOUNDS(p, kDbgRowIndex, dp, 4) ? __ldg(dp) : -1;
-      if (v >= 0 && v < p.total_rows) {
-        const int e = find_segment(p.offsets, p.E, v, static_cast<int>(p.total_rows));
-        d = v;
-        prow = __ldg(p.padded + e) + (v - __ldg(p.offsets + e));
-      } else {
-        bad |= v != -1;
-      }
-    }
-    s_code_row[j * kTileRows + lt] = d;
-    s_pad_row[j * kTileRows + lt] = prow;
-  }
-  if (bad && p.status != nullptr && MXFP4_IN_BOUNDS(p, kDbgStatus, p.status, 4))
-    atomicExch(p.status, MXFP4_EINDEX);
-  __syncthreads();
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int sub = lane & (kLanesPerRow - 1);
-  const int blk = sub >> 1;
-  const int lr0 = warp * (32 / kLanesPerRow) + (lane >> 3);
-  const int lim = ntok - lr0;
-  const uint8_t* xrow = p.x + (t0 + lr0) * p.ldx_bytes + sub * (kElems * 2);
-  const int64_t ldx_pass = p.ldx_bytes * kRowsPerPass;
-  const int kt0 = kc * kScatterChunkTiles;
-  const int kt_end = kt0 + kScatterChunkTiles < p.nKT ? kt0 + kScatterChunkTiles : p.nKT;
-  int buf = 0;
-  for (int kt = kt0; kt < kt_end; ++kt) {
-    const bool col_ok = kt * kTileBlocks + blk < p.sK;
-    const uint8_t* xp = xrow + static_cast<int64_t>(kt) * (kTileCols * 2);
-    uint4 v[kPasses][2];
-#pragma unroll
-    for (int i = 0; i < kPasses; ++i) {
-      v[i][0] = v[i][1] = make_uint4(0u, 0u, 0u, 0u);
-      if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgX, xp + i * ldx_pass, 32))
-        load32<kVec32>(xp + i * ldx_pass, v[i]);
+  const int64_t t = static_cast<int64_t>(blockIdx.x - p.E) * kScatterWarps + warp;
+  if (t >= p.num_tokens) return;  // whole warp; no block-wide barrier below
+  const int top_k = p.top_k;
+
+  // the token's routes, one per lane
+  int64_t co = -1, so = -1;
+  bool bad = false;
+  if (lane < top_k) {
+    const int32_t* dp = p.dest_rows + t * top_k + lane;
+    const int32_t v = MXFP4_IN_BOUNDS(p, kDbgRowIndex, dp, 4) ? __ldg(dp) : -1;
+    if (v >= 0 && v < p.total_rows) {
+      const int e = find_segment(p.offsets, p.E, v, static_cast<int>(p.total_rows));
+      co = static_cast<int64_t>(v) * p.code_ld;
+      so = scale_word_base(__ldg(p.padded + e) + (v - __ldg(p.offsets + e)), p.nKT);
+    } else {
+      bad = v != -1;
     }
-    uint2 code[kPasses];
-    uint8_t* const words = reinterpret_cast<uint8_t*>(s_words[buf]);
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && p.status != nullptr &&
+      MXFP4_IN_BOUNDS(p, kDbgStatus, p.status, 4))
+    atomicExch(p.status, MXFP4_EINDEX);
+  s_code[warp][lane] = co;
+  s_scale[warp][lane] = so;
+  __syncwarp();
+
+  const uint8_t* xrow = p.x + t * p.ldx_bytes + lane * (kElems * 2);
+  const int n_pass = (p.sK + 15) / 16;  // 16 blocks per pass
+  const uint64_t keep = l2_evict_last_policy();
+  for (int p0 = 0; p0 < n_pass; p0 += kScatterBatch) {
+    uint4 v[kScatterBatch][2];
 #pragma unroll
-    for (int i = 0; i < kPasses; ++i) {
-      const uint32_t s = lane_block_scale<false>(v[i]);
-      if ((lane & 1) == 0) words[(lr0 + kRowsPerPass * i) * 4 + blk] = static_cast<uint8_t>(s);
-      code[i] = lane_codes<false>(v[i], s);
+    for (int b = 0; b < kScatterBatch; ++b) {
+      v[b][0] = v[b][1] = make_uint4(0u, 0u, 0u, 0u);
+      const int pass = p0 + b;
+      const uint8_t* xp = xrow + static_cast<int64_t>(pass) * (kScatterPass * 2);
+      if (pass < n_pass && pass * 16 + (lane >> 1) < p.sK &&
+          MXFP4_IN_BOUNDS(p, kDbgX, xp, 32))
+        load32<kVec32>(xp, v[b]);
     }
-    const int64_t col = static_cast<int64_t>(kt) * (kTileCols / 2) + sub * (kElems / 2);
-    if (col_ok) {
-      for (int j = 0; j < top_k; ++j) {
+    uint2 code[kScatterBatch];
+    uint32_t word[kScatterBatch];
 #pragma unroll
-        for (int i = 0; i < kPasses; ++i) {
-          const int32_t d = s_code_row[j * kTileRows + lr0 + kRowsPerPass * i];
-          uint8_t* const cp = p.codes + static_cast<int64_t>(d) * p.code_ld + col;
-          if (d >= 0 && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 8)) st_stream_v2(cp, code[i]);
-        }
+    for (int b = 0; b < kScatterBatch; ++b) {
+      const uint32_t s = lane_block_scale<false>(v[b]);
+      code[b] = lane_codes<false>(v[b], s);
+      // scale word of k-tile (p0+b)*4 + lane/8: the s of lanes +0, +2, +4, +6
+      word[b] = s | (__shfl_down_sync(0xFFFFFFFFu, s, 2) << 8) |
+                (__shfl_down_sync(0xFFFFFFFFu, s, 4) << 16) |
+                (__shfl_down_sync(0xFFFFFFFFu, s, 6) << 24);
+    }
+    const int64_t cofs = static_cast<int64_t>(p0) * (kScatterPass / 2) + lane * (kElems / 2);
+    const int kt0 = p0 * 4 + (lane >> 3);
+    for (int j = 0; j < top_k; ++j) {
+      const int64_t c = s_code[warp][j];
+      const int64_t w = s_scale[warp][j];
+#pragma unroll
+      for (int b = 0; b < kScatterBatch; ++b) {
+        const int pass = p0 + b;
+        uint8_t* const cp = p.codes + c + cofs + b * (kScatterPass / 2);
+        if (c >= 0 && pass * 16 + (lane >> 1) < p.sK && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 8))
+          st_stream_v2(cp, code[b]);
+        const int kt = kt0 + 4 * b;
+        uint8_t* const wp = p.scales + w + static_cast<int64_t>(kt) * kChunkBytes;
+        if (w >= 0 && (lane & 7) == 0 && kt < p.nKT && MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4))
+          st_keep_u32(wp, word[b], keep);
       }
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < kTileRows * top_k; i += kThreads) {
-      const int32_t prow = s_pad_row[i];
-      if (prow < 0) continue;
-      uint32_t* const wp = reinterpret_cast<uint32_t*>(
-          p.scales + (static_cast<int64_t>(prow >> 7) * p.nKT + kt) * kChunkBytes +
-          (prow & 31) * 16 + ((prow & 127) >> 5) * 4);
-      if (MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4)) st_stream_u32(wp, s_words[buf][i & (kTileRows - 1)]);
-    }
-    buf ^= 1;
   }
 }
 
@@ -703,13 +695,10 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
   debug_range(p.dbg, kDbgRowIndex, dest_rows, num_tokens * top_k * 4);
   debug_range(p.dbg, kDbgStatus, status, status ? 4 : 0);
 #endif
-  const int64_t token_tiles = (num_tokens + kTileRows - 1) / kTileRows;
-  const int64_t grid =
-      E + token_tiles * ((p.nKT + kScatterChunkTiles - 1) / kScatterChunkTiles);
-  const size_t smem = static_cast<size_t>(top_k) * kTileRows * 2 * sizeof(int32_t);
+  const int64_t grid = E + (num_tokens + kScatterWarps - 1) / kScatterWarps;
   const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_scatter_kernel<true>
                                                : quantize_scatter_kernel<false>;
-  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, smem, stream, p);
+  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
 #ifdef MXFP4_DEBUG_BOUNDS
