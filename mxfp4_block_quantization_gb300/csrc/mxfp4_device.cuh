@@ -323,6 +323,63 @@ inline void debug_range(DebugRanges& r, int slot, const void* p, int64_t bytes) 
   r.hi[slot] = r.lo[slot] + static_cast<uintptr_t>(bytes > 0 ? bytes : 0);
 }
 
+// ------------------------------------------- one lane's 16 elements
+// The quantize kernels give each lane 16 consecutive elements of a row (one
+// 32-byte load, or two 16-byte loads when the input is only 16-byte
+// aligned); two neighbouring lanes form one 32-element block.
+constexpr int kElems = 16;                                  // elements per lane per pass
+constexpr int kLanesPerRow = kTileCols / kElems;            // 8 lanes cover 128 columns
+
+// One lane's 16 BF16 elements (32 bytes) of one row.
+template <bool kVec32>
+__device__ __forceinline__ void load32(const uint8_t* src, uint4 (&v)[2]) {
+  if constexpr (kVec32) {
+    ld_stream_v8(src, v[0], v[1]);
+  } else {
+    v[0] = ld_stream_v4(src);
+    v[1] = ld_stream_v4(src + 16);
+  }
+}
+
+// One lane's share of one pass: its 16 elements (two lanes per 32-element
+// block) -> the block's E8M0 scale exponent.  |x| per half with
+// max.xorsign.abs, sign bits cleared, then the larger half (the unsigned order
+// of non-negative BF16/FP16 patterns is the order of their magnitudes), then
+// the partner lane's half block.
+template <bool kF16>
+__device__ __forceinline__ uint32_t lane_block_scale(const uint4 (&v)[2]) {
+  uint32_t h;
+  if constexpr (kF16) {
+    h = max_abs_f16x2(max_abs_f16x2(max_abs_f16x2(v[0].x, v[0].y), max_abs_f16x2(v[0].z, v[0].w)),
+                      max_abs_f16x2(max_abs_f16x2(v[1].x, v[1].y), max_abs_f16x2(v[1].z, v[1].w)));
+  } else {
+    h = max_abs_bf16x2(
+        max_abs_bf16x2(max_abs_bf16x2(v[0].x, v[0].y), max_abs_bf16x2(v[0].z, v[0].w)),
+        max_abs_bf16x2(max_abs_bf16x2(v[1].x, v[1].y), max_abs_bf16x2(v[1].z, v[1].w)));
+  }
+  h &= 0x7FFF7FFFu;
+  uint32_t m = max(h & 0xFFFFu, h >> 16);
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  return kF16 ? e8m0_from_absmax_f32bits(f16_bits_to_f32_bits(m)) : e8m0_from_absmax_bf16(m);
+}
+
+// The lane's 16 codes (8 bytes): x * 2^(127-s) rounded to E2M1; s == 0 gives
+// zero codes.
+template <bool kF16>
+__device__ __forceinline__ uint2 lane_codes(const uint4 (&v)[2], uint32_t s) {
+  const float inv = inv_scale_from_e8m0(s);
+  uint2 code;
+  if constexpr (kF16) {
+    code.x = scale_cvt_e2m1x8_f16(v[0], inv);
+    code.y = scale_cvt_e2m1x8_f16(v[1], inv);
+  } else {
+    code.x = scale_cvt_e2m1x8(v[0], inv);
+    code.y = scale_cvt_e2m1x8(v[1], inv);
+  }
+  if (s == 0u) code = make_uint2(0u, 0u);
+  return code;
+}
+
 // L2 policy that keeps lines resident ahead of streaming traffic, and a
 // 4-byte store under such a policy: for small stores that several CTAs
 // complete sector by sector (a sector evicted half written costs a DRAM read

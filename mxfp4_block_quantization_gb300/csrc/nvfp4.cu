@@ -54,16 +54,6 @@ struct Nvfp4Params {
 enum : int { kDbgXY = 0, kDbgCodes, kDbgScales, kDbgG };
 
 template <bool kVec32>
-__device__ __forceinline__ void load32(const uint8_t* src, uint4 (&v)[2]) {
-  if constexpr (kVec32) {
-    ld_stream_v8(src, v[0], v[1]);
-  } else {
-    v[0] = ld_stream_v4(src);
-    v[1] = ld_stream_v4(src + 16);
-  }
-}
-
-template <bool kVec32>
 __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(const Nvfp4Params p) {
   __shared__ __align__(16) uint8_t chunk[2][kChunkBytes];
   pdl_wait();
