@@ -88,6 +88,10 @@ def lib():
         L.orc_nvfp4_quantize.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_float, _u8p, _u8p]
         L.orc_nvfp4_dequantize.restype = None
         L.orc_nvfp4_dequantize.argtypes = [_u8p, _u8p, _i64, _i64, ctypes.c_float, _u16p]
+        L.orc_e8m0_scale_legacy.restype = ctypes.c_uint8
+        L.orc_e8m0_scale_legacy.argtypes = [ctypes.c_float]
+        L.orc_quantize_flat_legacy.restype = None
+        L.orc_quantize_flat_legacy.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p]
         L.orc_quantize_grouped_scatter.restype = ctypes.c_int
         L.orc_quantize_grouped_scatter.argtypes = [_u16p, _i64, _i64, _i64, _i32p, ctypes.c_int32,
                                                    _i64, _i32p, ctypes.c_int32, _u8p, _u8p, _i32p]
@@ -180,6 +184,22 @@ def quantize_flat(xbits: np.ndarray):
     flat = np.zeros((M, K // 32), np.uint8)
     if M and K:
         lib().orc_quantize_flat(_p(x, _u16p), M, K, K, _p(codes, _u8p), _p(flat, _u8p))
+    return codes, flat
+
+
+def e8m0_scale_legacy(vecmax: float) -> int:
+    """The pre-fix scale biased_exp(vecMax/6) (comparison only)."""
+    return int(lib().orc_e8m0_scale_legacy(float(vecmax)))
+
+
+def quantize_flat_legacy(xbits: np.ndarray):
+    """Steps 1-4 with the pre-fix scale (comparison only): (codes, flat)."""
+    x = _c(xbits, np.uint16)
+    M, K = x.shape
+    codes = np.zeros((M, K // 2), np.uint8)
+    flat = np.zeros((M, K // 32), np.uint8)
+    if M and K:
+        lib().orc_quantize_flat_legacy(_p(x, _u16p), M, K, K, _p(codes, _u8p), _p(flat, _u8p))
     return codes, flat
 
 

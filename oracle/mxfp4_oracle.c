@@ -205,6 +205,38 @@ void orc_quantize_flat(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
   }
 }
 
+/* The scale the fix replaced, reproduced for comparison only ([PR43557]
+ * "Motivation": the old code took the biased exponent of max/6, and since
+ * floor(log2(a/b)) differs from floor(log2 a) - floor(log2 b) that scale is
+ * one too small for most inputs, leaving max/scale above 6).  Reading: the
+ * exponent field of the float32 quotient vecMax/6 (rounded to nearest),
+ * 0 for a zero block.  Never used by the library. */
+uint8_t orc_e8m0_scale_legacy(float vecmax) {
+  if (vecmax <= 0.0f) return 0;
+  float q = vecmax / 6.0f;
+  uint32_t bits;
+  memcpy(&bits, &q, sizeof bits);
+  return (uint8_t)((bits >> 23) & 0xFFu);
+}
+
+/* Steps 1-4 with the legacy scale in place of step 2 (comparison only). */
+void orc_quantize_flat_legacy(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                              uint8_t* codes, uint8_t* flat_scales) {
+  int64_t sK = K / 32;
+  for (int64_t r = 0; r < M; ++r) {
+    const uint16_t* row = x + r * ldx;
+    for (int64_t b = 0; b < sK; ++b) {
+      const uint16_t* blk = row + b * 32;
+      uint8_t s = orc_e8m0_scale_legacy(orc_block_absmax(blk, 32));
+      flat_scales[r * sK + b] = s;
+      uint8_t nib[32];
+      for (int i = 0; i < 32; ++i) nib[i] = orc_e2m1_encode(blk[i], s);
+      for (int j = 0; j < 16; ++j)
+        codes[r * (K / 2) + b * 16 + j] = (uint8_t)(nib[2 * j] | (nib[2 * j + 1] << 4));
+    }
+  }
+}
+
 /* Steps 1-4 for FP16 input: the same block max (as a float: every FP16
  * value is exact in float32), the same E8M0 rule on its float bits, the same
  * element rounding. */

@@ -63,6 +63,10 @@ size_t orc_scale_bytes(int64_t M, int64_t K);
 /* Steps 1-4: flat per-block scales [M, K/32] and packed codes [M, K/2]. */
 void orc_quantize_flat(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
                        uint8_t* codes, uint8_t* flat_scales);
+/* Comparison only: the pre-fix scale biased_exp(vecMax/6) and steps 1-4 with it. */
+uint8_t orc_e8m0_scale_legacy(float vecmax);
+void orc_quantize_flat_legacy(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                              uint8_t* codes, uint8_t* flat_scales);
 /* Step 5: flat [M, sK] scales <-> CUTLASS 128x4 tiled, zero-padded bytes. */
 void orc_tile_scales(const uint8_t* flat, int64_t M, int64_t sK, uint8_t* tiled);
 void orc_untile_scales(const uint8_t* tiled, int64_t M, int64_t sK, uint8_t* flat);
