@@ -54,3 +54,25 @@ def test_reference_arm_non_zero_rank_exits_quietly(capsys, monkeypatch):
     monkeypatch.setenv("RANK", "1")
     assert bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_json_contract(capsys, monkeypatch):
+    """The reference arm (the CPU oracle) prints one JSON line with the
+    contract's keys; its ratio against our arm uses the same metric, unit and
+    direction."""
+    import json
+    import bench
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3"]) == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["higher_is_better"] is True and d["steps"] == 3 and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
