@@ -800,3 +800,49 @@ def test_grouped_many_skewed_experts(mx):
     c2, s2, sro2, st2 = run_gather(mx, x_tok, row_index, off_d)
     assert st2 == 0 and np.array_equal(sro2, sro_o) and np.array_equal(c2, c_o)
     assert np.array_equal(s2[:used], s_o[:used])
+
+
+# ----------------------------------------- non-finite input: no fault, finite blocks exact
+def _with_nonfinite(x, seed):
+    """x with +-Inf / NaN planted in ~2 % of its 32-element blocks; returns
+    (tensor, boolean mask of the blocks left finite)."""
+    xb = bits(x).copy()
+    M, K = xb.shape
+    rng = np.random.default_rng(seed)
+    nb = K // 32
+    hit = rng.random((M, nb)) < 0.02
+    for r, b in zip(*np.nonzero(hit)):
+        xb[r, b * 32 + rng.integers(0, 32)] = rng.choice(
+            np.array([0x7F80, 0xFF80, 0x7FC0, 0xFFC1], np.uint16))
+    t = W.from_bits(xb).to(x.device)
+    return t, ~hit
+
+
+def _blocks_equal(c1, s1, c2, s2, M, K, ok):
+    """Codes and (untiled) scales of the blocks marked ok agree."""
+    f1 = oracle.untile(s1, M, K // 32)
+    f2 = oracle.untile(s2, M, K // 32)
+    assert np.array_equal(f1[ok], f2[ok])
+    n1 = c1.reshape(M, K // 32, 16)
+    n2 = c2.reshape(M, K // 32, 16)
+    assert np.array_equal(n1[ok], n2[ok])
+
+
+def test_nonfinite_inputs_do_not_fault(mx):
+    M, K = 300, 2880
+    x, ok = _with_nonfinite(W.dense_activation(11, M, K, device="cuda"), 1)
+    c, s = run_quantize(mx, x)                                  # guard bands checked
+    c_o, s_o = oracle.quantize(bits(x))
+    _blocks_equal(c, s, c_o, s_o, M, K, ok)
+    # FP16, NVFP4 and the grouped forms run without error on the same data
+    x16 = x.to(torch.float16)
+    cc = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    ss = torch.empty(mx.mxfp4_scale_bytes(M, K), dtype=torch.uint8, device="cuda")
+    mx.mxfp4_quantize_f16(x16, cc, ss)
+    mx.quantize_nvfp4(x, torch.tensor([1.0], device="cuda"))
+    off = torch.tensor([0, 100, 100, 300], dtype=torch.int32, device="cuda")
+    _, _, _, st = mx.quantize_grouped(x, off)
+    dst = torch.randperm(M, generator=torch.Generator().manual_seed(3)).to(torch.int32)
+    _, _, _, st2 = mx.quantize_grouped_scatter(x, dst.view(M, 1).cuda(), off)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(st2.item()) == 0
