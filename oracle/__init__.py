@@ -92,6 +92,9 @@ def lib():
         L.orc_e8m0_scale_legacy.argtypes = [ctypes.c_float]
         L.orc_quantize_flat_legacy.restype = None
         L.orc_quantize_flat_legacy.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p]
+        L.orc_nvfp4_quantize_grouped.restype = ctypes.c_int
+        L.orc_nvfp4_quantize_grouped.argtypes = [_u16p, _i64, _i64, _i32p, ctypes.c_int32, _f32p,
+                                                 _u8p, _u8p, _i32p]
         L.orc_quantize_grouped_scatter.restype = ctypes.c_int
         L.orc_quantize_grouped_scatter.argtypes = [_u16p, _i64, _i64, _i64, _i32p, ctypes.c_int32,
                                                    _i64, _i32p, ctypes.c_int32, _u8p, _u8p, _i32p]
@@ -444,6 +447,29 @@ def nvfp4_quantize(xbits: np.ndarray, g: float):
         lib().orc_nvfp4_quantize(_p(x, _u16p), M, K, K, float(np.float32(g)), _p(codes, _u8p),
                                  _p(scales, _u8p))
     return codes, scales
+
+
+def nvfp4_grouped_scale_bytes_bound(total_rows: int, E: int, K: int) -> int:
+    tiles = (total_rows + 127 * E) // 128
+    return tiles * 128 * ((K // 16 + 3) // 4 * 4)
+
+
+def nvfp4_quantize_grouped(xbits: np.ndarray, offsets: np.ndarray, g: np.ndarray):
+    """NVFP4 experts quant: (rc, codes, scales, scale_row_offsets); rc 0 or -6.
+    g: float32 [E] global scales, one per segment."""
+    x = _c(xbits, np.uint16)
+    off = _c(offsets, np.int32)
+    gs = _c(np.asarray(g, np.float32), np.float32)
+    total, K = x.shape
+    E = off.size - 1
+    assert gs.size == E
+    codes = np.zeros((total, K // 2), np.uint8)
+    scales = np.zeros(max(nvfp4_grouped_scale_bytes_bound(total, E, K), 1), np.uint8)
+    sro = np.zeros(E + 1, np.int32)
+    rc = lib().orc_nvfp4_quantize_grouped(_p(x, _u16p), total, K, _p(off, _i32p), E,
+                                          _p(gs, _f32p), _p(codes, _u8p), _p(scales, _u8p),
+                                          _p(sro, _i32p))
+    return rc, codes, scales, sro
 
 
 def nvfp4_dequantize(codes: np.ndarray, tiled: np.ndarray, M: int, K: int, g: float) -> np.ndarray:

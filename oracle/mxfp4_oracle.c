@@ -596,6 +596,34 @@ void orc_nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, fl
   free(flat);
 }
 
+/* NVFP4 experts quant: the grouped layout of step 6 with the NVFP4 block
+ * ([PR43557] item 3 names the experts-quant kernel, whose non-UE8M0 branch is
+ * the NVFP4 one).  Segment e = rows [o[e], o[e+1]) is quantized as its own
+ * matrix with its own global scale g[e]; codes keep the row order; its tiled
+ * E4M3 scales (16-element columns, padded to 128 rows) start at padded row
+ * P[e].  Bad offsets: -6, scale row offsets all -1, nothing else written. */
+int orc_nvfp4_quantize_grouped(const uint16_t* x, int64_t total_rows, int64_t K,
+                               const int32_t* offsets, int32_t E, const float* g,
+                               uint8_t* codes, uint8_t* scales, int32_t* scale_row_offsets) {
+  int ok = (E >= 0) && offsets[0] == 0 && (int64_t)offsets[E] == total_rows;
+  for (int32_t e = 0; ok && e < E; ++e) ok = offsets[e] <= offsets[e + 1];
+  if (!ok) {
+    for (int32_t e = 0; e <= E; ++e) scale_row_offsets[e] = -1;
+    return -6;
+  }
+  int64_t padded_sK = (K / 16 + 3) / 4 * 4;
+  int64_t P = 0;
+  for (int32_t e = 0; e < E; ++e) {
+    int64_t n = (int64_t)offsets[e + 1] - offsets[e];
+    scale_row_offsets[e] = (int32_t)P;
+    orc_nvfp4_quantize(x + (int64_t)offsets[e] * K, n, K, K, g[e],
+                       codes + (int64_t)offsets[e] * (K / 2), scales + P * padded_sK);
+    P += (n + 127) / 128 * 128;
+  }
+  scale_row_offsets[E] = (int32_t)P;
+  return 0;
+}
+
 void orc_nvfp4_dequantize(const uint8_t* codes, const uint8_t* tiled_scales, int64_t M, int64_t K,
                           float g, uint16_t* y) {
   int64_t sK = K / 16;

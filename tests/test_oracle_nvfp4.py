@@ -108,3 +108,38 @@ def test_nvfp4_tiled_layout_is_the_mx_layout_on_16_element_columns(orc):
     assert np.array_equal(codes, c2)
     assert tiled.size == orc.nvfp4_scale_bytes(200, 480) == 256 * 32
     assert np.array_equal(orc.untile(tiled, 200, 30), flat)
+
+
+def test_nvfp4_grouped_equals_per_segment_dense(orc):
+    """NVFP4 experts quant: each segment equals the dense NVFP4 quantize of
+    its rows with its own global scale, at its padded scale offset; empty
+    segments contribute nothing."""
+    g = W.moe_grouped(seed=3, tokens=90, top_k=2, num_experts=6, K=96)
+    xb = W.bf16_bits(g.x)
+    off = g.offsets.numpy().copy()
+    off[3] = off[2]                                   # make segment 2 empty
+    gs = np.array([1.0, 0.37, 5.0, 448 * 6 / 3.7, 2.0 ** -10, 17.0], np.float32)
+    rc, codes, scales, sro = orc.nvfp4_quantize_grouped(xb, off, gs)
+    assert rc == 0
+    pk = (96 // 16 + 3) // 4 * 4
+    P = 0
+    for e in range(6):
+        a, b = int(off[e]), int(off[e + 1])
+        assert sro[e] == P
+        if b > a:
+            c_e, s_e = orc.nvfp4_quantize(xb[a:b], float(gs[e]))
+            assert np.array_equal(codes[a:b], c_e), e
+            assert np.array_equal(scales[P * pk:P * pk + s_e.size], s_e), e
+        P += (b - a + 127) // 128 * 128
+    assert sro[6] == P
+
+
+def test_nvfp4_grouped_uniform_tiles_equal_dense_and_bad_offsets(orc):
+    xb = W.bf16_bits(W.small_matrix(5, 384, 64))
+    off = np.array([0, 128, 256, 384], np.int32)
+    rc, codes, scales, _ = orc.nvfp4_quantize_grouped(xb, off, np.full(3, 2.5, np.float32))
+    c_d, s_d = orc.nvfp4_quantize(xb, 2.5)
+    assert rc == 0 and np.array_equal(codes, c_d) and np.array_equal(scales[:s_d.size], s_d)
+    rc, _, _, sro = orc.nvfp4_quantize_grouped(xb, np.array([0, 200, 100, 384], np.int32),
+                                               np.ones(3, np.float32))
+    assert rc == -6 and (sro == -1).all()
