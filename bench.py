@@ -390,6 +390,18 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     out["grouped_moe_131072x7168_E384"] = entry(
         nb, ms, 2, f"{padded} padded scale rows; offsets kernel + quantize kernel")
 
+    # the same batch through the NVFP4 experts quant (a global scale per expert)
+    g_nv = torch.full((E,), 448.0 * 6.0 / 5.0, device="cuda")
+    sc_nv = torch.empty(mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K), dtype=torch.uint8,
+                        device="cuda")
+    ms = time_launches(lambda i: mx.mxfp4_quantize_nvfp4_grouped(g.x, g.offsets, g_nv, codes,
+                                                                 sc_nv, sro, st, stream), 30,
+                       stream)
+    nb_nv = 2 * total * K + total * K // 2 + padded * (K // 16) + 4 * (E + 1) + 4 * E
+    out["nvfp4_grouped_moe_131072x7168_E384"] = entry(
+        nb_nv, ms, 2, "per-expert global scales; offsets kernel + quantize kernel")
+    del sc_nv
+
     # the same MoE batch with the dispatch gather fused in: token rows
     # [16384, 7168] + int32 route->token indices, against the unfused pair
     # (torch index_select materialising the 1.9 GB permuted matrix, then the

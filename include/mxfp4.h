@@ -234,6 +234,39 @@ int mxfp4_swap_w13(const uint8_t* codes_in, const uint8_t* scales_in,
                    void* w13_bias_out, const float* w2_bias_in,
                    int64_t w2_bias_numel, void* w2_bias_out, void* stream);
 
+/* mxfp4_nvfp4_grouped_scale_bytes_bound — scale buffer size that always
+ * suffices for mxfp4_quantize_nvfp4_grouped:
+ * floor((total_rows + 127*E) / 128) * 128 * ceil(K/64) * 4 bytes
+ * (0 for invalid sizes). */
+size_t mxfp4_nvfp4_grouped_scale_bytes_bound(int64_t total_rows, int32_t E, int64_t K);
+
+/* mxfp4_quantize_nvfp4_grouped — NVFP4 "experts quant": the NVFP4 branch of
+ * the experts-quant kernel ([PR43557] "Implementation breakdown" items 1 and
+ * 3) over expert segments.  Rows [o[e], o[e+1]) of x form segment e; each
+ * segment is quantized exactly as mxfp4_quantize_nvfp4 would quantize it
+ * alone with global scale global_scales[e].  Codes keep the row order;
+ * segment e's tiled E4M3 scales (16-element columns, padded to 128 rows)
+ * start at byte P[e] * ceil(K/64) * 4, P[e] = sum_{e'<e} ceil(n_e'/128)*128.
+ * One global scale per expert is this library's reading (the pages show the
+ * scale as one argument of the conversion); a single scale for all experts
+ * is the case of E equal entries.
+ *
+ * x                  BF16 [total_rows, K], contiguous, 16-byte aligned; K % 16 == 0.
+ * expert_offsets     DEVICE int32 [E+1], 0 = o[0] <= ... <= o[E] = total_rows
+ *                    (checked on the device).
+ * global_scales      DEVICE float32 [E], positive finite (not checked).
+ * codes              [total_rows, K/2]; scales >= the bound above, 16-byte
+ *                    aligned; bytes past P[E] * ceil(K/64) * 4 are not touched.
+ * scale_row_offsets  DEVICE int32 [E+1], output P[0..E].
+ * status             DEVICE int32, output, may be NULL: MXFP4_OK or
+ *                    MXFP4_EOFFSETS (then scale_row_offsets is all -1 and
+ *                    codes/scales are left untouched).
+ */
+int mxfp4_quantize_nvfp4_grouped(const void* x, int64_t total_rows, int64_t K,
+                                 const int32_t* expert_offsets, int32_t E,
+                                 const float* global_scales, uint8_t* codes, uint8_t* scales,
+                                 int32_t* scale_row_offsets, int32_t* status, void* stream);
+
 /* ---------------------------------------------------------------- NVFP4
  * The other branch of the same quantize kernel on [PR43557] ("Implementation
  * breakdown" item 1, the non-UE8M0 branch of the cvt_warp_fp16_to_fp4

@@ -33,6 +33,8 @@ __all__ = [
     "quantize_grouped_gather", "mxfp4_quantize_grouped_scatter", "quantize_grouped_scatter",
     "MXFP4_SCATTER_MAX_TOP_K", "mxfp4_quantize_f16", "mxfp4_nvfp4_scale_bytes",
     "mxfp4_quantize_nvfp4", "mxfp4_dequantize_nvfp4", "quantize_nvfp4", "dequantize_nvfp4",
+    "mxfp4_nvfp4_grouped_scale_bytes_bound", "mxfp4_quantize_nvfp4_grouped",
+    "quantize_nvfp4_grouped",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300.so")
@@ -90,6 +92,10 @@ def _load(path=LIB_PATH):
     L.mxfp4_nvfp4_scale_bytes.argtypes = [i64, i64]
     L.mxfp4_quantize_nvfp4.restype = ctypes.c_int
     L.mxfp4_quantize_nvfp4.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp]
+    L.mxfp4_nvfp4_grouped_scale_bytes_bound.restype = ctypes.c_size_t
+    L.mxfp4_nvfp4_grouped_scale_bytes_bound.argtypes = [i64, i32, i64]
+    L.mxfp4_quantize_nvfp4_grouped.restype = ctypes.c_int
+    L.mxfp4_quantize_nvfp4_grouped.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp]
     L.mxfp4_dequantize_nvfp4.restype = ctypes.c_int
     L.mxfp4_dequantize_nvfp4.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     L.mxfp4_status_string.restype = ctypes.c_char_p
@@ -311,6 +317,35 @@ def mxfp4_quantize_nvfp4(x, global_scale, codes, scales, stream=None) -> None:
                "mxfp4_quantize_nvfp4")
 
 
+def mxfp4_nvfp4_grouped_scale_bytes_bound(total_rows: int, E: int, K: int) -> int:
+    return int(_lib.mxfp4_nvfp4_grouped_scale_bytes_bound(int(total_rows), int(E), int(K)))
+
+
+def mxfp4_quantize_nvfp4_grouped(x, expert_offsets, global_scales, codes, scales,
+                                 scale_row_offsets, status=None, stream=None) -> None:
+    """NVFP4 experts quant: segment e of the contiguous BF16 ``x`` with global
+    scale ``global_scales[e]`` (float32 device [E])."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("expert_offsets", expert_offsets, torch.int32)
+    _need_cuda("global_scales", global_scales, torch.float32)
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    _need_cuda("scale_row_offsets", scale_row_offsets, torch.int32)
+    _need_cuda("status", status, torch.int32)
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D tensor")
+    total, K = x.shape
+    E = expert_offsets.numel() - 1
+    if global_scales.numel() != E:
+        raise ValueError("global_scales needs one entry per expert")
+    with torch.cuda.device(_device_of(x, expert_offsets, global_scales, codes, scales,
+                                      scale_row_offsets, status)):
+        _check(_lib.mxfp4_quantize_nvfp4_grouped(
+            _ptr(x), total, K, _ptr(expert_offsets), E, _ptr(global_scales), _ptr(codes),
+            _ptr(scales), _ptr(scale_row_offsets), _ptr(status), _stream(stream, x.device)),
+            "mxfp4_quantize_nvfp4_grouped")
+
+
 def mxfp4_dequantize_nvfp4(codes, scales, global_scale, M: int, K: int, y, stream=None) -> None:
     _need_cuda("codes", codes, torch.uint8)
     _need_cuda("scales", scales, torch.uint8)
@@ -414,6 +449,22 @@ def quantize_nvfp4(x, global_scale, stream=None):
     scales = torch.empty(mxfp4_nvfp4_scale_bytes(M, K), dtype=torch.uint8, device=x.device)
     mxfp4_quantize_nvfp4(x, global_scale, codes, scales, stream)
     return codes, scales
+
+
+def quantize_nvfp4_grouped(x, expert_offsets, global_scales, stream=None):
+    """Returns (codes, scales, scale_row_offsets, status) of the NVFP4 experts
+    quant of the expert-sorted ``x``."""
+    total, K = x.shape
+    E = expert_offsets.numel() - 1
+    dev = x.device
+    codes = torch.empty((total, K // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty(max(mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K), 16),
+                         dtype=torch.uint8, device=dev)
+    sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    status = torch.empty(1, dtype=torch.int32, device=dev)
+    mxfp4_quantize_nvfp4_grouped(x, expert_offsets, global_scales, codes, scales, sro, status,
+                                 stream)
+    return codes, scales, sro, status
 
 
 def dequantize_nvfp4(codes, scales, global_scale, M: int, K: int, stream=None):

@@ -343,6 +343,52 @@ int mxfp4_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+size_t mxfp4_nvfp4_grouped_scale_bytes_bound(int64_t total_rows, int32_t E, int64_t K) {
+  if (total_rows < 0 || E < 0 || K <= 0 || K % 16 != 0) return 0;
+  const int64_t tiles = (total_rows + 127 * static_cast<int64_t>(E)) / 128;
+  return static_cast<size_t>(tiles * 128 * ceil_div(K / 16, 4) * 4);
+}
+
+int mxfp4_quantize_nvfp4_grouped(const void* x, int64_t total_rows, int64_t K,
+                                 const int32_t* expert_offsets, int32_t E,
+                                 const float* global_scales, uint8_t* codes, uint8_t* scales,
+                                 int32_t* scale_row_offsets, int32_t* status, void* stream) {
+  if (total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
+  if (K % 16 != 0) return MXFP4_ESHAPE;
+  if (!expert_offsets || !scale_row_offsets) return MXFP4_EINVAL;
+  const bool work = total_rows > 0 && K > 0;
+  if (work && (!x || !codes || !scales || !global_scales)) return MXFP4_EINVAL;
+  if (E == 0 && total_rows > 0) return MXFP4_EINVAL;
+  const int64_t bound_tiles = (total_rows + 127 * static_cast<int64_t>(E)) / 128;
+  if (total_rows + 127 * static_cast<int64_t>(E) > INT32_MAX) return MXFP4_ESHAPE;
+  if (bound_tiles * ceil_div(ceil_div(K / 16, 4), 2) > kMaxGrid) return MXFP4_ESHAPE;
+  if (total_rows > 0 && K > 0 && total_rows > (INT64_MAX / 4) / K) return MXFP4_ESHAPE;
+  if ((x && !aligned16(x)) || (codes && !aligned16(codes)) || (scales && !aligned16(scales)) ||
+      (reinterpret_cast<uintptr_t>(global_scales) & 3u) ||
+      (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) ||
+      (reinterpret_cast<uintptr_t>(scale_row_offsets) & 3u) ||
+      (reinterpret_cast<uintptr_t>(status) & 3u))
+    return MXFP4_EALIGN;
+  const Range ins[3] = {range_of(x, work ? total_rows * K * 2 : 0),
+                        range_of(global_scales, work ? static_cast<int64_t>(E) * 4 : 0),
+                        range_of(expert_offsets, (static_cast<int64_t>(E) + 1) * 4)};
+  const Range outs[4] = {
+      range_of(codes, total_rows * (K / 2)),
+      range_of(scales,
+               static_cast<int64_t>(mxfp4_nvfp4_grouped_scale_bytes_bound(total_rows, E, K))),
+      range_of(scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4),
+      range_of(status, status ? 4 : 0)};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 3; ++j)
+      if (overlap(outs[i], ins[j])) return MXFP4_EALIAS;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(outs[i], outs[j])) return MXFP4_EALIAS;
+  }
+  return from_cuda(mxfp4::launch_quantize_nvfp4_grouped(
+      x, total_rows, K, expert_offsets, E, global_scales, codes, scales, scale_row_offsets,
+      status, K == 0 ? 0 : bound_tiles, static_cast<cudaStream_t>(stream)));
+}
+
 int mxfp4_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, const float* global_scale,
                            int64_t M, int64_t K, void* y, void* stream) {
   if (M < 0 || K < 0) return MXFP4_EINVAL;

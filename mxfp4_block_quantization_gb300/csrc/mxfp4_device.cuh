@@ -380,6 +380,29 @@ __device__ __forceinline__ uint2 lane_codes(const uint4 (&v)[2], uint32_t s) {
   return code;
 }
 
+// ------------------------------------------------ grouped segment lookup
+// Segment holding padded row `prow`: the last e in [0, E) with P[e] <= prow
+// (empty segments share their start with the next one, so the last such e
+// is never empty when prow < P[E]).  A proportional estimate is checked
+// first with two independent probes (exact whenever the segments are close to
+// uniform, as with balanced MoE routing); otherwise a binary search over the
+// side the estimate excluded.  P is small and read by every CTA (L1/L2 hits).
+__device__ __forceinline__ int find_segment(const int32_t* __restrict__ P, int E, int prow,
+                                            int total) {
+  int e = static_cast<int>(static_cast<int64_t>(prow) * E / total);
+  e = e < E - 1 ? e : E - 1;
+  const int pe = __ldg(P + e);
+  const int pn = __ldg(P + e + 1);
+  if (pe <= prow && prow < pn) return e;
+  int lo, hi;
+  if (pe <= prow) { lo = e + 1; hi = E - 1; } else { lo = 0; hi = e - 1; }
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(P + mid) <= prow) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // L2 policy that keeps lines resident ahead of streaming traffic, and a
 // 4-byte store under such a policy: for small stores that several CTAs
 // complete sector by sector (a sector evicted half written costs a DRAM read

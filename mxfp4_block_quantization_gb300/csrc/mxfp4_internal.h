@@ -23,6 +23,11 @@ cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K
                                     uint8_t* scales, int32_t* scale_row_offsets,
                                     int32_t* status, int64_t bound_tiles, cudaStream_t stream);
 
+// Validates expert offsets and writes the padded row starts P[0..E] (and
+// the status word) on the device; every grouped launcher runs it first.
+cudaError_t launch_offsets(const int32_t* offsets, int32_t E, int64_t total_rows,
+                           int32_t* scale_row_offsets, int32_t* status, cudaStream_t stream);
+
 // Grouped quantize of gathered rows: output row r reads source row
 // row_index[r] of x (row stride ldx elements, num_src_rows rows).
 cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K,
@@ -42,6 +47,13 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
 cudaError_t launch_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
                                   const float* global_scale, uint8_t* codes, uint8_t* scales,
                                   cudaStream_t stream);
+// NVFP4 experts quant: per-segment global scales [E], grouped scale layout.
+cudaError_t launch_quantize_nvfp4_grouped(const void* x, int64_t total_rows, int64_t K,
+                                          const int32_t* offsets, int32_t E,
+                                          const float* global_scales, uint8_t* codes,
+                                          uint8_t* scales, int32_t* scale_row_offsets,
+                                          int32_t* status, int64_t bound_tiles,
+                                          cudaStream_t stream);
 cudaError_t launch_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales,
                                     const float* global_scale, int64_t M, int64_t K, void* y,
                                     cudaStream_t stream);

@@ -65,28 +65,6 @@ struct QuantizeParams {
 // Buffer slots of QuantizeParams::dbg.
 enum : int { kDbgX = 0, kDbgCodes, kDbgScales, kDbgOffsets, kDbgPadded, kDbgRowIndex, kDbgStatus };
 
-// Segment holding padded row `prow`: the last e in [0, E) with P[e] <= prow
-// (empty segments share their start with the next one, so the last such e
-// is never empty when prow < P[E]).  A proportional estimate is checked
-// first with two independent probes (exact whenever the segments are close to
-// uniform, as with balanced MoE routing); otherwise a binary search over the
-// side the estimate excluded.  P is small and read by every CTA (L1/L2 hits).
-__device__ __forceinline__ int find_segment(const int32_t* __restrict__ P, int E, int prow,
-                                            int total) {
-  int e = static_cast<int>(static_cast<int64_t>(prow) * E / total);
-  e = e < E - 1 ? e : E - 1;
-  const int pe = __ldg(P + e);
-  const int pn = __ldg(P + e + 1);
-  if (pe <= prow && prow < pn) return e;
-  int lo, hi;
-  if (pe <= prow) { lo = e + 1; hi = E - 1; } else { lo = 0; hi = e - 1; }
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(P + mid) <= prow) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 // Lane l of warp w covers elements [16*(l%8), 16*(l%8)+16) of row
 // 4*w + l/8 (+32 per pass): two lanes per 32-element block.
 //
@@ -496,6 +474,9 @@ bool vec32_ok(const void* x, int64_t ldx_bytes) {
   return (reinterpret_cast<uintptr_t>(x) % 32 == 0) && (ldx_bytes % 32 == 0);
 }
 
+
+}  // namespace
+
 cudaError_t launch_offsets(const int32_t* offsets, int32_t E, int64_t total_rows,
                            int32_t* scale_row_offsets, int32_t* status, cudaStream_t stream) {
   OffsetsParams q{};
@@ -511,8 +492,6 @@ cudaError_t launch_offsets(const int32_t* offsets, int32_t E, int64_t total_rows
 #endif
   return launch_pdl(grouped_offsets_kernel, 1, kScanThreads, 0, stream, q);
 }
-
-}  // namespace
 
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
                             uint8_t* scales, bool f16, cudaStream_t stream) {

@@ -217,3 +217,25 @@ def test_debug_library_exports_both_headers(lib):
     missing = [n for n in names if not hasattr(L, n)]
     assert not missing, missing
     assert not hasattr(ctypes.CDLL(lib.LIB_PATH), "mxfp4_debug_bounds_violations")
+
+
+def test_nvfp4_grouped_validation(lib):
+    f = lib._lib.mxfp4_quantize_nvfp4_grouped
+    # x, total, K, off, E, g, codes, scales, sro, status, stream
+    ok = [A, 300, 64, 3 * A, 3, 7 * A, 4 * A, 5 * A, 6 * A, None, None]
+
+    def call(**kw):
+        names = ["x", "tot", "K", "off", "E", "g", "c", "s", "sro", "st", "strm"]
+        a = dict(zip(names, ok))
+        a.update(kw)
+        return f(*[a[n] for n in names])
+
+    assert call(K=40) == lib.MXFP4_ESHAPE
+    assert call(g=None) == lib.MXFP4_EINVAL
+    assert call(E=0) == lib.MXFP4_EINVAL
+    assert call(x=A + 8) == lib.MXFP4_EALIGN
+    assert call(g=7 * A + 2) == lib.MXFP4_EALIGN
+    assert call(c=A + 64) == lib.MXFP4_EALIAS                # codes overlap x
+    assert call(sro=7 * A) == lib.MXFP4_EALIAS               # offsets out overlap the scales in
+    assert lib.mxfp4_nvfp4_grouped_scale_bytes_bound(300, 3, 64) == (300 + 381) // 128 * 128 * 4
+    assert lib.mxfp4_nvfp4_grouped_scale_bytes_bound(300, 3, 40) == 0

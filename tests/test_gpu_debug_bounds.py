@@ -136,6 +136,11 @@ def test_everything_in_bounds(libs):
     wide3[:, :1056] = g3.x_tokens
     cases.append(lambda: written(mx.quantize_grouped_scatter(wide3[:, :1056], g3.dest_rows,
                                                              g3.offsets), 1056))
+    # NVFP4 experts quant (K a multiple of 16 but not 32 included)
+    gn = W.moe_grouped(seed=10, tokens=150, top_k=3, num_experts=7, K=80, device="cuda")
+    gsn = torch.linspace(0.5, 40.0, 7, device="cuda")
+    cases.append(lambda: mx.quantize_nvfp4_grouped(gn.x, gn.offsets, gsn)[:1] +
+                 (mx.quantize_nvfp4_grouped(gn.x, gn.offsets, gsn)[2],))
     # swap: tiled with N % 128 == 0 and != 0, flat aligned and not
     for E, two_n, K, tiled in [(2, 256, 2048, True), (3, 200, 160, True), (3, 200, 160, False),
                                (2, 256, 64, False)]:

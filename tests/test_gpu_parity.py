@@ -846,3 +846,77 @@ def test_nonfinite_inputs_do_not_fault(mx):
     _, _, _, st2 = mx.quantize_grouped_scatter(x, dst.view(M, 1).cuda(), off)
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and int(st2.item()) == 0
+
+
+# -------------------------------------------------- NVFP4 experts quant
+def run_nvfp4_grouped(mx, x, offsets, gs):
+    total, K = x.shape
+    E = offsets.numel() - 1
+    codes = Guarded(total * (K // 2), shape=(total, K // 2))
+    scales = Guarded(mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K))
+    sro = Guarded(4 * (E + 1), torch.int32)
+    status = Guarded(4, torch.int32)
+    mx.mxfp4_quantize_nvfp4_grouped(x, offsets, gs, codes.t, scales.t, sro.t, status.t)
+    torch.cuda.synchronize()
+    for g in (codes, scales, sro, status):
+        g.check()
+    return (codes.t.cpu().numpy(), scales.t.cpu().numpy(), sro.t.cpu().numpy(),
+            int(status.t.cpu()[0]))
+
+
+def _expert_gscales(E, seed):
+    rng = np.random.default_rng(seed)
+    return np.float32(448.0 * 6.0) / np.exp(rng.uniform(0.0, 3.0, E)).astype(np.float32)
+
+
+@pytest.mark.parametrize("tokens,top_k,E,K", [(200, 4, 12, 288), (130, 2, 5, 80),
+                                              (64, 3, 9, 2880), (1, 1, 3, 16)])
+def test_nvfp4_grouped_matches_oracle(mx, tokens, top_k, E, K):
+    g = W.moe_grouped(seed=tokens + K, tokens=tokens, top_k=top_k, num_experts=E, K=K,
+                      device="cuda")
+    gs = _expert_gscales(E, K)
+    c, s, sro, st = run_nvfp4_grouped(mx, g.x, g.offsets, torch.from_numpy(gs).cuda())
+    rc, c_o, s_o, sro_o = oracle.nvfp4_quantize_grouped(bits(g.x), g.offsets.cpu().numpy(), gs)
+    assert st == 0 and rc == 0 and np.array_equal(sro, sro_o)
+    assert np.array_equal(c, c_o), _first_diff(c, c_o)
+    used = int(sro_o[-1]) * ((K // 16 + 3) // 4 * 4)
+    assert np.array_equal(s[:used], s_o[:used]), _first_diff(s[:used], s_o[:used])
+    assert (s[used:] == 0xA5).all(), "slack past P[E] must be untouched"
+
+
+def test_nvfp4_grouped_empty_segments_16b_input_and_bad_offsets(mx):
+    x = W.small_matrix(6, 400, 192).cuda()
+    gs = torch.tensor([1.0, 3.0, 0.5, 9.0, 2.0], device="cuda")
+    off = torch.tensor([0, 0, 129, 129, 400, 400], dtype=torch.int32, device="cuda")
+    for xx in (x, offset16(x)):
+        c, s, sro, st = run_nvfp4_grouped(mx, xx, off, gs)
+        rc, c_o, s_o, sro_o = oracle.nvfp4_quantize_grouped(bits(x), off.cpu().numpy(),
+                                                            gs.cpu().numpy())
+        used = int(sro_o[-1]) * 12
+        assert st == 0 and np.array_equal(c, c_o) and np.array_equal(s[:used], s_o[:used])
+    bad = torch.tensor([0, 300, 200, 200, 400, 400], dtype=torch.int32, device="cuda")
+    c, s, sro, st = run_nvfp4_grouped(mx, x, bad, gs)
+    assert st == mx.MXFP4_EOFFSETS and (sro == -1).all()
+    assert (c == 0xA5).all() and (s == 0xA5).all()
+
+
+def test_nvfp4_grouped_moe_full_size_sampled(mx):
+    """131,072 x 7168 expert-sorted rows, 384 experts with their own global
+    scales: every padded offset, and 8 experts' codes and scale chunks against
+    the oracle's dense NVFP4 of the segment."""
+    g = W.moe_grouped(seed=2, device="cuda")
+    E = g.num_experts
+    gs = _expert_gscales(E, 2)
+    codes, scales, sro, st = mx.quantize_nvfp4_grouped(g.x, g.offsets, torch.from_numpy(gs).cuda())
+    torch.cuda.synchronize()
+    assert int(st.cpu()[0]) == 0
+    off_h = g.offsets.cpu().numpy().astype(np.int64)
+    want_sro = np.concatenate([[0], np.cumsum((np.diff(off_h) + 127) // 128 * 128)])
+    assert np.array_equal(sro.cpu().numpy(), want_sro)
+    pk = 7168 // 16
+    for e in (0, 5, 77, 190, 250, 301, 350, E - 1):
+        a, b = int(off_h[e]), int(off_h[e + 1])
+        c_o, s_o = oracle.nvfp4_quantize(bits(g.x[a:b]), float(gs[e]))
+        assert np.array_equal(codes[a:b].cpu().numpy(), c_o), e
+        p0 = int(want_sro[e]) * pk
+        assert np.array_equal(scales[p0:p0 + s_o.size].cpu().numpy(), s_o), e
