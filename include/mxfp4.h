@@ -32,8 +32,8 @@
  *     value, before anything is enqueued; outputs are then untouched.
  *   - A failed kernel launch returns MXFP4_ECUDA.
  *   - Errors only the device can see (malformed expert offsets, gather
- *     indices out of range) are written to a caller-provided device status
- *     word.
+ *     indices or scatter entries out of range) are written to a
+ *     caller-provided device status word.
  *   - Size 0 (M == 0, K == 0, E == 0 with no rows) is a valid no-op.
  *   - No kernel of this library waits on another CTA or on the host.
  */
@@ -53,11 +53,12 @@ typedef enum {
   MXFP4_OK = 0,
   MXFP4_EINVAL = -1,   /* NULL pointer, negative size, bad flag value            */
   MXFP4_EALIGN = -2,   /* pointer or row stride breaks the 16-byte rule            */
-  MXFP4_ESHAPE = -3,   /* K % 32 != 0, ldx < K, odd two_n, size overflow          */
+  MXFP4_ESHAPE = -3,   /* K % 32 != 0 (16 for NVFP4), ldx < K, odd two_n, overflow */
   MXFP4_EALIAS = -4,   /* an output byte range overlaps an input or another output */
   MXFP4_ECUDA = -5,    /* the CUDA runtime refused a launch                        */
   MXFP4_EOFFSETS = -6, /* device-detected: expert offsets not 0 = o[0] <= ... <= o[E] = rows */
-  MXFP4_EINDEX = -7    /* device-detected: a gather row index outside [0, num_src_rows) */
+  MXFP4_EINDEX = -7    /* device-detected: a gather row index outside [0, num_src_rows),
+                          or a scatter entry outside [-1, total_rows) */
 } mxfp4_status;
 
 /* Bytes of the 128x4-tiled scale buffer of an [M, K] matrix:
