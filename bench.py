@@ -298,6 +298,37 @@ def time_launches(fn, iters, stream, warmup=3):
     return s.elapsed_time(e) / iters
 
 
+def tiled_scale_index(M, K, device="cpu"):
+    """[M, K/32] byte offsets of the scale bytes in the 128x4-tiled layout:
+    chunk (r/128, c/4) of 512 bytes, byte (r%32)*16 + ((r%128)/32)*4 + c%4."""
+    import torch
+    r = torch.arange(M, device=device).view(M, 1)
+    c = torch.arange(K // 32, device=device).view(1, K // 32)
+    nkt = (K // 32 + 3) // 4
+    return ((r // 128) * nkt + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4
+
+
+def reconstruction_report(mx, x, codes, scales):
+    """Reconstruction error of the headline matrix, from the GPU's own outputs
+    (outside every timed region): relative L2 of dequantize(quantize(x))
+    against x in float64, and the elements the E2M1 range clips, i.e. with
+    |x| > 6 * 2^(s-127) for their block's scale byte s (read back from the
+    128x4-tiled layout)."""
+    import torch
+    M, K = x.shape
+    y = mx.dequantize(codes, scales, M, K)
+    xd, yd = x.double(), y.double()
+    rel = float(torch.linalg.vector_norm(yd - xd) / torch.linalg.vector_norm(xd))
+    s = scales[tiled_scale_index(M, K, x.device)].to(torch.float64)
+    blk = torch.exp2(s - 127.0).repeat_interleave(32, dim=1)
+    live = (s > 0).repeat_interleave(32, dim=1)
+    sat = int(((xd.abs() > 6.0 * blk) & live).sum())
+    return {"rel_l2": round(rel, 6), "saturated_elements": sat,
+            "saturated_fraction": round(sat / (M * K), 6),
+            "matrix": f"{M}x{K} dense activation (the headline input)",
+            "how": "dequantize(quantize(x)) vs x in float64; saturated = |x| > 6 * 2^(s-127)"}
+
+
 def time_graph(fn, iters):
     """Per-call device time of `iters` calls fn(i, stream) captured once in a
     CUDA graph on a side stream and replayed there: for kernels shorter than
@@ -531,10 +562,12 @@ def run_ours(args):
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
+    torch.cuda.nvtx.range_push(f"timed: {args.steps} x mxfp4_quantize {M_DENSE}x{K_DENSE}")
     ev0.record(stream)
     for i in range(args.steps):
         step(i)
     ev1.record(stream)
+    torch.cuda.nvtx.range_pop()
     ev1.synchronize()
     torch.cuda.synchronize()
     t_wall1 = time.time()
@@ -599,12 +632,16 @@ def run_ours(args):
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push(f"e2e: {e2e_steps} pipelined host->device / quantize / device->host steps")
     e0.record(stream)
     e2e_run(e2e_steps)
     e1.record(stream)
+    torch.cuda.nvtx.range_pop()
     e1.synchronize()
     e2e_ms, e2e_bytes = aggregate(e0.elapsed_time(e1), nbytes * e2e_steps)
     e2e_val = e2e_bytes / (e2e_ms * 1e-3) / 1e9
+
+    quality = reconstruction_report(mx, x0, codes[0], scales[0]) if rank == 0 else None
 
     rows = None
     if not args.no_rows:
@@ -646,6 +683,7 @@ def run_ours(args):
             "gpu_launches": args.steps,
             "clocks": clocks.summary(t_wall0, t_wall1),
             "cpu_baseline": cpu,
+            "quality": quality,
             "rows": rows,
         }
         print(json.dumps(line), flush=True)

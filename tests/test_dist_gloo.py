@@ -76,3 +76,15 @@ def test_reference_arm_json_contract(capsys, monkeypatch):
     assert d["higher_is_better"] is True and d["steps"] == 3 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+
+
+def test_bench_untile_index_matches_oracle(orc):
+    """The benchmark's quality report reads scale bytes back through the same
+    layout as the oracle's untile."""
+    import numpy as np
+    import bench
+    rng = np.random.default_rng(4)
+    for M, K in ((129, 160), (300, 2880), (128, 256)):
+        tiled = rng.integers(0, 256, orc.scale_bytes(M, K), dtype=np.uint8)
+        idx = bench.tiled_scale_index(M, K).numpy()
+        assert np.array_equal(tiled[idx], orc.untile(tiled, M, K // 32))
