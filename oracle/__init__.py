@@ -95,6 +95,16 @@ def lib():
         L.orc_nvfp4_quantize_grouped.restype = ctypes.c_int
         L.orc_nvfp4_quantize_grouped.argtypes = [_u16p, _i64, _i64, _i32p, ctypes.c_int32, _f32p,
                                                  _u8p, _u8p, _i32p]
+        L.orc_quantize_grouped_f16.restype = ctypes.c_int
+        L.orc_quantize_grouped_f16.argtypes = [_u16p, _i64, _i64, _i32p, ctypes.c_int32,
+                                               _u8p, _u8p, _i32p]
+        L.orc_quantize_grouped_gather_f16.restype = ctypes.c_int
+        L.orc_quantize_grouped_gather_f16.argtypes = [_u16p, _i64, _i64, _i64, _i32p, _i64,
+                                                      _i32p, ctypes.c_int32, _u8p, _u8p, _i32p]
+        L.orc_quantize_grouped_scatter_f16.restype = ctypes.c_int
+        L.orc_quantize_grouped_scatter_f16.argtypes = [_u16p, _i64, _i64, _i64, _i32p,
+                                                       ctypes.c_int32, _i64, _i32p,
+                                                       ctypes.c_int32, _u8p, _u8p, _i32p]
         L.orc_quantize_grouped_scatter.restype = ctypes.c_int
         L.orc_quantize_grouped_scatter.argtypes = [_u16p, _i64, _i64, _i64, _i32p, ctypes.c_int32,
                                                    _i64, _i32p, ctypes.c_int32, _u8p, _u8p, _i32p]
@@ -241,7 +251,7 @@ def grouped_scale_bytes_bound(total_rows: int, E: int, K: int) -> int:
     return tiles * 128 * ((K // 32 + 3) // 4 * 4)
 
 
-def quantize_grouped(xbits: np.ndarray, offsets: np.ndarray):
+def quantize_grouped(xbits: np.ndarray, offsets: np.ndarray, f16: bool = False):
     """Step 6: (rc, codes, scales, scale_row_offsets); rc is 0 or -6."""
     x = _c(xbits, np.uint16)
     off = _c(offsets, np.int32)
@@ -250,8 +260,9 @@ def quantize_grouped(xbits: np.ndarray, offsets: np.ndarray):
     codes = np.zeros((total, K // 2), np.uint8)
     scales = np.zeros(max(grouped_scale_bytes_bound(total, E, K), 1), np.uint8)
     sro = np.zeros(E + 1, np.int32)
-    rc = lib().orc_quantize_grouped(_p(x, _u16p), total, K, _p(off, _i32p), E,
-                                    _p(codes, _u8p), _p(scales, _u8p), _p(sro, _i32p))
+    fn = lib().orc_quantize_grouped_f16 if f16 else lib().orc_quantize_grouped
+    rc = fn(_p(x, _u16p), total, K, _p(off, _i32p), E, _p(codes, _u8p), _p(scales, _u8p),
+            _p(sro, _i32p))
     return rc, codes, scales, sro
 
 
@@ -291,7 +302,8 @@ def quantize_flat_f16(hbits: np.ndarray):
     return codes, flat
 
 
-def quantize_grouped_gather(xbits: np.ndarray, row_index: np.ndarray, offsets: np.ndarray):
+def quantize_grouped_gather(xbits: np.ndarray, row_index: np.ndarray, offsets: np.ndarray,
+                            f16: bool = False):
     """Step 6 on rows x[row_index]: (rc, codes, scales, scale_row_offsets);
     rc is 0, -6 (bad offsets) or -7 (an index out of range, zero row)."""
     x = _c(xbits, np.uint16)
@@ -303,14 +315,14 @@ def quantize_grouped_gather(xbits: np.ndarray, row_index: np.ndarray, offsets: n
     codes = np.zeros((total, K // 2), np.uint8)
     scales = np.zeros(max(grouped_scale_bytes_bound(total, E, K), 1), np.uint8)
     sro = np.zeros(E + 1, np.int32)
-    rc = lib().orc_quantize_grouped_gather(_p(x, _u16p), n_src, K, K, _p(idx, _i32p), total,
-                                           _p(off, _i32p), E, _p(codes, _u8p), _p(scales, _u8p),
-                                           _p(sro, _i32p))
+    fn = lib().orc_quantize_grouped_gather_f16 if f16 else lib().orc_quantize_grouped_gather
+    rc = fn(_p(x, _u16p), n_src, K, K, _p(idx, _i32p), total, _p(off, _i32p), E,
+            _p(codes, _u8p), _p(scales, _u8p), _p(sro, _i32p))
     return rc, codes, scales, sro
 
 
 def quantize_grouped_scatter(xbits: np.ndarray, dest_rows: np.ndarray, offsets: np.ndarray,
-                             total_rows: int, codes=None, scales=None):
+                             total_rows: int, codes=None, scales=None, f16: bool = False):
     """Step 6 with the dispatch as a scatter: route j of token t is row
     dest_rows[t, j] of the expert-sorted batch (-1: not dispatched).
     Returns (rc, codes, scales, scale_row_offsets); rc is 0, -6 (bad offsets)
@@ -331,9 +343,9 @@ def quantize_grouped_scatter(xbits: np.ndarray, dest_rows: np.ndarray, offsets: 
               else np.array(scales, np.uint8, copy=True).ravel())
     assert scales.size >= grouped_scale_bytes_bound(total_rows, E, K)
     sro = np.zeros(E + 1, np.int32)
-    rc = lib().orc_quantize_grouped_scatter(_p(x, _u16p), T, K, K, _p(dst, _i32p), top_k,
-                                            total_rows, _p(off, _i32p), E, _p(codes, _u8p),
-                                            _p(scales, _u8p), _p(sro, _i32p))
+    fn = lib().orc_quantize_grouped_scatter_f16 if f16 else lib().orc_quantize_grouped_scatter
+    rc = fn(_p(x, _u16p), T, K, K, _p(dst, _i32p), top_k, total_rows, _p(off, _i32p), E,
+            _p(codes, _u8p), _p(scales, _u8p), _p(sro, _i32p))
     return rc, codes, scales, sro
 
 

@@ -314,9 +314,11 @@ void orc_quantize_f16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
  * this library's reading: every segment [o[e], o[e+1]) is quantized as its
  * own matrix, codes keep the row order, and segment e's tiled scales (padded
  * to a multiple of 128 rows by itself) start at padded row P[e]. */
-int orc_quantize_grouped(const uint16_t* x, int64_t total_rows, int64_t K,
-                         const int32_t* offsets, int32_t E, uint8_t* codes,
-                         uint8_t* scales, int32_t* scale_row_offsets) {
+typedef void (*dense_quantize_fn)(const uint16_t*, int64_t, int64_t, int64_t, uint8_t*, uint8_t*);
+
+static int grouped_with(dense_quantize_fn quantize, const uint16_t* x, int64_t total_rows,
+                        int64_t K, const int32_t* offsets, int32_t E, uint8_t* codes,
+                        uint8_t* scales, int32_t* scale_row_offsets) {
   int ok = (E >= 0) && offsets[0] == 0 && (int64_t)offsets[E] == total_rows;
   for (int32_t e = 0; ok && e < E; ++e) ok = offsets[e] <= offsets[e + 1];
   if (!ok) {
@@ -329,22 +331,37 @@ int orc_quantize_grouped(const uint16_t* x, int64_t total_rows, int64_t K,
   for (int32_t e = 0; e < E; ++e) {
     int64_t n = (int64_t)offsets[e + 1] - offsets[e];
     scale_row_offsets[e] = (int32_t)P;
-    orc_quantize(x + (int64_t)offsets[e] * K, n, K, K, codes + (int64_t)offsets[e] * (K / 2),
-                 scales + P * padded_sK);
+    quantize(x + (int64_t)offsets[e] * K, n, K, K, codes + (int64_t)offsets[e] * (K / 2),
+             scales + P * padded_sK);
     P += (n + 127) / 128 * 128;
   }
   scale_row_offsets[E] = (int32_t)P;
   return 0;
 }
 
+int orc_quantize_grouped(const uint16_t* x, int64_t total_rows, int64_t K,
+                         const int32_t* offsets, int32_t E, uint8_t* codes,
+                         uint8_t* scales, int32_t* scale_row_offsets) {
+  return grouped_with(orc_quantize, x, total_rows, K, offsets, E, codes, scales,
+                      scale_row_offsets);
+}
+
+/* The same for FP16 input (segments quantized by the FP16 dense quantize). */
+int orc_quantize_grouped_f16(const uint16_t* x, int64_t total_rows, int64_t K,
+                             const int32_t* offsets, int32_t E, uint8_t* codes,
+                             uint8_t* scales, int32_t* scale_row_offsets) {
+  return grouped_with(orc_quantize_f16, x, total_rows, K, offsets, E, codes, scales,
+                      scale_row_offsets);
+}
+
 /* Step 6 with the MoE dispatch gather in front ([PR43557] item 3: the
  * experts-quant input is the routed, expert-sorted activations): output row r
  * is source row row_index[r]; out-of-range indices give zero rows and -7.
  * Plainly: gather the rows, then the grouped quantize above. */
-int orc_quantize_grouped_gather(const uint16_t* x, int64_t num_src_rows, int64_t K, int64_t ldx,
-                                const int32_t* row_index, int64_t total_rows,
-                                const int32_t* offsets, int32_t E, uint8_t* codes,
-                                uint8_t* scales, int32_t* scale_row_offsets) {
+static int gather_with(dense_quantize_fn quantize, const uint16_t* x, int64_t num_src_rows,
+                       int64_t K, int64_t ldx, const int32_t* row_index, int64_t total_rows,
+                       const int32_t* offsets, int32_t E, uint8_t* codes, uint8_t* scales,
+                       int32_t* scale_row_offsets) {
   uint16_t* g = (uint16_t*)calloc((size_t)(total_rows * K) + 1, sizeof(uint16_t));
   int bad = 0;
   for (int64_t r = 0; r < total_rows; ++r) {
@@ -355,10 +372,26 @@ int orc_quantize_grouped_gather(const uint16_t* x, int64_t num_src_rows, int64_t
     }
     memcpy(g + r * K, x + src * ldx, (size_t)K * sizeof(uint16_t));
   }
-  int rc = orc_quantize_grouped(g, total_rows, K, offsets, E, codes, scales, scale_row_offsets);
+  int rc = grouped_with(quantize, g, total_rows, K, offsets, E, codes, scales, scale_row_offsets);
   free(g);
   if (rc != 0) return rc;
   return bad ? -7 : 0;
+}
+
+int orc_quantize_grouped_gather(const uint16_t* x, int64_t num_src_rows, int64_t K, int64_t ldx,
+                                const int32_t* row_index, int64_t total_rows,
+                                const int32_t* offsets, int32_t E, uint8_t* codes,
+                                uint8_t* scales, int32_t* scale_row_offsets) {
+  return gather_with(orc_quantize, x, num_src_rows, K, ldx, row_index, total_rows, offsets, E,
+                     codes, scales, scale_row_offsets);
+}
+
+int orc_quantize_grouped_gather_f16(const uint16_t* x, int64_t num_src_rows, int64_t K,
+                                    int64_t ldx, const int32_t* row_index, int64_t total_rows,
+                                    const int32_t* offsets, int32_t E, uint8_t* codes,
+                                    uint8_t* scales, int32_t* scale_row_offsets) {
+  return gather_with(orc_quantize_f16, x, num_src_rows, K, ldx, row_index, total_rows, offsets, E,
+                     codes, scales, scale_row_offsets);
 }
 
 /* Step 6 with the MoE dispatch as a scatter ([PR43557] item 3: the
@@ -371,10 +404,10 @@ int orc_quantize_grouped_gather(const uint16_t* x, int64_t num_src_rows, int64_t
  * segment's pad rows (zero scale bytes); rows no route targets are left as
  * they were.  An entry outside [-1, total_rows) is skipped and gives -7; bad
  * offsets give -6 and nothing is written but the -1 scale row offsets. */
-int orc_quantize_grouped_scatter(const uint16_t* x, int64_t num_tokens, int64_t K, int64_t ldx,
-                                 const int32_t* dest_rows, int32_t top_k, int64_t total_rows,
-                                 const int32_t* offsets, int32_t E, uint8_t* codes,
-                                 uint8_t* scales, int32_t* scale_row_offsets) {
+static int scatter_with(dense_quantize_fn quantize, const uint16_t* x, int64_t num_tokens,
+                        int64_t K, int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                        int64_t total_rows, const int32_t* offsets, int32_t E, uint8_t* codes,
+                        uint8_t* scales, int32_t* scale_row_offsets) {
   int bad = 0;
   uint16_t* g = (uint16_t*)calloc((size_t)(total_rows * K) + 1, sizeof(uint16_t));
   uint8_t* hit = (uint8_t*)calloc((size_t)total_rows + 1, 1);
@@ -396,7 +429,7 @@ int orc_quantize_grouped_scatter(const uint16_t* x, int64_t num_tokens, int64_t 
   int64_t bound_rows = (total_rows + 127 * (int64_t)(E > 0 ? E : 0)) / 128 * 128 + 128;
   uint8_t* tc = (uint8_t*)calloc((size_t)(total_rows * (K / 2)) + 1, 1);
   uint8_t* ts = (uint8_t*)calloc((size_t)(bound_rows * padded_sK) + 1, 1);
-  int rc = orc_quantize_grouped(g, total_rows, K, offsets, E, tc, ts, scale_row_offsets);
+  int rc = grouped_with(quantize, g, total_rows, K, offsets, E, tc, ts, scale_row_offsets);
   if (rc == 0) {
     for (int32_t e = 0; e < E; ++e) {
       int64_t n = (int64_t)offsets[e + 1] - offsets[e];
@@ -418,6 +451,23 @@ int orc_quantize_grouped_scatter(const uint16_t* x, int64_t num_tokens, int64_t 
   free(ts);
   if (rc != 0) return rc;
   return bad ? -7 : 0;
+}
+
+int orc_quantize_grouped_scatter(const uint16_t* x, int64_t num_tokens, int64_t K, int64_t ldx,
+                                 const int32_t* dest_rows, int32_t top_k, int64_t total_rows,
+                                 const int32_t* offsets, int32_t E, uint8_t* codes,
+                                 uint8_t* scales, int32_t* scale_row_offsets) {
+  return scatter_with(orc_quantize, x, num_tokens, K, ldx, dest_rows, top_k, total_rows, offsets,
+                      E, codes, scales, scale_row_offsets);
+}
+
+int orc_quantize_grouped_scatter_f16(const uint16_t* x, int64_t num_tokens, int64_t K,
+                                     int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                     int64_t total_rows, const int32_t* offsets, int32_t E,
+                                     uint8_t* codes, uint8_t* scales,
+                                     int32_t* scale_row_offsets) {
+  return scatter_with(orc_quantize_f16, x, num_tokens, K, ldx, dest_rows, top_k, total_rows,
+                      offsets, E, codes, scales, scale_row_offsets);
 }
 
 /* Step 7 — dequantize: for each element, its nibble and its block's scale

@@ -95,6 +95,19 @@ int orc_quantize_grouped_scatter(const uint16_t* x, int64_t num_tokens, int64_t 
                                  const int32_t* dest_rows, int32_t top_k, int64_t total_rows,
                                  const int32_t* offsets, int32_t E, uint8_t* codes,
                                  uint8_t* scales, int32_t* scale_row_offsets);
+/* FP16 input for the three grouped forms (segments quantized as orc_quantize_f16). */
+int orc_quantize_grouped_f16(const uint16_t* x, int64_t total_rows, int64_t K,
+                             const int32_t* offsets, int32_t E, uint8_t* codes,
+                             uint8_t* scales, int32_t* scale_row_offsets);
+int orc_quantize_grouped_gather_f16(const uint16_t* x, int64_t num_src_rows, int64_t K,
+                                    int64_t ldx, const int32_t* row_index, int64_t total_rows,
+                                    const int32_t* offsets, int32_t E, uint8_t* codes,
+                                    uint8_t* scales, int32_t* scale_row_offsets);
+int orc_quantize_grouped_scatter_f16(const uint16_t* x, int64_t num_tokens, int64_t K,
+                                     int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                     int64_t total_rows, const int32_t* offsets, int32_t E,
+                                     uint8_t* codes, uint8_t* scales,
+                                     int32_t* scale_row_offsets);
 /* Step 7: codes + tiled scales -> BF16 [M, K]. */
 void orc_dequantize(const uint8_t* codes, const uint8_t* tiled_scales,
                     int64_t M, int64_t K, uint16_t* y);

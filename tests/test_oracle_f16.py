@@ -57,3 +57,33 @@ def test_f16_and_bf16_agree_on_shared_values(orc):
     cb, sb = orc.quantize(W.bf16_bits(x))
     ch, sh = orc.quantize_f16(x16.view(torch.int16).numpy().view(np.uint16))
     assert np.array_equal(cb, ch) and np.array_equal(sb, sh)
+
+
+def test_f16_grouped_forms_compose(orc):
+    """FP16 grouped quantize equals the FP16 dense quantize of every segment;
+    the FP16 gather and scatter forms equal the FP16 grouped quantize of the
+    permuted matrix (the composition the BF16 forms are pinned by)."""
+    import torch
+    g = W.moe_grouped(seed=4, tokens=70, top_k=3, num_experts=6, K=96)
+    xt = g.x_tokens.float().to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    idx = g.row_index.numpy()
+    dst = g.dest_rows.numpy()
+    off = g.offsets.numpy()
+    xs = xt[idx]
+    rc, c, s, sro = orc.quantize_grouped(xs, off, f16=True)
+    assert rc == 0
+    pk = 4
+    for e in range(6):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            c_e, s_e = orc.quantize_f16(xs[a:b])
+            assert np.array_equal(c[a:b], c_e)
+            assert np.array_equal(s[sro[e] * pk:sro[e] * pk + s_e.size], s_e)
+    rc2, c2, s2, sro2 = orc.quantize_grouped_gather(xt, idx, off, f16=True)
+    rc3, c3, s3, sro3 = orc.quantize_grouped_scatter(xt, dst, off, idx.size, f16=True)
+    assert rc2 == rc3 == 0
+    for a_, b_ in ((c, c2), (s, s2), (c, c3), (s, s3), (sro, sro2), (sro, sro3)):
+        assert np.array_equal(a_, b_)
+    # and FP16 differs from reading the same bits as BF16 (the flag is live)
+    rc4, c4, _, _ = orc.quantize_grouped(xs, off)
+    assert not np.array_equal(c, c4)
