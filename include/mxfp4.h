@@ -195,6 +195,29 @@ int mxfp4_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
                                    uint8_t* scales, int32_t* scale_row_offsets,
                                    int32_t* status, void* stream);
 
+/* FP16 input for the grouped forms: mxfp4_quantize_grouped_f16,
+ * mxfp4_quantize_grouped_gather_f16 and mxfp4_quantize_grouped_scatter_f16
+ * take IEEE binary16 bit patterns in x and otherwise behave exactly as the
+ * BF16 calls of the same name (arguments, layouts, status, errors), with the
+ * element step of mxfp4_quantize_f16 ([PR43557] cvt_warp_fp16_to_fp4: the
+ * experts-quant kernel converts 16-bit inputs of either kind). */
+int mxfp4_quantize_grouped_f16(const void* x, int64_t total_rows, int64_t K,
+                               const int32_t* expert_offsets, int32_t E,
+                               uint8_t* codes, uint8_t* scales,
+                               int32_t* scale_row_offsets, int32_t* status,
+                               void* stream);
+int mxfp4_quantize_grouped_gather_f16(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
+                                      const int32_t* row_index, int64_t total_rows,
+                                      const int32_t* expert_offsets, int32_t E, uint8_t* codes,
+                                      uint8_t* scales, int32_t* scale_row_offsets,
+                                      int32_t* status, void* stream);
+int mxfp4_quantize_grouped_scatter_f16(const void* x, int64_t num_tokens, int64_t K, int64_t ldx,
+                                       const int32_t* dest_rows, int32_t top_k,
+                                       int64_t total_rows, const int32_t* expert_offsets,
+                                       int32_t E, uint8_t* codes, uint8_t* scales,
+                                       int32_t* scale_row_offsets, int32_t* status,
+                                       void* stream);
+
 /* mxfp4_dequantize — packed codes + tiled scales -> BF16 [M, K].
  *
  * The inverse mapping of the format ([PR46915] "Motivation": FP4 -> BF16

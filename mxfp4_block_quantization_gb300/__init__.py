@@ -31,7 +31,8 @@ __all__ = [
     "swap_w13", "MXFP4_OK", "MXFP4_EINVAL", "MXFP4_EALIGN", "MXFP4_ESHAPE", "MXFP4_EALIAS",
     "MXFP4_ECUDA", "MXFP4_EOFFSETS", "MXFP4_EINDEX", "mxfp4_quantize_grouped_gather",
     "quantize_grouped_gather", "mxfp4_quantize_grouped_scatter", "quantize_grouped_scatter",
-    "MXFP4_SCATTER_MAX_TOP_K", "mxfp4_quantize_f16", "mxfp4_nvfp4_scale_bytes",
+    "MXFP4_SCATTER_MAX_TOP_K", "mxfp4_quantize_f16", "mxfp4_quantize_grouped_f16",
+    "mxfp4_quantize_grouped_gather_f16", "mxfp4_quantize_grouped_scatter_f16", "mxfp4_nvfp4_scale_bytes",
     "mxfp4_quantize_nvfp4", "mxfp4_dequantize_nvfp4", "quantize_nvfp4", "dequantize_nvfp4",
     "mxfp4_nvfp4_grouped_scale_bytes_bound", "mxfp4_quantize_nvfp4_grouped",
     "quantize_nvfp4_grouped",
@@ -78,6 +79,14 @@ def _load(path=LIB_PATH):
     L.mxfp4_quantize_f16.argtypes = [vp, i64, i64, i64, vp, vp, vp]
     L.mxfp4_quantize_grouped.restype = ctypes.c_int
     L.mxfp4_quantize_grouped.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp]
+    L.mxfp4_quantize_grouped_f16.restype = ctypes.c_int
+    L.mxfp4_quantize_grouped_f16.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp]
+    L.mxfp4_quantize_grouped_gather_f16.restype = ctypes.c_int
+    L.mxfp4_quantize_grouped_gather_f16.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, vp,
+                                                    vp, vp, vp]
+    L.mxfp4_quantize_grouped_scatter_f16.restype = ctypes.c_int
+    L.mxfp4_quantize_grouped_scatter_f16.argtypes = [vp, i64, i64, i64, vp, i32, i64, vp, i32,
+                                                     vp, vp, vp, vp, vp]
     L.mxfp4_quantize_grouped_gather.restype = ctypes.c_int
     L.mxfp4_quantize_grouped_gather.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, vp, vp,
                                                 vp, vp]
@@ -190,11 +199,9 @@ def mxfp4_quantize_f16(x, codes, scales, stream=None) -> None:
                                        _stream(stream, x.device)), "mxfp4_quantize_f16")
 
 
-def mxfp4_quantize_grouped(x, expert_offsets, codes, scales, scale_row_offsets, status=None,
-                           stream=None) -> None:
-    """Per-expert quantize of contiguous BF16 rows ``x`` [total_rows, K]
-    delimited by int32 ``expert_offsets`` [E+1] (device)."""
-    _need_cuda("x", x, torch.bfloat16)
+def _grouped(x, expert_offsets, codes, scales, scale_row_offsets, status, stream, f16):
+    name = "mxfp4_quantize_grouped" + ("_f16" if f16 else "")
+    _need_cuda("x", x, torch.float16 if f16 else torch.bfloat16)
     _need_cuda("expert_offsets", expert_offsets, torch.int32)
     _need_cuda("codes", codes, torch.uint8)
     _need_cuda("scales", scales, torch.uint8)
@@ -205,17 +212,27 @@ def mxfp4_quantize_grouped(x, expert_offsets, codes, scales, scale_row_offsets, 
     total, K = x.shape
     E = expert_offsets.numel() - 1
     with torch.cuda.device(_device_of(x, expert_offsets, codes, scales, scale_row_offsets, status)):
-        _check(_lib.mxfp4_quantize_grouped(_ptr(x), total, K, _ptr(expert_offsets), E,
-                                           _ptr(codes), _ptr(scales), _ptr(scale_row_offsets),
-                                           _ptr(status), _stream(stream, x.device)),
-               "mxfp4_quantize_grouped")
+        _check(getattr(_lib, name)(_ptr(x), total, K, _ptr(expert_offsets), E, _ptr(codes),
+                                   _ptr(scales), _ptr(scale_row_offsets), _ptr(status),
+                                   _stream(stream, x.device)), name)
 
 
-def mxfp4_quantize_grouped_gather(x, row_index, expert_offsets, codes, scales, scale_row_offsets,
-                                  status=None, stream=None) -> None:
-    """Grouped quantize of the rows ``x[row_index]`` (int32 device indices)
-    without materialising the gathered BF16 matrix."""
-    _need_cuda("x", x, torch.bfloat16)
+def mxfp4_quantize_grouped(x, expert_offsets, codes, scales, scale_row_offsets, status=None,
+                           stream=None) -> None:
+    """Per-expert quantize of contiguous BF16 rows ``x`` [total_rows, K]
+    delimited by int32 ``expert_offsets`` [E+1] (device)."""
+    _grouped(x, expert_offsets, codes, scales, scale_row_offsets, status, stream, False)
+
+
+def mxfp4_quantize_grouped_f16(x, expert_offsets, codes, scales, scale_row_offsets, status=None,
+                               stream=None) -> None:
+    """mxfp4_quantize_grouped for FP16 ``x``."""
+    _grouped(x, expert_offsets, codes, scales, scale_row_offsets, status, stream, True)
+
+
+def _gather(x, row_index, expert_offsets, codes, scales, scale_row_offsets, status, stream, f16):
+    name = "mxfp4_quantize_grouped_gather" + ("_f16" if f16 else "")
+    _need_cuda("x", x, torch.float16 if f16 else torch.bfloat16)
     _need_cuda("row_index", row_index, torch.int32)
     _need_cuda("expert_offsets", expert_offsets, torch.int32)
     _need_cuda("codes", codes, torch.uint8)
@@ -230,19 +247,29 @@ def mxfp4_quantize_grouped_gather(x, row_index, expert_offsets, codes, scales, s
     E = expert_offsets.numel() - 1
     with torch.cuda.device(_device_of(x, row_index, expert_offsets, codes, scales,
                                       scale_row_offsets, status)):
-        _check(_lib.mxfp4_quantize_grouped_gather(
+        _check(getattr(_lib, name)(
             _ptr(x), n_src, K, x.stride(0), _ptr(row_index), row_index.numel(),
             _ptr(expert_offsets), E, _ptr(codes), _ptr(scales), _ptr(scale_row_offsets),
-            _ptr(status), _stream(stream, x.device)), "mxfp4_quantize_grouped_gather")
+            _ptr(status), _stream(stream, x.device)), name)
 
 
-def mxfp4_quantize_grouped_scatter(x, dest_rows, expert_offsets, total_rows: int, codes, scales,
-                                   scale_row_offsets, status=None, stream=None) -> None:
-    """Grouped quantize with the dispatch given token -> rows: route j of
-    token t is row ``dest_rows[t, j]`` (int32 device [T, top_k], -1 = not
-    dispatched) of the ``total_rows``-row expert-sorted batch.  Each token
-    row is read and quantized once; rows no route targets are not written."""
-    _need_cuda("x", x, torch.bfloat16)
+def mxfp4_quantize_grouped_gather(x, row_index, expert_offsets, codes, scales, scale_row_offsets,
+                                  status=None, stream=None) -> None:
+    """Grouped quantize of the rows ``x[row_index]`` (int32 device indices)
+    without materialising the gathered BF16 matrix."""
+    _gather(x, row_index, expert_offsets, codes, scales, scale_row_offsets, status, stream, False)
+
+
+def mxfp4_quantize_grouped_gather_f16(x, row_index, expert_offsets, codes, scales,
+                                      scale_row_offsets, status=None, stream=None) -> None:
+    """mxfp4_quantize_grouped_gather for FP16 ``x``."""
+    _gather(x, row_index, expert_offsets, codes, scales, scale_row_offsets, status, stream, True)
+
+
+def _scatter(x, dest_rows, expert_offsets, total_rows, codes, scales, scale_row_offsets, status,
+             stream, f16):
+    name = "mxfp4_quantize_grouped_scatter" + ("_f16" if f16 else "")
+    _need_cuda("x", x, torch.float16 if f16 else torch.bfloat16)
     _need_cuda("dest_rows", dest_rows, torch.int32)
     _need_cuda("expert_offsets", expert_offsets, torch.int32)
     _need_cuda("codes", codes, torch.uint8)
@@ -257,10 +284,28 @@ def mxfp4_quantize_grouped_scatter(x, dest_rows, expert_offsets, total_rows: int
     E = expert_offsets.numel() - 1
     with torch.cuda.device(_device_of(x, dest_rows, expert_offsets, codes, scales,
                                       scale_row_offsets, status)):
-        _check(_lib.mxfp4_quantize_grouped_scatter(
+        _check(getattr(_lib, name)(
             _ptr(x), T, K, x.stride(0), _ptr(dest_rows), dest_rows.shape[1], int(total_rows),
             _ptr(expert_offsets), E, _ptr(codes), _ptr(scales), _ptr(scale_row_offsets),
-            _ptr(status), _stream(stream, x.device)), "mxfp4_quantize_grouped_scatter")
+            _ptr(status), _stream(stream, x.device)), name)
+
+
+def mxfp4_quantize_grouped_scatter(x, dest_rows, expert_offsets, total_rows: int, codes, scales,
+                                   scale_row_offsets, status=None, stream=None) -> None:
+    """Grouped quantize with the dispatch given token -> rows: route j of
+    token t is row ``dest_rows[t, j]`` (int32 device [T, top_k], -1 = not
+    dispatched) of the ``total_rows``-row expert-sorted batch.  Each token
+    row is read and quantized once; rows no route targets are not written."""
+    _scatter(x, dest_rows, expert_offsets, total_rows, codes, scales, scale_row_offsets, status,
+             stream, False)
+
+
+def mxfp4_quantize_grouped_scatter_f16(x, dest_rows, expert_offsets, total_rows: int, codes,
+                                       scales, scale_row_offsets, status=None,
+                                       stream=None) -> None:
+    """mxfp4_quantize_grouped_scatter for FP16 ``x``."""
+    _scatter(x, dest_rows, expert_offsets, total_rows, codes, scales, scale_row_offsets, status,
+             stream, True)
 
 
 def mxfp4_dequantize(codes, scales, M: int, K: int, y, stream=None) -> None:
@@ -382,7 +427,7 @@ def quantize_grouped(x, expert_offsets, stream=None):
                          device=dev)
     sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
     status = torch.empty(1, dtype=torch.int32, device=dev)
-    mxfp4_quantize_grouped(x, expert_offsets, codes, scales, sro, status, stream)
+    _grouped(x, expert_offsets, codes, scales, sro, status, stream, x.dtype == torch.float16)
     return codes, scales, sro, status
 
 
@@ -397,7 +442,8 @@ def quantize_grouped_gather(x, row_index, expert_offsets, stream=None):
                          device=dev)
     sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
     status = torch.empty(1, dtype=torch.int32, device=dev)
-    mxfp4_quantize_grouped_gather(x, row_index, expert_offsets, codes, scales, sro, status, stream)
+    _gather(x, row_index, expert_offsets, codes, scales, sro, status, stream,
+            x.dtype == torch.float16)
     return codes, scales, sro, status
 
 
@@ -415,8 +461,8 @@ def quantize_grouped_scatter(x, dest_rows, expert_offsets, total_rows=None, stre
                          device=dev)
     sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
     status = torch.empty(1, dtype=torch.int32, device=dev)
-    mxfp4_quantize_grouped_scatter(x, dest_rows, expert_offsets, total, codes, scales, sro, status,
-                                   stream)
+    _scatter(x, dest_rows, expert_offsets, total, codes, scales, sro, status, stream,
+             x.dtype == torch.float16)
     return codes, scales, sro, status
 
 

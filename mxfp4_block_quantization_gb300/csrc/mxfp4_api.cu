@@ -97,24 +97,10 @@ int quantize_checked(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* 
                                           static_cast<cudaStream_t>(stream)));
 }
 
-}  // namespace
-
-extern "C" {
-
-int mxfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
-                   uint8_t* scales, void* stream) {
-  return quantize_checked(x, M, K, ldx, codes, scales, false, stream);
-}
-
-int mxfp4_quantize_f16(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
-                       uint8_t* scales, void* stream) {
-  return quantize_checked(x, M, K, ldx, codes, scales, true, stream);
-}
-
-int mxfp4_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
+int grouped_checked(const void* x, int64_t total_rows, int64_t K,
                            const int32_t* expert_offsets, int32_t E, uint8_t* codes,
                            uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
-                           void* stream) {
+                    bool f16, void* stream) {
   if (total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
   if (K % 32 != 0) return MXFP4_ESHAPE;
   if (!expert_offsets || !scale_row_offsets) return MXFP4_EINVAL;
@@ -145,15 +131,15 @@ int mxfp4_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
   }
   const int64_t tiles = (K == 0) ? 0 : bound_tiles;
   return from_cuda(mxfp4::launch_quantize_grouped(x, total_rows, K, expert_offsets, E, codes,
-                                                  scales, scale_row_offsets, status, tiles,
+                                                  scales, scale_row_offsets, status, tiles, f16,
                                                   static_cast<cudaStream_t>(stream)));
 }
 
-int mxfp4_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
+int gather_checked(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
                                   const int32_t* row_index, int64_t total_rows,
                                   const int32_t* expert_offsets, int32_t E, uint8_t* codes,
                                   uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
-                                  void* stream) {
+                   bool f16, void* stream) {
   if (num_src_rows < 0 || total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
   if (K % 32 != 0 || ldx < K) return MXFP4_ESHAPE;
   if (!expert_offsets || !scale_row_offsets) return MXFP4_EINVAL;
@@ -188,14 +174,15 @@ int mxfp4_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K
   }
   return from_cuda(mxfp4::launch_quantize_grouped_gather(
       x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E, codes, scales,
-      scale_row_offsets, status, K == 0 ? 0 : bound_tiles, static_cast<cudaStream_t>(stream)));
+      scale_row_offsets, status, K == 0 ? 0 : bound_tiles, f16,
+      static_cast<cudaStream_t>(stream)));
 }
 
-int mxfp4_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K, int64_t ldx,
+int scatter_checked(const void* x, int64_t num_tokens, int64_t K, int64_t ldx,
                                    const int32_t* dest_rows, int32_t top_k, int64_t total_rows,
                                    const int32_t* expert_offsets, int32_t E, uint8_t* codes,
                                    uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
-                                   void* stream) {
+                    bool f16, void* stream) {
   if (num_tokens < 0 || total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
   if (top_k < 1 || top_k > MXFP4_SCATTER_MAX_TOP_K) return MXFP4_EINVAL;
   if (K % 32 != 0 || ldx < K) return MXFP4_ESHAPE;
@@ -234,9 +221,79 @@ int mxfp4_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
   }
   return from_cuda(mxfp4::launch_quantize_grouped_scatter(
       x, reads ? num_tokens : 0, K, ldx, dest_rows, top_k, total_rows, expert_offsets, E, codes,
-      scales, scale_row_offsets, status, K == 0 ? 0 : bound_tiles,
+      scales, scale_row_offsets, status, K == 0 ? 0 : bound_tiles, f16,
       static_cast<cudaStream_t>(stream)));
 }
+
+}  // namespace
+
+extern "C" {
+
+int mxfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
+                   uint8_t* scales, void* stream) {
+  return quantize_checked(x, M, K, ldx, codes, scales, false, stream);
+}
+
+int mxfp4_quantize_f16(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
+                       uint8_t* scales, void* stream) {
+  return quantize_checked(x, M, K, ldx, codes, scales, true, stream);
+}
+
+int mxfp4_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
+                           const int32_t* expert_offsets, int32_t E, uint8_t* codes,
+                           uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
+                           void* stream) {
+  return grouped_checked(x, total_rows, K, expert_offsets, E, codes, scales, scale_row_offsets,
+                         status, false, stream);
+}
+
+int mxfp4_quantize_grouped_f16(const void* x, int64_t total_rows, int64_t K,
+                               const int32_t* expert_offsets, int32_t E, uint8_t* codes,
+                               uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
+                               void* stream) {
+  return grouped_checked(x, total_rows, K, expert_offsets, E, codes, scales, scale_row_offsets,
+                         status, true, stream);
+}
+
+int mxfp4_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
+                                  const int32_t* row_index, int64_t total_rows,
+                                  const int32_t* expert_offsets, int32_t E, uint8_t* codes,
+                                  uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
+                                  void* stream) {
+  return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E, codes,
+                        scales, scale_row_offsets, status, false, stream);
+}
+
+int mxfp4_quantize_grouped_gather_f16(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
+                                      const int32_t* row_index, int64_t total_rows,
+                                      const int32_t* expert_offsets, int32_t E, uint8_t* codes,
+                                      uint8_t* scales, int32_t* scale_row_offsets,
+                                      int32_t* status, void* stream) {
+  return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E, codes,
+                        scales, scale_row_offsets, status, true, stream);
+}
+
+int mxfp4_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K, int64_t ldx,
+                                   const int32_t* dest_rows, int32_t top_k, int64_t total_rows,
+                                   const int32_t* expert_offsets, int32_t E, uint8_t* codes,
+                                   uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
+                                   void* stream) {
+  return scatter_checked(x, num_tokens, K, ldx, dest_rows, top_k, total_rows, expert_offsets, E,
+                         codes, scales, scale_row_offsets, status, false, stream);
+}
+
+int mxfp4_quantize_grouped_scatter_f16(const void* x, int64_t num_tokens, int64_t K, int64_t ldx,
+                                       const int32_t* dest_rows, int32_t top_k,
+                                       int64_t total_rows, const int32_t* expert_offsets,
+                                       int32_t E, uint8_t* codes, uint8_t* scales,
+                                       int32_t* scale_row_offsets, int32_t* status,
+                                       void* stream) {
+  return scatter_checked(x, num_tokens, K, ldx, dest_rows, top_k, total_rows, expert_offsets, E,
+                         codes, scales, scale_row_offsets, status, true, stream);
+}
+
+
+
 
 int mxfp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int64_t K, void* y,
                      void* stream) {

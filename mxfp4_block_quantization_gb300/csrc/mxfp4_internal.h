@@ -17,11 +17,13 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
 
 // Grouped quantize: validates offsets and writes padded row starts, then
 // quantizes every segment.  `bound_tiles` is the host-side upper bound of
-// padded 128-row tiles.
+// padded 128-row tiles.  With f16 the input is IEEE binary16 instead of
+// BF16 (here and in the gather and scatter forms).
 cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
                                     const int32_t* offsets, int32_t E, uint8_t* codes,
                                     uint8_t* scales, int32_t* scale_row_offsets,
-                                    int32_t* status, int64_t bound_tiles, cudaStream_t stream);
+                                    int32_t* status, int64_t bound_tiles, bool f16,
+                                    cudaStream_t stream);
 
 // Validates expert offsets and writes the padded row starts P[0..E] (and
 // the status word) on the device; every grouped launcher runs it first.
@@ -35,13 +37,13 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
                                            int64_t total_rows, const int32_t* offsets, int32_t E,
                                            uint8_t* codes, uint8_t* scales,
                                            int32_t* scale_row_offsets, int32_t* status,
-                                           int64_t bound_tiles, cudaStream_t stream);
+                                           int64_t bound_tiles, bool f16, cudaStream_t stream);
 cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
                                             int64_t ldx, const int32_t* dest_rows, int32_t top_k,
                                             int64_t total_rows, const int32_t* offsets, int32_t E,
                                             uint8_t* codes, uint8_t* scales,
                                             int32_t* scale_row_offsets, int32_t* status,
-                                            int64_t bound_tiles, cudaStream_t stream);
+                                            int64_t bound_tiles, bool f16, cudaStream_t stream);
 
 // NVFP4 (16-element blocks, E4M3 scales, device global scale).
 cudaError_t launch_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,

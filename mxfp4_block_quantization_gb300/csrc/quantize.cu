@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
 // which the L2 keeps while the other routes of each row come by.
 constexpr int kGatherChunkTiles = 8;
 
-template <bool kVec32>
+template <bool kVec32, bool kF16>
 __global__ void __launch_bounds__(kGatherThreads) quantize_gather_kernel(const QuantizeParams p) {
   constexpr int kRowsPerPass = rows_per_pass(kGatherThreads);
   constexpr int kPasses = passes(kGatherThreads);
@@ -224,10 +224,10 @@ __global__ void __launch_bounds__(kGatherThreads) quantize_gather_kernel(const Q
                   sub * (kElems / 2);
 #pragma unroll
     for (int i = 0; i < kPasses; ++i) {
-      const uint32_t s = lane_block_scale<false>(v[i]);
+      const uint32_t s = lane_block_scale<kF16>(v[i]);
       if ((lane & 1) == 0)
         chunk[buf][chunk_offset(lr0 + kRowsPerPass * i, blk)] = static_cast<uint8_t>(s);
-      const uint2 code = lane_codes<false>(v[i], s);
+      const uint2 code = lane_codes<kF16>(v[i], s);
       if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgCodes, cp + i * cld_pass, 8))
         st_stream_v2(cp + i * cld_pass, code);
     }
@@ -289,7 +289,7 @@ __device__ __forceinline__ int64_t scale_word_base(int prow, int nKT) {
          ((prow & 127) >> 5) * 4;
 }
 
-template <bool kVec32>
+template <bool kVec32, bool kF16>
 __global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const ScatterParams p) {
   __shared__ int64_t s_code[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];   // d * K/2, or -1
   __shared__ int64_t s_scale[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];  // word base, or -1
@@ -363,8 +363,8 @@ __global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const Scatte
     uint32_t word[kScatterBatch];
 #pragma unroll
     for (int b = 0; b < kScatterBatch; ++b) {
-      const uint32_t s = lane_block_scale<false>(v[b]);
-      code[b] = lane_codes<false>(v[b], s);
+      const uint32_t s = lane_block_scale<kF16>(v[b]);
+      code[b] = lane_codes<kF16>(v[b], s);
       // scale word of k-tile (p0+b)*4 + lane/8: the s of lanes +0, +2, +4, +6
       word[b] = s | (__shfl_down_sync(0xFFFFFFFFu, s, 2) << 8) |
                 (__shfl_down_sync(0xFFFFFFFFu, s, 4) << 16) |
@@ -522,7 +522,8 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
 cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
                                     const int32_t* offsets, int32_t E, uint8_t* codes,
                                     uint8_t* scales, int32_t* scale_row_offsets,
-                                    int32_t* status, int64_t bound_tiles, cudaStream_t stream) {
+                                    int32_t* status, int64_t bound_tiles, bool f16,
+                                    cudaStream_t stream) {
   cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
   if (err != cudaSuccess || E == 0 || bound_tiles == 0) return err;
   QuantizeParams p{};
@@ -545,8 +546,11 @@ cudaError_t launch_quantize_grouped(const void* x, int64_t total_rows, int64_t K
   debug_range(p.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
 #endif
   const int64_t grid = bound_tiles * p.nKT;  // CTAs past the real padded total exit at once
-  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_tiles_kernel<true, true>
-                                               : quantize_tiles_kernel<true, false>;
+  const bool v32 = vec32_ok(x, p.ldx_bytes);
+  const auto kernel = f16 ? (v32 ? quantize_tiles_kernel<true, true, true>
+                                 : quantize_tiles_kernel<true, false, true>)
+                          : (v32 ? quantize_tiles_kernel<true, true>
+                                 : quantize_tiles_kernel<true, false>);
   return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
@@ -555,7 +559,7 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
                                            int64_t total_rows, const int32_t* offsets, int32_t E,
                                            uint8_t* codes, uint8_t* scales,
                                            int32_t* scale_row_offsets, int32_t* status,
-                                           int64_t bound_tiles, cudaStream_t stream) {
+                                           int64_t bound_tiles, bool f16, cudaStream_t stream) {
   cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
   if (err != cudaSuccess || E == 0 || bound_tiles == 0) return err;
   QuantizeParams p{};
@@ -584,8 +588,11 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
   debug_range(p.dbg, kDbgStatus, status, status ? 4 : 0);
 #endif
   const int64_t grid = bound_tiles * ((p.nKT + kGatherChunkTiles - 1) / kGatherChunkTiles);
-  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_gather_kernel<true>
-                                               : quantize_gather_kernel<false>;
+  const bool v32 = vec32_ok(x, p.ldx_bytes);
+  const auto kernel = f16 ? (v32 ? quantize_gather_kernel<true, true>
+                                 : quantize_gather_kernel<false, true>)
+                          : (v32 ? quantize_gather_kernel<true, false>
+                                 : quantize_gather_kernel<false, false>);
   return launch_pdl(kernel, static_cast<unsigned>(grid), kGatherThreads, 0, stream, p);
 }
 
@@ -594,7 +601,7 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
                                             int64_t total_rows, const int32_t* offsets, int32_t E,
                                             uint8_t* codes, uint8_t* scales,
                                             int32_t* scale_row_offsets, int32_t* status,
-                                            int64_t bound_tiles, cudaStream_t stream) {
+                                            int64_t bound_tiles, bool f16, cudaStream_t stream) {
   cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
   if (err != cudaSuccess || E == 0 || K == 0) return err;
   ScatterParams p{};
@@ -623,8 +630,11 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
   debug_range(p.dbg, kDbgStatus, status, status ? 4 : 0);
 #endif
   const int64_t grid = E + (num_tokens + kScatterWarps - 1) / kScatterWarps;
-  const auto kernel = vec32_ok(x, p.ldx_bytes) ? quantize_scatter_kernel<true>
-                                               : quantize_scatter_kernel<false>;
+  const bool v32 = vec32_ok(x, p.ldx_bytes);
+  const auto kernel = f16 ? (v32 ? quantize_scatter_kernel<true, true>
+                                 : quantize_scatter_kernel<false, true>)
+                          : (v32 ? quantize_scatter_kernel<true, false>
+                                 : quantize_scatter_kernel<false, false>);
   return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
