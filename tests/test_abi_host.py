@@ -239,3 +239,16 @@ def test_nvfp4_grouped_validation(lib):
     assert call(sro=7 * A) == lib.MXFP4_EALIAS               # offsets out overlap the scales in
     assert lib.mxfp4_nvfp4_grouped_scale_bytes_bound(300, 3, 64) == (300 + 381) // 128 * 128 * 4
     assert lib.mxfp4_nvfp4_grouped_scale_bytes_bound(300, 3, 40) == 0
+
+
+def test_f16_grouped_forms_share_the_validation(lib):
+    L = lib._lib
+    # K % 32 != 0 is refused by every FP16 grouped form, before any launch
+    assert L.mxfp4_quantize_grouped_f16(A, 10, 48, 2 * A, 1, 3 * A, 4 * A, 5 * A, None,
+                                        None) == lib.MXFP4_ESHAPE
+    assert L.mxfp4_quantize_grouped_gather_f16(A, 10, 48, 48, 2 * A, 10, 3 * A, 1, 4 * A, 5 * A,
+                                               6 * A, None, None) == lib.MXFP4_ESHAPE
+    assert L.mxfp4_quantize_grouped_scatter_f16(A, 10, 48, 48, 2 * A, 1, 10, 3 * A, 1, 4 * A,
+                                                5 * A, 6 * A, None, None) == lib.MXFP4_ESHAPE
+    assert L.mxfp4_quantize_grouped_scatter_f16(A, 10, 64, 64, 2 * A, 0, 10, 3 * A, 1, 4 * A,
+                                                5 * A, 6 * A, None, None) == lib.MXFP4_EINVAL

@@ -136,6 +136,11 @@ def test_everything_in_bounds(libs):
     wide3[:, :1056] = g3.x_tokens
     cases.append(lambda: written(mx.quantize_grouped_scatter(wide3[:, :1056], g3.dest_rows,
                                                              g3.offsets), 1056))
+    # FP16 input through the scatter and gather forms
+    cases.append(lambda: written(mx.quantize_grouped_scatter(g3.x_tokens.to(torch.float16),
+                                                             g3.dest_rows, g3.offsets), 1056))
+    cases.append(lambda: written(mx.quantize_grouped_gather(g3.x_tokens.to(torch.float16),
+                                                            g3.row_index, g3.offsets), 1056))
     # NVFP4 experts quant (K a multiple of 16 but not 32 included)
     gn = W.moe_grouped(seed=10, tokens=150, top_k=3, num_experts=7, K=80, device="cuda")
     gsn = torch.linspace(0.5, 40.0, 7, device="cuda")

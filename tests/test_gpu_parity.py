@@ -920,3 +920,63 @@ def test_nvfp4_grouped_moe_full_size_sampled(mx):
         assert np.array_equal(codes[a:b].cpu().numpy(), c_o), e
         p0 = int(want_sro[e]) * pk
         assert np.array_equal(scales[p0:p0 + s_o.size].cpu().numpy(), s_o), e
+
+
+# ----------------------------------------------- FP16 input, grouped forms
+def _f16(t):
+    return t.to(torch.float16)
+
+
+def _h_bits(t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_f16_grouped_gather_scatter_match_oracle(mx):
+    g = W.moe_grouped(seed=12, tokens=180, top_k=4, num_experts=10, K=288, device="cuda")
+    xt = _f16(g.x_tokens)
+    xs = _f16(g.x)
+    off = g.offsets
+    rc, c_o, s_o, sro_o = oracle.quantize_grouped(_h_bits(xs), off.cpu().numpy(), f16=True)
+    used = int(sro_o[-1]) * 12
+    for label, (c, s, sro, st) in (
+            ("grouped", mx.quantize_grouped(xs, off)),
+            ("grouped 16B", mx.quantize_grouped(offset16_any(xs), off)),
+            ("gather", mx.quantize_grouped_gather(xt, g.row_index, off)),
+            ("scatter", mx.quantize_grouped_scatter(xt, g.dest_rows, off))):
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0 and rc == 0, label
+        assert np.array_equal(sro.cpu().numpy(), sro_o), label
+        assert np.array_equal(c.cpu().numpy(), c_o), label
+        assert np.array_equal(s[:used].cpu().numpy(), s_o[:used]), label
+
+
+def offset16_any(x):
+    flat = torch.empty(x.numel() + 8, dtype=x.dtype, device=x.device)
+    y = flat[8:].view(x.shape)
+    y.copy_(x)
+    assert y.data_ptr() % 32 == 16
+    return y
+
+
+def test_f16_dispatch_full_size(mx):
+    """The MoE batch in FP16: the scatter and gather forms equal the grouped
+    quantize of the permuted FP16 matrix byte for byte; two experts also
+    against the oracle."""
+    g = W.moe_grouped(seed=2, device="cuda")
+    xt = _f16(g.x_tokens)
+    xs = _f16(g.x)
+    c1, s1, sro1, st1 = mx.quantize_grouped(xs, g.offsets)
+    c2, s2, sro2, st2 = mx.quantize_grouped_gather(xt, g.row_index, g.offsets)
+    c3, s3, sro3, st3 = mx.quantize_grouped_scatter(xt, g.dest_rows, g.offsets)
+    torch.cuda.synchronize()
+    assert int(st1.item()) == int(st2.item()) == int(st3.item()) == 0
+    used = int(sro1[-1].item()) * 224
+    assert torch.equal(c1, c2) and torch.equal(c1, c3)
+    assert torch.equal(s1[:used], s2[:used]) and torch.equal(s1[:used], s3[:used])
+    off_h = g.offsets.cpu().numpy()
+    for e in (3, 200):
+        a, b = int(off_h[e]), int(off_h[e + 1])
+        c_o, s_o = oracle.quantize_f16(_h_bits(xs[a:b]))
+        assert np.array_equal(c1[a:b].cpu().numpy(), c_o)
+        p0 = int(sro1[e].item()) * 224
+        assert np.array_equal(s1[p0:p0 + s_o.size].cpu().numpy(), s_o)
