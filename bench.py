@@ -452,6 +452,17 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     e_["unfused_us_per_call"] = round(ms_unfused * 1e3, 2)
     e_["speedup_vs_unfused"] = round(ms_unfused / ms_fused, 3)
     out["grouped_gather_moe_16384tok_top8_E384"] = e_
+    # the same gather call through the scatter path (inverse map built in a workspace)
+    ws = torch.empty(mx.mxfp4_gather_workspace_bytes(T, total), dtype=torch.uint8, device="cuda")
+    ms_ws = time_launches(
+        lambda i: mx.mxfp4_quantize_grouped_gather_ws(g.x_tokens, g.row_index, g.offsets, ws,
+                                                      codes, scales, sro, st, stream), 30, stream)
+    e_ = entry(nb, ms_ws, 6, "same call and bytes as the gather row; offsets, workspace memset, "
+               "3 inverse-map kernels, then the scatter kernel reads each token row once")
+    e_["speedup_vs_unfused"] = round(ms_unfused / ms_ws, 3)
+    e_["speedup_vs_per_row_gather"] = round(ms_fused / ms_ws, 3)
+    out["grouped_gather_ws_moe_16384tok_top8_E384"] = e_
+    del ws
     # the same dispatch given token -> rows (the router's sort output): each
     # token row read and quantized once, its codes written to its 8 rows
     ms_sc = time_launches(

@@ -162,6 +162,36 @@ int mxfp4_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K
                                   uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
                                   void* stream);
 
+/* mxfp4_quantize_grouped_gather_ws — mxfp4_quantize_grouped_gather with
+ * identical results (the same arguments, outputs, status and errors), run
+ * through the scatter path: from row_index the library builds its inverse
+ * (the rows of every source row) in `workspace`, then reads and quantizes
+ * every source row once and writes it to all its rows, instead of reading it
+ * once per row.  [PR43557] "Implementation breakdown" item 3.
+ *
+ * workspace        DEVICE scratch owned by the caller, 16-byte aligned, at
+ *                  least mxfp4_gather_workspace_bytes(num_src_rows, total_rows)
+ *                  bytes, not overlapping any other argument; its contents on
+ *                  entry do not matter and on return are unspecified.  Two
+ *                  calls in flight at once need two workspaces.
+ * num_src_rows     <= INT32_MAX / 4.
+ * Everything else: as mxfp4_quantize_grouped_gather.  The _f16 form takes
+ * IEEE binary16 input.
+ */
+size_t mxfp4_gather_workspace_bytes(int64_t num_src_rows, int64_t total_rows);
+int mxfp4_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
+                                     const int32_t* row_index, int64_t total_rows,
+                                     const int32_t* expert_offsets, int32_t E, void* workspace,
+                                     size_t workspace_bytes, uint8_t* codes, uint8_t* scales,
+                                     int32_t* scale_row_offsets, int32_t* status, void* stream);
+int mxfp4_quantize_grouped_gather_ws_f16(const void* x, int64_t num_src_rows, int64_t K,
+                                         int64_t ldx, const int32_t* row_index,
+                                         int64_t total_rows, const int32_t* expert_offsets,
+                                         int32_t E, void* workspace, size_t workspace_bytes,
+                                         uint8_t* codes, uint8_t* scales,
+                                         int32_t* scale_row_offsets, int32_t* status,
+                                         void* stream);
+
 /* mxfp4_quantize_grouped_scatter — the same dispatch given in the direction
  * a router's sort produces it (token, route -> row): each token row of x is
  * read and quantized once, and its codes and scale bytes are written to every

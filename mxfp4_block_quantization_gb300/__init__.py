@@ -32,7 +32,9 @@ __all__ = [
     "MXFP4_ECUDA", "MXFP4_EOFFSETS", "MXFP4_EINDEX", "mxfp4_quantize_grouped_gather",
     "quantize_grouped_gather", "mxfp4_quantize_grouped_scatter", "quantize_grouped_scatter",
     "MXFP4_SCATTER_MAX_TOP_K", "mxfp4_quantize_f16", "mxfp4_quantize_grouped_f16",
-    "mxfp4_quantize_grouped_gather_f16", "mxfp4_quantize_grouped_scatter_f16", "mxfp4_nvfp4_scale_bytes",
+    "mxfp4_quantize_grouped_gather_f16", "mxfp4_quantize_grouped_scatter_f16",
+    "mxfp4_gather_workspace_bytes", "mxfp4_quantize_grouped_gather_ws",
+    "mxfp4_quantize_grouped_gather_ws_f16", "mxfp4_nvfp4_scale_bytes",
     "mxfp4_quantize_nvfp4", "mxfp4_dequantize_nvfp4", "quantize_nvfp4", "dequantize_nvfp4",
     "mxfp4_nvfp4_grouped_scale_bytes_bound", "mxfp4_quantize_nvfp4_grouped",
     "quantize_nvfp4_grouped",
@@ -87,6 +89,12 @@ def _load(path=LIB_PATH):
     L.mxfp4_quantize_grouped_scatter_f16.restype = ctypes.c_int
     L.mxfp4_quantize_grouped_scatter_f16.argtypes = [vp, i64, i64, i64, vp, i32, i64, vp, i32,
                                                      vp, vp, vp, vp, vp]
+    L.mxfp4_gather_workspace_bytes.restype = ctypes.c_size_t
+    L.mxfp4_gather_workspace_bytes.argtypes = [i64, i64]
+    for name in ("mxfp4_quantize_grouped_gather_ws", "mxfp4_quantize_grouped_gather_ws_f16"):
+        getattr(L, name).restype = ctypes.c_int
+        getattr(L, name).argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, ctypes.c_size_t,
+                                     vp, vp, vp, vp, vp]
     L.mxfp4_quantize_grouped_gather.restype = ctypes.c_int
     L.mxfp4_quantize_grouped_gather.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, vp, vp,
                                                 vp, vp]
@@ -266,6 +274,51 @@ def mxfp4_quantize_grouped_gather_f16(x, row_index, expert_offsets, codes, scale
     _gather(x, row_index, expert_offsets, codes, scales, scale_row_offsets, status, stream, True)
 
 
+def mxfp4_gather_workspace_bytes(num_src_rows: int, total_rows: int) -> int:
+    return int(_lib.mxfp4_gather_workspace_bytes(int(num_src_rows), int(total_rows)))
+
+
+def _gather_ws(x, row_index, expert_offsets, workspace, codes, scales, scale_row_offsets, status,
+               stream, f16):
+    name = "mxfp4_quantize_grouped_gather_ws" + ("_f16" if f16 else "")
+    _need_cuda("x", x, torch.float16 if f16 else torch.bfloat16)
+    _need_cuda("row_index", row_index, torch.int32)
+    _need_cuda("expert_offsets", expert_offsets, torch.int32)
+    _need_cuda("workspace", workspace)
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    _need_cuda("scale_row_offsets", scale_row_offsets, torch.int32)
+    _need_cuda("status", status, torch.int32)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    if not row_index.is_contiguous() or not workspace.is_contiguous():
+        raise ValueError("row_index and workspace must be contiguous")
+    n_src, K = x.shape
+    E = expert_offsets.numel() - 1
+    with torch.cuda.device(_device_of(x, row_index, expert_offsets, workspace, codes, scales,
+                                      scale_row_offsets, status)):
+        _check(getattr(_lib, name)(
+            _ptr(x), n_src, K, x.stride(0), _ptr(row_index), row_index.numel(),
+            _ptr(expert_offsets), E, _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _ptr(codes), _ptr(scales), _ptr(scale_row_offsets), _ptr(status),
+            _stream(stream, x.device)), name)
+
+
+def mxfp4_quantize_grouped_gather_ws(x, row_index, expert_offsets, workspace, codes, scales,
+                                     scale_row_offsets, status=None, stream=None) -> None:
+    """mxfp4_quantize_grouped_gather through the scatter path: the inverse
+    map is built in ``workspace`` (device, >= mxfp4_gather_workspace_bytes)."""
+    _gather_ws(x, row_index, expert_offsets, workspace, codes, scales, scale_row_offsets, status,
+               stream, False)
+
+
+def mxfp4_quantize_grouped_gather_ws_f16(x, row_index, expert_offsets, workspace, codes, scales,
+                                         scale_row_offsets, status=None, stream=None) -> None:
+    """mxfp4_quantize_grouped_gather_ws for FP16 ``x``."""
+    _gather_ws(x, row_index, expert_offsets, workspace, codes, scales, scale_row_offsets, status,
+               stream, True)
+
+
 def _scatter(x, dest_rows, expert_offsets, total_rows, codes, scales, scale_row_offsets, status,
              stream, f16):
     name = "mxfp4_quantize_grouped_scatter" + ("_f16" if f16 else "")
@@ -431,19 +484,26 @@ def quantize_grouped(x, expert_offsets, stream=None):
     return codes, scales, sro, status
 
 
-def quantize_grouped_gather(x, row_index, expert_offsets, stream=None):
-    """Returns (codes, scales, scale_row_offsets, status) of x[row_index]."""
+def quantize_grouped_gather(x, row_index, expert_offsets, stream=None, via_scatter=True):
+    """Returns (codes, scales, scale_row_offsets, status) of x[row_index]
+    (BF16 or FP16 x).  By default through the scatter path, with a workspace
+    allocated here; via_scatter=False runs the per-row gather kernel."""
     K = x.shape[1]
     total = row_index.numel()
     E = expert_offsets.numel() - 1
     dev = x.device
+    f16 = x.dtype == torch.float16
     codes = torch.empty((total, K // 2), dtype=torch.uint8, device=dev)
     scales = torch.empty(max(mxfp4_grouped_scale_bytes_bound(total, E, K), 16), dtype=torch.uint8,
                          device=dev)
     sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
     status = torch.empty(1, dtype=torch.int32, device=dev)
-    _gather(x, row_index, expert_offsets, codes, scales, sro, status, stream,
-            x.dtype == torch.float16)
+    if via_scatter:
+        ws = torch.empty(max(mxfp4_gather_workspace_bytes(x.shape[0], total), 16),
+                         dtype=torch.uint8, device=dev)
+        _gather_ws(x, row_index, expert_offsets, ws, codes, scales, sro, status, stream, f16)
+    else:
+        _gather(x, row_index, expert_offsets, codes, scales, sro, status, stream, f16)
     return codes, scales, sro, status
 
 

@@ -136,9 +136,9 @@ int grouped_checked(const void* x, int64_t total_rows, int64_t K,
 }
 
 int gather_checked(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
-                                  const int32_t* row_index, int64_t total_rows,
-                                  const int32_t* expert_offsets, int32_t E, uint8_t* codes,
-                                  uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
+                   const int32_t* row_index, int64_t total_rows, const int32_t* expert_offsets,
+                   int32_t E, void* workspace, size_t workspace_bytes, uint8_t* codes,
+                   uint8_t* scales, int32_t* scale_row_offsets, int32_t* status, bool use_ws,
                    bool f16, void* stream) {
   if (num_src_rows < 0 || total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
   if (K % 32 != 0 || ldx < K) return MXFP4_ESHAPE;
@@ -150,6 +150,15 @@ int gather_checked(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
   if (total_rows + 127 * static_cast<int64_t>(E) > INT32_MAX) return MXFP4_ESHAPE;
   if (bound_tiles * ceil_div(K / 32, 4) > kMaxGrid) return MXFP4_ESHAPE;
   if (num_src_rows > 0 && ldx > 0 && num_src_rows > (INT64_MAX / 4) / ldx) return MXFP4_ESHAPE;
+  int64_t ws_bytes = 0;
+  if (use_ws) {
+    // token ids and route counts are int32 on the device
+    if (num_src_rows > INT32_MAX / 4) return MXFP4_ESHAPE;
+    ws_bytes = static_cast<int64_t>(mxfp4_gather_workspace_bytes(num_src_rows, total_rows));
+    if (work && (!workspace || workspace_bytes < static_cast<size_t>(ws_bytes)))
+      return MXFP4_EINVAL;
+    if (workspace && !aligned16(workspace)) return MXFP4_EALIGN;
+  }
   if ((x && (!aligned16(x) || ldx % 8 != 0)) || (codes && !aligned16(codes)) ||
       (scales && !aligned16(scales)) || (reinterpret_cast<uintptr_t>(row_index) & 3u) ||
       (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) ||
@@ -160,22 +169,28 @@ int gather_checked(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
       range_of(x, work ? ((num_src_rows - 1) * ldx + K) * 2 : 0),
       range_of(row_index, work ? total_rows * 4 : 0),
       range_of(expert_offsets, (static_cast<int64_t>(E) + 1) * 4)};
-  const Range outs[4] = {
+  const Range outs[5] = {
       range_of(codes, total_rows * (K / 2)),
       range_of(scales,
                static_cast<int64_t>(mxfp4_grouped_scale_bytes_bound(total_rows, E, K))),
       range_of(scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4),
-      range_of(status, status ? 4 : 0)};
-  for (int i = 0; i < 4; ++i) {
+      range_of(status, status ? 4 : 0),
+      range_of(workspace, use_ws && work ? ws_bytes : 0)};
+  for (int i = 0; i < 5; ++i) {
     for (int j = 0; j < 3; ++j)
       if (overlap(outs[i], ins[j])) return MXFP4_EALIAS;
-    for (int j = i + 1; j < 4; ++j)
+    for (int j = i + 1; j < 5; ++j)
       if (overlap(outs[i], outs[j])) return MXFP4_EALIAS;
   }
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (use_ws)
+    return from_cuda(mxfp4::launch_quantize_grouped_gather_ws(
+        x, work ? num_src_rows : 0, K, ldx, row_index, total_rows, expert_offsets, E,
+        static_cast<int32_t*>(workspace), codes, scales, scale_row_offsets, status,
+        K == 0 ? 0 : bound_tiles, f16, st));
   return from_cuda(mxfp4::launch_quantize_grouped_gather(
       x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E, codes, scales,
-      scale_row_offsets, status, K == 0 ? 0 : bound_tiles, f16,
-      static_cast<cudaStream_t>(stream)));
+      scale_row_offsets, status, K == 0 ? 0 : bound_tiles, f16, st));
 }
 
 int scatter_checked(const void* x, int64_t num_tokens, int64_t K, int64_t ldx,
@@ -260,8 +275,9 @@ int mxfp4_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K
                                   const int32_t* expert_offsets, int32_t E, uint8_t* codes,
                                   uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
                                   void* stream) {
-  return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E, codes,
-                        scales, scale_row_offsets, status, false, stream);
+  return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E,
+                        nullptr, 0, codes, scales, scale_row_offsets, status, false, false,
+                        stream);
 }
 
 int mxfp4_quantize_grouped_gather_f16(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
@@ -269,8 +285,37 @@ int mxfp4_quantize_grouped_gather_f16(const void* x, int64_t num_src_rows, int64
                                       const int32_t* expert_offsets, int32_t E, uint8_t* codes,
                                       uint8_t* scales, int32_t* scale_row_offsets,
                                       int32_t* status, void* stream) {
-  return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E, codes,
-                        scales, scale_row_offsets, status, true, stream);
+  return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E,
+                        nullptr, 0, codes, scales, scale_row_offsets, status, false, true,
+                        stream);
+}
+
+size_t mxfp4_gather_workspace_bytes(int64_t num_src_rows, int64_t total_rows) {
+  if (num_src_rows < 0 || total_rows < 0) return 0;
+  return static_cast<size_t>(ceil_div(mxfp4::gather_workspace_ints(num_src_rows, total_rows) * 4,
+                                      16) * 16);
+}
+
+int mxfp4_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
+                                     const int32_t* row_index, int64_t total_rows,
+                                     const int32_t* expert_offsets, int32_t E, void* workspace,
+                                     size_t workspace_bytes, uint8_t* codes, uint8_t* scales,
+                                     int32_t* scale_row_offsets, int32_t* status, void* stream) {
+  return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E,
+                        workspace, workspace_bytes, codes, scales, scale_row_offsets, status,
+                        true, false, stream);
+}
+
+int mxfp4_quantize_grouped_gather_ws_f16(const void* x, int64_t num_src_rows, int64_t K,
+                                         int64_t ldx, const int32_t* row_index,
+                                         int64_t total_rows, const int32_t* expert_offsets,
+                                         int32_t E, void* workspace, size_t workspace_bytes,
+                                         uint8_t* codes, uint8_t* scales,
+                                         int32_t* scale_row_offsets, int32_t* status,
+                                         void* stream) {
+  return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E,
+                        workspace, workspace_bytes, codes, scales, scale_row_offsets, status,
+                        true, true, stream);
 }
 
 int mxfp4_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K, int64_t ldx,

@@ -38,6 +38,16 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
                                            uint8_t* codes, uint8_t* scales,
                                            int32_t* scale_row_offsets, int32_t* status,
                                            int64_t bound_tiles, bool f16, cudaStream_t stream);
+// The same gather through the scatter path: the inverse map is built in
+// `workspace` (gather_workspace_ints(num_src_rows, total_rows) int32).
+int64_t gather_workspace_ints(int64_t num_src_rows, int64_t total_rows);
+cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_t K,
+                                              int64_t ldx, const int32_t* row_index,
+                                              int64_t total_rows, const int32_t* offsets,
+                                              int32_t E, int32_t* workspace, uint8_t* codes,
+                                              uint8_t* scales, int32_t* scale_row_offsets,
+                                              int32_t* status, int64_t bound_tiles, bool f16,
+                                              cudaStream_t stream);
 cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
                                             int64_t ldx, const int32_t* dest_rows, int32_t top_k,
                                             int64_t total_rows, const int32_t* offsets, int32_t E,

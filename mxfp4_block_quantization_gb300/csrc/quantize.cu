@@ -34,6 +34,7 @@ namespace {
 
 constexpr int kThreads = 256;                               // dense and grouped CTAs
 constexpr int kGatherThreads = 128;                         // gather CTAs: 8 passes per thread
+constexpr int kScanThreads = 1024;                          // single-CTA scans
 
 // Rows covered by one pass of a CTA of `threads` threads (4 rows per warp),
 // and passes per 128-row tile.
@@ -63,7 +64,10 @@ struct QuantizeParams {
 };
 
 // Buffer slots of QuantizeParams::dbg.
-enum : int { kDbgX = 0, kDbgCodes, kDbgScales, kDbgOffsets, kDbgPadded, kDbgRowIndex, kDbgStatus };
+enum : int {
+  kDbgX = 0, kDbgCodes, kDbgScales, kDbgOffsets, kDbgPadded, kDbgRowIndex, kDbgStatus,
+  kDbgWork  // the inverse-map workspace of the gather-through-scatter path
+};
 
 // Lane l of warp w covers elements [16*(l%8), 16*(l%8)+16) of row
 // 4*w + l/8 (+32 per pass): two lanes per 32-element block.
@@ -266,6 +270,10 @@ struct ScatterParams {
   int64_t ldx_bytes;                      // token row stride in bytes
   int64_t num_tokens;
   const int32_t* __restrict__ dest_rows;  // [num_tokens, top_k] row of every route, -1 = none
+  const int32_t* __restrict__ unit_token;  // or NULL; else warp u takes unit u: token
+  const int32_t* __restrict__ unit_first;  // unit_token[u], routes dest_rows[unit_first[u] ..
+  const int32_t* __restrict__ route_end;   // min(+32, route_end[token])), u < *n_units
+  const int32_t* __restrict__ n_units;
   int32_t top_k;
   int32_t E;
   int64_t total_rows;                     // rows of the expert-sorted batch
@@ -320,15 +328,33 @@ __global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const Scatte
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x - p.E) * kScatterWarps + warp;
-  if (t >= p.num_tokens) return;  // whole warp; no block-wide barrier below
-  const int top_k = p.top_k;
+  const int64_t w_id = static_cast<int64_t>(blockIdx.x - p.E) * kScatterWarps + warp;
+  // the token and its routes: a fixed top_k per token (warp = token), or one
+  // unit of at most 32 routes of a token (warp = unit)
+  int64_t t, rbase;
+  int nr;
+  if (p.unit_token == nullptr) {
+    if (w_id >= p.num_tokens) return;  // whole warp; no block-wide barrier below
+    t = w_id;
+    rbase = t * p.top_k;
+    nr = p.top_k;
+  } else {
+    if (!MXFP4_IN_BOUNDS(p, kDbgWork, p.n_units, 4) || w_id >= __ldg(p.n_units)) return;
+    if (!MXFP4_IN_BOUNDS(p, kDbgWork, p.unit_token + w_id, 4) ||
+        !MXFP4_IN_BOUNDS(p, kDbgWork, p.unit_first + w_id, 4))
+      return;
+    t = __ldg(p.unit_token + w_id);
+    rbase = __ldg(p.unit_first + w_id);
+    if (!MXFP4_IN_BOUNDS(p, kDbgWork, p.route_end + t, 4)) return;
+    const int left = __ldg(p.route_end + t) - static_cast<int>(rbase);
+    nr = left < 32 ? left : 32;
+  }
 
-  // the token's routes, one per lane
+  // routes, one per lane
   int64_t co = -1, so = -1;
   bool bad = false;
-  if (lane < top_k) {
-    const int32_t* dp = p.dest_rows + t * top_k + lane;
+  if (lane < nr) {
+    const int32_t* dp = p.dest_rows + rbase + lane;
     const int32_t v = MXFP4_IN_BOUNDS(p, kDbgRowIndex, dp, 4) ? __ldg(dp) : -1;
     if (v >= 0 && v < p.total_rows) {
       const int e = find_segment(p.offsets, p.E, v, static_cast<int>(p.total_rows));
@@ -372,7 +398,7 @@ __global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const Scatte
     }
     const int64_t cofs = static_cast<int64_t>(p0) * (kScatterPass / 2) + lane * (kElems / 2);
     const int kt0 = p0 * 4 + (lane >> 3);
-    for (int j = 0; j < top_k; ++j) {
+    for (int j = 0; j < nr; ++j) {
       const int64_t c = s_code[warp][j];
       const int64_t w = s_scale[warp][j];
 #pragma unroll
@@ -390,10 +416,201 @@ __global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const Scatte
   }
 }
 
+// ---------------------------------------------------------------------
+// The fused gather through the scatter path.  From the row -> token map,
+// four small kernels build its inverse in a caller-provided workspace: the
+// routes of every token (rows[start[t] .. start[t+1])), cut into units of at
+// most 32 routes (unit_token[u], unit_first[u], u < chunk_start[T]); the
+// scatter kernel then reads and quantizes every token row once per unit.
+// The route order within a token is arbitrary (atomics) and does not matter:
+// every route of a token receives the same bytes.
+struct InvertParams {
+  const int32_t* __restrict__ row_index;  // [R] token of every row
+  int64_t total_rows;                     // R
+  int64_t num_src_rows;                   // T
+  int32_t* __restrict__ count;            // [T], zero on entry
+  int32_t* __restrict__ start;            // [T+1] route ranges
+  int32_t* __restrict__ chunk_start;      // [T+1] unit ranges; chunk_start[T] = units
+  int32_t* __restrict__ unit_token;       // [U]
+  int32_t* __restrict__ unit_first;       // [U]
+  int32_t* __restrict__ rows;             // [R] rows grouped by token
+  int32_t* __restrict__ block_sums;       // [2 * ceil(T / kScanThreads)] routes, units per block
+  uint8_t* __restrict__ codes;            // rows with an index out of range are
+  uint8_t* __restrict__ scales;           //   zeroed here, codes and scale bytes
+  int64_t code_ld;
+  const int32_t* __restrict__ offsets;
+  const int32_t* __restrict__ padded;
+  int32_t E;
+  int32_t nKT;
+  int32_t* status;
+#ifdef MXFP4_DEBUG_BOUNDS
+  DebugRanges dbg;  // kDbgCodes, kDbgScales, kDbgOffsets, kDbgPadded, kDbgRowIndex, kDbgStatus, kDbgWork
+#endif
+};
+
+constexpr int kInvertThreads = 256;
+
+__device__ __forceinline__ bool invert_offsets_ok(const InvertParams& q) {
+  if (!MXFP4_IN_BOUNDS(q, kDbgPadded, q.padded, (q.E + 1) * 4) ||
+      !MXFP4_IN_BOUNDS(q, kDbgOffsets, q.offsets, (q.E + 1) * 4))
+    return false;
+  return __ldg(q.padded + q.E) >= 0;  // rejected offsets: nothing is written
+}
+
+// Routes per token; a row whose index is out of range becomes a zero row.
+__global__ void __launch_bounds__(kInvertThreads) invert_count_kernel(const InvertParams q) {
+  pdl_wait();
+  pdl_release();
+  if (!invert_offsets_ok(q)) return;
+  bool bad = false;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kInvertThreads;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kInvertThreads + threadIdx.x;
+       r < q.total_rows; r += stride) {
+    const int32_t* ip = q.row_index + r;
+    const int32_t t = MXFP4_IN_BOUNDS(q, kDbgRowIndex, ip, 4) ? __ldg(ip) : -1;
+    if (t >= 0 && t < q.num_src_rows) {
+      if (MXFP4_IN_BOUNDS(q, kDbgWork, q.count + t, 4)) atomicAdd(q.count + t, 1);
+      continue;
+    }
+    bad = true;
+    uint8_t* cp = q.codes + r * q.code_ld;
+    for (int64_t i = 0; i < q.code_ld; i += 16)
+      if (MXFP4_IN_BOUNDS(q, kDbgCodes, cp + i, 16))
+        *reinterpret_cast<uint4*>(cp + i) = make_uint4(0u, 0u, 0u, 0u);
+    const int e = find_segment(q.offsets, q.E, static_cast<int>(r), static_cast<int>(q.total_rows));
+    const int64_t base =
+        scale_word_base(__ldg(q.padded + e) + (static_cast<int>(r) - __ldg(q.offsets + e)), q.nKT);
+    for (int kt = 0; kt < q.nKT; ++kt) {
+      uint8_t* wp = q.scales + base + static_cast<int64_t>(kt) * kChunkBytes;
+      if (MXFP4_IN_BOUNDS(q, kDbgScales, wp, 4)) *reinterpret_cast<uint32_t*>(wp) = 0u;
+    }
+  }
+  if (bad && q.status != nullptr && MXFP4_IN_BOUNDS(q, kDbgStatus, q.status, 4))
+    atomicExch(q.status, MXFP4_EINDEX);
+}
+
+// Block-wide inclusive scan of two values (routes, units) over kScanThreads
+// threads; returns the exclusive prefixes and leaves the block totals in
+// s_tot[0..1].
+__device__ __forceinline__ void block_scan2(int32_t n, int32_t nu, int32_t& ex_n, int32_t& ex_u,
+                                            int32_t (*s_warp)[kScanThreads / 32],
+                                            int32_t* s_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int32_t inc0 = n, inc1 = nu;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int32_t a0 = __shfl_up_sync(0xFFFFFFFFu, inc0, d);
+    const int32_t a1 = __shfl_up_sync(0xFFFFFFFFu, inc1, d);
+    if (lane >= d) { inc0 += a0; inc1 += a1; }
+  }
+  if (lane == 31) { s_warp[0][warp] = inc0; s_warp[1][warp] = inc1; }
+  __syncthreads();
+  if (warp < 2) {
+    int32_t w = s_warp[warp][lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t a = __shfl_up_sync(0xFFFFFFFFu, w, d);
+      if (lane >= d) w += a;
+    }
+    s_warp[warp][lane] = w;  // inclusive over warps
+    if (lane == 31) s_tot[warp] = w;
+  }
+  __syncthreads();
+  ex_n = (warp > 0 ? s_warp[0][warp - 1] : 0) + inc0 - n;
+  ex_u = (warp > 0 ? s_warp[1][warp - 1] : 0) + inc1 - nu;
+}
+
+__device__ __forceinline__ int32_t route_count(const InvertParams& q, int64_t t) {
+  if (t >= q.num_src_rows || !MXFP4_IN_BOUNDS(q, kDbgWork, q.count + t, 4)) return 0;
+  return q.count[t];
+}
+
+// Per block of kScanThreads tokens: its total routes and units.
+__global__ void __launch_bounds__(kScanThreads) invert_block_sum_kernel(const InvertParams q) {
+  __shared__ int32_t s_warp[2][kScanThreads / 32];
+  __shared__ int32_t s_tot[2];
+  pdl_wait();
+  pdl_release();
+  if (!invert_offsets_ok(q)) return;
+  const int32_t n = route_count(q, static_cast<int64_t>(blockIdx.x) * kScanThreads + threadIdx.x);
+  int32_t ex_n, ex_u;
+  block_scan2(n, (n + 31) / 32, ex_n, ex_u, s_warp, s_tot);
+  if (threadIdx.x == 0 && MXFP4_IN_BOUNDS(q, kDbgWork, q.block_sums + 2 * blockIdx.x, 8)) {
+    q.block_sums[2 * blockIdx.x] = s_tot[0];
+    q.block_sums[2 * blockIdx.x + 1] = s_tot[1];
+  }
+}
+
+// Per block of tokens: the sums of the blocks before it, then its own scan:
+// start[t], chunk_start[t] and the units of its tokens; the last block also
+// writes start[T] and chunk_start[T] (the totals).
+__global__ void __launch_bounds__(kScanThreads) invert_scan_kernel(const InvertParams q) {
+  __shared__ int32_t s_warp[2][kScanThreads / 32];
+  __shared__ int32_t s_tot[2];
+  __shared__ int32_t s_base[2];
+  pdl_wait();
+  pdl_release();
+  if (!invert_offsets_ok(q)) return;
+  const int tid = threadIdx.x;
+  // the blocks before this one: a strided sum, then a block reduction
+  int32_t pn = 0, pu = 0;
+  for (int b = tid; b < static_cast<int>(blockIdx.x); b += kScanThreads)
+    if (MXFP4_IN_BOUNDS(q, kDbgWork, q.block_sums + 2 * b, 8)) {
+      pn += q.block_sums[2 * b];
+      pu += q.block_sums[2 * b + 1];
+    }
+  int32_t dummy_n, dummy_u;
+  block_scan2(pn, pu, dummy_n, dummy_u, s_warp, s_tot);
+  if (tid == 0) { s_base[0] = s_tot[0]; s_base[1] = s_tot[1]; }
+  __syncthreads();
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kScanThreads + tid;
+  const int32_t n = route_count(q, t);
+  const int32_t nu = (n + 31) / 32;
+  int32_t ex_n, ex_u;
+  block_scan2(n, nu, ex_n, ex_u, s_warp, s_tot);
+  const int32_t st = s_base[0] + ex_n;
+  const int32_t cs = s_base[1] + ex_u;
+  if (t < q.num_src_rows) {
+    if (MXFP4_IN_BOUNDS(q, kDbgWork, q.start + t, 4)) q.start[t] = st;
+    if (MXFP4_IN_BOUNDS(q, kDbgWork, q.chunk_start + t, 4)) q.chunk_start[t] = cs;
+    for (int32_t c = 0; c < nu; ++c) {
+      if (MXFP4_IN_BOUNDS(q, kDbgWork, q.unit_token + cs + c, 4) &&
+          MXFP4_IN_BOUNDS(q, kDbgWork, q.unit_first + cs + c, 4)) {
+        q.unit_token[cs + c] = static_cast<int32_t>(t);
+        q.unit_first[cs + c] = st + 32 * c;
+      }
+    }
+  }
+  if (blockIdx.x == gridDim.x - 1 && tid == 0) {
+    const int64_t T = q.num_src_rows;
+    if (MXFP4_IN_BOUNDS(q, kDbgWork, q.start + T, 4)) q.start[T] = s_base[0] + s_tot[0];
+    if (MXFP4_IN_BOUNDS(q, kDbgWork, q.chunk_start + T, 4))
+      q.chunk_start[T] = s_base[1] + s_tot[1];
+  }
+}
+
+// Every valid row into its token's route range (count returns to zero).
+__global__ void __launch_bounds__(kInvertThreads) invert_fill_kernel(const InvertParams q) {
+  pdl_wait();
+  pdl_release();
+  if (!invert_offsets_ok(q)) return;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kInvertThreads;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kInvertThreads + threadIdx.x;
+       r < q.total_rows; r += stride) {
+    const int32_t* ip = q.row_index + r;
+    const int32_t t = MXFP4_IN_BOUNDS(q, kDbgRowIndex, ip, 4) ? __ldg(ip) : -1;
+    if (t < 0 || t >= q.num_src_rows) continue;
+    if (!MXFP4_IN_BOUNDS(q, kDbgWork, q.count + t, 4) ||
+        !MXFP4_IN_BOUNDS(q, kDbgWork, q.start + t, 4))
+      continue;
+    const int32_t pos = q.start[t] + atomicSub(q.count + t, 1) - 1;
+    if (MXFP4_IN_BOUNDS(q, kDbgWork, q.rows + pos, 4)) q.rows[pos] = static_cast<int32_t>(r);
+  }
+}
+
 // Validates 0 = o[0] <= o[1] <= ... <= o[E] = total_rows and writes the
 // padded row starts P[e] = sum_{e'<e} ceil(n_e'/128)*128 (P[E] = total).
-// One CTA of 1024 threads; a block-wide scan per 1024 segments.
-constexpr int kScanThreads = 1024;
+// One CTA of kScanThreads threads; a block-wide scan per kScanThreads segments.
 
 struct OffsetsParams {
   const int32_t* __restrict__ off;
@@ -630,6 +847,112 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
   debug_range(p.dbg, kDbgStatus, status, status ? 4 : 0);
 #endif
   const int64_t grid = E + (num_tokens + kScatterWarps - 1) / kScatterWarps;
+  const bool v32 = vec32_ok(x, p.ldx_bytes);
+  const auto kernel = f16 ? (v32 ? quantize_scatter_kernel<true, true>
+                                 : quantize_scatter_kernel<false, true>)
+                          : (v32 ? quantize_scatter_kernel<true, false>
+                                 : quantize_scatter_kernel<false, false>);
+  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
+}
+
+int64_t gather_workspace_ints(int64_t num_src_rows, int64_t total_rows) {
+  const int64_t units = num_src_rows + total_rows / 32 + 1;
+  const int64_t blocks = (num_src_rows + kScanThreads - 1) / kScanThreads;
+  return 3 * num_src_rows + 2 + 2 * units + total_rows + 2 * (blocks > 0 ? blocks : 1);
+}
+
+cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_t K,
+                                              int64_t ldx, const int32_t* row_index,
+                                              int64_t total_rows, const int32_t* offsets,
+                                              int32_t E, int32_t* workspace, uint8_t* codes,
+                                              uint8_t* scales, int32_t* scale_row_offsets,
+                                              int32_t* status, int64_t bound_tiles, bool f16,
+                                              cudaStream_t stream) {
+  cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
+  if (err != cudaSuccess || E == 0 || K == 0) return err;
+  const int64_t T = num_src_rows;
+  const int64_t units = T + total_rows / 32 + 1;
+  InvertParams q{};
+  q.row_index = row_index;
+  q.total_rows = total_rows;
+  q.num_src_rows = T;
+  q.count = workspace;
+  q.start = q.count + T;
+  q.chunk_start = q.start + (T + 1);
+  q.unit_token = q.chunk_start + (T + 1);
+  q.unit_first = q.unit_token + units;
+  q.rows = q.unit_first + units;
+  q.block_sums = q.rows + total_rows;
+  q.codes = codes;
+  q.scales = scales;
+  q.code_ld = K / 2;
+  q.offsets = offsets;
+  q.padded = scale_row_offsets;
+  q.E = E;
+  q.nKT = (static_cast<int32_t>(K / kBlock) + kTileBlocks - 1) / kTileBlocks;
+  q.status = status;
+  const int64_t ws_bytes = gather_workspace_ints(T, total_rows) * 4;
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(q.dbg, kDbgCodes, codes, total_rows * (K / 2));
+  debug_range(q.dbg, kDbgScales, scales, bound_tiles * q.nKT * kChunkBytes);
+  debug_range(q.dbg, kDbgOffsets, offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(q.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(q.dbg, kDbgRowIndex, row_index, total_rows * 4);
+  debug_range(q.dbg, kDbgStatus, status, status ? 4 : 0);
+  debug_range(q.dbg, kDbgWork, workspace, ws_bytes);
+#endif
+  if (T > 0) {
+    err = cudaMemsetAsync(q.count, 0, static_cast<size_t>(T) * 4, stream);
+    if (err != cudaSuccess) return err;
+  }
+  const int64_t row_ctas_max = static_cast<int64_t>(sm_count()) * 8;
+  const int64_t need = (total_rows + kInvertThreads - 1) / kInvertThreads;
+  const unsigned row_ctas = static_cast<unsigned>(need < 1 ? 1 : (need < row_ctas_max ? need : row_ctas_max));
+  if ((err = launch_pdl(invert_count_kernel, row_ctas, kInvertThreads, 0, stream, q)) != cudaSuccess)
+    return err;
+  const unsigned scan_blocks =
+      static_cast<unsigned>(T > 0 ? (T + kScanThreads - 1) / kScanThreads : 1);
+  if ((err = launch_pdl(invert_block_sum_kernel, scan_blocks, kScanThreads, 0, stream, q)) !=
+      cudaSuccess)
+    return err;
+  if ((err = launch_pdl(invert_scan_kernel, scan_blocks, kScanThreads, 0, stream, q)) !=
+      cudaSuccess)
+    return err;
+  if ((err = launch_pdl(invert_fill_kernel, row_ctas, kInvertThreads, 0, stream, q)) != cudaSuccess)
+    return err;
+  ScatterParams p{};
+  p.x = static_cast<const uint8_t*>(x);
+  p.ldx_bytes = ldx * 2;
+  p.num_tokens = T;
+  p.dest_rows = q.rows;
+  p.unit_token = q.unit_token;
+  p.unit_first = q.unit_first;
+  p.route_end = q.start + 1;
+  p.n_units = q.chunk_start + T;
+  p.top_k = 0;
+  p.E = E;
+  p.total_rows = total_rows;
+  p.code_ld = K / 2;
+  p.codes = codes;
+  p.scales = scales;
+  p.offsets = offsets;
+  p.padded = scale_row_offsets;
+  p.status = status;
+  p.sK = static_cast<int32_t>(K / kBlock);
+  p.nKT = q.nKT;
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(p.dbg, kDbgX, x, T > 0 ? ((T - 1) * ldx + K) * 2 : 0);
+  debug_range(p.dbg, kDbgCodes, codes, total_rows * (K / 2));
+  debug_range(p.dbg, kDbgScales, scales, bound_tiles * p.nKT * kChunkBytes);
+  debug_range(p.dbg, kDbgOffsets, offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(p.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(p.dbg, kDbgRowIndex, q.rows, total_rows * 4);
+  debug_range(p.dbg, kDbgStatus, status, status ? 4 : 0);
+  debug_range(p.dbg, kDbgWork, workspace, ws_bytes);
+#else
+  (void)ws_bytes;
+#endif
+  const int64_t grid = E + (units + kScatterWarps - 1) / kScatterWarps;
   const bool v32 = vec32_ok(x, p.ldx_bytes);
   const auto kernel = f16 ? (v32 ? quantize_scatter_kernel<true, true>
                                  : quantize_scatter_kernel<false, true>)

@@ -252,3 +252,26 @@ def test_f16_grouped_forms_share_the_validation(lib):
                                                 5 * A, 6 * A, None, None) == lib.MXFP4_ESHAPE
     assert L.mxfp4_quantize_grouped_scatter_f16(A, 10, 64, 64, 2 * A, 0, 10, 3 * A, 1, 4 * A,
                                                 5 * A, 6 * A, None, None) == lib.MXFP4_EINVAL
+
+
+def test_gather_ws_validation(lib):
+    f = lib._lib.mxfp4_quantize_grouped_gather_ws
+    ws_need = lib.mxfp4_gather_workspace_bytes(50, 10)
+    assert ws_need % 16 == 0 and ws_need >= 4 * (3 * 50 + 2 + 2 * (50 + 10 // 32 + 1) + 10)
+    # x, n_src, K, ldx, idx, total, off, E, ws, ws_bytes, codes, scales, sro, status, stream
+    ok = [A, 50, 64, 64, 2 * A, 10, 3 * A, 2, 8 * A, ws_need, 4 * A, 5 * A, 6 * A, None, None]
+
+    def call(**kw):
+        names = ["x", "n", "K", "ldx", "idx", "tot", "off", "E", "ws", "wsb", "c", "s", "sro",
+                 "st", "strm"]
+        a = dict(zip(names, ok))
+        a.update(kw)
+        return f(*[a[n] for n in names])
+
+    assert call(ws=None) == lib.MXFP4_EINVAL
+    assert call(wsb=ws_need - 16) == lib.MXFP4_EINVAL
+    assert call(ws=8 * A + 8) == lib.MXFP4_EALIGN
+    assert call(ws=4 * A + 16) == lib.MXFP4_EALIAS            # workspace overlaps the codes
+    assert call(ws=2 * A) == lib.MXFP4_EALIAS                 # workspace overlaps the indices
+    assert call(K=48, ldx=48) == lib.MXFP4_ESHAPE
+    assert call(n=(1 << 31) // 4 + 1, ldx=64) == lib.MXFP4_ESHAPE

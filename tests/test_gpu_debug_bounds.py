@@ -120,6 +120,9 @@ def test_everything_in_bounds(libs):
     xt2 = W.normal_bf16((300, 160), seed=14, device="cuda")
     ri = torch.from_numpy(rng.integers(0, 300, int(sizes.sum())).astype(np.int32)).cuda()
     cases.append(lambda: written(mx.quantize_grouped_gather(xt2, ri, off_z), 160))
+    cases.append(lambda: written(mx.quantize_grouped_gather(xt2, ri, off_z, via_scatter=False), 160))
+    cases.append(lambda: written(mx.quantize_grouped_gather(xt, idx_bad, off6, via_scatter=False),
+                                 64))
     cases.append(lambda: written(mx.quantize_grouped(xt2.index_select(0, ri.long()), off_z), 160))
     # scatter: all routes, dropped routes, bad entries, no tokens, strided
     cases.append(lambda: written(mx.quantize_grouped_scatter(gsmall.x_tokens, gsmall.dest_rows,

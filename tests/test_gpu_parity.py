@@ -980,3 +980,87 @@ def test_f16_dispatch_full_size(mx):
         assert np.array_equal(c1[a:b].cpu().numpy(), c_o)
         p0 = int(sro1[e].item()) * 224
         assert np.array_equal(s1[p0:p0 + s_o.size].cpu().numpy(), s_o)
+
+
+# -------------------------------------- fused gather through the scatter path
+def run_gather_ws(mx, x, row_index, offsets, f16=False):
+    total = row_index.numel()
+    K = x.shape[1]
+    E = offsets.numel() - 1
+    codes = Guarded(total * (K // 2), shape=(total, K // 2))
+    scales = Guarded(mx.mxfp4_grouped_scale_bytes_bound(total, E, K))
+    sro = Guarded(4 * (E + 1), torch.int32)
+    status = Guarded(4, torch.int32)
+    ws = Guarded(mx.mxfp4_gather_workspace_bytes(x.shape[0], total))
+    ws.t.fill_(0x5A)                                  # contents on entry must not matter
+    fn = mx.mxfp4_quantize_grouped_gather_ws_f16 if f16 else mx.mxfp4_quantize_grouped_gather_ws
+    fn(x, row_index, offsets, ws.t, codes.t, scales.t, sro.t, status.t)
+    torch.cuda.synchronize()
+    for g in (codes, scales, sro, status, ws):
+        g.check()
+    return (codes.t.cpu().numpy(), scales.t.cpu().numpy(), sro.t.cpu().numpy(),
+            int(status.t.cpu()[0]))
+
+
+def _gather_oracle_check(got, xb, idx, off, K, f16=False):
+    c, s, sro, st = got
+    rc, c_o, s_o, sro_o = oracle.quantize_grouped_gather(xb, idx, off, f16=f16)
+    assert st == rc and np.array_equal(sro, sro_o)
+    assert np.array_equal(c, c_o), _first_diff(c, c_o)
+    used = int(sro_o[-1]) * ((K // 32 + 3) // 4 * 4)
+    assert np.array_equal(s[:used], s_o[:used]), _first_diff(s[:used], s_o[:used])
+
+
+def test_gather_ws_small_strided_and_aligned(mx):
+    g = W.moe_grouped(seed=2, tokens=200, top_k=4, num_experts=12, K=288, device="cuda")
+    xb = bits(g.x_tokens)
+    idx = g.token_of_row.numpy().astype(np.int32)
+    off = g.offsets.cpu().numpy()
+    _gather_oracle_check(run_gather_ws(mx, g.x_tokens, g.row_index, g.offsets), xb, idx, off, 288)
+    wide = torch.zeros((200, 320), dtype=torch.bfloat16, device="cuda")
+    wide[:, 16:304] = g.x_tokens
+    _gather_oracle_check(run_gather_ws(mx, wide[:, 16:304], g.row_index, g.offsets), xb, idx, off,
+                         288)
+    _gather_oracle_check(run_gather_ws(mx, offset16(g.x_tokens), g.row_index, g.offsets), xb, idx,
+                         off, 288)
+
+
+def test_gather_ws_bad_index_heavy_and_unused_tokens(mx):
+    """Out-of-range indices give zero rows; one token taken by 70 rows (three
+    units of up to 32 routes); most tokens taken by none."""
+    xt = W.small_matrix(3, 40, 64).cuda()
+    rng = np.random.default_rng(9)
+    idx = rng.integers(0, 5, 300).astype(np.int32)     # only tokens 0..4 are used
+    idx[rng.permutation(300)[:70]] = 7                  # token 7: 70 rows
+    idx[[5, 17, 250]] = [-1, 40, 1 << 20]               # out of range
+    off = np.array([0, 33, 33, 160, 300], np.int32)
+    got = run_gather_ws(mx, xt, torch.from_numpy(idx).cuda(), torch.from_numpy(off).cuda())
+    assert got[3] == mx.MXFP4_EINDEX
+    _gather_oracle_check(got, bits(xt), idx, off, 64)
+    assert not got[0][[5, 17, 250]].any()
+
+
+def test_gather_ws_bad_offsets_write_nothing(mx):
+    xt = W.small_matrix(3, 16, 64).cuda()
+    idx = torch.arange(20, dtype=torch.int32, device="cuda") % 16
+    off = torch.tensor([0, 12, 8, 20], dtype=torch.int32, device="cuda")
+    c, s, sro, st = run_gather_ws(mx, xt, idx, off)
+    assert st == mx.MXFP4_EOFFSETS and (sro == -1).all()
+    assert (c == 0xA5).all() and (s == 0xA5).all()
+
+
+def test_gather_ws_fp16_and_full_size(mx):
+    g = W.moe_grouped(seed=13, tokens=130, top_k=3, num_experts=6, K=96, device="cuda")
+    x16 = g.x_tokens.to(torch.float16)
+    hb = x16.cpu().view(torch.int16).numpy().view(np.uint16)
+    _gather_oracle_check(run_gather_ws(mx, x16, g.row_index, g.offsets, f16=True), hb,
+                         g.token_of_row.numpy().astype(np.int32), g.offsets.cpu().numpy(), 96,
+                         f16=True)
+    G = W.moe_grouped(seed=2, device="cuda")
+    c1, s1, sro1, st1 = mx.quantize_grouped_gather(G.x_tokens, G.row_index, G.offsets)
+    c2, s2, sro2, st2 = mx.quantize_grouped_gather(G.x_tokens, G.row_index, G.offsets,
+                                                   via_scatter=False)
+    torch.cuda.synchronize()
+    assert int(st1.item()) == 0 and int(st2.item()) == 0 and torch.equal(sro1, sro2)
+    used = int(sro1[-1].item()) * 224
+    assert torch.equal(c1, c2) and torch.equal(s1[:used], s2[:used])
