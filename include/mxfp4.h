@@ -57,8 +57,10 @@ typedef enum {
   MXFP4_EALIAS = -4,   /* an output byte range overlaps an input or another output */
   MXFP4_ECUDA = -5,    /* the CUDA runtime refused a launch                        */
   MXFP4_EOFFSETS = -6, /* device-detected: expert offsets not 0 = o[0] <= ... <= o[E] = rows */
-  MXFP4_EINDEX = -7    /* device-detected: a gather row index outside [0, num_src_rows),
+  MXFP4_EINDEX = -7,   /* device-detected: a gather row index outside [0, num_src_rows),
                           or a scatter entry outside [-1, total_rows) */
+  MXFP4_ESCRATCH = -8  /* the call needs more scratch than the library's fixed buffer
+                          (mxfp4_quantize_grouped_gather_noalloc) */
 } mxfp4_status;
 
 /* Bytes of the 128x4-tiled scale buffer of an [M, K] matrix:
@@ -191,6 +193,32 @@ int mxfp4_quantize_grouped_gather_ws_f16(const void* x, int64_t num_src_rows, in
                                          uint8_t* codes, uint8_t* scales,
                                          int32_t* scale_row_offsets, int32_t* status,
                                          void* stream);
+
+/* mxfp4_quantize_grouped_gather_noalloc — mxfp4_quantize_grouped_gather_ws
+ * without a caller workspace and without any allocation: the inverse map is
+ * built in a fixed scratch buffer of MXFP4_NOALLOC_SCRATCH_BYTES inside the
+ * library (a device array every GPU that loads the library holds until the
+ * process exits).  For callers that cannot allocate device memory.  No
+ * counterpart exists in the method's sources.
+ *
+ * Arguments, outputs, status and errors as mxfp4_quantize_grouped_gather, and
+ * MXFP4_ESCRATCH (returned before anything is enqueued) when
+ * mxfp4_gather_workspace_bytes(num_src_rows, total_rows) exceeds
+ * MXFP4_NOALLOC_SCRATCH_BYTES.
+ * Every call shares the one buffer of its device: two calls that can overlap
+ * on the GPU (different streams, or a graph replayed concurrently) race and
+ * give wrong results; serialise them.  The buffer keeps the last call's
+ * contents; each call clears what must start at zero.  The first call on a
+ * device looks up the buffer's device address (a host-side query, once per
+ * device): make that first call outside any stream capture.
+ */
+#define MXFP4_NOALLOC_SCRATCH_BYTES (4u << 20)
+int mxfp4_quantize_grouped_gather_noalloc(const void* x, int64_t num_src_rows, int64_t K,
+                                          int64_t ldx, const int32_t* row_index,
+                                          int64_t total_rows, const int32_t* expert_offsets,
+                                          int32_t E, uint8_t* codes, uint8_t* scales,
+                                          int32_t* scale_row_offsets, int32_t* status,
+                                          void* stream);
 
 /* mxfp4_quantize_grouped_scatter — the same dispatch given in the direction
  * a router's sort produces it (token, route -> row): each token row of x is

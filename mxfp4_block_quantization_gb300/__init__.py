@@ -34,7 +34,8 @@ __all__ = [
     "MXFP4_SCATTER_MAX_TOP_K", "mxfp4_quantize_f16", "mxfp4_quantize_grouped_f16",
     "mxfp4_quantize_grouped_gather_f16", "mxfp4_quantize_grouped_scatter_f16",
     "mxfp4_gather_workspace_bytes", "mxfp4_quantize_grouped_gather_ws",
-    "mxfp4_quantize_grouped_gather_ws_f16", "mxfp4_nvfp4_scale_bytes",
+    "mxfp4_quantize_grouped_gather_ws_f16", "mxfp4_quantize_grouped_gather_noalloc",
+    "MXFP4_ESCRATCH", "MXFP4_NOALLOC_SCRATCH_BYTES", "mxfp4_nvfp4_scale_bytes",
     "mxfp4_quantize_nvfp4", "mxfp4_dequantize_nvfp4", "quantize_nvfp4", "dequantize_nvfp4",
     "mxfp4_nvfp4_grouped_scale_bytes_bound", "mxfp4_quantize_nvfp4_grouped",
     "quantize_nvfp4_grouped",
@@ -46,6 +47,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb
 DEBUG_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300_debug.so")
 
 MXFP4_SCATTER_MAX_TOP_K = 32
+MXFP4_NOALLOC_SCRATCH_BYTES = 4 << 20
 MXFP4_OK = 0
 MXFP4_EINVAL = -1
 MXFP4_EALIGN = -2
@@ -54,6 +56,7 @@ MXFP4_EALIAS = -4
 MXFP4_ECUDA = -5
 MXFP4_EOFFSETS = -6
 MXFP4_EINDEX = -7
+MXFP4_ESCRATCH = -8
 
 
 class MXFP4Error(RuntimeError):
@@ -95,6 +98,9 @@ def _load(path=LIB_PATH):
         getattr(L, name).restype = ctypes.c_int
         getattr(L, name).argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, ctypes.c_size_t,
                                      vp, vp, vp, vp, vp]
+    L.mxfp4_quantize_grouped_gather_noalloc.restype = ctypes.c_int
+    L.mxfp4_quantize_grouped_gather_noalloc.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp,
+                                                        vp, vp, vp, vp]
     L.mxfp4_quantize_grouped_gather.restype = ctypes.c_int
     L.mxfp4_quantize_grouped_gather.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, vp, vp,
                                                 vp, vp]
@@ -310,6 +316,31 @@ def mxfp4_quantize_grouped_gather_ws(x, row_index, expert_offsets, workspace, co
     map is built in ``workspace`` (device, >= mxfp4_gather_workspace_bytes)."""
     _gather_ws(x, row_index, expert_offsets, workspace, codes, scales, scale_row_offsets, status,
                stream, False)
+
+
+def mxfp4_quantize_grouped_gather_noalloc(x, row_index, expert_offsets, codes, scales,
+                                          scale_row_offsets, status=None, stream=None) -> None:
+    """mxfp4_quantize_grouped_gather_ws with the library's fixed scratch
+    buffer (no workspace, no allocation); calls must not overlap on the GPU."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("row_index", row_index, torch.int32)
+    _need_cuda("expert_offsets", expert_offsets, torch.int32)
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    _need_cuda("scale_row_offsets", scale_row_offsets, torch.int32)
+    _need_cuda("status", status, torch.int32)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    if not row_index.is_contiguous():
+        raise ValueError("row_index must be contiguous")
+    n_src, K = x.shape
+    E = expert_offsets.numel() - 1
+    with torch.cuda.device(_device_of(x, row_index, expert_offsets, codes, scales,
+                                      scale_row_offsets, status)):
+        _check(_lib.mxfp4_quantize_grouped_gather_noalloc(
+            _ptr(x), n_src, K, x.stride(0), _ptr(row_index), row_index.numel(),
+            _ptr(expert_offsets), E, _ptr(codes), _ptr(scales), _ptr(scale_row_offsets),
+            _ptr(status), _stream(stream, x.device)), "mxfp4_quantize_grouped_gather_noalloc")
 
 
 def mxfp4_quantize_grouped_gather_ws_f16(x, row_index, expert_offsets, workspace, codes, scales,

@@ -32,6 +32,26 @@ int sm_count() {
   return cached[dev];
 }
 
+// Fixed scratch of mxfp4_quantize_grouped_gather_noalloc: the inverse-map
+// workspace of the gather-through-scatter path, for callers that cannot
+// allocate.  Host code only ever uses its device address, looked up once per
+// device with that device current.
+static __device__ __align__(256) int32_t g_noalloc_scratch[MXFP4_NOALLOC_SCRATCH_BYTES / 4];
+
+int32_t* noalloc_scratch() {
+  static std::mutex mu;
+  static int32_t* cached[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    cached[dev] = static_cast<int32_t*>(ptr);
+  }
+  return cached[dev];
+}
+
 }  // namespace mxfp4
 
 namespace {
@@ -306,6 +326,22 @@ int mxfp4_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_
                         true, false, stream);
 }
 
+int mxfp4_quantize_grouped_gather_noalloc(const void* x, int64_t num_src_rows, int64_t K,
+                                          int64_t ldx, const int32_t* row_index,
+                                          int64_t total_rows, const int32_t* expert_offsets,
+                                          int32_t E, uint8_t* codes, uint8_t* scales,
+                                          int32_t* scale_row_offsets, int32_t* status,
+                                          void* stream) {
+  if (num_src_rows < 0 || total_rows < 0) return MXFP4_EINVAL;
+  if (mxfp4_gather_workspace_bytes(num_src_rows, total_rows) > MXFP4_NOALLOC_SCRATCH_BYTES)
+    return MXFP4_ESCRATCH;
+  int32_t* scratch = mxfp4::noalloc_scratch();
+  if (scratch == nullptr) return MXFP4_ECUDA;
+  return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E,
+                        scratch, MXFP4_NOALLOC_SCRATCH_BYTES, codes, scales, scale_row_offsets,
+                        status, true, false, stream);
+}
+
 int mxfp4_quantize_grouped_gather_ws_f16(const void* x, int64_t num_src_rows, int64_t K,
                                          int64_t ldx, const int32_t* row_index,
                                          int64_t total_rows, const int32_t* expert_offsets,
@@ -520,7 +556,12 @@ const char* mxfp4_status_string(int status) {
     case MXFP4_EALIAS: return "MXFP4_EALIAS: an output overlaps an input or another output";
     case MXFP4_ECUDA: return "MXFP4_ECUDA: kernel launch failed";
     case MXFP4_EOFFSETS: return "MXFP4_EOFFSETS: expert offsets are not 0 <= ... <= total_rows";
-    case MXFP4_EINDEX: return "MXFP4_EINDEX: a gather row index is outside [0, num_src_rows)";
+    case MXFP4_EINDEX:
+      return "MXFP4_EINDEX: a gather row index is outside [0, num_src_rows) or a scatter entry "
+             "outside [-1, total_rows)";
+    case MXFP4_ESCRATCH:
+      return "MXFP4_ESCRATCH: the call needs more than the library's fixed scratch buffer "
+             "(MXFP4_NOALLOC_SCRATCH_BYTES); use mxfp4_quantize_grouped_gather_ws";
     default: return "unknown mxfp4 status";
   }
 }

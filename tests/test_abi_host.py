@@ -275,3 +275,14 @@ def test_gather_ws_validation(lib):
     assert call(ws=2 * A) == lib.MXFP4_EALIAS                 # workspace overlaps the indices
     assert call(K=48, ldx=48) == lib.MXFP4_ESHAPE
     assert call(n=(1 << 31) // 4 + 1, ldx=64) == lib.MXFP4_ESHAPE
+
+
+def test_noalloc_gather_rejects_oversized_scratch(lib):
+    """Sizes whose inverse map would not fit the library's fixed scratch are
+    refused with MXFP4_ESCRATCH before any device work (no GPU needed)."""
+    f = lib._lib.mxfp4_quantize_grouped_gather_noalloc
+    assert lib.mxfp4_gather_workspace_bytes(10_000_000, 1) > lib.MXFP4_NOALLOC_SCRATCH_BYTES
+    rc = f(A, 10_000_000, 64, 64, 2 * A, 1, 3 * A, 1, 4 * A, 5 * A, 6 * A, None, None)
+    assert rc == lib.MXFP4_ESCRATCH
+    assert "MXFP4_ESCRATCH" in lib.mxfp4_status_string(rc)
+    assert f(A, -1, 64, 64, 2 * A, 1, 3 * A, 1, 4 * A, 5 * A, 6 * A, None, None) == lib.MXFP4_EINVAL

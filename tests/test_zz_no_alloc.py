@@ -1,0 +1,53 @@
+"""The gather entry point that allocates nothing (its scratch is a fixed
+device buffer inside the library), through the C ABI: two calls in a row,
+each compared byte for byte with the per-row gather entry point on the same
+inputs.  Collected last on purpose."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from mxfp4_block_quantization_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _outputs(mx, total, K, E):
+    codes = torch.full((total, K // 2), 0xA5, dtype=torch.uint8, device="cuda")
+    scales = torch.full((mx.mxfp4_grouped_scale_bytes_bound(total, E, K),), 0xA5,
+                        dtype=torch.uint8, device="cuda")
+    sro = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    st = torch.empty(1, dtype=torch.int32, device="cuda")
+    return codes, scales, sro, st
+
+
+def _call(fn, x, idx, off, out):
+    vp = ctypes.c_void_p
+    codes, scales, sro, st = out
+    s = vp(torch.cuda.current_stream().cuda_stream)
+    return fn(vp(x.data_ptr()), x.shape[0], x.shape[1], x.stride(0), vp(idx.data_ptr()),
+              idx.numel(), vp(off.data_ptr()), off.numel() - 1, vp(codes.data_ptr()),
+              vp(scales.data_ptr()), vp(sro.data_ptr()), vp(st.data_ptr()), s)
+
+
+def test_noalloc_gather_two_calls_match_the_gather_entry_point():
+    assert torch.cuda.is_available()
+    import mxfp4_block_quantization_gb300 as mx
+    L = mx._lib
+    for seed, tokens, top_k, E, K in ((21, 300, 4, 11, 288), (22, 2048, 8, 64, 1024)):
+        g = W.moe_grouped(seed=seed, tokens=tokens, top_k=top_k, num_experts=E, K=K,
+                          device="cuda")
+        total = g.row_index.numel()
+        need = mx.mxfp4_gather_workspace_bytes(tokens, total)
+        assert need <= mx.MXFP4_NOALLOC_SCRATCH_BYTES
+        ref = _outputs(mx, total, K, E)
+        assert _call(L.mxfp4_quantize_grouped_gather, g.x_tokens, g.row_index, g.offsets,
+                     ref) == mx.MXFP4_OK
+        got = _outputs(mx, total, K, E)
+        assert _call(L.mxfp4_quantize_grouped_gather_noalloc, g.x_tokens, g.row_index,
+                     g.offsets, got) == mx.MXFP4_OK
+        torch.cuda.synchronize()
+        assert int(got[3].item()) == int(ref[3].item()) == mx.MXFP4_OK
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b), seed
