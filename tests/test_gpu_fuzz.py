@@ -1,0 +1,134 @@
+"""Seeded random cases across every quantize form, each compared with the
+oracle byte for byte: random row counts, K, row strides, 16- versus 32-byte
+alignment, BF16 / FP16, expert segment sizes (empty ones included), routings
+with dropped routes, top_k, and NVFP4 global scales."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp4_block_quantization_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mx():
+    assert torch.cuda.is_available()
+    import mxfp4_block_quantization_gb300 as m
+    return m
+
+
+def _bits(t):
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _place(x, rng):
+    """x in a buffer with a random extra row stride and a 16- or 32-byte
+    aligned base."""
+    M, K = x.shape
+    pad = int(rng.integers(0, 3)) * 8
+    off = int(rng.integers(0, 2)) * 8
+    buf = torch.zeros(M * (K + pad) + off + 8, dtype=x.dtype, device="cuda")
+    y = buf[off:off + M * (K + pad)].view(M, K + pad)[:, :K]
+    y.copy_(x)
+    return y
+
+
+def _random_x(rng, M, K, f16):
+    x = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32))
+    x = x * torch.exp2(torch.from_numpy(rng.uniform(-10, 10, (M, 1)).astype(np.float32)))
+    return x.to(torch.float16 if f16 else torch.bfloat16).cuda()
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fuzz_dense(mx, seed):
+    rng = np.random.default_rng(100 + seed)
+    M, K = int(rng.integers(1, 700)), 32 * int(rng.integers(1, 100))
+    f16 = bool(seed % 3 == 0)
+    x = _place(_random_x(rng, M, K, f16), rng)
+    c, s = mx.quantize(x)
+    c_o, s_o = (oracle.quantize_f16 if f16 else oracle.quantize)(_bits(x))
+    assert np.array_equal(c.cpu().numpy(), c_o) and np.array_equal(s.cpu().numpy(), s_o), (M, K)
+    if not f16:
+        y = mx.dequantize(c, s, M, K)
+        assert np.array_equal(_bits(y), oracle.dequantize(c_o, s_o, M, K))
+
+
+def _random_offsets(rng, E, total):
+    cuts = np.sort(rng.integers(0, total + 1, E - 1))
+    cuts[rng.random(E - 1) < 0.2] = cuts[0] if E > 1 else 0  # some empty segments
+    cuts = np.sort(cuts)
+    return np.concatenate([[0], cuts, [total]]).astype(np.int32)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fuzz_grouped_gather_scatter(mx, seed):
+    rng = np.random.default_rng(200 + seed)
+    T, top_k = int(rng.integers(1, 400)), int(rng.integers(1, 13))
+    K = 32 * int(rng.integers(1, 60))
+    E = int(rng.integers(1, 40))
+    f16 = bool(seed % 2)
+    xt = _random_x(rng, T, K, f16)
+    # routing: every route a distinct row; 15 % of routes dropped
+    total = T * top_k
+    perm = rng.permutation(total).astype(np.int32)
+    dest = perm.reshape(T, top_k).copy()
+    drop = rng.random((T, top_k)) < 0.15
+    dest[drop] = -1
+    row_tok = np.full(total, -1, np.int32)
+    for t in range(T):
+        for j in range(top_k):
+            if dest[t, j] >= 0:
+                row_tok[dest[t, j]] = t
+    off = _random_offsets(rng, E, total)
+    xb = _bits(xt)
+    xp = _place(xt, rng)
+    off_d = torch.from_numpy(off).cuda()
+    # scatter: untargeted rows keep the prefill
+    nsb = mx.mxfp4_grouped_scale_bytes_bound(total, E, K)
+    c0 = rng.integers(0, 256, (total, K // 2), dtype=np.uint8)
+    s0 = rng.integers(0, 256, nsb, dtype=np.uint8)
+    codes = torch.from_numpy(c0).cuda()
+    scales = torch.from_numpy(s0).cuda()
+    sro = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    st = torch.empty(1, dtype=torch.int32, device="cuda")
+    fn = mx.mxfp4_quantize_grouped_scatter_f16 if f16 else mx.mxfp4_quantize_grouped_scatter
+    fn(xp, torch.from_numpy(dest).cuda(), off_d, total, codes, scales, sro, st)
+    rc, c_o, s_o, sro_o = oracle.quantize_grouped_scatter(xb, dest, off, total, c0, s0, f16=f16)
+    torch.cuda.synchronize()
+    assert int(st.item()) == rc == 0
+    assert np.array_equal(codes.cpu().numpy(), c_o) and np.array_equal(scales.cpu().numpy(), s_o)
+    # gather (both kernels): dropped rows have index -1 -> zero rows, EINDEX
+    rc_g, cg_o, sg_o, _ = oracle.quantize_grouped_gather(xb, row_tok, off, f16=f16)
+    used = int(sro_o[-1]) * ((K // 32 + 3) // 4 * 4)
+    for via in (True, False):
+        c, s, r, stt = mx.quantize_grouped_gather(xp, torch.from_numpy(row_tok).cuda(), off_d,
+                                                  via_scatter=via)
+        torch.cuda.synchronize()
+        assert int(stt.item()) == rc_g
+        assert np.array_equal(c.cpu().numpy(), cg_o), via
+        assert np.array_equal(s[:used].cpu().numpy(), sg_o[:used]), via
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_fuzz_nvfp4(mx, seed):
+    rng = np.random.default_rng(300 + seed)
+    M, K = int(rng.integers(1, 500)), 16 * int(rng.integers(1, 120))
+    x = _place(_random_x(rng, M, K, False), rng)
+    g = float(np.float32(448.0 * 6.0 / np.exp(rng.uniform(-3, 8))))
+    c, s = mx.quantize_nvfp4(x, torch.tensor([g], device="cuda"))
+    c_o, s_o = oracle.nvfp4_quantize(_bits(x), g)
+    assert np.array_equal(c.cpu().numpy(), c_o) and np.array_equal(s.cpu().numpy(), s_o)
+    if M > 1 and x.is_contiguous() and x.data_ptr() % 16 == 0:
+        E = int(rng.integers(1, 9))
+        off = _random_offsets(rng, E, M)
+        gs = (448.0 * 6.0 / np.exp(rng.uniform(-3, 8, E))).astype(np.float32)
+        cg, sg, sro, st = mx.quantize_nvfp4_grouped(x, torch.from_numpy(off).cuda(),
+                                                    torch.from_numpy(gs).cuda())
+        rc, cg_o, sg_o, sro_o = oracle.nvfp4_quantize_grouped(_bits(x), off, gs)
+        torch.cuda.synchronize()
+        assert int(st.item()) == rc == 0
+        used = int(sro_o[-1]) * ((K // 16 + 3) // 4 * 4)
+        assert np.array_equal(cg.cpu().numpy(), cg_o)
+        assert np.array_equal(sg[:used].cpu().numpy(), sg_o[:used])
