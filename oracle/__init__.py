@@ -105,6 +105,11 @@ def lib():
         L.orc_quantize_grouped_scatter_f16.argtypes = [_u16p, _i64, _i64, _i64, _i32p,
                                                        ctypes.c_int32, _i64, _i32p,
                                                        ctypes.c_int32, _u8p, _u8p, _i32p]
+        L.orc_nvfp4_quantize_f16.restype = None
+        L.orc_nvfp4_quantize_f16.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_float, _u8p, _u8p]
+        L.orc_nvfp4_quantize_grouped_f16.restype = ctypes.c_int
+        L.orc_nvfp4_quantize_grouped_f16.argtypes = [_u16p, _i64, _i64, _i32p, ctypes.c_int32,
+                                                     _f32p, _u8p, _u8p, _i32p]
         L.orc_quantize_grouped_scatter.restype = ctypes.c_int
         L.orc_quantize_grouped_scatter.argtypes = [_u16p, _i64, _i64, _i64, _i32p, ctypes.c_int32,
                                                    _i64, _i32p, ctypes.c_int32, _u8p, _u8p, _i32p]
@@ -449,15 +454,15 @@ def nvfp4_quantize_flat(xbits: np.ndarray, g: float):
     return codes, flat
 
 
-def nvfp4_quantize(xbits: np.ndarray, g: float):
+def nvfp4_quantize(xbits: np.ndarray, g: float, f16: bool = False):
     """NVFP4 on BF16 [M, K]: (codes [M, K/2], 128x4-tiled E4M3 scales)."""
     x = _c(xbits, np.uint16)
     M, K = x.shape
     codes = np.zeros((M, K // 2), np.uint8)
     scales = np.zeros(nvfp4_scale_bytes(M, K), np.uint8)
     if M and K:
-        lib().orc_nvfp4_quantize(_p(x, _u16p), M, K, K, float(np.float32(g)), _p(codes, _u8p),
-                                 _p(scales, _u8p))
+        fn = lib().orc_nvfp4_quantize_f16 if f16 else lib().orc_nvfp4_quantize
+        fn(_p(x, _u16p), M, K, K, float(np.float32(g)), _p(codes, _u8p), _p(scales, _u8p))
     return codes, scales
 
 
@@ -466,7 +471,8 @@ def nvfp4_grouped_scale_bytes_bound(total_rows: int, E: int, K: int) -> int:
     return tiles * 128 * ((K // 16 + 3) // 4 * 4)
 
 
-def nvfp4_quantize_grouped(xbits: np.ndarray, offsets: np.ndarray, g: np.ndarray):
+def nvfp4_quantize_grouped(xbits: np.ndarray, offsets: np.ndarray, g: np.ndarray,
+                           f16: bool = False):
     """NVFP4 experts quant: (rc, codes, scales, scale_row_offsets); rc 0 or -6.
     g: float32 [E] global scales, one per segment."""
     x = _c(xbits, np.uint16)
@@ -478,9 +484,9 @@ def nvfp4_quantize_grouped(xbits: np.ndarray, offsets: np.ndarray, g: np.ndarray
     codes = np.zeros((total, K // 2), np.uint8)
     scales = np.zeros(max(nvfp4_grouped_scale_bytes_bound(total, E, K), 1), np.uint8)
     sro = np.zeros(E + 1, np.int32)
-    rc = lib().orc_nvfp4_quantize_grouped(_p(x, _u16p), total, K, _p(off, _i32p), E,
-                                          _p(gs, _f32p), _p(codes, _u8p), _p(scales, _u8p),
-                                          _p(sro, _i32p))
+    fn = lib().orc_nvfp4_quantize_grouped_f16 if f16 else lib().orc_nvfp4_quantize_grouped
+    rc = fn(_p(x, _u16p), total, K, _p(off, _i32p), E, _p(gs, _f32p), _p(codes, _u8p),
+            _p(scales, _u8p), _p(sro, _i32p))
     return rc, codes, scales, sro
 
 

@@ -597,10 +597,15 @@ uint8_t orc_e4m3_from_double(double d) {
 static float f32_of_bf16(uint16_t b) { return bf16_to_float(b); }
 
 /* Steps of one 16-element block: its E4M3 scale byte and 16 nibbles. */
-static void nvfp4_block(const uint16_t* x, float g, uint8_t* sf_byte, uint8_t* nib) {
+/* A 16-bit element as float (exact for both input formats). */
+static float f32_of_f16(uint16_t h) { return (float)orc_f16_to_double(h); }
+typedef float (*to_f32_fn)(uint16_t);
+
+static void nvfp4_block_of(to_f32_fn to_f32, const uint16_t* x, float g, uint8_t* sf_byte,
+                           uint8_t* nib) {
   float vmax = 0.0f;
   for (int i = 0; i < 16; ++i) {
-    float a = f32_of_bf16((uint16_t)(x[i] & 0x7FFFu));
+    float a = to_f32((uint16_t)(x[i] & 0x7FFFu));
     if (a > vmax) vmax = a;
   }
   float q = vmax / 6.0f; /* each float step rounds once (no contraction) */
@@ -614,7 +619,7 @@ static void nvfp4_block(const uint16_t* x, float g, uint8_t* sf_byte, uint8_t* n
   }
   float inv = g / sfv;
   for (int i = 0; i < 16; ++i) {
-    float y = f32_of_bf16(x[i]) * inv;
+    float y = to_f32(x[i]) * inv;
     nib[i] = e2m1_round((double)y, (x[i] >> 15) & 1u);
   }
 }
@@ -624,26 +629,43 @@ size_t orc_nvfp4_scale_bytes(int64_t M, int64_t K) {
   return (size_t)((M + 127) / 128 * 128 * ((K / 16 + 3) / 4 * 4));
 }
 
-void orc_nvfp4_quantize_flat(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float g,
-                             uint8_t* codes, uint8_t* flat_scales) {
+static void nvfp4_flat_of(to_f32_fn to_f32, const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                          float g, uint8_t* codes, uint8_t* flat_scales) {
   int64_t sK = K / 16;
   for (int64_t r = 0; r < M; ++r)
     for (int64_t b = 0; b < sK; ++b) {
       uint8_t nib[16];
-      nvfp4_block(x + r * ldx + b * 16, g, &flat_scales[r * sK + b], nib);
+      nvfp4_block_of(to_f32, x + r * ldx + b * 16, g, &flat_scales[r * sK + b], nib);
       for (int j = 0; j < 8; ++j)
         codes[r * (K / 2) + b * 8 + j] = (uint8_t)(nib[2 * j] | (nib[2 * j + 1] << 4));
     }
 }
 
-void orc_nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float g,
-                        uint8_t* codes, uint8_t* tiled_scales) {
+void orc_nvfp4_quantize_flat(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float g,
+                             uint8_t* codes, uint8_t* flat_scales) {
+  nvfp4_flat_of(f32_of_bf16, x, M, K, ldx, g, codes, flat_scales);
+}
+
+static void nvfp4_quantize_of(to_f32_fn to_f32, const uint16_t* x, int64_t M, int64_t K,
+                              int64_t ldx, float g, uint8_t* codes, uint8_t* tiled_scales) {
   int64_t sK = K / 16;
   if (M <= 0 || sK <= 0) return;
   uint8_t* flat = (uint8_t*)calloc((size_t)(M * sK), 1);
-  orc_nvfp4_quantize_flat(x, M, K, ldx, g, codes, flat);
+  nvfp4_flat_of(to_f32, x, M, K, ldx, g, codes, flat);
   orc_tile_scales(flat, M, sK, tiled_scales); /* same 128x4 tiling, 16-element columns */
   free(flat);
+}
+
+void orc_nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float g,
+                        uint8_t* codes, uint8_t* tiled_scales) {
+  nvfp4_quantize_of(f32_of_bf16, x, M, K, ldx, g, codes, tiled_scales);
+}
+
+/* The same NVFP4 steps on IEEE binary16 input (every FP16 value is exact in
+ * float32, so only the decoding of the element changes). */
+void orc_nvfp4_quantize_f16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float g,
+                            uint8_t* codes, uint8_t* tiled_scales) {
+  nvfp4_quantize_of(f32_of_f16, x, M, K, ldx, g, codes, tiled_scales);
 }
 
 /* NVFP4 experts quant: the grouped layout of step 6 with the NVFP4 block
@@ -652,9 +674,9 @@ void orc_nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, fl
  * matrix with its own global scale g[e]; codes keep the row order; its tiled
  * E4M3 scales (16-element columns, padded to 128 rows) start at padded row
  * P[e].  Bad offsets: -6, scale row offsets all -1, nothing else written. */
-int orc_nvfp4_quantize_grouped(const uint16_t* x, int64_t total_rows, int64_t K,
-                               const int32_t* offsets, int32_t E, const float* g,
-                               uint8_t* codes, uint8_t* scales, int32_t* scale_row_offsets) {
+static int nvfp4_grouped_of(to_f32_fn to_f32, const uint16_t* x, int64_t total_rows, int64_t K,
+                            const int32_t* offsets, int32_t E, const float* g, uint8_t* codes,
+                            uint8_t* scales, int32_t* scale_row_offsets) {
   int ok = (E >= 0) && offsets[0] == 0 && (int64_t)offsets[E] == total_rows;
   for (int32_t e = 0; ok && e < E; ++e) ok = offsets[e] <= offsets[e + 1];
   if (!ok) {
@@ -666,12 +688,26 @@ int orc_nvfp4_quantize_grouped(const uint16_t* x, int64_t total_rows, int64_t K,
   for (int32_t e = 0; e < E; ++e) {
     int64_t n = (int64_t)offsets[e + 1] - offsets[e];
     scale_row_offsets[e] = (int32_t)P;
-    orc_nvfp4_quantize(x + (int64_t)offsets[e] * K, n, K, K, g[e],
-                       codes + (int64_t)offsets[e] * (K / 2), scales + P * padded_sK);
+    nvfp4_quantize_of(to_f32, x + (int64_t)offsets[e] * K, n, K, K, g[e],
+                      codes + (int64_t)offsets[e] * (K / 2), scales + P * padded_sK);
     P += (n + 127) / 128 * 128;
   }
   scale_row_offsets[E] = (int32_t)P;
   return 0;
+}
+
+int orc_nvfp4_quantize_grouped(const uint16_t* x, int64_t total_rows, int64_t K,
+                               const int32_t* offsets, int32_t E, const float* g,
+                               uint8_t* codes, uint8_t* scales, int32_t* scale_row_offsets) {
+  return nvfp4_grouped_of(f32_of_bf16, x, total_rows, K, offsets, E, g, codes, scales,
+                          scale_row_offsets);
+}
+
+int orc_nvfp4_quantize_grouped_f16(const uint16_t* x, int64_t total_rows, int64_t K,
+                                   const int32_t* offsets, int32_t E, const float* g,
+                                   uint8_t* codes, uint8_t* scales, int32_t* scale_row_offsets) {
+  return nvfp4_grouped_of(f32_of_f16, x, total_rows, K, offsets, E, g, codes, scales,
+                          scale_row_offsets);
 }
 
 void orc_nvfp4_dequantize(const uint8_t* codes, const uint8_t* tiled_scales, int64_t M, int64_t K,

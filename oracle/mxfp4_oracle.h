@@ -139,6 +139,12 @@ void orc_nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, fl
 int orc_nvfp4_quantize_grouped(const uint16_t* x, int64_t total_rows, int64_t K,
                                const int32_t* offsets, int32_t E, const float* g,
                                uint8_t* codes, uint8_t* scales, int32_t* scale_row_offsets);
+/* NVFP4 on IEEE binary16 input (dense and experts quant). */
+void orc_nvfp4_quantize_f16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float g,
+                            uint8_t* codes, uint8_t* tiled_scales);
+int orc_nvfp4_quantize_grouped_f16(const uint16_t* x, int64_t total_rows, int64_t K,
+                                   const int32_t* offsets, int32_t E, const float* g,
+                                   uint8_t* codes, uint8_t* scales, int32_t* scale_row_offsets);
 void orc_nvfp4_dequantize(const uint8_t* codes, const uint8_t* tiled_scales, int64_t M, int64_t K,
                           float g, uint16_t* y);
 

@@ -143,3 +143,32 @@ def test_nvfp4_grouped_uniform_tiles_equal_dense_and_bad_offsets(orc):
     rc, _, _, sro = orc.nvfp4_quantize_grouped(xb, np.array([0, 200, 100, 384], np.int32),
                                                np.ones(3, np.float32))
     assert rc == -6 and (sro == -1).all()
+
+
+def test_nvfp4_f16_equals_bf16_on_shared_values(orc):
+    """NVFP4 on FP16 input decodes the element and nothing else: on values
+    both formats hold exactly (BF16 values inside FP16's normal range) the
+    FP16 and BF16 paths give the same bytes, dense and grouped; FP16 values
+    BF16 cannot hold change the result."""
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal((200, 96)) * np.exp2(rng.uniform(-8, 8, (200, 1))))
+    xb = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+    xh = xb.to(torch.float16)
+    assert torch.equal(xh.float(), xb.float())                 # exact in both
+    bb = xb.view(torch.int16).numpy().view(np.uint16)
+    hb = xh.view(torch.int16).numpy().view(np.uint16)
+    for g in (1.0, 37.5, 448 * 6 / 300.0):
+        c1, s1 = orc.nvfp4_quantize(bb, g)
+        c2, s2 = orc.nvfp4_quantize(hb, g, f16=True)
+        assert np.array_equal(c1, c2) and np.array_equal(s1, s2)
+    off = np.array([0, 70, 70, 200], np.int32)
+    gs = np.array([2.0, 5.0, 0.75], np.float32)
+    r1 = orc.nvfp4_quantize_grouped(bb, off, gs)
+    r2 = orc.nvfp4_quantize_grouped(hb, off, gs, f16=True)
+    assert r1[0] == r2[0] == 0 and all(np.array_equal(a, b) for a, b in zip(r1[1:], r2[1:]))
+    # an FP16 value with more than 8 significant bits changes some code or scale
+    hf = torch.from_numpy(x.astype(np.float32)).to(torch.float16)
+    hf_b = hf.view(torch.int16).numpy().view(np.uint16)
+    c3, _ = orc.nvfp4_quantize(hf_b, 1.0, f16=True)
+    c4, _ = orc.nvfp4_quantize(bb, 1.0)
+    assert not np.array_equal(c3, c4)
