@@ -403,6 +403,12 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     ms = time_launches(lambda i: mx.mxfp4_dequantize_nvfp4(cs_nv[i % R], ss_nv[i % R], g_nv, M, K,
                                                            xs_nv[i % R], stream), 200, stream)
     out["nvfp4_dequantize_4096x7168"] = entry(nb_nv, ms, 1, f"{R} rotating sets")
+    # the NVFP4 quantize of the same activation in FP16
+    for j in range(R):
+        xs_nv[j] = xs_nv[j].to(torch.float16)
+    ms = time_launches(lambda i: mx.mxfp4_quantize_nvfp4_f16(xs_nv[i % R], g_nv, cs_nv[i % R],
+                                                             ss_nv[i % R], stream), 200, stream)
+    out["nvfp4_quantize_f16_4096x7168"] = entry(nb_nv, ms, 1, f"{R} rotating sets")
     del xs_nv, cs_nv, ss_nv
 
     # grouped MoE activations: 16384 tokens x top-8 over 384 experts, K = 7168

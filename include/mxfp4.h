@@ -348,6 +348,14 @@ int mxfp4_quantize_nvfp4_grouped(const void* x, int64_t total_rows, int64_t K,
                                  const int32_t* expert_offsets, int32_t E,
                                  const float* global_scales, uint8_t* codes, uint8_t* scales,
                                  int32_t* scale_row_offsets, int32_t* status, void* stream);
+/* The same experts quant for IEEE binary16 input (x holds FP16 bit patterns;
+ * everything else as mxfp4_quantize_nvfp4_grouped, element step as
+ * mxfp4_quantize_nvfp4_f16). */
+int mxfp4_quantize_nvfp4_grouped_f16(const void* x, int64_t total_rows, int64_t K,
+                                     const int32_t* expert_offsets, int32_t E,
+                                     const float* global_scales, uint8_t* codes,
+                                     uint8_t* scales, int32_t* scale_row_offsets,
+                                     int32_t* status, void* stream);
 
 /* ---------------------------------------------------------------- NVFP4
  * The other branch of the same quantize kernel on [PR43557] ("Implementation
@@ -372,6 +380,14 @@ size_t mxfp4_nvfp4_scale_bytes(int64_t M, int64_t K);
 int mxfp4_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
                          const float* global_scale, uint8_t* codes, uint8_t* scales,
                          void* stream);
+/* mxfp4_quantize_nvfp4_f16 — NVFP4 of IEEE binary16 input ([PR43557]
+ * cvt_warp_fp16_to_fp4 takes either 16-bit type on both branches).  The
+ * block max is a packed half2 max widened to float32 exactly; every later
+ * step is the float32 sequence above.  Arguments, layouts, alignment and
+ * errors exactly as mxfp4_quantize_nvfp4 (x holds FP16 bit patterns). */
+int mxfp4_quantize_nvfp4_f16(const void* x, int64_t M, int64_t K, int64_t ldx,
+                             const float* global_scale, uint8_t* codes, uint8_t* scales,
+                             void* stream);
 int mxfp4_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales,
                            const float* global_scale, int64_t M, int64_t K, void* y,
                            void* stream);

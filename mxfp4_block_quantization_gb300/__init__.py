@@ -38,7 +38,7 @@ __all__ = [
     "MXFP4_ESCRATCH", "MXFP4_NOALLOC_SCRATCH_BYTES", "mxfp4_nvfp4_scale_bytes",
     "mxfp4_quantize_nvfp4", "mxfp4_dequantize_nvfp4", "quantize_nvfp4", "dequantize_nvfp4",
     "mxfp4_nvfp4_grouped_scale_bytes_bound", "mxfp4_quantize_nvfp4_grouped",
-    "quantize_nvfp4_grouped",
+    "quantize_nvfp4_grouped", "mxfp4_quantize_nvfp4_f16", "mxfp4_quantize_nvfp4_grouped_f16",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300.so")
@@ -113,12 +113,14 @@ def _load(path=LIB_PATH):
     L.mxfp4_swap_w13.argtypes = [vp, vp, vp, i32, i64, i64, i32, vp, vp, vp, vp, i64, vp, vp]
     L.mxfp4_nvfp4_scale_bytes.restype = ctypes.c_size_t
     L.mxfp4_nvfp4_scale_bytes.argtypes = [i64, i64]
-    L.mxfp4_quantize_nvfp4.restype = ctypes.c_int
-    L.mxfp4_quantize_nvfp4.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp]
+    for name in ("mxfp4_quantize_nvfp4", "mxfp4_quantize_nvfp4_f16"):
+        getattr(L, name).restype = ctypes.c_int
+        getattr(L, name).argtypes = [vp, i64, i64, i64, vp, vp, vp, vp]
     L.mxfp4_nvfp4_grouped_scale_bytes_bound.restype = ctypes.c_size_t
     L.mxfp4_nvfp4_grouped_scale_bytes_bound.argtypes = [i64, i32, i64]
-    L.mxfp4_quantize_nvfp4_grouped.restype = ctypes.c_int
-    L.mxfp4_quantize_nvfp4_grouped.argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp]
+    for name in ("mxfp4_quantize_nvfp4_grouped", "mxfp4_quantize_nvfp4_grouped_f16"):
+        getattr(L, name).restype = ctypes.c_int
+        getattr(L, name).argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp]
     L.mxfp4_dequantize_nvfp4.restype = ctypes.c_int
     L.mxfp4_dequantize_nvfp4.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     L.mxfp4_status_string.restype = ctypes.c_char_p
@@ -430,10 +432,9 @@ def mxfp4_nvfp4_scale_bytes(M: int, K: int) -> int:
     return int(_lib.mxfp4_nvfp4_scale_bytes(int(M), int(K)))
 
 
-def mxfp4_quantize_nvfp4(x, global_scale, codes, scales, stream=None) -> None:
-    """NVFP4: BF16 ``x`` [M, K] with float32 ``global_scale`` (1 element,
-    device) -> codes [M, K/2] + tiled E4M3 scales."""
-    _need_cuda("x", x, torch.bfloat16)
+def _nvfp4(x, global_scale, codes, scales, stream, f16) -> None:
+    name = "mxfp4_quantize_nvfp4" + ("_f16" if f16 else "")
+    _need_cuda("x", x, torch.float16 if f16 else torch.bfloat16)
     _need_cuda("global_scale", global_scale, torch.float32)
     _need_cuda("codes", codes, torch.uint8)
     _need_cuda("scales", scales, torch.uint8)
@@ -441,20 +442,29 @@ def mxfp4_quantize_nvfp4(x, global_scale, codes, scales, stream=None) -> None:
         raise ValueError("x must be 2-D with unit column stride")
     M, K = x.shape
     with torch.cuda.device(_device_of(x, global_scale, codes, scales)):
-        _check(_lib.mxfp4_quantize_nvfp4(_ptr(x), M, K, x.stride(0), _ptr(global_scale),
-                                         _ptr(codes), _ptr(scales), _stream(stream, x.device)),
-               "mxfp4_quantize_nvfp4")
+        _check(getattr(_lib, name)(_ptr(x), M, K, x.stride(0), _ptr(global_scale), _ptr(codes),
+                                   _ptr(scales), _stream(stream, x.device)), name)
+
+
+def mxfp4_quantize_nvfp4(x, global_scale, codes, scales, stream=None) -> None:
+    """NVFP4: BF16 ``x`` [M, K] with float32 ``global_scale`` (1 element,
+    device) -> codes [M, K/2] + tiled E4M3 scales."""
+    _nvfp4(x, global_scale, codes, scales, stream, False)
+
+
+def mxfp4_quantize_nvfp4_f16(x, global_scale, codes, scales, stream=None) -> None:
+    """NVFP4 of FP16 ``x``; everything else as mxfp4_quantize_nvfp4."""
+    _nvfp4(x, global_scale, codes, scales, stream, True)
 
 
 def mxfp4_nvfp4_grouped_scale_bytes_bound(total_rows: int, E: int, K: int) -> int:
     return int(_lib.mxfp4_nvfp4_grouped_scale_bytes_bound(int(total_rows), int(E), int(K)))
 
 
-def mxfp4_quantize_nvfp4_grouped(x, expert_offsets, global_scales, codes, scales,
-                                 scale_row_offsets, status=None, stream=None) -> None:
-    """NVFP4 experts quant: segment e of the contiguous BF16 ``x`` with global
-    scale ``global_scales[e]`` (float32 device [E])."""
-    _need_cuda("x", x, torch.bfloat16)
+def _nvfp4_grouped(x, expert_offsets, global_scales, codes, scales, scale_row_offsets, status,
+                   stream, f16) -> None:
+    name = "mxfp4_quantize_nvfp4_grouped" + ("_f16" if f16 else "")
+    _need_cuda("x", x, torch.float16 if f16 else torch.bfloat16)
     _need_cuda("expert_offsets", expert_offsets, torch.int32)
     _need_cuda("global_scales", global_scales, torch.float32)
     _need_cuda("codes", codes, torch.uint8)
@@ -469,10 +479,24 @@ def mxfp4_quantize_nvfp4_grouped(x, expert_offsets, global_scales, codes, scales
         raise ValueError("global_scales needs one entry per expert")
     with torch.cuda.device(_device_of(x, expert_offsets, global_scales, codes, scales,
                                       scale_row_offsets, status)):
-        _check(_lib.mxfp4_quantize_nvfp4_grouped(
+        _check(getattr(_lib, name)(
             _ptr(x), total, K, _ptr(expert_offsets), E, _ptr(global_scales), _ptr(codes),
-            _ptr(scales), _ptr(scale_row_offsets), _ptr(status), _stream(stream, x.device)),
-            "mxfp4_quantize_nvfp4_grouped")
+            _ptr(scales), _ptr(scale_row_offsets), _ptr(status), _stream(stream, x.device)), name)
+
+
+def mxfp4_quantize_nvfp4_grouped(x, expert_offsets, global_scales, codes, scales,
+                                 scale_row_offsets, status=None, stream=None) -> None:
+    """NVFP4 experts quant: segment e of the contiguous BF16 ``x`` with global
+    scale ``global_scales[e]`` (float32 device [E])."""
+    _nvfp4_grouped(x, expert_offsets, global_scales, codes, scales, scale_row_offsets, status,
+                   stream, False)
+
+
+def mxfp4_quantize_nvfp4_grouped_f16(x, expert_offsets, global_scales, codes, scales,
+                                     scale_row_offsets, status=None, stream=None) -> None:
+    """NVFP4 experts quant of FP16 ``x``; everything else as the BF16 form."""
+    _nvfp4_grouped(x, expert_offsets, global_scales, codes, scales, scale_row_offsets, status,
+                   stream, True)
 
 
 def mxfp4_dequantize_nvfp4(codes, scales, global_scale, M: int, K: int, y, stream=None) -> None:
@@ -580,17 +604,18 @@ def swap_w13(codes, scales, w13_bias=None, w2_bias=None, scales_tiled=True, stre
 
 
 def quantize_nvfp4(x, global_scale, stream=None):
-    """Returns (codes uint8 [M, K/2], E4M3 scales uint8 [nvfp4_scale_bytes])."""
+    """Returns (codes uint8 [M, K/2], E4M3 scales uint8 [nvfp4_scale_bytes])
+    of BF16 or FP16 ``x``."""
     M, K = x.shape
     codes = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
     scales = torch.empty(mxfp4_nvfp4_scale_bytes(M, K), dtype=torch.uint8, device=x.device)
-    mxfp4_quantize_nvfp4(x, global_scale, codes, scales, stream)
+    _nvfp4(x, global_scale, codes, scales, stream, x.dtype == torch.float16)
     return codes, scales
 
 
 def quantize_nvfp4_grouped(x, expert_offsets, global_scales, stream=None):
     """Returns (codes, scales, scale_row_offsets, status) of the NVFP4 experts
-    quant of the expert-sorted ``x``."""
+    quant of the expert-sorted ``x`` (BF16 or FP16)."""
     total, K = x.shape
     E = expert_offsets.numel() - 1
     dev = x.device
@@ -599,8 +624,8 @@ def quantize_nvfp4_grouped(x, expert_offsets, global_scales, stream=None):
                          dtype=torch.uint8, device=dev)
     sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
     status = torch.empty(1, dtype=torch.int32, device=dev)
-    mxfp4_quantize_nvfp4_grouped(x, expert_offsets, global_scales, codes, scales, sro, status,
-                                 stream)
+    _nvfp4_grouped(x, expert_offsets, global_scales, codes, scales, sro, status, stream,
+                   x.dtype == torch.float16)
     return codes, scales, sro, status
 
 

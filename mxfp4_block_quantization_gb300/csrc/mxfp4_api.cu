@@ -458,9 +458,12 @@ size_t mxfp4_nvfp4_scale_bytes(int64_t M, int64_t K) {
   return static_cast<size_t>(ceil_div(M, 128) * 128 * ceil_div(K / 16, 4) * 4);
 }
 
-int mxfp4_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
-                         const float* global_scale, uint8_t* codes, uint8_t* scales,
-                         void* stream) {
+}  // extern "C"
+
+namespace {
+
+int nvfp4_checked(const void* x, int64_t M, int64_t K, int64_t ldx, const float* global_scale,
+                  uint8_t* codes, uint8_t* scales, bool f16, void* stream) {
   if (M < 0 || K < 0) return MXFP4_EINVAL;
   if (K % 16 != 0 || ldx < K) return MXFP4_ESHAPE;
   if (M == 0 || K == 0) return MXFP4_OK;
@@ -477,8 +480,24 @@ int mxfp4_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
   if (overlap(rx, rc) || overlap(rx, rs) || overlap(rc, rs) || overlap(rg, rc) ||
       overlap(rg, rs))
     return MXFP4_EALIAS;
-  return from_cuda(mxfp4::launch_quantize_nvfp4(x, M, K, ldx, global_scale, codes, scales,
+  return from_cuda(mxfp4::launch_quantize_nvfp4(x, M, K, ldx, global_scale, codes, scales, f16,
                                                 static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxfp4_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
+                         const float* global_scale, uint8_t* codes, uint8_t* scales,
+                         void* stream) {
+  return nvfp4_checked(x, M, K, ldx, global_scale, codes, scales, false, stream);
+}
+
+int mxfp4_quantize_nvfp4_f16(const void* x, int64_t M, int64_t K, int64_t ldx,
+                             const float* global_scale, uint8_t* codes, uint8_t* scales,
+                             void* stream) {
+  return nvfp4_checked(x, M, K, ldx, global_scale, codes, scales, true, stream);
 }
 
 size_t mxfp4_nvfp4_grouped_scale_bytes_bound(int64_t total_rows, int32_t E, int64_t K) {
@@ -487,10 +506,14 @@ size_t mxfp4_nvfp4_grouped_scale_bytes_bound(int64_t total_rows, int32_t E, int6
   return static_cast<size_t>(tiles * 128 * ceil_div(K / 16, 4) * 4);
 }
 
-int mxfp4_quantize_nvfp4_grouped(const void* x, int64_t total_rows, int64_t K,
-                                 const int32_t* expert_offsets, int32_t E,
-                                 const float* global_scales, uint8_t* codes, uint8_t* scales,
-                                 int32_t* scale_row_offsets, int32_t* status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int nvfp4_grouped_checked(const void* x, int64_t total_rows, int64_t K,
+                          const int32_t* expert_offsets, int32_t E, const float* global_scales,
+                          uint8_t* codes, uint8_t* scales, int32_t* scale_row_offsets,
+                          int32_t* status, bool f16, void* stream) {
   if (total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
   if (K % 16 != 0) return MXFP4_ESHAPE;
   if (!expert_offsets || !scale_row_offsets) return MXFP4_EINVAL;
@@ -524,7 +547,28 @@ int mxfp4_quantize_nvfp4_grouped(const void* x, int64_t total_rows, int64_t K,
   }
   return from_cuda(mxfp4::launch_quantize_nvfp4_grouped(
       x, total_rows, K, expert_offsets, E, global_scales, codes, scales, scale_row_offsets,
-      status, K == 0 ? 0 : bound_tiles, static_cast<cudaStream_t>(stream)));
+      status, K == 0 ? 0 : bound_tiles, f16, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxfp4_quantize_nvfp4_grouped(const void* x, int64_t total_rows, int64_t K,
+                                 const int32_t* expert_offsets, int32_t E,
+                                 const float* global_scales, uint8_t* codes, uint8_t* scales,
+                                 int32_t* scale_row_offsets, int32_t* status, void* stream) {
+  return nvfp4_grouped_checked(x, total_rows, K, expert_offsets, E, global_scales, codes, scales,
+                               scale_row_offsets, status, false, stream);
+}
+
+int mxfp4_quantize_nvfp4_grouped_f16(const void* x, int64_t total_rows, int64_t K,
+                                     const int32_t* expert_offsets, int32_t E,
+                                     const float* global_scales, uint8_t* codes,
+                                     uint8_t* scales, int32_t* scale_row_offsets,
+                                     int32_t* status, void* stream) {
+  return nvfp4_grouped_checked(x, total_rows, K, expert_offsets, E, global_scales, codes, scales,
+                               scale_row_offsets, status, true, stream);
 }
 
 int mxfp4_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, const float* global_scale,

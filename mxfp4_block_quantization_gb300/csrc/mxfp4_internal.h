@@ -58,13 +58,13 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
 // NVFP4 (16-element blocks, E4M3 scales, device global scale).
 cudaError_t launch_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
                                   const float* global_scale, uint8_t* codes, uint8_t* scales,
-                                  cudaStream_t stream);
+                                  bool f16, cudaStream_t stream);
 // NVFP4 experts quant: per-segment global scales [E], grouped scale layout.
 cudaError_t launch_quantize_nvfp4_grouped(const void* x, int64_t total_rows, int64_t K,
                                           const int32_t* offsets, int32_t E,
                                           const float* global_scales, uint8_t* codes,
                                           uint8_t* scales, int32_t* scale_row_offsets,
-                                          int32_t* status, int64_t bound_tiles,
+                                          int32_t* status, int64_t bound_tiles, bool f16,
                                           cudaStream_t stream);
 cudaError_t launch_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales,
                                     const float* global_scale, int64_t M, int64_t K, void* y,

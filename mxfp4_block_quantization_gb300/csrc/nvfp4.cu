@@ -57,30 +57,43 @@ enum : int { kDbgXY = 0, kDbgCodes, kDbgScales, kDbgG };
 
 // One lane's 16-element block -> its E4M3 scale byte:
 //   q = vecMax / 6; sf = g * q; byte = E4M3(sf).
+template <bool kF16>
 __device__ __forceinline__ uint32_t nv_scale_byte(const uint4 (&v)[2], float g) {
-  const uint32_t h = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(v[0].x, v[0].y),
-                                                   max_abs_bf16x2(v[0].z, v[0].w)),
-                                    max_abs_bf16x2(max_abs_bf16x2(v[1].x, v[1].y),
-                                                   max_abs_bf16x2(v[1].z, v[1].w))) &
-                     0x7FFF7FFFu;
+  uint32_t h;
+  if constexpr (kF16) {
+    h = max_abs_f16x2(max_abs_f16x2(max_abs_f16x2(v[0].x, v[0].y), max_abs_f16x2(v[0].z, v[0].w)),
+                      max_abs_f16x2(max_abs_f16x2(v[1].x, v[1].y), max_abs_f16x2(v[1].z, v[1].w)));
+  } else {
+    h = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(v[0].x, v[0].y),
+                                      max_abs_bf16x2(v[0].z, v[0].w)),
+                       max_abs_bf16x2(max_abs_bf16x2(v[1].x, v[1].y),
+                                      max_abs_bf16x2(v[1].z, v[1].w)));
+  }
+  h &= 0x7FFF7FFFu;
   const uint32_t m = max(h & 0xFFFFu, h >> 16);
-  const float vmax = __uint_as_float(m << 16);
+  const float vmax = __uint_as_float(kF16 ? f16_bits_to_f32_bits(m) : m << 16);
   const float q = vmax / 6.0f;  // IEEE float32 division (no fast-math)
   return cvt_e4m3_satfinite(g * q);
 }
 
 // The block's 8 code bytes: x * inv rounded to E2M1, inv = g / float(byte);
 // zero codes for byte 0.
+template <bool kF16>
 __device__ __forceinline__ uint2 nv_codes(const uint4 (&v)[2], uint32_t byte, float inv) {
   uint2 code = make_uint2(0u, 0u);
   if (byte != 0u) {
-    code.x = scale_cvt_e2m1x8(v[0], inv);
-    code.y = scale_cvt_e2m1x8(v[1], inv);
+    if constexpr (kF16) {
+      code.x = scale_cvt_e2m1x8_f16(v[0], inv);
+      code.y = scale_cvt_e2m1x8_f16(v[1], inv);
+    } else {
+      code.x = scale_cvt_e2m1x8(v[0], inv);
+      code.y = scale_cvt_e2m1x8(v[1], inv);
+    }
   }
   return code;
 }
 
-template <bool kVec32>
+template <bool kVec32, bool kF16>
 __global__ void __launch_bounds__(kThreads, 5) nvfp4_quantize_kernel(const Nvfp4Params p) {
   __shared__ __align__(16) uint8_t chunk[2][kChunkBytes];
   pdl_wait();
@@ -112,9 +125,9 @@ __global__ void __launch_bounds__(kThreads, 5) nvfp4_quantize_kernel(const Nvfp4
   }
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
-    const uint32_t byte = nv_scale_byte(v[i], g);
+    const uint32_t byte = nv_scale_byte<kF16>(v[i], g);
     chunk[half][lr0 * 16 + i * 4 + cc] = static_cast<uint8_t>(byte);
-    const uint2 code = nv_codes(v[i], byte, byte != 0u ? g / e4m3_to_f32(byte) : 0.0f);
+    const uint2 code = nv_codes<kF16>(v[i], byte, byte != 0u ? g / e4m3_to_f32(byte) : 0.0f);
     if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgCodes, cp + i * cld_pass, 8))
       st_stream_v2(cp + i * cld_pass, code);
   }
@@ -156,7 +169,7 @@ struct Nvfp4GroupedParams {
 #endif
 };
 
-template <bool kVec32>
+template <bool kVec32, bool kF16>
 __global__ void __launch_bounds__(kThreads, 5) nvfp4_quantize_grouped_kernel(const Nvfp4GroupedParams p) {
   __shared__ __align__(16) uint8_t chunk[2][kChunkBytes];
   __shared__ float inv_tab[128];  // g[e] / float(byte), byte = 0 .. 127
@@ -201,9 +214,9 @@ __global__ void __launch_bounds__(kThreads, 5) nvfp4_quantize_grouped_kernel(con
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
-    const uint32_t byte = nv_scale_byte(v[i], g);
+    const uint32_t byte = nv_scale_byte<kF16>(v[i], g);
     chunk[half][lr0 * 16 + i * 4 + cc] = static_cast<uint8_t>(byte);
-    const uint2 code = nv_codes(v[i], byte, inv_tab[byte]);
+    const uint2 code = nv_codes<kF16>(v[i], byte, inv_tab[byte]);
     if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgCodes, cp + i * cld_pass, 8))
       st_stream_v2(cp + i * cld_pass, code);
   }
@@ -297,7 +310,7 @@ Nvfp4Params make_params(int64_t M, int64_t K) {
 
 cudaError_t launch_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t ldx,
                                   const float* global_scale, uint8_t* codes, uint8_t* scales,
-                                  cudaStream_t stream) {
+                                  bool f16, cudaStream_t stream) {
   Nvfp4Params p = make_params(M, K);
   p.x = static_cast<const uint8_t*>(x);
   p.ldx_bytes = ldx * 2;
@@ -312,15 +325,18 @@ cudaError_t launch_quantize_nvfp4(const void* x, int64_t M, int64_t K, int64_t l
   debug_range(p.dbg, kDbgG, global_scale, 4);
 #endif
   const bool v32 = reinterpret_cast<uintptr_t>(x) % 32 == 0 && p.ldx_bytes % 32 == 0;
-  return launch_pdl(v32 ? nvfp4_quantize_kernel<true> : nvfp4_quantize_kernel<false>,
-                    static_cast<unsigned>(grid), kThreads, 0, stream, p);
+  const auto kernel = f16 ? (v32 ? nvfp4_quantize_kernel<true, true>
+                                 : nvfp4_quantize_kernel<false, true>)
+                          : (v32 ? nvfp4_quantize_kernel<true, false>
+                                 : nvfp4_quantize_kernel<false, false>);
+  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
 cudaError_t launch_quantize_nvfp4_grouped(const void* x, int64_t total_rows, int64_t K,
                                           const int32_t* offsets, int32_t E,
                                           const float* global_scales, uint8_t* codes,
                                           uint8_t* scales, int32_t* scale_row_offsets,
-                                          int32_t* status, int64_t bound_tiles,
+                                          int32_t* status, int64_t bound_tiles, bool f16,
                                           cudaStream_t stream) {
   cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
   if (err != cudaSuccess || E == 0 || bound_tiles == 0) return err;
@@ -348,8 +364,11 @@ cudaError_t launch_quantize_nvfp4_grouped(const void* x, int64_t total_rows, int
 #endif
   const int64_t grid = bound_tiles * p.nCT;  // CTAs past the real padded total exit at once
   const bool v32 = reinterpret_cast<uintptr_t>(x) % 32 == 0 && p.ldx_bytes % 32 == 0;
-  return launch_pdl(v32 ? nvfp4_quantize_grouped_kernel<true> : nvfp4_quantize_grouped_kernel<false>,
-                    static_cast<unsigned>(grid), kThreads, 0, stream, p);
+  const auto kernel = f16 ? (v32 ? nvfp4_quantize_grouped_kernel<true, true>
+                                 : nvfp4_quantize_grouped_kernel<false, true>)
+                          : (v32 ? nvfp4_quantize_grouped_kernel<true, false>
+                                 : nvfp4_quantize_grouped_kernel<false, false>);
+  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
 cudaError_t launch_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales,

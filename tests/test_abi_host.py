@@ -241,6 +241,21 @@ def test_nvfp4_grouped_validation(lib):
     assert lib.mxfp4_nvfp4_grouped_scale_bytes_bound(300, 3, 40) == 0
 
 
+def test_nvfp4_f16_forms_share_the_validation(lib):
+    q = lib._lib.mxfp4_quantize_nvfp4_f16
+    assert q(A, 4, 24, 24, 9 * A, 2 * A, 3 * A, None) == lib.MXFP4_ESHAPE
+    assert q(A, 4, 64, 64, None, 2 * A, 3 * A, None) == lib.MXFP4_EINVAL
+    assert q(A + 8, 4, 64, 64, 9 * A, 2 * A, 3 * A, None) == lib.MXFP4_EALIGN
+    assert q(A, 4, 64, 64, 9 * A, A + 64, 3 * A, None) == lib.MXFP4_EALIAS
+    assert q(None, 0, 64, 64, None, None, None, None) == lib.MXFP4_OK
+    f = lib._lib.mxfp4_quantize_nvfp4_grouped_f16
+    assert f(A, 300, 40, 3 * A, 3, 7 * A, 4 * A, 5 * A, 6 * A, None, None) == lib.MXFP4_ESHAPE
+    assert f(A, 300, 64, 3 * A, 3, None, 4 * A, 5 * A, 6 * A, None, None) == lib.MXFP4_EINVAL
+    assert f(A, 300, 64, 3 * A, 3, 7 * A + 2, 4 * A, 5 * A, 6 * A, None,
+             None) == lib.MXFP4_EALIGN
+    assert f(A, 300, 64, 3 * A, 3, 7 * A, A + 64, 5 * A, 6 * A, None, None) == lib.MXFP4_EALIAS
+
+
 def test_f16_grouped_forms_share_the_validation(lib):
     L = lib._lib
     # K % 32 != 0 is refused by every FP16 grouped form, before any launch

@@ -115,10 +115,11 @@ def test_fuzz_grouped_gather_scatter(mx, seed):
 def test_fuzz_nvfp4(mx, seed):
     rng = np.random.default_rng(300 + seed)
     M, K = int(rng.integers(1, 500)), 16 * int(rng.integers(1, 120))
-    x = _place(_random_x(rng, M, K, False), rng)
+    f16 = bool(seed % 2 == 1)
+    x = _place(_random_x(rng, M, K, f16), rng)
     g = float(np.float32(448.0 * 6.0 / np.exp(rng.uniform(-3, 8))))
     c, s = mx.quantize_nvfp4(x, torch.tensor([g], device="cuda"))
-    c_o, s_o = oracle.nvfp4_quantize(_bits(x), g)
+    c_o, s_o = oracle.nvfp4_quantize(_bits(x), g, f16=f16)
     assert np.array_equal(c.cpu().numpy(), c_o) and np.array_equal(s.cpu().numpy(), s_o)
     if M > 1 and x.is_contiguous() and x.data_ptr() % 16 == 0:
         E = int(rng.integers(1, 9))
@@ -126,7 +127,7 @@ def test_fuzz_nvfp4(mx, seed):
         gs = (448.0 * 6.0 / np.exp(rng.uniform(-3, 8, E))).astype(np.float32)
         cg, sg, sro, st = mx.quantize_nvfp4_grouped(x, torch.from_numpy(off).cuda(),
                                                     torch.from_numpy(gs).cuda())
-        rc, cg_o, sg_o, sro_o = oracle.nvfp4_quantize_grouped(_bits(x), off, gs)
+        rc, cg_o, sg_o, sro_o = oracle.nvfp4_quantize_grouped(_bits(x), off, gs, f16=f16)
         torch.cuda.synchronize()
         assert int(st.item()) == rc == 0
         used = int(sro_o[-1]) * ((K // 16 + 3) // 4 * 4)

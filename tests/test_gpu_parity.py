@@ -710,6 +710,89 @@ def test_nvfp4_scale_sweep_every_bf16_max(mx):
     assert_nvfp4_parity(mx, W.from_bits(xb, "cuda"), 1.0)
 
 
+# ----------------------------------------------------- NVFP4, FP16 input
+def run_nvfp4_f16(mx, x, g):
+    M, K = x.shape
+    gs = torch.tensor([g], dtype=torch.float32, device="cuda")
+    codes = Guarded(M * (K // 2), shape=(M, K // 2))
+    scales = Guarded(mx.mxfp4_nvfp4_scale_bytes(M, K))
+    mx.mxfp4_quantize_nvfp4_f16(x, gs, codes.t, scales.t)
+    torch.cuda.synchronize()
+    codes.check()
+    scales.check()
+    return codes.t.cpu().numpy(), scales.t.cpu().numpy()
+
+
+def assert_nvfp4_f16_parity(mx, x, g):
+    c, s = run_nvfp4_f16(mx, x, g)
+    c_o, s_o = oracle.nvfp4_quantize(f16_bits(x), float(np.float32(g)), f16=True)
+    assert np.array_equal(s, s_o), _first_diff(s, s_o)
+    assert np.array_equal(c, c_o), _first_diff(c, c_o)
+
+
+@pytest.mark.parametrize("g", [1.0, 0.37, 2688.0 / 25.0])
+def test_nvfp4_f16_dense(mx, g):
+    x = W.dense_activation(33, 1000, 2880, device="cuda").float()
+    x[::7, ::5] *= 2.0 ** -12                                    # FP16 subnormals too
+    assert_nvfp4_f16_parity(mx, x.to(torch.float16), g)
+
+
+@pytest.mark.parametrize("M,K", [(1, 16), (129, 80), (4096, 7168)])
+def test_nvfp4_f16_ragged_and_full_size(mx, M, K):
+    x = W.dense_activation(34, M, K, device="cuda").to(torch.float16)
+    assert_nvfp4_f16_parity(mx, x, 448.0 * 6.0 / float(x.float().abs().max()))
+    assert_nvfp4_f16_parity(mx, offset16_any(x), 1.0)
+
+
+@pytest.mark.parametrize("g", [1.0, 4096.0])
+def test_nvfp4_f16_scale_sweep_every_f16_max(mx, g):
+    """Each 16-element block takes a different block max: every positive
+    finite FP16 value, subnormals included.  With g = 1 the scales run from
+    zero through E4M3 subnormals to saturation at 448; g = 4096 moves the
+    FP16 subnormal maxima onto normal E4M3 scales."""
+    rng = np.random.default_rng(19)
+    vmax = np.arange(1, 0x7C00, dtype=np.uint16)
+    rest = rng.integers(0, 0x10000, (vmax.size, 15), dtype=np.uint32).astype(np.uint16)
+    rest = np.where((rest & 0x7FFF) <= vmax[:, None], rest, rest & 0x8000 | (vmax[:, None] >> 1))
+    blocks = np.concatenate([vmax[:, None], rest], axis=1)
+    blocks = np.concatenate([blocks, np.zeros(((-blocks.shape[0]) % 16, 16), np.uint16)])
+    hb = blocks.reshape(-1, 256)
+    x = torch.from_numpy(hb.view(np.int16)).view(torch.float16).cuda()
+    assert_nvfp4_f16_parity(mx, x, g)
+
+
+def test_nvfp4_grouped_f16_matches_oracle(mx):
+    g = W.moe_grouped(seed=21, tokens=200, top_k=4, num_experts=12, K=288, device="cuda")
+    gs = _expert_gscales(12, 21)
+    xs = g.x.to(torch.float16)
+    off = g.offsets
+    rc, c_o, s_o, sro_o = oracle.nvfp4_quantize_grouped(f16_bits(xs), off.cpu().numpy(), gs,
+                                                        f16=True)
+    used = int(sro_o[-1]) * ((288 // 16 + 3) // 4 * 4)
+    for xx in (xs, offset16_any(xs)):
+        total, K = xx.shape
+        E = off.numel() - 1
+        codes = Guarded(total * (K // 2), shape=(total, K // 2))
+        scales = Guarded(mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K))
+        sro = Guarded(4 * (E + 1), torch.int32)
+        status = Guarded(4, torch.int32)
+        mx.mxfp4_quantize_nvfp4_grouped_f16(xx, off, torch.from_numpy(gs).cuda(), codes.t,
+                                            scales.t, sro.t, status.t)
+        torch.cuda.synchronize()
+        for t in (codes, scales, sro, status):
+            t.check()
+        assert int(status.t.cpu()[0]) == 0 and rc == 0
+        assert np.array_equal(sro.t.cpu().numpy(), sro_o)
+        c, s = codes.t.cpu().numpy(), scales.t.cpu().numpy()
+        assert np.array_equal(c, c_o), _first_diff(c, c_o)
+        assert np.array_equal(s[:used], s_o[:used]), _first_diff(s[:used], s_o[:used])
+        assert (s[used:] == 0xA5).all(), "slack past P[E] must be untouched"
+    # the high-level call dispatches on dtype
+    c, s, sro, st = mx.quantize_nvfp4_grouped(xs, off, torch.from_numpy(gs).cuda())
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and np.array_equal(c.cpu().numpy(), c_o)
+
+
 # ------------------------------------------------ streams, graphs, 64-bit
 def test_non_default_stream(mx):
     x = W.dense_activation(41, 512, 1024, device="cuda")
