@@ -459,7 +459,8 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     e_["speedup_vs_unfused"] = round(ms_unfused / ms_fused, 3)
     out["grouped_gather_moe_16384tok_top8_E384"] = e_
     # the same gather call through the scatter path (inverse map built in a workspace)
-    ws = torch.empty(mx.mxfp4_gather_workspace_bytes(T, total), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(mx.mxfp4_gather_workspace_bytes(T, total, E, K), dtype=torch.uint8,
+                     device="cuda")
     ms_ws = time_launches(
         lambda i: mx.mxfp4_quantize_grouped_gather_ws(g.x_tokens, g.row_index, g.offsets, ws,
                                                       codes, scales, sro, st, stream), 30, stream)

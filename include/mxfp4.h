@@ -172,15 +172,28 @@ int mxfp4_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K
  * once per row.  [PR43557] "Implementation breakdown" item 3.
  *
  * workspace        DEVICE scratch owned by the caller, 16-byte aligned, at
- *                  least mxfp4_gather_workspace_bytes(num_src_rows, total_rows)
- *                  bytes, not overlapping any other argument; its contents on
- *                  entry do not matter and on return are unspecified.  Two
- *                  calls in flight at once need two workspaces.
+ *                  least mxfp4_gather_workspace_bytes(num_src_rows, total_rows,
+ *                  E, K) bytes, not overlapping any other argument; its
+ *                  contents on entry do not matter and on return are
+ *                  unspecified.  Two calls in flight at once need two
+ *                  workspaces.
  * num_src_rows     <= INT32_MAX / 4.
  * Everything else: as mxfp4_quantize_grouped_gather.  The _f16 form takes
  * IEEE binary16 input.
+ *
+ * mxfp4_gather_workspace_bytes: the inverse map, 4 * (3T + 2 + 2U + R + 2B)
+ * bytes (T = num_src_rows, R = total_rows, U = T + R/32 + 1 units of at most
+ * 32 rows, B = ceil(T / 1024) scan blocks), the source row of every padded
+ * row, 4 * floor((R + 127E) / 128) * 128 bytes, then, from the next 16-byte
+ * boundary, T rows of ceil(K/128) 4-byte scale words, each row padded to a
+ * multiple of 4 words: each source row's scale words are stored there once,
+ * and a second kernel writes the tiled scales of all rows in whole 512-byte
+ * chunks.  0 for negative sizes, K % 32 != 0, num_src_rows > INT32_MAX / 4
+ * or R + 127E > INT32_MAX.  With K = 0 it is the inverse map alone, rounded
+ * up to 16 bytes.
  */
-size_t mxfp4_gather_workspace_bytes(int64_t num_src_rows, int64_t total_rows);
+size_t mxfp4_gather_workspace_bytes(int64_t num_src_rows, int64_t total_rows, int32_t E,
+                                    int64_t K);
 int mxfp4_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
                                      const int32_t* row_index, int64_t total_rows,
                                      const int32_t* expert_offsets, int32_t E, void* workspace,
@@ -202,9 +215,13 @@ int mxfp4_quantize_grouped_gather_ws_f16(const void* x, int64_t num_src_rows, in
  * counterpart exists in the method's sources.
  *
  * Arguments, outputs, status and errors as mxfp4_quantize_grouped_gather, and
- * MXFP4_ESCRATCH (returned before anything is enqueued) when
- * mxfp4_gather_workspace_bytes(num_src_rows, total_rows) exceeds
- * MXFP4_NOALLOC_SCRATCH_BYTES.
+ * MXFP4_ESCRATCH (returned before anything is enqueued) when the inverse map
+ * alone, mxfp4_gather_workspace_bytes(num_src_rows, total_rows, E, 0),
+ * exceeds MXFP4_NOALLOC_SCRATCH_BYTES.  When the whole workspace
+ * (mxfp4_gather_workspace_bytes(num_src_rows, total_rows, E, K)) fits, the
+ * call runs exactly as mxfp4_quantize_grouped_gather_ws; otherwise the
+ * scatter stores every row's scale words into the tiled layout itself (same
+ * results, slower).
  * Every call shares the one buffer of its device: two calls that can overlap
  * on the GPU (different streams, or a graph replayed concurrently) race and
  * give wrong results; serialise them.  The buffer keeps the last call's

@@ -93,7 +93,7 @@ def _load(path=LIB_PATH):
     L.mxfp4_quantize_grouped_scatter_f16.argtypes = [vp, i64, i64, i64, vp, i32, i64, vp, i32,
                                                      vp, vp, vp, vp, vp]
     L.mxfp4_gather_workspace_bytes.restype = ctypes.c_size_t
-    L.mxfp4_gather_workspace_bytes.argtypes = [i64, i64]
+    L.mxfp4_gather_workspace_bytes.argtypes = [i64, i64, i32, i64]
     for name in ("mxfp4_quantize_grouped_gather_ws", "mxfp4_quantize_grouped_gather_ws_f16"):
         getattr(L, name).restype = ctypes.c_int
         getattr(L, name).argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, ctypes.c_size_t,
@@ -282,8 +282,9 @@ def mxfp4_quantize_grouped_gather_f16(x, row_index, expert_offsets, codes, scale
     _gather(x, row_index, expert_offsets, codes, scales, scale_row_offsets, status, stream, True)
 
 
-def mxfp4_gather_workspace_bytes(num_src_rows: int, total_rows: int) -> int:
-    return int(_lib.mxfp4_gather_workspace_bytes(int(num_src_rows), int(total_rows)))
+def mxfp4_gather_workspace_bytes(num_src_rows: int, total_rows: int, E: int, K: int) -> int:
+    return int(_lib.mxfp4_gather_workspace_bytes(int(num_src_rows), int(total_rows), int(E),
+                                                 int(K)))
 
 
 def _gather_ws(x, row_index, expert_offsets, workspace, codes, scales, scale_row_offsets, status,
@@ -554,7 +555,7 @@ def quantize_grouped_gather(x, row_index, expert_offsets, stream=None, via_scatt
     sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
     status = torch.empty(1, dtype=torch.int32, device=dev)
     if via_scatter:
-        ws = torch.empty(max(mxfp4_gather_workspace_bytes(x.shape[0], total), 16),
+        ws = torch.empty(max(mxfp4_gather_workspace_bytes(x.shape[0], total, E, K), 16),
                          dtype=torch.uint8, device=dev)
         _gather_ws(x, row_index, expert_offsets, ws, codes, scales, sro, status, stream, f16)
     else:

@@ -155,11 +155,27 @@ int grouped_checked(const void* x, int64_t total_rows, int64_t K,
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+// How a gather call runs: the per-row gather kernel, or the scatter path with
+// the inverse map in a workspace, its scale words stored straight into the
+// tiled layout (kInverse) or staged per token and tiled by a second kernel
+// (kInverseStaged, the larger workspace).
+enum class GatherPath { kPerRow, kInverse, kInverseStaged };
+
+int64_t gather_ws_bytes(int64_t num_src_rows, int64_t total_rows, int32_t E, int64_t K,
+                        bool staged) {
+  const int64_t map = mxfp4::gather_workspace_ints(num_src_rows, total_rows) +
+                      (staged ? mxfp4::gather_tok_ints(total_rows, E) : 0);
+  return ceil_div(map * 4, 16) * 16 +
+         (staged ? mxfp4::gather_stage_ints(num_src_rows, K) * 4 : 0);
+}
+
 int gather_checked(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
                    const int32_t* row_index, int64_t total_rows, const int32_t* expert_offsets,
                    int32_t E, void* workspace, size_t workspace_bytes, uint8_t* codes,
-                   uint8_t* scales, int32_t* scale_row_offsets, int32_t* status, bool use_ws,
+                   uint8_t* scales, int32_t* scale_row_offsets, int32_t* status, GatherPath path,
                    bool f16, void* stream) {
+  const bool use_ws = path != GatherPath::kPerRow;
+  const bool staged = path == GatherPath::kInverseStaged;
   if (num_src_rows < 0 || total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
   if (K % 32 != 0 || ldx < K) return MXFP4_ESHAPE;
   if (!expert_offsets || !scale_row_offsets) return MXFP4_EINVAL;
@@ -174,7 +190,8 @@ int gather_checked(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
   if (use_ws) {
     // token ids and route counts are int32 on the device
     if (num_src_rows > INT32_MAX / 4) return MXFP4_ESHAPE;
-    ws_bytes = static_cast<int64_t>(mxfp4_gather_workspace_bytes(num_src_rows, total_rows));
+    if (num_src_rows > (INT64_MAX / 8) / (K / 128 + 1)) return MXFP4_ESHAPE;
+    ws_bytes = gather_ws_bytes(num_src_rows, total_rows, E, K, staged);
     if (work && (!workspace || workspace_bytes < static_cast<size_t>(ws_bytes)))
       return MXFP4_EINVAL;
     if (workspace && !aligned16(workspace)) return MXFP4_EALIGN;
@@ -206,7 +223,7 @@ int gather_checked(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
   if (use_ws)
     return from_cuda(mxfp4::launch_quantize_grouped_gather_ws(
         x, work ? num_src_rows : 0, K, ldx, row_index, total_rows, expert_offsets, E,
-        static_cast<int32_t*>(workspace), codes, scales, scale_row_offsets, status,
+        static_cast<int32_t*>(workspace), staged, codes, scales, scale_row_offsets, status,
         K == 0 ? 0 : bound_tiles, f16, st));
   return from_cuda(mxfp4::launch_quantize_grouped_gather(
       x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E, codes, scales,
@@ -296,8 +313,8 @@ int mxfp4_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K
                                   uint8_t* scales, int32_t* scale_row_offsets, int32_t* status,
                                   void* stream) {
   return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E,
-                        nullptr, 0, codes, scales, scale_row_offsets, status, false, false,
-                        stream);
+                        nullptr, 0, codes, scales, scale_row_offsets, status,
+                        GatherPath::kPerRow, false, stream);
 }
 
 int mxfp4_quantize_grouped_gather_f16(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
@@ -306,14 +323,16 @@ int mxfp4_quantize_grouped_gather_f16(const void* x, int64_t num_src_rows, int64
                                       uint8_t* scales, int32_t* scale_row_offsets,
                                       int32_t* status, void* stream) {
   return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E,
-                        nullptr, 0, codes, scales, scale_row_offsets, status, false, true,
-                        stream);
+                        nullptr, 0, codes, scales, scale_row_offsets, status,
+                        GatherPath::kPerRow, true, stream);
 }
 
-size_t mxfp4_gather_workspace_bytes(int64_t num_src_rows, int64_t total_rows) {
-  if (num_src_rows < 0 || total_rows < 0) return 0;
-  return static_cast<size_t>(ceil_div(mxfp4::gather_workspace_ints(num_src_rows, total_rows) * 4,
-                                      16) * 16);
+size_t mxfp4_gather_workspace_bytes(int64_t num_src_rows, int64_t total_rows, int32_t E,
+                                    int64_t K) {
+  if (num_src_rows < 0 || total_rows < 0 || E < 0 || K < 0 || K % 32 != 0) return 0;
+  if (num_src_rows > INT32_MAX / 4 || total_rows + 127 * static_cast<int64_t>(E) > INT32_MAX)
+    return 0;
+  return static_cast<size_t>(gather_ws_bytes(num_src_rows, total_rows, E, K, K > 0));
 }
 
 int mxfp4_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
@@ -323,7 +342,7 @@ int mxfp4_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_
                                      int32_t* scale_row_offsets, int32_t* status, void* stream) {
   return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E,
                         workspace, workspace_bytes, codes, scales, scale_row_offsets, status,
-                        true, false, stream);
+                        GatherPath::kInverseStaged, false, stream);
 }
 
 int mxfp4_quantize_grouped_gather_noalloc(const void* x, int64_t num_src_rows, int64_t K,
@@ -332,14 +351,23 @@ int mxfp4_quantize_grouped_gather_noalloc(const void* x, int64_t num_src_rows, i
                                           int32_t E, uint8_t* codes, uint8_t* scales,
                                           int32_t* scale_row_offsets, int32_t* status,
                                           void* stream) {
-  if (num_src_rows < 0 || total_rows < 0) return MXFP4_EINVAL;
-  if (mxfp4_gather_workspace_bytes(num_src_rows, total_rows) > MXFP4_NOALLOC_SCRATCH_BYTES)
+  if (num_src_rows < 0 || total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
+  if (num_src_rows > INT32_MAX / 4 || total_rows + 127 * static_cast<int64_t>(E) > INT32_MAX)
+    return MXFP4_ESCRATCH;
+  // the staged form when its larger workspace fits in the scratch array
+  const GatherPath path =
+      K % 32 == 0 && gather_ws_bytes(num_src_rows, total_rows, E, K, true) <=
+                         static_cast<int64_t>(MXFP4_NOALLOC_SCRATCH_BYTES)
+          ? GatherPath::kInverseStaged
+          : GatherPath::kInverse;
+  if (gather_ws_bytes(num_src_rows, total_rows, E, K, false) >
+      static_cast<int64_t>(MXFP4_NOALLOC_SCRATCH_BYTES))
     return MXFP4_ESCRATCH;
   int32_t* scratch = mxfp4::noalloc_scratch();
   if (scratch == nullptr) return MXFP4_ECUDA;
   return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E,
                         scratch, MXFP4_NOALLOC_SCRATCH_BYTES, codes, scales, scale_row_offsets,
-                        status, true, false, stream);
+                        status, path, false, stream);
 }
 
 int mxfp4_quantize_grouped_gather_ws_f16(const void* x, int64_t num_src_rows, int64_t K,
@@ -351,7 +379,7 @@ int mxfp4_quantize_grouped_gather_ws_f16(const void* x, int64_t num_src_rows, in
                                          void* stream) {
   return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E,
                         workspace, workspace_bytes, codes, scales, scale_row_offsets, status,
-                        true, true, stream);
+                        GatherPath::kInverseStaged, true, stream);
 }
 
 int mxfp4_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K, int64_t ldx,

@@ -39,15 +39,23 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
                                            int32_t* scale_row_offsets, int32_t* status,
                                            int64_t bound_tiles, bool f16, cudaStream_t stream);
 // The same gather through the scatter path: the inverse map is built in
-// `workspace` (gather_workspace_ints(num_src_rows, total_rows) int32).
+// `workspace` (gather_workspace_ints(num_src_rows, total_rows) int32).  With
+// `staged`, the workspace also holds gather_tok_ints(total_rows, E) int32
+// (the token of every padded row) and, from the next 16-byte boundary,
+// gather_stage_ints(num_src_rows, K) int32: the scatter then stores each
+// token's scale words there once and a tile kernel writes the tiled scales
+// whole; without it the scatter stores every row's scale words into the tiled
+// layout itself.
 int64_t gather_workspace_ints(int64_t num_src_rows, int64_t total_rows);
+int64_t gather_tok_ints(int64_t total_rows, int64_t E);
+int64_t gather_stage_ints(int64_t num_src_rows, int64_t K);
 cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_t K,
                                               int64_t ldx, const int32_t* row_index,
                                               int64_t total_rows, const int32_t* offsets,
-                                              int32_t E, int32_t* workspace, uint8_t* codes,
-                                              uint8_t* scales, int32_t* scale_row_offsets,
-                                              int32_t* status, int64_t bound_tiles, bool f16,
-                                              cudaStream_t stream);
+                                              int32_t E, int32_t* workspace, bool staged,
+                                              uint8_t* codes, uint8_t* scales,
+                                              int32_t* scale_row_offsets, int32_t* status,
+                                              int64_t bound_tiles, bool f16, cudaStream_t stream);
 cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
                                             int64_t ldx, const int32_t* dest_rows, int32_t top_k,
                                             int64_t total_rows, const int32_t* offsets, int32_t E,

@@ -283,12 +283,19 @@ struct ScatterParams {
   const int32_t* __restrict__ offsets;    // [E+1] row offsets of the segments
   const int32_t* __restrict__ padded;     // [E+1] padded row starts
   int32_t* status;                        // may be NULL
+  uint32_t* __restrict__ stage;           // kStaged: [num_tokens, stage_ld(nKT)] scale words
+                                          //   of every token, tiled by tile_scales_kernel
+  int32_t pad_ctas;                       // leading CTAs that zero pad scale rows (E or 0)
   int32_t sK;
   int32_t nKT;
 #ifdef MXFP4_DEBUG_BOUNDS
   DebugRanges dbg;                        // slots as in QuantizeParams (kDbgRowIndex: dest_rows)
 #endif
 };
+
+// Row stride, in 4-byte words, of the staged per-token scale words: nKT
+// rounded up to 16 bytes so that the tile kernel reads them as uint4.
+__host__ __device__ __forceinline__ int64_t stage_ld(int nKT) { return (nKT + 3) & ~3; }
 
 // Byte offset of the scale word (4 scale columns of one k-tile) of padded row
 // `prow` in k-tile 0; k-tile kt adds kt * 512.
@@ -297,8 +304,8 @@ __device__ __forceinline__ int64_t scale_word_base(int prow, int nKT) {
          ((prow & 127) >> 5) * 4;
 }
 
-template <bool kVec32, bool kF16>
-__global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const ScatterParams p) {
+template <bool kVec32, bool kF16, bool kStaged>
+__global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_kernel(const ScatterParams p) {
   __shared__ int64_t s_code[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];   // d * K/2, or -1
   __shared__ int64_t s_scale[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];  // word base, or -1
 
@@ -311,7 +318,7 @@ __global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const Scatte
   const int total_padded = __ldg(p.padded + p.E);
   if (total_padded < 0) return;  // rejected offsets
 
-  if (static_cast<int>(blockIdx.x) < p.E) {
+  if (static_cast<int>(blockIdx.x) < p.pad_ctas) {
     // pad rows [n, ceil128(n)) of expert e: zero scale words, row-fastest
     const int e = blockIdx.x;
     const int n = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
@@ -328,7 +335,7 @@ __global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const Scatte
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t w_id = static_cast<int64_t>(blockIdx.x - p.E) * kScatterWarps + warp;
+  const int64_t w_id = static_cast<int64_t>(blockIdx.x - p.pad_ctas) * kScatterWarps + warp;
   // the token and its routes: a fixed top_k per token (warp = token), or one
   // unit of at most 32 routes of a token (warp = unit)
   int64_t t, rbase;
@@ -357,9 +364,11 @@ __global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const Scatte
     const int32_t* dp = p.dest_rows + rbase + lane;
     const int32_t v = MXFP4_IN_BOUNDS(p, kDbgRowIndex, dp, 4) ? __ldg(dp) : -1;
     if (v >= 0 && v < p.total_rows) {
-      const int e = find_segment(p.offsets, p.E, v, static_cast<int>(p.total_rows));
       co = static_cast<int64_t>(v) * p.code_ld;
-      so = scale_word_base(__ldg(p.padded + e) + (v - __ldg(p.offsets + e)), p.nKT);
+      if constexpr (!kStaged) {
+        const int e = find_segment(p.offsets, p.E, v, static_cast<int>(p.total_rows));
+        so = scale_word_base(__ldg(p.padded + e) + (v - __ldg(p.offsets + e)), p.nKT);
+      }
     } else {
       bad = v != -1;
     }
@@ -398,6 +407,15 @@ __global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const Scatte
     }
     const int64_t cofs = static_cast<int64_t>(p0) * (kScatterPass / 2) + lane * (kElems / 2);
     const int kt0 = p0 * 4 + (lane >> 3);
+    if (kStaged && (lane & 7) == 0) {
+      // the token's words once (every unit of a token stores the same values)
+#pragma unroll
+      for (int b = 0; b < kScatterBatch; ++b) {
+        const int kt = kt0 + 4 * b;
+        uint32_t* const sp = p.stage + t * stage_ld(p.nKT) + kt;
+        if (kt < p.nKT && MXFP4_IN_BOUNDS(p, kDbgWork, sp, 4)) st_keep_u32(sp, word[b], keep);
+      }
+    }
     for (int j = 0; j < nr; ++j) {
       const int64_t c = s_code[warp][j];
       const int64_t w = s_scale[warp][j];
@@ -407,12 +425,99 @@ __global__ void __launch_bounds__(kThreads) quantize_scatter_kernel(const Scatte
         uint8_t* const cp = p.codes + c + cofs + b * (kScatterPass / 2);
         if (c >= 0 && pass * 16 + (lane >> 1) < p.sK && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 8))
           st_stream_v2(cp, code[b]);
-        const int kt = kt0 + 4 * b;
-        uint8_t* const wp = p.scales + w + static_cast<int64_t>(kt) * kChunkBytes;
-        if (w >= 0 && (lane & 7) == 0 && kt < p.nKT && MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4))
-          st_keep_u32(wp, word[b], keep);
+        if constexpr (!kStaged) {
+          const int kt = kt0 + 4 * b;
+          uint8_t* const wp = p.scales + w + static_cast<int64_t>(kt) * kChunkBytes;
+          if (w >= 0 && (lane & 7) == 0 && kt < p.nKT && MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4))
+            st_keep_u32(wp, word[b], keep);
+        }
       }
     }
+  }
+}
+
+// Tiled scales of the gathered batch from the staged per-token words: one CTA
+// per padded 128-row tile.  Padded row pr takes the words of token
+// tok1[pr] - 1 (written by invert_count_kernel for row o[e] + pr - P[e] of
+// segment e); pad rows and rows whose index is out of range keep tok1 = 0 and
+// get zero words.  The tile's 128 x nKT words pass through shared memory (64
+// k-tiles at a time) so that every 512-byte chunk is written whole, 16 bytes
+// per thread, instead of 4-byte words scattered over the chunks.
+struct TileScalesParams {
+  const int32_t* __restrict__ tok1;       // [grid * 128] token + 1 of every padded row, 0: none
+  const uint32_t* __restrict__ stage;     // [T, stage_ld(nKT)], 16-byte aligned
+  uint8_t* __restrict__ scales;
+  const int32_t* __restrict__ padded;
+  int32_t E;
+  int32_t nKT;
+#ifdef MXFP4_DEBUG_BOUNDS
+  DebugRanges dbg;  // kDbgScales, kDbgPadded, kDbgRowIndex (tok1), kDbgWork (stage)
+#endif
+};
+
+constexpr int kTileCols = 64;  // k-tiles per shared-memory pass
+constexpr int kTileQuads = kTileRows * (kTileCols / 4) / kThreads;  // uint4 loads per thread
+static_assert(kThreads == 16 * 16 && kTileQuads * 16 == kTileRows,
+              "tile_scales_kernel: 16 quads x 16 rows per step, kTileQuads steps");
+
+__global__ void __launch_bounds__(kThreads) tile_scales_kernel(const TileScalesParams p) {
+  __shared__ uint32_t s_w[kTileRows][kTileCols + 1];  // odd stride: conflict-free columns
+  __shared__ int32_t s_tok[kTileRows];
+
+  pdl_wait();
+  pdl_release();
+
+  if (!MXFP4_IN_BOUNDS(p, kDbgPadded, p.padded + p.E, 4)) return;
+  const int pr0 = static_cast<int>(blockIdx.x) * kTileRows;
+  // both loads in flight together: the tile's tokens and the padded total
+  int32_t t1 = 0;
+  if (threadIdx.x < kTileRows) {
+    const int32_t* tp = p.tok1 + pr0 + threadIdx.x;
+    if (MXFP4_IN_BOUNDS(p, kDbgRowIndex, tp, 4)) t1 = __ldg(tp);
+  }
+  const int total_padded = __ldg(p.padded + p.E);
+  if (total_padded < 0 || pr0 >= total_padded) return;  // whole CTA: nothing past P[E]
+  if (threadIdx.x < kTileRows) s_tok[threadIdx.x] = t1 - 1;
+  __syncthreads();
+
+  uint8_t* const tile = p.scales + static_cast<int64_t>(blockIdx.x) * p.nKT * kChunkBytes;
+  const int64_t ld = stage_ld(p.nKT);
+  const int qd = threadIdx.x & 15;  // this thread's 16-byte quad of a row: words 4qd .. 4qd+3
+  const int rb = threadIdx.x >> 4;  // and its rows rb, rb + 16, ...
+  for (int c0 = 0; c0 < p.nKT; c0 += kTileCols) {
+    const int cw = p.nKT - c0 < kTileCols ? p.nKT - c0 : kTileCols;
+    const bool in_row = 4 * qd < cw;
+    // every load of the pass in flight before the first shared-memory store
+    uint4 v[kTileQuads];
+#pragma unroll
+    for (int j = 0; j < kTileQuads; ++j) {
+      const int32_t t = s_tok[rb + 16 * j];
+      v[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (t >= 0 && in_row) {
+        const uint32_t* sp = p.stage + static_cast<int64_t>(t) * ld + c0 + 4 * qd;
+        if (MXFP4_IN_BOUNDS(p, kDbgWork, sp, 16)) v[j] = __ldg(reinterpret_cast<const uint4*>(sp));
+      }
+    }
+    if (in_row) {
+#pragma unroll
+      for (int j = 0; j < kTileQuads; ++j) {
+        uint32_t* const w = &s_w[rb + 16 * j][4 * qd];  // words past cw are never read
+        w[0] = v[j].x;
+        w[1] = v[j].y;
+        w[2] = v[j].z;
+        w[3] = v[j].w;
+      }
+    }
+    __syncthreads();
+    // piece (c, o): rows o, o+32, o+64, o+96 of k-tile c0 + c, bytes o*16 of its chunk
+    for (int i = threadIdx.x; i < cw * 32; i += kThreads) {
+      const int c = i >> 5;
+      const int o = i & 31;
+      uint8_t* const dp = tile + static_cast<int64_t>(c0 + c) * kChunkBytes + o * 16;
+      if (MXFP4_IN_BOUNDS(p, kDbgScales, dp, 16))
+        st_stream_v4(dp, make_uint4(s_w[o][c], s_w[o + 32][c], s_w[o + 64][c], s_w[o + 96][c]));
+    }
+    __syncthreads();
   }
 }
 
@@ -435,6 +540,8 @@ struct InvertParams {
   int32_t* __restrict__ unit_first;       // [U]
   int32_t* __restrict__ rows;             // [R] rows grouped by token
   int32_t* __restrict__ block_sums;       // [2 * ceil(T / kScanThreads)] routes, units per block
+  int32_t* __restrict__ tok1;             // or NULL; else [padded rows], zero on entry: token + 1
+                                          //   of every padded row with a valid index
   uint8_t* __restrict__ codes;            // rows with an index out of range are
   uint8_t* __restrict__ scales;           //   zeroed here, codes and scale bytes
   int64_t code_ld;
@@ -470,6 +577,12 @@ __global__ void __launch_bounds__(kInvertThreads) invert_count_kernel(const Inve
     const int32_t t = MXFP4_IN_BOUNDS(q, kDbgRowIndex, ip, 4) ? __ldg(ip) : -1;
     if (t >= 0 && t < q.num_src_rows) {
       if (MXFP4_IN_BOUNDS(q, kDbgWork, q.count + t, 4)) atomicAdd(q.count + t, 1);
+      if (q.tok1 != nullptr) {
+        const int e =
+            find_segment(q.offsets, q.E, static_cast<int>(r), static_cast<int>(q.total_rows));
+        int32_t* const tp = q.tok1 + __ldg(q.padded + e) + (static_cast<int>(r) - __ldg(q.offsets + e));
+        if (MXFP4_IN_BOUNDS(q, kDbgWork, tp, 4)) *tp = t + 1;
+      }
       continue;
     }
     bad = true;
@@ -830,6 +943,8 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
   p.scales = scales;
   p.sK = static_cast<int32_t>(K / kBlock);
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
+  p.stage = nullptr;
+  p.pad_ctas = E;
   p.offsets = offsets;
   p.padded = scale_row_offsets;
   p.E = E;
@@ -848,10 +963,10 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
 #endif
   const int64_t grid = E + (num_tokens + kScatterWarps - 1) / kScatterWarps;
   const bool v32 = vec32_ok(x, p.ldx_bytes);
-  const auto kernel = f16 ? (v32 ? quantize_scatter_kernel<true, true>
-                                 : quantize_scatter_kernel<false, true>)
-                          : (v32 ? quantize_scatter_kernel<true, false>
-                                 : quantize_scatter_kernel<false, false>);
+  const auto kernel = f16 ? (v32 ? quantize_scatter_kernel<true, true, false>
+                                 : quantize_scatter_kernel<false, true, false>)
+                          : (v32 ? quantize_scatter_kernel<true, false, false>
+                                 : quantize_scatter_kernel<false, false, false>);
   return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
@@ -861,13 +976,21 @@ int64_t gather_workspace_ints(int64_t num_src_rows, int64_t total_rows) {
   return 3 * num_src_rows + 2 + 2 * units + total_rows + 2 * (blocks > 0 ? blocks : 1);
 }
 
+int64_t gather_tok_ints(int64_t total_rows, int64_t E) {
+  return (total_rows + 127 * E) / kTileRows * kTileRows;
+}
+
+int64_t gather_stage_ints(int64_t num_src_rows, int64_t K) {
+  return num_src_rows * stage_ld(static_cast<int>((K / kBlock + kTileBlocks - 1) / kTileBlocks));
+}
+
 cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_t K,
                                               int64_t ldx, const int32_t* row_index,
                                               int64_t total_rows, const int32_t* offsets,
-                                              int32_t E, int32_t* workspace, uint8_t* codes,
-                                              uint8_t* scales, int32_t* scale_row_offsets,
-                                              int32_t* status, int64_t bound_tiles, bool f16,
-                                              cudaStream_t stream) {
+                                              int32_t E, int32_t* workspace, bool staged,
+                                              uint8_t* codes, uint8_t* scales,
+                                              int32_t* scale_row_offsets, int32_t* status,
+                                              int64_t bound_tiles, bool f16, cudaStream_t stream) {
   cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
   if (err != cudaSuccess || E == 0 || K == 0) return err;
   const int64_t T = num_src_rows;
@@ -876,8 +999,11 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   q.row_index = row_index;
   q.total_rows = total_rows;
   q.num_src_rows = T;
+  // staged: [count T][tok1 PT] cleared by one memset, then the map, then the words
+  const int64_t PT = staged ? gather_tok_ints(total_rows, E) : 0;
   q.count = workspace;
-  q.start = q.count + T;
+  q.tok1 = staged ? workspace + T : nullptr;
+  q.start = q.count + T + PT;
   q.chunk_start = q.start + (T + 1);
   q.unit_token = q.chunk_start + (T + 1);
   q.unit_first = q.unit_token + units;
@@ -891,7 +1017,9 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   q.E = E;
   q.nKT = (static_cast<int32_t>(K / kBlock) + kTileBlocks - 1) / kTileBlocks;
   q.status = status;
-  const int64_t ws_bytes = gather_workspace_ints(T, total_rows) * 4;
+  // the staged words start at the first 16-byte boundary after the inverse map
+  const int64_t map_ints = (gather_workspace_ints(T, total_rows) + PT + 3) & ~int64_t{3};
+  const int64_t ws_bytes = (map_ints + (staged ? gather_stage_ints(T, K) : 0)) * 4;
 #ifdef MXFP4_DEBUG_BOUNDS
   debug_range(q.dbg, kDbgCodes, codes, total_rows * (K / 2));
   debug_range(q.dbg, kDbgScales, scales, bound_tiles * q.nKT * kChunkBytes);
@@ -901,8 +1029,8 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   debug_range(q.dbg, kDbgStatus, status, status ? 4 : 0);
   debug_range(q.dbg, kDbgWork, workspace, ws_bytes);
 #endif
-  if (T > 0) {
-    err = cudaMemsetAsync(q.count, 0, static_cast<size_t>(T) * 4, stream);
+  if (T + PT > 0) {
+    err = cudaMemsetAsync(q.count, 0, static_cast<size_t>(T + PT) * 4, stream);
     if (err != cudaSuccess) return err;
   }
   const int64_t row_ctas_max = static_cast<int64_t>(sm_count()) * 8;
@@ -938,6 +1066,8 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   p.offsets = offsets;
   p.padded = scale_row_offsets;
   p.status = status;
+  p.stage = staged ? reinterpret_cast<uint32_t*>(workspace + map_ints) : nullptr;
+  p.pad_ctas = staged ? 0 : E;
   p.sK = static_cast<int32_t>(K / kBlock);
   p.nKT = q.nKT;
 #ifdef MXFP4_DEBUG_BOUNDS
@@ -952,13 +1082,32 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
 #else
   (void)ws_bytes;
 #endif
-  const int64_t grid = E + (units + kScatterWarps - 1) / kScatterWarps;
+  const int64_t grid = p.pad_ctas + (units + kScatterWarps - 1) / kScatterWarps;
   const bool v32 = vec32_ok(x, p.ldx_bytes);
-  const auto kernel = f16 ? (v32 ? quantize_scatter_kernel<true, true>
-                                 : quantize_scatter_kernel<false, true>)
-                          : (v32 ? quantize_scatter_kernel<true, false>
-                                 : quantize_scatter_kernel<false, false>);
-  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
+  using Kernel = void (*)(const ScatterParams);
+  static constexpr Kernel kKernels[2][2][2] = {
+      {{quantize_scatter_kernel<false, false, false>, quantize_scatter_kernel<false, false, true>},
+       {quantize_scatter_kernel<false, true, false>, quantize_scatter_kernel<false, true, true>}},
+      {{quantize_scatter_kernel<true, false, false>, quantize_scatter_kernel<true, false, true>},
+       {quantize_scatter_kernel<true, true, false>, quantize_scatter_kernel<true, true, true>}}};
+  err = launch_pdl(kKernels[v32][f16][staged], static_cast<unsigned>(grid), kThreads, 0, stream,
+                   p);
+  if (err != cudaSuccess || !staged || bound_tiles == 0) return err;
+  TileScalesParams ts{};
+  ts.tok1 = q.tok1;
+  ts.stage = p.stage;
+  ts.scales = scales;
+  ts.padded = scale_row_offsets;
+  ts.E = E;
+  ts.nKT = q.nKT;
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(ts.dbg, kDbgScales, scales, bound_tiles * ts.nKT * kChunkBytes);
+  debug_range(ts.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(ts.dbg, kDbgRowIndex, q.tok1, PT * 4);
+  debug_range(ts.dbg, kDbgWork, p.stage, T * stage_ld(ts.nKT) * 4);
+#endif
+  return launch_pdl(tile_scales_kernel, static_cast<unsigned>(bound_tiles), kThreads, 0, stream,
+                    ts);
 }
 
 #ifdef MXFP4_DEBUG_BOUNDS

@@ -271,8 +271,19 @@ def test_f16_grouped_forms_share_the_validation(lib):
 
 def test_gather_ws_validation(lib):
     f = lib._lib.mxfp4_quantize_grouped_gather_ws
-    ws_need = lib.mxfp4_gather_workspace_bytes(50, 10)
-    assert ws_need % 16 == 0 and ws_need >= 4 * (3 * 50 + 2 + 2 * (50 + 10 // 32 + 1) + 10)
+    ws_need = lib.mxfp4_gather_workspace_bytes(50, 10, 2, 64)
+    # inverse map 4 * (3T + 2 + 2U + R + 2B), U = T + R/32 + 1, B = 1; the token of each of
+    # the floor((R + 127E)/128)*128 padded rows; then, from the next 16-byte boundary, T rows
+    # of ceil(K/128) scale words padded to 4 words
+    inv = 4 * (3 * 50 + 2 + 2 * (50 + 10 // 32 + 1) + 10 + 2)
+    tok = 4 * ((10 + 127 * 2) // 128 * 128)
+    assert inv == 1064 and tok == 1024 and ws_need == 2096 + 50 * 4 * 4
+    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 0) == 1072     # the map alone, rounded
+    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 7168) == 2096 + 50 * 56 * 4
+    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 160) == 2096 + 50 * 4 * 4  # 2 words -> 4
+    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 48) == 0
+    assert lib.mxfp4_gather_workspace_bytes(50, 10, -1, 64) == 0
+    assert lib.mxfp4_gather_workspace_bytes(-1, 10, 2, 64) == 0
     # x, n_src, K, ldx, idx, total, off, E, ws, ws_bytes, codes, scales, sro, status, stream
     ok = [A, 50, 64, 64, 2 * A, 10, 3 * A, 2, 8 * A, ws_need, 4 * A, 5 * A, 6 * A, None, None]
 
@@ -296,7 +307,7 @@ def test_noalloc_gather_rejects_oversized_scratch(lib):
     """Sizes whose inverse map would not fit the library's fixed scratch are
     refused with MXFP4_ESCRATCH before any device work (no GPU needed)."""
     f = lib._lib.mxfp4_quantize_grouped_gather_noalloc
-    assert lib.mxfp4_gather_workspace_bytes(10_000_000, 1) > lib.MXFP4_NOALLOC_SCRATCH_BYTES
+    assert lib.mxfp4_gather_workspace_bytes(10_000_000, 1, 1, 0) > lib.MXFP4_NOALLOC_SCRATCH_BYTES
     rc = f(A, 10_000_000, 64, 64, 2 * A, 1, 3 * A, 1, 4 * A, 5 * A, 6 * A, None, None)
     assert rc == lib.MXFP4_ESCRATCH
     assert "MXFP4_ESCRATCH" in lib.mxfp4_status_string(rc)

@@ -1074,7 +1074,7 @@ def run_gather_ws(mx, x, row_index, offsets, f16=False):
     scales = Guarded(mx.mxfp4_grouped_scale_bytes_bound(total, E, K))
     sro = Guarded(4 * (E + 1), torch.int32)
     status = Guarded(4, torch.int32)
-    ws = Guarded(mx.mxfp4_gather_workspace_bytes(x.shape[0], total))
+    ws = Guarded(mx.mxfp4_gather_workspace_bytes(x.shape[0], total, E, K))
     ws.t.fill_(0x5A)                                  # contents on entry must not matter
     fn = mx.mxfp4_quantize_grouped_gather_ws_f16 if f16 else mx.mxfp4_quantize_grouped_gather_ws
     fn(x, row_index, offsets, ws.t, codes.t, scales.t, sro.t, status.t)

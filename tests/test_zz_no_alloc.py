@@ -35,12 +35,16 @@ def test_noalloc_gather_two_calls_match_the_gather_entry_point():
     assert torch.cuda.is_available()
     import mxfp4_block_quantization_gb300 as mx
     L = mx._lib
-    for seed, tokens, top_k, E, K in ((21, 300, 4, 11, 288), (22, 2048, 8, 64, 1024)):
+    # the last case's staged scale words do not fit the scratch: the call then
+    # stores the tiled scale words from the scatter kernel itself
+    for seed, tokens, top_k, E, K in ((21, 300, 4, 11, 288), (22, 2048, 8, 64, 1024),
+                                      (23, 16384, 4, 32, 7168)):
         g = W.moe_grouped(seed=seed, tokens=tokens, top_k=top_k, num_experts=E, K=K,
                           device="cuda")
         total = g.row_index.numel()
-        need = mx.mxfp4_gather_workspace_bytes(tokens, total)
-        assert need <= mx.MXFP4_NOALLOC_SCRATCH_BYTES
+        scratch = mx.MXFP4_NOALLOC_SCRATCH_BYTES
+        assert (mx.mxfp4_gather_workspace_bytes(tokens, total, E, K) <= scratch) == (tokens < 16384)
+        assert mx.mxfp4_gather_workspace_bytes(tokens, total, E, 0) <= scratch
         ref = _outputs(mx, total, K, E)
         assert _call(L.mxfp4_quantize_grouped_gather, g.x_tokens, g.row_index, g.offsets,
                      ref) == mx.MXFP4_OK
