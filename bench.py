@@ -464,8 +464,9 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     ms_ws = time_launches(
         lambda i: mx.mxfp4_quantize_grouped_gather_ws(g.x_tokens, g.row_index, g.offsets, ws,
                                                       codes, scales, sro, st, stream), 30, stream)
-    e_ = entry(nb, ms_ws, 6, "same call and bytes as the gather row; offsets, workspace memset, "
-               "3 inverse-map kernels, then the scatter kernel reads each token row once")
+    e_ = entry(nb, ms_ws, 4, "same call and bytes as the gather row; offsets kernel, workspace "
+               "memset, bucket map kernel, scatter kernel (each token row read once, its scale "
+               "words staged once), tile kernel (tiled scales in whole chunks)")
     e_["speedup_vs_unfused"] = round(ms_unfused / ms_ws, 3)
     e_["speedup_vs_per_row_gather"] = round(ms_fused / ms_ws, 3)
     out["grouped_gather_ws_moe_16384tok_top8_E384"] = e_

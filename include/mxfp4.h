@@ -169,7 +169,8 @@ int mxfp4_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K
  * through the scatter path: from row_index the library builds its inverse
  * (the rows of every source row) in `workspace`, then reads and quantizes
  * every source row once and writes it to all its rows, instead of reading it
- * once per row.  [PR43557] "Implementation breakdown" item 3.
+ * once per row (a source row with more than 32 rows is read once more for
+ * each row past its 32nd).  [PR43557] "Implementation breakdown" item 3.
  *
  * workspace        DEVICE scratch owned by the caller, 16-byte aligned, at
  *                  least mxfp4_gather_workspace_bytes(num_src_rows, total_rows,
@@ -181,10 +182,11 @@ int mxfp4_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K
  * Everything else: as mxfp4_quantize_grouped_gather.  The _f16 form takes
  * IEEE binary16 input.
  *
- * mxfp4_gather_workspace_bytes: the inverse map, 4 * (3T + 2 + 2U + R + 2B)
- * bytes (T = num_src_rows, R = total_rows, U = T + R/32 + 1 units of at most
- * 32 rows, B = ceil(T / 1024) scan blocks), the source row of every padded
- * row, 4 * floor((R + 127E) / 128) * 128 bytes, then, from the next 16-byte
+ * mxfp4_gather_workspace_bytes: the inverse map, 4 * (33T + 1 + 2R) bytes
+ * (T = num_src_rows, R = total_rows: a route count and a 32-row bucket per
+ * source row, an overflow list of rows past a source row's 32nd), the source
+ * row of every padded row, 4 * floor((R + 127E) / 128) * 128 bytes, then,
+ * from the next 16-byte
  * boundary, T rows of ceil(K/128) 4-byte scale words, each row padded to a
  * multiple of 4 words: each source row's scale words are stored there once,
  * and a second kernel writes the tiled scales of all rows in whole 512-byte

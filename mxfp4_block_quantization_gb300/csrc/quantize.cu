@@ -269,11 +269,14 @@ struct ScatterParams {
   const uint8_t* __restrict__ x;          // BF16 token rows
   int64_t ldx_bytes;                      // token row stride in bytes
   int64_t num_tokens;
-  const int32_t* __restrict__ dest_rows;  // [num_tokens, top_k] row of every route, -1 = none
-  const int32_t* __restrict__ unit_token;  // or NULL; else warp u takes unit u: token
-  const int32_t* __restrict__ unit_first;  // unit_token[u], routes dest_rows[unit_first[u] ..
-  const int32_t* __restrict__ route_end;   // min(+32, route_end[token])), u < *n_units
-  const int32_t* __restrict__ n_units;
+  const int32_t* __restrict__ dest_rows;  // token-major: [num_tokens, top_k] row of every route,
+                                          //   -1 = none; bucket mode: [num_tokens, kBucket]
+  const int32_t* __restrict__ count;      // NULL: token-major; else bucket mode: warp t < T
+                                          //   takes rows dest_rows[t*kBucket ..] of count[t]
+  const int32_t* __restrict__ ovf_n;      //   (at most kBucket), warps past T walk the
+  const int32_t* __restrict__ ovf_row;    //   overflow list: ovf_row[j] of token ovf_tok[j],
+  const int32_t* __restrict__ ovf_tok;    //   j < *ovf_n, n_ovf_warps warps in all
+  int32_t n_ovf_warps;
   int32_t top_k;
   int32_t E;
   int64_t total_rows;                     // rows of the expert-sorted batch
@@ -304,64 +307,17 @@ __device__ __forceinline__ int64_t scale_word_base(int prow, int nKT) {
          ((prow & 127) >> 5) * 4;
 }
 
+// One warp: token row t, quantized once, to the nr (<= 32) rows dsts[0..nr).
 template <bool kVec32, bool kF16, bool kStaged>
-__global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_kernel(const ScatterParams p) {
-  __shared__ int64_t s_code[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];   // d * K/2, or -1
-  __shared__ int64_t s_scale[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];  // word base, or -1
-
-  pdl_wait();
-  pdl_release();
-
-  if (!MXFP4_IN_BOUNDS(p, kDbgPadded, p.padded, (p.E + 1) * 4) ||
-      !MXFP4_IN_BOUNDS(p, kDbgOffsets, p.offsets, (p.E + 1) * 4))
-    return;
-  const int total_padded = __ldg(p.padded + p.E);
-  if (total_padded < 0) return;  // rejected offsets
-
-  if (static_cast<int>(blockIdx.x) < p.pad_ctas) {
-    // pad rows [n, ceil128(n)) of expert e: zero scale words, row-fastest
-    const int e = blockIdx.x;
-    const int n = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
-    const int npad = ((n + kTileRows - 1) / kTileRows) * kTileRows - n;
-    const int P0 = __ldg(p.padded + e) + n;
-    const uint64_t keep = l2_evict_last_policy();
-    for (int i = threadIdx.x; i < npad * p.nKT; i += kThreads) {
-      const int kt = i / npad;
-      uint8_t* wp = p.scales + scale_word_base(P0 + (i - kt * npad), p.nKT) + kt * kChunkBytes;
-      if (MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4)) st_keep_u32(wp, 0u, keep);
-    }
-    return;
-  }
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t w_id = static_cast<int64_t>(blockIdx.x - p.pad_ctas) * kScatterWarps + warp;
-  // the token and its routes: a fixed top_k per token (warp = token), or one
-  // unit of at most 32 routes of a token (warp = unit)
-  int64_t t, rbase;
-  int nr;
-  if (p.unit_token == nullptr) {
-    if (w_id >= p.num_tokens) return;  // whole warp; no block-wide barrier below
-    t = w_id;
-    rbase = t * p.top_k;
-    nr = p.top_k;
-  } else {
-    if (!MXFP4_IN_BOUNDS(p, kDbgWork, p.n_units, 4) || w_id >= __ldg(p.n_units)) return;
-    if (!MXFP4_IN_BOUNDS(p, kDbgWork, p.unit_token + w_id, 4) ||
-        !MXFP4_IN_BOUNDS(p, kDbgWork, p.unit_first + w_id, 4))
-      return;
-    t = __ldg(p.unit_token + w_id);
-    rbase = __ldg(p.unit_first + w_id);
-    if (!MXFP4_IN_BOUNDS(p, kDbgWork, p.route_end + t, 4)) return;
-    const int left = __ldg(p.route_end + t) - static_cast<int>(rbase);
-    nr = left < 32 ? left : 32;
-  }
-
+__device__ __forceinline__ void scatter_token(const ScatterParams& p, int64_t t,
+                                              const int32_t* dsts, int nr, int warp, int lane,
+                                              int64_t (*s_code)[MXFP4_SCATTER_MAX_TOP_K],
+                                              int64_t (*s_scale)[MXFP4_SCATTER_MAX_TOP_K]) {
   // routes, one per lane
   int64_t co = -1, so = -1;
   bool bad = false;
   if (lane < nr) {
-    const int32_t* dp = p.dest_rows + rbase + lane;
+    const int32_t* dp = dsts + lane;
     const int32_t v = MXFP4_IN_BOUNDS(p, kDbgRowIndex, dp, 4) ? __ldg(dp) : -1;
     if (v >= 0 && v < p.total_rows) {
       co = static_cast<int64_t>(v) * p.code_ld;
@@ -377,7 +333,8 @@ __global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_ke
       MXFP4_IN_BOUNDS(p, kDbgStatus, p.status, 4))
     atomicExch(p.status, MXFP4_EINDEX);
   s_code[warp][lane] = co;
-  s_scale[warp][lane] = so;
+  // staged: no per-route scale words; slot 0 holds the token's stage row instead
+  s_scale[warp][lane] = kStaged ? reinterpret_cast<int64_t>(p.stage + t * stage_ld(p.nKT)) : so;
   __syncwarp();
 
   const uint8_t* xrow = p.x + t * p.ldx_bytes + lane * (kElems * 2);
@@ -408,11 +365,12 @@ __global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_ke
     const int64_t cofs = static_cast<int64_t>(p0) * (kScatterPass / 2) + lane * (kElems / 2);
     const int kt0 = p0 * 4 + (lane >> 3);
     if (kStaged && (lane & 7) == 0) {
-      // the token's words once (every unit of a token stores the same values)
+      // the token's words once (every warp of a token stores the same values)
+      uint32_t* const srow = reinterpret_cast<uint32_t*>(s_scale[warp][0]);
 #pragma unroll
       for (int b = 0; b < kScatterBatch; ++b) {
         const int kt = kt0 + 4 * b;
-        uint32_t* const sp = p.stage + t * stage_ld(p.nKT) + kt;
+        uint32_t* const sp = srow + kt;
         if (kt < p.nKT && MXFP4_IN_BOUNDS(p, kDbgWork, sp, 4)) st_keep_u32(sp, word[b], keep);
       }
     }
@@ -434,11 +392,93 @@ __global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_ke
       }
     }
   }
+  __syncwarp();  // s_code / s_scale are rewritten by the warp's next token
+}
+
+// Overflow entry j (bucket mode): its token and row; false past the list.
+__device__ __forceinline__ bool overflow_entry(const ScatterParams& p, int64_t j, int64_t& t,
+                                               const int32_t*& dsts) {
+  if (!MXFP4_IN_BOUNDS(p, kDbgWork, p.ovf_n, 4)) return false;
+  const int64_t n = __ldg(p.ovf_n);
+  if (j >= n || j >= p.total_rows || !MXFP4_IN_BOUNDS(p, kDbgWork, p.ovf_tok + j, 4))
+    return false;
+  t = __ldg(p.ovf_tok + j);
+  dsts = p.ovf_row + j;
+  return true;
+}
+
+template <bool kVec32, bool kF16, bool kStaged>
+__global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_kernel(const ScatterParams p) {
+  __shared__ int64_t s_code[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];   // d * K/2, or -1
+  __shared__ int64_t s_scale[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];  // word base, or -1
+  __shared__ int64_t s_next[kScatterWarps];  // overflow warps: their current entry
+
+  pdl_wait();
+  pdl_release();
+
+  if (!MXFP4_IN_BOUNDS(p, kDbgPadded, p.padded, (p.E + 1) * 4) ||
+      !MXFP4_IN_BOUNDS(p, kDbgOffsets, p.offsets, (p.E + 1) * 4))
+    return;
+  const int total_padded = __ldg(p.padded + p.E);
+  if (total_padded < 0) return;  // rejected offsets
+
+  if (static_cast<int>(blockIdx.x) < p.pad_ctas) {
+    // pad rows [n, ceil128(n)) of expert e: zero scale words, row-fastest
+    const int e = blockIdx.x;
+    const int n = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+    const int npad = ((n + kTileRows - 1) / kTileRows) * kTileRows - n;
+    const int P0 = __ldg(p.padded + e) + n;
+    const uint64_t keep = l2_evict_last_policy();
+    for (int i = threadIdx.x; i < npad * p.nKT; i += kThreads) {
+      const int kt = i / npad;
+      uint8_t* wp = p.scales + scale_word_base(P0 + (i - kt * npad), p.nKT) + kt * kChunkBytes;
+      if (MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4)) st_keep_u32(wp, 0u, keep);
+    }
+    return;
+  }
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t w_id = static_cast<int64_t>(blockIdx.x - p.pad_ctas) * kScatterWarps + warp;
+  // whole warps return below; there is no block-wide barrier after this point
+  int64_t t;
+  const int32_t* dsts;
+  int nr;
+  if (p.count == nullptr) {  // token-major: warp = token, top_k routes
+    if (w_id >= p.num_tokens) return;
+    t = w_id;
+    dsts = p.dest_rows + w_id * p.top_k;
+    nr = p.top_k;
+  } else if (w_id < p.num_tokens) {  // bucket mode: the token's first kBucket rows
+    if (!MXFP4_IN_BOUNDS(p, kDbgWork, p.count + w_id, 4)) return;
+    const int c = __ldg(p.count + w_id);
+    if (c <= 0) return;
+    t = w_id;
+    dsts = p.dest_rows + w_id * MXFP4_SCATTER_MAX_TOP_K;
+    nr = c < MXFP4_SCATTER_MAX_TOP_K ? c : MXFP4_SCATTER_MAX_TOP_K;
+  } else {  // bucket mode: the overflow list, one row per entry, warp-strided
+    const int64_t j = w_id - p.num_tokens;
+    if (!overflow_entry(p, j, t, dsts)) return;
+    s_next[warp] = j;
+    nr = 1;
+  }
+  for (;;) {
+    scatter_token<kVec32, kF16, kStaged>(p, t, dsts, nr, warp, lane, s_code, s_scale);
+    // only overflow warps go on; their cursor is kept in shared memory so that
+    // nothing stays live across the body above
+    if (p.count == nullptr ||
+        static_cast<int64_t>(blockIdx.x - p.pad_ctas) * kScatterWarps + warp < p.num_tokens)
+      return;
+    const int64_t j = s_next[warp] + p.n_ovf_warps;
+    if (!overflow_entry(p, j, t, dsts)) return;
+    __syncwarp();
+    s_next[warp] = j;
+  }
 }
 
 // Tiled scales of the gathered batch from the staged per-token words: one CTA
 // per padded 128-row tile.  Padded row pr takes the words of token
-// tok1[pr] - 1 (written by invert_count_kernel for row o[e] + pr - P[e] of
+// tok1[pr] - 1 (written by invert_bucket_kernel for row o[e] + pr - P[e] of
 // segment e); pad rows and rows whose index is out of range keep tok1 = 0 and
 // get zero words.  The tile's 128 x nKT words pass through shared memory (64
 // k-tiles at a time) so that every 512-byte chunk is written whole, 16 bytes
@@ -522,28 +562,29 @@ __global__ void __launch_bounds__(kThreads) tile_scales_kernel(const TileScalesP
 }
 
 // ---------------------------------------------------------------------
-// The fused gather through the scatter path.  From the row -> token map,
-// four small kernels build its inverse in a caller-provided workspace: the
-// routes of every token (rows[start[t] .. start[t+1])), cut into units of at
-// most 32 routes (unit_token[u], unit_first[u], u < chunk_start[T]); the
-// scatter kernel then reads and quantizes every token row once per unit.
-// The route order within a token is arbitrary (atomics) and does not matter:
+// The fused gather through the scatter path.  One kernel builds the inverse
+// of the row -> token map in a caller-provided workspace: every valid row r of
+// token t takes slot atomicAdd(count[t], 1) of the token's bucket of
+// kBucket rows, or, past kBucket routes, an entry of one overflow list.  The
+// scatter kernel then reads and quantizes every token row once for the rows
+// in its bucket (one warp per token) and once more per overflow entry.  The
+// order of the rows in a bucket is arbitrary (atomics) and does not matter:
 // every route of a token receives the same bytes.
+constexpr int kBucket = MXFP4_SCATTER_MAX_TOP_K;  // rows per token bucket (one warp)
+
 struct InvertParams {
   const int32_t* __restrict__ row_index;  // [R] token of every row
   int64_t total_rows;                     // R
   int64_t num_src_rows;                   // T
-  int32_t* __restrict__ count;            // [T], zero on entry
-  int32_t* __restrict__ start;            // [T+1] route ranges
-  int32_t* __restrict__ chunk_start;      // [T+1] unit ranges; chunk_start[T] = units
-  int32_t* __restrict__ unit_token;       // [U]
-  int32_t* __restrict__ unit_first;       // [U]
-  int32_t* __restrict__ rows;             // [R] rows grouped by token
-  int32_t* __restrict__ block_sums;       // [2 * ceil(T / kScanThreads)] routes, units per block
+  int32_t* __restrict__ count;            // [T], zero on entry: routes of every token
+  int32_t* __restrict__ ovf_n;            // [1], zero on entry: overflow entries
+  int32_t* __restrict__ bucket;           // [T, kBucket] the first kBucket rows of every token
+  int32_t* __restrict__ ovf_row;          // [R] rows past their token's kBucket-th
+  int32_t* __restrict__ ovf_tok;          // [R] and their tokens
   int32_t* __restrict__ tok1;             // or NULL; else [padded rows], zero on entry: token + 1
                                           //   of every padded row with a valid index
-  uint8_t* __restrict__ codes;            // rows with an index out of range are
-  uint8_t* __restrict__ scales;           //   zeroed here, codes and scale bytes
+  uint8_t* __restrict__ codes;            // rows with an index out of range are zeroed
+  uint8_t* __restrict__ scales;           //   here: codes, and scale words unless tok1
   int64_t code_ld;
   const int32_t* __restrict__ offsets;
   const int32_t* __restrict__ padded;
@@ -557,32 +598,38 @@ struct InvertParams {
 
 constexpr int kInvertThreads = 256;
 
-__device__ __forceinline__ bool invert_offsets_ok(const InvertParams& q) {
-  if (!MXFP4_IN_BOUNDS(q, kDbgPadded, q.padded, (q.E + 1) * 4) ||
-      !MXFP4_IN_BOUNDS(q, kDbgOffsets, q.offsets, (q.E + 1) * 4))
-    return false;
-  return __ldg(q.padded + q.E) >= 0;  // rejected offsets: nothing is written
-}
-
-// Routes per token; a row whose index is out of range becomes a zero row.
-__global__ void __launch_bounds__(kInvertThreads) invert_count_kernel(const InvertParams q) {
+__global__ void __launch_bounds__(kInvertThreads) invert_bucket_kernel(const InvertParams q) {
   pdl_wait();
   pdl_release();
-  if (!invert_offsets_ok(q)) return;
+  if (!MXFP4_IN_BOUNDS(q, kDbgPadded, q.padded, (q.E + 1) * 4) ||
+      !MXFP4_IN_BOUNDS(q, kDbgOffsets, q.offsets, (q.E + 1) * 4) || __ldg(q.padded + q.E) < 0)
+    return;  // rejected offsets: nothing is written
   bool bad = false;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kInvertThreads;
   for (int64_t r = static_cast<int64_t>(blockIdx.x) * kInvertThreads + threadIdx.x;
        r < q.total_rows; r += stride) {
     const int32_t* ip = q.row_index + r;
     const int32_t t = MXFP4_IN_BOUNDS(q, kDbgRowIndex, ip, 4) ? __ldg(ip) : -1;
-    if (t >= 0 && t < q.num_src_rows) {
-      if (MXFP4_IN_BOUNDS(q, kDbgWork, q.count + t, 4)) atomicAdd(q.count + t, 1);
-      if (q.tok1 != nullptr) {
-        const int e =
-            find_segment(q.offsets, q.E, static_cast<int>(r), static_cast<int>(q.total_rows));
-        int32_t* const tp = q.tok1 + __ldg(q.padded + e) + (static_cast<int>(r) - __ldg(q.offsets + e));
-        if (MXFP4_IN_BOUNDS(q, kDbgWork, tp, 4)) *tp = t + 1;
+    const bool valid = t >= 0 && t < q.num_src_rows;
+    if (valid && MXFP4_IN_BOUNDS(q, kDbgWork, q.count + t, 4)) {
+      const int32_t pos = atomicAdd(q.count + t, 1);
+      if (pos < kBucket) {
+        int32_t* const bp = q.bucket + static_cast<int64_t>(t) * kBucket + pos;
+        if (MXFP4_IN_BOUNDS(q, kDbgWork, bp, 4)) *bp = static_cast<int32_t>(r);
+      } else if (MXFP4_IN_BOUNDS(q, kDbgWork, q.ovf_n, 4)) {
+        const int32_t j = atomicAdd(q.ovf_n, 1);  // < R: each row adds at most once
+        if (MXFP4_IN_BOUNDS(q, kDbgWork, q.ovf_row + j, 4) &&
+            MXFP4_IN_BOUNDS(q, kDbgWork, q.ovf_tok + j, 4)) {
+          q.ovf_row[j] = static_cast<int32_t>(r);
+          q.ovf_tok[j] = t;
+        }
       }
+    }
+    if (valid && q.tok1 == nullptr) continue;
+    const int e = find_segment(q.offsets, q.E, static_cast<int>(r), static_cast<int>(q.total_rows));
+    const int prow = __ldg(q.padded + e) + (static_cast<int>(r) - __ldg(q.offsets + e));
+    if (valid) {
+      if (MXFP4_IN_BOUNDS(q, kDbgWork, q.tok1 + prow, 4)) q.tok1[prow] = t + 1;
       continue;
     }
     bad = true;
@@ -590,9 +637,8 @@ __global__ void __launch_bounds__(kInvertThreads) invert_count_kernel(const Inve
     for (int64_t i = 0; i < q.code_ld; i += 16)
       if (MXFP4_IN_BOUNDS(q, kDbgCodes, cp + i, 16))
         *reinterpret_cast<uint4*>(cp + i) = make_uint4(0u, 0u, 0u, 0u);
-    const int e = find_segment(q.offsets, q.E, static_cast<int>(r), static_cast<int>(q.total_rows));
-    const int64_t base =
-        scale_word_base(__ldg(q.padded + e) + (static_cast<int>(r) - __ldg(q.offsets + e)), q.nKT);
+    if (q.tok1 != nullptr) continue;  // the tile kernel writes its zero scale words
+    const int64_t base = scale_word_base(prow, q.nKT);
     for (int kt = 0; kt < q.nKT; ++kt) {
       uint8_t* wp = q.scales + base + static_cast<int64_t>(kt) * kChunkBytes;
       if (MXFP4_IN_BOUNDS(q, kDbgScales, wp, 4)) *reinterpret_cast<uint32_t*>(wp) = 0u;
@@ -600,125 +646,6 @@ __global__ void __launch_bounds__(kInvertThreads) invert_count_kernel(const Inve
   }
   if (bad && q.status != nullptr && MXFP4_IN_BOUNDS(q, kDbgStatus, q.status, 4))
     atomicExch(q.status, MXFP4_EINDEX);
-}
-
-// Block-wide inclusive scan of two values (routes, units) over kScanThreads
-// threads; returns the exclusive prefixes and leaves the block totals in
-// s_tot[0..1].
-__device__ __forceinline__ void block_scan2(int32_t n, int32_t nu, int32_t& ex_n, int32_t& ex_u,
-                                            int32_t (*s_warp)[kScanThreads / 32],
-                                            int32_t* s_tot) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int32_t inc0 = n, inc1 = nu;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int32_t a0 = __shfl_up_sync(0xFFFFFFFFu, inc0, d);
-    const int32_t a1 = __shfl_up_sync(0xFFFFFFFFu, inc1, d);
-    if (lane >= d) { inc0 += a0; inc1 += a1; }
-  }
-  if (lane == 31) { s_warp[0][warp] = inc0; s_warp[1][warp] = inc1; }
-  __syncthreads();
-  if (warp < 2) {
-    int32_t w = s_warp[warp][lane];
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int32_t a = __shfl_up_sync(0xFFFFFFFFu, w, d);
-      if (lane >= d) w += a;
-    }
-    s_warp[warp][lane] = w;  // inclusive over warps
-    if (lane == 31) s_tot[warp] = w;
-  }
-  __syncthreads();
-  ex_n = (warp > 0 ? s_warp[0][warp - 1] : 0) + inc0 - n;
-  ex_u = (warp > 0 ? s_warp[1][warp - 1] : 0) + inc1 - nu;
-}
-
-__device__ __forceinline__ int32_t route_count(const InvertParams& q, int64_t t) {
-  if (t >= q.num_src_rows || !MXFP4_IN_BOUNDS(q, kDbgWork, q.count + t, 4)) return 0;
-  return q.count[t];
-}
-
-// Per block of kScanThreads tokens: its total routes and units.
-__global__ void __launch_bounds__(kScanThreads) invert_block_sum_kernel(const InvertParams q) {
-  __shared__ int32_t s_warp[2][kScanThreads / 32];
-  __shared__ int32_t s_tot[2];
-  pdl_wait();
-  pdl_release();
-  if (!invert_offsets_ok(q)) return;
-  const int32_t n = route_count(q, static_cast<int64_t>(blockIdx.x) * kScanThreads + threadIdx.x);
-  int32_t ex_n, ex_u;
-  block_scan2(n, (n + 31) / 32, ex_n, ex_u, s_warp, s_tot);
-  if (threadIdx.x == 0 && MXFP4_IN_BOUNDS(q, kDbgWork, q.block_sums + 2 * blockIdx.x, 8)) {
-    q.block_sums[2 * blockIdx.x] = s_tot[0];
-    q.block_sums[2 * blockIdx.x + 1] = s_tot[1];
-  }
-}
-
-// Per block of tokens: the sums of the blocks before it, then its own scan:
-// start[t], chunk_start[t] and the units of its tokens; the last block also
-// writes start[T] and chunk_start[T] (the totals).
-__global__ void __launch_bounds__(kScanThreads) invert_scan_kernel(const InvertParams q) {
-  __shared__ int32_t s_warp[2][kScanThreads / 32];
-  __shared__ int32_t s_tot[2];
-  __shared__ int32_t s_base[2];
-  pdl_wait();
-  pdl_release();
-  if (!invert_offsets_ok(q)) return;
-  const int tid = threadIdx.x;
-  // the blocks before this one: a strided sum, then a block reduction
-  int32_t pn = 0, pu = 0;
-  for (int b = tid; b < static_cast<int>(blockIdx.x); b += kScanThreads)
-    if (MXFP4_IN_BOUNDS(q, kDbgWork, q.block_sums + 2 * b, 8)) {
-      pn += q.block_sums[2 * b];
-      pu += q.block_sums[2 * b + 1];
-    }
-  int32_t dummy_n, dummy_u;
-  block_scan2(pn, pu, dummy_n, dummy_u, s_warp, s_tot);
-  if (tid == 0) { s_base[0] = s_tot[0]; s_base[1] = s_tot[1]; }
-  __syncthreads();
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kScanThreads + tid;
-  const int32_t n = route_count(q, t);
-  const int32_t nu = (n + 31) / 32;
-  int32_t ex_n, ex_u;
-  block_scan2(n, nu, ex_n, ex_u, s_warp, s_tot);
-  const int32_t st = s_base[0] + ex_n;
-  const int32_t cs = s_base[1] + ex_u;
-  if (t < q.num_src_rows) {
-    if (MXFP4_IN_BOUNDS(q, kDbgWork, q.start + t, 4)) q.start[t] = st;
-    if (MXFP4_IN_BOUNDS(q, kDbgWork, q.chunk_start + t, 4)) q.chunk_start[t] = cs;
-    for (int32_t c = 0; c < nu; ++c) {
-      if (MXFP4_IN_BOUNDS(q, kDbgWork, q.unit_token + cs + c, 4) &&
-          MXFP4_IN_BOUNDS(q, kDbgWork, q.unit_first + cs + c, 4)) {
-        q.unit_token[cs + c] = static_cast<int32_t>(t);
-        q.unit_first[cs + c] = st + 32 * c;
-      }
-    }
-  }
-  if (blockIdx.x == gridDim.x - 1 && tid == 0) {
-    const int64_t T = q.num_src_rows;
-    if (MXFP4_IN_BOUNDS(q, kDbgWork, q.start + T, 4)) q.start[T] = s_base[0] + s_tot[0];
-    if (MXFP4_IN_BOUNDS(q, kDbgWork, q.chunk_start + T, 4))
-      q.chunk_start[T] = s_base[1] + s_tot[1];
-  }
-}
-
-// Every valid row into its token's route range (count returns to zero).
-__global__ void __launch_bounds__(kInvertThreads) invert_fill_kernel(const InvertParams q) {
-  pdl_wait();
-  pdl_release();
-  if (!invert_offsets_ok(q)) return;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kInvertThreads;
-  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kInvertThreads + threadIdx.x;
-       r < q.total_rows; r += stride) {
-    const int32_t* ip = q.row_index + r;
-    const int32_t t = MXFP4_IN_BOUNDS(q, kDbgRowIndex, ip, 4) ? __ldg(ip) : -1;
-    if (t < 0 || t >= q.num_src_rows) continue;
-    if (!MXFP4_IN_BOUNDS(q, kDbgWork, q.count + t, 4) ||
-        !MXFP4_IN_BOUNDS(q, kDbgWork, q.start + t, 4))
-      continue;
-    const int32_t pos = q.start[t] + atomicSub(q.count + t, 1) - 1;
-    if (MXFP4_IN_BOUNDS(q, kDbgWork, q.rows + pos, 4)) q.rows[pos] = static_cast<int32_t>(r);
-  }
 }
 
 // Validates 0 = o[0] <= o[1] <= ... <= o[E] = total_rows and writes the
@@ -970,10 +897,12 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
   return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
 }
 
+// Workspace of the gather through the scatter path, in int32:
+//   [count T][ovf_n 1][tok1 PT, staged only]  cleared by one memset
+//   [bucket T x kBucket][ovf_row R][ovf_tok R]
+//   [stage T x stage_ld(nKT), staged only]    from the next 16-byte boundary
 int64_t gather_workspace_ints(int64_t num_src_rows, int64_t total_rows) {
-  const int64_t units = num_src_rows + total_rows / 32 + 1;
-  const int64_t blocks = (num_src_rows + kScanThreads - 1) / kScanThreads;
-  return 3 * num_src_rows + 2 + 2 * units + total_rows + 2 * (blocks > 0 ? blocks : 1);
+  return num_src_rows * (1 + kBucket) + 1 + 2 * total_rows;
 }
 
 int64_t gather_tok_ints(int64_t total_rows, int64_t E) {
@@ -992,23 +921,22 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
                                               int32_t* scale_row_offsets, int32_t* status,
                                               int64_t bound_tiles, bool f16, cudaStream_t stream) {
   cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
-  if (err != cudaSuccess || E == 0 || K == 0) return err;
+  // no rows: every segment is empty and nothing else is written (the caller
+  // need not pass a workspace then)
+  if (err != cudaSuccess || E == 0 || K == 0 || total_rows == 0) return err;
   const int64_t T = num_src_rows;
-  const int64_t units = T + total_rows / 32 + 1;
+  const int64_t R = total_rows;
+  const int64_t PT = staged ? gather_tok_ints(R, E) : 0;
   InvertParams q{};
   q.row_index = row_index;
-  q.total_rows = total_rows;
+  q.total_rows = R;
   q.num_src_rows = T;
-  // staged: [count T][tok1 PT] cleared by one memset, then the map, then the words
-  const int64_t PT = staged ? gather_tok_ints(total_rows, E) : 0;
   q.count = workspace;
-  q.tok1 = staged ? workspace + T : nullptr;
-  q.start = q.count + T + PT;
-  q.chunk_start = q.start + (T + 1);
-  q.unit_token = q.chunk_start + (T + 1);
-  q.unit_first = q.unit_token + units;
-  q.rows = q.unit_first + units;
-  q.block_sums = q.rows + total_rows;
+  q.ovf_n = workspace + T;
+  q.tok1 = staged ? workspace + T + 1 : nullptr;
+  q.bucket = workspace + T + 1 + PT;
+  q.ovf_row = q.bucket + T * kBucket;
+  q.ovf_tok = q.ovf_row + R;
   q.codes = codes;
   q.scales = scales;
   q.code_ld = K / 2;
@@ -1017,49 +945,38 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   q.E = E;
   q.nKT = (static_cast<int32_t>(K / kBlock) + kTileBlocks - 1) / kTileBlocks;
   q.status = status;
-  // the staged words start at the first 16-byte boundary after the inverse map
-  const int64_t map_ints = (gather_workspace_ints(T, total_rows) + PT + 3) & ~int64_t{3};
+  const int64_t map_ints = (gather_workspace_ints(T, R) + PT + 3) & ~int64_t{3};
   const int64_t ws_bytes = (map_ints + (staged ? gather_stage_ints(T, K) : 0)) * 4;
 #ifdef MXFP4_DEBUG_BOUNDS
-  debug_range(q.dbg, kDbgCodes, codes, total_rows * (K / 2));
+  debug_range(q.dbg, kDbgCodes, codes, R * (K / 2));
   debug_range(q.dbg, kDbgScales, scales, bound_tiles * q.nKT * kChunkBytes);
   debug_range(q.dbg, kDbgOffsets, offsets, (static_cast<int64_t>(E) + 1) * 4);
   debug_range(q.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
-  debug_range(q.dbg, kDbgRowIndex, row_index, total_rows * 4);
+  debug_range(q.dbg, kDbgRowIndex, row_index, R * 4);
   debug_range(q.dbg, kDbgStatus, status, status ? 4 : 0);
   debug_range(q.dbg, kDbgWork, workspace, ws_bytes);
 #endif
-  if (T + PT > 0) {
-    err = cudaMemsetAsync(q.count, 0, static_cast<size_t>(T + PT) * 4, stream);
-    if (err != cudaSuccess) return err;
-  }
+  err = cudaMemsetAsync(workspace, 0, static_cast<size_t>(T + 1 + PT) * 4, stream);
+  if (err != cudaSuccess) return err;
   const int64_t row_ctas_max = static_cast<int64_t>(sm_count()) * 8;
-  const int64_t need = (total_rows + kInvertThreads - 1) / kInvertThreads;
-  const unsigned row_ctas = static_cast<unsigned>(need < 1 ? 1 : (need < row_ctas_max ? need : row_ctas_max));
-  if ((err = launch_pdl(invert_count_kernel, row_ctas, kInvertThreads, 0, stream, q)) != cudaSuccess)
-    return err;
-  const unsigned scan_blocks =
-      static_cast<unsigned>(T > 0 ? (T + kScanThreads - 1) / kScanThreads : 1);
-  if ((err = launch_pdl(invert_block_sum_kernel, scan_blocks, kScanThreads, 0, stream, q)) !=
+  const int64_t need = (R + kInvertThreads - 1) / kInvertThreads;
+  const unsigned row_ctas =
+      static_cast<unsigned>(need < 1 ? 1 : (need < row_ctas_max ? need : row_ctas_max));
+  if ((err = launch_pdl(invert_bucket_kernel, row_ctas, kInvertThreads, 0, stream, q)) !=
       cudaSuccess)
-    return err;
-  if ((err = launch_pdl(invert_scan_kernel, scan_blocks, kScanThreads, 0, stream, q)) !=
-      cudaSuccess)
-    return err;
-  if ((err = launch_pdl(invert_fill_kernel, row_ctas, kInvertThreads, 0, stream, q)) != cudaSuccess)
     return err;
   ScatterParams p{};
   p.x = static_cast<const uint8_t*>(x);
   p.ldx_bytes = ldx * 2;
   p.num_tokens = T;
-  p.dest_rows = q.rows;
-  p.unit_token = q.unit_token;
-  p.unit_first = q.unit_first;
-  p.route_end = q.start + 1;
-  p.n_units = q.chunk_start + T;
+  p.dest_rows = q.bucket;
+  p.count = q.count;
+  p.ovf_n = q.ovf_n;
+  p.ovf_row = q.ovf_row;
+  p.ovf_tok = q.ovf_tok;
   p.top_k = 0;
   p.E = E;
-  p.total_rows = total_rows;
+  p.total_rows = R;
   p.code_ld = K / 2;
   p.codes = codes;
   p.scales = scales;
@@ -1070,19 +987,25 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   p.pad_ctas = staged ? 0 : E;
   p.sK = static_cast<int32_t>(K / kBlock);
   p.nKT = q.nKT;
+  // one warp per token, then up to one CTA per SM of warps for the overflow
+  // list (the token CTAs' spare warps walk it too)
+  const int64_t token_ctas = (T + kScatterWarps - 1) / kScatterWarps;
+  const int64_t ovf_need = (R + kScatterWarps - 1) / kScatterWarps;
+  const int64_t ovf_ctas = ovf_need < sm_count() ? ovf_need : sm_count();
+  p.n_ovf_warps = static_cast<int32_t>((token_ctas + ovf_ctas) * kScatterWarps - T);
 #ifdef MXFP4_DEBUG_BOUNDS
   debug_range(p.dbg, kDbgX, x, T > 0 ? ((T - 1) * ldx + K) * 2 : 0);
-  debug_range(p.dbg, kDbgCodes, codes, total_rows * (K / 2));
+  debug_range(p.dbg, kDbgCodes, codes, R * (K / 2));
   debug_range(p.dbg, kDbgScales, scales, bound_tiles * p.nKT * kChunkBytes);
   debug_range(p.dbg, kDbgOffsets, offsets, (static_cast<int64_t>(E) + 1) * 4);
   debug_range(p.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
-  debug_range(p.dbg, kDbgRowIndex, q.rows, total_rows * 4);
+  debug_range(p.dbg, kDbgRowIndex, q.bucket, (T * kBucket + R) * 4);  // buckets + ovf_row
   debug_range(p.dbg, kDbgStatus, status, status ? 4 : 0);
   debug_range(p.dbg, kDbgWork, workspace, ws_bytes);
 #else
   (void)ws_bytes;
 #endif
-  const int64_t grid = p.pad_ctas + (units + kScatterWarps - 1) / kScatterWarps;
+  const int64_t grid = p.pad_ctas + token_ctas + ovf_ctas;
   const bool v32 = vec32_ok(x, p.ldx_bytes);
   using Kernel = void (*)(const ScatterParams);
   static constexpr Kernel kKernels[2][2][2] = {

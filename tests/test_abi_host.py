@@ -272,15 +272,15 @@ def test_f16_grouped_forms_share_the_validation(lib):
 def test_gather_ws_validation(lib):
     f = lib._lib.mxfp4_quantize_grouped_gather_ws
     ws_need = lib.mxfp4_gather_workspace_bytes(50, 10, 2, 64)
-    # inverse map 4 * (3T + 2 + 2U + R + 2B), U = T + R/32 + 1, B = 1; the token of each of
-    # the floor((R + 127E)/128)*128 padded rows; then, from the next 16-byte boundary, T rows
-    # of ceil(K/128) scale words padded to 4 words
-    inv = 4 * (3 * 50 + 2 + 2 * (50 + 10 // 32 + 1) + 10 + 2)
+    # inverse map 4 * (33T + 1 + 2R): counts, overflow counter, 32-row buckets, overflow
+    # rows and tokens; the token of each of the floor((R + 127E)/128)*128 padded rows; then,
+    # from the next 16-byte boundary, T rows of ceil(K/128) scale words padded to 4 words
+    inv = 4 * (33 * 50 + 1 + 2 * 10)
     tok = 4 * ((10 + 127 * 2) // 128 * 128)
-    assert inv == 1064 and tok == 1024 and ws_need == 2096 + 50 * 4 * 4
-    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 0) == 1072     # the map alone, rounded
-    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 7168) == 2096 + 50 * 56 * 4
-    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 160) == 2096 + 50 * 4 * 4  # 2 words -> 4
+    assert inv == 6684 and tok == 1024 and ws_need == 7712 + 50 * 4 * 4
+    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 0) == 6688     # the map alone, rounded
+    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 7168) == 7712 + 50 * 56 * 4
+    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 160) == 7712 + 50 * 4 * 4  # 2 words -> 4
     assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 48) == 0
     assert lib.mxfp4_gather_workspace_bytes(50, 10, -1, 64) == 0
     assert lib.mxfp4_gather_workspace_bytes(-1, 10, 2, 64) == 0

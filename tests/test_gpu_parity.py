@@ -1109,8 +1109,8 @@ def test_gather_ws_small_strided_and_aligned(mx):
 
 
 def test_gather_ws_bad_index_heavy_and_unused_tokens(mx):
-    """Out-of-range indices give zero rows; one token taken by 70 rows (three
-    units of up to 32 routes); most tokens taken by none."""
+    """Out-of-range indices give zero rows; one token taken by 70 rows (32 in
+    its bucket, 38 on the overflow list); most tokens taken by none."""
     xt = W.small_matrix(3, 40, 64).cuda()
     rng = np.random.default_rng(9)
     idx = rng.integers(0, 5, 300).astype(np.int32)     # only tokens 0..4 are used
@@ -1121,6 +1121,17 @@ def test_gather_ws_bad_index_heavy_and_unused_tokens(mx):
     assert got[3] == mx.MXFP4_EINDEX
     _gather_oracle_check(got, bits(xt), idx, off, 64)
     assert not got[0][[5, 17, 250]].any()
+
+
+def test_gather_ws_long_overflow_list(mx):
+    """5000 rows from 3 tokens: all but 96 rows go to the overflow list, more
+    entries than overflow warps, so each of those warps takes several."""
+    xt = W.small_matrix(4, 3, 256).cuda()
+    rng = np.random.default_rng(11)
+    idx = rng.integers(0, 3, 5000).astype(np.int32)
+    off = np.array([0, 1000, 1000, 3100, 5000], np.int32)
+    _gather_oracle_check(run_gather_ws(mx, xt, torch.from_numpy(idx).cuda(),
+                                       torch.from_numpy(off).cuda()), bits(xt), idx, off, 256)
 
 
 def test_gather_ws_bad_offsets_write_nothing(mx):
