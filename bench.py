@@ -481,6 +481,21 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     e_["speedup_vs_unfused"] = round(ms_unfused / ms_sc, 3)
     e_["speedup_vs_fused_gather"] = round(ms_fused / ms_sc, 3)
     out["grouped_scatter_moe_16384tok_top8_E384"] = e_
+    # the same scatter call with a workspace: each token's scale words staged
+    # once, the tiled scales written whole by a second kernel
+    ws = torch.empty(mx.mxfp4_scatter_workspace_bytes(T, total, E, K), dtype=torch.uint8,
+                     device="cuda")
+    ms_sw = time_launches(
+        lambda i: mx.mxfp4_quantize_grouped_scatter_ws(g.x_tokens, g.dest_rows, g.offsets, total,
+                                                       ws, codes, scales, sro, st, stream),
+        30, stream)
+    e_ = entry(nb, ms_sw, 4, "same call and bytes as the scatter row; offsets kernel, workspace "
+               "memset, route map kernel, scatter kernel (scale words staged once per token), "
+               "tile kernel")
+    e_["speedup_vs_unfused"] = round(ms_unfused / ms_sw, 3)
+    e_["speedup_vs_direct_scatter"] = round(ms_sc / ms_sw, 3)
+    out["grouped_scatter_ws_moe_16384tok_top8_E384"] = e_
+    del ws
     del g, codes, scales, xg
 
     # expert weights: w13 [128, 1536, 2048], w2 [128, 2048, 768], then the swap

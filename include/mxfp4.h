@@ -272,6 +272,47 @@ int mxfp4_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
                                    uint8_t* scales, int32_t* scale_row_offsets,
                                    int32_t* status, void* stream);
 
+/* mxfp4_quantize_grouped_scatter_ws — mxfp4_quantize_grouped_scatter with
+ * identical results (the same arguments, outputs, status and errors; rows
+ * that no route targets keep their codes and their scale bytes) and a
+ * caller-provided workspace: the scatter kernel stores each token's scale
+ * words once into the workspace instead of every route's words into the
+ * tiled layout, then a second kernel writes the tiled scales in whole
+ * 512-byte chunks (an untargeted row's scale bytes are read back and written
+ * unchanged).
+ *
+ * workspace        DEVICE scratch owned by the caller, 16-byte aligned, at
+ *                  least mxfp4_scatter_workspace_bytes(num_tokens,
+ *                  total_rows, E, K) bytes, not overlapping any other
+ *                  argument; its contents on entry do not matter and on
+ *                  return are unspecified.  Two calls in flight at once need
+ *                  two workspaces.
+ * num_tokens       <= INT32_MAX / 4.
+ * The _f16 form takes IEEE binary16 input.
+ *
+ * mxfp4_scatter_workspace_bytes: 4 * floor((R + 127E) / 128) * 128 bytes
+ * (the token of every padded row, R = total_rows) plus num_tokens rows of
+ * ceil(K/128) 4-byte scale words, each row padded to a multiple of 4 words;
+ * 0 for negative sizes, K % 32 != 0, num_tokens > INT32_MAX / 4 or
+ * R + 127E > INT32_MAX.
+ */
+size_t mxfp4_scatter_workspace_bytes(int64_t num_tokens, int64_t total_rows, int32_t E,
+                                     int64_t K);
+int mxfp4_quantize_grouped_scatter_ws(const void* x, int64_t num_tokens, int64_t K, int64_t ldx,
+                                      const int32_t* dest_rows, int32_t top_k,
+                                      int64_t total_rows, const int32_t* expert_offsets,
+                                      int32_t E, void* workspace, size_t workspace_bytes,
+                                      uint8_t* codes, uint8_t* scales,
+                                      int32_t* scale_row_offsets, int32_t* status,
+                                      void* stream);
+int mxfp4_quantize_grouped_scatter_ws_f16(const void* x, int64_t num_tokens, int64_t K,
+                                          int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                          int64_t total_rows, const int32_t* expert_offsets,
+                                          int32_t E, void* workspace, size_t workspace_bytes,
+                                          uint8_t* codes, uint8_t* scales,
+                                          int32_t* scale_row_offsets, int32_t* status,
+                                          void* stream);
+
 /* FP16 input for the grouped forms: mxfp4_quantize_grouped_f16,
  * mxfp4_quantize_grouped_gather_f16 and mxfp4_quantize_grouped_scatter_f16
  * take IEEE binary16 bit patterns in x and otherwise behave exactly as the

@@ -31,6 +31,8 @@ __all__ = [
     "swap_w13", "MXFP4_OK", "MXFP4_EINVAL", "MXFP4_EALIGN", "MXFP4_ESHAPE", "MXFP4_EALIAS",
     "MXFP4_ECUDA", "MXFP4_EOFFSETS", "MXFP4_EINDEX", "mxfp4_quantize_grouped_gather",
     "quantize_grouped_gather", "mxfp4_quantize_grouped_scatter", "quantize_grouped_scatter",
+    "mxfp4_scatter_workspace_bytes", "mxfp4_quantize_grouped_scatter_ws",
+    "mxfp4_quantize_grouped_scatter_ws_f16",
     "MXFP4_SCATTER_MAX_TOP_K", "mxfp4_quantize_f16", "mxfp4_quantize_grouped_f16",
     "mxfp4_quantize_grouped_gather_f16", "mxfp4_quantize_grouped_scatter_f16",
     "mxfp4_gather_workspace_bytes", "mxfp4_quantize_grouped_gather_ws",
@@ -107,6 +109,12 @@ def _load(path=LIB_PATH):
     L.mxfp4_quantize_grouped_scatter.restype = ctypes.c_int
     L.mxfp4_quantize_grouped_scatter.argtypes = [vp, i64, i64, i64, vp, i32, i64, vp, i32, vp,
                                                  vp, vp, vp, vp]
+    L.mxfp4_scatter_workspace_bytes.restype = ctypes.c_size_t
+    L.mxfp4_scatter_workspace_bytes.argtypes = [i64, i64, i32, i64]
+    for name in ("mxfp4_quantize_grouped_scatter_ws", "mxfp4_quantize_grouped_scatter_ws_f16"):
+        getattr(L, name).restype = ctypes.c_int
+        getattr(L, name).argtypes = [vp, i64, i64, i64, vp, i32, i64, vp, i32, vp,
+                                     ctypes.c_size_t, vp, vp, vp, vp, vp]
     L.mxfp4_dequantize.restype = ctypes.c_int
     L.mxfp4_dequantize.argtypes = [vp, vp, i64, i64, vp, vp]
     L.mxfp4_swap_w13.restype = ctypes.c_int
@@ -354,9 +362,11 @@ def mxfp4_quantize_grouped_gather_ws_f16(x, row_index, expert_offsets, workspace
 
 
 def _scatter(x, dest_rows, expert_offsets, total_rows, codes, scales, scale_row_offsets, status,
-             stream, f16):
-    name = "mxfp4_quantize_grouped_scatter" + ("_f16" if f16 else "")
+             stream, f16, workspace=None):
+    name = ("mxfp4_quantize_grouped_scatter" + ("_ws" if workspace is not None else "") +
+            ("_f16" if f16 else ""))
     _need_cuda("x", x, torch.float16 if f16 else torch.bfloat16)
+    _need_cuda("workspace", workspace, torch.uint8)
     _need_cuda("dest_rows", dest_rows, torch.int32)
     _need_cuda("expert_offsets", expert_offsets, torch.int32)
     _need_cuda("codes", codes, torch.uint8)
@@ -369,11 +379,12 @@ def _scatter(x, dest_rows, expert_offsets, total_rows, codes, scales, scale_row_
         raise ValueError("dest_rows must be a contiguous [num_tokens, top_k] tensor")
     T, K = x.shape
     E = expert_offsets.numel() - 1
+    ws = () if workspace is None else (_ptr(workspace), workspace.numel())
     with torch.cuda.device(_device_of(x, dest_rows, expert_offsets, codes, scales,
-                                      scale_row_offsets, status)):
+                                      scale_row_offsets, status, workspace)):
         _check(getattr(_lib, name)(
             _ptr(x), T, K, x.stride(0), _ptr(dest_rows), dest_rows.shape[1], int(total_rows),
-            _ptr(expert_offsets), E, _ptr(codes), _ptr(scales), _ptr(scale_row_offsets),
+            _ptr(expert_offsets), E, *ws, _ptr(codes), _ptr(scales), _ptr(scale_row_offsets),
             _ptr(status), _stream(stream, x.device)), name)
 
 
@@ -393,6 +404,29 @@ def mxfp4_quantize_grouped_scatter_f16(x, dest_rows, expert_offsets, total_rows:
     """mxfp4_quantize_grouped_scatter for FP16 ``x``."""
     _scatter(x, dest_rows, expert_offsets, total_rows, codes, scales, scale_row_offsets, status,
              stream, True)
+
+
+def mxfp4_scatter_workspace_bytes(num_tokens: int, total_rows: int, E: int, K: int) -> int:
+    return int(_lib.mxfp4_scatter_workspace_bytes(int(num_tokens), int(total_rows), int(E),
+                                                  int(K)))
+
+
+def mxfp4_quantize_grouped_scatter_ws(x, dest_rows, expert_offsets, total_rows: int, workspace,
+                                      codes, scales, scale_row_offsets, status=None,
+                                      stream=None) -> None:
+    """mxfp4_quantize_grouped_scatter with identical results, staging each
+    token's scale words once in ``workspace`` (uint8 device, >=
+    mxfp4_scatter_workspace_bytes) and writing the tiled scales whole."""
+    _scatter(x, dest_rows, expert_offsets, total_rows, codes, scales, scale_row_offsets, status,
+             stream, False, workspace)
+
+
+def mxfp4_quantize_grouped_scatter_ws_f16(x, dest_rows, expert_offsets, total_rows: int,
+                                          workspace, codes, scales, scale_row_offsets,
+                                          status=None, stream=None) -> None:
+    """mxfp4_quantize_grouped_scatter_ws for FP16 ``x``."""
+    _scatter(x, dest_rows, expert_offsets, total_rows, codes, scales, scale_row_offsets, status,
+             stream, True, workspace)
 
 
 def mxfp4_dequantize(codes, scales, M: int, K: int, y, stream=None) -> None:
@@ -563,11 +597,14 @@ def quantize_grouped_gather(x, row_index, expert_offsets, stream=None, via_scatt
     return codes, scales, sro, status
 
 
-def quantize_grouped_scatter(x, dest_rows, expert_offsets, total_rows=None, stream=None):
+def quantize_grouped_scatter(x, dest_rows, expert_offsets, total_rows=None, stream=None,
+                             staged=True):
     """Returns (codes, scales, scale_row_offsets, status) of the expert-sorted
     batch that ``dest_rows`` dispatches ``x`` into.  ``total_rows`` defaults
     to ``dest_rows.numel()`` (every route dispatched); rows that no route
-    targets come back zero."""
+    targets come back zero.  By default each token's scale words are staged
+    in a workspace allocated here (same results); staged=False stores every
+    route's scale words directly."""
     K = x.shape[1]
     total = dest_rows.numel() if total_rows is None else int(total_rows)
     E = expert_offsets.numel() - 1
@@ -577,8 +614,12 @@ def quantize_grouped_scatter(x, dest_rows, expert_offsets, total_rows=None, stre
                          device=dev)
     sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
     status = torch.empty(1, dtype=torch.int32, device=dev)
+    ws = None
+    if staged:
+        ws = torch.empty(max(mxfp4_scatter_workspace_bytes(x.shape[0], total, E, K), 16),
+                         dtype=torch.uint8, device=dev)
     _scatter(x, dest_rows, expert_offsets, total, codes, scales, sro, status, stream,
-             x.dtype == torch.float16)
+             x.dtype == torch.float16, ws)
     return codes, scales, sro, status
 
 

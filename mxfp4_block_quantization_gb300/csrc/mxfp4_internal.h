@@ -56,10 +56,15 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
                                               uint8_t* codes, uint8_t* scales,
                                               int32_t* scale_row_offsets, int32_t* status,
                                               int64_t bound_tiles, bool f16, cudaStream_t stream);
+// The scatter (token -> rows).  With a workspace (scatter_workspace_ints
+// int32, 16-byte aligned) every token's scale words are staged once and a
+// tile kernel writes the tiled scales; with NULL every route's scale words are
+// stored into the tiled layout by the scatter kernel itself.
+int64_t scatter_workspace_ints(int64_t num_tokens, int64_t total_rows, int64_t E, int64_t K);
 cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
                                             int64_t ldx, const int32_t* dest_rows, int32_t top_k,
                                             int64_t total_rows, const int32_t* offsets, int32_t E,
-                                            uint8_t* codes, uint8_t* scales,
+                                            int32_t* workspace, uint8_t* codes, uint8_t* scales,
                                             int32_t* scale_row_offsets, int32_t* status,
                                             int64_t bound_tiles, bool f16, cudaStream_t stream);
 

@@ -265,6 +265,51 @@ constexpr int kScatterWarps = kThreads / 32;  // tokens per CTA
 constexpr int kScatterBatch = 4;              // passes with loads in flight together
 constexpr int kScatterPass = 32 * kElems;     // elements per warp pass (4 k-tiles)
 
+constexpr int kInvertThreads = 256;
+constexpr int kSmemSegs = 2048;  // up to this many segments are searched in shared memory
+
+// Row -> padded row for the per-row map kernels.  With E <= cap the
+// offsets and padded starts are copied to shared memory once per CTA (every
+// thread of the block must call the constructor: it has a barrier) and each
+// row's segment is a binary search there; otherwise find_segment on global
+// memory.
+struct SegmentSearch {
+  int32_t* s_off;
+  int32_t* s_pad;
+  const int32_t* off;
+  const int32_t* pad;
+  int E;
+  int total;
+  bool smem;
+  // s_off and s_pad hold cap + 1 entries each
+  __device__ SegmentSearch(int32_t* so, int32_t* sp, const int32_t* o, const int32_t* pd, int e,
+                           int tot, int cap = kSmemSegs)
+      : s_off(so), s_pad(sp), off(o), pad(pd), E(e), total(tot), smem(e <= cap) {
+    if (smem)
+      for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+        s_off[i] = __ldg(off + i);
+        s_pad[i] = __ldg(pad + i);
+      }
+    __syncthreads();
+  }
+  __device__ int rows_of(int e) const {  // n_e
+    return smem ? s_off[e + 1] - s_off[e] : __ldg(off + e + 1) - __ldg(off + e);
+  }
+  __device__ int padded_start(int e) const { return smem ? s_pad[e] : __ldg(pad + e); }
+  __device__ int padded_row(int v) const {  // v in [0, total)
+    if (!smem) {
+      const int e = find_segment(off, E, v, total);
+      return __ldg(pad + e) + (v - __ldg(off + e));
+    }
+    int lo = 0, hi = E - 1;  // the largest e with o[e] <= v: its segment is not empty
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_off[mid] <= v) lo = mid; else hi = mid - 1;
+    }
+    return s_pad[lo] + (v - s_off[lo]);
+  }
+};
+
 struct ScatterParams {
   const uint8_t* __restrict__ x;          // BF16 token rows
   int64_t ldx_bytes;                      // token row stride in bytes
@@ -291,6 +336,8 @@ struct ScatterParams {
   int32_t pad_ctas;                       // leading CTAs that zero pad scale rows (E or 0)
   int32_t sK;
   int32_t nKT;
+  int32_t map_ctas;                       // kStaged, token-major: the next CTAs write tok1,
+  int32_t* __restrict__ tok1;             //   the token + 1 of every padded row (-1: pad row)
 #ifdef MXFP4_DEBUG_BOUNDS
   DebugRanges dbg;                        // slots as in QuantizeParams (kDbgRowIndex: dest_rows)
 #endif
@@ -395,6 +442,41 @@ __device__ __forceinline__ void scatter_token(const ScatterParams& p, int64_t t,
   __syncwarp();  // s_code / s_scale are rewritten by the warp's next token
 }
 
+// Map CTA m of the staged token-major scatter: the token + 1 of every padded
+// row a route lands on, and -1 for the pad rows of every segment (rows no
+// route targets keep the 0 of the memset).  The tile kernel reads the map
+// after this launch has completed.  The offsets and padded starts (up to
+// kMapSegs + 1 each) reuse the warps' route arrays s_code and s_scale.
+constexpr int kMapSegs = 511;
+static_assert((kMapSegs + 1) * 4 == kScatterWarps * MXFP4_SCATTER_MAX_TOP_K * 8,
+              "one segment array fills one route array");
+__device__ __forceinline__ void scatter_route_map(const ScatterParams& p, int m, int32_t* s_off,
+                                                  int32_t* s_pad) {
+  const SegmentSearch seg(s_off, s_pad, p.offsets, p.padded, p.E,
+                          static_cast<int>(p.total_rows), kMapSegs);
+  const int64_t gid = static_cast<int64_t>(m) * kThreads + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(p.map_ctas) * kThreads;
+  // the pad rows: item k is pad slot k % 128 of segment k / 128, so that
+  // consecutive threads store consecutive rows of one segment
+  for (int64_t k = gid; k < static_cast<int64_t>(p.E) * kTileRows; k += stride) {
+    const int e = static_cast<int>(k / kTileRows);
+    const int i = static_cast<int>(k % kTileRows);
+    const int n = seg.rows_of(e);
+    const int npad = (n + kTileRows - 1) / kTileRows * kTileRows - n;
+    if (i >= npad) continue;
+    int32_t* const tp = p.tok1 + seg.padded_start(e) + n + i;
+    if (MXFP4_IN_BOUNDS(p, kDbgWork, tp, 4)) *tp = -1;
+  }
+  const int64_t n_routes = p.num_tokens * p.top_k;
+  for (int64_t i = gid; i < n_routes; i += stride) {
+    const int32_t* dp = p.dest_rows + i;
+    const int32_t v = MXFP4_IN_BOUNDS(p, kDbgRowIndex, dp, 4) ? __ldg(dp) : -1;
+    if (v < 0 || v >= p.total_rows) continue;  // the token warps report bad entries
+    int32_t* const tp = p.tok1 + seg.padded_row(v);
+    if (MXFP4_IN_BOUNDS(p, kDbgWork, tp, 4)) *tp = static_cast<int32_t>(i / p.top_k) + 1;
+  }
+}
+
 // Overflow entry j (bucket mode): its token and row; false past the list.
 __device__ __forceinline__ bool overflow_entry(const ScatterParams& p, int64_t j, int64_t& t,
                                                const int32_t*& dsts) {
@@ -437,9 +519,18 @@ __global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_ke
     return;
   }
 
+  if constexpr (kStaged) {
+    const int m = static_cast<int>(blockIdx.x) - p.pad_ctas;
+    if (m < p.map_ctas) {  // uniform over the block
+      scatter_route_map(p, m, reinterpret_cast<int32_t*>(&s_code[0][0]),
+                        reinterpret_cast<int32_t*>(&s_scale[0][0]));
+      return;
+    }
+  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t w_id = static_cast<int64_t>(blockIdx.x - p.pad_ctas) * kScatterWarps + warp;
+  const int lead = p.pad_ctas + (kStaged ? p.map_ctas : 0);  // CTAs before the token warps
+  const int64_t w_id = static_cast<int64_t>(blockIdx.x - lead) * kScatterWarps + warp;
   // whole warps return below; there is no block-wide barrier after this point
   int64_t t;
   const int32_t* dsts;
@@ -467,7 +558,8 @@ __global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_ke
     // only overflow warps go on; their cursor is kept in shared memory so that
     // nothing stays live across the body above
     if (p.count == nullptr ||
-        static_cast<int64_t>(blockIdx.x - p.pad_ctas) * kScatterWarps + warp < p.num_tokens)
+        static_cast<int64_t>(blockIdx.x - p.pad_ctas - (kStaged ? p.map_ctas : 0)) *
+                    kScatterWarps + warp < p.num_tokens)
       return;
     const int64_t j = s_next[warp] + p.n_ovf_warps;
     if (!overflow_entry(p, j, t, dsts)) return;
@@ -476,31 +568,42 @@ __global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_ke
   }
 }
 
-// Tiled scales of the gathered batch from the staged per-token words: one CTA
-// per padded 128-row tile.  Padded row pr takes the words of token
-// tok1[pr] - 1 (written by invert_bucket_kernel for row o[e] + pr - P[e] of
-// segment e); pad rows and rows whose index is out of range keep tok1 = 0 and
-// get zero words.  The tile's 128 x nKT words pass through shared memory (64
-// k-tiles at a time) so that every 512-byte chunk is written whole, 16 bytes
+// Tiled scales of the gathered or scattered batch from the staged per-token
+// words: one CTA per padded 128-row tile.  Padded row pr takes the words of
+// token tok1[pr] - 1 (for the gather written by invert_bucket_kernel for row
+// o[e] + pr - P[e] of segment e, for the scatter by the map CTAs of the
+// scatter launch).  In the gather, pad rows and rows whose index is out of
+// range keep tok1 = 0 and get zero words; in the scatter, pad rows are marked
+// -1 and get zero words, and rows that no route targets (0) keep the words
+// they held.  The tile's 128 x nKT words pass through shared memory, 32
+// k-tiles at a time, so that every 512-byte chunk is written whole, 16 bytes
 // per thread, instead of 4-byte words scattered over the chunks.
 struct TileScalesParams {
-  const int32_t* __restrict__ tok1;       // [grid * 128] token + 1 of every padded row, 0: none
+  const int32_t* __restrict__ tok1;       // [grid * 128] token + 1 of every padded row, 0: none,
+                                          //   -1: pad row (keep_unset only)
   const uint32_t* __restrict__ stage;     // [T, stage_ld(nKT)], 16-byte aligned
   uint8_t* __restrict__ scales;
   const int32_t* __restrict__ padded;
   int32_t E;
   int32_t nKT;
+  int32_t keep_unset;                     // rows with tok1 == 0 keep their scale words (the
+                                          //   scatter leaves untargeted rows untouched)
 #ifdef MXFP4_DEBUG_BOUNDS
   DebugRanges dbg;  // kDbgScales, kDbgPadded, kDbgRowIndex (tok1), kDbgWork (stage)
 #endif
 };
 
-constexpr int kTileCols = 64;  // k-tiles per shared-memory pass
-constexpr int kTileQuads = kTileRows * (kTileCols / 4) / kThreads;  // uint4 loads per thread
-static_assert(kThreads == 16 * 16 && kTileQuads * 16 == kTileRows,
-              "tile_scales_kernel: 16 quads x 16 rows per step, kTileQuads steps");
+// 128 threads and 32 k-tiles (17 KB of shared memory) per pass: ten CTAs per
+// SM, so the 1405 tiles of the MoE batch run in one wave.
+constexpr int kTileThreads = 128;
+constexpr int kTileCols = 32;                                  // k-tiles per shared-memory pass
+constexpr int kTileQuadsPerRow = kTileCols / 4;                // 16-byte quads of a row
+constexpr int kTileRowStep = kTileThreads / kTileQuadsPerRow;  // rows per load step
+constexpr int kTileQuads = kTileRows / kTileRowStep;           // uint4 loads per thread
+static_assert(kTileRows % kTileRowStep == 0 && kTileRows <= kTileThreads,
+              "tile_scales_kernel: whole load steps, one token per thread");
 
-__global__ void __launch_bounds__(kThreads) tile_scales_kernel(const TileScalesParams p) {
+__global__ void __launch_bounds__(kTileThreads, 10) tile_scales_kernel(const TileScalesParams p) {
   __shared__ uint32_t s_w[kTileRows][kTileCols + 1];  // odd stride: conflict-free columns
   __shared__ int32_t s_tok[kTileRows];
 
@@ -522,8 +625,8 @@ __global__ void __launch_bounds__(kThreads) tile_scales_kernel(const TileScalesP
 
   uint8_t* const tile = p.scales + static_cast<int64_t>(blockIdx.x) * p.nKT * kChunkBytes;
   const int64_t ld = stage_ld(p.nKT);
-  const int qd = threadIdx.x & 15;  // this thread's 16-byte quad of a row: words 4qd .. 4qd+3
-  const int rb = threadIdx.x >> 4;  // and its rows rb, rb + 16, ...
+  const int qd = threadIdx.x % kTileQuadsPerRow;  // this thread's quad: words 4qd .. 4qd+3
+  const int rb = threadIdx.x / kTileQuadsPerRow;  // and its rows rb, rb + kTileRowStep, ...
   for (int c0 = 0; c0 < p.nKT; c0 += kTileCols) {
     const int cw = p.nKT - c0 < kTileCols ? p.nKT - c0 : kTileCols;
     const bool in_row = 4 * qd < cw;
@@ -531,17 +634,29 @@ __global__ void __launch_bounds__(kThreads) tile_scales_kernel(const TileScalesP
     uint4 v[kTileQuads];
 #pragma unroll
     for (int j = 0; j < kTileQuads; ++j) {
-      const int32_t t = s_tok[rb + 16 * j];
+      const int r = rb + kTileRowStep * j;
+      const int32_t t = s_tok[r];  // token, -1: no token, -2: pad row
       v[j] = make_uint4(0u, 0u, 0u, 0u);
       if (t >= 0 && in_row) {
         const uint32_t* sp = p.stage + static_cast<int64_t>(t) * ld + c0 + 4 * qd;
         if (MXFP4_IN_BOUNDS(p, kDbgWork, sp, 16)) v[j] = __ldg(reinterpret_cast<const uint4*>(sp));
+      } else if (t == -1 && p.keep_unset && in_row) {
+        // an untargeted row keeps its words: read them back (this pass's
+        // chunks are written only after the barrier below)
+        const uint8_t* op = tile + static_cast<int64_t>(c0 + 4 * qd) * kChunkBytes +
+                            (r & 31) * 16 + (r >> 5) * 4;
+        uint32_t w4[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (c0 + 4 * qd + i < p.nKT && MXFP4_IN_BOUNDS(p, kDbgScales, op + i * kChunkBytes, 4))
+            w4[i] = *reinterpret_cast<const uint32_t*>(op + i * kChunkBytes);
+        v[j] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
     }
     if (in_row) {
 #pragma unroll
       for (int j = 0; j < kTileQuads; ++j) {
-        uint32_t* const w = &s_w[rb + 16 * j][4 * qd];  // words past cw are never read
+        uint32_t* const w = &s_w[rb + kTileRowStep * j][4 * qd];  // words past cw: never read
         w[0] = v[j].x;
         w[1] = v[j].y;
         w[2] = v[j].z;
@@ -550,7 +665,7 @@ __global__ void __launch_bounds__(kThreads) tile_scales_kernel(const TileScalesP
     }
     __syncthreads();
     // piece (c, o): rows o, o+32, o+64, o+96 of k-tile c0 + c, bytes o*16 of its chunk
-    for (int i = threadIdx.x; i < cw * 32; i += kThreads) {
+    for (int i = threadIdx.x; i < cw * 32; i += kTileThreads) {
       const int c = i >> 5;
       const int o = i & 31;
       uint8_t* const dp = tile + static_cast<int64_t>(c0 + c) * kChunkBytes + o * 16;
@@ -596,14 +711,16 @@ struct InvertParams {
 #endif
 };
 
-constexpr int kInvertThreads = 256;
-
 __global__ void __launch_bounds__(kInvertThreads) invert_bucket_kernel(const InvertParams q) {
+  __shared__ int32_t s_off[kSmemSegs + 1];
+  __shared__ int32_t s_pad[kSmemSegs + 1];
   pdl_wait();
   pdl_release();
   if (!MXFP4_IN_BOUNDS(q, kDbgPadded, q.padded, (q.E + 1) * 4) ||
       !MXFP4_IN_BOUNDS(q, kDbgOffsets, q.offsets, (q.E + 1) * 4) || __ldg(q.padded + q.E) < 0)
-    return;  // rejected offsets: nothing is written
+    return;  // rejected offsets: nothing is written (uniform over the block)
+  const SegmentSearch seg(s_off, s_pad, q.offsets, q.padded, q.E,
+                          static_cast<int>(q.total_rows));
   bool bad = false;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kInvertThreads;
   for (int64_t r = static_cast<int64_t>(blockIdx.x) * kInvertThreads + threadIdx.x;
@@ -626,8 +743,7 @@ __global__ void __launch_bounds__(kInvertThreads) invert_bucket_kernel(const Inv
       }
     }
     if (valid && q.tok1 == nullptr) continue;
-    const int e = find_segment(q.offsets, q.E, static_cast<int>(r), static_cast<int>(q.total_rows));
-    const int prow = __ldg(q.padded + e) + (static_cast<int>(r) - __ldg(q.offsets + e));
+    const int prow = seg.padded_row(static_cast<int>(r));
     if (valid) {
       if (MXFP4_IN_BOUNDS(q, kDbgWork, q.tok1 + prow, 4)) q.tok1[prow] = t + 1;
       continue;
@@ -853,14 +969,34 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
   return launch_pdl(kernel, static_cast<unsigned>(grid), kGatherThreads, 0, stream, p);
 }
 
+int64_t scatter_workspace_ints(int64_t num_tokens, int64_t total_rows, int64_t E, int64_t K) {
+  return gather_tok_ints(total_rows, E) + gather_stage_ints(num_tokens, K);
+}
+
 cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
                                             int64_t ldx, const int32_t* dest_rows, int32_t top_k,
                                             int64_t total_rows, const int32_t* offsets, int32_t E,
-                                            uint8_t* codes, uint8_t* scales,
+                                            int32_t* workspace, uint8_t* codes, uint8_t* scales,
                                             int32_t* scale_row_offsets, int32_t* status,
                                             int64_t bound_tiles, bool f16, cudaStream_t stream) {
   cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
   if (err != cudaSuccess || E == 0 || K == 0) return err;
+  // staged: [tok1 PT][stage num_tokens x stage_ld(nKT)] (PT is a multiple of 128)
+  const bool staged = workspace != nullptr && total_rows > 0;
+  const int64_t PT = staged ? gather_tok_ints(total_rows, E) : 0;
+  const int32_t nKT = (static_cast<int32_t>(K / kBlock) + kTileBlocks - 1) / kTileBlocks;
+  int32_t map_ctas = 0;
+  if (staged) {
+    err = cudaMemsetAsync(workspace, 0, static_cast<size_t>(PT) * 4, stream);
+    if (err != cudaSuccess) return err;
+    // the row map (routes and pad rows, about 4 items per thread) runs in the
+    // first CTAs of the scatter launch, beside the token warps
+    const int64_t items = num_tokens * top_k > static_cast<int64_t>(E) * kTileRows
+                              ? num_tokens * top_k
+                              : static_cast<int64_t>(E) * kTileRows;
+    const int64_t need = (items + 4 * kThreads - 1) / (4 * kThreads);
+    map_ctas = static_cast<int32_t>(need < 1 ? 1 : (need < sm_count() ? need : sm_count()));
+  }
   ScatterParams p{};
   p.x = static_cast<const uint8_t*>(x);
   p.ldx_bytes = ldx * 2;
@@ -869,9 +1005,11 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
   p.codes = codes;
   p.scales = scales;
   p.sK = static_cast<int32_t>(K / kBlock);
-  p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
-  p.stage = nullptr;
-  p.pad_ctas = E;
+  p.nKT = nKT;
+  p.stage = staged ? reinterpret_cast<uint32_t*>(workspace + PT) : nullptr;
+  p.pad_ctas = staged ? 0 : E;
+  p.map_ctas = map_ctas;
+  p.tok1 = staged ? workspace : nullptr;
   p.offsets = offsets;
   p.padded = scale_row_offsets;
   p.E = E;
@@ -887,14 +1025,39 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
   debug_range(p.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
   debug_range(p.dbg, kDbgRowIndex, dest_rows, num_tokens * top_k * 4);
   debug_range(p.dbg, kDbgStatus, status, status ? 4 : 0);
+  debug_range(p.dbg, kDbgWork, workspace, staged ? (PT + gather_stage_ints(num_tokens, K)) * 4 : 0);
 #endif
-  const int64_t grid = E + (num_tokens + kScatterWarps - 1) / kScatterWarps;
+  const int64_t grid =
+      p.pad_ctas + p.map_ctas + (num_tokens + kScatterWarps - 1) / kScatterWarps;
   const bool v32 = vec32_ok(x, p.ldx_bytes);
-  const auto kernel = f16 ? (v32 ? quantize_scatter_kernel<true, true, false>
-                                 : quantize_scatter_kernel<false, true, false>)
-                          : (v32 ? quantize_scatter_kernel<true, false, false>
-                                 : quantize_scatter_kernel<false, false, false>);
-  return launch_pdl(kernel, static_cast<unsigned>(grid), kThreads, 0, stream, p);
+  using Kernel = void (*)(const ScatterParams);
+  static constexpr Kernel kKernels[2][2][2] = {
+      {{quantize_scatter_kernel<false, false, false>, quantize_scatter_kernel<false, false, true>},
+       {quantize_scatter_kernel<false, true, false>, quantize_scatter_kernel<false, true, true>}},
+      {{quantize_scatter_kernel<true, false, false>, quantize_scatter_kernel<true, false, true>},
+       {quantize_scatter_kernel<true, true, false>, quantize_scatter_kernel<true, true, true>}}};
+  if (grid > 0) {
+    err = launch_pdl(kKernels[v32][f16][staged], static_cast<unsigned>(grid), kThreads, 0, stream,
+                     p);
+    if (err != cudaSuccess) return err;
+  }
+  if (!staged || bound_tiles == 0) return cudaSuccess;
+  TileScalesParams ts{};
+  ts.tok1 = workspace;
+  ts.stage = p.stage;
+  ts.scales = scales;
+  ts.padded = scale_row_offsets;
+  ts.E = E;
+  ts.nKT = nKT;
+  ts.keep_unset = 1;
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(ts.dbg, kDbgScales, scales, bound_tiles * ts.nKT * kChunkBytes);
+  debug_range(ts.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(ts.dbg, kDbgRowIndex, workspace, PT * 4);
+  debug_range(ts.dbg, kDbgWork, p.stage, gather_stage_ints(num_tokens, K) * 4);
+#endif
+  return launch_pdl(tile_scales_kernel, static_cast<unsigned>(bound_tiles), kTileThreads, 0, stream,
+                    ts);
 }
 
 // Workspace of the gather through the scatter path, in int32:
@@ -1029,7 +1192,7 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   debug_range(ts.dbg, kDbgRowIndex, q.tok1, PT * 4);
   debug_range(ts.dbg, kDbgWork, p.stage, T * stage_ld(ts.nKT) * 4);
 #endif
-  return launch_pdl(tile_scales_kernel, static_cast<unsigned>(bound_tiles), kThreads, 0, stream,
+  return launch_pdl(tile_scales_kernel, static_cast<unsigned>(bound_tiles), kTileThreads, 0, stream,
                     ts);
 }
 

@@ -177,6 +177,36 @@ def test_grouped_scatter_validation(lib):
     assert call(T=0, x=None, dst=None, off=None) == lib.MXFP4_EINVAL
 
 
+def test_grouped_scatter_ws_validation(lib):
+    f = lib._lib.mxfp4_quantize_grouped_scatter_ws
+    need = lib.mxfp4_scatter_workspace_bytes(50, 400, 2, 64)
+    # token of every padded row (floor((R + 127E)/128)*128 ints), then T rows of 4 words
+    assert need == 4 * ((400 + 254) // 128 * 128) + 50 * 4 * 4
+    assert lib.mxfp4_scatter_workspace_bytes(50, 400, 2, 7168) == 4 * 640 + 50 * 56 * 4
+    assert lib.mxfp4_scatter_workspace_bytes(50, 400, 2, 48) == 0
+    assert lib.mxfp4_scatter_workspace_bytes(50, 400, -1, 64) == 0
+    # x, T, K, ldx, dest, top_k, total, off, E, ws, ws_bytes, codes, scales, sro, status, stream
+    ok = [A, 50, 64, 64, 2 * A, 8, 400, 3 * A, 2, 8 * A, need, 4 * A, 5 * A, 6 * A, None, None]
+
+    def call(**kw):
+        names = ["x", "T", "K", "ldx", "dst", "k", "tot", "off", "E", "ws", "wsb", "c", "s",
+                 "sro", "st", "strm"]
+        a = dict(zip(names, ok))
+        a.update(kw)
+        return f(*[a[n] for n in names])
+
+    assert call(ws=None) == lib.MXFP4_EINVAL
+    assert call(wsb=need - 16) == lib.MXFP4_EINVAL
+    assert call(ws=8 * A + 8) == lib.MXFP4_EALIGN
+    assert call(ws=4 * A + 16) == lib.MXFP4_EALIAS            # workspace overlaps the codes
+    assert call(ws=2 * A) == lib.MXFP4_EALIAS                 # workspace overlaps the routes
+    assert call(k=0) == lib.MXFP4_EINVAL
+    assert call(K=48, ldx=48) == lib.MXFP4_ESHAPE
+    assert call(T=(1 << 31) // 4 + 1) == lib.MXFP4_ESHAPE
+    assert lib._lib.mxfp4_quantize_grouped_scatter_ws_f16(*ok[:2], 48, 48, *ok[4:]) == \
+        lib.MXFP4_ESHAPE
+
+
 def test_quantize_f16_validation(lib):
     f = lib._lib.mxfp4_quantize_f16
     assert f(A, 4, 48, 48, 2 * A, 3 * A, None) == lib.MXFP4_ESHAPE

@@ -132,6 +132,8 @@ def test_everything_in_bounds(libs):
     dsc[5, 0] = 1 << 20
     cases.append(lambda: written(mx.quantize_grouped_scatter(gsmall.x_tokens, dsc,
                                                              gsmall.offsets), 288))
+    cases.append(lambda: written(mx.quantize_grouped_scatter(gsmall.x_tokens, dsc, gsmall.offsets,
+                                                             staged=False), 288))
     cases.append(lambda: written(mx.quantize_grouped_scatter(gsmall.x_tokens[:0], dsc[:0],
                                                              gsmall.offsets, dsc.numel()), 288))
     g3 = W.moe_grouped(seed=9, tokens=130, top_k=3, num_experts=5, K=1056, device="cuda")

@@ -89,16 +89,26 @@ def test_fuzz_grouped_gather_scatter(mx, seed):
     nsb = mx.mxfp4_grouped_scale_bytes_bound(total, E, K)
     c0 = rng.integers(0, 256, (total, K // 2), dtype=np.uint8)
     s0 = rng.integers(0, 256, nsb, dtype=np.uint8)
-    codes = torch.from_numpy(c0).cuda()
-    scales = torch.from_numpy(s0).cuda()
-    sro = torch.empty(E + 1, dtype=torch.int32, device="cuda")
-    st = torch.empty(1, dtype=torch.int32, device="cuda")
-    fn = mx.mxfp4_quantize_grouped_scatter_f16 if f16 else mx.mxfp4_quantize_grouped_scatter
-    fn(xp, torch.from_numpy(dest).cuda(), off_d, total, codes, scales, sro, st)
     rc, c_o, s_o, sro_o = oracle.quantize_grouped_scatter(xb, dest, off, total, c0, s0, f16=f16)
-    torch.cuda.synchronize()
-    assert int(st.item()) == rc == 0
-    assert np.array_equal(codes.cpu().numpy(), c_o) and np.array_equal(scales.cpu().numpy(), s_o)
+    for staged in (False, True):                       # per-route scale words / workspace
+        codes = torch.from_numpy(c0).cuda()
+        scales = torch.from_numpy(s0).cuda()
+        sro = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+        st = torch.empty(1, dtype=torch.int32, device="cuda")
+        args = (xp, torch.from_numpy(dest).cuda(), off_d, total)
+        if staged:
+            ws = torch.empty(mx.mxfp4_scatter_workspace_bytes(T, total, E, K), dtype=torch.uint8,
+                             device="cuda")
+            fn = (mx.mxfp4_quantize_grouped_scatter_ws_f16 if f16
+                  else mx.mxfp4_quantize_grouped_scatter_ws)
+            fn(*args, ws, codes, scales, sro, st)
+        else:
+            fn = mx.mxfp4_quantize_grouped_scatter_f16 if f16 else mx.mxfp4_quantize_grouped_scatter
+            fn(*args, codes, scales, sro, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == rc == 0, staged
+        assert np.array_equal(codes.cpu().numpy(), c_o), staged
+        assert np.array_equal(scales.cpu().numpy(), s_o), staged
     # gather (both kernels): dropped rows have index -1 -> zero rows, EINDEX
     rc_g, cg_o, sg_o, _ = oracle.quantize_grouped_gather(xb, row_tok, off, f16=f16)
     used = int(sro_o[-1]) * ((K // 32 + 3) // 4 * 4)

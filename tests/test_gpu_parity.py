@@ -389,7 +389,15 @@ def test_grouped_gather_moe_full_size(mx):
 
 
 # ------------------------------------------------- fused dispatch scatter
-def run_scatter(mx, x, dest, offsets, total, seed=0):
+@pytest.fixture(params=[False, True], ids=["direct", "ws"])
+def scatter_ws(request):
+    """Every scatter case runs both forms: scale words stored per route
+    (mxfp4_quantize_grouped_scatter) and staged in a workspace
+    (mxfp4_quantize_grouped_scatter_ws)."""
+    return request.param
+
+
+def run_scatter(mx, x, dest, offsets, total, seed=0, ws=False):
     """Scatter form through the C ABI into guard-banded buffers whose inner
     bytes start random (the same bytes go to the oracle, so untouched rows
     and slack compare equal); returns the GPU and oracle results."""
@@ -405,9 +413,18 @@ def run_scatter(mx, x, dest, offsets, total, seed=0):
     scales.t.copy_(torch.from_numpy(s0))
     sro = Guarded(4 * (E + 1), torch.int32)
     status = Guarded(4, torch.int32)
-    mx.mxfp4_quantize_grouped_scatter(x, dest, offsets, total, codes.t, scales.t, sro.t, status.t)
+    guards = [codes, scales, sro, status]
+    if ws:
+        work = Guarded(max(mx.mxfp4_scatter_workspace_bytes(x.shape[0], total, E, K), 16))
+        work.t.fill_(0x5A)                            # contents on entry must not matter
+        guards.append(work)
+        mx.mxfp4_quantize_grouped_scatter_ws(x, dest, offsets, total, work.t, codes.t, scales.t,
+                                             sro.t, status.t)
+    else:
+        mx.mxfp4_quantize_grouped_scatter(x, dest, offsets, total, codes.t, scales.t, sro.t,
+                                          status.t)
     torch.cuda.synchronize()
-    for g in (codes, scales, sro, status):
+    for g in guards:
         g.check()
     gpu = (codes.t.cpu().numpy(), scales.t.cpu().numpy(), sro.t.cpu().numpy(),
            int(status.t.cpu()[0]))
@@ -425,9 +442,10 @@ def assert_scatter_parity(gpu, orc, want_status=0):
     assert np.array_equal(s, s_o), _first_diff(s, s_o)
 
 
-def test_grouped_scatter_small(mx):
+def test_grouped_scatter_small(mx, scatter_ws):
     g = W.moe_grouped(seed=2, tokens=200, top_k=4, num_experts=12, K=288, device="cuda")
-    gpu, orc = run_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, g.row_index.numel())
+    gpu, orc = run_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, g.row_index.numel(),
+                           ws=scatter_ws)
     assert_scatter_parity(gpu, orc)
     c_g, s_g, sro_g, _ = run_gather(mx, g.x_tokens, g.row_index, g.offsets)
     used = int(sro_g[-1]) * 12
@@ -436,65 +454,68 @@ def test_grouped_scatter_small(mx):
 
 @pytest.mark.parametrize("tokens,top_k,E,K", [
     (1, 1, 1, 32), (129, 3, 5, 160), (300, 2, 7, 2880), (64, 32, 40, 96), (257, 8, 16, 1056)])
-def test_grouped_scatter_shapes(mx, tokens, top_k, E, K):
+def test_grouped_scatter_shapes(mx, tokens, top_k, E, K, scatter_ws):
     g = W.moe_grouped(seed=tokens + K, tokens=tokens, top_k=top_k, num_experts=E, K=K,
                       device="cuda")
-    gpu, orc = run_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, g.row_index.numel(), seed=K)
+    gpu, orc = run_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, g.row_index.numel(), seed=K,
+                           ws=scatter_ws)
     assert_scatter_parity(gpu, orc)
 
 
-def test_grouped_scatter_dropped_routes(mx):
+def test_grouped_scatter_dropped_routes(mx, scatter_ws):
     """20 % of the routes not dispatched (-1): their rows keep their previous
     bytes, codes and scale bytes alike; pad rows are zeroed."""
     g = W.moe_grouped(seed=6, tokens=300, top_k=4, num_experts=9, K=160, device="cuda")
     dst = g.dest_rows.clone()
     drop = torch.rand(dst.shape, generator=torch.Generator().manual_seed(1)) < 0.2
     dst[drop.cuda()] = -1
-    gpu, orc = run_scatter(mx, g.x_tokens, dst, g.offsets, g.row_index.numel(), seed=3)
+    gpu, orc = run_scatter(mx, g.x_tokens, dst, g.offsets, g.row_index.numel(), seed=3,
+                           ws=scatter_ws)
     assert_scatter_parity(gpu, orc)
 
 
-def test_grouped_scatter_empty_experts_and_no_tokens(mx):
+def test_grouped_scatter_empty_experts_and_no_tokens(mx, scatter_ws):
     x = W.small_matrix(4, 100, 256).cuda()
     off = torch.tensor([0, 0, 130, 130, 200, 200], dtype=torch.int32, device="cuda")
     perm = torch.randperm(200, generator=torch.Generator().manual_seed(2)).to(torch.int32)
     dst = perm.view(100, 2).cuda()
-    gpu, orc = run_scatter(mx, x, dst, off, 200, seed=4)
+    gpu, orc = run_scatter(mx, x, dst, off, 200, seed=4, ws=scatter_ws)
     assert_scatter_parity(gpu, orc)
     # no tokens at all: every row untargeted, only the pad rows are written
-    gpu, orc = run_scatter(mx, x[:0], dst[:0], off, 200, seed=5)
+    gpu, orc = run_scatter(mx, x[:0], dst[:0], off, 200, seed=5, ws=scatter_ws)
     assert_scatter_parity(gpu, orc)
 
 
-def test_grouped_scatter_bad_entries(mx):
+def test_grouped_scatter_bad_entries(mx, scatter_ws):
     g = W.moe_grouped(seed=7, tokens=140, top_k=2, num_experts=3, K=64, device="cuda")
     total = g.row_index.numel()
     dst = g.dest_rows.clone()
     dst[3, 1] = total
     dst[7, 0] = -2
     dst[139, 1] = 1 << 30
-    gpu, orc = run_scatter(mx, g.x_tokens, dst, g.offsets, total, seed=6)
+    gpu, orc = run_scatter(mx, g.x_tokens, dst, g.offsets, total, seed=6, ws=scatter_ws)
     assert orc[3] == -7
     assert_scatter_parity(gpu, orc, want_status=mx.MXFP4_EINDEX)
 
 
 @pytest.mark.parametrize("off", [[1, 10, 20], [0, 12, 8, 20], [0, 10, 19]])
-def test_grouped_scatter_bad_offsets(mx, off):
+def test_grouped_scatter_bad_offsets(mx, off, scatter_ws):
     x = W.small_matrix(3, 10, 64).cuda()
     dst = torch.arange(20, dtype=torch.int32, device="cuda").view(10, 2)
     o = torch.tensor(off, dtype=torch.int32, device="cuda")
-    gpu, orc = run_scatter(mx, x, dst, o, 20, seed=7)
+    gpu, orc = run_scatter(mx, x, dst, o, 20, seed=7, ws=scatter_ws)
     assert orc[3] == -6 and gpu[3] == mx.MXFP4_EOFFSETS
     assert (gpu[2] == -1).all()
     assert np.array_equal(gpu[0], orc[0]) and np.array_equal(gpu[1], orc[1])  # untouched
 
 
-def test_grouped_scatter_strided_and_16b_aligned(mx):
+def test_grouped_scatter_strided_and_16b_aligned(mx, scatter_ws):
     g = W.moe_grouped(seed=8, tokens=150, top_k=3, num_experts=6, K=256, device="cuda")
     wide = torch.zeros((150, 392), dtype=torch.bfloat16, device="cuda")
     wide[:, 8:264] = g.x_tokens
     for x in (wide[:, 8:264], offset16(g.x_tokens)):
-        gpu, orc = run_scatter(mx, x, g.dest_rows, g.offsets, g.row_index.numel(), seed=8)
+        gpu, orc = run_scatter(mx, x, g.dest_rows, g.offsets, g.row_index.numel(), seed=8,
+                               ws=scatter_ws)
         assert_scatter_parity(gpu, orc)
 
 
@@ -505,11 +526,13 @@ def test_grouped_scatter_moe_full_size(mx):
     g = W.moe_grouped(seed=2, device="cuda")
     c1, s1, sro1, st1 = mx.quantize_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets)
     c2, s2, sro2, st2 = mx.quantize_grouped_gather(g.x_tokens, g.row_index, g.offsets)
+    c3, s3, sro3, st3 = mx.quantize_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets,
+                                                    staged=False)
     torch.cuda.synchronize()
-    assert int(st1.cpu()[0]) == 0 and int(st2.cpu()[0]) == 0
-    assert torch.equal(sro1, sro2) and torch.equal(c1, c2)
+    assert int(st1.cpu()[0]) == 0 and int(st2.cpu()[0]) == 0 and int(st3.cpu()[0]) == 0
+    assert torch.equal(sro1, sro2) and torch.equal(c1, c2) and torch.equal(c1, c3)
     used = int(sro1[-1].item()) * 224
-    assert torch.equal(s1[:used], s2[:used])
+    assert torch.equal(s1[:used], s2[:used]) and torch.equal(s1[:used], s3[:used])
     off_h = g.offsets.cpu().numpy().astype(np.int64)
     sro_h = sro1.cpu().numpy().astype(np.int64)
     for e in (0, 17, 200, 383):
