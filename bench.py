@@ -536,6 +536,52 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     return out
 
 
+DISPATCH_CALLS = ("gather", "gather_ws", "scatter", "scatter_ws")
+
+
+def run_one_call(args):
+    """--call NAME: one dispatch call on the MoE batch (16384 tokens x top-8
+    over 384 experts, K = 7168), repeated --reps times after one warm-up, and
+    one JSON line with its mean CUDA-event time.  For profiling a single call
+    (ncu -k on this command sees only its kernels)."""
+    import torch
+    import mxfp4_block_quantization_gb300 as mx
+    from mxfp4_block_quantization_gb300 import workloads as W
+    g = W.moe_grouped(seed=2, device="cuda")
+    T, K = g.x_tokens.shape
+    total = g.row_index.numel()
+    E = g.num_experts
+    codes = torch.empty((total, K // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(mx.mxfp4_grouped_scale_bytes_bound(total, E, K), dtype=torch.uint8,
+                         device="cuda")
+    sro = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    st = torch.empty(1, dtype=torch.int32, device="cuda")
+    ws_bytes = {"gather_ws": lambda: mx.mxfp4_gather_workspace_bytes(T, total, E, K),
+                "scatter_ws": lambda: mx.mxfp4_scatter_workspace_bytes(T, total, E, K)}
+    ws = (torch.empty(ws_bytes[args.call](), dtype=torch.uint8, device="cuda")
+          if args.call in ws_bytes else None)
+    fn = {
+        "gather": lambda: mx.mxfp4_quantize_grouped_gather(g.x_tokens, g.row_index, g.offsets,
+                                                           codes, scales, sro, st),
+        "gather_ws": lambda: mx.mxfp4_quantize_grouped_gather_ws(
+            g.x_tokens, g.row_index, g.offsets, ws, codes, scales, sro, st),
+        "scatter": lambda: mx.mxfp4_quantize_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets,
+                                                             total, codes, scales, sro, st),
+        "scatter_ws": lambda: mx.mxfp4_quantize_grouped_scatter_ws(
+            g.x_tokens, g.dest_rows, g.offsets, total, ws, codes, scales, sro, st),
+    }[args.call]
+    fn()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.reps):
+        fn()
+    t1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"call": args.call, "reps": args.reps, "status": int(st.item()),
+                      "us_per_call": round(t0.elapsed_time(t1) * 1e3 / args.reps, 2)}))
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -735,6 +781,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--call", choices=DISPATCH_CALLS,
+                    help="only time this dispatch call on the MoE batch (for profiling)")
+    ap.add_argument("--reps", type=int, default=5, help="repetitions of --call")
     ap.add_argument("--settle", type=float, default=1.0,
                     help="seconds of untimed launches after the warm-up steps (clock settling)")
     args = ap.parse_args(argv)
@@ -742,6 +791,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.call:
+        return run_one_call(args)
     return run_ours(args)
 
 

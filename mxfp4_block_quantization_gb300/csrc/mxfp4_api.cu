@@ -689,6 +689,7 @@ int mxfp4_version(void) { return 100; }
 int64_t mxfp4_debug_bounds_violations(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return -1;
   return static_cast<int64_t>(mxfp4::debug_violations_quantize()) +
+         mxfp4::debug_violations_dispatch() +
          mxfp4::debug_violations_dequantize() + mxfp4::debug_violations_nvfp4() +
          mxfp4::debug_violations_swap();
 }

@@ -297,6 +297,12 @@ __device__ __forceinline__ uint32_t f16_bits_to_f32_bits(uint32_t h) {
 // arguments.  An access outside its range is skipped (a skipped load yields
 // zeros) and counted in a per-translation-unit device counter; nothing
 // traps.  In the normal build the checks compile away.
+// 256-bit loads need every lane address 32-byte aligned: the base and the
+// row stride (the column offsets are multiples of 32 bytes).
+inline bool vec32_ok(const void* x, int64_t ldx_bytes) {
+  return (reinterpret_cast<uintptr_t>(x) % 32 == 0) && (ldx_bytes % 32 == 0);
+}
+
 struct DebugRanges {
   uintptr_t lo[8];
   uintptr_t hi[8];

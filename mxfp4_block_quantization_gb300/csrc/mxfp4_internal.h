@@ -111,6 +111,7 @@ int sm_count();
 // Bounds build: out-of-range accesses counted by each translation unit since
 // the last read (reading resets the counter).
 unsigned int debug_violations_quantize();
+unsigned int debug_violations_dispatch();
 unsigned int debug_violations_dequantize();
 unsigned int debug_violations_nvfp4();
 unsigned int debug_violations_swap();

@@ -16,11 +16,10 @@
 // form one 32-element block, reduced with one xor-shuffle.  All four passes'
 // loads are issued before any compute (32 KB in flight per CTA, four to five
 // CTAs per SM).  The fused-gather variant (quantize_gather_kernel) keeps one
-// 128-row tile per CTA but walks a chunk of k-tiles; the scatter variant
-// (quantize_scatter_kernel) gives each warp one token row, read once, whose
-// codes and scale words go to all the rows its routes land on.  Launches use
-// programmatic dependent launch, so a grid is already resident when its
-// predecessor in the stream drains.
+// 128-row tile per CTA but walks a chunk of k-tiles; the scatter forms, one
+// warp per token row, are in dispatch.cu.  Launches use programmatic
+// dependent launch, so a grid is already resident when its predecessor in the
+// stream drains.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -63,11 +62,9 @@ struct QuantizeParams {
 #endif
 };
 
+
 // Buffer slots of QuantizeParams::dbg.
-enum : int {
-  kDbgX = 0, kDbgCodes, kDbgScales, kDbgOffsets, kDbgPadded, kDbgRowIndex, kDbgStatus,
-  kDbgWork  // the inverse-map workspace of the gather-through-scatter path
-};
+enum : int { kDbgX = 0, kDbgCodes, kDbgScales, kDbgOffsets, kDbgPadded, kDbgRowIndex, kDbgStatus };
 
 // Lane l of warp w covers elements [16*(l%8), 16*(l%8)+16) of row
 // 4*w + l/8 (+32 per pass): two lanes per 32-element block.
@@ -246,524 +243,6 @@ __global__ void __launch_bounds__(kGatherThreads) quantize_gather_kernel(const Q
   }
 }
 
-// Fused dispatch scatter: route j of token t lands on row dest_rows[t][j] of
-// the expert-sorted batch.  The first E CTAs zero the scale bytes of expert
-// e's pad rows.  In every other CTA each warp owns one token: lanes 0..top_k-1
-// resolve the token's routes (code row, padded scale row from the route's
-// segment) once, then the warp streams the token row in passes of 512
-// elements (lane = 16 elements, 32 bytes), kScatterBatch passes' loads in
-// flight at a time, quantizes each pass once and stores it to every
-// destination: per route one contiguous 256-byte run of codes (two full
-// lines) and, from lanes 0, 8, 16, 24, the 4-byte scale word of each of the
-// pass's four k-tiles.  Each destination row's codes thus leave the SM as one
-// contiguous stream; DRAM traffic is the algorithmic one (token rows read
-// once, every output byte written once).  The scale words are stored with an
-// L2 evict-last policy: a 16-byte group of the tiled layout holds the words
-// of four rows 32 apart, which different warps write at different times, and
-// the codes stream past them (evict-first) in the meantime.
-constexpr int kScatterWarps = kThreads / 32;  // tokens per CTA
-constexpr int kScatterBatch = 4;              // passes with loads in flight together
-constexpr int kScatterPass = 32 * kElems;     // elements per warp pass (4 k-tiles)
-
-constexpr int kInvertThreads = 256;
-constexpr int kSmemSegs = 2048;  // up to this many segments are searched in shared memory
-
-// Row -> padded row for the per-row map kernels.  With E <= cap the
-// offsets and padded starts are copied to shared memory once per CTA (every
-// thread of the block must call the constructor: it has a barrier) and each
-// row's segment is a binary search there; otherwise find_segment on global
-// memory.
-struct SegmentSearch {
-  int32_t* s_off;
-  int32_t* s_pad;
-  const int32_t* off;
-  const int32_t* pad;
-  int E;
-  int total;
-  bool smem;
-  // s_off and s_pad hold cap + 1 entries each
-  __device__ SegmentSearch(int32_t* so, int32_t* sp, const int32_t* o, const int32_t* pd, int e,
-                           int tot, int cap = kSmemSegs)
-      : s_off(so), s_pad(sp), off(o), pad(pd), E(e), total(tot), smem(e <= cap) {
-    if (smem)
-      for (int i = threadIdx.x; i <= E; i += blockDim.x) {
-        s_off[i] = __ldg(off + i);
-        s_pad[i] = __ldg(pad + i);
-      }
-    __syncthreads();
-  }
-  __device__ int rows_of(int e) const {  // n_e
-    return smem ? s_off[e + 1] - s_off[e] : __ldg(off + e + 1) - __ldg(off + e);
-  }
-  __device__ int padded_start(int e) const { return smem ? s_pad[e] : __ldg(pad + e); }
-  __device__ int padded_row(int v) const {  // v in [0, total)
-    if (!smem) {
-      const int e = find_segment(off, E, v, total);
-      return __ldg(pad + e) + (v - __ldg(off + e));
-    }
-    int lo = 0, hi = E - 1;  // the largest e with o[e] <= v: its segment is not empty
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_off[mid] <= v) lo = mid; else hi = mid - 1;
-    }
-    return s_pad[lo] + (v - s_off[lo]);
-  }
-};
-
-struct ScatterParams {
-  const uint8_t* __restrict__ x;          // BF16 token rows
-  int64_t ldx_bytes;                      // token row stride in bytes
-  int64_t num_tokens;
-  const int32_t* __restrict__ dest_rows;  // token-major: [num_tokens, top_k] row of every route,
-                                          //   -1 = none; bucket mode: [num_tokens, kBucket]
-  const int32_t* __restrict__ count;      // NULL: token-major; else bucket mode: warp t < T
-                                          //   takes rows dest_rows[t*kBucket ..] of count[t]
-  const int32_t* __restrict__ ovf_n;      //   (at most kBucket), warps past T walk the
-  const int32_t* __restrict__ ovf_row;    //   overflow list: ovf_row[j] of token ovf_tok[j],
-  const int32_t* __restrict__ ovf_tok;    //   j < *ovf_n, n_ovf_warps warps in all
-  int32_t n_ovf_warps;
-  int32_t top_k;
-  int32_t E;
-  int64_t total_rows;                     // rows of the expert-sorted batch
-  int64_t code_ld;                        // K/2
-  uint8_t* __restrict__ codes;
-  uint8_t* __restrict__ scales;
-  const int32_t* __restrict__ offsets;    // [E+1] row offsets of the segments
-  const int32_t* __restrict__ padded;     // [E+1] padded row starts
-  int32_t* status;                        // may be NULL
-  uint32_t* __restrict__ stage;           // kStaged: [num_tokens, stage_ld(nKT)] scale words
-                                          //   of every token, tiled by tile_scales_kernel
-  int32_t pad_ctas;                       // leading CTAs that zero pad scale rows (E or 0)
-  int32_t sK;
-  int32_t nKT;
-  int32_t map_ctas;                       // kStaged, token-major: the next CTAs write tok1,
-  int32_t* __restrict__ tok1;             //   the token + 1 of every padded row (-1: pad row)
-#ifdef MXFP4_DEBUG_BOUNDS
-  DebugRanges dbg;                        // slots as in QuantizeParams (kDbgRowIndex: dest_rows)
-#endif
-};
-
-// Row stride, in 4-byte words, of the staged per-token scale words: nKT
-// rounded up to 16 bytes so that the tile kernel reads them as uint4.
-__host__ __device__ __forceinline__ int64_t stage_ld(int nKT) { return (nKT + 3) & ~3; }
-
-// Byte offset of the scale word (4 scale columns of one k-tile) of padded row
-// `prow` in k-tile 0; k-tile kt adds kt * 512.
-__device__ __forceinline__ int64_t scale_word_base(int prow, int nKT) {
-  return static_cast<int64_t>(prow >> 7) * nKT * kChunkBytes + (prow & 31) * 16 +
-         ((prow & 127) >> 5) * 4;
-}
-
-// One warp: token row t, quantized once, to the nr (<= 32) rows dsts[0..nr).
-template <bool kVec32, bool kF16, bool kStaged>
-__device__ __forceinline__ void scatter_token(const ScatterParams& p, int64_t t,
-                                              const int32_t* dsts, int nr, int warp, int lane,
-                                              int64_t (*s_code)[MXFP4_SCATTER_MAX_TOP_K],
-                                              int64_t (*s_scale)[MXFP4_SCATTER_MAX_TOP_K]) {
-  // routes, one per lane
-  int64_t co = -1, so = -1;
-  bool bad = false;
-  if (lane < nr) {
-    const int32_t* dp = dsts + lane;
-    const int32_t v = MXFP4_IN_BOUNDS(p, kDbgRowIndex, dp, 4) ? __ldg(dp) : -1;
-    if (v >= 0 && v < p.total_rows) {
-      co = static_cast<int64_t>(v) * p.code_ld;
-      if constexpr (!kStaged) {
-        const int e = find_segment(p.offsets, p.E, v, static_cast<int>(p.total_rows));
-        so = scale_word_base(__ldg(p.padded + e) + (v - __ldg(p.offsets + e)), p.nKT);
-      }
-    } else {
-      bad = v != -1;
-    }
-  }
-  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && p.status != nullptr &&
-      MXFP4_IN_BOUNDS(p, kDbgStatus, p.status, 4))
-    atomicExch(p.status, MXFP4_EINDEX);
-  s_code[warp][lane] = co;
-  // staged: no per-route scale words; slot 0 holds the token's stage row instead
-  s_scale[warp][lane] = kStaged ? reinterpret_cast<int64_t>(p.stage + t * stage_ld(p.nKT)) : so;
-  __syncwarp();
-
-  const uint8_t* xrow = p.x + t * p.ldx_bytes + lane * (kElems * 2);
-  const int n_pass = (p.sK + 15) / 16;  // 16 blocks per pass
-  const uint64_t keep = l2_evict_last_policy();
-  for (int p0 = 0; p0 < n_pass; p0 += kScatterBatch) {
-    uint4 v[kScatterBatch][2];
-#pragma unroll
-    for (int b = 0; b < kScatterBatch; ++b) {
-      v[b][0] = v[b][1] = make_uint4(0u, 0u, 0u, 0u);
-      const int pass = p0 + b;
-      const uint8_t* xp = xrow + static_cast<int64_t>(pass) * (kScatterPass * 2);
-      if (pass < n_pass && pass * 16 + (lane >> 1) < p.sK &&
-          MXFP4_IN_BOUNDS(p, kDbgX, xp, 32))
-        load32<kVec32>(xp, v[b]);
-    }
-    uint2 code[kScatterBatch];
-    uint32_t word[kScatterBatch];
-#pragma unroll
-    for (int b = 0; b < kScatterBatch; ++b) {
-      const uint32_t s = lane_block_scale<kF16>(v[b]);
-      code[b] = lane_codes<kF16>(v[b], s);
-      // scale word of k-tile (p0+b)*4 + lane/8: the s of lanes +0, +2, +4, +6
-      word[b] = s | (__shfl_down_sync(0xFFFFFFFFu, s, 2) << 8) |
-                (__shfl_down_sync(0xFFFFFFFFu, s, 4) << 16) |
-                (__shfl_down_sync(0xFFFFFFFFu, s, 6) << 24);
-    }
-    const int64_t cofs = static_cast<int64_t>(p0) * (kScatterPass / 2) + lane * (kElems / 2);
-    const int kt0 = p0 * 4 + (lane >> 3);
-    if (kStaged && (lane & 7) == 0) {
-      // the token's words once (every warp of a token stores the same values)
-      uint32_t* const srow = reinterpret_cast<uint32_t*>(s_scale[warp][0]);
-#pragma unroll
-      for (int b = 0; b < kScatterBatch; ++b) {
-        const int kt = kt0 + 4 * b;
-        uint32_t* const sp = srow + kt;
-        if (kt < p.nKT && MXFP4_IN_BOUNDS(p, kDbgWork, sp, 4)) st_keep_u32(sp, word[b], keep);
-      }
-    }
-    for (int j = 0; j < nr; ++j) {
-      const int64_t c = s_code[warp][j];
-      const int64_t w = s_scale[warp][j];
-#pragma unroll
-      for (int b = 0; b < kScatterBatch; ++b) {
-        const int pass = p0 + b;
-        uint8_t* const cp = p.codes + c + cofs + b * (kScatterPass / 2);
-        if (c >= 0 && pass * 16 + (lane >> 1) < p.sK && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 8))
-          st_stream_v2(cp, code[b]);
-        if constexpr (!kStaged) {
-          const int kt = kt0 + 4 * b;
-          uint8_t* const wp = p.scales + w + static_cast<int64_t>(kt) * kChunkBytes;
-          if (w >= 0 && (lane & 7) == 0 && kt < p.nKT && MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4))
-            st_keep_u32(wp, word[b], keep);
-        }
-      }
-    }
-  }
-  __syncwarp();  // s_code / s_scale are rewritten by the warp's next token
-}
-
-// Map CTA m of the staged token-major scatter: the token + 1 of every padded
-// row a route lands on, and -1 for the pad rows of every segment (rows no
-// route targets keep the 0 of the memset).  The tile kernel reads the map
-// after this launch has completed.  The offsets and padded starts (up to
-// kMapSegs + 1 each) reuse the warps' route arrays s_code and s_scale.
-constexpr int kMapSegs = 511;
-static_assert((kMapSegs + 1) * 4 == kScatterWarps * MXFP4_SCATTER_MAX_TOP_K * 8,
-              "one segment array fills one route array");
-__device__ __forceinline__ void scatter_route_map(const ScatterParams& p, int m, int32_t* s_off,
-                                                  int32_t* s_pad) {
-  const SegmentSearch seg(s_off, s_pad, p.offsets, p.padded, p.E,
-                          static_cast<int>(p.total_rows), kMapSegs);
-  const int64_t gid = static_cast<int64_t>(m) * kThreads + threadIdx.x;
-  const int64_t stride = static_cast<int64_t>(p.map_ctas) * kThreads;
-  // the pad rows: item k is pad slot k % 128 of segment k / 128, so that
-  // consecutive threads store consecutive rows of one segment
-  for (int64_t k = gid; k < static_cast<int64_t>(p.E) * kTileRows; k += stride) {
-    const int e = static_cast<int>(k / kTileRows);
-    const int i = static_cast<int>(k % kTileRows);
-    const int n = seg.rows_of(e);
-    const int npad = (n + kTileRows - 1) / kTileRows * kTileRows - n;
-    if (i >= npad) continue;
-    int32_t* const tp = p.tok1 + seg.padded_start(e) + n + i;
-    if (MXFP4_IN_BOUNDS(p, kDbgWork, tp, 4)) *tp = -1;
-  }
-  const int64_t n_routes = p.num_tokens * p.top_k;
-  for (int64_t i = gid; i < n_routes; i += stride) {
-    const int32_t* dp = p.dest_rows + i;
-    const int32_t v = MXFP4_IN_BOUNDS(p, kDbgRowIndex, dp, 4) ? __ldg(dp) : -1;
-    if (v < 0 || v >= p.total_rows) continue;  // the token warps report bad entries
-    int32_t* const tp = p.tok1 + seg.padded_row(v);
-    if (MXFP4_IN_BOUNDS(p, kDbgWork, tp, 4)) *tp = static_cast<int32_t>(i / p.top_k) + 1;
-  }
-}
-
-// Overflow entry j (bucket mode): its token and row; false past the list.
-__device__ __forceinline__ bool overflow_entry(const ScatterParams& p, int64_t j, int64_t& t,
-                                               const int32_t*& dsts) {
-  if (!MXFP4_IN_BOUNDS(p, kDbgWork, p.ovf_n, 4)) return false;
-  const int64_t n = __ldg(p.ovf_n);
-  if (j >= n || j >= p.total_rows || !MXFP4_IN_BOUNDS(p, kDbgWork, p.ovf_tok + j, 4))
-    return false;
-  t = __ldg(p.ovf_tok + j);
-  dsts = p.ovf_row + j;
-  return true;
-}
-
-template <bool kVec32, bool kF16, bool kStaged>
-__global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_kernel(const ScatterParams p) {
-  __shared__ int64_t s_code[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];   // d * K/2, or -1
-  __shared__ int64_t s_scale[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];  // word base, or -1
-  __shared__ int64_t s_next[kScatterWarps];  // overflow warps: their current entry
-
-  pdl_wait();
-  pdl_release();
-
-  if (!MXFP4_IN_BOUNDS(p, kDbgPadded, p.padded, (p.E + 1) * 4) ||
-      !MXFP4_IN_BOUNDS(p, kDbgOffsets, p.offsets, (p.E + 1) * 4))
-    return;
-  const int total_padded = __ldg(p.padded + p.E);
-  if (total_padded < 0) return;  // rejected offsets
-
-  if (static_cast<int>(blockIdx.x) < p.pad_ctas) {
-    // pad rows [n, ceil128(n)) of expert e: zero scale words, row-fastest
-    const int e = blockIdx.x;
-    const int n = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
-    const int npad = ((n + kTileRows - 1) / kTileRows) * kTileRows - n;
-    const int P0 = __ldg(p.padded + e) + n;
-    const uint64_t keep = l2_evict_last_policy();
-    for (int i = threadIdx.x; i < npad * p.nKT; i += kThreads) {
-      const int kt = i / npad;
-      uint8_t* wp = p.scales + scale_word_base(P0 + (i - kt * npad), p.nKT) + kt * kChunkBytes;
-      if (MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4)) st_keep_u32(wp, 0u, keep);
-    }
-    return;
-  }
-
-  if constexpr (kStaged) {
-    const int m = static_cast<int>(blockIdx.x) - p.pad_ctas;
-    if (m < p.map_ctas) {  // uniform over the block
-      scatter_route_map(p, m, reinterpret_cast<int32_t*>(&s_code[0][0]),
-                        reinterpret_cast<int32_t*>(&s_scale[0][0]));
-      return;
-    }
-  }
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int lead = p.pad_ctas + (kStaged ? p.map_ctas : 0);  // CTAs before the token warps
-  const int64_t w_id = static_cast<int64_t>(blockIdx.x - lead) * kScatterWarps + warp;
-  // whole warps return below; there is no block-wide barrier after this point
-  int64_t t;
-  const int32_t* dsts;
-  int nr;
-  if (p.count == nullptr) {  // token-major: warp = token, top_k routes
-    if (w_id >= p.num_tokens) return;
-    t = w_id;
-    dsts = p.dest_rows + w_id * p.top_k;
-    nr = p.top_k;
-  } else if (w_id < p.num_tokens) {  // bucket mode: the token's first kBucket rows
-    if (!MXFP4_IN_BOUNDS(p, kDbgWork, p.count + w_id, 4)) return;
-    const int c = __ldg(p.count + w_id);
-    if (c <= 0) return;
-    t = w_id;
-    dsts = p.dest_rows + w_id * MXFP4_SCATTER_MAX_TOP_K;
-    nr = c < MXFP4_SCATTER_MAX_TOP_K ? c : MXFP4_SCATTER_MAX_TOP_K;
-  } else {  // bucket mode: the overflow list, one row per entry, warp-strided
-    const int64_t j = w_id - p.num_tokens;
-    if (!overflow_entry(p, j, t, dsts)) return;
-    s_next[warp] = j;
-    nr = 1;
-  }
-  for (;;) {
-    scatter_token<kVec32, kF16, kStaged>(p, t, dsts, nr, warp, lane, s_code, s_scale);
-    // only overflow warps go on; their cursor is kept in shared memory so that
-    // nothing stays live across the body above
-    if (p.count == nullptr ||
-        static_cast<int64_t>(blockIdx.x - p.pad_ctas - (kStaged ? p.map_ctas : 0)) *
-                    kScatterWarps + warp < p.num_tokens)
-      return;
-    const int64_t j = s_next[warp] + p.n_ovf_warps;
-    if (!overflow_entry(p, j, t, dsts)) return;
-    __syncwarp();
-    s_next[warp] = j;
-  }
-}
-
-// Tiled scales of the gathered or scattered batch from the staged per-token
-// words: one CTA per padded 128-row tile.  Padded row pr takes the words of
-// token tok1[pr] - 1 (for the gather written by invert_bucket_kernel for row
-// o[e] + pr - P[e] of segment e, for the scatter by the map CTAs of the
-// scatter launch).  In the gather, pad rows and rows whose index is out of
-// range keep tok1 = 0 and get zero words; in the scatter, pad rows are marked
-// -1 and get zero words, and rows that no route targets (0) keep the words
-// they held.  The tile's 128 x nKT words pass through shared memory, 32
-// k-tiles at a time, so that every 512-byte chunk is written whole, 16 bytes
-// per thread, instead of 4-byte words scattered over the chunks.
-struct TileScalesParams {
-  const int32_t* __restrict__ tok1;       // [grid * 128] token + 1 of every padded row, 0: none,
-                                          //   -1: pad row (keep_unset only)
-  const uint32_t* __restrict__ stage;     // [T, stage_ld(nKT)], 16-byte aligned
-  uint8_t* __restrict__ scales;
-  const int32_t* __restrict__ padded;
-  int32_t E;
-  int32_t nKT;
-  int32_t keep_unset;                     // rows with tok1 == 0 keep their scale words (the
-                                          //   scatter leaves untargeted rows untouched)
-#ifdef MXFP4_DEBUG_BOUNDS
-  DebugRanges dbg;  // kDbgScales, kDbgPadded, kDbgRowIndex (tok1), kDbgWork (stage)
-#endif
-};
-
-// 128 threads and 32 k-tiles (17 KB of shared memory) per pass: ten CTAs per
-// SM, so the 1405 tiles of the MoE batch run in one wave.
-constexpr int kTileThreads = 128;
-constexpr int kTileCols = 32;                                  // k-tiles per shared-memory pass
-constexpr int kTileQuadsPerRow = kTileCols / 4;                // 16-byte quads of a row
-constexpr int kTileRowStep = kTileThreads / kTileQuadsPerRow;  // rows per load step
-constexpr int kTileQuads = kTileRows / kTileRowStep;           // uint4 loads per thread
-static_assert(kTileRows % kTileRowStep == 0 && kTileRows <= kTileThreads,
-              "tile_scales_kernel: whole load steps, one token per thread");
-
-__global__ void __launch_bounds__(kTileThreads, 10) tile_scales_kernel(const TileScalesParams p) {
-  __shared__ uint32_t s_w[kTileRows][kTileCols + 1];  // odd stride: conflict-free columns
-  __shared__ int32_t s_tok[kTileRows];
-
-  pdl_wait();
-  pdl_release();
-
-  if (!MXFP4_IN_BOUNDS(p, kDbgPadded, p.padded + p.E, 4)) return;
-  const int pr0 = static_cast<int>(blockIdx.x) * kTileRows;
-  // both loads in flight together: the tile's tokens and the padded total
-  int32_t t1 = 0;
-  if (threadIdx.x < kTileRows) {
-    const int32_t* tp = p.tok1 + pr0 + threadIdx.x;
-    if (MXFP4_IN_BOUNDS(p, kDbgRowIndex, tp, 4)) t1 = __ldg(tp);
-  }
-  const int total_padded = __ldg(p.padded + p.E);
-  if (total_padded < 0 || pr0 >= total_padded) return;  // whole CTA: nothing past P[E]
-  if (threadIdx.x < kTileRows) s_tok[threadIdx.x] = t1 - 1;
-  __syncthreads();
-
-  uint8_t* const tile = p.scales + static_cast<int64_t>(blockIdx.x) * p.nKT * kChunkBytes;
-  const int64_t ld = stage_ld(p.nKT);
-  const int qd = threadIdx.x % kTileQuadsPerRow;  // this thread's quad: words 4qd .. 4qd+3
-  const int rb = threadIdx.x / kTileQuadsPerRow;  // and its rows rb, rb + kTileRowStep, ...
-  for (int c0 = 0; c0 < p.nKT; c0 += kTileCols) {
-    const int cw = p.nKT - c0 < kTileCols ? p.nKT - c0 : kTileCols;
-    const bool in_row = 4 * qd < cw;
-    // every load of the pass in flight before the first shared-memory store
-    uint4 v[kTileQuads];
-#pragma unroll
-    for (int j = 0; j < kTileQuads; ++j) {
-      const int r = rb + kTileRowStep * j;
-      const int32_t t = s_tok[r];  // token, -1: no token, -2: pad row
-      v[j] = make_uint4(0u, 0u, 0u, 0u);
-      if (t >= 0 && in_row) {
-        const uint32_t* sp = p.stage + static_cast<int64_t>(t) * ld + c0 + 4 * qd;
-        if (MXFP4_IN_BOUNDS(p, kDbgWork, sp, 16)) v[j] = __ldg(reinterpret_cast<const uint4*>(sp));
-      } else if (t == -1 && p.keep_unset && in_row) {
-        // an untargeted row keeps its words: read them back (this pass's
-        // chunks are written only after the barrier below)
-        const uint8_t* op = tile + static_cast<int64_t>(c0 + 4 * qd) * kChunkBytes +
-                            (r & 31) * 16 + (r >> 5) * 4;
-        uint32_t w4[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (c0 + 4 * qd + i < p.nKT && MXFP4_IN_BOUNDS(p, kDbgScales, op + i * kChunkBytes, 4))
-            w4[i] = *reinterpret_cast<const uint32_t*>(op + i * kChunkBytes);
-        v[j] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
-    }
-    if (in_row) {
-#pragma unroll
-      for (int j = 0; j < kTileQuads; ++j) {
-        uint32_t* const w = &s_w[rb + kTileRowStep * j][4 * qd];  // words past cw: never read
-        w[0] = v[j].x;
-        w[1] = v[j].y;
-        w[2] = v[j].z;
-        w[3] = v[j].w;
-      }
-    }
-    __syncthreads();
-    // piece (c, o): rows o, o+32, o+64, o+96 of k-tile c0 + c, bytes o*16 of its chunk
-    for (int i = threadIdx.x; i < cw * 32; i += kTileThreads) {
-      const int c = i >> 5;
-      const int o = i & 31;
-      uint8_t* const dp = tile + static_cast<int64_t>(c0 + c) * kChunkBytes + o * 16;
-      if (MXFP4_IN_BOUNDS(p, kDbgScales, dp, 16))
-        st_stream_v4(dp, make_uint4(s_w[o][c], s_w[o + 32][c], s_w[o + 64][c], s_w[o + 96][c]));
-    }
-    __syncthreads();
-  }
-}
-
-// ---------------------------------------------------------------------
-// The fused gather through the scatter path.  One kernel builds the inverse
-// of the row -> token map in a caller-provided workspace: every valid row r of
-// token t takes slot atomicAdd(count[t], 1) of the token's bucket of
-// kBucket rows, or, past kBucket routes, an entry of one overflow list.  The
-// scatter kernel then reads and quantizes every token row once for the rows
-// in its bucket (one warp per token) and once more per overflow entry.  The
-// order of the rows in a bucket is arbitrary (atomics) and does not matter:
-// every route of a token receives the same bytes.
-constexpr int kBucket = MXFP4_SCATTER_MAX_TOP_K;  // rows per token bucket (one warp)
-
-struct InvertParams {
-  const int32_t* __restrict__ row_index;  // [R] token of every row
-  int64_t total_rows;                     // R
-  int64_t num_src_rows;                   // T
-  int32_t* __restrict__ count;            // [T], zero on entry: routes of every token
-  int32_t* __restrict__ ovf_n;            // [1], zero on entry: overflow entries
-  int32_t* __restrict__ bucket;           // [T, kBucket] the first kBucket rows of every token
-  int32_t* __restrict__ ovf_row;          // [R] rows past their token's kBucket-th
-  int32_t* __restrict__ ovf_tok;          // [R] and their tokens
-  int32_t* __restrict__ tok1;             // or NULL; else [padded rows], zero on entry: token + 1
-                                          //   of every padded row with a valid index
-  uint8_t* __restrict__ codes;            // rows with an index out of range are zeroed
-  uint8_t* __restrict__ scales;           //   here: codes, and scale words unless tok1
-  int64_t code_ld;
-  const int32_t* __restrict__ offsets;
-  const int32_t* __restrict__ padded;
-  int32_t E;
-  int32_t nKT;
-  int32_t* status;
-#ifdef MXFP4_DEBUG_BOUNDS
-  DebugRanges dbg;  // kDbgCodes, kDbgScales, kDbgOffsets, kDbgPadded, kDbgRowIndex, kDbgStatus, kDbgWork
-#endif
-};
-
-__global__ void __launch_bounds__(kInvertThreads) invert_bucket_kernel(const InvertParams q) {
-  __shared__ int32_t s_off[kSmemSegs + 1];
-  __shared__ int32_t s_pad[kSmemSegs + 1];
-  pdl_wait();
-  pdl_release();
-  if (!MXFP4_IN_BOUNDS(q, kDbgPadded, q.padded, (q.E + 1) * 4) ||
-      !MXFP4_IN_BOUNDS(q, kDbgOffsets, q.offsets, (q.E + 1) * 4) || __ldg(q.padded + q.E) < 0)
-    return;  // rejected offsets: nothing is written (uniform over the block)
-  const SegmentSearch seg(s_off, s_pad, q.offsets, q.padded, q.E,
-                          static_cast<int>(q.total_rows));
-  bool bad = false;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kInvertThreads;
-  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kInvertThreads + threadIdx.x;
-       r < q.total_rows; r += stride) {
-    const int32_t* ip = q.row_index + r;
-    const int32_t t = MXFP4_IN_BOUNDS(q, kDbgRowIndex, ip, 4) ? __ldg(ip) : -1;
-    const bool valid = t >= 0 && t < q.num_src_rows;
-    if (valid && MXFP4_IN_BOUNDS(q, kDbgWork, q.count + t, 4)) {
-      const int32_t pos = atomicAdd(q.count + t, 1);
-      if (pos < kBucket) {
-        int32_t* const bp = q.bucket + static_cast<int64_t>(t) * kBucket + pos;
-        if (MXFP4_IN_BOUNDS(q, kDbgWork, bp, 4)) *bp = static_cast<int32_t>(r);
-      } else if (MXFP4_IN_BOUNDS(q, kDbgWork, q.ovf_n, 4)) {
-        const int32_t j = atomicAdd(q.ovf_n, 1);  // < R: each row adds at most once
-        if (MXFP4_IN_BOUNDS(q, kDbgWork, q.ovf_row + j, 4) &&
-            MXFP4_IN_BOUNDS(q, kDbgWork, q.ovf_tok + j, 4)) {
-          q.ovf_row[j] = static_cast<int32_t>(r);
-          q.ovf_tok[j] = t;
-        }
-      }
-    }
-    if (valid && q.tok1 == nullptr) continue;
-    const int prow = seg.padded_row(static_cast<int>(r));
-    if (valid) {
-      if (MXFP4_IN_BOUNDS(q, kDbgWork, q.tok1 + prow, 4)) q.tok1[prow] = t + 1;
-      continue;
-    }
-    bad = true;
-    uint8_t* cp = q.codes + r * q.code_ld;
-    for (int64_t i = 0; i < q.code_ld; i += 16)
-      if (MXFP4_IN_BOUNDS(q, kDbgCodes, cp + i, 16))
-        *reinterpret_cast<uint4*>(cp + i) = make_uint4(0u, 0u, 0u, 0u);
-    if (q.tok1 != nullptr) continue;  // the tile kernel writes its zero scale words
-    const int64_t base = scale_word_base(prow, q.nKT);
-    for (int kt = 0; kt < q.nKT; ++kt) {
-      uint8_t* wp = q.scales + base + static_cast<int64_t>(kt) * kChunkBytes;
-      if (MXFP4_IN_BOUNDS(q, kDbgScales, wp, 4)) *reinterpret_cast<uint32_t*>(wp) = 0u;
-    }
-  }
-  if (bad && q.status != nullptr && MXFP4_IN_BOUNDS(q, kDbgStatus, q.status, 4))
-    atomicExch(q.status, MXFP4_EINDEX);
-}
-
 // Validates 0 = o[0] <= o[1] <= ... <= o[E] = total_rows and writes the
 // padded row starts P[e] = sum_{e'<e} ceil(n_e'/128)*128 (P[E] = total).
 // One CTA of kScanThreads threads; a block-wide scan per kScanThreads segments.
@@ -841,11 +320,6 @@ __global__ void __launch_bounds__(kScanThreads) grouped_offsets_kernel(const Off
   if (tid == 0 && status != nullptr) *status = s_bad ? MXFP4_EOFFSETS : MXFP4_OK;
 }
 
-// 256-bit loads need every lane address 32-byte aligned: the base and the
-// row stride (the column offsets are multiples of 32 bytes).
-bool vec32_ok(const void* x, int64_t ldx_bytes) {
-  return (reinterpret_cast<uintptr_t>(x) % 32 == 0) && (ldx_bytes % 32 == 0);
-}
 
 
 }  // namespace
@@ -967,233 +441,6 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
                           : (v32 ? quantize_gather_kernel<true, false>
                                  : quantize_gather_kernel<false, false>);
   return launch_pdl(kernel, static_cast<unsigned>(grid), kGatherThreads, 0, stream, p);
-}
-
-int64_t scatter_workspace_ints(int64_t num_tokens, int64_t total_rows, int64_t E, int64_t K) {
-  return gather_tok_ints(total_rows, E) + gather_stage_ints(num_tokens, K);
-}
-
-cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
-                                            int64_t ldx, const int32_t* dest_rows, int32_t top_k,
-                                            int64_t total_rows, const int32_t* offsets, int32_t E,
-                                            int32_t* workspace, uint8_t* codes, uint8_t* scales,
-                                            int32_t* scale_row_offsets, int32_t* status,
-                                            int64_t bound_tiles, bool f16, cudaStream_t stream) {
-  cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
-  if (err != cudaSuccess || E == 0 || K == 0) return err;
-  // staged: [tok1 PT][stage num_tokens x stage_ld(nKT)] (PT is a multiple of 128)
-  const bool staged = workspace != nullptr && total_rows > 0;
-  const int64_t PT = staged ? gather_tok_ints(total_rows, E) : 0;
-  const int32_t nKT = (static_cast<int32_t>(K / kBlock) + kTileBlocks - 1) / kTileBlocks;
-  int32_t map_ctas = 0;
-  if (staged) {
-    err = cudaMemsetAsync(workspace, 0, static_cast<size_t>(PT) * 4, stream);
-    if (err != cudaSuccess) return err;
-    // the row map (routes and pad rows, about 4 items per thread) runs in the
-    // first CTAs of the scatter launch, beside the token warps
-    const int64_t items = num_tokens * top_k > static_cast<int64_t>(E) * kTileRows
-                              ? num_tokens * top_k
-                              : static_cast<int64_t>(E) * kTileRows;
-    const int64_t need = (items + 4 * kThreads - 1) / (4 * kThreads);
-    map_ctas = static_cast<int32_t>(need < 1 ? 1 : (need < sm_count() ? need : sm_count()));
-  }
-  ScatterParams p{};
-  p.x = static_cast<const uint8_t*>(x);
-  p.ldx_bytes = ldx * 2;
-  p.num_tokens = num_tokens;
-  p.code_ld = K / 2;
-  p.codes = codes;
-  p.scales = scales;
-  p.sK = static_cast<int32_t>(K / kBlock);
-  p.nKT = nKT;
-  p.stage = staged ? reinterpret_cast<uint32_t*>(workspace + PT) : nullptr;
-  p.pad_ctas = staged ? 0 : E;
-  p.map_ctas = map_ctas;
-  p.tok1 = staged ? workspace : nullptr;
-  p.offsets = offsets;
-  p.padded = scale_row_offsets;
-  p.E = E;
-  p.status = status;
-  p.dest_rows = dest_rows;
-  p.top_k = top_k;
-  p.total_rows = total_rows;
-#ifdef MXFP4_DEBUG_BOUNDS
-  debug_range(p.dbg, kDbgX, x, num_tokens > 0 ? ((num_tokens - 1) * ldx + K) * 2 : 0);
-  debug_range(p.dbg, kDbgCodes, codes, total_rows * (K / 2));
-  debug_range(p.dbg, kDbgScales, scales, bound_tiles * p.nKT * kChunkBytes);
-  debug_range(p.dbg, kDbgOffsets, offsets, (static_cast<int64_t>(E) + 1) * 4);
-  debug_range(p.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
-  debug_range(p.dbg, kDbgRowIndex, dest_rows, num_tokens * top_k * 4);
-  debug_range(p.dbg, kDbgStatus, status, status ? 4 : 0);
-  debug_range(p.dbg, kDbgWork, workspace, staged ? (PT + gather_stage_ints(num_tokens, K)) * 4 : 0);
-#endif
-  const int64_t grid =
-      p.pad_ctas + p.map_ctas + (num_tokens + kScatterWarps - 1) / kScatterWarps;
-  const bool v32 = vec32_ok(x, p.ldx_bytes);
-  using Kernel = void (*)(const ScatterParams);
-  static constexpr Kernel kKernels[2][2][2] = {
-      {{quantize_scatter_kernel<false, false, false>, quantize_scatter_kernel<false, false, true>},
-       {quantize_scatter_kernel<false, true, false>, quantize_scatter_kernel<false, true, true>}},
-      {{quantize_scatter_kernel<true, false, false>, quantize_scatter_kernel<true, false, true>},
-       {quantize_scatter_kernel<true, true, false>, quantize_scatter_kernel<true, true, true>}}};
-  if (grid > 0) {
-    err = launch_pdl(kKernels[v32][f16][staged], static_cast<unsigned>(grid), kThreads, 0, stream,
-                     p);
-    if (err != cudaSuccess) return err;
-  }
-  if (!staged || bound_tiles == 0) return cudaSuccess;
-  TileScalesParams ts{};
-  ts.tok1 = workspace;
-  ts.stage = p.stage;
-  ts.scales = scales;
-  ts.padded = scale_row_offsets;
-  ts.E = E;
-  ts.nKT = nKT;
-  ts.keep_unset = 1;
-#ifdef MXFP4_DEBUG_BOUNDS
-  debug_range(ts.dbg, kDbgScales, scales, bound_tiles * ts.nKT * kChunkBytes);
-  debug_range(ts.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
-  debug_range(ts.dbg, kDbgRowIndex, workspace, PT * 4);
-  debug_range(ts.dbg, kDbgWork, p.stage, gather_stage_ints(num_tokens, K) * 4);
-#endif
-  return launch_pdl(tile_scales_kernel, static_cast<unsigned>(bound_tiles), kTileThreads, 0, stream,
-                    ts);
-}
-
-// Workspace of the gather through the scatter path, in int32:
-//   [count T][ovf_n 1][tok1 PT, staged only]  cleared by one memset
-//   [bucket T x kBucket][ovf_row R][ovf_tok R]
-//   [stage T x stage_ld(nKT), staged only]    from the next 16-byte boundary
-int64_t gather_workspace_ints(int64_t num_src_rows, int64_t total_rows) {
-  return num_src_rows * (1 + kBucket) + 1 + 2 * total_rows;
-}
-
-int64_t gather_tok_ints(int64_t total_rows, int64_t E) {
-  return (total_rows + 127 * E) / kTileRows * kTileRows;
-}
-
-int64_t gather_stage_ints(int64_t num_src_rows, int64_t K) {
-  return num_src_rows * stage_ld(static_cast<int>((K / kBlock + kTileBlocks - 1) / kTileBlocks));
-}
-
-cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_t K,
-                                              int64_t ldx, const int32_t* row_index,
-                                              int64_t total_rows, const int32_t* offsets,
-                                              int32_t E, int32_t* workspace, bool staged,
-                                              uint8_t* codes, uint8_t* scales,
-                                              int32_t* scale_row_offsets, int32_t* status,
-                                              int64_t bound_tiles, bool f16, cudaStream_t stream) {
-  cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
-  // no rows: every segment is empty and nothing else is written (the caller
-  // need not pass a workspace then)
-  if (err != cudaSuccess || E == 0 || K == 0 || total_rows == 0) return err;
-  const int64_t T = num_src_rows;
-  const int64_t R = total_rows;
-  const int64_t PT = staged ? gather_tok_ints(R, E) : 0;
-  InvertParams q{};
-  q.row_index = row_index;
-  q.total_rows = R;
-  q.num_src_rows = T;
-  q.count = workspace;
-  q.ovf_n = workspace + T;
-  q.tok1 = staged ? workspace + T + 1 : nullptr;
-  q.bucket = workspace + T + 1 + PT;
-  q.ovf_row = q.bucket + T * kBucket;
-  q.ovf_tok = q.ovf_row + R;
-  q.codes = codes;
-  q.scales = scales;
-  q.code_ld = K / 2;
-  q.offsets = offsets;
-  q.padded = scale_row_offsets;
-  q.E = E;
-  q.nKT = (static_cast<int32_t>(K / kBlock) + kTileBlocks - 1) / kTileBlocks;
-  q.status = status;
-  const int64_t map_ints = (gather_workspace_ints(T, R) + PT + 3) & ~int64_t{3};
-  const int64_t ws_bytes = (map_ints + (staged ? gather_stage_ints(T, K) : 0)) * 4;
-#ifdef MXFP4_DEBUG_BOUNDS
-  debug_range(q.dbg, kDbgCodes, codes, R * (K / 2));
-  debug_range(q.dbg, kDbgScales, scales, bound_tiles * q.nKT * kChunkBytes);
-  debug_range(q.dbg, kDbgOffsets, offsets, (static_cast<int64_t>(E) + 1) * 4);
-  debug_range(q.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
-  debug_range(q.dbg, kDbgRowIndex, row_index, R * 4);
-  debug_range(q.dbg, kDbgStatus, status, status ? 4 : 0);
-  debug_range(q.dbg, kDbgWork, workspace, ws_bytes);
-#endif
-  err = cudaMemsetAsync(workspace, 0, static_cast<size_t>(T + 1 + PT) * 4, stream);
-  if (err != cudaSuccess) return err;
-  const int64_t row_ctas_max = static_cast<int64_t>(sm_count()) * 8;
-  const int64_t need = (R + kInvertThreads - 1) / kInvertThreads;
-  const unsigned row_ctas =
-      static_cast<unsigned>(need < 1 ? 1 : (need < row_ctas_max ? need : row_ctas_max));
-  if ((err = launch_pdl(invert_bucket_kernel, row_ctas, kInvertThreads, 0, stream, q)) !=
-      cudaSuccess)
-    return err;
-  ScatterParams p{};
-  p.x = static_cast<const uint8_t*>(x);
-  p.ldx_bytes = ldx * 2;
-  p.num_tokens = T;
-  p.dest_rows = q.bucket;
-  p.count = q.count;
-  p.ovf_n = q.ovf_n;
-  p.ovf_row = q.ovf_row;
-  p.ovf_tok = q.ovf_tok;
-  p.top_k = 0;
-  p.E = E;
-  p.total_rows = R;
-  p.code_ld = K / 2;
-  p.codes = codes;
-  p.scales = scales;
-  p.offsets = offsets;
-  p.padded = scale_row_offsets;
-  p.status = status;
-  p.stage = staged ? reinterpret_cast<uint32_t*>(workspace + map_ints) : nullptr;
-  p.pad_ctas = staged ? 0 : E;
-  p.sK = static_cast<int32_t>(K / kBlock);
-  p.nKT = q.nKT;
-  // one warp per token, then up to one CTA per SM of warps for the overflow
-  // list (the token CTAs' spare warps walk it too)
-  const int64_t token_ctas = (T + kScatterWarps - 1) / kScatterWarps;
-  const int64_t ovf_need = (R + kScatterWarps - 1) / kScatterWarps;
-  const int64_t ovf_ctas = ovf_need < sm_count() ? ovf_need : sm_count();
-  p.n_ovf_warps = static_cast<int32_t>((token_ctas + ovf_ctas) * kScatterWarps - T);
-#ifdef MXFP4_DEBUG_BOUNDS
-  debug_range(p.dbg, kDbgX, x, T > 0 ? ((T - 1) * ldx + K) * 2 : 0);
-  debug_range(p.dbg, kDbgCodes, codes, R * (K / 2));
-  debug_range(p.dbg, kDbgScales, scales, bound_tiles * p.nKT * kChunkBytes);
-  debug_range(p.dbg, kDbgOffsets, offsets, (static_cast<int64_t>(E) + 1) * 4);
-  debug_range(p.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
-  debug_range(p.dbg, kDbgRowIndex, q.bucket, (T * kBucket + R) * 4);  // buckets + ovf_row
-  debug_range(p.dbg, kDbgStatus, status, status ? 4 : 0);
-  debug_range(p.dbg, kDbgWork, workspace, ws_bytes);
-#else
-  (void)ws_bytes;
-#endif
-  const int64_t grid = p.pad_ctas + token_ctas + ovf_ctas;
-  const bool v32 = vec32_ok(x, p.ldx_bytes);
-  using Kernel = void (*)(const ScatterParams);
-  static constexpr Kernel kKernels[2][2][2] = {
-      {{quantize_scatter_kernel<false, false, false>, quantize_scatter_kernel<false, false, true>},
-       {quantize_scatter_kernel<false, true, false>, quantize_scatter_kernel<false, true, true>}},
-      {{quantize_scatter_kernel<true, false, false>, quantize_scatter_kernel<true, false, true>},
-       {quantize_scatter_kernel<true, true, false>, quantize_scatter_kernel<true, true, true>}}};
-  err = launch_pdl(kKernels[v32][f16][staged], static_cast<unsigned>(grid), kThreads, 0, stream,
-                   p);
-  if (err != cudaSuccess || !staged || bound_tiles == 0) return err;
-  TileScalesParams ts{};
-  ts.tok1 = q.tok1;
-  ts.stage = p.stage;
-  ts.scales = scales;
-  ts.padded = scale_row_offsets;
-  ts.E = E;
-  ts.nKT = q.nKT;
-#ifdef MXFP4_DEBUG_BOUNDS
-  debug_range(ts.dbg, kDbgScales, scales, bound_tiles * ts.nKT * kChunkBytes);
-  debug_range(ts.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
-  debug_range(ts.dbg, kDbgRowIndex, q.tok1, PT * 4);
-  debug_range(ts.dbg, kDbgWork, p.stage, T * stage_ld(ts.nKT) * 4);
-#endif
-  return launch_pdl(tile_scales_kernel, static_cast<unsigned>(bound_tiles), kTileThreads, 0, stream,
-                    ts);
 }
 
 #ifdef MXFP4_DEBUG_BOUNDS
