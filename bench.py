@@ -232,10 +232,25 @@ def cpu_baseline(xb, min_seconds=2.0, max_reps=20):
         if el >= min_seconds or reps >= max_reps:
             break
     gbs = quant_bytes(M, K) * reps / el / 1e9
+    # the same oracle on one core, on the first 512 rows
+    rows = min(M, 512)
+    x1 = np.ascontiguousarray(xb[:rows])
+    oracle.quantize(x1)
+    reps1, t1 = 0, time.perf_counter()
+    while True:
+        oracle.quantize(x1)
+        reps1 += 1
+        el1 = time.perf_counter() - t1
+        if el1 >= min_seconds / 2 or reps1 >= 4 * max_reps:
+            break
+    gbs1 = quant_bytes(rows, K) * reps1 / el1 / 1e9
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": used, "kind": "oracle",
             "sample": f"full {M}x{K} dense activation matrix x {reps} passes "
                       f"({el:.2f} s wall, {el * used:.1f} core-s), oracle split into "
-                      f"128-row partitions over {used} host threads"}
+                      f"128-row partitions over {used} host threads",
+            "single_core": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                            "sample": f"first {rows} rows x {reps1} passes ({el1:.2f} s), "
+                                      "one thread"}}
 
 
 # ---------------------------------------------------------- reference arm
