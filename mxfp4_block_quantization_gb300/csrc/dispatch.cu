@@ -366,14 +366,12 @@ __global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_ke
 // per thread, instead of 4-byte words scattered over the chunks.
 struct TileScalesParams {
   const int32_t* __restrict__ tok1;       // [grid * 128] token + 1 of every padded row, 0: none,
-                                          //   -1: pad row (keep_unset only)
+                                          //   -1: pad row (kKeep only)
   const uint32_t* __restrict__ stage;     // [T, stage_ld(nKT)], 16-byte aligned
   uint8_t* __restrict__ scales;
   const int32_t* __restrict__ padded;
   int32_t E;
   int32_t nKT;
-  int32_t keep_unset;                     // rows with tok1 == 0 keep their scale words (the
-                                          //   scatter leaves untargeted rows untouched)
 #ifdef MXFP4_DEBUG_BOUNDS
   DebugRanges dbg;  // kDbgScales, kDbgPadded, kDbgRowIndex (tok1), kDbgWork (stage)
 #endif
@@ -389,9 +387,13 @@ constexpr int kTileQuads = kTileRows / kTileRowStep;           // uint4 loads pe
 static_assert(kTileRows % kTileRowStep == 0 && kTileRows <= kTileThreads,
               "tile_scales_kernel: whole load steps, one token per thread");
 
+// kKeep: rows with tok1 == 0 keep their words (the scatter); otherwise they
+// get zero words like pad rows (the gather).
+template <bool kKeep>
 __global__ void __launch_bounds__(kTileThreads, 10) tile_scales_kernel(const TileScalesParams p) {
   __shared__ uint32_t s_w[kTileRows][kTileCols + 1];  // odd stride: conflict-free columns
   __shared__ int32_t s_tok[kTileRows];
+  __shared__ const uint32_t* s_row[kTileRows];        // the row's staged words, or NULL
 
   pdl_wait();
   pdl_release();
@@ -406,11 +408,14 @@ __global__ void __launch_bounds__(kTileThreads, 10) tile_scales_kernel(const Til
   }
   const int total_padded = __ldg(p.padded + p.E);
   if (total_padded < 0 || pr0 >= total_padded) return;  // whole CTA: nothing past P[E]
-  if (threadIdx.x < kTileRows) s_tok[threadIdx.x] = t1 - 1;
+  if (threadIdx.x < kTileRows) {
+    s_tok[threadIdx.x] = t1 - 1;
+    s_row[threadIdx.x] =
+        t1 > 0 ? p.stage + static_cast<int64_t>(t1 - 1) * stage_ld(p.nKT) : nullptr;
+  }
   __syncthreads();
 
   uint8_t* const tile = p.scales + static_cast<int64_t>(blockIdx.x) * p.nKT * kChunkBytes;
-  const int64_t ld = stage_ld(p.nKT);
   const int qd = threadIdx.x % kTileQuadsPerRow;  // this thread's quad: words 4qd .. 4qd+3
   const int rb = threadIdx.x / kTileQuadsPerRow;  // and its rows rb, rb + kTileRowStep, ...
   for (int c0 = 0; c0 < p.nKT; c0 += kTileCols) {
@@ -421,12 +426,12 @@ __global__ void __launch_bounds__(kTileThreads, 10) tile_scales_kernel(const Til
 #pragma unroll
     for (int j = 0; j < kTileQuads; ++j) {
       const int r = rb + kTileRowStep * j;
-      const int32_t t = s_tok[r];  // token, -1: no token, -2: pad row
+      const uint32_t* const rp = s_row[r];
       v[j] = make_uint4(0u, 0u, 0u, 0u);
-      if (t >= 0 && in_row) {
-        const uint32_t* sp = p.stage + static_cast<int64_t>(t) * ld + c0 + 4 * qd;
+      if (rp != nullptr && in_row) {
+        const uint32_t* sp = rp + c0 + 4 * qd;
         if (MXFP4_IN_BOUNDS(p, kDbgWork, sp, 16)) v[j] = __ldg(reinterpret_cast<const uint4*>(sp));
-      } else if (t == -1 && p.keep_unset && in_row) {
+      } else if (kKeep && in_row && s_tok[r] == -1) {
         // an untargeted row keeps its words: read them back (this pass's
         // chunks are written only after the barrier below)
         const uint8_t* op = tile + static_cast<int64_t>(c0 + 4 * qd) * kChunkBytes +
@@ -632,15 +637,14 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
   ts.padded = scale_row_offsets;
   ts.E = E;
   ts.nKT = nKT;
-  ts.keep_unset = 1;
 #ifdef MXFP4_DEBUG_BOUNDS
   debug_range(ts.dbg, kDbgScales, scales, bound_tiles * ts.nKT * kChunkBytes);
   debug_range(ts.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
   debug_range(ts.dbg, kDbgRowIndex, workspace, PT * 4);
   debug_range(ts.dbg, kDbgWork, p.stage, gather_stage_ints(num_tokens, K) * 4);
 #endif
-  return launch_pdl(tile_scales_kernel, static_cast<unsigned>(bound_tiles), kTileThreads, 0, stream,
-                    ts);
+  return launch_pdl(tile_scales_kernel<true>, static_cast<unsigned>(bound_tiles), kTileThreads, 0,
+                    stream, ts);
 }
 
 // Workspace of the gather through the scatter path, in int32:
@@ -775,8 +779,8 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   debug_range(ts.dbg, kDbgRowIndex, q.tok1, PT * 4);
   debug_range(ts.dbg, kDbgWork, p.stage, T * stage_ld(ts.nKT) * 4);
 #endif
-  return launch_pdl(tile_scales_kernel, static_cast<unsigned>(bound_tiles), kTileThreads, 0, stream,
-                    ts);
+  return launch_pdl(tile_scales_kernel<false>, static_cast<unsigned>(bound_tiles), kTileThreads,
+                    0, stream, ts);
 }
 
 #ifdef MXFP4_DEBUG_BOUNDS
