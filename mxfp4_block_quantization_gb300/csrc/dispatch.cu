@@ -567,16 +567,19 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
                                             int32_t* workspace, uint8_t* codes, uint8_t* scales,
                                             int32_t* scale_row_offsets, int32_t* status,
                                             int64_t bound_tiles, bool f16, cudaStream_t stream) {
-  cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
-  if (err != cudaSuccess || E == 0 || K == 0) return err;
   // staged: [tok1 PT][stage num_tokens x stage_ld(nKT)] (PT is a multiple of 128)
-  const bool staged = workspace != nullptr && total_rows > 0;
+  const bool staged = workspace != nullptr && total_rows > 0 && E > 0 && K > 0;
   const int64_t PT = staged ? gather_tok_ints(total_rows, E) : 0;
+  cudaError_t err = cudaSuccess;
+  if (staged) {  // first, so that the kernels below follow one another directly
+    err = cudaMemsetAsync(workspace, 0, static_cast<size_t>(PT) * 4, stream);
+    if (err != cudaSuccess) return err;
+  }
+  err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
+  if (err != cudaSuccess || E == 0 || K == 0) return err;
   const int32_t nKT = (static_cast<int32_t>(K / kBlock) + kTileBlocks - 1) / kTileBlocks;
   int32_t map_ctas = 0;
   if (staged) {
-    err = cudaMemsetAsync(workspace, 0, static_cast<size_t>(PT) * 4, stream);
-    if (err != cudaSuccess) return err;
     // the row map (routes and pad rows, about 4 items per thread) runs in the
     // first CTAs of the scatter launch, beside the token warps
     const int64_t items = num_tokens * top_k > static_cast<int64_t>(E) * kTileRows
@@ -670,13 +673,19 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
                                               uint8_t* codes, uint8_t* scales,
                                               int32_t* scale_row_offsets, int32_t* status,
                                               int64_t bound_tiles, bool f16, cudaStream_t stream) {
-  cudaError_t err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
-  // no rows: every segment is empty and nothing else is written (the caller
-  // need not pass a workspace then)
-  if (err != cudaSuccess || E == 0 || K == 0 || total_rows == 0) return err;
   const int64_t T = num_src_rows;
   const int64_t R = total_rows;
   const int64_t PT = staged ? gather_tok_ints(R, E) : 0;
+  // no rows: every segment is empty and nothing but the offsets is written
+  // (the caller need not pass a workspace then)
+  const bool work = E > 0 && K > 0 && R > 0;
+  cudaError_t err = cudaSuccess;
+  if (work) {  // first, so that the kernels below follow one another directly
+    err = cudaMemsetAsync(workspace, 0, static_cast<size_t>(T + 1 + PT) * 4, stream);
+    if (err != cudaSuccess) return err;
+  }
+  err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
+  if (err != cudaSuccess || !work) return err;
   InvertParams q{};
   q.row_index = row_index;
   q.total_rows = R;
@@ -706,8 +715,6 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   debug_range(q.dbg, kDbgStatus, status, status ? 4 : 0);
   debug_range(q.dbg, kDbgWork, workspace, ws_bytes);
 #endif
-  err = cudaMemsetAsync(workspace, 0, static_cast<size_t>(T + 1 + PT) * 4, stream);
-  if (err != cudaSuccess) return err;
   const int64_t row_ctas_max = static_cast<int64_t>(sm_count()) * 8;
   const int64_t need = (R + kInvertThreads - 1) / kInvertThreads;
   const unsigned row_ctas =
