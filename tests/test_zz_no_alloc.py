@@ -55,3 +55,16 @@ def test_noalloc_gather_two_calls_match_the_gather_entry_point():
         assert int(got[3].item()) == int(ref[3].item()) == mx.MXFP4_OK
         for a, b in zip(got, ref):
             assert torch.equal(a, b), seed
+        # out-of-range indices: zero rows and MXFP4_EINDEX in both modes
+        bad = g.row_index.clone()
+        bad[::97] = -1
+        bad[5] = tokens
+        ref = _outputs(mx, total, K, E)
+        _call(L.mxfp4_quantize_grouped_gather, g.x_tokens, bad, g.offsets, ref)
+        got = _outputs(mx, total, K, E)
+        assert _call(L.mxfp4_quantize_grouped_gather_noalloc, g.x_tokens, bad, g.offsets,
+                     got) == mx.MXFP4_OK
+        torch.cuda.synchronize()
+        assert int(got[3].item()) == int(ref[3].item()) == mx.MXFP4_EINDEX
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b), seed
