@@ -486,6 +486,16 @@ def test_grouped_scatter_empty_experts_and_no_tokens(mx, scatter_ws):
     assert_scatter_parity(gpu, orc)
 
 
+def test_grouped_scatter_more_experts_than_shared_memory_holds(mx, scatter_ws):
+    """600 experts (most of them empty at 900 routes): above the 511 segments
+    the staged form's map CTAs keep in shared memory, so they search the
+    offsets in global memory."""
+    g = W.moe_grouped(seed=31, tokens=300, top_k=3, num_experts=600, K=96, device="cuda")
+    gpu, orc = run_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, g.row_index.numel(), seed=31,
+                           ws=scatter_ws)
+    assert_scatter_parity(gpu, orc)
+
+
 def test_grouped_scatter_bad_entries(mx, scatter_ws):
     g = W.moe_grouped(seed=7, tokens=140, top_k=2, num_experts=3, K=64, device="cuda")
     total = g.row_index.numel()
@@ -1144,6 +1154,15 @@ def test_gather_ws_bad_index_heavy_and_unused_tokens(mx):
     assert got[3] == mx.MXFP4_EINDEX
     _gather_oracle_check(got, bits(xt), idx, off, 64)
     assert not got[0][[5, 17, 250]].any()
+
+
+def test_gather_ws_more_experts_than_shared_memory_holds(mx):
+    """3000 experts: above the 2048 segments the map kernel keeps in shared
+    memory, so every row's segment is searched in global memory."""
+    g = W.moe_grouped(seed=32, tokens=400, top_k=5, num_experts=3000, K=64, device="cuda")
+    _gather_oracle_check(run_gather_ws(mx, g.x_tokens, g.row_index, g.offsets),
+                         bits(g.x_tokens), g.token_of_row.numpy().astype(np.int32),
+                         g.offsets.cpu().numpy(), 64)
 
 
 def test_gather_ws_long_overflow_list(mx):
