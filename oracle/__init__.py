@@ -110,6 +110,11 @@ def lib():
         L.orc_nvfp4_quantize_grouped_f16.restype = ctypes.c_int
         L.orc_nvfp4_quantize_grouped_f16.argtypes = [_u16p, _i64, _i64, _i32p, ctypes.c_int32,
                                                      _f32p, _u8p, _u8p, _i32p]
+        for name in ("orc_nvfp4_quantize_grouped_scatter",
+                     "orc_nvfp4_quantize_grouped_scatter_f16"):
+            getattr(L, name).restype = ctypes.c_int
+            getattr(L, name).argtypes = [_u16p, _i64, _i64, _i64, _i32p, ctypes.c_int32, _i64,
+                                         _i32p, ctypes.c_int32, _f32p, _u8p, _u8p, _i32p]
         L.orc_quantize_grouped_scatter.restype = ctypes.c_int
         L.orc_quantize_grouped_scatter.argtypes = [_u16p, _i64, _i64, _i64, _i32p, ctypes.c_int32,
                                                    _i64, _i32p, ctypes.c_int32, _u8p, _u8p, _i32p]
@@ -487,6 +492,37 @@ def nvfp4_quantize_grouped(xbits: np.ndarray, offsets: np.ndarray, g: np.ndarray
     fn = lib().orc_nvfp4_quantize_grouped_f16 if f16 else lib().orc_nvfp4_quantize_grouped
     rc = fn(_p(x, _u16p), total, K, _p(off, _i32p), E, _p(gs, _f32p), _p(codes, _u8p),
             _p(scales, _u8p), _p(sro, _i32p))
+    return rc, codes, scales, sro
+
+
+def nvfp4_quantize_grouped_scatter(xbits: np.ndarray, dest_rows: np.ndarray, offsets: np.ndarray,
+                                   total_rows: int, g: np.ndarray, codes=None, scales=None,
+                                   f16: bool = False):
+    """The NVFP4 experts quant with the dispatch as a scatter (route j of
+    token t is row dest_rows[t, j], -1: not dispatched), segment e with global
+    scale g[e].  Returns (rc, codes, scales, scale_row_offsets); rc 0, -6 or
+    -7.  `codes` / `scales`, when given, are the buffers' previous contents
+    (rows that no route targets keep them)."""
+    x = _c(xbits, np.uint16)
+    dst = _c(dest_rows, np.int32)
+    off = _c(offsets, np.int32)
+    gs = _c(np.asarray(g, np.float32), np.float32)
+    T, K = x.shape
+    top_k = dst.shape[1] if dst.ndim == 2 else 1
+    assert dst.size == T * top_k
+    E = off.size - 1
+    assert gs.size == E
+    codes = (np.zeros((total_rows, K // 2), np.uint8) if codes is None
+             else np.array(codes, np.uint8, copy=True).reshape(total_rows, K // 2))
+    nsb = max(nvfp4_grouped_scale_bytes_bound(total_rows, E, K), 1)
+    scales = (np.zeros(nsb, np.uint8) if scales is None
+              else np.array(scales, np.uint8, copy=True).ravel())
+    assert scales.size >= nvfp4_grouped_scale_bytes_bound(total_rows, E, K)
+    sro = np.zeros(E + 1, np.int32)
+    fn = (lib().orc_nvfp4_quantize_grouped_scatter_f16 if f16
+          else lib().orc_nvfp4_quantize_grouped_scatter)
+    rc = fn(_p(x, _u16p), T, K, K, _p(dst, _i32p), top_k, total_rows, _p(off, _i32p), E,
+            _p(gs, _f32p), _p(codes, _u8p), _p(scales, _u8p), _p(sro, _i32p))
     return rc, codes, scales, sro
 
 

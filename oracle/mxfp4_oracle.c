@@ -710,6 +710,80 @@ int orc_nvfp4_quantize_grouped_f16(const uint16_t* x, int64_t total_rows, int64_
                           scale_row_offsets);
 }
 
+/* NVFP4 experts quant with the dispatch as a scatter: route j of token t
+ * lands on row dest_rows[t * top_k + j] of the expert-sorted batch (-1: not
+ * dispatched).  The result is the NVFP4 experts quant above of the batch the
+ * routes fill, each expert segment with its own global scale g[e]; rows that
+ * no route targets keep their bytes (codes and scales), pad rows get zero
+ * scales.  Entries outside [-1, total_rows) are skipped (-7); bad offsets as
+ * in the experts quant (-6). */
+static int nvfp4_scatter_of(to_f32_fn to_f32, const uint16_t* x, int64_t num_tokens, int64_t K,
+                            int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                            int64_t total_rows, const int32_t* offsets, int32_t E,
+                            const float* g, uint8_t* codes, uint8_t* scales,
+                            int32_t* scale_row_offsets) {
+  int bad = 0;
+  uint16_t* batch = (uint16_t*)calloc((size_t)(total_rows * K) + 1, sizeof(uint16_t));
+  uint8_t* hit = (uint8_t*)calloc((size_t)total_rows + 1, 1);
+  for (int64_t t = 0; t < num_tokens; ++t)
+    for (int32_t j = 0; j < top_k; ++j) {
+      int64_t d = dest_rows[t * top_k + j];
+      if (d == -1) continue;
+      if (d < -1 || d >= total_rows) {
+        bad = 1;
+        continue;
+      }
+      memcpy(batch + d * K, x + t * ldx, (size_t)K * sizeof(uint16_t));
+      hit[d] = 1;
+    }
+  int64_t nkt = (K / 16 + 3) / 4;
+  int64_t padded_sK = nkt * 4;
+  int64_t bound_rows = (total_rows + 127 * (int64_t)(E > 0 ? E : 0)) / 128 * 128 + 128;
+  uint8_t* tc = (uint8_t*)calloc((size_t)(total_rows * (K / 2)) + 1, 1);
+  uint8_t* ts = (uint8_t*)calloc((size_t)(bound_rows * padded_sK) + 1, 1);
+  int rc = nvfp4_grouped_of(to_f32, batch, total_rows, K, offsets, E, g, tc, ts,
+                            scale_row_offsets);
+  if (rc == 0) {
+    for (int32_t e = 0; e < E; ++e) {
+      int64_t n = (int64_t)offsets[e + 1] - offsets[e];
+      int64_t base = (int64_t)scale_row_offsets[e] * padded_sK;
+      for (int64_t prow = 0; prow < (n + 127) / 128 * 128; ++prow) {
+        int64_t d = offsets[e] + prow;
+        if (prow < n && !hit[d]) continue; /* untargeted: left as it was */
+        if (prow < n) memcpy(codes + d * (K / 2), tc + d * (K / 2), (size_t)(K / 2));
+        for (int64_t c = 0; c < padded_sK; ++c) {
+          int64_t i = base + tiled_index(prow, c, nkt);
+          scales[i] = ts[i];
+        }
+      }
+    }
+  }
+  free(batch);
+  free(hit);
+  free(tc);
+  free(ts);
+  if (rc != 0) return rc;
+  return bad ? -7 : 0;
+}
+
+int orc_nvfp4_quantize_grouped_scatter(const uint16_t* x, int64_t num_tokens, int64_t K,
+                                       int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                       int64_t total_rows, const int32_t* offsets, int32_t E,
+                                       const float* g, uint8_t* codes, uint8_t* scales,
+                                       int32_t* scale_row_offsets) {
+  return nvfp4_scatter_of(f32_of_bf16, x, num_tokens, K, ldx, dest_rows, top_k, total_rows,
+                          offsets, E, g, codes, scales, scale_row_offsets);
+}
+
+int orc_nvfp4_quantize_grouped_scatter_f16(const uint16_t* x, int64_t num_tokens, int64_t K,
+                                           int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                           int64_t total_rows, const int32_t* offsets, int32_t E,
+                                           const float* g, uint8_t* codes, uint8_t* scales,
+                                           int32_t* scale_row_offsets) {
+  return nvfp4_scatter_of(f32_of_f16, x, num_tokens, K, ldx, dest_rows, top_k, total_rows,
+                          offsets, E, g, codes, scales, scale_row_offsets);
+}
+
 void orc_nvfp4_dequantize(const uint8_t* codes, const uint8_t* tiled_scales, int64_t M, int64_t K,
                           float g, uint16_t* y) {
   int64_t sK = K / 16;

@@ -145,6 +145,19 @@ void orc_nvfp4_quantize_f16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
 int orc_nvfp4_quantize_grouped_f16(const uint16_t* x, int64_t total_rows, int64_t K,
                                    const int32_t* offsets, int32_t E, const float* g,
                                    uint8_t* codes, uint8_t* scales, int32_t* scale_row_offsets);
+/* NVFP4 experts quant with the dispatch as a scatter (route j of token t ->
+ * row dest_rows[t * top_k + j], -1 = none): untargeted rows keep their bytes,
+ * pad rows zero scales; returns 0, -6 (bad offsets) or -7 (bad entries). */
+int orc_nvfp4_quantize_grouped_scatter(const uint16_t* x, int64_t num_tokens, int64_t K,
+                                       int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                       int64_t total_rows, const int32_t* offsets, int32_t E,
+                                       const float* g, uint8_t* codes, uint8_t* scales,
+                                       int32_t* scale_row_offsets);
+int orc_nvfp4_quantize_grouped_scatter_f16(const uint16_t* x, int64_t num_tokens, int64_t K,
+                                           int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                           int64_t total_rows, const int32_t* offsets, int32_t E,
+                                           const float* g, uint8_t* codes, uint8_t* scales,
+                                           int32_t* scale_row_offsets);
 void orc_nvfp4_dequantize(const uint8_t* codes, const uint8_t* tiled_scales, int64_t M, int64_t K,
                           float g, uint16_t* y);
 

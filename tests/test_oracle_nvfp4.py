@@ -173,3 +173,109 @@ def test_nvfp4_f16_equals_bf16_on_shared_values(orc):
     c3, _ = orc.nvfp4_quantize(hf_b, 1.0, f16=True)
     c4, _ = orc.nvfp4_quantize(bb, 1.0)
     assert not np.array_equal(c3, c4)
+
+
+# ------------------------------------------------ NVFP4 experts quant, scatter
+def test_nvfp4_scatter_hand_example(orc):
+    """Two tokens of one 16-element block, two experts with global scales 1
+    and 2; token 0 -> rows 0 (expert 0) and 2 (expert 1), token 1 -> row 1
+    (expert 0), its second route dropped, so row 3 keeps its bytes.
+      row 0: block N1 at g = 1: vecMax 6, sf 1.0 = 0x38, codes 7 D 3 2;
+      row 1: block N7's x at g = 1: vecMax 3, q = 0.5, sf 0.5 = 0x30,
+             inv = 1 / 0.5 = 2 (as N7's inv at g = 2), codes 7 4 B;
+      row 2: block N1 at g = 2: sf 2.0 = 0x40, inv = 2 / 2 = 1, codes 7 D 3 2.
+    One scale column (K = 16), so padded row p of a segment puts its byte at
+    (p % 32) * 16 + (p / 32) * 4 of the segment's 512-byte chunk; expert 1's
+    chunk starts at byte 128 * 4 = 512."""
+    x = np.zeros((2, 16), np.uint16)
+    x[0, :4] = [0x40C0, 0xC040, 0x3FC0, 0x3F40]
+    x[1, :3] = [0x4040, 0x3F80, 0xBF40]
+    dest = np.array([[0, 2], [1, -1]], np.int32)
+    off = np.array([0, 2, 4], np.int32)
+    g = np.array([1.0, 2.0], np.float32)
+    c0 = np.full((4, 8), 0xEE, np.uint8)
+    s0 = np.full(orc.nvfp4_grouped_scale_bytes_bound(4, 2, 16), 0xEE, np.uint8)
+    rc, c, s, sro = orc.nvfp4_quantize_grouped_scatter(x, dest, off, 4, g, c0, s0)
+    assert rc == 0 and list(sro) == [0, 128, 256]
+    want_c = np.zeros((4, 8), np.uint8)
+    want_c[0, :2] = [0xD7, 0x23]
+    want_c[1, :2] = [0x47, 0x0B]
+    want_c[2, :2] = [0xD7, 0x23]
+    want_c[3] = 0xEE                                   # untargeted row: kept
+    assert np.array_equal(c, want_c)
+    want_s = np.zeros(1024, np.uint8)
+    want_s[0], want_s[16], want_s[512] = 0x38, 0x30, 0x40
+    want_s[528:532] = 0xEE                             # row 3 = expert 1's padded row 1: kept
+    assert np.array_equal(s, want_s)
+
+
+def _permuted(xb, dest, total):
+    rows = np.zeros((total, xb.shape[1]), np.uint16)
+    hit = np.zeros(total, bool)
+    for t in range(dest.shape[0]):
+        for d in dest[t]:
+            if d >= 0:
+                rows[d] = xb[t]
+                hit[d] = True
+    return rows, hit
+
+
+@pytest.mark.parametrize("f16", [False, True])
+def test_nvfp4_scatter_equals_experts_quant_of_the_permuted_batch(orc, f16):
+    g = W.moe_grouped(seed=41, tokens=150, top_k=3, num_experts=7, K=80)
+    xt = g.x_tokens
+    if f16:
+        xt = xt.float().clamp(-60000, 60000).to(torch.float16)
+        xb = xt.view(torch.int16).numpy().view(np.uint16)
+    else:
+        xb = W.bf16_bits(xt)
+    dest = g.dest_rows.numpy()
+    off = g.offsets.numpy()
+    total = dest.size
+    gs = (448.0 * 6.0 / np.exp(np.random.default_rng(41).uniform(0, 3, 7))).astype(np.float32)
+    perm, _ = _permuted(xb, dest, total)
+    rc0, c0, s0, sro0 = orc.nvfp4_quantize_grouped(perm, off, gs, f16=f16)
+    rc, c, s, sro = orc.nvfp4_quantize_grouped_scatter(xb, dest, off, total, gs, f16=f16)
+    assert rc == rc0 == 0 and np.array_equal(sro, sro0)
+    assert np.array_equal(c, c0) and np.array_equal(s, s0)
+    # dropped routes: targeted rows and pad rows as above, untargeted rows keep
+    # a random prefill (codes and all their scale bytes)
+    rng = np.random.default_rng(42)
+    dd = dest.copy()
+    dd[rng.random(dd.shape) < 0.25] = -1
+    cp = rng.integers(0, 256, c0.shape, dtype=np.uint8)
+    sp = rng.integers(0, 256, s0.shape, dtype=np.uint8)
+    rc, c, s, _ = orc.nvfp4_quantize_grouped_scatter(xb, dd, off, total, gs, cp, sp, f16=f16)
+    _, hit = _permuted(xb, dd, total)
+    assert rc == 0
+    assert np.array_equal(c[hit], c0[hit]) and np.array_equal(c[~hit], cp[~hit])
+    nkt = (80 // 16 + 3) // 4
+    for e in range(7):
+        for p in range((off[e + 1] - off[e] + 127) // 128 * 128):
+            r = off[e] + p
+            base = int(sro0[e]) * nkt * 4
+            idx = [base + (p // 128 * nkt + c // 4) * 512 + (p % 32) * 16 + (p % 128) // 32 * 4
+                   + c % 4 for c in range(nkt * 4)]
+            src = sp if (p < off[e + 1] - off[e] and not hit[r]) else s0
+            assert np.array_equal(s[idx], src[idx]), (e, p)
+
+
+def test_nvfp4_scatter_bad_entries_and_offsets(orc):
+    g = W.moe_grouped(seed=43, tokens=40, top_k=2, num_experts=3, K=32)
+    xb = W.bf16_bits(g.x_tokens)
+    dest = g.dest_rows.numpy().copy()
+    off = g.offsets.numpy()
+    gs = np.array([1.0, 5.0, 0.25], np.float32)
+    clean = dest.copy()
+    clean[3, 1] = -1
+    clean[7, 0] = -1
+    dest[3, 1] = 80            # == total_rows: outside
+    dest[7, 0] = -5
+    r1 = orc.nvfp4_quantize_grouped_scatter(xb, dest, off, 80, gs)
+    r2 = orc.nvfp4_quantize_grouped_scatter(xb, clean, off, 80, gs)
+    assert r1[0] == -7 and r2[0] == 0
+    assert all(np.array_equal(a, b) for a, b in zip(r1[1:], r2[1:]))
+    bad = np.array([0, 50, 40, 80], np.int32)
+    cp = np.full((80, 16), 0x5A, np.uint8)
+    rc, c, s, sro = orc.nvfp4_quantize_grouped_scatter(xb, clean, bad, 80, gs, cp)
+    assert rc == -6 and (sro == -1).all() and (c == 0x5A).all() and not s.any()
