@@ -511,6 +511,27 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     e_["speedup_vs_direct_scatter"] = round(ms_sc / ms_sw, 3)
     out["grouped_scatter_ws_moe_16384tok_top8_E384"] = e_
     del ws
+    # the NVFP4 experts quant with the same dispatch fused in (a global scale
+    # per expert), against gathering the 1.9 GB batch first
+    g_nv = torch.full((E,), 448.0 * 6.0 / 5.0, device="cuda")
+    sc_nv = torch.empty(mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K), dtype=torch.uint8,
+                        device="cuda")
+    ms_nvs = time_launches(
+        lambda i: mx.mxfp4_quantize_nvfp4_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets,
+                                                          total, g_nv, codes, sc_nv, sro, st,
+                                                          stream), 30, stream)
+    ms_nvu = time_launches(
+        lambda i: (torch.index_select(g.x_tokens, 0, g.row_index, out=xg),
+                   mx.mxfp4_quantize_nvfp4_grouped(xg, g.offsets, g_nv, codes, sc_nv, sro, st,
+                                                   stream)), 30, stream)
+    nb_nvs = (2 * T * K + 4 * total + total * K // 2 + padded * (K // 16) + 4 * (E + 1) + 4 * E)
+    e_ = entry(nb_nvs, ms_nvs, 2, "bytes = token rows read once + route->row map + codes + "
+               "E4M3 scales (16-element columns) + offsets + global scales; each route's "
+               "scale words stored into the tiled layout")
+    e_["unfused_us_per_call"] = round(ms_nvu * 1e3, 2)
+    e_["speedup_vs_unfused"] = round(ms_nvu / ms_nvs, 3)
+    out["nvfp4_grouped_scatter_moe_16384tok_top8_E384"] = e_
+    del sc_nv
     del g, codes, scales, xg
 
     # expert weights: w13 [128, 1536, 2048], w2 [128, 2048, 768], then the swap

@@ -417,6 +417,38 @@ int mxfp4_quantize_nvfp4_grouped_f16(const void* x, int64_t total_rows, int64_t 
                                      uint8_t* scales, int32_t* scale_row_offsets,
                                      int32_t* status, void* stream);
 
+/* mxfp4_quantize_nvfp4_grouped_scatter — the NVFP4 experts quant with the
+ * MoE dispatch fused in as a scatter: route j of token t lands on row
+ * dest_rows[t][j] of the expert-sorted batch (-1: not dispatched).  Each
+ * token row is read once and its block maxima taken once; each route's codes
+ * and E4M3 scales use the global scale of the segment its row falls in, so
+ * the result equals mxfp4_quantize_nvfp4_grouped of the batch the routes
+ * fill.  [PR43557] "Implementation breakdown" items 1 and 3 (the NVFP4 branch
+ * of the experts quant of the routed activations).
+ *
+ * x, dest_rows, top_k, total_rows, expert_offsets, E, status: as in
+ * mxfp4_quantize_grouped_scatter (rows no route targets are not written; pad
+ * rows get zero scale bytes; entries outside [-1, total_rows) are skipped and
+ * reported as MXFP4_EINDEX; no row may be the target of two tokens), with
+ * K % 16 == 0.
+ * global_scales, codes, scales, scale_row_offsets: as in
+ * mxfp4_quantize_nvfp4_grouped (scales >= mxfp4_nvfp4_grouped_scale_bytes_bound).
+ * The _f16 form takes IEEE binary16 input.
+ */
+int mxfp4_quantize_nvfp4_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
+                                         int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                         int64_t total_rows, const int32_t* expert_offsets,
+                                         int32_t E, const float* global_scales, uint8_t* codes,
+                                         uint8_t* scales, int32_t* scale_row_offsets,
+                                         int32_t* status, void* stream);
+int mxfp4_quantize_nvfp4_grouped_scatter_f16(const void* x, int64_t num_tokens, int64_t K,
+                                             int64_t ldx, const int32_t* dest_rows,
+                                             int32_t top_k, int64_t total_rows,
+                                             const int32_t* expert_offsets, int32_t E,
+                                             const float* global_scales, uint8_t* codes,
+                                             uint8_t* scales, int32_t* scale_row_offsets,
+                                             int32_t* status, void* stream);
+
 /* ---------------------------------------------------------------- NVFP4
  * The other branch of the same quantize kernel on [PR43557] ("Implementation
  * breakdown" item 1, the non-UE8M0 branch of the cvt_warp_fp16_to_fp4

@@ -41,6 +41,8 @@ __all__ = [
     "mxfp4_quantize_nvfp4", "mxfp4_dequantize_nvfp4", "quantize_nvfp4", "dequantize_nvfp4",
     "mxfp4_nvfp4_grouped_scale_bytes_bound", "mxfp4_quantize_nvfp4_grouped",
     "quantize_nvfp4_grouped", "mxfp4_quantize_nvfp4_f16", "mxfp4_quantize_nvfp4_grouped_f16",
+    "mxfp4_quantize_nvfp4_grouped_scatter", "mxfp4_quantize_nvfp4_grouped_scatter_f16",
+    "quantize_nvfp4_grouped_scatter",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300.so")
@@ -129,6 +131,11 @@ def _load(path=LIB_PATH):
     for name in ("mxfp4_quantize_nvfp4_grouped", "mxfp4_quantize_nvfp4_grouped_f16"):
         getattr(L, name).restype = ctypes.c_int
         getattr(L, name).argtypes = [vp, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp]
+    for name in ("mxfp4_quantize_nvfp4_grouped_scatter",
+                 "mxfp4_quantize_nvfp4_grouped_scatter_f16"):
+        getattr(L, name).restype = ctypes.c_int
+        getattr(L, name).argtypes = [vp, i64, i64, i64, vp, i32, i64, vp, i32, vp, vp, vp, vp, vp,
+                                     vp]
     L.mxfp4_dequantize_nvfp4.restype = ctypes.c_int
     L.mxfp4_dequantize_nvfp4.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     L.mxfp4_status_string.restype = ctypes.c_char_p
@@ -534,6 +541,51 @@ def mxfp4_quantize_nvfp4_grouped_f16(x, expert_offsets, global_scales, codes, sc
                    stream, True)
 
 
+def _nvfp4_scatter(x, dest_rows, expert_offsets, total_rows, global_scales, codes, scales,
+                   scale_row_offsets, status, stream, f16) -> None:
+    name = "mxfp4_quantize_nvfp4_grouped_scatter" + ("_f16" if f16 else "")
+    _need_cuda("x", x, torch.float16 if f16 else torch.bfloat16)
+    _need_cuda("dest_rows", dest_rows, torch.int32)
+    _need_cuda("expert_offsets", expert_offsets, torch.int32)
+    _need_cuda("global_scales", global_scales, torch.float32)
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    _need_cuda("scale_row_offsets", scale_row_offsets, torch.int32)
+    _need_cuda("status", status, torch.int32)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    if dest_rows.dim() != 2 or dest_rows.shape[0] != x.shape[0] or not dest_rows.is_contiguous():
+        raise ValueError("dest_rows must be a contiguous [num_tokens, top_k] tensor")
+    T, K = x.shape
+    E = expert_offsets.numel() - 1
+    if global_scales.numel() != E:
+        raise ValueError("global_scales needs one entry per expert")
+    with torch.cuda.device(_device_of(x, dest_rows, expert_offsets, global_scales, codes, scales,
+                                      scale_row_offsets, status)):
+        _check(getattr(_lib, name)(
+            _ptr(x), T, K, x.stride(0), _ptr(dest_rows), dest_rows.shape[1], int(total_rows),
+            _ptr(expert_offsets), E, _ptr(global_scales), _ptr(codes), _ptr(scales),
+            _ptr(scale_row_offsets), _ptr(status), _stream(stream, x.device)), name)
+
+
+def mxfp4_quantize_nvfp4_grouped_scatter(x, dest_rows, expert_offsets, total_rows: int,
+                                         global_scales, codes, scales, scale_row_offsets,
+                                         status=None, stream=None) -> None:
+    """NVFP4 experts quant with the dispatch as a scatter: route j of token t
+    is row ``dest_rows[t, j]`` (-1 = not dispatched); segment e uses
+    ``global_scales[e]``.  Rows no route targets are not written."""
+    _nvfp4_scatter(x, dest_rows, expert_offsets, total_rows, global_scales, codes, scales,
+                   scale_row_offsets, status, stream, False)
+
+
+def mxfp4_quantize_nvfp4_grouped_scatter_f16(x, dest_rows, expert_offsets, total_rows: int,
+                                             global_scales, codes, scales, scale_row_offsets,
+                                             status=None, stream=None) -> None:
+    """mxfp4_quantize_nvfp4_grouped_scatter for FP16 ``x``."""
+    _nvfp4_scatter(x, dest_rows, expert_offsets, total_rows, global_scales, codes, scales,
+                   scale_row_offsets, status, stream, True)
+
+
 def mxfp4_dequantize_nvfp4(codes, scales, global_scale, M: int, K: int, y, stream=None) -> None:
     _need_cuda("codes", codes, torch.uint8)
     _need_cuda("scales", scales, torch.uint8)
@@ -668,6 +720,25 @@ def quantize_nvfp4_grouped(x, expert_offsets, global_scales, stream=None):
     status = torch.empty(1, dtype=torch.int32, device=dev)
     _nvfp4_grouped(x, expert_offsets, global_scales, codes, scales, sro, status, stream,
                    x.dtype == torch.float16)
+    return codes, scales, sro, status
+
+
+def quantize_nvfp4_grouped_scatter(x, dest_rows, expert_offsets, global_scales, total_rows=None,
+                                   stream=None):
+    """Returns (codes, scales, scale_row_offsets, status) of the NVFP4 experts
+    quant of the batch ``dest_rows`` dispatches ``x`` (BF16 or FP16) into;
+    rows no route targets come back zero."""
+    K = x.shape[1]
+    total = dest_rows.numel() if total_rows is None else int(total_rows)
+    E = expert_offsets.numel() - 1
+    dev = x.device
+    codes = torch.zeros((total, K // 2), dtype=torch.uint8, device=dev)
+    scales = torch.zeros(max(mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K), 16),
+                         dtype=torch.uint8, device=dev)
+    sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    status = torch.empty(1, dtype=torch.int32, device=dev)
+    _nvfp4_scatter(x, dest_rows, expert_offsets, total, global_scales, codes, scales, sro, status,
+                   stream, x.dtype == torch.float16)
     return codes, scales, sro, status
 
 

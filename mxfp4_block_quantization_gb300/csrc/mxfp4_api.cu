@@ -644,6 +644,85 @@ int mxfp4_quantize_nvfp4_grouped_f16(const void* x, int64_t total_rows, int64_t 
                                scale_row_offsets, status, true, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+int nvfp4_scatter_checked(const void* x, int64_t num_tokens, int64_t K, int64_t ldx,
+                          const int32_t* dest_rows, int32_t top_k, int64_t total_rows,
+                          const int32_t* expert_offsets, int32_t E, const float* global_scales,
+                          uint8_t* codes, uint8_t* scales, int32_t* scale_row_offsets,
+                          int32_t* status, bool f16, void* stream) {
+  if (num_tokens < 0 || total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
+  if (top_k < 1 || top_k > MXFP4_SCATTER_MAX_TOP_K) return MXFP4_EINVAL;
+  if (K % 16 != 0 || ldx < K) return MXFP4_ESHAPE;
+  if (!expert_offsets || !scale_row_offsets) return MXFP4_EINVAL;
+  const bool rows = total_rows > 0 && K > 0;
+  const bool reads = rows && num_tokens > 0;
+  if (rows && (!codes || !scales || !global_scales)) return MXFP4_EINVAL;
+  if (reads && (!x || !dest_rows)) return MXFP4_EINVAL;
+  if (E == 0 && total_rows > 0) return MXFP4_EINVAL;
+  const int64_t bound_tiles = (total_rows + 127 * static_cast<int64_t>(E)) / 128;
+  if (total_rows + 127 * static_cast<int64_t>(E) > INT32_MAX) return MXFP4_ESHAPE;
+  if (E + ceil_div(num_tokens, 8) > kMaxGrid) return MXFP4_ESHAPE;
+  if (num_tokens > (INT64_MAX / 4) / (ldx > top_k ? ldx : top_k)) return MXFP4_ESHAPE;
+  if ((x && (!aligned16(x) || ldx % 8 != 0)) || (codes && !aligned16(codes)) ||
+      (scales && !aligned16(scales)) || (reinterpret_cast<uintptr_t>(dest_rows) & 3u) ||
+      (reinterpret_cast<uintptr_t>(global_scales) & 3u) ||
+      (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) ||
+      (reinterpret_cast<uintptr_t>(scale_row_offsets) & 3u) ||
+      (reinterpret_cast<uintptr_t>(status) & 3u))
+    return MXFP4_EALIGN;
+  const Range ins[4] = {
+      range_of(x, reads ? ((num_tokens - 1) * ldx + K) * 2 : 0),
+      range_of(dest_rows, reads ? num_tokens * top_k * 4 : 0),
+      range_of(expert_offsets, (static_cast<int64_t>(E) + 1) * 4),
+      range_of(global_scales, rows ? static_cast<int64_t>(E) * 4 : 0)};
+  const Range outs[4] = {
+      range_of(codes, total_rows * (K / 2)),
+      range_of(scales,
+               static_cast<int64_t>(mxfp4_nvfp4_grouped_scale_bytes_bound(total_rows, E, K))),
+      range_of(scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4),
+      range_of(status, status ? 4 : 0)};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 4; ++j)
+      if (overlap(outs[i], ins[j])) return MXFP4_EALIAS;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(outs[i], outs[j])) return MXFP4_EALIAS;
+  }
+  return from_cuda(mxfp4::launch_quantize_nvfp4_grouped_scatter(
+      x, reads ? num_tokens : 0, K, ldx, dest_rows, top_k, total_rows, expert_offsets, E,
+      global_scales, codes, scales, scale_row_offsets, status, K == 0 ? 0 : bound_tiles, f16,
+      static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxfp4_quantize_nvfp4_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
+                                         int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                         int64_t total_rows, const int32_t* expert_offsets,
+                                         int32_t E, const float* global_scales, uint8_t* codes,
+                                         uint8_t* scales, int32_t* scale_row_offsets,
+                                         int32_t* status, void* stream) {
+  return nvfp4_scatter_checked(x, num_tokens, K, ldx, dest_rows, top_k, total_rows,
+                               expert_offsets, E, global_scales, codes, scales, scale_row_offsets,
+                               status, false, stream);
+}
+
+int mxfp4_quantize_nvfp4_grouped_scatter_f16(const void* x, int64_t num_tokens, int64_t K,
+                                             int64_t ldx, const int32_t* dest_rows,
+                                             int32_t top_k, int64_t total_rows,
+                                             const int32_t* expert_offsets, int32_t E,
+                                             const float* global_scales, uint8_t* codes,
+                                             uint8_t* scales, int32_t* scale_row_offsets,
+                                             int32_t* status, void* stream) {
+  return nvfp4_scatter_checked(x, num_tokens, K, ldx, dest_rows, top_k, total_rows,
+                               expert_offsets, E, global_scales, codes, scales, scale_row_offsets,
+                               status, true, stream);
+}
+
 int mxfp4_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, const float* global_scale,
                            int64_t M, int64_t K, void* y, void* stream) {
   if (M < 0 || K < 0) return MXFP4_EINVAL;

@@ -207,6 +207,33 @@ def test_grouped_scatter_ws_validation(lib):
         lib.MXFP4_ESHAPE
 
 
+def test_nvfp4_grouped_scatter_validation(lib):
+    f = lib._lib.mxfp4_quantize_nvfp4_grouped_scatter
+    # x, T, K, ldx, dest, top_k, total, off, E, g, codes, scales, sro, status, stream
+    ok = [A, 50, 64, 64, 2 * A, 8, 400, 3 * A, 2, 9 * A, 4 * A, 5 * A, 6 * A, None, None]
+
+    def call(**kw):
+        names = ["x", "T", "K", "ldx", "dst", "k", "tot", "off", "E", "g", "c", "s", "sro",
+                 "st", "strm"]
+        a = dict(zip(names, ok))
+        a.update(kw)
+        return f(*[a[n] for n in names])
+
+    assert call(K=40, ldx=40) == lib.MXFP4_ESHAPE          # K % 16 != 0
+    assert call(ldx=48) == lib.MXFP4_ESHAPE                 # ldx < K
+    assert call(k=0) == lib.MXFP4_EINVAL
+    assert call(k=lib.MXFP4_SCATTER_MAX_TOP_K + 1) == lib.MXFP4_EINVAL
+    assert call(g=None) == lib.MXFP4_EINVAL
+    assert call(dst=None) == lib.MXFP4_EINVAL
+    assert call(E=0) == lib.MXFP4_EINVAL
+    assert call(g=9 * A + 2) == lib.MXFP4_EALIGN
+    assert call(x=A + 8) == lib.MXFP4_EALIGN
+    assert call(c=2 * A + 16) == lib.MXFP4_EALIAS            # codes overlap the routes
+    assert call(s=9 * A - 64) == lib.MXFP4_EALIAS            # scales overlap the global scales
+    assert lib._lib.mxfp4_quantize_nvfp4_grouped_scatter_f16(
+        *ok[:2], 40, 40, *ok[4:]) == lib.MXFP4_ESHAPE
+
+
 def test_quantize_f16_validation(lib):
     f = lib._lib.mxfp4_quantize_f16
     assert f(A, 4, 48, 48, 2 * A, 3 * A, None) == lib.MXFP4_ESHAPE

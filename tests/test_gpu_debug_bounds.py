@@ -146,6 +146,13 @@ def test_everything_in_bounds(libs):
                                                              g3.dest_rows, g3.offsets), 1056))
     cases.append(lambda: written(mx.quantize_grouped_gather(g3.x_tokens.to(torch.float16),
                                                             g3.row_index, g3.offsets), 1056))
+    # NVFP4 experts quant with the dispatch as a scatter: dropped routes, bad entries
+    gsc = torch.linspace(0.5, 40.0, 5, device="cuda")
+    g3d = g3.dest_rows.clone()
+    g3d[::4, 1] = -1
+    g3d[2, 0] = 1 << 20
+    cases.append(lambda: written(mx.quantize_nvfp4_grouped_scatter(g3.x_tokens, g3d, g3.offsets,
+                                                                   gsc), 2 * 1056))  # K/16 cols
     # NVFP4 experts quant (K a multiple of 16 but not 32 included)
     gn = W.moe_grouped(seed=10, tokens=150, top_k=3, num_experts=7, K=80, device="cuda")
     gsn = torch.linspace(0.5, 40.0, 7, device="cuda")

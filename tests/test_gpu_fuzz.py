@@ -109,6 +109,22 @@ def test_fuzz_grouped_gather_scatter(mx, seed):
         assert int(st.item()) == rc == 0, staged
         assert np.array_equal(codes.cpu().numpy(), c_o), staged
         assert np.array_equal(scales.cpu().numpy(), s_o), staged
+    # the NVFP4 experts quant of the same routing, a global scale per expert
+    gs = (448.0 * 6.0 / np.exp(rng.uniform(-3, 8, E))).astype(np.float32)
+    nsb_nv = mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K)
+    s0_nv = rng.integers(0, 256, nsb_nv, dtype=np.uint8)
+    rc_nv, cn_o, sn_o, _ = oracle.nvfp4_quantize_grouped_scatter(xb, dest, off, total, gs, c0,
+                                                                 s0_nv, f16=f16)
+    codes = torch.from_numpy(c0).cuda()
+    scales = torch.from_numpy(s0_nv).cuda()
+    fn = (mx.mxfp4_quantize_nvfp4_grouped_scatter_f16 if f16
+          else mx.mxfp4_quantize_nvfp4_grouped_scatter)
+    fn(xp, torch.from_numpy(dest).cuda(), off_d, total, torch.from_numpy(gs).cuda(), codes,
+       scales, sro, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == rc_nv == 0
+    assert np.array_equal(codes.cpu().numpy(), cn_o)
+    assert np.array_equal(scales.cpu().numpy(), sn_o)
     # gather (both kernels): dropped rows have index -1 -> zero rows, EINDEX
     rc_g, cg_o, sg_o, _ = oracle.quantize_grouped_gather(xb, row_tok, off, f16=f16)
     used = int(sro_o[-1]) * ((K // 32 + 3) // 4 * 4)

@@ -1038,6 +1038,105 @@ def test_nvfp4_grouped_moe_full_size_sampled(mx):
         assert np.array_equal(scales[p0:p0 + s_o.size].cpu().numpy(), s_o), e
 
 
+# ------------------------------------ NVFP4 experts quant, dispatch as scatter
+def run_nvfp4_scatter(mx, x, dest, offsets, total, gs, seed=0):
+    """The NVFP4 scatter through the C ABI into guard-banded buffers with a
+    random prefill (the oracle gets the same bytes); returns GPU and oracle
+    results."""
+    K = x.shape[1]
+    E = offsets.numel() - 1
+    f16 = x.dtype == torch.float16
+    rng = np.random.default_rng(seed)
+    nsb = mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K)
+    c0 = rng.integers(0, 256, (total, K // 2), dtype=np.uint8)
+    s0 = rng.integers(0, 256, nsb, dtype=np.uint8)
+    codes = Guarded(total * (K // 2), shape=(total, K // 2))
+    scales = Guarded(nsb)
+    codes.t.copy_(torch.from_numpy(c0))
+    scales.t.copy_(torch.from_numpy(s0))
+    sro = Guarded(4 * (E + 1), torch.int32)
+    status = Guarded(4, torch.int32)
+    fn = (mx.mxfp4_quantize_nvfp4_grouped_scatter_f16 if f16
+          else mx.mxfp4_quantize_nvfp4_grouped_scatter)
+    fn(x, dest, offsets, total, torch.from_numpy(gs).cuda(), codes.t, scales.t, sro.t, status.t)
+    torch.cuda.synchronize()
+    for g in (codes, scales, sro, status):
+        g.check()
+    gpu = (codes.t.cpu().numpy(), scales.t.cpu().numpy(), sro.t.cpu().numpy(),
+           int(status.t.cpu()[0]))
+    xb = (x.contiguous().cpu().view(torch.int16).numpy().view(np.uint16) if f16
+          else bits(x.contiguous()))
+    rc, c_o, s_o, sro_o = oracle.nvfp4_quantize_grouped_scatter(
+        xb, dest.cpu().numpy(), offsets.cpu().numpy(), total, gs, c0, s0, f16=f16)
+    return gpu, (c_o, s_o, sro_o, rc)
+
+
+@pytest.mark.parametrize("tokens,top_k,E,K", [
+    (1, 1, 1, 16), (129, 3, 5, 80), (300, 2, 7, 2880), (64, 32, 40, 96), (257, 8, 16, 1056)])
+def test_nvfp4_scatter_shapes(mx, tokens, top_k, E, K):
+    g = W.moe_grouped(seed=tokens + K + 5, tokens=tokens, top_k=top_k, num_experts=E, K=K,
+                      device="cuda")
+    gs = _expert_gscales(E, K)
+    gpu, orc = run_nvfp4_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, g.row_index.numel(),
+                                 gs, seed=K)
+    assert_scatter_parity(gpu, orc)
+
+
+@pytest.mark.parametrize("f16", [False, True])
+def test_nvfp4_scatter_dropped_routes_strided_and_aligned(mx, f16):
+    g = W.moe_grouped(seed=51, tokens=300, top_k=4, num_experts=9, K=160, device="cuda")
+    dst = g.dest_rows.clone()
+    drop = torch.rand(dst.shape, generator=torch.Generator().manual_seed(5)) < 0.2
+    dst[drop.cuda()] = -1
+    gs = _expert_gscales(9, 51)
+    xt = g.x_tokens.to(torch.float16) if f16 else g.x_tokens
+    wide = torch.zeros((300, 184), dtype=xt.dtype, device="cuda")
+    wide[:, 8:168] = xt
+    for x in (xt, wide[:, 8:168], offset16_any(xt)):
+        gpu, orc = run_nvfp4_scatter(mx, x, dst, g.offsets, g.row_index.numel(), gs, seed=52)
+        assert_scatter_parity(gpu, orc)
+
+
+def test_nvfp4_scatter_bad_entries_offsets_and_no_tokens(mx):
+    g = W.moe_grouped(seed=53, tokens=140, top_k=2, num_experts=3, K=64, device="cuda")
+    total = g.row_index.numel()
+    gs = np.array([1.0, 7.5, 0.3], np.float32)
+    dst = g.dest_rows.clone()
+    dst[3, 1] = total
+    dst[7, 0] = -2
+    gpu, orc = run_nvfp4_scatter(mx, g.x_tokens, dst, g.offsets, total, gs, seed=54)
+    assert orc[3] == -7
+    assert_scatter_parity(gpu, orc, want_status=mx.MXFP4_EINDEX)
+    gpu, orc = run_nvfp4_scatter(mx, g.x_tokens[:0], dst[:0], g.offsets, total, gs, seed=55)
+    assert_scatter_parity(gpu, orc)
+    bad = torch.tensor([0, 200, 100, total], dtype=torch.int32, device="cuda")
+    gpu, orc = run_nvfp4_scatter(mx, g.x_tokens, g.dest_rows, bad, total, gs, seed=56)
+    assert orc[3] == -6 and gpu[3] == mx.MXFP4_EOFFSETS and (gpu[2] == -1).all()
+    assert np.array_equal(gpu[0], orc[0]) and np.array_equal(gpu[1], orc[1])  # untouched
+
+
+def test_nvfp4_scatter_moe_full_size(mx):
+    """16384 tokens x top-8 over 384 experts with their own global scales,
+    K = 7168: byte for byte the NVFP4 experts quant of the gathered batch;
+    three experts also against the oracle."""
+    g = W.moe_grouped(seed=2, device="cuda")
+    E = g.num_experts
+    gs = torch.from_numpy(_expert_gscales(E, 2)).cuda()
+    c1, s1, sro1, st1 = mx.quantize_nvfp4_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets, gs)
+    c2, s2, sro2, st2 = mx.quantize_nvfp4_grouped(g.x, g.offsets, gs)
+    torch.cuda.synchronize()
+    assert int(st1.item()) == int(st2.item()) == 0 and torch.equal(sro1, sro2)
+    used = int(sro1[-1].item()) * (7168 // 16)
+    assert torch.equal(c1, c2) and torch.equal(s1[:used], s2[:used])
+    off_h = g.offsets.cpu().numpy()
+    for e in (0, 200, E - 1):
+        a, b = int(off_h[e]), int(off_h[e + 1])
+        c_o, s_o = oracle.nvfp4_quantize(bits(g.x[a:b]), float(gs[e]))
+        assert np.array_equal(c1[a:b].cpu().numpy(), c_o), e
+        p0 = int(sro1[e].item()) * (7168 // 16)
+        assert np.array_equal(s1[p0:p0 + s_o.size].cpu().numpy(), s_o), e
+
+
 # ----------------------------------------------- FP16 input, grouped forms
 def _f16(t):
     return t.to(torch.float16)
