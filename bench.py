@@ -531,7 +531,21 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     e_["unfused_us_per_call"] = round(ms_nvu * 1e3, 2)
     e_["speedup_vs_unfused"] = round(ms_nvu / ms_nvs, 3)
     out["nvfp4_grouped_scatter_moe_16384tok_top8_E384"] = e_
-    del sc_nv
+    # the same call with a workspace: each route's scale bytes staged by padded
+    # row, the tiled scales written whole by a second kernel
+    ws = torch.empty(mx.mxfp4_nvfp4_scatter_workspace_bytes(total, E, K), dtype=torch.uint8,
+                     device="cuda")
+    ms_nvw = time_launches(
+        lambda i: mx.mxfp4_quantize_nvfp4_grouped_scatter_ws(g.x_tokens, g.dest_rows, g.offsets,
+                                                             total, g_nv, ws, codes, sc_nv, sro,
+                                                             st, stream), 30, stream)
+    e_ = entry(nb_nvs, ms_nvw, 3, "same call and bytes as the row above; offsets kernel, "
+               "workspace memset, scatter kernel (its first CTAs write the padded-row map), "
+               "tile kernel")
+    e_["speedup_vs_unfused"] = round(ms_nvu / ms_nvw, 3)
+    e_["speedup_vs_direct"] = round(ms_nvs / ms_nvw, 3)
+    out["nvfp4_grouped_scatter_ws_moe_16384tok_top8_E384"] = e_
+    del sc_nv, ws
     del g, codes, scales, xg
 
     # expert weights: w13 [128, 1536, 2048], w2 [128, 2048, 768], then the swap

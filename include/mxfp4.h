@@ -449,6 +449,41 @@ int mxfp4_quantize_nvfp4_grouped_scatter_f16(const void* x, int64_t num_tokens, 
                                              uint8_t* scales, int32_t* scale_row_offsets,
                                              int32_t* status, void* stream);
 
+/* mxfp4_quantize_nvfp4_grouped_scatter_ws — the same call with identical
+ * results (rows no route targets keep their codes and scale bytes) and a
+ * caller-provided workspace: each route's scale bytes are stored as one
+ * contiguous row of the workspace (indexed by the route's padded row) instead
+ * of as 4-byte words scattered over the tiled layout, and a second kernel
+ * writes the tiled scales in whole 512-byte chunks.
+ *
+ * workspace        DEVICE scratch owned by the caller, 16-byte aligned, at
+ *                  least mxfp4_nvfp4_scatter_workspace_bytes(total_rows, E, K)
+ *                  bytes, not overlapping any other argument; contents on
+ *                  entry do not matter, on return unspecified.
+ *
+ * mxfp4_nvfp4_scatter_workspace_bytes: PT * (4 + 4 * ceil4(ceil(K/64)))
+ * bytes, PT = floor((total_rows + 127E) / 128) * 128 padded rows (the padded
+ * row of every routed row, then one staged scale row per padded row); 0 for
+ * negative sizes, K % 16 != 0 or total_rows + 127E > INT32_MAX.
+ */
+size_t mxfp4_nvfp4_scatter_workspace_bytes(int64_t total_rows, int32_t E, int64_t K);
+int mxfp4_quantize_nvfp4_grouped_scatter_ws(const void* x, int64_t num_tokens, int64_t K,
+                                            int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                            int64_t total_rows, const int32_t* expert_offsets,
+                                            int32_t E, const float* global_scales,
+                                            void* workspace, size_t workspace_bytes,
+                                            uint8_t* codes, uint8_t* scales,
+                                            int32_t* scale_row_offsets, int32_t* status,
+                                            void* stream);
+int mxfp4_quantize_nvfp4_grouped_scatter_ws_f16(const void* x, int64_t num_tokens, int64_t K,
+                                                int64_t ldx, const int32_t* dest_rows,
+                                                int32_t top_k, int64_t total_rows,
+                                                const int32_t* expert_offsets, int32_t E,
+                                                const float* global_scales, void* workspace,
+                                                size_t workspace_bytes, uint8_t* codes,
+                                                uint8_t* scales, int32_t* scale_row_offsets,
+                                                int32_t* status, void* stream);
+
 /* ---------------------------------------------------------------- NVFP4
  * The other branch of the same quantize kernel on [PR43557] ("Implementation
  * breakdown" item 1, the non-UE8M0 branch of the cvt_warp_fp16_to_fp4

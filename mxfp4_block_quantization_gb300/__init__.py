@@ -42,7 +42,8 @@ __all__ = [
     "mxfp4_nvfp4_grouped_scale_bytes_bound", "mxfp4_quantize_nvfp4_grouped",
     "quantize_nvfp4_grouped", "mxfp4_quantize_nvfp4_f16", "mxfp4_quantize_nvfp4_grouped_f16",
     "mxfp4_quantize_nvfp4_grouped_scatter", "mxfp4_quantize_nvfp4_grouped_scatter_f16",
-    "quantize_nvfp4_grouped_scatter",
+    "quantize_nvfp4_grouped_scatter", "mxfp4_nvfp4_scatter_workspace_bytes",
+    "mxfp4_quantize_nvfp4_grouped_scatter_ws", "mxfp4_quantize_nvfp4_grouped_scatter_ws_f16",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300.so")
@@ -136,6 +137,13 @@ def _load(path=LIB_PATH):
         getattr(L, name).restype = ctypes.c_int
         getattr(L, name).argtypes = [vp, i64, i64, i64, vp, i32, i64, vp, i32, vp, vp, vp, vp, vp,
                                      vp]
+    for name in ("mxfp4_quantize_nvfp4_grouped_scatter_ws",
+                 "mxfp4_quantize_nvfp4_grouped_scatter_ws_f16"):
+        getattr(L, name).restype = ctypes.c_int
+        getattr(L, name).argtypes = [vp, i64, i64, i64, vp, i32, i64, vp, i32, vp, vp,
+                                     ctypes.c_size_t, vp, vp, vp, vp, vp]
+    L.mxfp4_nvfp4_scatter_workspace_bytes.restype = ctypes.c_size_t
+    L.mxfp4_nvfp4_scatter_workspace_bytes.argtypes = [i64, i32, i64]
     L.mxfp4_dequantize_nvfp4.restype = ctypes.c_int
     L.mxfp4_dequantize_nvfp4.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     L.mxfp4_status_string.restype = ctypes.c_char_p
@@ -542,9 +550,11 @@ def mxfp4_quantize_nvfp4_grouped_f16(x, expert_offsets, global_scales, codes, sc
 
 
 def _nvfp4_scatter(x, dest_rows, expert_offsets, total_rows, global_scales, codes, scales,
-                   scale_row_offsets, status, stream, f16) -> None:
-    name = "mxfp4_quantize_nvfp4_grouped_scatter" + ("_f16" if f16 else "")
+                   scale_row_offsets, status, stream, f16, workspace=None) -> None:
+    name = ("mxfp4_quantize_nvfp4_grouped_scatter" + ("_ws" if workspace is not None else "") +
+            ("_f16" if f16 else ""))
     _need_cuda("x", x, torch.float16 if f16 else torch.bfloat16)
+    _need_cuda("workspace", workspace, torch.uint8)
     _need_cuda("dest_rows", dest_rows, torch.int32)
     _need_cuda("expert_offsets", expert_offsets, torch.int32)
     _need_cuda("global_scales", global_scales, torch.float32)
@@ -560,11 +570,12 @@ def _nvfp4_scatter(x, dest_rows, expert_offsets, total_rows, global_scales, code
     E = expert_offsets.numel() - 1
     if global_scales.numel() != E:
         raise ValueError("global_scales needs one entry per expert")
+    ws = () if workspace is None else (_ptr(workspace), workspace.numel())
     with torch.cuda.device(_device_of(x, dest_rows, expert_offsets, global_scales, codes, scales,
-                                      scale_row_offsets, status)):
+                                      scale_row_offsets, status, workspace)):
         _check(getattr(_lib, name)(
             _ptr(x), T, K, x.stride(0), _ptr(dest_rows), dest_rows.shape[1], int(total_rows),
-            _ptr(expert_offsets), E, _ptr(global_scales), _ptr(codes), _ptr(scales),
+            _ptr(expert_offsets), E, _ptr(global_scales), *ws, _ptr(codes), _ptr(scales),
             _ptr(scale_row_offsets), _ptr(status), _stream(stream, x.device)), name)
 
 
@@ -584,6 +595,29 @@ def mxfp4_quantize_nvfp4_grouped_scatter_f16(x, dest_rows, expert_offsets, total
     """mxfp4_quantize_nvfp4_grouped_scatter for FP16 ``x``."""
     _nvfp4_scatter(x, dest_rows, expert_offsets, total_rows, global_scales, codes, scales,
                    scale_row_offsets, status, stream, True)
+
+
+def mxfp4_nvfp4_scatter_workspace_bytes(total_rows: int, E: int, K: int) -> int:
+    return int(_lib.mxfp4_nvfp4_scatter_workspace_bytes(int(total_rows), int(E), int(K)))
+
+
+def mxfp4_quantize_nvfp4_grouped_scatter_ws(x, dest_rows, expert_offsets, total_rows: int,
+                                            global_scales, workspace, codes, scales,
+                                            scale_row_offsets, status=None, stream=None) -> None:
+    """mxfp4_quantize_nvfp4_grouped_scatter with identical results, each
+    route's scale bytes staged by padded row in ``workspace`` (uint8 device, >=
+    mxfp4_nvfp4_scatter_workspace_bytes) and tiled by a second kernel."""
+    _nvfp4_scatter(x, dest_rows, expert_offsets, total_rows, global_scales, codes, scales,
+                   scale_row_offsets, status, stream, False, workspace)
+
+
+def mxfp4_quantize_nvfp4_grouped_scatter_ws_f16(x, dest_rows, expert_offsets, total_rows: int,
+                                                global_scales, workspace, codes, scales,
+                                                scale_row_offsets, status=None,
+                                                stream=None) -> None:
+    """mxfp4_quantize_nvfp4_grouped_scatter_ws for FP16 ``x``."""
+    _nvfp4_scatter(x, dest_rows, expert_offsets, total_rows, global_scales, codes, scales,
+                   scale_row_offsets, status, stream, True, workspace)
 
 
 def mxfp4_dequantize_nvfp4(codes, scales, global_scale, M: int, K: int, y, stream=None) -> None:
@@ -724,10 +758,12 @@ def quantize_nvfp4_grouped(x, expert_offsets, global_scales, stream=None):
 
 
 def quantize_nvfp4_grouped_scatter(x, dest_rows, expert_offsets, global_scales, total_rows=None,
-                                   stream=None):
+                                   stream=None, staged=True):
     """Returns (codes, scales, scale_row_offsets, status) of the NVFP4 experts
     quant of the batch ``dest_rows`` dispatches ``x`` (BF16 or FP16) into;
-    rows no route targets come back zero."""
+    rows no route targets come back zero.  By default the scale bytes are
+    staged in a workspace allocated here (same results); staged=False stores
+    each route's scale words straight into the tiled layout."""
     K = x.shape[1]
     total = dest_rows.numel() if total_rows is None else int(total_rows)
     E = expert_offsets.numel() - 1
@@ -737,8 +773,12 @@ def quantize_nvfp4_grouped_scatter(x, dest_rows, expert_offsets, global_scales, 
                          dtype=torch.uint8, device=dev)
     sro = torch.empty(E + 1, dtype=torch.int32, device=dev)
     status = torch.empty(1, dtype=torch.int32, device=dev)
+    ws = None
+    if staged:
+        ws = torch.empty(max(mxfp4_nvfp4_scatter_workspace_bytes(total, E, K), 16),
+                         dtype=torch.uint8, device=dev)
     _nvfp4_scatter(x, dest_rows, expert_offsets, total, global_scales, codes, scales, sro, status,
-                   stream, x.dtype == torch.float16)
+                   stream, x.dtype == torch.float16, ws)
     return codes, scales, sro, status
 
 

@@ -15,6 +15,7 @@
 
 #include "mxfp4_device.cuh"
 #include "mxfp4_internal.h"
+#include "nvfp4_device.cuh"
 #include "../../include/mxfp4.h"
 
 namespace mxfp4 {
@@ -228,15 +229,18 @@ __device__ __forceinline__ void scatter_token(const ScatterParams& p, int64_t t,
   __syncwarp();  // s_code / s_scale are rewritten by the warp's next token
 }
 
-// Map CTA m of the staged token-major scatter: the token + 1 of every padded
-// row a route lands on, and -1 for the pad rows of every segment (rows no
-// route targets keep the 0 of the memset).  The tile kernel reads the map
-// after this launch has completed.  The offsets and padded starts (up to
-// kMapSegs + 1 each) reuse the warps' route arrays s_code and s_scale.
+// Map CTA m of the staged token-major scatter: the token + 1 (or the padded
+// row + 1) of every padded row a route lands on, and -1 for the pad rows of
+// every segment (rows no route targets keep the 0 of the memset).  The tile
+// kernel reads the map after this launch has completed.  The offsets and
+// padded starts (up to kMapSegs + 1 each) reuse the warps' route arrays.
 constexpr int kMapSegs = 511;
 static_assert((kMapSegs + 1) * 4 == kScatterWarps * MXFP4_SCATTER_MAX_TOP_K * 8,
               "one segment array fills one route array");
-__device__ __forceinline__ void scatter_route_map(const ScatterParams& p, int m, int32_t* s_off,
+// kRowValue: record padded row + 1 (the NVFP4 scatter stages each route's
+// scale bytes by padded row) instead of token + 1.
+template <bool kRowValue = false, typename P>
+__device__ __forceinline__ void scatter_route_map(const P& p, int m, int32_t* s_off,
                                                   int32_t* s_pad) {
   const SegmentSearch seg(s_off, s_pad, p.offsets, p.padded, p.E,
                           static_cast<int>(p.total_rows), kMapSegs);
@@ -258,8 +262,10 @@ __device__ __forceinline__ void scatter_route_map(const ScatterParams& p, int m,
     const int32_t* dp = p.dest_rows + i;
     const int32_t v = MXFP4_IN_BOUNDS(p, kDbgRowIndex, dp, 4) ? __ldg(dp) : -1;
     if (v < 0 || v >= p.total_rows) continue;  // the token warps report bad entries
-    int32_t* const tp = p.tok1 + seg.padded_row(v);
-    if (MXFP4_IN_BOUNDS(p, kDbgWork, tp, 4)) *tp = static_cast<int32_t>(i / p.top_k) + 1;
+    const int prow = seg.padded_row(v);
+    int32_t* const tp = p.tok1 + prow;
+    if (MXFP4_IN_BOUNDS(p, kDbgWork, tp, 4))
+      *tp = kRowValue ? prow + 1 : static_cast<int32_t>(i / p.top_k) + 1;
   }
 }
 
@@ -351,6 +357,189 @@ __global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_ke
     if (!overflow_entry(p, j, t, dsts)) return;
     __syncwarp();
     s_next[warp] = j;
+  }
+}
+
+// NVFP4 experts quant with the MoE dispatch as a scatter: route j of token t
+// lands on row dest_rows[t][j] of the expert-sorted batch, whose segment e
+// has global scale g[e].  One warp per token: the row is read once, in passes
+// of 512 elements (lane = one 16-element block), and each block's max and
+// q = vecMax / 6 are taken once; then, per route, the block's E4M3 byte
+// (g[e] * q), inverse scale and codes with that route's global scale (a
+// token's codes differ per expert).  Codes leave as one 256-byte run per
+// route and pass.  The scale bytes go either
+//   direct: as the 4-byte word of each k-tile (4 lanes) into the tiled layout
+//     of every route, under an L2 evict-last policy (14.7 M scattered words on
+//     the MoE batch); the first E CTAs zero the segments' pad rows; or
+//   staged (kStaged): as one 32-byte run per route and pass into the route's
+//     padded row of a workspace, which tile_scales_kernel then writes to the
+//     tiled layout whole; the first map_ctas CTAs record each routed row's
+//     padded row (pad rows -1) beside the token warps.
+struct Nvfp4ScatterParams {
+  const uint8_t* __restrict__ x;          // 16-bit token rows
+  int64_t ldx_bytes;
+  int64_t num_tokens;
+  const int32_t* __restrict__ dest_rows;  // [num_tokens, top_k], -1 = not dispatched
+  const float* __restrict__ g;            // [E] global scales
+  uint8_t* __restrict__ codes;
+  uint8_t* __restrict__ scales;
+  const int32_t* __restrict__ offsets;    // [E+1]
+  const int32_t* __restrict__ padded;     // [E+1], written by the offsets kernel
+  int32_t* status;                        // may be NULL
+  int64_t total_rows;
+  int64_t code_ld;                        // K/2
+  int32_t top_k;
+  int32_t E;
+  int32_t sK;                             // K/16
+  int32_t nKT;                            // ceil(sK/4)
+  int32_t pad_ctas;                       // direct: E CTAs zero the pad rows
+  int32_t map_ctas;                       // staged: CTAs writing tok1
+  int32_t* __restrict__ tok1;             // staged: [padded rows] padded row + 1, -1 pad row
+  uint8_t* __restrict__ stage;            // staged: [padded rows, 4 * stage_ld(nKT)] scale bytes
+#ifdef MXFP4_DEBUG_BOUNDS
+  DebugRanges dbg;                        // kDbg slots; kDbgWork: the workspace
+  DebugRanges dbg_g;                      // slot 0: the global scales
+#endif
+};
+
+#ifdef MXFP4_DEBUG_BOUNDS
+#define MXFP4_IN_BOUNDS_G(params, ptr, bytes) \
+  ::mxfp4::debug_in_bounds((params).dbg_g, 0, (ptr), (bytes))
+#else
+#define MXFP4_IN_BOUNDS_G(params, ptr, bytes) true
+#endif
+
+constexpr int kNvScBatch = 2;  // passes with loads in flight together (4 CTAs per SM)
+
+// Byte offset of the scale word of padded row prow in k-tile 0 of the tiled
+// layout (k-tile kt adds kt * 512) — or, staged, of its workspace row.
+template <bool kStaged>
+__device__ __forceinline__ int64_t nv_row_base(int prow, int nKT) {
+  if constexpr (kStaged) return static_cast<int64_t>(prow) * stage_ld(nKT) * 4;
+  return scale_word_base(prow, nKT);
+}
+
+__device__ __forceinline__ void st_keep_u8(void* p, uint32_t v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.u8 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(policy)
+               : "memory");
+}
+
+template <bool kVec32, bool kF16, bool kStaged>
+__global__ void __launch_bounds__(kThreads) nvfp4_scatter_kernel(const Nvfp4ScatterParams p) {
+  __shared__ int64_t s_code[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];  // d * K/2, or -1
+  __shared__ int64_t s_word[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];  // scale row base
+  __shared__ float s_g[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];       // the route's scale
+
+  pdl_wait();
+  pdl_release();
+
+  if (!MXFP4_IN_BOUNDS(p, kDbgPadded, p.padded, (p.E + 1) * 4) ||
+      !MXFP4_IN_BOUNDS(p, kDbgOffsets, p.offsets, (p.E + 1) * 4))
+    return;
+  if (__ldg(p.padded + p.E) < 0) return;  // rejected offsets: nothing is written
+
+  if (static_cast<int>(blockIdx.x) < p.pad_ctas) {
+    // pad rows [n, ceil128(n)) of segment e: zero scale words, row-fastest
+    const int e = blockIdx.x;
+    const int n = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+    const int npad = ((n + kTileRows - 1) / kTileRows) * kTileRows - n;
+    const int P0 = __ldg(p.padded + e) + n;
+    const uint64_t keep = l2_evict_last_policy();
+    for (int i = threadIdx.x; i < npad * p.nKT; i += kThreads) {
+      const int kt = i / npad;
+      uint8_t* wp = p.scales + scale_word_base(P0 + (i - kt * npad), p.nKT) + kt * kChunkBytes;
+      if (MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4)) st_keep_u32(wp, 0u, keep);
+    }
+    return;
+  }
+  if constexpr (kStaged) {
+    const int m = static_cast<int>(blockIdx.x) - p.pad_ctas;
+    if (m < p.map_ctas) {  // uniform over the block
+      scatter_route_map<true>(p, m, reinterpret_cast<int32_t*>(&s_code[0][0]),
+                              reinterpret_cast<int32_t*>(&s_word[0][0]));
+      return;
+    }
+  }
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int lead = p.pad_ctas + (kStaged ? p.map_ctas : 0);
+  const int64_t t = static_cast<int64_t>(blockIdx.x - lead) * kScatterWarps + warp;
+  if (t >= p.num_tokens) return;  // whole warp; no block-wide barrier below
+
+  // routes, one per lane
+  int64_t co = -1, wo = -1;
+  float ge = 0.0f;
+  bool bad = false;
+  if (lane < p.top_k) {
+    const int32_t* dp = p.dest_rows + t * p.top_k + lane;
+    const int32_t v = MXFP4_IN_BOUNDS(p, kDbgRowIndex, dp, 4) ? __ldg(dp) : -1;
+    if (v >= 0 && v < p.total_rows) {
+      const int e = find_segment(p.offsets, p.E, v, static_cast<int>(p.total_rows));
+      co = static_cast<int64_t>(v) * p.code_ld;
+      wo = nv_row_base<kStaged>(__ldg(p.padded + e) + (v - __ldg(p.offsets + e)), p.nKT);
+      ge = MXFP4_IN_BOUNDS_G(p, p.g + e, 4) ? __ldg(p.g + e) : 0.0f;
+    } else {
+      bad = v != -1;
+    }
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && p.status != nullptr &&
+      MXFP4_IN_BOUNDS(p, kDbgStatus, p.status, 4))
+    atomicExch(p.status, MXFP4_EINDEX);
+  s_code[warp][lane] = co;
+  s_word[warp][lane] = wo;
+  s_g[warp][lane] = ge;
+  __syncwarp();
+
+  const uint8_t* xrow = p.x + t * p.ldx_bytes + lane * 32;
+  const int n_pass = (p.sK + 31) / 32;  // 32 blocks per pass
+  const uint64_t keep = l2_evict_last_policy();
+  for (int p0 = 0; p0 < n_pass; p0 += kNvScBatch) {
+    uint4 v[kNvScBatch][2];
+    float q[kNvScBatch];
+#pragma unroll
+    for (int b = 0; b < kNvScBatch; ++b) {
+      v[b][0] = v[b][1] = make_uint4(0u, 0u, 0u, 0u);
+      const int blk = (p0 + b) * 32 + lane;
+      const uint8_t* xp = xrow + static_cast<int64_t>(p0 + b) * 1024;
+      if (p0 + b < n_pass && blk < p.sK && MXFP4_IN_BOUNDS(p, kDbgX, xp, 32))
+        load32<kVec32>(xp, v[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < kNvScBatch; ++b) q[b] = nv_block_q<kF16>(v[b]);
+    for (int j = 0; j < p.top_k; ++j) {
+      const int64_t c = s_code[warp][j];
+      if (c < 0) continue;  // the same for every lane of the warp
+      const int64_t w = s_word[warp][j];
+      const float g = s_g[warp][j];
+#pragma unroll
+      for (int b = 0; b < kNvScBatch; ++b) {
+        const int pass = p0 + b;
+        const int blk = pass * 32 + lane;
+        const uint32_t byte = cvt_e4m3_satfinite(g * q[b]);
+        const uint2 code = nv_codes<kF16>(v[b], byte, byte != 0u ? g / e4m3_to_f32(byte) : 0.0f);
+        uint8_t* const cp = p.codes + c + static_cast<int64_t>(blk) * 8;
+        if (pass < n_pass && blk < p.sK && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 8))
+          st_stream_v2(cp, code);
+        if constexpr (kStaged) {
+          // the route's scale bytes, 32 per pass, into its workspace row (zero
+          // for the pad columns past sK)
+          uint8_t* const bp = p.stage + w + blk;
+          if (pass < n_pass && blk < 4 * p.nKT && MXFP4_IN_BOUNDS(p, kDbgWork, bp, 1))
+            st_keep_u8(bp, byte, keep);
+        } else {
+          // scale word of k-tile pass*8 + lane/4: the bytes of lanes +0..+3
+          const uint32_t word = byte | (__shfl_down_sync(0xFFFFFFFFu, byte, 1) << 8) |
+                                (__shfl_down_sync(0xFFFFFFFFu, byte, 2) << 16) |
+                                (__shfl_down_sync(0xFFFFFFFFu, byte, 3) << 24);
+          const int kt = pass * 8 + (lane >> 2);
+          uint8_t* const wp = p.scales + w + static_cast<int64_t>(kt) * kChunkBytes;
+          if (pass < n_pass && (lane & 3) == 0 && kt < p.nKT &&
+              MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4))
+            st_keep_u32(wp, word, keep);
+        }
+      }
+    }
   }
 }
 
@@ -787,6 +976,101 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   debug_range(ts.dbg, kDbgWork, p.stage, T * stage_ld(ts.nKT) * 4);
 #endif
   return launch_pdl(tile_scales_kernel<false>, static_cast<unsigned>(bound_tiles), kTileThreads,
+                    0, stream, ts);
+}
+
+// NVFP4 experts quant with the dispatch as a scatter.  Workspace (staged):
+// [tok1: PT int32][stage: PT rows x stage_ld(nKT) words], PT padded rows.
+int64_t nvfp4_scatter_workspace_ints(int64_t total_rows, int64_t E, int64_t K) {
+  const int32_t nKT = static_cast<int32_t>((K / 16 + kTileBlocks - 1) / kTileBlocks);
+  return gather_tok_ints(total_rows, E) * (1 + stage_ld(nKT));
+}
+
+cudaError_t launch_quantize_nvfp4_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
+                                                  int64_t ldx, const int32_t* dest_rows,
+                                                  int32_t top_k, int64_t total_rows,
+                                                  const int32_t* offsets, int32_t E,
+                                                  const float* global_scales, int32_t* workspace,
+                                                  uint8_t* codes, uint8_t* scales,
+                                                  int32_t* scale_row_offsets, int32_t* status,
+                                                  int64_t bound_tiles, bool f16,
+                                                  cudaStream_t stream) {
+  const bool staged = workspace != nullptr && total_rows > 0 && E > 0 && K > 0;
+  const int64_t PT = staged ? gather_tok_ints(total_rows, E) : 0;
+  cudaError_t err = cudaSuccess;
+  if (staged) {  // first, so that the kernels below follow one another directly
+    err = cudaMemsetAsync(workspace, 0, static_cast<size_t>(PT) * 4, stream);
+    if (err != cudaSuccess) return err;
+  }
+  err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
+  if (err != cudaSuccess || E == 0 || K == 0) return err;
+  Nvfp4ScatterParams p{};
+  p.x = static_cast<const uint8_t*>(x);
+  p.ldx_bytes = ldx * 2;
+  p.num_tokens = num_tokens;
+  p.dest_rows = dest_rows;
+  p.g = global_scales;
+  p.codes = codes;
+  p.scales = scales;
+  p.offsets = offsets;
+  p.padded = scale_row_offsets;
+  p.status = status;
+  p.total_rows = total_rows;
+  p.code_ld = K / 2;
+  p.top_k = top_k;
+  p.E = E;
+  p.sK = static_cast<int32_t>(K / 16);
+  p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
+  p.pad_ctas = staged ? 0 : E;
+  if (staged) {
+    const int64_t items = num_tokens * top_k > static_cast<int64_t>(E) * kTileRows
+                              ? num_tokens * top_k
+                              : static_cast<int64_t>(E) * kTileRows;
+    const int64_t need = (items + 4 * kThreads - 1) / (4 * kThreads);
+    p.map_ctas = static_cast<int32_t>(need < 1 ? 1 : (need < sm_count() ? need : sm_count()));
+    p.tok1 = workspace;
+    p.stage = reinterpret_cast<uint8_t*>(workspace + PT);
+  }
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(p.dbg, kDbgX, x, num_tokens > 0 ? ((num_tokens - 1) * ldx + K) * 2 : 0);
+  debug_range(p.dbg, kDbgCodes, codes, total_rows * (K / 2));
+  debug_range(p.dbg, kDbgScales, scales, bound_tiles * p.nKT * kChunkBytes);
+  debug_range(p.dbg, kDbgOffsets, offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(p.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(p.dbg, kDbgRowIndex, dest_rows, num_tokens * top_k * 4);
+  debug_range(p.dbg, kDbgStatus, status, status ? 4 : 0);
+  debug_range(p.dbg, kDbgWork, workspace, staged ? PT * (1 + stage_ld(p.nKT)) * 4 : 0);
+  debug_range(p.dbg_g, 0, global_scales, static_cast<int64_t>(E) * 4);
+#endif
+  const int64_t grid =
+      p.pad_ctas + p.map_ctas + (num_tokens + kScatterWarps - 1) / kScatterWarps;
+  const bool v32 = vec32_ok(x, p.ldx_bytes);
+  using Kernel = void (*)(const Nvfp4ScatterParams);
+  static constexpr Kernel kKernels[2][2][2] = {
+      {{nvfp4_scatter_kernel<false, false, false>, nvfp4_scatter_kernel<false, false, true>},
+       {nvfp4_scatter_kernel<false, true, false>, nvfp4_scatter_kernel<false, true, true>}},
+      {{nvfp4_scatter_kernel<true, false, false>, nvfp4_scatter_kernel<true, false, true>},
+       {nvfp4_scatter_kernel<true, true, false>, nvfp4_scatter_kernel<true, true, true>}}};
+  if (grid > 0) {
+    err = launch_pdl(kKernels[v32][f16][staged], static_cast<unsigned>(grid), kThreads, 0, stream,
+                     p);
+    if (err != cudaSuccess) return err;
+  }
+  if (!staged || bound_tiles == 0) return cudaSuccess;
+  TileScalesParams ts{};
+  ts.tok1 = workspace;
+  ts.stage = reinterpret_cast<const uint32_t*>(p.stage);
+  ts.scales = scales;
+  ts.padded = scale_row_offsets;
+  ts.E = E;
+  ts.nKT = p.nKT;
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(ts.dbg, kDbgScales, scales, bound_tiles * ts.nKT * kChunkBytes);
+  debug_range(ts.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(ts.dbg, kDbgRowIndex, workspace, PT * 4);
+  debug_range(ts.dbg, kDbgWork, p.stage, PT * stage_ld(ts.nKT) * 4);
+#endif
+  return launch_pdl(tile_scales_kernel<true>, static_cast<unsigned>(bound_tiles), kTileThreads,
                     0, stream, ts);
 }
 

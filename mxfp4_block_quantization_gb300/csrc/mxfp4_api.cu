@@ -651,8 +651,9 @@ namespace {
 int nvfp4_scatter_checked(const void* x, int64_t num_tokens, int64_t K, int64_t ldx,
                           const int32_t* dest_rows, int32_t top_k, int64_t total_rows,
                           const int32_t* expert_offsets, int32_t E, const float* global_scales,
-                          uint8_t* codes, uint8_t* scales, int32_t* scale_row_offsets,
-                          int32_t* status, bool f16, void* stream) {
+                          void* workspace, size_t workspace_bytes, bool use_ws, uint8_t* codes,
+                          uint8_t* scales, int32_t* scale_row_offsets, int32_t* status, bool f16,
+                          void* stream) {
   if (num_tokens < 0 || total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
   if (top_k < 1 || top_k > MXFP4_SCATTER_MAX_TOP_K) return MXFP4_EINVAL;
   if (K % 16 != 0 || ldx < K) return MXFP4_ESHAPE;
@@ -666,6 +667,13 @@ int nvfp4_scatter_checked(const void* x, int64_t num_tokens, int64_t K, int64_t 
   if (total_rows + 127 * static_cast<int64_t>(E) > INT32_MAX) return MXFP4_ESHAPE;
   if (E + ceil_div(num_tokens, 8) > kMaxGrid) return MXFP4_ESHAPE;
   if (num_tokens > (INT64_MAX / 4) / (ldx > top_k ? ldx : top_k)) return MXFP4_ESHAPE;
+  int64_t ws_bytes = 0;
+  if (use_ws) {
+    ws_bytes = mxfp4::nvfp4_scatter_workspace_ints(total_rows, E, K) * 4;
+    if (rows && (!workspace || workspace_bytes < static_cast<size_t>(ws_bytes)))
+      return MXFP4_EINVAL;
+    if (workspace && !aligned16(workspace)) return MXFP4_EALIGN;
+  }
   if ((x && (!aligned16(x) || ldx % 8 != 0)) || (codes && !aligned16(codes)) ||
       (scales && !aligned16(scales)) || (reinterpret_cast<uintptr_t>(dest_rows) & 3u) ||
       (reinterpret_cast<uintptr_t>(global_scales) & 3u) ||
@@ -678,21 +686,23 @@ int nvfp4_scatter_checked(const void* x, int64_t num_tokens, int64_t K, int64_t 
       range_of(dest_rows, reads ? num_tokens * top_k * 4 : 0),
       range_of(expert_offsets, (static_cast<int64_t>(E) + 1) * 4),
       range_of(global_scales, rows ? static_cast<int64_t>(E) * 4 : 0)};
-  const Range outs[4] = {
+  const Range outs[5] = {
       range_of(codes, total_rows * (K / 2)),
       range_of(scales,
                static_cast<int64_t>(mxfp4_nvfp4_grouped_scale_bytes_bound(total_rows, E, K))),
       range_of(scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4),
-      range_of(status, status ? 4 : 0)};
-  for (int i = 0; i < 4; ++i) {
+      range_of(status, status ? 4 : 0),
+      range_of(workspace, use_ws && rows ? ws_bytes : 0)};
+  for (int i = 0; i < 5; ++i) {
     for (int j = 0; j < 4; ++j)
       if (overlap(outs[i], ins[j])) return MXFP4_EALIAS;
-    for (int j = i + 1; j < 4; ++j)
+    for (int j = i + 1; j < 5; ++j)
       if (overlap(outs[i], outs[j])) return MXFP4_EALIAS;
   }
   return from_cuda(mxfp4::launch_quantize_nvfp4_grouped_scatter(
       x, reads ? num_tokens : 0, K, ldx, dest_rows, top_k, total_rows, expert_offsets, E,
-      global_scales, codes, scales, scale_row_offsets, status, K == 0 ? 0 : bound_tiles, f16,
+      global_scales, use_ws && rows ? static_cast<int32_t*>(workspace) : nullptr, codes, scales,
+      scale_row_offsets, status, K == 0 ? 0 : bound_tiles, f16,
       static_cast<cudaStream_t>(stream)));
 }
 
@@ -707,8 +717,8 @@ int mxfp4_quantize_nvfp4_grouped_scatter(const void* x, int64_t num_tokens, int6
                                          uint8_t* scales, int32_t* scale_row_offsets,
                                          int32_t* status, void* stream) {
   return nvfp4_scatter_checked(x, num_tokens, K, ldx, dest_rows, top_k, total_rows,
-                               expert_offsets, E, global_scales, codes, scales, scale_row_offsets,
-                               status, false, stream);
+                               expert_offsets, E, global_scales, nullptr, 0, false, codes, scales,
+                               scale_row_offsets, status, false, stream);
 }
 
 int mxfp4_quantize_nvfp4_grouped_scatter_f16(const void* x, int64_t num_tokens, int64_t K,
@@ -719,8 +729,40 @@ int mxfp4_quantize_nvfp4_grouped_scatter_f16(const void* x, int64_t num_tokens, 
                                              uint8_t* scales, int32_t* scale_row_offsets,
                                              int32_t* status, void* stream) {
   return nvfp4_scatter_checked(x, num_tokens, K, ldx, dest_rows, top_k, total_rows,
-                               expert_offsets, E, global_scales, codes, scales, scale_row_offsets,
-                               status, true, stream);
+                               expert_offsets, E, global_scales, nullptr, 0, false, codes, scales,
+                               scale_row_offsets, status, true, stream);
+}
+
+size_t mxfp4_nvfp4_scatter_workspace_bytes(int64_t total_rows, int32_t E, int64_t K) {
+  if (total_rows < 0 || E < 0 || K < 0 || K % 16 != 0) return 0;
+  if (total_rows + 127 * static_cast<int64_t>(E) > INT32_MAX) return 0;
+  return static_cast<size_t>(mxfp4::nvfp4_scatter_workspace_ints(total_rows, E, K) * 4);
+}
+
+int mxfp4_quantize_nvfp4_grouped_scatter_ws(const void* x, int64_t num_tokens, int64_t K,
+                                            int64_t ldx, const int32_t* dest_rows, int32_t top_k,
+                                            int64_t total_rows, const int32_t* expert_offsets,
+                                            int32_t E, const float* global_scales,
+                                            void* workspace, size_t workspace_bytes,
+                                            uint8_t* codes, uint8_t* scales,
+                                            int32_t* scale_row_offsets, int32_t* status,
+                                            void* stream) {
+  return nvfp4_scatter_checked(x, num_tokens, K, ldx, dest_rows, top_k, total_rows,
+                               expert_offsets, E, global_scales, workspace, workspace_bytes, true,
+                               codes, scales, scale_row_offsets, status, false, stream);
+}
+
+int mxfp4_quantize_nvfp4_grouped_scatter_ws_f16(const void* x, int64_t num_tokens, int64_t K,
+                                                int64_t ldx, const int32_t* dest_rows,
+                                                int32_t top_k, int64_t total_rows,
+                                                const int32_t* expert_offsets, int32_t E,
+                                                const float* global_scales, void* workspace,
+                                                size_t workspace_bytes, uint8_t* codes,
+                                                uint8_t* scales, int32_t* scale_row_offsets,
+                                                int32_t* status, void* stream) {
+  return nvfp4_scatter_checked(x, num_tokens, K, ldx, dest_rows, top_k, total_rows,
+                               expert_offsets, E, global_scales, workspace, workspace_bytes, true,
+                               codes, scales, scale_row_offsets, status, true, stream);
 }
 
 int mxfp4_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, const float* global_scale,

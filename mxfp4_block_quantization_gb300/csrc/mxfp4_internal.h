@@ -80,13 +80,18 @@ cudaError_t launch_quantize_nvfp4_grouped(const void* x, int64_t total_rows, int
                                           int32_t* status, int64_t bound_tiles, bool f16,
                                           cudaStream_t stream);
 // NVFP4 experts quant with the dispatch as a scatter (token, route -> row).
+// With a workspace (nvfp4_scatter_workspace_ints int32, 16-byte aligned)
+// each route's scale bytes are staged by padded row and a tile kernel writes
+// the tiled scales; with NULL they go into the tiled layout directly.
+int64_t nvfp4_scatter_workspace_ints(int64_t total_rows, int64_t E, int64_t K);
 cudaError_t launch_quantize_nvfp4_grouped_scatter(const void* x, int64_t num_tokens, int64_t K,
                                                   int64_t ldx, const int32_t* dest_rows,
                                                   int32_t top_k, int64_t total_rows,
                                                   const int32_t* offsets, int32_t E,
-                                                  const float* global_scales, uint8_t* codes,
-                                                  uint8_t* scales, int32_t* scale_row_offsets,
-                                                  int32_t* status, int64_t bound_tiles, bool f16,
+                                                  const float* global_scales, int32_t* workspace,
+                                                  uint8_t* codes, uint8_t* scales,
+                                                  int32_t* scale_row_offsets, int32_t* status,
+                                                  int64_t bound_tiles, bool f16,
                                                   cudaStream_t stream);
 cudaError_t launch_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales,
                                     const float* global_scale, int64_t M, int64_t K, void* y,

@@ -234,6 +234,32 @@ def test_nvfp4_grouped_scatter_validation(lib):
         *ok[:2], 40, 40, *ok[4:]) == lib.MXFP4_ESHAPE
 
 
+def test_nvfp4_grouped_scatter_ws_validation(lib):
+    f = lib._lib.mxfp4_quantize_nvfp4_grouped_scatter_ws
+    need = lib.mxfp4_nvfp4_scatter_workspace_bytes(400, 2, 64)
+    # PT = floor((400 + 254) / 128) * 128 = 640 padded rows: the row map (4 B) and a staged
+    # row of ceil(64/64) = 1 scale word, padded to 4 words (16 B), per padded row
+    assert need == 640 * (4 + 16)
+    assert lib.mxfp4_nvfp4_scatter_workspace_bytes(400, 2, 7168) == 640 * (4 + 448)
+    assert lib.mxfp4_nvfp4_scatter_workspace_bytes(400, 2, 40) == 0
+    # x, T, K, ldx, dest, top_k, total, off, E, g, ws, ws_bytes, codes, scales, sro, st, stream
+    ok = [A, 50, 64, 64, 2 * A, 8, 400, 3 * A, 2, 9 * A, 8 * A, need, 4 * A, 5 * A, 6 * A,
+          None, None]
+
+    def call(**kw):
+        names = ["x", "T", "K", "ldx", "dst", "k", "tot", "off", "E", "g", "ws", "wsb", "c", "s",
+                 "sro", "st", "strm"]
+        a = dict(zip(names, ok))
+        a.update(kw)
+        return f(*[a[n] for n in names])
+
+    assert call(ws=None) == lib.MXFP4_EINVAL
+    assert call(wsb=need - 16) == lib.MXFP4_EINVAL
+    assert call(ws=8 * A + 8) == lib.MXFP4_EALIGN
+    assert call(ws=4 * A + 16) == lib.MXFP4_EALIAS            # workspace overlaps the codes
+    assert call(K=40, ldx=40) == lib.MXFP4_ESHAPE
+
+
 def test_quantize_f16_validation(lib):
     f = lib._lib.mxfp4_quantize_f16
     assert f(A, 4, 48, 48, 2 * A, 3 * A, None) == lib.MXFP4_ESHAPE

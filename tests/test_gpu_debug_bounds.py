@@ -153,6 +153,8 @@ def test_everything_in_bounds(libs):
     g3d[2, 0] = 1 << 20
     cases.append(lambda: written(mx.quantize_nvfp4_grouped_scatter(g3.x_tokens, g3d, g3.offsets,
                                                                    gsc), 2 * 1056))  # K/16 cols
+    cases.append(lambda: written(mx.quantize_nvfp4_grouped_scatter(g3.x_tokens, g3d, g3.offsets,
+                                                                   gsc, staged=False), 2 * 1056))
     # NVFP4 experts quant (K a multiple of 16 but not 32 included)
     gn = W.moe_grouped(seed=10, tokens=150, top_k=3, num_experts=7, K=80, device="cuda")
     gsn = torch.linspace(0.5, 40.0, 7, device="cuda")

@@ -115,16 +115,24 @@ def test_fuzz_grouped_gather_scatter(mx, seed):
     s0_nv = rng.integers(0, 256, nsb_nv, dtype=np.uint8)
     rc_nv, cn_o, sn_o, _ = oracle.nvfp4_quantize_grouped_scatter(xb, dest, off, total, gs, c0,
                                                                  s0_nv, f16=f16)
-    codes = torch.from_numpy(c0).cuda()
-    scales = torch.from_numpy(s0_nv).cuda()
-    fn = (mx.mxfp4_quantize_nvfp4_grouped_scatter_f16 if f16
-          else mx.mxfp4_quantize_nvfp4_grouped_scatter)
-    fn(xp, torch.from_numpy(dest).cuda(), off_d, total, torch.from_numpy(gs).cuda(), codes,
-       scales, sro, st)
-    torch.cuda.synchronize()
-    assert int(st.item()) == rc_nv == 0
-    assert np.array_equal(codes.cpu().numpy(), cn_o)
-    assert np.array_equal(scales.cpu().numpy(), sn_o)
+    for staged in (False, True):
+        codes = torch.from_numpy(c0).cuda()
+        scales = torch.from_numpy(s0_nv).cuda()
+        args = (xp, torch.from_numpy(dest).cuda(), off_d, total, torch.from_numpy(gs).cuda())
+        if staged:
+            ws = torch.empty(max(mx.mxfp4_nvfp4_scatter_workspace_bytes(total, E, K), 16),
+                             dtype=torch.uint8, device="cuda")
+            fn = (mx.mxfp4_quantize_nvfp4_grouped_scatter_ws_f16 if f16
+                  else mx.mxfp4_quantize_nvfp4_grouped_scatter_ws)
+            fn(*args, ws, codes, scales, sro, st)
+        else:
+            fn = (mx.mxfp4_quantize_nvfp4_grouped_scatter_f16 if f16
+                  else mx.mxfp4_quantize_nvfp4_grouped_scatter)
+            fn(*args, codes, scales, sro, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == rc_nv == 0, staged
+        assert np.array_equal(codes.cpu().numpy(), cn_o), staged
+        assert np.array_equal(scales.cpu().numpy(), sn_o), staged
     # gather (both kernels): dropped rows have index -1 -> zero rows, EINDEX
     rc_g, cg_o, sg_o, _ = oracle.quantize_grouped_gather(xb, row_tok, off, f16=f16)
     used = int(sro_o[-1]) * ((K // 32 + 3) // 4 * 4)

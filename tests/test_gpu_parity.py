@@ -1039,7 +1039,7 @@ def test_nvfp4_grouped_moe_full_size_sampled(mx):
 
 
 # ------------------------------------ NVFP4 experts quant, dispatch as scatter
-def run_nvfp4_scatter(mx, x, dest, offsets, total, gs, seed=0):
+def run_nvfp4_scatter(mx, x, dest, offsets, total, gs, seed=0, ws=False):
     """The NVFP4 scatter through the C ABI into guard-banded buffers with a
     random prefill (the oracle gets the same bytes); returns GPU and oracle
     results."""
@@ -1056,11 +1056,21 @@ def run_nvfp4_scatter(mx, x, dest, offsets, total, gs, seed=0):
     scales.t.copy_(torch.from_numpy(s0))
     sro = Guarded(4 * (E + 1), torch.int32)
     status = Guarded(4, torch.int32)
-    fn = (mx.mxfp4_quantize_nvfp4_grouped_scatter_f16 if f16
-          else mx.mxfp4_quantize_nvfp4_grouped_scatter)
-    fn(x, dest, offsets, total, torch.from_numpy(gs).cuda(), codes.t, scales.t, sro.t, status.t)
+    guards = [codes, scales, sro, status]
+    g_d = torch.from_numpy(gs).cuda()
+    if ws:
+        work = Guarded(max(mx.mxfp4_nvfp4_scatter_workspace_bytes(total, E, K), 16))
+        work.t.fill_(0x5A)                            # contents on entry must not matter
+        guards.append(work)
+        fn = (mx.mxfp4_quantize_nvfp4_grouped_scatter_ws_f16 if f16
+              else mx.mxfp4_quantize_nvfp4_grouped_scatter_ws)
+        fn(x, dest, offsets, total, g_d, work.t, codes.t, scales.t, sro.t, status.t)
+    else:
+        fn = (mx.mxfp4_quantize_nvfp4_grouped_scatter_f16 if f16
+              else mx.mxfp4_quantize_nvfp4_grouped_scatter)
+        fn(x, dest, offsets, total, g_d, codes.t, scales.t, sro.t, status.t)
     torch.cuda.synchronize()
-    for g in (codes, scales, sro, status):
+    for g in guards:
         g.check()
     gpu = (codes.t.cpu().numpy(), scales.t.cpu().numpy(), sro.t.cpu().numpy(),
            int(status.t.cpu()[0]))
@@ -1073,17 +1083,17 @@ def run_nvfp4_scatter(mx, x, dest, offsets, total, gs, seed=0):
 
 @pytest.mark.parametrize("tokens,top_k,E,K", [
     (1, 1, 1, 16), (129, 3, 5, 80), (300, 2, 7, 2880), (64, 32, 40, 96), (257, 8, 16, 1056)])
-def test_nvfp4_scatter_shapes(mx, tokens, top_k, E, K):
+def test_nvfp4_scatter_shapes(mx, tokens, top_k, E, K, scatter_ws):
     g = W.moe_grouped(seed=tokens + K + 5, tokens=tokens, top_k=top_k, num_experts=E, K=K,
                       device="cuda")
     gs = _expert_gscales(E, K)
     gpu, orc = run_nvfp4_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, g.row_index.numel(),
-                                 gs, seed=K)
+                                 gs, seed=K, ws=scatter_ws)
     assert_scatter_parity(gpu, orc)
 
 
 @pytest.mark.parametrize("f16", [False, True])
-def test_nvfp4_scatter_dropped_routes_strided_and_aligned(mx, f16):
+def test_nvfp4_scatter_dropped_routes_strided_and_aligned(mx, f16, scatter_ws):
     g = W.moe_grouped(seed=51, tokens=300, top_k=4, num_experts=9, K=160, device="cuda")
     dst = g.dest_rows.clone()
     drop = torch.rand(dst.shape, generator=torch.Generator().manual_seed(5)) < 0.2
@@ -1093,24 +1103,28 @@ def test_nvfp4_scatter_dropped_routes_strided_and_aligned(mx, f16):
     wide = torch.zeros((300, 184), dtype=xt.dtype, device="cuda")
     wide[:, 8:168] = xt
     for x in (xt, wide[:, 8:168], offset16_any(xt)):
-        gpu, orc = run_nvfp4_scatter(mx, x, dst, g.offsets, g.row_index.numel(), gs, seed=52)
+        gpu, orc = run_nvfp4_scatter(mx, x, dst, g.offsets, g.row_index.numel(), gs, seed=52,
+                                     ws=scatter_ws)
         assert_scatter_parity(gpu, orc)
 
 
-def test_nvfp4_scatter_bad_entries_offsets_and_no_tokens(mx):
+def test_nvfp4_scatter_bad_entries_offsets_and_no_tokens(mx, scatter_ws):
     g = W.moe_grouped(seed=53, tokens=140, top_k=2, num_experts=3, K=64, device="cuda")
     total = g.row_index.numel()
     gs = np.array([1.0, 7.5, 0.3], np.float32)
     dst = g.dest_rows.clone()
     dst[3, 1] = total
     dst[7, 0] = -2
-    gpu, orc = run_nvfp4_scatter(mx, g.x_tokens, dst, g.offsets, total, gs, seed=54)
+    gpu, orc = run_nvfp4_scatter(mx, g.x_tokens, dst, g.offsets, total, gs, seed=54,
+                                 ws=scatter_ws)
     assert orc[3] == -7
     assert_scatter_parity(gpu, orc, want_status=mx.MXFP4_EINDEX)
-    gpu, orc = run_nvfp4_scatter(mx, g.x_tokens[:0], dst[:0], g.offsets, total, gs, seed=55)
+    gpu, orc = run_nvfp4_scatter(mx, g.x_tokens[:0], dst[:0], g.offsets, total, gs, seed=55,
+                                 ws=scatter_ws)
     assert_scatter_parity(gpu, orc)
     bad = torch.tensor([0, 200, 100, total], dtype=torch.int32, device="cuda")
-    gpu, orc = run_nvfp4_scatter(mx, g.x_tokens, g.dest_rows, bad, total, gs, seed=56)
+    gpu, orc = run_nvfp4_scatter(mx, g.x_tokens, g.dest_rows, bad, total, gs, seed=56,
+                                 ws=scatter_ws)
     assert orc[3] == -6 and gpu[3] == mx.MXFP4_EOFFSETS and (gpu[2] == -1).all()
     assert np.array_equal(gpu[0], orc[0]) and np.array_equal(gpu[1], orc[1])  # untouched
 
@@ -1124,10 +1138,14 @@ def test_nvfp4_scatter_moe_full_size(mx):
     gs = torch.from_numpy(_expert_gscales(E, 2)).cuda()
     c1, s1, sro1, st1 = mx.quantize_nvfp4_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets, gs)
     c2, s2, sro2, st2 = mx.quantize_nvfp4_grouped(g.x, g.offsets, gs)
+    c3, s3, sro3, st3 = mx.quantize_nvfp4_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets, gs,
+                                                          staged=False)
     torch.cuda.synchronize()
-    assert int(st1.item()) == int(st2.item()) == 0 and torch.equal(sro1, sro2)
+    assert int(st1.item()) == int(st2.item()) == int(st3.item()) == 0
+    assert torch.equal(sro1, sro2) and torch.equal(sro1, sro3)
     used = int(sro1[-1].item()) * (7168 // 16)
     assert torch.equal(c1, c2) and torch.equal(s1[:used], s2[:used])
+    assert torch.equal(c1, c3) and torch.equal(s1[:used], s3[:used])
     off_h = g.offsets.cpu().numpy()
     for e in (0, 200, E - 1):
         a, b = int(off_h[e]), int(off_h[e + 1])
