@@ -586,7 +586,8 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     return out
 
 
-DISPATCH_CALLS = ("gather", "gather_ws", "scatter", "scatter_ws")
+DISPATCH_CALLS = ("gather", "gather_ws", "scatter", "scatter_ws", "nvfp4_scatter",
+                  "nvfp4_scatter_ws")
 
 
 def run_one_call(args):
@@ -607,7 +608,12 @@ def run_one_call(args):
     sro = torch.empty(E + 1, dtype=torch.int32, device="cuda")
     st = torch.empty(1, dtype=torch.int32, device="cuda")
     ws_bytes = {"gather_ws": lambda: mx.mxfp4_gather_workspace_bytes(T, total, E, K),
-                "scatter_ws": lambda: mx.mxfp4_scatter_workspace_bytes(T, total, E, K)}
+                "scatter_ws": lambda: mx.mxfp4_scatter_workspace_bytes(T, total, E, K),
+                "nvfp4_scatter_ws": lambda: mx.mxfp4_nvfp4_scatter_workspace_bytes(total, E, K)}
+    gs = torch.full((E,), 448.0 * 6.0 / 5.0, device="cuda")
+    if args.call.startswith("nvfp4"):
+        scales = torch.empty(mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K),
+                             dtype=torch.uint8, device="cuda")
     ws = (torch.empty(ws_bytes[args.call](), dtype=torch.uint8, device="cuda")
           if args.call in ws_bytes else None)
     fn = {
@@ -619,6 +625,10 @@ def run_one_call(args):
                                                              total, codes, scales, sro, st),
         "scatter_ws": lambda: mx.mxfp4_quantize_grouped_scatter_ws(
             g.x_tokens, g.dest_rows, g.offsets, total, ws, codes, scales, sro, st),
+        "nvfp4_scatter": lambda: mx.mxfp4_quantize_nvfp4_grouped_scatter(
+            g.x_tokens, g.dest_rows, g.offsets, total, gs, codes, scales, sro, st),
+        "nvfp4_scatter_ws": lambda: mx.mxfp4_quantize_nvfp4_grouped_scatter_ws(
+            g.x_tokens, g.dest_rows, g.offsets, total, gs, ws, codes, scales, sro, st),
     }[args.call]
     fn()
     torch.cuda.synchronize()
