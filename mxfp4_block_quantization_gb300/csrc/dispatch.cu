@@ -1,14 +1,18 @@
 // dispatch.cu — the MoE dispatch fused into the grouped quantize, for
 // sm_103a: the scatter (token -> rows, quantize_scatter_kernel, one warp per
 // token row, read and quantized once), the gather through the same kernel
-// (invert_bucket_kernel inverts the row -> token map first), and the staged
-// forms, where every token's scale words are stored once to a workspace and
-// tile_scales_kernel writes the 128x4-tiled scales in whole chunks.
+// (invert_bucket_kernel inverts the row -> token map first), the NVFP4
+// experts quant as a scatter (nvfp4_scatter_kernel: codes and scales per
+// route, each expert with its own global scale), and the staged forms, where
+// the scale bytes are stored to a workspace (MXFP4: once per token; NVFP4:
+// per route, by padded row) and tile_scales_kernel writes the 128x4-tiled
+// scales in whole chunks.
 //
 // Method: vLLM PR #43557 page ("Fix the E8M0 scale computation in the MXFP4
 // MoE CUTLASS kernel"), "Implementation breakdown" items 1 and 3 (the experts
 // quant of the routed activations); the per-element and per-block steps are
-// those of quantize.cu (shared through mxfp4_device.cuh).
+// those of quantize.cu and nvfp4.cu (shared through mxfp4_device.cuh and
+// nvfp4_device.cuh).
 #include <cstdint>
 
 #include <cuda_runtime.h>

@@ -18,7 +18,9 @@
 // scale chunks; lane l of warp w covers one 16-element block of row
 // 4*w + l/8 in each of 4 passes of 32 rows, so the block max needs no shuffle.
 // Both quantize kernels are bounded to 48 registers, 5 CTAs per SM (12.95 us
-// against 13.33 us at 4 CTAs per SM on a 4096 x 7168 activation).
+// against 13.33 us at 4 CTAs per SM on a 4096 x 7168 activation).  The block
+// steps are in nvfp4_device.cuh; the experts quant with the dispatch fused in
+// is in dispatch.cu.
 #include <cstdint>
 
 #include <cuda_runtime.h>
