@@ -413,7 +413,7 @@ struct Nvfp4ScatterParams {
 #define MXFP4_IN_BOUNDS_G(params, ptr, bytes) true
 #endif
 
-constexpr int kNvScBatch = 1;  // passes with loads in flight together (5 CTAs per SM)
+constexpr int kNvScBatch = 2;  // passes with loads in flight together (4 CTAs per SM)
 
 // Byte offset of the scale word of padded row prow in k-tile 0 of the tiled
 // layout (k-tile kt adds kt * 512) — or, staged, of its workspace row.
@@ -426,66 +426,6 @@ __device__ __forceinline__ int64_t nv_row_base(int prow, int nKT) {
 __device__ __forceinline__ void st_keep_u8(void* p, uint32_t v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.u8 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(policy)
                : "memory");
-}
-
-// Eight elements already widened to float32 (bit patterns e[0..7], element
-// 2i in the low nibble of byte i) -> one word of E2M1 codes of e * f: packed
-// f32x2 products, then the saturating round-to-nearest E2M1 conversion.  The
-// NVFP4 scatter widens a token's block once and converts it per route.
-__device__ __forceinline__ uint32_t cvt_e2m1x8_f32(const uint32_t (&e)[8], float f) {
-  uint32_t r;
-  asm("{\n\t"
-      ".reg .b64 p0, p1, p2, p3, fs;\n\t"
-      ".reg .b32 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
-      ".reg .b8 q0, q1, q2, q3;\n\t"
-      "mov.b64 fs, {%9, %9};\n\t"
-      "mov.b64 p0, {%1, %2};\n\t"
-      "mov.b64 p1, {%3, %4};\n\t"
-      "mov.b64 p2, {%5, %6};\n\t"
-      "mov.b64 p3, {%7, %8};\n\t"
-      "mul.rn.f32x2 p0, p0, fs;\n\t"
-      "mul.rn.f32x2 p1, p1, fs;\n\t"
-      "mul.rn.f32x2 p2, p2, fs;\n\t"
-      "mul.rn.f32x2 p3, p3, fs;\n\t"
-      "mov.b64 {l0, h0}, p0;\n\t"
-      "mov.b64 {l1, h1}, p1;\n\t"
-      "mov.b64 {l2, h2}, p2;\n\t"
-      "mov.b64 {l3, h3}, p3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 q0, h0, l0;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 q1, h1, l1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 q2, h2, l2;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 q3, h3, l3;\n\t"
-      "mov.b32 %0, {q0, q1, q2, q3};\n\t"
-      "}"
-      : "=r"(r)
-      : "r"(e[0]), "r"(e[1]), "r"(e[2]), "r"(e[3]), "r"(e[4]), "r"(e[5]), "r"(e[6]), "r"(e[7]),
-        "f"(f));
-  return r;
-}
-
-// The 16 elements of a lane's block widened to float32 bit patterns, in
-// element order (exact for BF16 and FP16).
-template <bool kF16>
-__device__ __forceinline__ void widen16(const uint4 (&v)[2], uint32_t (&lo)[8], uint32_t (&hi)[8]) {
-  const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t a, b;
-    if constexpr (kF16) {
-      a = f16_bits_to_f32_bits(w[i] & 0xFFFFu);
-      b = f16_bits_to_f32_bits(w[i] >> 16);
-    } else {
-      a = w[i] << 16;
-      b = w[i] & 0xFFFF0000u;
-    }
-    if (i < 4) {
-      lo[2 * i] = a;
-      lo[2 * i + 1] = b;
-    } else {
-      hi[2 * (i - 4)] = a;
-      hi[2 * (i - 4) + 1] = b;
-    }
-  }
 }
 
 template <bool kVec32, bool kF16, bool kStaged>
@@ -569,12 +509,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_scatter_kernel(const Nvfp4Scat
       if (p0 + b < n_pass && blk < p.sK && MXFP4_IN_BOUNDS(p, kDbgX, xp, 32))
         load32<kVec32>(xp, v[b]);
     }
-    uint32_t lo[kNvScBatch][8], hi[kNvScBatch][8];  // the blocks widened once per token
 #pragma unroll
-    for (int b = 0; b < kNvScBatch; ++b) {
-      q[b] = nv_block_q<kF16>(v[b]);
-      widen16<kF16>(v[b], lo[b], hi[b]);
-    }
+    for (int b = 0; b < kNvScBatch; ++b) q[b] = nv_block_q<kF16>(v[b]);
     for (int j = 0; j < p.top_k; ++j) {
       const int64_t c = s_code[warp][j];
       if (c < 0) continue;  // the same for every lane of the warp
@@ -585,12 +521,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_scatter_kernel(const Nvfp4Scat
         const int pass = p0 + b;
         const int blk = pass * 32 + lane;
         const uint32_t byte = cvt_e4m3_satfinite(g * q[b]);
-        uint2 code = make_uint2(0u, 0u);  // byte 0: zero codes
-        if (byte != 0u) {
-          const float inv = g / e4m3_to_f32(byte);
-          code.x = cvt_e2m1x8_f32(lo[b], inv);
-          code.y = cvt_e2m1x8_f32(hi[b], inv);
-        }
+        const uint2 code = nv_codes<kF16>(v[b], byte, byte != 0u ? g / e4m3_to_f32(byte) : 0.0f);
         uint8_t* const cp = p.codes + c + static_cast<int64_t>(blk) * 8;
         if (pass < n_pass && blk < p.sK && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 8))
           st_stream_v2(cp, code);
