@@ -157,6 +157,17 @@ int mxfp4_quantize_grouped(const void* x, int64_t total_rows, int64_t K,
  *                    MXFP4_EINDEX when some row_index is outside
  *                    [0, num_src_rows): such rows are quantized as zero rows
  *                    and no out-of-range memory is read.
+ *
+ * How it runs (the results do not depend on it).  When the inverse map and
+ * staged scale words of mxfp4_quantize_grouped_gather_ws fit in the codes of
+ * the last quarter of the output rows, the call takes that path and uses
+ * those rows of `codes` as its workspace: it clears them, builds the inverse
+ * map there, quantizes every source row once into the other rows, then
+ * writes the borrowed rows' own codes last, from their source rows.  Until
+ * the stream reaches the end of the call, those rows of `codes` hold
+ * workspace data.  If the offsets are malformed, the clear is skipped and
+ * no code row is written.  Otherwise (small batches) every output row
+ * reads its source row itself.
  */
 int mxfp4_quantize_grouped_gather(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
                                   const int32_t* row_index, int64_t total_rows,

@@ -129,6 +129,8 @@ struct ScatterParams {
   int32_t nKT;
   int32_t map_ctas;                       // kStaged, token-major: the next CTAs write tok1,
   int32_t* __restrict__ tok1;             //   the token + 1 of every padded row (-1: pad row)
+  int64_t code_rows;                      // codes are written for rows < code_rows only (the
+                                          //   rows past it hold a borrowed workspace)
 #ifdef MXFP4_DEBUG_BOUNDS
   DebugRanges dbg;                        // slots as in QuantizeParams (kDbgRowIndex: dest_rows)
 #endif
@@ -158,7 +160,7 @@ __device__ __forceinline__ void scatter_token(const ScatterParams& p, int64_t t,
     const int32_t* dp = dsts + lane;
     const int32_t v = MXFP4_IN_BOUNDS(p, kDbgRowIndex, dp, 4) ? __ldg(dp) : -1;
     if (v >= 0 && v < p.total_rows) {
-      co = static_cast<int64_t>(v) * p.code_ld;
+      co = v < p.code_rows ? static_cast<int64_t>(v) * p.code_ld : -1;
       if constexpr (!kStaged) {
         const int e = find_segment(p.offsets, p.E, v, static_cast<int>(p.total_rows));
         so = scale_word_base(__ldg(p.padded + e) + (v - __ldg(p.offsets + e)), p.nKT);
@@ -361,6 +363,67 @@ __global__ void __launch_bounds__(kThreads, kStaged ? 5 : 0) quantize_scatter_ke
     if (!overflow_entry(p, j, t, dsts)) return;
     __syncwarp();
     s_next[warp] = j;
+  }
+}
+
+// The gather without a caller workspace borrows the last rows of its own
+// codes output as the workspace: the kernels above leave those rows' codes
+// unwritten (code_rows), and gather_row_codes_kernel writes them last, once
+// the workspace is no longer read.  clear_words_kernel zeroes the workspace's
+// counters only for valid offsets, so that rejected offsets still leave the
+// outputs untouched.
+__global__ void __launch_bounds__(kThreads) clear_words_kernel(const int32_t* padded, int32_t E,
+                                                              uint4* words, int64_t n16) {
+  pdl_wait();
+  pdl_release();
+  if (__ldg(padded + E) < 0) return;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * kThreads)
+    words[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+struct RowCodesParams {
+  const uint8_t* __restrict__ x;          // 16-bit source rows
+  int64_t ldx_bytes;
+  int64_t num_src_rows;
+  const int32_t* __restrict__ row_index;  // [R] source row of every row
+  int64_t r0;                             // rows [r0, R) get their codes here
+  int64_t total_rows;                     // R
+  uint8_t* __restrict__ codes;
+  int64_t code_ld;
+  const int32_t* __restrict__ padded;
+  int32_t E;
+  int32_t sK;
+#ifdef MXFP4_DEBUG_BOUNDS
+  DebugRanges dbg;  // kDbgX, kDbgCodes, kDbgPadded, kDbgRowIndex
+#endif
+};
+
+// One warp per row r in [r0, R): the codes of source row row_index[r] (zero
+// codes for an index out of range), in passes of 512 elements.
+template <bool kVec32, bool kF16>
+__global__ void __launch_bounds__(kThreads) gather_row_codes_kernel(const RowCodesParams p) {
+  pdl_wait();
+  pdl_release();
+  if (!MXFP4_IN_BOUNDS(p, kDbgPadded, p.padded + p.E, 4) || __ldg(p.padded + p.E) < 0) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t r = p.r0 + static_cast<int64_t>(blockIdx.x) * kScatterWarps + (threadIdx.x >> 5);
+  if (r >= p.total_rows) return;  // whole warp
+  const int32_t* ip = p.row_index + r;
+  const int32_t t = MXFP4_IN_BOUNDS(p, kDbgRowIndex, ip, 4) ? __ldg(ip) : -1;
+  const bool valid = t >= 0 && t < p.num_src_rows;
+  const uint8_t* xrow = p.x + (valid ? t : 0) * p.ldx_bytes + lane * (kElems * 2);
+  uint8_t* crow = p.codes + r * p.code_ld + lane * (kElems / 2);
+  const int n_pass = (p.sK + 15) / 16;
+  for (int pass = 0; pass < n_pass; ++pass) {
+    const bool col = pass * 16 + (lane >> 1) < p.sK;
+    uint4 v[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    const uint8_t* xp = xrow + static_cast<int64_t>(pass) * (kScatterPass * 2);
+    if (valid && col && MXFP4_IN_BOUNDS(p, kDbgX, xp, 32)) load32<kVec32>(xp, v);
+    const uint32_t sc = lane_block_scale<kF16>(v);  // all lanes: the pair shares a shuffle
+    const uint2 code = lane_codes<kF16>(v, sc);
+    uint8_t* const cp = crow + static_cast<int64_t>(pass) * (kScatterPass / 2);
+    if (col && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 8)) st_stream_v2(cp, code);
   }
 }
 
@@ -690,6 +753,7 @@ struct InvertParams {
   int32_t E;
   int32_t nKT;
   int32_t* status;
+  int64_t code_rows;                      // zero codes only for bad rows below it
 #ifdef MXFP4_DEBUG_BOUNDS
   DebugRanges dbg;  // kDbgCodes, kDbgScales, kDbgOffsets, kDbgPadded, kDbgRowIndex, kDbgStatus, kDbgWork
 #endif
@@ -734,7 +798,7 @@ __global__ void __launch_bounds__(kInvertThreads) invert_bucket_kernel(const Inv
     }
     bad = true;
     uint8_t* cp = q.codes + r * q.code_ld;
-    for (int64_t i = 0; i < q.code_ld; i += 16)
+    for (int64_t i = 0; r < q.code_rows && i < q.code_ld; i += 16)
       if (MXFP4_IN_BOUNDS(q, kDbgCodes, cp + i, 16))
         *reinterpret_cast<uint4*>(cp + i) = make_uint4(0u, 0u, 0u, 0u);
     if (q.tok1 != nullptr) continue;  // the tile kernel writes its zero scale words
@@ -801,6 +865,7 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
   p.dest_rows = dest_rows;
   p.top_k = top_k;
   p.total_rows = total_rows;
+  p.code_rows = total_rows;
 #ifdef MXFP4_DEBUG_BOUNDS
   debug_range(p.dbg, kDbgX, x, num_tokens > 0 ? ((num_tokens - 1) * ldx + K) * 2 : 0);
   debug_range(p.dbg, kDbgCodes, codes, total_rows * (K / 2));
@@ -859,13 +924,17 @@ int64_t gather_stage_ints(int64_t num_src_rows, int64_t K) {
   return num_src_rows * stage_ld(static_cast<int>((K / kBlock + kTileBlocks - 1) / kTileBlocks));
 }
 
-cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_t K,
-                                              int64_t ldx, const int32_t* row_index,
-                                              int64_t total_rows, const int32_t* offsets,
-                                              int32_t E, int32_t* workspace, bool staged,
-                                              uint8_t* codes, uint8_t* scales,
-                                              int32_t* scale_row_offsets, int32_t* status,
-                                              int64_t bound_tiles, bool f16, cudaStream_t stream) {
+namespace {
+
+// The gather through the scatter path.  borrowed: the workspace is the tail
+// of `codes` from row code_rows on; it is cleared by a kernel (only for valid
+// offsets) and those rows' codes are written last by gather_row_codes_kernel.
+cudaError_t gather_ws_impl(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
+                           const int32_t* row_index, int64_t total_rows, const int32_t* offsets,
+                           int32_t E, int32_t* workspace, bool staged, bool borrowed,
+                           int64_t code_rows, uint8_t* codes, uint8_t* scales,
+                           int32_t* scale_row_offsets, int32_t* status, int64_t bound_tiles,
+                           bool f16, cudaStream_t stream) {
   const int64_t T = num_src_rows;
   const int64_t R = total_rows;
   const int64_t PT = staged ? gather_tok_ints(R, E) : 0;
@@ -873,12 +942,20 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   // (the caller need not pass a workspace then)
   const bool work = E > 0 && K > 0 && R > 0;
   cudaError_t err = cudaSuccess;
-  if (work) {  // first, so that the kernels below follow one another directly
+  if (work && !borrowed) {  // first, so that the kernels below follow one another directly
     err = cudaMemsetAsync(workspace, 0, static_cast<size_t>(T + 1 + PT) * 4, stream);
     if (err != cudaSuccess) return err;
   }
   err = launch_offsets(offsets, E, total_rows, scale_row_offsets, status, stream);
   if (err != cudaSuccess || !work) return err;
+  if (borrowed) {  // T + 1 + PT ints, rounded up to whole uint4 (the map region is larger)
+    const int64_t n16 = (T + 1 + PT + 3) / 4;
+    const int64_t need = (n16 + kThreads - 1) / kThreads;
+    const unsigned ctas = static_cast<unsigned>(need < sm_count() ? need : sm_count());
+    err = launch_pdl(clear_words_kernel, ctas, kThreads, 0, stream, scale_row_offsets, E,
+                     reinterpret_cast<uint4*>(workspace), n16);
+    if (err != cudaSuccess) return err;
+  }
   InvertParams q{};
   q.row_index = row_index;
   q.total_rows = R;
@@ -897,6 +974,7 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   q.E = E;
   q.nKT = (static_cast<int32_t>(K / kBlock) + kTileBlocks - 1) / kTileBlocks;
   q.status = status;
+  q.code_rows = code_rows;
   const int64_t map_ints = (gather_workspace_ints(T, R) + PT + 3) & ~int64_t{3};
   const int64_t ws_bytes = (map_ints + (staged ? gather_stage_ints(T, K) : 0)) * 4;
 #ifdef MXFP4_DEBUG_BOUNDS
@@ -937,6 +1015,7 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   p.pad_ctas = staged ? 0 : E;
   p.sK = static_cast<int32_t>(K / kBlock);
   p.nKT = q.nKT;
+  p.code_rows = code_rows;
   // one warp per token, then up to one CTA per SM of warps for the overflow
   // list (the token CTAs' spare warps walk it too)
   const int64_t token_ctas = (T + kScatterWarps - 1) / kScatterWarps;
@@ -979,8 +1058,75 @@ cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_row
   debug_range(ts.dbg, kDbgRowIndex, q.tok1, PT * 4);
   debug_range(ts.dbg, kDbgWork, p.stage, T * stage_ld(ts.nKT) * 4);
 #endif
-  return launch_pdl(tile_scales_kernel<false>, static_cast<unsigned>(bound_tiles), kTileThreads,
-                    0, stream, ts);
+  err = launch_pdl(tile_scales_kernel<false>, static_cast<unsigned>(bound_tiles), kTileThreads,
+                   0, stream, ts);
+  if (err != cudaSuccess || code_rows >= R) return err;
+  RowCodesParams rc{};
+  rc.x = static_cast<const uint8_t*>(x);
+  rc.ldx_bytes = ldx * 2;
+  rc.num_src_rows = T;
+  rc.row_index = row_index;
+  rc.r0 = code_rows;
+  rc.total_rows = R;
+  rc.codes = codes;
+  rc.code_ld = K / 2;
+  rc.padded = scale_row_offsets;
+  rc.E = E;
+  rc.sK = static_cast<int32_t>(K / kBlock);
+#ifdef MXFP4_DEBUG_BOUNDS
+  debug_range(rc.dbg, kDbgX, x, T > 0 ? ((T - 1) * ldx + K) * 2 : 0);
+  debug_range(rc.dbg, kDbgCodes, codes, R * (K / 2));
+  debug_range(rc.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
+  debug_range(rc.dbg, kDbgRowIndex, row_index, R * 4);
+#endif
+  const int64_t rows = R - code_rows;
+  const auto row_kernel = f16 ? (v32 ? gather_row_codes_kernel<true, true>
+                                     : gather_row_codes_kernel<false, true>)
+                              : (v32 ? gather_row_codes_kernel<true, false>
+                                     : gather_row_codes_kernel<false, false>);
+  return launch_pdl(row_kernel, static_cast<unsigned>((rows + kScatterWarps - 1) / kScatterWarps),
+                    kThreads, 0, stream, rc);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_t K,
+                                              int64_t ldx, const int32_t* row_index,
+                                              int64_t total_rows, const int32_t* offsets,
+                                              int32_t E, int32_t* workspace, bool staged,
+                                              uint8_t* codes, uint8_t* scales,
+                                              int32_t* scale_row_offsets, int32_t* status,
+                                              int64_t bound_tiles, bool f16, cudaStream_t stream) {
+  return gather_ws_impl(x, num_src_rows, K, ldx, row_index, total_rows, offsets, E, workspace,
+                        staged, false, total_rows, codes, scales, scale_row_offsets, status,
+                        bound_tiles, f16, stream);
+}
+
+int64_t gather_borrow_rows(int64_t num_src_rows, int64_t total_rows, int64_t E, int64_t K) {
+  if (K <= 0 || total_rows <= 0) return -1;
+  const int64_t map_ints =
+      (gather_workspace_ints(num_src_rows, total_rows) + gather_tok_ints(total_rows, E) + 3) &
+      ~int64_t{3};
+  const int64_t bytes = (map_ints + gather_stage_ints(num_src_rows, K)) * 4;
+  const int64_t rows = (bytes + K / 2 - 1) / (K / 2);
+  return rows * 4 <= total_rows ? rows : -1;  // the codes of at most a quarter of the rows
+}
+
+cudaError_t launch_quantize_grouped_gather_borrowed(const void* x, int64_t num_src_rows,
+                                                    int64_t K, int64_t ldx,
+                                                    const int32_t* row_index, int64_t total_rows,
+                                                    const int32_t* offsets, int32_t E,
+                                                    uint8_t* codes, uint8_t* scales,
+                                                    int32_t* scale_row_offsets, int32_t* status,
+                                                    int64_t bound_tiles, bool f16,
+                                                    cudaStream_t stream) {
+  const int64_t tail = gather_borrow_rows(num_src_rows, total_rows, E, K);
+  if (tail < 0) return cudaErrorInvalidValue;
+  const int64_t r0 = total_rows - tail;
+  int32_t* const workspace = reinterpret_cast<int32_t*>(codes + r0 * (K / 2));
+  return gather_ws_impl(x, num_src_rows, K, ldx, row_index, total_rows, offsets, E, workspace,
+                        true, true, r0, codes, scales, scale_row_offsets, status, bound_tiles,
+                        f16, stream);
 }
 
 // NVFP4 experts quant with the dispatch as a scatter.  Workspace (staged):

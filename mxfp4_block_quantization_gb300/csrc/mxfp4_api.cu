@@ -225,6 +225,13 @@ int gather_checked(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
         x, work ? num_src_rows : 0, K, ldx, row_index, total_rows, expert_offsets, E,
         static_cast<int32_t*>(workspace), staged, codes, scales, scale_row_offsets, status,
         K == 0 ? 0 : bound_tiles, f16, st));
+  // no workspace: through the scatter path in the borrowed tail of the codes
+  // output when it is large enough, else the per-row gather kernel
+  if (work && E > 0 && num_src_rows <= INT32_MAX / 4 &&
+      mxfp4::gather_borrow_rows(num_src_rows, total_rows, E, K) >= 0)
+    return from_cuda(mxfp4::launch_quantize_grouped_gather_borrowed(
+        x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E, codes, scales,
+        scale_row_offsets, status, bound_tiles, f16, st));
   return from_cuda(mxfp4::launch_quantize_grouped_gather(
       x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E, codes, scales,
       scale_row_offsets, status, K == 0 ? 0 : bound_tiles, f16, st));

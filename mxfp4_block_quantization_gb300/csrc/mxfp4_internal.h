@@ -47,6 +47,19 @@ cudaError_t launch_quantize_grouped_gather(const void* x, int64_t num_src_rows, 
 // whole; without it the scatter stores every row's scale words into the tiled
 // layout itself.
 int64_t gather_workspace_ints(int64_t num_src_rows, int64_t total_rows);
+// The gather without a workspace can borrow the last gather_borrow_rows(...)
+// rows of its codes output (at most a quarter of them; -1 when they do not
+// suffice): those rows hold the staged workspace until their own codes are
+// written last.  Same results as the other gather forms.
+int64_t gather_borrow_rows(int64_t num_src_rows, int64_t total_rows, int64_t E, int64_t K);
+cudaError_t launch_quantize_grouped_gather_borrowed(const void* x, int64_t num_src_rows,
+                                                    int64_t K, int64_t ldx,
+                                                    const int32_t* row_index, int64_t total_rows,
+                                                    const int32_t* offsets, int32_t E,
+                                                    uint8_t* codes, uint8_t* scales,
+                                                    int32_t* scale_row_offsets, int32_t* status,
+                                                    int64_t bound_tiles, bool f16,
+                                                    cudaStream_t stream);
 int64_t gather_tok_ints(int64_t total_rows, int64_t E);
 int64_t gather_stage_ints(int64_t num_src_rows, int64_t K);
 cudaError_t launch_quantize_grouped_gather_ws(const void* x, int64_t num_src_rows, int64_t K,

@@ -124,6 +124,12 @@ def test_everything_in_bounds(libs):
     cases.append(lambda: written(mx.quantize_grouped_gather(xt, idx_bad, off6, via_scatter=False),
                                  64))
     cases.append(lambda: written(mx.quantize_grouped(xt2.index_select(0, ri.long()), off_z), 160))
+    # the gather without a workspace, large enough to borrow the tail of its codes output
+    g4 = W.moe_grouped(seed=62, tokens=2048, top_k=8, num_experts=64, K=1024, device="cuda")
+    ri4 = g4.row_index.clone()
+    ri4[[3, ri4.numel() - 2]] = -1
+    cases.append(lambda: written(mx.quantize_grouped_gather(g4.x_tokens, ri4, g4.offsets,
+                                                            via_scatter=False), 1024))
     # scatter: all routes, dropped routes, bad entries, no tokens, strided
     cases.append(lambda: written(mx.quantize_grouped_scatter(gsmall.x_tokens, gsmall.dest_rows,
                                                              gsmall.offsets), 288))

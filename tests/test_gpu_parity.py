@@ -1293,6 +1293,46 @@ def test_gather_ws_long_overflow_list(mx):
                                        torch.from_numpy(off).cuda()), bits(xt), idx, off, 256)
 
 
+@pytest.mark.parametrize("f16", [False, True])
+def test_gather_without_workspace_borrows_its_codes_tail(mx, f16):
+    """The gather without a workspace, large enough to run through the scatter
+    path in the last rows of its own codes output (2048 tokens x top-8, K =
+    1024: 1104 of 16384 rows borrowed): against the oracle, with out-of-range
+    indices in the borrowed tail and in the body; rejected offsets leave the
+    codes, tail included, untouched."""
+    g = W.moe_grouped(seed=61, tokens=2048, top_k=8, num_experts=64, K=1024, device="cuda")
+    xt = g.x_tokens.to(torch.float16) if f16 else g.x_tokens
+    hb = (xt.cpu().view(torch.int16).numpy().view(np.uint16) if f16 else bits(xt))
+    idx = g.token_of_row.numpy().astype(np.int32)
+    total = idx.size
+    idx[[5, 9000, total - 1, total - 700]] = [-1, 2048, -3, 1 << 20]
+    off = g.offsets
+    E = off.numel() - 1
+    codes = Guarded(total * 512, shape=(total, 512))
+    scales = Guarded(mx.mxfp4_grouped_scale_bytes_bound(total, E, 1024))
+    sro = Guarded(4 * (E + 1), torch.int32)
+    status = Guarded(4, torch.int32)
+    fn = mx.mxfp4_quantize_grouped_gather_f16 if f16 else mx.mxfp4_quantize_grouped_gather
+    fn(xt, torch.from_numpy(idx).cuda(), off, codes.t, scales.t, sro.t, status.t)
+    torch.cuda.synchronize()
+    for t in (codes, scales, sro, status):
+        t.check()
+    got = (codes.t.cpu().numpy(), scales.t.cpu().numpy(), sro.t.cpu().numpy(),
+           int(status.t.cpu()[0]))
+    _gather_oracle_check(got, hb, idx, off.cpu().numpy(), 1024, f16=f16)
+    assert got[3] == mx.MXFP4_EINDEX
+    assert not got[0][[5, 9000, total - 1, total - 700]].any()
+    # rejected offsets: nothing written, the borrowed tail included
+    bad = off.clone()
+    bad[3] = bad[4] + 1
+    codes2 = Guarded(total * 512, shape=(total, 512))
+    fn(xt, torch.from_numpy(idx).cuda(), bad, codes2.t, scales.t, sro.t, status.t)
+    torch.cuda.synchronize()
+    codes2.check()
+    assert int(status.t.cpu()[0]) == mx.MXFP4_EOFFSETS
+    assert (codes2.t == 0xA5).all()
+
+
 def test_gather_ws_bad_offsets_write_nothing(mx):
     xt = W.small_matrix(3, 16, 64).cuda()
     idx = torch.arange(20, dtype=torch.int32, device="cuda") % 16
