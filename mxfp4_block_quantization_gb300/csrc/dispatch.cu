@@ -399,31 +399,47 @@ struct RowCodesParams {
 #endif
 };
 
-// One warp per row r in [r0, R): the codes of source row row_index[r] (zero
-// codes for an index out of range), in passes of 512 elements.
+// Rows r in [r0, R) get the codes of source row row_index[r] (zero codes for
+// an index out of range).  One warp per row and group of kRowGroup passes of
+// 512 elements: the group's loads are issued first, so that a batch of a few
+// thousand rows still keeps enough loads in flight.
+constexpr int kRowGroup = 4;
+
 template <bool kVec32, bool kF16>
 __global__ void __launch_bounds__(kThreads) gather_row_codes_kernel(const RowCodesParams p) {
   pdl_wait();
   pdl_release();
   if (!MXFP4_IN_BOUNDS(p, kDbgPadded, p.padded + p.E, 4) || __ldg(p.padded + p.E) < 0) return;
   const int lane = threadIdx.x & 31;
-  const int64_t r = p.r0 + static_cast<int64_t>(blockIdx.x) * kScatterWarps + (threadIdx.x >> 5);
+  const int n_pass = (p.sK + 15) / 16;
+  const int n_grp = (n_pass + kRowGroup - 1) / kRowGroup;
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * kScatterWarps + (threadIdx.x >> 5);
+  const int64_t r = p.r0 + w / n_grp;
   if (r >= p.total_rows) return;  // whole warp
+  const int pass0 = static_cast<int>(w % n_grp) * kRowGroup;
   const int32_t* ip = p.row_index + r;
   const int32_t t = MXFP4_IN_BOUNDS(p, kDbgRowIndex, ip, 4) ? __ldg(ip) : -1;
   const bool valid = t >= 0 && t < p.num_src_rows;
   const uint8_t* xrow = p.x + (valid ? t : 0) * p.ldx_bytes + lane * (kElems * 2);
   uint8_t* crow = p.codes + r * p.code_ld + lane * (kElems / 2);
-  const int n_pass = (p.sK + 15) / 16;
-  for (int pass = 0; pass < n_pass; ++pass) {
-    const bool col = pass * 16 + (lane >> 1) < p.sK;
-    uint4 v[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+  uint4 v[kRowGroup][2];
+#pragma unroll
+  for (int i = 0; i < kRowGroup; ++i) {
+    const int pass = pass0 + i;
+    v[i][0] = make_uint4(0u, 0u, 0u, 0u);
+    v[i][1] = make_uint4(0u, 0u, 0u, 0u);
     const uint8_t* xp = xrow + static_cast<int64_t>(pass) * (kScatterPass * 2);
-    if (valid && col && MXFP4_IN_BOUNDS(p, kDbgX, xp, 32)) load32<kVec32>(xp, v);
-    const uint32_t sc = lane_block_scale<kF16>(v);  // all lanes: the pair shares a shuffle
-    const uint2 code = lane_codes<kF16>(v, sc);
+    if (valid && pass * 16 + (lane >> 1) < p.sK && MXFP4_IN_BOUNDS(p, kDbgX, xp, 32))
+      load32<kVec32>(xp, v[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < kRowGroup; ++i) {
+    const int pass = pass0 + i;
+    const uint32_t sc = lane_block_scale<kF16>(v[i]);  // all lanes: the pair shares a shuffle
+    const uint2 code = lane_codes<kF16>(v[i], sc);
     uint8_t* const cp = crow + static_cast<int64_t>(pass) * (kScatterPass / 2);
-    if (col && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 8)) st_stream_v2(cp, code);
+    if (pass * 16 + (lane >> 1) < p.sK && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 8))
+      st_stream_v2(cp, code);
   }
 }
 
@@ -1079,12 +1095,13 @@ cudaError_t gather_ws_impl(const void* x, int64_t num_src_rows, int64_t K, int64
   debug_range(rc.dbg, kDbgPadded, scale_row_offsets, (static_cast<int64_t>(E) + 1) * 4);
   debug_range(rc.dbg, kDbgRowIndex, row_index, R * 4);
 #endif
-  const int64_t rows = R - code_rows;
+  const int64_t n_pass = (K / kBlock + 15) / 16;
+  const int64_t warps = (R - code_rows) * ((n_pass + kRowGroup - 1) / kRowGroup);
   const auto row_kernel = f16 ? (v32 ? gather_row_codes_kernel<true, true>
                                      : gather_row_codes_kernel<false, true>)
                               : (v32 ? gather_row_codes_kernel<true, false>
                                      : gather_row_codes_kernel<false, false>);
-  return launch_pdl(row_kernel, static_cast<unsigned>((rows + kScatterWarps - 1) / kScatterWarps),
+  return launch_pdl(row_kernel, static_cast<unsigned>((warps + kScatterWarps - 1) / kScatterWarps),
                     kThreads, 0, stream, rc);
 }
 
