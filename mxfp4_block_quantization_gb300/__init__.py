@@ -663,7 +663,9 @@ def quantize_grouped(x, expert_offsets, stream=None):
 def quantize_grouped_gather(x, row_index, expert_offsets, stream=None, via_scatter=True):
     """Returns (codes, scales, scale_row_offsets, status) of x[row_index]
     (BF16 or FP16 x).  By default through the scatter path, with a workspace
-    allocated here; via_scatter=False runs the per-row gather kernel."""
+    allocated here; via_scatter=False calls the entry point without a
+    workspace, which borrows the tail of its codes output as one when that
+    fits and otherwise runs the per-row gather kernel (same results)."""
     K = x.shape[1]
     total = row_index.numel()
     E = expert_offsets.numel() - 1
