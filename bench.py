@@ -529,7 +529,8 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     nb_nvs = (2 * T * K + 4 * total + total * K // 2 + padded * (K // 16) + 4 * (E + 1) + 4 * E)
     e_ = entry(nb_nvs, ms_nvs, 2, "bytes = token rows read once + route->row map + codes + "
                "E4M3 scales (16-element columns) + offsets + global scales; each route's "
-               "scale words stored into the tiled layout")
+               "scale words stored into the tiled layout; one global scale shared by every "
+               "expert, so a token's routes share their bytes and codes")
     e_["unfused_us_per_call"] = round(ms_nvu * 1e3, 2)
     e_["speedup_vs_unfused"] = round(ms_nvu / ms_nvs, 3)
     out["nvfp4_grouped_scatter_moe_16384tok_top8_E384"] = e_
@@ -547,6 +548,18 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     e_["speedup_vs_unfused"] = round(ms_nvu / ms_nvw, 3)
     e_["speedup_vs_direct"] = round(ms_nvs / ms_nvw, 3)
     out["nvfp4_grouped_scatter_ws_moe_16384tok_top8_E384"] = e_
+    # the same with a global scale of its own per expert: every route of a
+    # token computes its own E4M3 bytes, inverse scales and codes
+    g_own = 448.0 * 6.0 / torch.exp(torch.rand(E, generator=torch.Generator().manual_seed(2)) * 3.0)
+    g_own = g_own.to("cuda")
+    ms_nvo = time_launches(
+        lambda i: mx.mxfp4_quantize_nvfp4_grouped_scatter_ws(g.x_tokens, g.dest_rows, g.offsets,
+                                                             total, g_own, ws, codes, sc_nv, sro,
+                                                             st, stream), 30, stream)
+    e_ = entry(nb_nvs, ms_nvo, 3, "the row above with a global scale of its own per expert "
+               "(448 * 6 / e^U(0,3)): each route quantizes its blocks itself")
+    e_["speedup_vs_unfused"] = round(ms_nvu / ms_nvo, 3)
+    out["nvfp4_grouped_scatter_ws_own_gscales_moe_16384tok_top8_E384"] = e_
     del sc_nv, ws
     del g, codes, scales, xg
 

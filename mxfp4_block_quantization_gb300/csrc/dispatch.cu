@@ -508,7 +508,7 @@ __device__ __forceinline__ void st_keep_u8(void* p, uint32_t v, uint64_t policy)
 }
 
 template <bool kVec32, bool kF16, bool kStaged>
-__global__ void __launch_bounds__(kThreads) nvfp4_scatter_kernel(const Nvfp4ScatterParams p) {
+__global__ void __launch_bounds__(kThreads, 4) nvfp4_scatter_kernel(const Nvfp4ScatterParams p) {
   __shared__ int64_t s_code[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];  // d * K/2, or -1
   __shared__ int64_t s_word[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];  // scale row base
   __shared__ float s_g[kScatterWarps][MXFP4_SCATTER_MAX_TOP_K];       // the route's scale
@@ -574,9 +574,43 @@ __global__ void __launch_bounds__(kThreads) nvfp4_scatter_kernel(const Nvfp4Scat
   s_g[warp][lane] = ge;
   __syncwarp();
 
+  // A token whose routes all land in experts of one global scale (the same
+  // bits) has the same bytes and codes on every route: those are computed
+  // once per pass and stored to each route.  Any other token takes the
+  // per-route loop.  Decided once per token, outside the route loops.
+  const unsigned routed = __ballot_sync(0xFFFFFFFFu, co >= 0);
+  if (routed == 0u) return;  // whole warp: nothing to write
+  const float g0 = __shfl_sync(0xFFFFFFFFu, ge, __ffs(static_cast<int>(routed)) - 1);
+  const bool one_scale =
+      __all_sync(0xFFFFFFFFu, co < 0 || __float_as_uint(ge) == __float_as_uint(g0));
+
   const uint8_t* xrow = p.x + t * p.ldx_bytes + lane * 32;
   const int n_pass = (p.sK + 31) / 32;  // 32 blocks per pass
   const uint64_t keep = l2_evict_last_policy();
+  // the stores of pass p0 + b for the route with codes at c and scale row w
+  auto put = [&](int64_t c, int64_t w, int p0, int b, uint32_t byte, uint2 code) {
+    const int pass = p0 + b;
+    const int blk = pass * 32 + lane;
+    uint8_t* const cp = p.codes + c + static_cast<int64_t>(blk) * 8;
+    if (pass < n_pass && blk < p.sK && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 8))
+      st_stream_v2(cp, code);
+    if constexpr (kStaged) {
+      // the route's scale bytes, 32 per pass, into its workspace row (zero
+      // for the pad columns past sK)
+      uint8_t* const bp = p.stage + w + blk;
+      if (pass < n_pass && blk < 4 * p.nKT && MXFP4_IN_BOUNDS(p, kDbgWork, bp, 1))
+        st_keep_u8(bp, byte, keep);
+    } else {
+      // scale word of k-tile pass*8 + lane/4: the bytes of lanes +0..+3
+      const uint32_t word = byte | (__shfl_down_sync(0xFFFFFFFFu, byte, 1) << 8) |
+                            (__shfl_down_sync(0xFFFFFFFFu, byte, 2) << 16) |
+                            (__shfl_down_sync(0xFFFFFFFFu, byte, 3) << 24);
+      const int kt = pass * 8 + (lane >> 2);
+      uint8_t* const wp = p.scales + w + static_cast<int64_t>(kt) * kChunkBytes;
+      if (pass < n_pass && (lane & 3) == 0 && kt < p.nKT && MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4))
+        st_keep_u32(wp, word, keep);
+    }
+  };
   for (int p0 = 0; p0 < n_pass; p0 += kNvScBatch) {
     uint4 v[kNvScBatch][2];
     float q[kNvScBatch];
@@ -590,36 +624,33 @@ __global__ void __launch_bounds__(kThreads) nvfp4_scatter_kernel(const Nvfp4Scat
     }
 #pragma unroll
     for (int b = 0; b < kNvScBatch; ++b) q[b] = nv_block_q<kF16>(v[b]);
-    for (int j = 0; j < p.top_k; ++j) {
-      const int64_t c = s_code[warp][j];
-      if (c < 0) continue;  // the same for every lane of the warp
-      const int64_t w = s_word[warp][j];
-      const float g = s_g[warp][j];
+    if (one_scale) {  // uniform over the warp
+      uint32_t bytes[kNvScBatch];
+      uint2 codes[kNvScBatch];
 #pragma unroll
       for (int b = 0; b < kNvScBatch; ++b) {
-        const int pass = p0 + b;
-        const int blk = pass * 32 + lane;
-        const uint32_t byte = cvt_e4m3_satfinite(g * q[b]);
-        const uint2 code = nv_codes<kF16>(v[b], byte, byte != 0u ? g / e4m3_to_f32(byte) : 0.0f);
-        uint8_t* const cp = p.codes + c + static_cast<int64_t>(blk) * 8;
-        if (pass < n_pass && blk < p.sK && MXFP4_IN_BOUNDS(p, kDbgCodes, cp, 8))
-          st_stream_v2(cp, code);
-        if constexpr (kStaged) {
-          // the route's scale bytes, 32 per pass, into its workspace row (zero
-          // for the pad columns past sK)
-          uint8_t* const bp = p.stage + w + blk;
-          if (pass < n_pass && blk < 4 * p.nKT && MXFP4_IN_BOUNDS(p, kDbgWork, bp, 1))
-            st_keep_u8(bp, byte, keep);
-        } else {
-          // scale word of k-tile pass*8 + lane/4: the bytes of lanes +0..+3
-          const uint32_t word = byte | (__shfl_down_sync(0xFFFFFFFFu, byte, 1) << 8) |
-                                (__shfl_down_sync(0xFFFFFFFFu, byte, 2) << 16) |
-                                (__shfl_down_sync(0xFFFFFFFFu, byte, 3) << 24);
-          const int kt = pass * 8 + (lane >> 2);
-          uint8_t* const wp = p.scales + w + static_cast<int64_t>(kt) * kChunkBytes;
-          if (pass < n_pass && (lane & 3) == 0 && kt < p.nKT &&
-              MXFP4_IN_BOUNDS(p, kDbgScales, wp, 4))
-            st_keep_u32(wp, word, keep);
+        bytes[b] = cvt_e4m3_satfinite(g0 * q[b]);
+        codes[b] = nv_codes<kF16>(v[b], bytes[b],
+                                  bytes[b] != 0u ? g0 / e4m3_to_f32(bytes[b]) : 0.0f);
+      }
+      for (int j = 0; j < p.top_k; ++j) {
+        const int64_t c = s_code[warp][j];
+        if (c < 0) continue;  // the same for every lane of the warp
+        const int64_t w = s_word[warp][j];
+#pragma unroll
+        for (int b = 0; b < kNvScBatch; ++b) put(c, w, p0, b, bytes[b], codes[b]);
+      }
+    } else {
+      for (int j = 0; j < p.top_k; ++j) {
+        const int64_t c = s_code[warp][j];
+        if (c < 0) continue;
+        const int64_t w = s_word[warp][j];
+        const float g = s_g[warp][j];
+#pragma unroll
+        for (int b = 0; b < kNvScBatch; ++b) {
+          const uint32_t byte = cvt_e4m3_satfinite(g * q[b]);
+          put(c, w, p0, b, byte,
+              nv_codes<kF16>(v[b], byte, byte != 0u ? g / e4m3_to_f32(byte) : 0.0f));
         }
       }
     }

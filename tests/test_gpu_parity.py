@@ -1129,6 +1129,26 @@ def test_nvfp4_scatter_bad_entries_offsets_and_no_tokens(mx, scatter_ws):
     assert np.array_equal(gpu[0], orc[0]) and np.array_equal(gpu[1], orc[1])  # untouched
 
 
+@pytest.mark.parametrize("f16", [False, True])
+def test_nvfp4_scatter_shared_global_scales(mx, f16, scatter_ws):
+    """Experts that share a global scale (all of them, then runs of equal and
+    distinct scales, with dropped routes in between): a token's routes to
+    such experts get equal codes and scale bytes, the rest their own; every
+    byte against the oracle, over several passes and a ragged tail."""
+    g = W.moe_grouped(seed=57, tokens=300, top_k=6, num_experts=12, K=2880 + 32,
+                      device="cuda")
+    dst = g.dest_rows.clone()
+    drop = torch.rand(dst.shape, generator=torch.Generator().manual_seed(7)) < 0.15
+    dst[drop.cuda()] = -1
+    xt = g.x_tokens.to(torch.float16) if f16 else g.x_tokens
+    shared = np.full(12, 448.0 * 6.0 / 5.0, np.float32)
+    runs = np.array([1.0, 1.0, 3.0, 3.0, 1.0, 0.5, 0.5, 0.5, 7.0, 1.0, 1.0, 3.0], np.float32)
+    for gs in (shared, runs * np.float32(448.0 * 6.0 / 20.0)):
+        gpu, orc = run_nvfp4_scatter(mx, xt, dst, g.offsets, g.row_index.numel(), gs, seed=58,
+                                     ws=scatter_ws)
+        assert_scatter_parity(gpu, orc)
+
+
 def test_nvfp4_scatter_moe_full_size(mx):
     """16384 tokens x top-8 over 384 experts with their own global scales,
     K = 7168: byte for byte the NVFP4 experts quant of the gathered batch;
@@ -1153,6 +1173,28 @@ def test_nvfp4_scatter_moe_full_size(mx):
         assert np.array_equal(c1[a:b].cpu().numpy(), c_o), e
         p0 = int(sro1[e].item()) * (7168 // 16)
         assert np.array_equal(s1[p0:p0 + s_o.size].cpu().numpy(), s_o), e
+
+
+def test_nvfp4_scatter_moe_full_size_one_global_scale(mx):
+    """The same batch with one global scale for every expert (each token's
+    routes then share their bytes and codes): both scatter forms equal the
+    NVFP4 experts quant of the gathered batch, one expert also the oracle."""
+    g = W.moe_grouped(seed=2, device="cuda")
+    E = g.num_experts
+    gs = torch.full((E,), 448.0 * 6.0 / 5.0, device="cuda")
+    c2, s2, sro2, st2 = mx.quantize_nvfp4_grouped(g.x, g.offsets, gs)
+    for staged in (True, False):
+        c1, s1, sro1, st1 = mx.quantize_nvfp4_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets,
+                                                              gs, staged=staged)
+        torch.cuda.synchronize()
+        assert int(st1.item()) == int(st2.item()) == 0
+        assert torch.equal(sro1, sro2)
+        used = int(sro1[-1].item()) * (7168 // 16)
+        assert torch.equal(c1, c2) and torch.equal(s1[:used], s2[:used]), staged
+    off_h = g.offsets.cpu().numpy()
+    a, b = int(off_h[77]), int(off_h[78])
+    c_o, s_o = oracle.nvfp4_quantize(bits(g.x[a:b]), float(gs[77]))
+    assert np.array_equal(c2[a:b].cpu().numpy(), c_o)
 
 
 # ----------------------------------------------- FP16 input, grouped forms
