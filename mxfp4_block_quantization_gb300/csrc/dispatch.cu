@@ -449,8 +449,9 @@ __global__ void __launch_bounds__(kThreads) gather_row_codes_kernel(const RowCod
 // of 512 elements (lane = one 16-element block), and each block's max and
 // q = vecMax / 6 are taken once; then, per route, the block's E4M3 byte
 // (g[e] * q), inverse scale and codes with that route's global scale (a
-// token's codes differ per expert).  Codes leave as one 256-byte run per
-// route and pass.  The scale bytes go either
+// token's codes differ per expert), or once for all routes when the token's
+// experts share one global scale.  Codes leave as one 256-byte run per route
+// and pass.  The scale bytes go either
 //   direct: as the 4-byte word of each k-tile (4 lanes) into the tiled layout
 //     of every route, under an L2 evict-last policy (14.7 M scattered words on
 //     the MoE batch); the first E CTAs zero the segments' pad rows; or
