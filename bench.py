@@ -268,8 +268,8 @@ def run_reference(args):
     t0 = time.perf_counter()
     oracle.quantize(xb_full[:8])
     per_row = (time.perf_counter() - t0) / 8
-    budget = min(0.25, 90.0 / max(steps_total, 1))
-    rows = int(max(1, min(M_DENSE, budget / max(per_row, 1e-9))))
+    step_s = min(0.25, 90.0 / max(steps_total, 1))  # seconds of oracle work per step
+    rows = int(max(1, min(M_DENSE, step_s / max(per_row, 1e-9))))
     xb = np.ascontiguousarray(xb_full[:rows])
     for _ in range(args.warmup):
         oracle.quantize(xb)
