@@ -161,6 +161,12 @@ def test_everything_in_bounds(libs):
                                                                    gsc), 2 * 1056))  # K/16 cols
     cases.append(lambda: written(mx.quantize_nvfp4_grouped_scatter(g3.x_tokens, g3d, g3.offsets,
                                                                    gsc, staged=False), 2 * 1056))
+    # the same with one global scale for every expert (routes share their bytes and codes)
+    gs1 = torch.full((5,), 6.5, device="cuda")
+    cases.append(lambda: written(mx.quantize_nvfp4_grouped_scatter(g3.x_tokens, g3d, g3.offsets,
+                                                                   gs1), 2 * 1056))
+    cases.append(lambda: written(mx.quantize_nvfp4_grouped_scatter(g3.x_tokens, g3d, g3.offsets,
+                                                                   gs1, staged=False), 2 * 1056))
     # NVFP4 experts quant (K a multiple of 16 but not 32 included)
     gn = W.moe_grouped(seed=10, tokens=150, top_k=3, num_experts=7, K=80, device="cuda")
     gsn = torch.linspace(0.5, 40.0, 7, device="cuda")
