@@ -1335,6 +1335,19 @@ def test_gather_ws_long_overflow_list(mx):
                                        torch.from_numpy(off).cuda()), bits(xt), idx, off, 256)
 
 
+def test_gather_per_row_kernel_many_tiles(mx):
+    """K = 64 leaves too few code bytes to lend a workspace: the call without
+    one runs the per-row gather kernel, here over 32,768 rows in 64 segments
+    (hundreds of padded tiles), every byte against the oracle."""
+    g = W.moe_grouped(seed=63, tokens=4096, top_k=8, num_experts=64, K=64, device="cuda")
+    total = g.row_index.numel()
+    ws = mx.mxfp4_gather_workspace_bytes(4096, total, 64, 64)
+    assert -(-ws // 32) * 4 > total  # more than a quarter of the rows' codes: no borrowing
+    got = run_gather(mx, g.x_tokens, g.row_index, g.offsets)
+    _gather_oracle_check(got, bits(g.x_tokens), g.token_of_row.numpy().astype(np.int32),
+                         g.offsets.cpu().numpy(), 64)
+
+
 @pytest.mark.parametrize("f16", [False, True])
 def test_gather_without_workspace_borrows_its_codes_tail(mx, f16):
     """The gather without a workspace, large enough to run through the scatter
