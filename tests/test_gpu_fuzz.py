@@ -109,8 +109,14 @@ def test_fuzz_grouped_gather_scatter(mx, seed):
         assert int(st.item()) == rc == 0, staged
         assert np.array_equal(codes.cpu().numpy(), c_o), staged
         assert np.array_equal(scales.cpu().numpy(), s_o), staged
-    # the NVFP4 experts quant of the same routing, a global scale per expert
+    # the NVFP4 experts quant of the same routing, a global scale per expert:
+    # all distinct, one shared by every expert, or a few values repeated (a
+    # token whose experts share one scale computes its bytes once)
     gs = (448.0 * 6.0 / np.exp(rng.uniform(-3, 8, E))).astype(np.float32)
+    if seed % 3 == 1:
+        gs[:] = gs[0]
+    elif seed % 3 == 2:
+        gs = gs[rng.integers(0, min(3, E), E)]
     nsb_nv = mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K)
     s0_nv = rng.integers(0, 256, nsb_nv, dtype=np.uint8)
     rc_nv, cn_o, sn_o, _ = oracle.nvfp4_quantize_grouped_scatter(xb, dest, off, total, gs, c0,
