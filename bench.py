@@ -543,8 +543,9 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
                                                              total, g_nv, ws, codes, sc_nv, sro,
                                                              st, stream), 30, stream)
     e_ = entry(nb_nvs, ms_nvw, 3, "same call and bytes as the row above; offsets kernel, "
-               "workspace memset, scatter kernel (its first CTAs write the padded-row map), "
-               "tile kernel")
+               "workspace memset, scatter kernel (its first CTAs mark the pad rows, each "
+               "token warp maps its routes to their staged rows; a token whose experts "
+               "share one scale stages its bytes once), tile kernel")
     e_["speedup_vs_unfused"] = round(ms_nvu / ms_nvw, 3)
     e_["speedup_vs_direct"] = round(ms_nvs / ms_nvw, 3)
     out["nvfp4_grouped_scatter_ws_moe_16384tok_top8_E384"] = e_

@@ -243,9 +243,10 @@ __device__ __forceinline__ void scatter_token(const ScatterParams& p, int64_t t,
 constexpr int kMapSegs = 511;
 static_assert((kMapSegs + 1) * 4 == kScatterWarps * MXFP4_SCATTER_MAX_TOP_K * 8,
               "one segment array fills one route array");
-// kRowValue: record padded row + 1 (the NVFP4 scatter stages each route's
-// scale bytes by padded row) instead of token + 1.
-template <bool kRowValue = false, typename P>
+// kPadOnly: write the pad rows only (the NVFP4 scatter's token warps write
+// their own routes' entries, each pointing at the row of staged scale bytes
+// the route reads).
+template <bool kPadOnly = false, typename P>
 __device__ __forceinline__ void scatter_route_map(const P& p, int m, int32_t* s_off,
                                                   int32_t* s_pad) {
   const SegmentSearch seg(s_off, s_pad, p.offsets, p.padded, p.E,
@@ -263,6 +264,7 @@ __device__ __forceinline__ void scatter_route_map(const P& p, int m, int32_t* s_
     int32_t* const tp = p.tok1 + seg.padded_start(e) + n + i;
     if (MXFP4_IN_BOUNDS(p, kDbgWork, tp, 4)) *tp = -1;
   }
+  if constexpr (kPadOnly) return;
   const int64_t n_routes = p.num_tokens * p.top_k;
   for (int64_t i = gid; i < n_routes; i += stride) {
     const int32_t* dp = p.dest_rows + i;
@@ -270,8 +272,7 @@ __device__ __forceinline__ void scatter_route_map(const P& p, int m, int32_t* s_
     if (v < 0 || v >= p.total_rows) continue;  // the token warps report bad entries
     const int prow = seg.padded_row(v);
     int32_t* const tp = p.tok1 + prow;
-    if (MXFP4_IN_BOUNDS(p, kDbgWork, tp, 4))
-      *tp = kRowValue ? prow + 1 : static_cast<int32_t>(i / p.top_k) + 1;
+    if (MXFP4_IN_BOUNDS(p, kDbgWork, tp, 4)) *tp = static_cast<int32_t>(i / p.top_k) + 1;
   }
 }
 
@@ -457,8 +458,10 @@ __global__ void __launch_bounds__(kThreads) gather_row_codes_kernel(const RowCod
 //     the MoE batch); the first E CTAs zero the segments' pad rows; or
 //   staged (kStaged): as one 32-byte run per route and pass into the route's
 //     padded row of a workspace, which tile_scales_kernel then writes to the
-//     tiled layout whole; the first map_ctas CTAs record each routed row's
-//     padded row (pad rows -1) beside the token warps.
+//     tiled layout whole.  Each token warp records, for each route, the
+//     workspace row its bytes are in (+1): its own, or for a token whose
+//     routes share one scale the first route's, the only row it stages.  The
+//     first map_ctas CTAs mark the pad rows -1 beside the token warps.
 struct Nvfp4ScatterParams {
   const uint8_t* __restrict__ x;          // 16-bit token rows
   int64_t ldx_bytes;
@@ -553,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_scatter_kernel(const Nvfp4S
 
   // routes, one per lane
   int64_t co = -1, wo = -1;
+  int32_t prow = -1;
   float ge = 0.0f;
   bool bad = false;
   if (lane < p.top_k) {
@@ -561,7 +565,8 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_scatter_kernel(const Nvfp4S
     if (v >= 0 && v < p.total_rows) {
       const int e = find_segment(p.offsets, p.E, v, static_cast<int>(p.total_rows));
       co = static_cast<int64_t>(v) * p.code_ld;
-      wo = nv_row_base<kStaged>(__ldg(p.padded + e) + (v - __ldg(p.offsets + e)), p.nKT);
+      prow = __ldg(p.padded + e) + (v - __ldg(p.offsets + e));
+      wo = nv_row_base<kStaged>(prow, p.nKT);
       ge = MXFP4_IN_BOUNDS_G(p, p.g + e, 4) ? __ldg(p.g + e) : 0.0f;
     } else {
       bad = v != -1;
@@ -581,15 +586,23 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_scatter_kernel(const Nvfp4S
   // per-route loop.  Decided once per token, outside the route loops.
   const unsigned routed = __ballot_sync(0xFFFFFFFFu, co >= 0);
   if (routed == 0u) return;  // whole warp: nothing to write
-  const float g0 = __shfl_sync(0xFFFFFFFFu, ge, __ffs(static_cast<int>(routed)) - 1);
+  const int first = __ffs(static_cast<int>(routed)) - 1;  // the first route
+  const float g0 = __shfl_sync(0xFFFFFFFFu, ge, first);
   const bool one_scale =
       __all_sync(0xFFFFFFFFu, co < 0 || __float_as_uint(ge) == __float_as_uint(g0));
+  if constexpr (kStaged) {
+    // each route's map entry: the staged row its scale bytes are read from,
+    // + 1; with one scale the token stages them once, in its first route's row
+    const int32_t prow0 = __shfl_sync(0xFFFFFFFFu, prow, first);
+    int32_t* const tp = p.tok1 + prow;
+    if (co >= 0 && MXFP4_IN_BOUNDS(p, kDbgWork, tp, 4)) *tp = (one_scale ? prow0 : prow) + 1;
+  }
 
   const uint8_t* xrow = p.x + t * p.ldx_bytes + lane * 32;
   const int n_pass = (p.sK + 31) / 32;  // 32 blocks per pass
   const uint64_t keep = l2_evict_last_policy();
   // the stores of pass p0 + b for the route with codes at c and scale row w
-  auto put = [&](int64_t c, int64_t w, int p0, int b, uint32_t byte, uint2 code) {
+  auto put = [&](int64_t c, int64_t w, int p0, int b, uint32_t byte, uint2 code, bool stage) {
     const int pass = p0 + b;
     const int blk = pass * 32 + lane;
     uint8_t* const cp = p.codes + c + static_cast<int64_t>(blk) * 8;
@@ -599,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_scatter_kernel(const Nvfp4S
       // the route's scale bytes, 32 per pass, into its workspace row (zero
       // for the pad columns past sK)
       uint8_t* const bp = p.stage + w + blk;
-      if (pass < n_pass && blk < 4 * p.nKT && MXFP4_IN_BOUNDS(p, kDbgWork, bp, 1))
+      if (stage && pass < n_pass && blk < 4 * p.nKT && MXFP4_IN_BOUNDS(p, kDbgWork, bp, 1))
         st_keep_u8(bp, byte, keep);
     } else {
       // scale word of k-tile pass*8 + lane/4: the bytes of lanes +0..+3
@@ -639,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_scatter_kernel(const Nvfp4S
         if (c < 0) continue;  // the same for every lane of the warp
         const int64_t w = s_word[warp][j];
 #pragma unroll
-        for (int b = 0; b < kNvScBatch; ++b) put(c, w, p0, b, bytes[b], codes[b]);
+        for (int b = 0; b < kNvScBatch; ++b) put(c, w, p0, b, bytes[b], codes[b], j == first);
       }
     } else {
       for (int j = 0; j < p.top_k; ++j) {
@@ -651,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_scatter_kernel(const Nvfp4S
         for (int b = 0; b < kNvScBatch; ++b) {
           const uint32_t byte = cvt_e4m3_satfinite(g * q[b]);
           put(c, w, p0, b, byte,
-              nv_codes<kF16>(v[b], byte, byte != 0u ? g / e4m3_to_f32(byte) : 0.0f));
+              nv_codes<kF16>(v[b], byte, byte != 0u ? g / e4m3_to_f32(byte) : 0.0f), true);
         }
       }
     }
@@ -662,7 +675,9 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_scatter_kernel(const Nvfp4S
 // words: one CTA per padded 128-row tile.  Padded row pr takes the words of
 // token tok1[pr] - 1 (for the gather written by invert_bucket_kernel for row
 // o[e] + pr - P[e] of segment e, for the scatter by the map CTAs of the
-// scatter launch).  In the gather, pad rows and rows whose index is out of
+// scatter launch; in the NVFP4 scatter the staged rows are rows of scale
+// bytes, one per route or one per token, written by the token warps).  In
+// the gather, pad rows and rows whose index is out of
 // range keep tok1 = 0 and get zero words; in the scatter, pad rows are marked
 // -1 and get zero words, and rows that no route targets (0) keep the words
 // they held.  The tile's 128 x nKT words pass through shared memory, 32
@@ -1222,9 +1237,8 @@ cudaError_t launch_quantize_nvfp4_grouped_scatter(const void* x, int64_t num_tok
   p.nKT = (p.sK + kTileBlocks - 1) / kTileBlocks;
   p.pad_ctas = staged ? 0 : E;
   if (staged) {
-    const int64_t items = num_tokens * top_k > static_cast<int64_t>(E) * kTileRows
-                              ? num_tokens * top_k
-                              : static_cast<int64_t>(E) * kTileRows;
+    // the map CTAs write the pad rows only (the token warps the routed rows)
+    const int64_t items = static_cast<int64_t>(E) * kTileRows;
     const int64_t need = (items + 4 * kThreads - 1) / (4 * kThreads);
     p.map_ctas = static_cast<int32_t>(need < 1 ? 1 : (need < sm_count() ? need : sm_count()));
     p.tok1 = workspace;
