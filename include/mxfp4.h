@@ -465,7 +465,9 @@ int mxfp4_quantize_nvfp4_grouped_scatter_f16(const void* x, int64_t num_tokens, 
  * caller-provided workspace: each route's scale bytes are stored as one
  * contiguous row of the workspace (indexed by the route's padded row) instead
  * of as 4-byte words scattered over the tiled layout, and a second kernel
- * writes the tiled scales in whole 512-byte chunks.
+ * writes the tiled scales in whole 512-byte chunks.  A token whose routes all
+ * land in experts of one global scale (the same bits) has the same scale
+ * bytes on every route; it stores them once, in its first route's row.
  *
  * workspace        DEVICE scratch owned by the caller, 16-byte aligned, at
  *                  least mxfp4_nvfp4_scatter_workspace_bytes(total_rows, E, K)
@@ -473,8 +475,9 @@ int mxfp4_quantize_nvfp4_grouped_scatter_f16(const void* x, int64_t num_tokens, 
  *                  entry do not matter, on return unspecified.
  *
  * mxfp4_nvfp4_scatter_workspace_bytes: PT * (4 + 4 * ceil4(ceil(K/64)))
- * bytes, PT = floor((total_rows + 127E) / 128) * 128 padded rows (the padded
- * row of every routed row, then one staged scale row per padded row); 0 for
+ * bytes, PT = floor((total_rows + 127E) / 128) * 128 padded rows (for every
+ * padded row the staged row its scale bytes are read from, then one staged
+ * scale row per padded row); 0 for
  * negative sizes, K % 16 != 0 or total_rows + 127E > INT32_MAX.
  */
 size_t mxfp4_nvfp4_scatter_workspace_bytes(int64_t total_rows, int32_t E, int64_t K);
