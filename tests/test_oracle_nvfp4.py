@@ -260,6 +260,35 @@ def test_nvfp4_scatter_equals_experts_quant_of_the_permuted_batch(orc, f16):
             assert np.array_equal(s[idx], src[idx]), (e, p)
 
 
+def test_nvfp4_scatter_one_scale_every_route_is_the_dense_row(orc):
+    """With one global scale for every expert, each route of a token carries
+    the dense NVFP4 quantization of its token row: the same codes, and in
+    every scale column the same E4M3 byte (read through the tiled layout:
+    padded row p, column c at ((p/128)*nKT + c/4)*512 + (p%32)*16 +
+    ((p%128)/32)*4 + c%4, segment e's rows starting at its padded start)."""
+    g = W.moe_grouped(seed=43, tokens=40, top_k=4, num_experts=6, K=96)
+    xb = W.bf16_bits(g.x_tokens)
+    dest = g.dest_rows.numpy()
+    off = g.offsets.numpy()
+    gs = np.full(6, 448.0 * 6.0 / 5.0, np.float32)
+    rc, c, s, sro = orc.nvfp4_quantize_grouped_scatter(xb, dest, off, dest.size, gs)
+    assert rc == 0
+    sK = 96 // 16
+    nKT = (sK + 3) // 4
+
+    def col_bytes(buf, p):
+        return [int(buf[((p // 128) * nKT + k // 4) * 512 + (p % 32) * 16 +
+                        ((p % 128) // 32) * 4 + k % 4]) for k in range(sK)]
+
+    for t in range(40):
+        cd, sd = orc.nvfp4_quantize(xb[t:t + 1], float(gs[0]))
+        for v in dest[t]:
+            e = int(np.searchsorted(off, v, side="right")) - 1
+            p = int(sro[e]) + int(v) - int(off[e])
+            assert np.array_equal(c[v], cd[0]), (t, v)
+            assert col_bytes(s, p) == col_bytes(sd, 0), (t, v)
+
+
 def test_nvfp4_scatter_bad_entries_and_offsets(orc):
     g = W.moe_grouped(seed=43, tokens=40, top_k=2, num_experts=3, K=32)
     xb = W.bf16_bits(g.x_tokens)
