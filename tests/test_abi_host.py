@@ -147,6 +147,11 @@ def test_grouped_gather_validation(lib):
     assert call(ldx=68) == lib.MXFP4_EALIGN
     assert call(c=2 * A + 16) == lib.MXFP4_EALIAS            # codes overlap the indices
     assert call(sro=A + 64) == lib.MXFP4_EALIAS              # offsets out overlap x
+    # the call may use the tail of codes as its workspace: nothing else may
+    # share those bytes
+    assert call(c=3 * A) == lib.MXFP4_EALIAS                 # codes overlap the offsets
+    assert call(st=4 * A + 64) == lib.MXFP4_EALIAS           # status inside the codes
+    assert call(sro=4 * A + 256) == lib.MXFP4_EALIAS         # offsets out inside the codes
 
 
 def test_grouped_scatter_validation(lib):
