@@ -422,6 +422,16 @@ __device__ __forceinline__ void st_keep_u32(void* p, uint32_t v, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
 }
 
+// L2 prefetch of the 128-byte line holding p.  It returns no data, so a
+// kernel may issue it before its grid-dependency wait: the L2 is where this
+// GPU's writes become coherent, so the loads after the wait read the
+// predecessor's writes whatever the prefetch brought in.  Issued by the CTAs
+// that start while the preceding grid drains, it fills the DRAM idle time of
+// that grid's last wave.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Programmatic dependent launch: wait until the preceding grid of the stream
 // has completed and its writes are visible (no-op without a predecessor),
 // and allow the next grid of the stream to be scheduled.

@@ -81,14 +81,26 @@ __global__ void __launch_bounds__(kThreads) quantize_tiles_kernel(const Quantize
   constexpr int kPasses = passes(kThreads);
   __shared__ __align__(16) uint8_t chunk[kChunkBytes];
 
-  pdl_wait();
-  pdl_release();
-
   // Tile order: m-tile-major, so consecutive CTAs read adjacent column slices
   // of the same rows.
   const int unit = blockIdx.x;
   const int mt = unit / p.nKT;
   const int kt = unit - mt * p.nKT;
+
+  if constexpr (!kGrouped) {
+    // The dense tile's rows are known before the wait: thread t asks the L2
+    // for half t % 2 (two scale blocks, 128 bytes) of tile row t / 2, when
+    // that half holds a real block.
+    const int64_t pr = static_cast<int64_t>(mt) * kTileRows + (threadIdx.x >> 1);
+    const int half = threadIdx.x & 1;
+    const uint8_t* pp = p.x + pr * p.ldx_bytes + static_cast<int64_t>(kt) * (kTileCols * 2) +
+                        half * (kTileCols);
+    if (pr < p.M && kt * kTileBlocks + 2 * half < p.sK && MXFP4_IN_BOUNDS(p, kDbgX, pp, 1))
+      prefetch_l2(pp);
+  }
+
+  pdl_wait();
+  pdl_release();
   int64_t row0, row_end;
   if constexpr (kGrouped) {
     // every offset index read below lies in [0, E]
