@@ -257,7 +257,7 @@ def cpu_baseline(xb, min_seconds=2.0, max_reps=20):
 def run_reference(args):
     import numpy as np
     import oracle
-    from mxfp4_block_quantization_gb300 import workloads as W
+    import workloads as W
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
@@ -613,7 +613,7 @@ def run_one_call(args):
     (ncu -k on this command sees only its kernels)."""
     import torch
     import mxfp4_block_quantization_gb300 as mx
-    from mxfp4_block_quantization_gb300 import workloads as W
+    import workloads as W
     g = W.moe_grouped(seed=2, device="cuda")
     T, K = g.x_tokens.shape
     total = g.row_index.numel()
@@ -666,7 +666,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     import mxfp4_block_quantization_gb300 as mx
-    from mxfp4_block_quantization_gb300 import workloads as W
+    import workloads as W
 
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)

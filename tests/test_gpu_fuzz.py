@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from mxfp4_block_quantization_gb300 import workloads as W
+import workloads as W
 
 pytestmark = pytest.mark.gpu
 

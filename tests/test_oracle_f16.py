@@ -1,7 +1,7 @@
 """Pins of the oracle's FP16-input path (same MX method, binary16 input)."""
 import numpy as np
 
-from mxfp4_block_quantization_gb300 import workloads as W
+import workloads as W
 
 E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 ALL = np.arange(65536, dtype=np.uint32).astype(np.uint16)

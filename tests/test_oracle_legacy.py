@@ -9,7 +9,7 @@ library never uses it) and these tests pin it and report what it costs on
 the workloads."""
 import numpy as np
 
-from mxfp4_block_quantization_gb300 import workloads as W
+import workloads as W
 
 
 def _bf16_values(bits):

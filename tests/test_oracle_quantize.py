@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from conftest import load_golden
-from mxfp4_block_quantization_gb300 import workloads as W
+import workloads as W
 
 
 def _nibbles(codes):

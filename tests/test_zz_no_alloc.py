@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from mxfp4_block_quantization_gb300 import workloads as W
+import workloads as W
 
 pytestmark = pytest.mark.gpu
 

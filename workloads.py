@@ -3,7 +3,9 @@
 This module only draws and shapes input tensors; it holds none of the
 method's arithmetic (no scale, rounding or layout logic).  Both the GPU
 library's tests/benchmark and the CPU oracle's tests take their inputs from
-here.  Every generator is deterministic for a given seed and device; values
+here.  It sits outside the library package and imports only torch, so a
+process that draws inputs for the oracle alone maps no part of the CUDA
+library.  Every generator is deterministic for a given seed and device; values
 are drawn as float32 with ``torch.Generator`` and rounded to BF16 by torch's
 round-to-nearest-even cast.
 
