@@ -227,8 +227,11 @@ int mxfp4_quantize_grouped_gather_ws_f16(const void* x, int64_t num_src_rows, in
  * process exits).  For callers that cannot allocate device memory.  No
  * counterpart exists in the method's sources.
  *
- * Arguments, outputs, status and errors as mxfp4_quantize_grouped_gather, and
- * MXFP4_ESCRATCH (returned before anything is enqueued) when the inverse map
+ * Arguments, outputs and status as mxfp4_quantize_grouped_gather.  Errors are
+ * checked in the same order as mxfp4_quantize_grouped_gather_ws (so a shape
+ * fault or a size beyond the int32 limits is MXFP4_ESHAPE, a NULL pointer
+ * MXFP4_EINVAL); where that call would check the workspace size, this one
+ * returns MXFP4_ESCRATCH (before anything is enqueued) when the inverse map
  * alone, mxfp4_gather_workspace_bytes(num_src_rows, total_rows, E, 0),
  * exceeds MXFP4_NOALLOC_SCRATCH_BYTES.  When the whole workspace
  * (mxfp4_gather_workspace_bytes(num_src_rows, total_rows, E, K)) fits, the
@@ -238,9 +241,11 @@ int mxfp4_quantize_grouped_gather_ws_f16(const void* x, int64_t num_src_rows, in
  * Every call shares the one buffer of its device: two calls that can overlap
  * on the GPU (different streams, or a graph replayed concurrently) race and
  * give wrong results; serialise them.  The buffer keeps the last call's
- * contents; each call clears what must start at zero.  The first call on a
- * device looks up the buffer's device address (a host-side query, once per
- * device): make that first call outside any stream capture.
+ * contents; each call clears what must start at zero.  A call looks up the
+ * buffer's device address (a host-side query) on its device's first call
+ * and again when the current context has changed since (after
+ * cudaDeviceReset the buffer lives at a new address): make the first call
+ * on a device, and the first after a reset, outside any stream capture.
  */
 #define MXFP4_NOALLOC_SCRATCH_BYTES (4u << 20)
 int mxfp4_quantize_grouped_gather_noalloc(const void* x, int64_t num_src_rows, int64_t K,

@@ -34,20 +34,61 @@ int sm_count() {
 
 // Fixed scratch of mxfp4_quantize_grouped_gather_noalloc: the inverse-map
 // workspace of the gather-through-scatter path, for callers that cannot
-// allocate.  Host code only ever uses its device address, looked up once per
-// device with that device current.
+// allocate.  Host code only ever uses its device address, looked up with the
+// device current.
 static __device__ __align__(256) int32_t g_noalloc_scratch[MXFP4_NOALLOC_SCRATCH_BYTES / 4];
 
+// The process-unique id of the calling thread's current context (the
+// driver's cuCtxGetCurrent and cuCtxGetId, reached through the runtime's
+// driver entry points so that the library does not link libcuda), or 0 when
+// there is none or the entry points are unavailable.
+unsigned long long current_context_id() {
+  using GetCurrent = int (*)(void**);
+  using GetId = int (*)(void*, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  void* ctx = nullptr;
+  if (get_current(&ctx) != 0 || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  return get_id(ctx, &id) == 0 ? id : 0;
+}
+
+// Device address of the scratch array in the current context.  The address
+// is looked up on a device's first call and again whenever the current
+// context is not the one it was looked up in (a cudaDeviceReset destroys the
+// primary context, and the array then lives at a new address in the next
+// one); context ids are never reused within a process.  Without a context id
+// the address is looked up on every call.
 int32_t* noalloc_scratch() {
   static std::mutex mu;
   static int32_t* cached[64] = {nullptr};
+  static unsigned long long cached_ctx[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (cached[dev] == nullptr) {
+  const unsigned long long id = current_context_id();
+  if (id == 0 || cached[dev] == nullptr || cached_ctx[dev] != id) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
     cached[dev] = static_cast<int32_t*>(ptr);
+    // the lookup made the device's context current if none was
+    cached_ctx[dev] = id != 0 ? id : current_context_id();
   }
   return cached[dev];
 }
@@ -158,8 +199,10 @@ int grouped_checked(const void* x, int64_t total_rows, int64_t K,
 // How a gather call runs: the per-row gather kernel, or the scatter path with
 // the inverse map in a workspace, its scale words stored straight into the
 // tiled layout (kInverse) or staged per token and tiled by a second kernel
-// (kInverseStaged, the larger workspace).
-enum class GatherPath { kPerRow, kInverse, kInverseStaged };
+// (kInverseStaged, the larger workspace).  kScratch: the scatter path in the
+// library's fixed scratch array, staged when the whole workspace fits it,
+// else kInverse; MXFP4_ESCRATCH when not even the inverse map fits.
+enum class GatherPath { kPerRow, kInverse, kInverseStaged, kScratch };
 
 int64_t gather_ws_bytes(int64_t num_src_rows, int64_t total_rows, int32_t E, int64_t K,
                         bool staged) {
@@ -175,7 +218,8 @@ int gather_checked(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
                    uint8_t* scales, int32_t* scale_row_offsets, int32_t* status, GatherPath path,
                    bool f16, void* stream) {
   const bool use_ws = path != GatherPath::kPerRow;
-  const bool staged = path == GatherPath::kInverseStaged;
+  const bool in_scratch = path == GatherPath::kScratch;
+  bool staged = path == GatherPath::kInverseStaged;
   if (num_src_rows < 0 || total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
   if (K % 32 != 0 || ldx < K) return MXFP4_ESHAPE;
   if (!expert_offsets || !scale_row_offsets) return MXFP4_EINVAL;
@@ -191,6 +235,16 @@ int gather_checked(const void* x, int64_t num_src_rows, int64_t K, int64_t ldx,
     // token ids and route counts are int32 on the device
     if (num_src_rows > INT32_MAX / 4) return MXFP4_ESHAPE;
     if (num_src_rows > (INT64_MAX / 8) / (K / 128 + 1)) return MXFP4_ESHAPE;
+    if (in_scratch) {
+      // the staged form when its whole workspace fits the library's array;
+      // the array's address is looked up only for a call that fits it
+      staged = gather_ws_bytes(num_src_rows, total_rows, E, K, true) <=
+               static_cast<int64_t>(workspace_bytes);
+      if (work && gather_ws_bytes(num_src_rows, total_rows, E, K, staged) >
+                      static_cast<int64_t>(workspace_bytes))
+        return MXFP4_ESCRATCH;
+      if (work && (workspace = mxfp4::noalloc_scratch()) == nullptr) return MXFP4_ECUDA;
+    }
     ws_bytes = gather_ws_bytes(num_src_rows, total_rows, E, K, staged);
     if (work && (!workspace || workspace_bytes < static_cast<size_t>(ws_bytes)))
       return MXFP4_EINVAL;
@@ -350,6 +404,8 @@ size_t mxfp4_gather_workspace_bytes(int64_t num_src_rows, int64_t total_rows, in
   if (num_src_rows < 0 || total_rows < 0 || E < 0 || K < 0 || K % 32 != 0) return 0;
   if (num_src_rows > INT32_MAX / 4 || total_rows + 127 * static_cast<int64_t>(E) > INT32_MAX)
     return 0;
+  // the same bounds the calls apply: k tiles and staged words stay countable
+  if (ceil_div(K / 32, 4) > kMaxGrid || num_src_rows > (INT64_MAX / 8) / (K / 128 + 1)) return 0;
   return static_cast<size_t>(gather_ws_bytes(num_src_rows, total_rows, E, K, K > 0));
 }
 
@@ -369,23 +425,9 @@ int mxfp4_quantize_grouped_gather_noalloc(const void* x, int64_t num_src_rows, i
                                           int32_t E, uint8_t* codes, uint8_t* scales,
                                           int32_t* scale_row_offsets, int32_t* status,
                                           void* stream) {
-  if (num_src_rows < 0 || total_rows < 0 || K < 0 || E < 0) return MXFP4_EINVAL;
-  if (num_src_rows > INT32_MAX / 4 || total_rows + 127 * static_cast<int64_t>(E) > INT32_MAX)
-    return MXFP4_ESCRATCH;
-  // the staged form when its larger workspace fits in the scratch array
-  const GatherPath path =
-      K % 32 == 0 && gather_ws_bytes(num_src_rows, total_rows, E, K, true) <=
-                         static_cast<int64_t>(MXFP4_NOALLOC_SCRATCH_BYTES)
-          ? GatherPath::kInverseStaged
-          : GatherPath::kInverse;
-  if (gather_ws_bytes(num_src_rows, total_rows, E, K, false) >
-      static_cast<int64_t>(MXFP4_NOALLOC_SCRATCH_BYTES))
-    return MXFP4_ESCRATCH;
-  int32_t* scratch = mxfp4::noalloc_scratch();
-  if (scratch == nullptr) return MXFP4_ECUDA;
   return gather_checked(x, num_src_rows, K, ldx, row_index, total_rows, expert_offsets, E,
-                        scratch, MXFP4_NOALLOC_SCRATCH_BYTES, codes, scales, scale_row_offsets,
-                        status, path, false, stream);
+                        nullptr, MXFP4_NOALLOC_SCRATCH_BYTES, codes, scales, scale_row_offsets,
+                        status, GatherPath::kScratch, false, stream);
 }
 
 int mxfp4_quantize_grouped_gather_ws_f16(const void* x, int64_t num_src_rows, int64_t K,

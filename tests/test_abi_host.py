@@ -400,3 +400,44 @@ def test_noalloc_gather_rejects_oversized_scratch(lib):
     assert rc == lib.MXFP4_ESCRATCH
     assert "MXFP4_ESCRATCH" in lib.mxfp4_status_string(rc)
     assert f(A, -1, 64, 64, 2 * A, 1, 3 * A, 1, 4 * A, 5 * A, 6 * A, None, None) == lib.MXFP4_EINVAL
+
+
+def test_noalloc_gather_checks_shapes_before_its_scratch_size(lib):
+    """The call without allocation reports the same errors as the workspace
+    call in the same order, so a shape fault or an int32 overflow is
+    MXFP4_ESHAPE even when the sizes would not fit the scratch either, and
+    MXFP4_ESCRATCH is left for a well-formed call that is too large."""
+    f = lib._lib.mxfp4_quantize_grouped_gather_noalloc
+    big = 10_000_000                                   # map far beyond the scratch
+    # x, n_src, K, ldx, idx, total, off, E, codes, scales, sro, status, stream
+    ok = [A, big, 64, 64, 2 * A, 1, 3 * A, 1, 4 * A, 5 * A, 6 * A, None, None]
+
+    def call(**kw):
+        names = ["x", "n", "K", "ldx", "idx", "tot", "off", "E", "c", "s", "sro", "st", "strm"]
+        a = dict(zip(names, ok))
+        a.update(kw)
+        return f(*[a[n] for n in names])
+
+    assert call() == lib.MXFP4_ESCRATCH
+    assert call(K=48, ldx=48) == lib.MXFP4_ESHAPE             # K % 32 != 0
+    assert call(ldx=32) == lib.MXFP4_ESHAPE                   # ldx < K
+    assert call(n=(1 << 31) // 4 + 1) == lib.MXFP4_ESHAPE     # token ids must stay int32
+    assert call(tot=(1 << 31) - 100, E=2) == lib.MXFP4_ESHAPE  # padded rows overflow int32
+    assert call(off=None) == lib.MXFP4_EINVAL
+    assert call(E=0) == lib.MXFP4_EINVAL                      # rows but no expert
+    assert call(n=0) == lib.MXFP4_EINVAL                      # rows but no source row
+    # the workspace call gives the same codes for the same faults
+    g = lib._lib.mxfp4_quantize_grouped_gather_ws
+    assert g(A, big, 48, 48, 2 * A, 1, 3 * A, 1, 8 * A, 1 << 40, 4 * A, 5 * A, 6 * A, None,
+             None) == lib.MXFP4_ESHAPE
+    assert g(A, (1 << 31) // 4 + 1, 64, 64, 2 * A, 1, 3 * A, 1, 8 * A, 1 << 40, 4 * A, 5 * A,
+             6 * A, None, None) == lib.MXFP4_ESHAPE
+
+
+def test_gather_workspace_bytes_is_zero_beyond_the_call_limits(lib):
+    """The size query returns 0 (no valid call) where the calls themselves
+    would refuse the shape, instead of a truncated size."""
+    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 1 << 40) == 0
+    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 1 << 38) == 0
+    assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 1 << 20) > 0
+    assert lib.mxfp4_gather_workspace_bytes((1 << 31) // 4 + 1, 10, 2, 64) == 0

@@ -35,10 +35,13 @@ def test_noalloc_gather_two_calls_match_the_gather_entry_point():
     assert torch.cuda.is_available()
     import mxfp4_block_quantization_gb300 as mx
     L = mx._lib
-    # the last case's staged scale words do not fit the scratch: the call then
-    # stores the tiled scale words from the scatter kernel itself
+    # the third case's staged scale words do not fit the scratch: the call then
+    # stores the tiled scale words from the scatter kernel itself.  The last
+    # case repeats the first, small staged one after that large call has
+    # left its contents in the shared array, so what must start at zero is
+    # shown to be cleared by the call itself.
     for seed, tokens, top_k, E, K in ((21, 300, 4, 11, 288), (22, 2048, 8, 64, 1024),
-                                      (23, 16384, 4, 32, 7168)):
+                                      (23, 16384, 4, 32, 7168), (21, 300, 4, 11, 288)):
         g = W.moe_grouped(seed=seed, tokens=tokens, top_k=top_k, num_experts=E, K=K,
                           device="cuda")
         total = g.row_index.numel()
@@ -68,3 +71,27 @@ def test_noalloc_gather_two_calls_match_the_gather_entry_point():
         assert int(got[3].item()) == int(ref[3].item()) == mx.MXFP4_EINDEX
         for a, b in zip(got, ref):
             assert torch.equal(a, b), seed
+
+
+def test_noalloc_gather_python_wrapper_matches_the_c_call():
+    """The binding's wrapper (device guard, dtype checks, status handling)
+    gives the bytes of the raw C call, and raises on a refused call."""
+    assert torch.cuda.is_available()
+    import mxfp4_block_quantization_gb300 as mx
+    g = W.moe_grouped(seed=24, tokens=512, top_k=4, num_experts=9, K=320, device="cuda")
+    total, E, K = g.row_index.numel(), 9, 320
+    ref = _outputs(mx, total, K, E)
+    assert _call(mx._lib.mxfp4_quantize_grouped_gather_noalloc, g.x_tokens, g.row_index,
+                 g.offsets, ref) == mx.MXFP4_OK
+    got = _outputs(mx, total, K, E)
+    mx.mxfp4_quantize_grouped_gather_noalloc(g.x_tokens, g.row_index, g.offsets, *got)
+    torch.cuda.synchronize()
+    assert int(got[3].item()) == mx.MXFP4_OK
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+    with pytest.raises(mx.MXFP4Error):
+        mx.mxfp4_quantize_grouped_gather_noalloc(g.x_tokens[:, :K - 16], g.row_index, g.offsets,
+                                                 *got)
+    with pytest.raises(ValueError):
+        mx.mxfp4_quantize_grouped_gather_noalloc(g.x_tokens.float(), g.row_index, g.offsets,
+                                                 *got)
