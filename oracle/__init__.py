@@ -12,6 +12,7 @@ saturation reports computed from oracle outputs have no independent pin
 """
 import ctypes
 import os
+import threading
 
 import numpy as np
 
@@ -427,6 +428,135 @@ def quantize_rows_into(xbits: np.ndarray, row0: int, row1: int, codes: np.ndarra
     lib().orc_quantize(xs.ctypes.data_as(_u16p), row1 - row0, K, K,
                        cs.ctypes.data_as(_u8p),
                        scales[off:].ctypes.data_as(_u8p))
+
+
+# ------------------------------------------- the same routines on host threads
+# Full-size comparisons run the unchanged single-threaded routines above on
+# independent parts of one problem, one host thread per part (the C calls
+# release the GIL): 128-row bands of a dense matrix (every scale chunk belongs
+# to one band), or contiguous ranges of experts of a grouped batch (each
+# range is a grouped problem of its own whose padded scale rows start where
+# the earlier experts' end).  The results equal the single calls byte for
+# byte; the CPU tests check that on shapes with ragged and empty parts.
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _run_parts(fn, parts):
+    errors = []
+
+    def run(args):
+        try:
+            fn(*args)
+        except BaseException as e:  # re-raised on the calling thread
+            errors.append(e)
+
+    ths = [threading.Thread(target=run, args=(a,)) for a in parts]
+    for t in ths:
+        t.start()
+    for t in ths:
+        t.join()
+    if errors:
+        raise errors[0]
+
+
+def _row_bands(M: int, threads: int):
+    tiles = (M + 127) // 128
+    per = max(1, (tiles + threads - 1) // threads)
+    return [(t * 128, min(M, (t + per) * 128)) for t in range(0, tiles, per)]
+
+
+def _expert_ranges(off: np.ndarray, threads: int):
+    """Contiguous expert ranges [e0, e1) of about equal row counts."""
+    E = off.size - 1
+    cuts = np.searchsorted(off, np.linspace(0, off[-1], threads + 1)[1:-1], side="left")
+    bounds = sorted({0, E, *[int(min(max(c, 1), E - 1)) for c in cuts]}) if E > 1 else [0, E]
+    return [(a, b) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+
+
+def quantize_threads(xbits: np.ndarray, threads: int = 0):
+    """quantize() of a whole matrix, the routine run on 128-row bands."""
+    x = _c(xbits, np.uint16)
+    M, K = x.shape
+    codes = np.zeros((M, K // 2), np.uint8)
+    scales = np.zeros(scale_bytes(M, K), np.uint8)
+    if M and K:
+        _run_parts(lambda a, b: quantize_rows_into(x, a, b, codes, scales),
+                   _row_bands(M, threads or host_threads()))
+    return codes, scales
+
+
+def dequantize_threads(codes: np.ndarray, tiled: np.ndarray, M: int, K: int,
+                       threads: int = 0) -> np.ndarray:
+    """dequantize() of a whole matrix, the routine run on 128-row bands."""
+    c = _c(codes, np.uint8).reshape(M, K // 2)
+    t = _c(tiled, np.uint8).ravel()
+    y = np.zeros((M, K), np.uint16)
+    chunk_row = (K // 32 + 3) // 4 * 512          # scale bytes of one 128-row band
+    if M and K:
+        def band(a, b):
+            lib().orc_dequantize(_p(c[a:b], _u8p), _p(t[a // 128 * chunk_row:], _u8p), b - a, K,
+                                 _p(y[a:b], _u16p))
+        _run_parts(band, _row_bands(M, threads or host_threads()))
+    return y
+
+
+def _grouped_threads(single, call, xbits, offsets, cols, g, threads):
+    x = _c(xbits, np.uint16)
+    off32 = _c(offsets, np.int32)
+    off = off32.astype(np.int64)
+    total, K = x.shape
+    E = off.size - 1
+    if E < 1 or off[0] != 0 or off[-1] != total or np.any(np.diff(off) < 0):
+        return single()                          # the single call reports the bad offsets
+    pk = (cols + 3) // 4 * 4
+    padded = np.concatenate([[0], np.cumsum((np.diff(off) + 127) // 128 * 128)])
+    codes = np.zeros((total, K // 2), np.uint8)
+    scales = np.zeros(max(int(padded[-1]) * pk, 1), np.uint8)
+    sro = np.zeros(E + 1, np.int32)
+    rcs = []
+
+    def rng(e0, e1):
+        a, b = int(off[e0]), int(off[e1])
+        sub = (off32[e0:e1 + 1] - off32[e0]).astype(np.int32)
+        sub_sro = np.zeros(e1 - e0 + 1, np.int32)
+        rcs.append(call(x[a:b], b - a, K, sub, e1 - e0, None if g is None else g[e0:e1],
+                        codes[a:b], scales[int(padded[e0]) * pk:], sub_sro))
+        sro[e0:e1] = sub_sro[:-1] + int(padded[e0])
+
+    _run_parts(rng, _expert_ranges(off, threads or host_threads()))
+    sro[E] = int(padded[E])
+    return (0 if all(r == 0 for r in rcs) else min(rcs)), codes, scales, sro
+
+
+def quantize_grouped_threads(xbits: np.ndarray, offsets: np.ndarray, threads: int = 0):
+    """quantize_grouped() with ranges of experts on host threads; the scale
+    buffer ends at the last padded row (the bound's slack is not returned)."""
+    def call(x, n, K, sub, E, _g, c, s, sro):
+        return lib().orc_quantize_grouped(_p(x, _u16p), n, K, _p(sub, _i32p), E, _p(c, _u8p),
+                                          _p(s, _u8p), _p(sro, _i32p))
+    K = xbits.shape[1]
+    return _grouped_threads(lambda: quantize_grouped(xbits, offsets), call, xbits, offsets,
+                            K // 32, None, threads)
+
+
+def nvfp4_quantize_grouped_threads(xbits: np.ndarray, offsets: np.ndarray, g: np.ndarray,
+                                   threads: int = 0):
+    """nvfp4_quantize_grouped() with ranges of experts on host threads; the
+    scale buffer ends at the last padded row."""
+    gs = _c(np.asarray(g, np.float32), np.float32)
+
+    def call(x, n, K, sub, E, g_sub, c, s, sro):
+        g_sub = np.ascontiguousarray(g_sub, np.float32)
+        return lib().orc_nvfp4_quantize_grouped(_p(x, _u16p), n, K, _p(sub, _i32p), E,
+                                                _p(g_sub, _f32p), _p(c, _u8p), _p(s, _u8p),
+                                                _p(sro, _i32p))
+    K = xbits.shape[1]
+    return _grouped_threads(lambda: nvfp4_quantize_grouped(xbits, offsets, gs), call, xbits,
+                            offsets, K // 16, gs, threads)
 
 
 # ------------------------------------------------------------------ NVFP4

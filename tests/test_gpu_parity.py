@@ -21,6 +21,37 @@ def mx():
     return m
 
 
+# The full MoE batch (16384 tokens x top-8 over 384 experts, K = 7168; the
+# grouped workload at its benchmark size) and the oracle's results for it,
+# computed once per module with the unchanged single-threaded routines on
+# ranges of experts over all host cores.
+@pytest.fixture(scope="module")
+def moe():
+    return W.moe_grouped(seed=2, device="cuda")
+
+
+@pytest.fixture(scope="module")
+def moe_oracle(moe):
+    rc, c, s, sro = oracle.quantize_grouped_threads(bits(moe.x), moe.offsets.cpu().numpy())
+    assert rc == 0
+    return c, s, sro
+
+
+@pytest.fixture(scope="module")
+def moe_nvfp4_oracle(moe):
+    gs = _expert_gscales(moe.num_experts, 2)
+    rc, c, s, sro = oracle.nvfp4_quantize_grouped_threads(bits(moe.x), moe.offsets.cpu().numpy(),
+                                                          gs)
+    assert rc == 0
+    return gs, c, s, sro
+
+
+def assert_full(got, want, what):
+    """Every byte of a full-size output equal to the oracle's."""
+    assert got.shape == want.shape, what
+    assert np.array_equal(got, want), f"{what}: {_first_diff(got, want)}"
+
+
 class Guarded:
     """A uint8 (or other dtype) device buffer framed by 0xA5 guard bands."""
 
@@ -219,30 +250,63 @@ def test_grouped_bad_offsets(mx, off):
     assert (c == 0xA5).all() and (s == 0xA5).all(), "outputs must stay untouched"
 
 
-def test_grouped_moe_full_size_sampled(mx):
-    """131072 rows (16384 tokens x top-8 over 384 experts), K = 7168: every
-    padded offset checked; codes and scale chunks of 12 random experts (and
-    the first and last) compared with the oracle segment by segment."""
-    g = W.moe_grouped(seed=2, device="cuda")
-    x, off = g.x, g.offsets
+def test_grouped_moe_full_size(mx, moe, moe_oracle):
+    """131072 rows (16384 tokens x top-8 over 384 experts), K = 7168, against
+    the oracle in full: every code byte, every scale byte of the 147,968
+    padded rows (pad rows and pad columns included), every padded offset; the
+    bound's slack past the last padded row and the guard bands untouched."""
+    x, off = moe.x, moe.offsets
     total, K = x.shape
     E = off.numel() - 1
-    codes, scales, sro, st = mx.quantize_grouped(x, off)
+    bound = mx.mxfp4_grouped_scale_bytes_bound(total, E, K)
+    codes = Guarded(total * (K // 2), shape=(total, K // 2))
+    scales = Guarded(bound)
+    sro = Guarded(4 * (E + 1), torch.int32)
+    st = Guarded(4, torch.int32)
+    mx.mxfp4_quantize_grouped(x, off, codes.t, scales.t, sro.t, st.t)
     torch.cuda.synchronize()
-    assert int(st.cpu()[0]) == 0
-    off_h = off.cpu().numpy().astype(np.int64)
-    n = np.diff(off_h)
-    want_sro = np.concatenate([[0], np.cumsum((n + 127) // 128 * 128)])
-    assert np.array_equal(sro.cpu().numpy(), want_sro)
-    pk = K // 32
-    rng = np.random.default_rng(0)
-    for e in sorted(set(rng.choice(E, 12, replace=False).tolist()) | {0, E - 1}):
+    for g in (codes, scales, sro, st):
+        g.check()
+    assert int(st.t.item()) == 0
+    c_o, s_o, sro_o = moe_oracle
+    assert_full(sro.t.cpu().numpy(), sro_o, "scale row offsets")
+    assert_full(codes.t.cpu().numpy(), c_o, "codes")
+    s_h = scales.t.cpu().numpy()
+    assert_full(s_h[:s_o.size], s_o, "tiled scales")
+    assert (s_h[s_o.size:] == 0xA5).all(), "slack past the last padded row was written"
+
+
+def test_grouped_moe_full_size_dequantize(mx, moe, moe_oracle):
+    """The dequantize of every expert segment of the full MoE batch (each
+    segment its own matrix with its own tiled scales), all 131072 x 7168
+    BF16 outputs against the oracle's dequantize of the same segments."""
+    c_o, s_o, sro_o = moe_oracle
+    total, K = moe.x.shape
+    off_h = moe.offsets.cpu().numpy().astype(np.int64)
+    pk = (K // 32 + 3) // 4 * 4
+    codes = torch.from_numpy(c_o).cuda()
+    scales = torch.from_numpy(s_o).cuda()
+    y = Guarded(total * K * 2, torch.bfloat16, (total, K))
+    E = off_h.size - 1
+    for e in range(E):
         a, b = int(off_h[e]), int(off_h[e + 1])
-        xb = bits(x[a:b])
-        c_o, s_o = oracle.quantize(xb)
-        assert np.array_equal(codes[a:b].cpu().numpy(), c_o), e
-        p0 = int(want_sro[e]) * pk
-        assert np.array_equal(scales[p0:p0 + s_o.size].cpu().numpy(), s_o), e
+        if b > a:
+            p0 = int(sro_o[e]) * pk
+            mx.mxfp4_dequantize(codes[a:b], scales[p0:p0 + mx.mxfp4_scale_bytes(b - a, K)],
+                                b - a, K, y.t[a:b])
+    torch.cuda.synchronize()
+    y.check()
+    want = np.zeros((total, K), np.uint16)
+
+    def seg(e0, e1):
+        for e in range(e0, e1):
+            a, b = int(off_h[e]), int(off_h[e + 1])
+            p0 = int(sro_o[e]) * pk
+            want[a:b] = oracle.dequantize(c_o[a:b], s_o[p0:p0 + oracle.scale_bytes(b - a, K)],
+                                          b - a, K)
+    step = -(-E // oracle.host_threads())
+    oracle._run_parts(seg, [(e, min(E, e + step)) for e in range(0, E, step)])
+    assert_full(bits(y.t), want, "dequantized BF16")
 
 
 # ------------------------------------------------------------------- swap
@@ -293,32 +357,40 @@ def test_swap_page_arange_layout(mx):
     assert b2.tolist() == [[0x0000, 0x3F80, 0x4000, 0x4040]]
 
 
-def test_expert_weights_full_size_sampled(mx):
+def test_expert_weights_full_size(mx):
     """128 experts: w13 [128, 1536, 2048] and w2 [128, 2048, 768] quantized
     as dense [E*rows, K] matrices (each expert a whole number of 128-row
-    tiles), then the w13 swap; 3 experts of each compared with the oracle."""
+    tiles, so its tiled scales are its own chunks), their dequantize, then
+    the w13 swap of codes, tiled scales and both biases: every byte of every
+    output against the oracle, guard bands intact."""
     w = W.expert_weights(3, device="cuda")
     E, two_n, H = w.w13.shape
-    codes13, scales13 = mx.quantize(w.w13.view(E * two_n, H))
-    codes2, scales2 = mx.quantize(w.w2.view(-1, w.w2.shape[2]))
-    per13 = mx.mxfp4_scale_bytes(two_n, H)
-    c_sw, s_sw, b13_sw, b2_sw = mx.swap_w13(codes13.view(E, two_n, H // 2), scales13,
-                                            w.w13_bias, w.w2_bias, scales_tiled=True)
-    torch.cuda.synchronize()
-    N2 = w.w2.shape[1]
-    per2 = mx.mxfp4_scale_bytes(N2, w.w2.shape[2])
-    for e in (0, 57, E - 1):
-        c_o, s_o = oracle.quantize(bits(w.w13[e]))
-        assert np.array_equal(codes13[e * two_n:(e + 1) * two_n].cpu().numpy(), c_o)
-        assert np.array_equal(scales13[e * per13:(e + 1) * per13].cpu().numpy(), s_o)
-        sw = oracle.swap_w13(c_o[None], s_o, w.w13_bias[e:e + 1].cpu().numpy(), 1, two_n, H, 1)
-        assert np.array_equal(c_sw[e].cpu().numpy(), sw[0][0])
-        assert np.array_equal(s_sw[e * per13:(e + 1) * per13].cpu().numpy(), sw[1])
-        assert np.array_equal(bits(b13_sw[e:e + 1]), sw[2])
-        c2_o, s2_o = oracle.quantize(bits(w.w2[e]))
-        assert np.array_equal(codes2[e * N2:(e + 1) * N2].cpu().numpy(), c2_o)
-        assert np.array_equal(scales2[e * per2:(e + 1) * per2].cpu().numpy(), s2_o)
-    assert np.array_equal(bits(b2_sw), oracle.cast_bf16(w.w2_bias.cpu().numpy()))
+    outs = {}
+    for name, xw in (("w13", w.w13.view(E * two_n, H)), ("w2", w.w2.view(-1, w.w2.shape[2]))):
+        M, K = xw.shape
+        c = Guarded(M * (K // 2), shape=(M, K // 2))
+        sc = Guarded(mx.mxfp4_scale_bytes(M, K))
+        mx.mxfp4_quantize(xw, c.t, sc.t)
+        y = Guarded(M * K * 2, torch.bfloat16, (M, K))
+        mx.mxfp4_dequantize(c.t, sc.t, M, K, y.t)
+        torch.cuda.synchronize()
+        for g in (c, sc, y):
+            g.check()
+        c_o, s_o = oracle.quantize_threads(bits(xw))
+        assert_full(c.t.cpu().numpy(), c_o, f"{name} codes")
+        assert_full(sc.t.cpu().numpy(), s_o, f"{name} tiled scales")
+        assert_full(bits(y.t), oracle.dequantize_threads(c_o, s_o, M, K), f"{name} dequantize")
+        outs[name] = (c.t, sc.t, c_o, s_o)
+    c13, s13, c13_o, s13_o = outs["w13"]
+    c_sw, s_sw, b13_sw, b2_sw = run_swap(mx, c13_o.reshape(E, two_n, H // 2), s13_o,
+                                         w.w13_bias.cpu().numpy(), w.w2_bias.cpu().numpy(), E,
+                                         two_n, H, 1)
+    want = oracle.swap_w13(c13_o.reshape(E, two_n, H // 2), s13_o, w.w13_bias.cpu().numpy(), E,
+                           two_n, H, 1, w.w2_bias.cpu().numpy())
+    assert_full(c_sw, want[0], "swapped codes")
+    assert_full(s_sw, want[1], "swapped tiled scales")
+    assert_full(b13_sw, want[2], "w13 bias (swapped, BF16)")
+    assert_full(b2_sw, want[3], "w2 bias (BF16)")
 
 
 # ------------------------------------------------- fused gather + grouped
@@ -375,10 +447,11 @@ def test_grouped_gather_bad_index(mx):
     assert np.array_equal(s[:used], s_o[:used])
 
 
-def test_grouped_gather_moe_full_size(mx):
+def test_grouped_gather_moe_full_size(mx, moe, moe_oracle):
     """16384 tokens x top-8 over 384 experts, K = 7168: the fused gather
-    equals the grouped quantize of the gathered matrix, every byte."""
-    g = W.moe_grouped(seed=2, device="cuda")
+    equals the grouped quantize of the gathered matrix and the oracle, every
+    byte."""
+    g = moe
     c1, s1, sro1, st1 = mx.quantize_grouped_gather(g.x_tokens, g.row_index, g.offsets)
     c2, s2, sro2, st2 = mx.quantize_grouped(g.x, g.offsets)
     torch.cuda.synchronize()
@@ -386,6 +459,10 @@ def test_grouped_gather_moe_full_size(mx):
     assert torch.equal(sro1, sro2) and torch.equal(c1, c2)
     used = int(sro1[-1].item()) * 224
     assert torch.equal(s1[:used], s2[:used])
+    c_o, s_o, sro_o = moe_oracle
+    assert_full(sro1.cpu().numpy(), sro_o, "scale row offsets")
+    assert_full(c1.cpu().numpy(), c_o, "codes")
+    assert_full(s1[:used].cpu().numpy(), s_o, "tiled scales")
 
 
 # ------------------------------------------------- fused dispatch scatter
@@ -529,11 +606,11 @@ def test_grouped_scatter_strided_and_16b_aligned(mx, scatter_ws):
         assert_scatter_parity(gpu, orc)
 
 
-def test_grouped_scatter_moe_full_size(mx):
-    """16384 tokens x top-8 over 384 experts, K = 7168: every byte equals the
-    fused gather's (itself equal to the grouped quantize of the gathered
-    matrix); four experts' segments also against the oracle directly."""
-    g = W.moe_grouped(seed=2, device="cuda")
+def test_grouped_scatter_moe_full_size(mx, moe, moe_oracle):
+    """16384 tokens x top-8 over 384 experts, K = 7168: both scatter forms
+    equal the fused gather (itself equal to the grouped quantize of the
+    gathered matrix), and every byte equals the oracle."""
+    g = moe
     c1, s1, sro1, st1 = mx.quantize_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets)
     c2, s2, sro2, st2 = mx.quantize_grouped_gather(g.x_tokens, g.row_index, g.offsets)
     c3, s3, sro3, st3 = mx.quantize_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets,
@@ -543,14 +620,10 @@ def test_grouped_scatter_moe_full_size(mx):
     assert torch.equal(sro1, sro2) and torch.equal(c1, c2) and torch.equal(c1, c3)
     used = int(sro1[-1].item()) * 224
     assert torch.equal(s1[:used], s2[:used]) and torch.equal(s1[:used], s3[:used])
-    off_h = g.offsets.cpu().numpy().astype(np.int64)
-    sro_h = sro1.cpu().numpy().astype(np.int64)
-    for e in (0, 17, 200, 383):
-        a, b = int(off_h[e]), int(off_h[e + 1])
-        c_o, s_o = oracle.quantize(bits(g.x[a:b]))
-        assert np.array_equal(c1[a:b].cpu().numpy(), c_o), e
-        p0 = int(sro_h[e]) * 224
-        assert np.array_equal(s1[p0:p0 + s_o.size].cpu().numpy(), s_o), e
+    c_o, s_o, sro_o = moe_oracle
+    assert_full(sro1.cpu().numpy(), sro_o, "scale row offsets")
+    assert_full(c1.cpu().numpy(), c_o, "codes")
+    assert_full(s1[:used].cpu().numpy(), s_o, "tiled scales")
 
 
 # ----------------------- inputs aligned to 16 bytes but not to 32 bytes
@@ -1016,26 +1089,28 @@ def test_nvfp4_grouped_empty_segments_16b_input_and_bad_offsets(mx):
     assert (c == 0xA5).all() and (s == 0xA5).all()
 
 
-def test_nvfp4_grouped_moe_full_size_sampled(mx):
+def test_nvfp4_grouped_moe_full_size(mx, moe, moe_nvfp4_oracle):
     """131,072 x 7168 expert-sorted rows, 384 experts with their own global
-    scales: every padded offset, and 8 experts' codes and scale chunks against
-    the oracle's dense NVFP4 of the segment."""
-    g = W.moe_grouped(seed=2, device="cuda")
-    E = g.num_experts
-    gs = _expert_gscales(E, 2)
-    codes, scales, sro, st = mx.quantize_nvfp4_grouped(g.x, g.offsets, torch.from_numpy(gs).cuda())
+    scales, against the oracle in full: every code byte, every E4M3 scale
+    byte of the padded rows, every padded offset, the slack untouched."""
+    gs, c_o, s_o, sro_o = moe_nvfp4_oracle
+    total, K = moe.x.shape
+    E = moe.num_experts
+    codes = Guarded(total * (K // 2), shape=(total, K // 2))
+    scales = Guarded(mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K))
+    sro = Guarded(4 * (E + 1), torch.int32)
+    st = Guarded(4, torch.int32)
+    mx.mxfp4_quantize_nvfp4_grouped(moe.x, moe.offsets, torch.from_numpy(gs).cuda(), codes.t,
+                                    scales.t, sro.t, st.t)
     torch.cuda.synchronize()
-    assert int(st.cpu()[0]) == 0
-    off_h = g.offsets.cpu().numpy().astype(np.int64)
-    want_sro = np.concatenate([[0], np.cumsum((np.diff(off_h) + 127) // 128 * 128)])
-    assert np.array_equal(sro.cpu().numpy(), want_sro)
-    pk = 7168 // 16
-    for e in (0, 5, 77, 190, 250, 301, 350, E - 1):
-        a, b = int(off_h[e]), int(off_h[e + 1])
-        c_o, s_o = oracle.nvfp4_quantize(bits(g.x[a:b]), float(gs[e]))
-        assert np.array_equal(codes[a:b].cpu().numpy(), c_o), e
-        p0 = int(want_sro[e]) * pk
-        assert np.array_equal(scales[p0:p0 + s_o.size].cpu().numpy(), s_o), e
+    for g in (codes, scales, sro, st):
+        g.check()
+    assert int(st.t.item()) == 0
+    assert_full(sro.t.cpu().numpy(), sro_o, "scale row offsets")
+    assert_full(codes.t.cpu().numpy(), c_o, "codes")
+    s_h = scales.t.cpu().numpy()
+    assert_full(s_h[:s_o.size], s_o, "E4M3 tiled scales")
+    assert (s_h[s_o.size:] == 0xA5).all(), "slack past the last padded row was written"
 
 
 # ------------------------------------ NVFP4 experts quant, dispatch as scatter
@@ -1149,13 +1224,13 @@ def test_nvfp4_scatter_shared_global_scales(mx, f16, scatter_ws):
         assert_scatter_parity(gpu, orc)
 
 
-def test_nvfp4_scatter_moe_full_size(mx):
+def test_nvfp4_scatter_moe_full_size(mx, moe, moe_nvfp4_oracle):
     """16384 tokens x top-8 over 384 experts with their own global scales,
-    K = 7168: byte for byte the NVFP4 experts quant of the gathered batch;
-    three experts also against the oracle."""
-    g = W.moe_grouped(seed=2, device="cuda")
-    E = g.num_experts
-    gs = torch.from_numpy(_expert_gscales(E, 2)).cuda()
+    K = 7168: both scatter forms equal the NVFP4 experts quant of the
+    gathered batch byte for byte, and every byte equals the oracle."""
+    g = moe
+    gs_h, c_o, s_o, sro_o = moe_nvfp4_oracle
+    gs = torch.from_numpy(gs_h).cuda()
     c1, s1, sro1, st1 = mx.quantize_nvfp4_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets, gs)
     c2, s2, sro2, st2 = mx.quantize_nvfp4_grouped(g.x, g.offsets, gs)
     c3, s3, sro3, st3 = mx.quantize_nvfp4_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets, gs,
@@ -1166,20 +1241,17 @@ def test_nvfp4_scatter_moe_full_size(mx):
     used = int(sro1[-1].item()) * (7168 // 16)
     assert torch.equal(c1, c2) and torch.equal(s1[:used], s2[:used])
     assert torch.equal(c1, c3) and torch.equal(s1[:used], s3[:used])
-    off_h = g.offsets.cpu().numpy()
-    for e in (0, 200, E - 1):
-        a, b = int(off_h[e]), int(off_h[e + 1])
-        c_o, s_o = oracle.nvfp4_quantize(bits(g.x[a:b]), float(gs[e]))
-        assert np.array_equal(c1[a:b].cpu().numpy(), c_o), e
-        p0 = int(sro1[e].item()) * (7168 // 16)
-        assert np.array_equal(s1[p0:p0 + s_o.size].cpu().numpy(), s_o), e
+    assert_full(sro1.cpu().numpy(), sro_o, "scale row offsets")
+    assert_full(c1.cpu().numpy(), c_o, "codes")
+    assert_full(s1[:used].cpu().numpy(), s_o, "E4M3 tiled scales")
 
 
-def test_nvfp4_scatter_moe_full_size_one_global_scale(mx):
+def test_nvfp4_scatter_moe_full_size_one_global_scale(mx, moe):
     """The same batch with one global scale for every expert (each token's
     routes then share their bytes and codes): both scatter forms equal the
-    NVFP4 experts quant of the gathered batch, one expert also the oracle."""
-    g = W.moe_grouped(seed=2, device="cuda")
+    NVFP4 experts quant of the gathered batch, and that equals the oracle in
+    full."""
+    g = moe
     E = g.num_experts
     gs = torch.full((E,), 448.0 * 6.0 / 5.0, device="cuda")
     c2, s2, sro2, st2 = mx.quantize_nvfp4_grouped(g.x, g.offsets, gs)
@@ -1191,10 +1263,12 @@ def test_nvfp4_scatter_moe_full_size_one_global_scale(mx):
         assert torch.equal(sro1, sro2)
         used = int(sro1[-1].item()) * (7168 // 16)
         assert torch.equal(c1, c2) and torch.equal(s1[:used], s2[:used]), staged
-    off_h = g.offsets.cpu().numpy()
-    a, b = int(off_h[77]), int(off_h[78])
-    c_o, s_o = oracle.nvfp4_quantize(bits(g.x[a:b]), float(gs[77]))
-    assert np.array_equal(c2[a:b].cpu().numpy(), c_o)
+    rc, c_o, s_o, sro_o = oracle.nvfp4_quantize_grouped_threads(
+        bits(g.x), g.offsets.cpu().numpy(), gs.cpu().numpy())
+    assert rc == 0
+    assert_full(sro2.cpu().numpy(), sro_o, "scale row offsets")
+    assert_full(c2.cpu().numpy(), c_o, "codes")
+    assert_full(s2[:s_o.size].cpu().numpy(), s_o, "E4M3 tiled scales")
 
 
 # ----------------------------------------------- FP16 input, grouped forms
