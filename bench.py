@@ -245,16 +245,16 @@ def cpu_baseline(xb, min_seconds=2.0, max_reps=20):
             break
     gbs1 = quant_bytes(rows, K) * reps1 / el1 / 1e9
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": used, "kind": "oracle",
-            "sample": f"full {M}x{K} dense activation matrix x {reps} passes "
-                      f"({el:.2f} s wall, {el * used:.1f} core-s), oracle split into "
-                      f"128-row partitions over {used} host threads",
-            "single_core": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
-                            "sample": f"first {rows} rows x {reps1} passes ({el1:.2f} s), "
-                                      "one thread"}}
+            "sample": f"full {M}x{K} matrix x {reps} passes, 128-row bands on {used} threads",
+            "single_core_GB_per_s": round(gbs1, 4)}
 
 
 # ---------------------------------------------------------- reference arm
 def run_reference(args):
+    """The CPU oracle (single-threaded, unchanged) as the reference arm: each
+    step quantizes the first rows of the dense activation matrix, as many as
+    keep the whole run within about two minutes.  Imports the oracle and the
+    input generators only: the CUDA library is never loaded here."""
     import numpy as np
     import oracle
     import workloads as W
@@ -279,17 +279,18 @@ def run_reference(args):
     el = time.perf_counter() - t0
     nbytes = quant_bytes(rows, K_DENSE)
     gbs = nbytes * args.steps / el / 1e9
+    sample = (f"first {rows} rows of the {M_DENSE}x{K_DENSE} dense activation per step "
+              f"({nbytes} algorithmic bytes), single-threaded CPU oracle")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"dense activation quantize {M_DENSE}x{K_DENSE} BF16 "
-                               "(N(0,1) x 2^U(-8,8) per row, seed 1)",
-                   "parallelism": "single host thread"},
+        "config": {"workload": f"dense activation quantize, first {rows} rows of "
+                               f"{M_DENSE}x{K_DENSE} BF16 (N(0,1) x 2^U(-8,8) per row, seed 1)",
+                   "bytes_per_step": nbytes, "parallelism": "single host thread"},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"first {rows} rows of the {M_DENSE}x{K_DENSE} matrix per step "
-                                   f"({nbytes} algorithmic bytes), single-threaded CPU oracle"},
+                         "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -298,19 +299,42 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- our arm
-def time_launches(fn, iters, stream, warmup=3):
+class Flush:
+    """A buffer of 2x the L2, written (by torch) before each timed batch: the
+    batch starts with a cold L2, and while the device writes it the host has
+    already queued the batch's launches, so a batch's device time holds no
+    host launch latency."""
+
+    def __init__(self, l2_bytes, device=None):
+        import torch
+        self.buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=device or "cuda")
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+def time_batches(fn, stream, flush, per_batch, batches, warmup=3):
+    """fn(i) launched in `batches` batches of `per_batch` calls, each batch
+    timed by CUDA events on `stream` after an L2 flush.  Returns (mean,
+    median) milliseconds per call: the mean over all calls, the median over
+    batches of each batch's mean."""
     import torch
     for i in range(warmup):
         fn(i)
     torch.cuda.synchronize()
-    s = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for i in range(iters):
-        fn(i)
-    e.record(stream)
-    e.synchronize()
-    return s.elapsed_time(e) / iters
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(batches)]
+    i = 0
+    for s_, e_ in evs:
+        flush()
+        s_.record(stream)
+        for _ in range(per_batch):
+            fn(i)
+            i += 1
+        e_.record(stream)
+    torch.cuda.synchronize()
+    per = [s_.elapsed_time(e_) / per_batch for s_, e_ in evs]
+    return sum(per) / len(per), statistics.median(per)
 
 
 def tiled_scale_index(M, K, device="cpu"):
@@ -326,9 +350,9 @@ def tiled_scale_index(M, K, device="cpu"):
 def reconstruction_report(mx, x, codes, scales):
     """Reconstruction error of the headline matrix, from the GPU's own outputs
     (outside every timed region): relative L2 of dequantize(quantize(x))
-    against x in float64, and the elements the E2M1 range clips, i.e. with
-    |x| > 6 * 2^(s-127) for their block's scale byte s (read back from the
-    128x4-tiled layout)."""
+    against x in float64, and the fraction of elements the E2M1 range clips,
+    i.e. with |x| > 6 * 2^(s-127) for their block's scale byte s (read back
+    from the 128x4-tiled layout)."""
     import torch
     M, K = x.shape
     y = mx.dequantize(codes, scales, M, K)
@@ -338,16 +362,14 @@ def reconstruction_report(mx, x, codes, scales):
     blk = torch.exp2(s - 127.0).repeat_interleave(32, dim=1)
     live = (s > 0).repeat_interleave(32, dim=1)
     sat = int(((xd.abs() > 6.0 * blk) & live).sum())
-    return {"rel_l2": round(rel, 6), "saturated_elements": sat,
-            "saturated_fraction": round(sat / (M * K), 6),
-            "matrix": f"{M}x{K} dense activation (the headline input)",
-            "how": "dequantize(quantize(x)) vs x in float64; saturated = |x| > 6 * 2^(s-127)"}
+    return {"rel_l2": round(rel, 6), "clipped_frac": round(sat / (M * K), 6)}
 
 
-def time_graph(fn, iters):
+def time_graph(fn, iters, replays=5):
     """Per-call device time of `iters` calls fn(i, stream) captured once in a
-    CUDA graph on a side stream and replayed there: for kernels shorter than
-    a Python call, so that the host's launch rate does not set the time."""
+    CUDA graph on a side stream and replayed `replays` times: for kernels
+    shorter than a Python call, so that the host's launch rate does not set
+    the time.  Returns (mean, median over replays) milliseconds per call."""
     import torch
     side = torch.cuda.Stream()
     for i in range(3):
@@ -357,29 +379,41 @@ def time_graph(fn, iters):
     with torch.cuda.graph(g, stream=side):
         for i in range(iters):
             fn(i, side)
+    per = []
     with torch.cuda.stream(side):
         g.replay()
         torch.cuda.synchronize()
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        s.record(side)
-        g.replay()
-        e.record(side)
-    e.synchronize()
-    return s.elapsed_time(e) / iters
+        for _ in range(replays):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(side)
+            g.replay()
+            e.record(side)
+            e.synchronize()
+            per.append(s.elapsed_time(e) / iters)
+    return sum(per) / len(per), statistics.median(per)
 
 
-def measure_rows(mx, W, stream, peak, l2_bytes):
-    """Each remaining hot-path row on its own workload (kernel time, inputs
-    resident in HBM, operands rotated or larger than L2)."""
+ROW_FIELDS = ["GB/s", "frac of measured peak", "mean us", "median us"]
+
+
+def measure_rows(mx, W, stream, peak, l2_bytes, flush):
+    """Each remaining hot-path row on its own workload (device time, inputs
+    resident in HBM, operands rotated or larger than L2, an L2 flush before
+    each timed batch).  Every row is [GB/s, fraction of the peak, mean us,
+    median us] over the row's algorithmic bytes; `extra` holds the unfused
+    baselines the fused dispatch calls are compared with."""
     import torch
-    out = {}
+    rows, extra = {}, {}
 
-    def entry(nbytes, ms, launches, note):
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        return {"GB_per_s": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
-                "us_per_call": round(ms * 1e3, 2), "bytes_per_call": int(nbytes),
-                "launches_per_call": launches, "note": note}
+    def row(name, nbytes, t):
+        mean, med = t
+        gbs = nbytes / (mean * 1e-3) / 1e9
+        rows[name] = [round(gbs, 1), round(gbs / peak, 4), round(mean * 1e3, 2),
+                      round(med * 1e3, 2)]
+
+    def tb(fn, per_batch, batches=5):
+        return time_batches(fn, stream, flush, per_batch, batches)
 
     # dequantize 4096 x 7168 (rotate buffers beyond 2x L2)
     M, K = M_DENSE, K_DENSE
@@ -390,179 +424,115 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     cs = [codes.clone() for _ in range(R)]
     ss = [scales.clone() for _ in range(R)]
     ys = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(R)]
-    ms = time_launches(lambda i: mx.mxfp4_dequantize(cs[i % R], ss[i % R], M, K, ys[i % R], stream),
-                       200, stream)
-    out["dequantize_4096x7168"] = entry(nb, ms, 1, f"{R} rotating sets")
+    row("dequant_4096x7168", nb,
+        tb(lambda i: mx.mxfp4_dequantize(cs[i % R], ss[i % R], M, K, ys[i % R], stream), 40))
     del cs, ss, ys, x, codes, scales
 
     # the same activation in FP16 (same method, binary16 input)
     x16s = [W.dense_activation(1, M, K, device="cuda").to(torch.float16) for _ in range(R)]
     cs16 = [torch.empty((M, K // 2), dtype=torch.uint8, device="cuda") for _ in range(R)]
     ss16 = [torch.empty(M * 224, dtype=torch.uint8, device="cuda") for _ in range(R)]
-    ms = time_launches(lambda i: mx.mxfp4_quantize_f16(x16s[i % R], cs16[i % R], ss16[i % R], stream),
-                       200, stream)
-    out["quantize_f16_4096x7168"] = entry(quant_bytes(M, K), ms, 1, f"{R} rotating sets")
+    row("f16_quant_4096x7168", quant_bytes(M, K),
+        tb(lambda i: mx.mxfp4_quantize_f16(x16s[i % R], cs16[i % R], ss16[i % R], stream), 40))
     del x16s, cs16, ss16
 
     # NVFP4 (16-element blocks, E4M3 scales, global scale 448*6/amax): quantize
-    # and dequantize of the same 4096 x 7168 activation
+    # and dequantize of the same 4096 x 7168 activation, and the FP16 quantize
     xs_nv = [W.dense_activation(1, M, K, device="cuda") for _ in range(R)]
     g_nv = torch.tensor([448.0 * 6.0 / float(xs_nv[0].float().abs().max())], device="cuda")
     sb_nv = mx.mxfp4_nvfp4_scale_bytes(M, K)
     cs_nv = [torch.empty((M, K // 2), dtype=torch.uint8, device="cuda") for _ in range(R)]
     ss_nv = [torch.empty(sb_nv, dtype=torch.uint8, device="cuda") for _ in range(R)]
-    ms = time_launches(lambda i: mx.mxfp4_quantize_nvfp4(xs_nv[i % R], g_nv, cs_nv[i % R],
-                                                         ss_nv[i % R], stream), 200, stream)
     nb_nv = 2 * M * K + M * K // 2 + sb_nv
-    out["nvfp4_quantize_4096x7168"] = entry(nb_nv, ms, 1, f"{R} rotating sets")
-    ms = time_launches(lambda i: mx.mxfp4_dequantize_nvfp4(cs_nv[i % R], ss_nv[i % R], g_nv, M, K,
-                                                           xs_nv[i % R], stream), 200, stream)
-    out["nvfp4_dequantize_4096x7168"] = entry(nb_nv, ms, 1, f"{R} rotating sets")
-    # the NVFP4 quantize of the same activation in FP16
+    row("nvfp4_quant_4096x7168", nb_nv,
+        tb(lambda i: mx.mxfp4_quantize_nvfp4(xs_nv[i % R], g_nv, cs_nv[i % R], ss_nv[i % R],
+                                             stream), 40))
+    row("nvfp4_dequant_4096x7168", nb_nv,
+        tb(lambda i: mx.mxfp4_dequantize_nvfp4(cs_nv[i % R], ss_nv[i % R], g_nv, M, K,
+                                               xs_nv[i % R], stream), 40))
     for j in range(R):
         xs_nv[j] = xs_nv[j].to(torch.float16)
-    ms = time_launches(lambda i: mx.mxfp4_quantize_nvfp4_f16(xs_nv[i % R], g_nv, cs_nv[i % R],
-                                                             ss_nv[i % R], stream), 200, stream)
-    out["nvfp4_quantize_f16_4096x7168"] = entry(nb_nv, ms, 1, f"{R} rotating sets")
+    row("nvfp4_f16_quant_4096x7168", nb_nv,
+        tb(lambda i: mx.mxfp4_quantize_nvfp4_f16(xs_nv[i % R], g_nv, cs_nv[i % R], ss_nv[i % R],
+                                                 stream), 40))
     del xs_nv, cs_nv, ss_nv
 
     # grouped MoE activations: 16384 tokens x top-8 over 384 experts, K = 7168
     g = W.moe_grouped(seed=2, device="cuda")
     total, K = g.x.shape
     E = g.num_experts
+    T = g.x_tokens.shape[0]
     codes = torch.empty((total, K // 2), dtype=torch.uint8, device="cuda")
     scales = torch.empty(mx.mxfp4_grouped_scale_bytes_bound(total, E, K), dtype=torch.uint8,
                          device="cuda")
     sro = torch.empty(E + 1, dtype=torch.int32, device="cuda")
     st = torch.empty(1, dtype=torch.int32, device="cuda")
-    ms = time_launches(lambda i: mx.mxfp4_quantize_grouped(g.x, g.offsets, codes, scales, sro, st,
-                                                           stream), 30, stream)
+    t_grouped = tb(lambda i: mx.mxfp4_quantize_grouped(g.x, g.offsets, codes, scales, sro, st,
+                                                       stream), 6)
     padded = int(sro[-1].item())
-    nb = 2 * total * K + total * K // 2 + padded * (K // 32) + 4 * (E + 1)
-    out["grouped_moe_131072x7168_E384"] = entry(
-        nb, ms, 2, f"{padded} padded scale rows; offsets kernel + quantize kernel")
-
-    # the same batch through the NVFP4 experts quant (a global scale per expert)
+    row("grouped_moe_131072x7168_E384",
+        2 * total * K + total * K // 2 + padded * (K // 32) + 4 * (E + 1), t_grouped)
     g_nv = torch.full((E,), 448.0 * 6.0 / 5.0, device="cuda")
     sc_nv = torch.empty(mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K), dtype=torch.uint8,
                         device="cuda")
-    ms = time_launches(lambda i: mx.mxfp4_quantize_nvfp4_grouped(g.x, g.offsets, g_nv, codes,
-                                                                 sc_nv, sro, st, stream), 30,
-                       stream)
-    nb_nv = 2 * total * K + total * K // 2 + padded * (K // 16) + 4 * (E + 1) + 4 * E
-    out["nvfp4_grouped_moe_131072x7168_E384"] = entry(
-        nb_nv, ms, 2, "per-expert global scales; offsets kernel + quantize kernel")
-    del sc_nv
+    nb_nvg = 2 * total * K + total * K // 2 + padded * (K // 16) + 4 * (E + 1) + 4 * E
+    row("nvfp4_grouped_moe_131072x7168_E384", nb_nvg,
+        tb(lambda i: mx.mxfp4_quantize_nvfp4_grouped(g.x, g.offsets, g_nv, codes, sc_nv, sro, st,
+                                                     stream), 6))
 
-    # the same MoE batch with the dispatch gather fused in: token rows
-    # [16384, 7168] + int32 route->token indices, against the unfused pair
-    # (torch index_select materialising the 1.9 GB permuted matrix, then the
-    # grouped quantize)
-    T = g.x_tokens.shape[0]
+    # the same MoE batch with the dispatch fused in: token rows [16384, 7168]
+    # read once + int32 route maps, against the unfused pair (torch
+    # index_select materialising the 1.9 GB permuted matrix, then the grouped
+    # quantize)
     xg = torch.empty_like(g.x)
-    ms_fused = time_launches(
-        lambda i: mx.mxfp4_quantize_grouped_gather(g.x_tokens, g.row_index, g.offsets, codes,
-                                                   scales, sro, st, stream), 30, stream)
-    ms_unfused = time_launches(
-        lambda i: (torch.index_select(g.x_tokens, 0, g.row_index, out=xg),
-                   mx.mxfp4_quantize_grouped(xg, g.offsets, codes, scales, sro, st, stream)),
-        30, stream)
     nb = 2 * T * K + 4 * total + total * K // 2 + padded * (K // 32) + 4 * (E + 1)
-    e_ = entry(nb, ms_fused, 6, "bytes = token rows read once + indices + codes + scales; "
-               "no workspace: the call borrows the codes of its last rows for the inverse map "
-               "and staged scale words, runs the gather_ws kernels (each token row read once) "
-               "and writes the borrowed rows' codes last, from their own token rows")
-    e_["unfused_us_per_call"] = round(ms_unfused * 1e3, 2)
-    e_["speedup_vs_unfused"] = round(ms_unfused / ms_fused, 3)
-    out["grouped_gather_moe_16384tok_top8_E384"] = e_
-    # the same gather call through the scatter path (inverse map built in a workspace)
+    t_unf = tb(lambda i: (torch.index_select(g.x_tokens, 0, g.row_index, out=xg),
+                          mx.mxfp4_quantize_grouped(xg, g.offsets, codes, scales, sro, st,
+                                                    stream)), 6)
+    extra["unfused_gather_then_grouped_us"] = round(t_unf[0] * 1e3, 2)
+    row("gather_moe_16384tok_top8", nb,
+        tb(lambda i: mx.mxfp4_quantize_grouped_gather(g.x_tokens, g.row_index, g.offsets, codes,
+                                                      scales, sro, st, stream), 6))
     ws = torch.empty(mx.mxfp4_gather_workspace_bytes(T, total, E, K), dtype=torch.uint8,
                      device="cuda")
-    ms_ws = time_launches(
-        lambda i: mx.mxfp4_quantize_grouped_gather_ws(g.x_tokens, g.row_index, g.offsets, ws,
-                                                      codes, scales, sro, st, stream), 30, stream)
-    e_ = entry(nb, ms_ws, 4, "same call and bytes as the gather row; offsets kernel, workspace "
-               "memset, bucket map kernel, scatter kernel (each token row read once, its scale "
-               "words staged once), tile kernel (tiled scales in whole chunks)")
-    e_["speedup_vs_unfused"] = round(ms_unfused / ms_ws, 3)
-    e_["speedup_vs_gather"] = round(ms_fused / ms_ws, 3)
-    out["grouped_gather_ws_moe_16384tok_top8_E384"] = e_
+    row("gather_ws_moe_16384tok_top8", nb,
+        tb(lambda i: mx.mxfp4_quantize_grouped_gather_ws(g.x_tokens, g.row_index, g.offsets, ws,
+                                                         codes, scales, sro, st, stream), 6))
     del ws
-    # the same dispatch given token -> rows (the router's sort output): each
-    # token row read and quantized once, its codes written to its 8 rows
-    ms_sc = time_launches(
-        lambda i: mx.mxfp4_quantize_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets, total,
-                                                    codes, scales, sro, st, stream), 30, stream)
-    e_ = entry(nb, ms_sc, 2, "bytes = token rows read once + route->row map + codes + scales; "
-               "pad CTAs zero the segments' pad scale rows in the same launch")
-    e_["speedup_vs_unfused"] = round(ms_unfused / ms_sc, 3)
-    e_["speedup_vs_fused_gather"] = round(ms_fused / ms_sc, 3)
-    out["grouped_scatter_moe_16384tok_top8_E384"] = e_
-    # the same scatter call with a workspace: each token's scale words staged
-    # once, the tiled scales written whole by a second kernel
+    row("scatter_moe_16384tok_top8", nb,
+        tb(lambda i: mx.mxfp4_quantize_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets, total,
+                                                       codes, scales, sro, st, stream), 6))
     ws = torch.empty(mx.mxfp4_scatter_workspace_bytes(T, total, E, K), dtype=torch.uint8,
                      device="cuda")
-    ms_sw = time_launches(
-        lambda i: mx.mxfp4_quantize_grouped_scatter_ws(g.x_tokens, g.dest_rows, g.offsets, total,
-                                                       ws, codes, scales, sro, st, stream),
-        30, stream)
-    e_ = entry(nb, ms_sw, 4, "same call and bytes as the scatter row; offsets kernel, workspace "
-               "memset, route map kernel, scatter kernel (scale words staged once per token), "
-               "tile kernel")
-    e_["speedup_vs_unfused"] = round(ms_unfused / ms_sw, 3)
-    e_["speedup_vs_direct_scatter"] = round(ms_sc / ms_sw, 3)
-    out["grouped_scatter_ws_moe_16384tok_top8_E384"] = e_
+    row("scatter_ws_moe_16384tok_top8", nb,
+        tb(lambda i: mx.mxfp4_quantize_grouped_scatter_ws(g.x_tokens, g.dest_rows, g.offsets,
+                                                          total, ws, codes, scales, sro, st,
+                                                          stream), 6))
     del ws
-    # the NVFP4 experts quant with the same dispatch fused in (a global scale
-    # per expert), against gathering the 1.9 GB batch first
-    g_nv = torch.full((E,), 448.0 * 6.0 / 5.0, device="cuda")
-    sc_nv = torch.empty(mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K), dtype=torch.uint8,
-                        device="cuda")
-    ms_nvs = time_launches(
-        lambda i: mx.mxfp4_quantize_nvfp4_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets,
-                                                          total, g_nv, codes, sc_nv, sro, st,
-                                                          stream), 30, stream)
-    ms_nvu = time_launches(
-        lambda i: (torch.index_select(g.x_tokens, 0, g.row_index, out=xg),
-                   mx.mxfp4_quantize_nvfp4_grouped(xg, g.offsets, g_nv, codes, sc_nv, sro, st,
-                                                   stream)), 30, stream)
-    nb_nvs = (2 * T * K + 4 * total + total * K // 2 + padded * (K // 16) + 4 * (E + 1) + 4 * E)
-    e_ = entry(nb_nvs, ms_nvs, 2, "bytes = token rows read once + route->row map + codes + "
-               "E4M3 scales (16-element columns) + offsets + global scales; each route's "
-               "scale words stored into the tiled layout; one global scale shared by every "
-               "expert, so a token's routes share their bytes and codes")
-    e_["unfused_us_per_call"] = round(ms_nvu * 1e3, 2)
-    e_["speedup_vs_unfused"] = round(ms_nvu / ms_nvs, 3)
-    out["nvfp4_grouped_scatter_moe_16384tok_top8_E384"] = e_
-    # the same call with a workspace: each route's scale bytes staged by padded
-    # row, the tiled scales written whole by a second kernel
+    # the NVFP4 experts quant with the same dispatch fused in; one global
+    # scale shared by every expert, then a scale of its own per expert
+    nb_nvs = 2 * T * K + 4 * total + total * K // 2 + padded * (K // 16) + 4 * (E + 1) + 4 * E
+    t_nvu = tb(lambda i: (torch.index_select(g.x_tokens, 0, g.row_index, out=xg),
+                          mx.mxfp4_quantize_nvfp4_grouped(xg, g.offsets, g_nv, codes, sc_nv, sro,
+                                                          st, stream)), 6)
+    extra["unfused_gather_then_nvfp4_grouped_us"] = round(t_nvu[0] * 1e3, 2)
+    row("nvfp4_scatter_shared_g_moe", nb_nvs,
+        tb(lambda i: mx.mxfp4_quantize_nvfp4_grouped_scatter(g.x_tokens, g.dest_rows, g.offsets,
+                                                             total, g_nv, codes, sc_nv, sro, st,
+                                                             stream), 6))
     ws = torch.empty(mx.mxfp4_nvfp4_scatter_workspace_bytes(total, E, K), dtype=torch.uint8,
                      device="cuda")
-    ms_nvw = time_launches(
-        lambda i: mx.mxfp4_quantize_nvfp4_grouped_scatter_ws(g.x_tokens, g.dest_rows, g.offsets,
-                                                             total, g_nv, ws, codes, sc_nv, sro,
-                                                             st, stream), 30, stream)
-    e_ = entry(nb_nvs, ms_nvw, 3, "same call and bytes as the row above; offsets kernel, "
-               "workspace memset, scatter kernel (its first CTAs mark the pad rows, each "
-               "token warp maps its routes to their staged rows; a token whose experts "
-               "share one scale stages its bytes once), tile kernel")
-    e_["speedup_vs_unfused"] = round(ms_nvu / ms_nvw, 3)
-    e_["speedup_vs_direct"] = round(ms_nvs / ms_nvw, 3)
-    out["nvfp4_grouped_scatter_ws_moe_16384tok_top8_E384"] = e_
-    # the same with a global scale of its own per expert: every route of a
-    # token computes its own E4M3 bytes, inverse scales and codes
+    row("nvfp4_scatter_ws_shared_g_moe", nb_nvs,
+        tb(lambda i: mx.mxfp4_quantize_nvfp4_grouped_scatter_ws(g.x_tokens, g.dest_rows,
+                                                                g.offsets, total, g_nv, ws, codes,
+                                                                sc_nv, sro, st, stream), 6))
     g_own = 448.0 * 6.0 / torch.exp(torch.rand(E, generator=torch.Generator().manual_seed(2)) * 3.0)
     g_own = g_own.to("cuda")
-    ms_nvo = time_launches(
-        lambda i: mx.mxfp4_quantize_nvfp4_grouped_scatter_ws(g.x_tokens, g.dest_rows, g.offsets,
-                                                             total, g_own, ws, codes, sc_nv, sro,
-                                                             st, stream), 30, stream)
-    e_ = entry(nb_nvs, ms_nvo, 3, "the row above with a global scale of its own per expert "
-               "(448 * 6 / e^U(0,3)): each route quantizes its blocks itself")
-    e_["speedup_vs_unfused"] = round(ms_nvu / ms_nvo, 3)
-    out["nvfp4_grouped_scatter_ws_own_gscales_moe_16384tok_top8_E384"] = e_
-    del sc_nv, ws
-    del g, codes, scales, xg
+    row("nvfp4_scatter_ws_own_g_moe", nb_nvs,
+        tb(lambda i: mx.mxfp4_quantize_nvfp4_grouped_scatter_ws(g.x_tokens, g.dest_rows,
+                                                                g.offsets, total, g_own, ws,
+                                                                codes, sc_nv, sro, st, stream), 6))
+    del sc_nv, ws, g, codes, scales, xg
 
     # expert weights: w13 [128, 1536, 2048], w2 [128, 2048, 768], then the swap
     w = W.expert_weights(3, device="cuda")
@@ -573,21 +543,23 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     s13 = torch.empty(mx.mxfp4_scale_bytes(E * two_n, H), dtype=torch.uint8, device="cuda")
     c2 = torch.empty((x2.shape[0], x2.shape[1] // 2), dtype=torch.uint8, device="cuda")
     s2 = torch.empty(mx.mxfp4_scale_bytes(*x2.shape), dtype=torch.uint8, device="cuda")
-    ms = time_launches(lambda i: mx.mxfp4_quantize(x13, c13, s13, stream), 30, stream)
-    out["expert_w13_quantize_196608x2048"] = entry(quant_bytes(*x13.shape), ms, 1, "")
-    ms = time_launches(lambda i: mx.mxfp4_quantize(x2, c2, s2, stream), 30, stream)
-    out["expert_w2_quantize_262144x768"] = entry(quant_bytes(*x2.shape), ms, 1, "")
+    row("w13_quant_196608x2048", quant_bytes(*x13.shape),
+        tb(lambda i: mx.mxfp4_quantize(x13, c13, s13, stream), 6))
+    row("w2_quant_262144x768", quant_bytes(*x2.shape),
+        tb(lambda i: mx.mxfp4_quantize(x2, c2, s2, stream), 6))
     c_o = torch.empty_like(c13)
     s_o = torch.empty_like(s13)
     b13 = torch.empty(w.w13_bias.shape, dtype=torch.bfloat16, device="cuda")
     b2 = torch.empty(w.w2_bias.shape, dtype=torch.bfloat16, device="cuda")
-    ms = time_launches(lambda i: mx.mxfp4_swap_w13(c13, s13, w.w13_bias, E, two_n, H, 1, c_o, s_o,
-                                                   b13, w.w2_bias, b2, stream), 30, stream)
     nb = 2 * (c13.numel() + s13.numel()) + w.w13_bias.numel() * 6 + w.w2_bias.numel() * 6
-    out["swap_w13_E128_2N1536_K2048"] = entry(nb, ms, 1, "codes + tiled scales + both biases")
+    row("swap_w13_E128_2N1536_K2048", nb,
+        tb(lambda i: mx.mxfp4_swap_w13(c13, s13, w.w13_bias, E, two_n, H, 1, c_o, s_o, b13,
+                                       w.w2_bias, b2, stream), 6))
     del w, c13, s13, c2, s2, c_o, s_o
 
-    # edge-case matrix 1000 x 2880 (latency-scale; rotate 2x L2 worth of sets)
+    # edge-case matrix 1000 x 2880 (latency-scale; rotate 2x L2 worth of sets;
+    # 500 launches replayed from one CUDA graph, the kernel being shorter than
+    # a Python call)
     xe = W.edge_cases(4).cuda()
     nb = quant_bytes(1000, 2880)
     R = max(2, -(-2 * l2_bytes // nb) + 1)
@@ -595,25 +567,48 @@ def measure_rows(mx, W, stream, peak, l2_bytes):
     cs = [torch.empty((1000, 1440), dtype=torch.uint8, device="cuda") for _ in range(R)]
     ss = [torch.empty(mx.mxfp4_scale_bytes(1000, 2880), dtype=torch.uint8, device="cuda")
           for _ in range(R)]
-    ms = time_graph(lambda i, st: mx.mxfp4_quantize(xs[i % R], cs[i % R], ss[i % R], st), 500)
-    out["edge_quantize_1000x2880"] = entry(
-        nb, ms, 1, f"{R} rotating sets; 500 launches replayed from one CUDA graph "
-        "(the kernel is shorter than a Python call); latency-bound size")
-    return out
+    row("edge_quant_1000x2880", nb,
+        time_graph(lambda i, st: mx.mxfp4_quantize(xs[i % R], cs[i % R], ss[i % R], st), 500))
+    return rows, extra
 
 
 DISPATCH_CALLS = ("gather", "gather_ws", "scatter", "scatter_ws", "nvfp4_scatter",
-                  "nvfp4_scatter_ws")
+                  "nvfp4_scatter_ws", "nvfp4_scatter_ws_own_g")
+SINGLE_CALLS = DISPATCH_CALLS + ("dense", "w13")
 
 
 def run_one_call(args):
-    """--call NAME: one dispatch call on the MoE batch (16384 tokens x top-8
-    over 384 experts, K = 7168), repeated --reps times after one warm-up, and
-    one JSON line with its mean CUDA-event time.  For profiling a single call
-    (ncu -k on this command sees only its kernels)."""
+    """--call NAME: one call repeated --reps times after one warm-up, and one
+    JSON line with its mean CUDA-event time.  For profiling a single call
+    (ncu -k on this command sees only its kernels).  NAME is a dispatch call
+    on the MoE batch (16384 tokens x top-8 over 384 experts, K = 7168;
+    nvfp4_scatter_ws_own_g with a global scale of its own per expert), the
+    dense quantize of the 4096 x 7168 activation, or the dense quantize of the
+    w13 expert weights [128 x 1536, 2048]."""
     import torch
     import mxfp4_block_quantization_gb300 as mx
     import workloads as W
+    if args.call in ("dense", "w13"):
+        if args.call == "dense":
+            x = W.dense_activation(1, M_DENSE, K_DENSE, device="cuda")
+        else:
+            w13 = W.expert_weights(3, device="cuda").w13
+            x = w13.view(-1, w13.shape[2])
+        codes = torch.empty((x.shape[0], x.shape[1] // 2), dtype=torch.uint8, device="cuda")
+        scales = torch.empty(mx.mxfp4_scale_bytes(*x.shape), dtype=torch.uint8, device="cuda")
+        fn = lambda: mx.mxfp4_quantize(x, codes, scales)  # noqa: E731
+        fn()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.reps):
+            fn()
+        t1.record()
+        torch.cuda.synchronize()
+        us = t0.elapsed_time(t1) * 1e3 / args.reps
+        print(json.dumps({"call": args.call, "reps": args.reps, "us_per_call": round(us, 2),
+                          "bytes_per_call": quant_bytes(*x.shape)}))
+        return 0
     g = W.moe_grouped(seed=2, device="cuda")
     T, K = g.x_tokens.shape
     total = g.row_index.numel()
@@ -625,8 +620,13 @@ def run_one_call(args):
     st = torch.empty(1, dtype=torch.int32, device="cuda")
     ws_bytes = {"gather_ws": lambda: mx.mxfp4_gather_workspace_bytes(T, total, E, K),
                 "scatter_ws": lambda: mx.mxfp4_scatter_workspace_bytes(T, total, E, K),
-                "nvfp4_scatter_ws": lambda: mx.mxfp4_nvfp4_scatter_workspace_bytes(total, E, K)}
+                "nvfp4_scatter_ws": lambda: mx.mxfp4_nvfp4_scatter_workspace_bytes(total, E, K),
+                "nvfp4_scatter_ws_own_g":
+                    lambda: mx.mxfp4_nvfp4_scatter_workspace_bytes(total, E, K)}
     gs = torch.full((E,), 448.0 * 6.0 / 5.0, device="cuda")
+    if args.call == "nvfp4_scatter_ws_own_g":
+        gs = (448.0 * 6.0 / torch.exp(torch.rand(E, generator=torch.Generator().manual_seed(2))
+                                      * 3.0)).to("cuda")
     if args.call.startswith("nvfp4"):
         scales = torch.empty(mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K),
                              dtype=torch.uint8, device="cuda")
@@ -645,7 +645,9 @@ def run_one_call(args):
             g.x_tokens, g.dest_rows, g.offsets, total, gs, codes, scales, sro, st),
         "nvfp4_scatter_ws": lambda: mx.mxfp4_quantize_nvfp4_grouped_scatter_ws(
             g.x_tokens, g.dest_rows, g.offsets, total, gs, ws, codes, scales, sro, st),
-    }[args.call]
+    }
+    fn["nvfp4_scatter_ws_own_g"] = fn["nvfp4_scatter_ws"]
+    fn = fn[args.call]
     fn()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -712,13 +714,18 @@ def run_ours(args):
             i += 1
         torch.cuda.synchronize()
 
-    # ---- timed region
+    # ---- timed region: an L2 flush (torch writes 2x L2) is queued first, so
+    # that the first step finds a cold L2 like every later one and the host
+    # has the steps queued by the time the flush ends; the events bracket the
+    # K steps alone
+    flush = Flush(l2_bytes, dev)
     barrier()
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
     torch.cuda.nvtx.range_push(f"timed: {args.steps} x mxfp4_quantize {M_DENSE}x{K_DENSE}")
+    flush()
     ev0.record(stream)
     for i in range(args.steps):
         step(i)
@@ -734,6 +741,9 @@ def run_ours(args):
     ms_per_step = max_ms / args.steps
     value = total_bytes / (max_ms * 1e-3) / 1e9
     kernel_gbs = nbytes / (local_ms / args.steps * 1e-3) / 1e9
+    # the same kernel over 25 more batches of K steps (outside the timed
+    # region): the median over batches of the per-step time
+    _, med_ms = time_batches(step, stream, flush, args.steps, 25)
 
     # ---- e2e through the public API with pinned host buffers: per step the
     # matrix goes host -> device in 4 row chunks on a copy stream, each chunk
@@ -826,9 +836,9 @@ def run_ours(args):
 
     quality = reconstruction_report(mx, x0, codes[0], scales[0]) if rank == 0 else None
 
-    rows = None
+    rows, extra = None, None
     if not args.no_rows:
-        rows = measure_rows(mx, W, stream, peak, l2_bytes)
+        rows, extra = measure_rows(mx, W, stream, peak, l2_bytes, flush)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -836,44 +846,43 @@ def run_ours(args):
 
     traffic = profiled_traffic()
     if rank == 0:
+        clk = clocks.summary(t_wall0, t_wall1)
+        if clk is not None:
+            clk.pop("window", None)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {
-                "workload": f"dense activation quantize {M_DENSE}x{K_DENSE} BF16 "
-                            "(N(0,1) x 2^U(-8,8) per row, seed 1) -> E2M1 codes + 128x4-tiled "
-                            "E8M0 scales",
-                "M": M_DENSE, "K": K_DENSE, "bytes_per_step": nbytes,
-                "l2": f"{R} rotating input/output sets ({R * nbytes / 1e6:.0f} MB > 2x L2 "
-                      f"{l2_bytes / 1e6:.0f} MB)",
+                "workload": f"dense activation quantize {M_DENSE}x{K_DENSE} BF16, "
+                            "N(0,1) x 2^U(-8,8) per row, seed 1",
+                "bytes_per_step": nbytes,
+                "l2": f"{R} rotating input/output sets ({R * nbytes / 1e6:.0f} MB > 2x L2) "
+                      "and an L2 flush before the timed steps",
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             },
             "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(kernel_gbs / peak, 4),
-                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
-                         if peak_src == "measured" else "fallback 6.8 TB/s",
-                         "traffic": traffic,
-                         "kernel": "quantize_tiles_kernel (dense BF16, 32-byte loads)",
-                         "algorithmic_bytes_per_launch": nbytes},
+                         "peak_src": "measured burst copy" if peak_src == "measured"
+                         else "fallback 6.8 TB/s",
+                         "traffic": traffic, "traffic_src": "ncu DRAM read+write per launch",
+                         "kernel": "quantize_tiles_kernel",
+                         "median_us": round(med_ms * 1e3, 3)},
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": x_host.numel() * 2,
                     "d2h_bytes_per_step": c_host.numel() + s_host.numel(),
-                    "how": f"pinned host buffers; {n_chunks} row chunks, host->device copy, "
-                           "mxfp4_quantize and device->host copy pipelined on 3 streams, also across "
-                           "steps (per-chunk buffer-reuse events)",
                     "host_link_GB_per_s": round(link_gbs, 2),
-                    "frac_of_host_link": round(e2e_val / link_gbs, 4),
-                    "host_link_how": "the same bytes per step as plain pinned copies on the "
-                                     "two copy streams, no kernel (this rank's GPU)"},
+                    "frac_of_host_link": round(e2e_val / link_gbs, 4)},
             "gpu_launches": args.steps,
-            "clocks": clocks.summary(t_wall0, t_wall1),
+            "clocks": clk,
             "cpu_baseline": cpu,
             "quality": quality,
+            "extra": extra,
+            "rows_fields": ROW_FIELDS,
             "rows": rows,
         }
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -888,8 +897,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--call", choices=DISPATCH_CALLS,
-                    help="only time this dispatch call on the MoE batch (for profiling)")
+    ap.add_argument("--call", choices=SINGLE_CALLS,
+                    help="only time this one call (for profiling)")
     ap.add_argument("--reps", type=int, default=5, help="repetitions of --call")
     ap.add_argument("--settle", type=float, default=1.0,
                     help="seconds of untimed launches after the warm-up steps (clock settling)")
