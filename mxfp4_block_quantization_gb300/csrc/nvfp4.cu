@@ -61,11 +61,19 @@ enum : int { kDbgXY = 0, kDbgCodes, kDbgScales, kDbgG };
 template <bool kVec32, bool kF16>
 __global__ void __launch_bounds__(kThreads, 5) nvfp4_quantize_kernel(const Nvfp4Params p) {
   __shared__ __align__(16) uint8_t chunk[2][kChunkBytes];
-  pdl_wait();
-  pdl_release();
   const int ct = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.nCT));
   const int64_t mt = blockIdx.x / static_cast<uint32_t>(p.nCT);
   const int64_t row0 = mt * kTileRows;
+  {
+    // before the grid-dependency wait: thread t asks the L2 for half t % 2
+    // (four blocks, 128 bytes) of tile row t / 2 when that half holds a block
+    const int64_t pr = row0 + (threadIdx.x >> 1);
+    const int h = threadIdx.x & 1;
+    const uint8_t* pp = p.x + pr * p.ldx_bytes + static_cast<int64_t>(ct) * (kCtaCols * 2) + h * 128;
+    if (pr < p.M && ct * 8 + 4 * h < p.sK && MXFP4_IN_BOUNDS(p, kDbgXY, pp, 1)) prefetch_l2(pp);
+  }
+  pdl_wait();
+  pdl_release();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int sub = lane & 7;                 // 16-element block inside the 128 columns
@@ -214,11 +222,11 @@ __device__ __forceinline__ uint4 decode8_nv(uint32_t c, float sfv, float inv_g) 
 
 template <bool kVec32>
 __global__ void __launch_bounds__(kThreads) nvfp4_dequantize_kernel(const Nvfp4Params p) {
-  pdl_wait();
-  pdl_release();
   const int ct = static_cast<int>(blockIdx.x % static_cast<uint32_t>(p.nCT));
   const int64_t mt = blockIdx.x / static_cast<uint32_t>(p.nCT);
   const int64_t row0 = mt * kTileRows;
+  pdl_wait();
+  pdl_release();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int sub = lane & 7;
