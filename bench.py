@@ -872,7 +872,7 @@ def run_ours(args):
                          "unit": "GB/s", "frac": round(kernel_gbs / peak, 4),
                          "peak_src": "measured burst copy" if peak_src == "measured"
                          else "fallback 6.8 TB/s",
-                         "traffic": traffic, "traffic_src": "ncu DRAM read+write per launch",
+                         "traffic": traffic, "traffic_src": "ncu DRAM read+write of a mid-sequence launch",
                          "kernel": "quantize_tiles_kernel",
                          "median_us": round(med_ms * 1e3, 3)},
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s",
