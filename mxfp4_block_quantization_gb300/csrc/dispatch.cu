@@ -680,9 +680,12 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_scatter_kernel(const Nvfp4S
 // the gather, pad rows and rows whose index is out of
 // range keep tok1 = 0 and get zero words; in the scatter, pad rows are marked
 // -1 and get zero words, and rows that no route targets (0) keep the words
-// they held.  The tile's 128 x nKT words pass through shared memory, 32
-// k-tiles at a time, so that every 512-byte chunk is written whole, 16 bytes
-// per thread, instead of 4-byte words scattered over the chunks.
+// they held.  The words pass through shared memory so that every 512-byte
+// chunk is written whole, 16 bytes per thread, instead of 4-byte words
+// scattered over the chunks.  One CTA covers one tile and kTileCols of its
+// k-tiles (one load phase, one barrier, one store phase): the several CTAs of
+// a tile and their neighbours on an SM are in different phases at any time,
+// so the loads of some overlap the stores of others.
 struct TileScalesParams {
   const int32_t* __restrict__ tok1;       // [grid * 128] token + 1 of every padded row, 0: none,
                                           //   -1: pad row (kKeep only)
@@ -691,15 +694,16 @@ struct TileScalesParams {
   const int32_t* __restrict__ padded;
   int32_t E;
   int32_t nKT;
+  int32_t n_kc;                           // CTAs per tile: ceil(nKT / kTileCols)
 #ifdef MXFP4_DEBUG_BOUNDS
   DebugRanges dbg;  // kDbgScales, kDbgPadded, kDbgRowIndex (tok1), kDbgWork (stage)
 #endif
 };
 
-// 128 threads and 32 k-tiles (17 KB of shared memory) per pass: ten CTAs per
-// SM, so the 1405 tiles of the MoE batch run in one wave.
+// 128 threads and 16 k-tiles (9 KB of shared memory) per CTA, up to twelve
+// CTAs per SM.
 constexpr int kTileThreads = 128;
-constexpr int kTileCols = 32;                                  // k-tiles per shared-memory pass
+constexpr int kTileCols = 16;                                  // k-tiles per CTA
 constexpr int kTileQuadsPerRow = kTileCols / 4;                // 16-byte quads of a row
 constexpr int kTileRowStep = kTileThreads / kTileQuadsPerRow;  // rows per load step
 constexpr int kTileQuads = kTileRows / kTileRowStep;           // uint4 loads per thread
@@ -709,7 +713,7 @@ static_assert(kTileRows % kTileRowStep == 0 && kTileRows <= kTileThreads,
 // kKeep: rows with tok1 == 0 keep their words (the scatter); otherwise they
 // get zero words like pad rows (the gather).
 template <bool kKeep>
-__global__ void __launch_bounds__(kTileThreads, 10) tile_scales_kernel(const TileScalesParams p) {
+__global__ void __launch_bounds__(kTileThreads, 12) tile_scales_kernel(const TileScalesParams p) {
   __shared__ uint32_t s_w[kTileRows][kTileCols + 1];  // odd stride: conflict-free columns
   __shared__ int32_t s_tok[kTileRows];
   __shared__ const uint32_t* s_row[kTileRows];        // the row's staged words, or NULL
@@ -718,7 +722,9 @@ __global__ void __launch_bounds__(kTileThreads, 10) tile_scales_kernel(const Til
   pdl_release();
 
   if (!MXFP4_IN_BOUNDS(p, kDbgPadded, p.padded + p.E, 4)) return;
-  const int pr0 = static_cast<int>(blockIdx.x) * kTileRows;
+  const int tile_id = static_cast<int>(blockIdx.x) / p.n_kc;
+  const int c0 = (static_cast<int>(blockIdx.x) - tile_id * p.n_kc) * kTileCols;
+  const int pr0 = tile_id * kTileRows;
   // both loads in flight together: the tile's tokens and the padded total
   int32_t t1 = 0;
   if (threadIdx.x < kTileRows) {
@@ -734,10 +740,10 @@ __global__ void __launch_bounds__(kTileThreads, 10) tile_scales_kernel(const Til
   }
   __syncthreads();
 
-  uint8_t* const tile = p.scales + static_cast<int64_t>(blockIdx.x) * p.nKT * kChunkBytes;
+  uint8_t* const tile = p.scales + static_cast<int64_t>(tile_id) * p.nKT * kChunkBytes;
   const int qd = threadIdx.x % kTileQuadsPerRow;  // this thread's quad: words 4qd .. 4qd+3
   const int rb = threadIdx.x / kTileQuadsPerRow;  // and its rows rb, rb + kTileRowStep, ...
-  for (int c0 = 0; c0 < p.nKT; c0 += kTileCols) {
+  {
     const int cw = p.nKT - c0 < kTileCols ? p.nKT - c0 : kTileCols;
     const bool in_row = 4 * qd < cw;
     // every load of the pass in flight before the first shared-memory store
@@ -782,8 +788,15 @@ __global__ void __launch_bounds__(kTileThreads, 10) tile_scales_kernel(const Til
       if (MXFP4_IN_BOUNDS(p, kDbgScales, dp, 16))
         st_stream_v4(dp, make_uint4(s_w[o][c], s_w[o + 32][c], s_w[o + 64][c], s_w[o + 96][c]));
     }
-    __syncthreads();
   }
+}
+
+// The tile kernel's launch over `tiles` padded tiles.
+cudaError_t launch_tile_scales(bool keep, TileScalesParams ts, int64_t tiles, cudaStream_t stream) {
+  ts.n_kc = (ts.nKT + kTileCols - 1) / kTileCols;
+  const unsigned grid = static_cast<unsigned>(tiles * ts.n_kc);
+  return keep ? launch_pdl(tile_scales_kernel<true>, grid, kTileThreads, 0, stream, ts)
+              : launch_pdl(tile_scales_kernel<false>, grid, kTileThreads, 0, stream, ts);
 }
 
 // ---------------------------------------------------------------------
@@ -967,8 +980,7 @@ cudaError_t launch_quantize_grouped_scatter(const void* x, int64_t num_tokens, i
   debug_range(ts.dbg, kDbgRowIndex, workspace, PT * 4);
   debug_range(ts.dbg, kDbgWork, p.stage, gather_stage_ints(num_tokens, K) * 4);
 #endif
-  return launch_pdl(tile_scales_kernel<true>, static_cast<unsigned>(bound_tiles), kTileThreads, 0,
-                    stream, ts);
+  return launch_tile_scales(true, ts, bound_tiles, stream);
 }
 
 // Workspace of the gather through the scatter path, in int32:
@@ -1121,8 +1133,7 @@ cudaError_t gather_ws_impl(const void* x, int64_t num_src_rows, int64_t K, int64
   debug_range(ts.dbg, kDbgRowIndex, q.tok1, PT * 4);
   debug_range(ts.dbg, kDbgWork, p.stage, T * stage_ld(ts.nKT) * 4);
 #endif
-  err = launch_pdl(tile_scales_kernel<false>, static_cast<unsigned>(bound_tiles), kTileThreads,
-                   0, stream, ts);
+  err = launch_tile_scales(false, ts, bound_tiles, stream);
   if (err != cudaSuccess || code_rows >= R) return err;
   RowCodesParams rc{};
   rc.x = static_cast<const uint8_t*>(x);
@@ -1283,8 +1294,7 @@ cudaError_t launch_quantize_nvfp4_grouped_scatter(const void* x, int64_t num_tok
   debug_range(ts.dbg, kDbgRowIndex, workspace, PT * 4);
   debug_range(ts.dbg, kDbgWork, p.stage, PT * stage_ld(ts.nKT) * 4);
 #endif
-  return launch_pdl(tile_scales_kernel<true>, static_cast<unsigned>(bound_tiles), kTileThreads,
-                    0, stream, ts);
+  return launch_tile_scales(true, ts, bound_tiles, stream);
 }
 
 #ifdef MXFP4_DEBUG_BOUNDS
