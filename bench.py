@@ -747,9 +747,9 @@ def run_ours(args):
     ms_per_step = max_ms / args.steps
     value = total_bytes / (max_ms * 1e-3) / 1e9
     kernel_gbs = nbytes / (local_ms / args.steps * 1e-3) / 1e9
-    # the same kernel over 25 more batches of K steps (outside the timed
-    # region): the median over batches of the per-step time
-    _, med_ms = time_batches(step, stream, sweep, args.steps, 25)
+    # the same kernel over 25 more batches of K steps, at most 200 (outside
+    # the timed region): the median over batches of the per-step time
+    _, med_ms = time_batches(step, stream, sweep, min(args.steps, 200), 25)
 
     # ---- e2e through the public API with pinned host buffers: per step the
     # matrix goes host -> device in 4 row chunks on a copy stream, each chunk
