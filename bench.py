@@ -764,7 +764,7 @@ def run_ours(args):
     x_dev = torch.empty_like(x0)
     c_dev = torch.empty_like(codes[0])
     s_dev = torch.empty_like(scales[0])
-    n_chunks = 4
+    n_chunks = args.e2e_chunks
     chunk_rows = M_DENSE // n_chunks                # a multiple of 128: whole scale tiles
     tile_bytes = sb // (M_DENSE // 128)
     s_h2d, s_comp, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -906,6 +906,8 @@ def main(argv=None):
     ap.add_argument("--call", choices=SINGLE_CALLS,
                     help="only time this one call (for profiling)")
     ap.add_argument("--reps", type=int, default=5, help="repetitions of --call")
+    ap.add_argument("--e2e-chunks", type=int, default=4, choices=(1, 2, 4, 8, 16, 32),
+                    help="row chunks per step of the pipelined e2e measurement")
     ap.add_argument("--settle", type=float, default=1.0,
                     help="seconds of untimed launches after the warm-up steps (clock settling)")
     args = ap.parse_args(argv)
