@@ -412,7 +412,8 @@ size_t mxfp4_nvfp4_grouped_scale_bytes_bound(int64_t total_rows, int32_t E, int6
  * x                  BF16 [total_rows, K], contiguous, 16-byte aligned; K % 16 == 0.
  * expert_offsets     DEVICE int32 [E+1], 0 = o[0] <= ... <= o[E] = total_rows
  *                    (checked on the device).
- * global_scales      DEVICE float32 [E], positive finite (not checked).
+ * global_scales      DEVICE float32 [E], positive finite (not checked); below
+ *                    2^119 for fully specified results, as mxfp4_quantize_nvfp4.
  * codes              [total_rows, K/2]; scales >= the bound above, 16-byte
  *                    aligned; bytes past P[E] * ceil(K/64) * 4 are not touched.
  * scale_row_offsets  DEVICE int32 [E+1], output P[0..E].
@@ -516,7 +517,13 @@ int mxfp4_quantize_nvfp4_grouped_scatter_ws_f16(const void* x, int64_t num_token
  *   blocks whose byte is 0 emit zero codes;
  *   dequantize: y = BF16_RNE((e2m1(code) * float(byte)) * (1 / g)).
  * g is the per-tensor global scale (SFScaleVal), a positive finite float
- * read from DEVICE memory (global_scale, 4-byte aligned).
+ * read from DEVICE memory (global_scale, 4-byte aligned).  The results are
+ * specified for g < 2^119, where g / float(byte) stays finite for every
+ * nonzero byte (the smallest is 2^-9).  Above it a block with a small byte
+ * has inv = +inf, its zero elements give 0 * inf = NaN, and their codes are
+ * unspecified (E2M1 has no NaN; the sequence above does not say how one is
+ * encoded); every other output is as above.  A caller's 448 * 6 / amax
+ * exceeds 2^119 only for amax below 4e-33.
  * Scales use the 128x4 tiled layout of mxfp4_quantize over K/16 scale
  * columns: mxfp4_nvfp4_scale_bytes(M, K) = ceil(M/128)*128 * ceil(K/64)*4
  * bytes, pad bytes 0x00.  Codes: [M, K/2], element 2j in the low nibble.

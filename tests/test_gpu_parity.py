@@ -1271,6 +1271,86 @@ def test_nvfp4_scatter_moe_full_size_one_global_scale(mx, moe):
     assert_full(s2[:s_o.size].cpu().numpy(), s_o, "E4M3 tiled scales")
 
 
+# ------------------------------------ NVFP4 at the ends of the global scale
+# g * vecMax / 6 overflowing to +inf (the E4M3 byte saturates at 448, the
+# products x * g / 448 overflow and the codes saturate at +-6), g below the
+# point where any block gets a nonzero E4M3 byte (byte 0, zero codes), and a
+# subnormal g; every step is the float32 arithmetic both sides share.  The
+# results are specified for g < 2^119 (g / float(byte) finite for every
+# nonzero byte); 6.5e35 is just below that bound.
+EXTREME_G = [6.5e35, 1.0e30, 1.0e-3, 1.0e-30, 1.0e-40]
+
+
+@pytest.mark.parametrize("g", EXTREME_G)
+def test_nvfp4_extreme_global_scale(mx, g):
+    """Dense NVFP4 quantize of the edge-case matrix (heavy tails, zero and
+    subnormal blocks) bit-exact against the oracle; the dequantize too where
+    1/g is finite (for a subnormal g, 1/g = +inf and a zero code gives
+    0 * inf = NaN, whose payload the two sides need not share)."""
+    x = W.edge_cases(4).cuda()
+    M, K = x.shape
+    c, s, y = run_nvfp4(mx, x, g)
+    g32 = np.float32(g)
+    c_o, s_o = oracle.nvfp4_quantize(bits(x), float(g32))
+    assert np.array_equal(s, s_o), _first_diff(s, s_o)
+    assert np.array_equal(c, c_o), _first_diff(c, c_o)
+    if g >= 1.0e30:
+        assert (s_o == 0x7E).sum() > s_o.size // 2          # saturated E4M3 bytes
+        assert ((c_o & 0x77) == 0x77).any()                 # and saturated codes
+    if g <= 1.0e-30:
+        assert not s_o.any() and not c_o.any()              # no block reaches 2^-9
+    with np.errstate(divide="ignore", over="ignore"):
+        inv_finite = np.isfinite(np.float32(1.0) / g32)
+    if inv_finite:
+        y_o = oracle.nvfp4_dequantize(c_o, s_o, M, K, float(g32))
+        assert np.array_equal(y, y_o), _first_diff(y, y_o)
+
+
+def test_nvfp4_global_scale_beyond_its_range(mx):
+    """g = 3e38, past 2^119: a block of BF16 subnormals gets a small E4M3
+    byte, g / float(byte) overflows to +inf and its zero elements give
+    0 * inf = NaN, whose E2M1 code is unspecified.  The call must not fault,
+    the guard bands hold, every scale byte is exact, and so is every code
+    except those NaN products'."""
+    x = W.edge_cases(4).cuda()
+    M, K = x.shape
+    g32 = np.float32(3.0e38)
+    c, s, _ = run_nvfp4(mx, x, float(g32))
+    xb = bits(x)
+    c_o, s_o = oracle.nvfp4_quantize(xb, float(g32))
+    assert np.array_equal(s, s_o), _first_diff(s, s_o)
+    byte = oracle.untile(s_o, M, K // 16)                    # [M, K/16] block bytes
+    sfv = np.array([oracle.e4m3_to_double(b) for b in range(256)], np.float32)[byte]
+    with np.errstate(divide="ignore", over="ignore"):
+        inv_inf = np.isinf(g32 / np.where(sfv > 0, sfv, np.float32(1)))
+    nan_el = ((xb & 0x7FFF) == 0) & np.repeat(inv_inf & (byte != 0), 16, axis=1)
+    assert nan_el.any(), "the case must occur"
+    keep = np.ones((M, K), bool)
+    keep[nan_el] = False
+    nib = lambda c_: np.stack([c_ & 0xF, c_ >> 4], axis=2).reshape(M, K)  # noqa: E731
+    assert np.array_equal(nib(c)[keep], nib(c_o)[keep])
+
+
+@pytest.mark.parametrize("shared", [False, True], ids=["per_expert", "shared"])
+def test_nvfp4_grouped_and_scatter_extreme_global_scales(mx, scatter_ws, shared):
+    """The experts quant and both scatter forms with global scales at the
+    ends of float32: one of EXTREME_G per expert (and 1.0), or the largest
+    shared by every expert (the scatter's one-scale path)."""
+    g = W.moe_grouped(seed=9, tokens=300, top_k=4, num_experts=6, K=320, device="cuda")
+    total = g.row_index.numel()
+    gs = (np.full(6, EXTREME_G[0], np.float32) if shared
+          else np.array(EXTREME_G[:2] + [1.0] + EXTREME_G[2:], np.float32))
+    c, s, sro, st = run_nvfp4_grouped(mx, g.x, g.offsets, torch.from_numpy(gs).cuda())
+    rc, c_o, s_o, sro_o = oracle.nvfp4_quantize_grouped(bits(g.x), g.offsets.cpu().numpy(), gs)
+    assert st == 0 and rc == 0 and np.array_equal(sro, sro_o)
+    assert np.array_equal(c, c_o), _first_diff(c, c_o)
+    used = int(sro_o[-1]) * 20
+    assert np.array_equal(s[:used], s_o[:used]), _first_diff(s[:used], s_o[:used])
+    gpu, orc = run_nvfp4_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, total, gs, seed=9,
+                                 ws=scatter_ws)
+    assert_scatter_parity(gpu, orc)
+
+
 # ----------------------------------------------- FP16 input, grouped forms
 def _f16(t):
     return t.to(torch.float16)
