@@ -515,7 +515,9 @@ int mxfp4_quantize_nvfp4_grouped_scatter_ws_f16(const void* x, int64_t num_token
  *   q = vecMax / 6; sf = g * q; byte = E4M3_RNE_satfinite(sf);
  *   inv = g / float(byte); code = E2M1_RNE_saturating(x * inv);
  *   blocks whose byte is 0 emit zero codes;
- *   dequantize: y = BF16_RNE((e2m1(code) * float(byte)) * (1 / g)).
+ *   dequantize: y = BF16_RNE((e2m1(code) * float(byte)) * (1 / g)), and
+ *   0x7FC0 (the BF16 NaN) for every element of a block whose scale byte is
+ *   the E4M3 NaN (0x7F or 0xFF); specified for g >= 2^-127 (1 / g finite).
  * g is the per-tensor global scale (SFScaleVal), a positive finite float
  * read from DEVICE memory (global_scale, 4-byte aligned).  The results are
  * specified for g < 2^119, where g / float(byte) stays finite for every

@@ -254,9 +254,15 @@ __global__ void __launch_bounds__(kThreads) nvfp4_dequantize_kernel(const Nvfp4P
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
     const uint32_t word = i == 0 ? sr.x : i == 1 ? sr.y : i == 2 ? sr.z : sr.w;
-    const float sfv = e4m3_to_f32((word >> (8 * cc)) & 0xFFu);
-    const uint4 o0 = decode8_nv(c[i].x, sfv, inv_g);
-    const uint4 o1 = decode8_nv(c[i].y, sfv, inv_g);
+    const uint32_t sb = (word >> (8 * cc)) & 0xFFu;
+    uint4 o0, o1;
+    if ((sb & 0x7Fu) == 0x7Fu) {  // the E4M3 NaN: the canonical BF16 NaN, as E8M0 255
+      o0 = o1 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+    } else {
+      const float sfv = e4m3_to_f32(sb);
+      o0 = decode8_nv(c[i].x, sfv, inv_g);
+      o1 = decode8_nv(c[i].y, sfv, inv_g);
+    }
     if (col_ok && kRowsPerPass * i < lim && MXFP4_IN_BOUNDS(p, kDbgXY, yp + i * yld_pass, 32)) {
       if constexpr (kVec32) {
         st_stream_v8(yp + i * yld_pass, o0, o1);

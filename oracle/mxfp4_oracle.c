@@ -795,7 +795,12 @@ void orc_nvfp4_dequantize(const uint8_t* codes, const uint8_t* tiled_scales, int
     for (int64_t k = 0; k < K; ++k) {
       uint8_t byte = codes[r * (K / 2) + k / 2];
       uint8_t nib = (k % 2 == 0) ? (byte & 0xFu) : (byte >> 4);
-      float sfv = (float)orc_e4m3_to_double(flat[r * sK + k / 16]);
+      uint8_t sb = flat[r * sK + k / 16];
+      if ((sb & 0x7Fu) == 0x7Fu) { /* the E4M3 NaN: the canonical BF16 NaN, as E8M0 255 */
+        y[r * K + k] = 0x7FC0u;
+        continue;
+      }
+      float sfv = (float)orc_e4m3_to_double(sb);
       float t = (float)orc_e2m1_decode(nib) * sfv; /* exact */
       float v = t * inv_g;
       y[r * K + k] = orc_double_to_bf16_rne((double)v);

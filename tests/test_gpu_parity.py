@@ -1306,6 +1306,28 @@ def test_nvfp4_extreme_global_scale(mx, g):
         assert np.array_equal(y, y_o), _first_diff(y, y_o)
 
 
+@pytest.mark.parametrize("g", [1.0, 0.37, 1.0e30, 1.0e-30])
+def test_nvfp4_dequantize_every_code_and_scale_byte(mx, g):
+    """All 16 codes x all 256 E4M3 scale bytes (negative, subnormal and the
+    NaN bytes, whose blocks give 0x7FC0), both store widths, against the
+    oracle."""
+    M, K = 256, 256
+    flat = (np.arange(M * (K // 16)) % 256).astype(np.uint8).reshape(M, K // 16)
+    nib = np.tile(np.arange(16), M * K // 16).reshape(M, K)
+    codes = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    tiled = oracle.tile(flat)
+    want = oracle.nvfp4_dequantize(codes, tiled, M, K, float(np.float32(g)))
+    gs = torch.tensor([g], dtype=torch.float32, device="cuda")
+    for off in (0, 8):                  # 32-byte and only 16-byte aligned outputs
+        y = Guarded(M * K * 2 + 16, torch.bfloat16, None)
+        out = y.t[off:off + M * K].view(M, K)
+        mx.mxfp4_dequantize_nvfp4(torch.from_numpy(codes).cuda(), torch.from_numpy(tiled).cuda(),
+                                  gs, M, K, out)
+        torch.cuda.synchronize()
+        y.check()
+        assert np.array_equal(bits(out), want), _first_diff(bits(out), want)
+
+
 def test_nvfp4_global_scale_beyond_its_range(mx):
     """g = 3e38, past 2^119: a block of BF16 subnormals gets a small E4M3
     byte, g / float(byte) overflows to +inf and its zero elements give

@@ -308,3 +308,30 @@ def test_nvfp4_scatter_bad_entries_and_offsets(orc):
     cp = np.full((80, 16), 0x5A, np.uint8)
     rc, c, s, sro = orc.nvfp4_quantize_grouped_scatter(xb, clean, bad, 80, gs, cp)
     assert rc == -6 and (sro == -1).all() and (c == 0x5A).all() and not s.any()
+
+
+@pytest.mark.parametrize("g", [1.0, 0.37, 2688.0 / 25.0, 1.0e30, 1.0e-30])
+def test_nvfp4_dequantize_every_code_and_scale_byte(orc, g):
+    """All 16 codes x all 256 E4M3 scale bytes (negative, subnormal and the
+    NaN bytes 0x7F / 0xFF included) against torch: the E4M3 value from
+    torch's float8_e4m3fn, the float32 products (e2m1 * float(byte)) *
+    float32(1/g), torch's BF16 cast; the NaN bytes give 0x7FC0 for the block
+    (the library's NaN, as for the E8M0 NaN 255)."""
+    torch = pytest.importorskip("torch")
+    e2m1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, -0.0, -.5, -1, -1.5, -2, -3, -4, -6], np.float32)
+    M, K = 256, 256                         # one scale byte per 16-element block
+    sb = np.arange(M * (K // 16)) % 256     # every byte, 16 times over
+    flat = sb.astype(np.uint8).reshape(M, K // 16)
+    nib = np.tile(np.arange(16), M * K // 16).reshape(M, K)
+    codes = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    y = orc.nvfp4_dequantize(codes, orc.tile(flat), M, K, g)
+    sfv = torch.from_numpy(flat).view(torch.float8_e4m3fn).float().numpy()
+    inv = np.float32(1.0) / np.float32(g)
+    prod = (e2m1[nib] * np.repeat(sfv, 16, axis=1)).astype(np.float32) * inv
+    want = torch.from_numpy(prod.astype(np.float32)).to(torch.bfloat16).view(torch.int16)
+    want = want.numpy().view(np.uint16).copy()
+    nan_blk = np.repeat((flat & 0x7F) == 0x7F, 16, axis=1)
+    want[nan_blk] = 0x7FC0
+    assert not np.isnan(prod[~nan_blk]).any()
+    assert np.array_equal(y, want), (np.argwhere(y != want)[:3], y[y != want][:3],
+                                     want[y != want][:3])
