@@ -1373,6 +1373,52 @@ def test_nvfp4_grouped_and_scatter_extreme_global_scales(mx, scatter_ws, shared)
     assert_scatter_parity(gpu, orc)
 
 
+# --------------------------------------- wide rows and a single expert
+@pytest.mark.parametrize("K", [32768, 16 * 1027])
+def test_every_form_on_wide_rows(mx, K, scatter_ws):
+    """Rows of 32,768 elements (256 k-tiles: 16 tile-kernel CTAs per tile, 64
+    passes per token row) and of 16,432 (an NVFP4 width with a ragged last
+    k-tile): dense MXFP4 and NVFP4 quantize and dequantize, the grouped
+    quantize, and the dispatch as gather and as scatter (MXFP4 and NVFP4),
+    all against the oracle."""
+    g = W.moe_grouped(seed=K % 97, tokens=40, top_k=3, num_experts=5, K=K, device="cuda")
+    total = g.row_index.numel()
+    if K % 32 == 0:
+        assert_quant_parity(mx, g.x_tokens[:33].contiguous())
+        c, s, sro, st = run_grouped(mx, g.x, g.offsets)
+        rc, c_o, s_o, sro_o = oracle.quantize_grouped(bits(g.x), g.offsets.cpu().numpy())
+        assert st == rc == 0 and np.array_equal(sro, sro_o) and np.array_equal(c, c_o)
+        used = int(sro_o[-1]) * ((K // 32 + 3) // 4 * 4)
+        assert np.array_equal(s[:used], s_o[:used])
+        _gather_oracle_check(run_gather_ws(mx, g.x_tokens, g.row_index, g.offsets),
+                             bits(g.x_tokens), g.row_index.cpu().numpy(),
+                             g.offsets.cpu().numpy(), K)
+        assert_scatter_parity(*run_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, total,
+                                           seed=K, ws=scatter_ws))
+    assert_nvfp4_parity(mx, g.x_tokens[:33].contiguous(), 2688.0 / 25.0)
+    gs = _expert_gscales(5, K)
+    assert_scatter_parity(*run_nvfp4_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, total, gs,
+                                             seed=K, ws=scatter_ws))
+
+
+def test_every_grouped_form_with_one_expert(mx, scatter_ws):
+    """E = 1: every row in one segment (its own scale tiles), top_k = 1."""
+    g = W.moe_grouped(seed=77, tokens=300, top_k=1, num_experts=1, K=640, device="cuda")
+    total = g.row_index.numel()
+    c, s, sro, st = run_grouped(mx, g.x, g.offsets)
+    rc, c_o, s_o, sro_o = oracle.quantize_grouped(bits(g.x), g.offsets.cpu().numpy())
+    assert st == rc == 0 and sro.tolist() == [0, 384] and np.array_equal(c, c_o)
+    assert np.array_equal(s[:384 * 20], s_o[:384 * 20])
+    _gather_oracle_check(run_gather_ws(mx, g.x_tokens, g.row_index, g.offsets),
+                         bits(g.x_tokens), g.row_index.cpu().numpy(), g.offsets.cpu().numpy(),
+                         640)
+    assert_scatter_parity(*run_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, total, seed=77,
+                                       ws=scatter_ws))
+    assert_scatter_parity(*run_nvfp4_scatter(mx, g.x_tokens, g.dest_rows, g.offsets, total,
+                                             np.array([3.5], np.float32), seed=77,
+                                             ws=scatter_ws))
+
+
 # ----------------------------------------------- FP16 input, grouped forms
 def _f16(t):
     return t.to(torch.float16)
