@@ -87,6 +87,9 @@ def lib():
         L.orc_nvfp4_quantize_flat.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_float, _u8p, _u8p]
         L.orc_nvfp4_quantize.restype = None
         L.orc_nvfp4_quantize.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_float, _u8p, _u8p]
+        L.orc_moe_route.restype = ctypes.c_int
+        L.orc_moe_route.argtypes = [_i32p, _i64, ctypes.c_int32, ctypes.c_int32, _i32p, _i32p,
+                                    _i32p]
         L.orc_nvfp4_dequantize.restype = None
         L.orc_nvfp4_dequantize.argtypes = [_u8p, _u8p, _i64, _i64, ctypes.c_float, _u16p]
         L.orc_e8m0_scale_legacy.restype = ctypes.c_uint8
@@ -428,6 +431,21 @@ def quantize_rows_into(xbits: np.ndarray, row0: int, row1: int, codes: np.ndarra
     lib().orc_quantize(xs.ctypes.data_as(_u16p), row1 - row0, K, K,
                        cs.ctypes.data_as(_u8p),
                        scales[off:].ctypes.data_as(_u8p))
+
+
+# --------------------------------------------------- dispatch permutation
+def moe_route(topk_ids: np.ndarray, num_experts: int):
+    """The dispatch permutation from the router's expert ids [T, top_k]:
+    (rc, offsets [E+1], dest_rows [T, top_k], row_index [rows]); rc 0 or -7."""
+    ids = _c(topk_ids, np.int32)
+    T = ids.shape[0]
+    top_k = ids.shape[1] if ids.ndim == 2 else 1
+    off = np.zeros(num_experts + 1, np.int32)
+    dest = np.zeros((T, top_k), np.int32)
+    rows = np.zeros(max(ids.size, 1), np.int32)
+    rc = lib().orc_moe_route(_p(ids, _i32p), T, top_k, num_experts, _p(off, _i32p),
+                             _p(dest, _i32p), _p(rows, _i32p))
+    return rc, off, dest, rows[:int(off[-1])]
 
 
 # ------------------------------------------- the same routines on host threads

@@ -811,3 +811,34 @@ void orc_nvfp4_dequantize(const uint8_t* codes, const uint8_t* tiled_scales, int
 void orc_e4m3_from_double_many(const double* d, int64_t n, uint8_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_from_double(d[i]);
 }
+
+/* The MoE dispatch permutation from the router's choices ([PR43557]
+ * "Implementation breakdown" item 3: the experts quant takes the routed
+ * activations sorted by expert; this is the sort).  Entry i = t * top_k + j
+ * of topk_ids is expert topk_ids[i] of route j of token t.  Rows are the
+ * entries with a valid expert (0 <= id < E) in order of expert, then of i;
+ * offsets[e] is the first row of expert e, offsets[E] the number of rows;
+ * dest_rows[i] is the row of entry i (-1 for an entry not dispatched) and
+ * row_index[row] its token (may be NULL).  Returns 0, or -7 when some id is
+ * neither -1 (not dispatched) nor in [0, E). */
+int orc_moe_route(const int32_t* topk_ids, int64_t num_tokens, int32_t top_k, int32_t E,
+                  int32_t* offsets, int32_t* dest_rows, int32_t* row_index) {
+  const int64_t n = num_tokens * top_k;
+  int bad = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    dest_rows[i] = -1;
+    if (topk_ids[i] != -1 && (topk_ids[i] < 0 || topk_ids[i] >= E)) bad = 1;
+  }
+  int64_t row = 0;
+  for (int32_t e = 0; e < E; ++e) {
+    offsets[e] = (int32_t)row;
+    for (int64_t i = 0; i < n; ++i)
+      if (topk_ids[i] == e) {
+        dest_rows[i] = (int32_t)row;
+        if (row_index != NULL) row_index[row] = (int32_t)(i / top_k);
+        ++row;
+      }
+  }
+  offsets[E] = (int32_t)row;
+  return bad ? -7 : 0;
+}

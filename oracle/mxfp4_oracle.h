@@ -160,6 +160,12 @@ int orc_nvfp4_quantize_grouped_scatter_f16(const uint16_t* x, int64_t num_tokens
                                            int32_t* scale_row_offsets);
 void orc_nvfp4_dequantize(const uint8_t* codes, const uint8_t* tiled_scales, int64_t M, int64_t K,
                           float g, uint16_t* y);
+/* The dispatch permutation from the router's expert ids [num_tokens, top_k]:
+ * rows in order of expert, then of entry index; offsets [E+1], dest_rows
+ * [num_tokens * top_k] (-1: not dispatched), row_index [rows] (may be NULL).
+ * Returns 0 or -7 (an id neither -1 nor in [0, E); it is not dispatched). */
+int orc_moe_route(const int32_t* topk_ids, int64_t num_tokens, int32_t top_k, int32_t E,
+                  int32_t* offsets, int32_t* dest_rows, int32_t* row_index);
 
 #ifdef __cplusplus
 }
