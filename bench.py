@@ -514,6 +514,26 @@ def measure_rows(mx, W, stream, peak, l2_bytes, sweep):
                                                           total, ws, codes, scales, sro, st,
                                                           stream), 6))
     del ws
+    # the dispatch permutation itself, from the router's expert ids (every
+    # route's expert read back from its row's segment): ids in, offsets,
+    # token -> rows and row -> token out; then routed straight into the
+    # scatter quantize with a workspace
+    off_h = g.offsets.cpu()
+    ids = (torch.searchsorted(off_h, g.dest_rows.cpu(), right=True) - 1).to(torch.int32).cuda()
+    r_off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    r_dest = torch.empty_like(g.dest_rows)
+    r_rows = torch.empty(total, dtype=torch.int32, device="cuda")
+    r_ws = torch.empty(mx.mxfp4_route_workspace_bytes(T, g.dest_rows.shape[1], E),
+                       dtype=torch.uint8, device="cuda")
+    route = lambda i: mx.mxfp4_moe_route(ids, E, r_ws, r_off, r_dest, r_rows, st, stream)  # noqa: E731
+    row("route_moe_16384tok_top8_E384", 12 * total + 4 * (E + 1), tb(route, 40))
+    assert torch.equal(r_off, g.offsets) and torch.equal(r_dest, g.dest_rows)
+    ws = torch.empty(mx.mxfp4_scatter_workspace_bytes(T, total, E, K), dtype=torch.uint8,
+                     device="cuda")
+    row("route_then_scatter_ws_moe", nb,
+        tb(lambda i: (route(i), mx.mxfp4_quantize_grouped_scatter_ws(
+            g.x_tokens, r_dest, r_off, total, ws, codes, scales, sro, st, stream)), 6))
+    del ws
     # the NVFP4 experts quant with the same dispatch fused in; one global
     # scale shared by every expert, then a scale of its own per expert
     nb_nvs = 2 * T * K + 4 * total + total * K // 2 + padded * (K // 16) + 4 * (E + 1) + 4 * E
@@ -579,7 +599,7 @@ def measure_rows(mx, W, stream, peak, l2_bytes, sweep):
 
 DISPATCH_CALLS = ("gather", "gather_ws", "scatter", "scatter_ws", "nvfp4_scatter",
                   "nvfp4_scatter_ws", "nvfp4_scatter_ws_own_g")
-SINGLE_CALLS = DISPATCH_CALLS + ("dense", "w13")
+SINGLE_CALLS = DISPATCH_CALLS + ("dense", "w13", "route")
 
 
 def run_one_call(args):
@@ -618,6 +638,23 @@ def run_one_call(args):
     T, K = g.x_tokens.shape
     total = g.row_index.numel()
     E = g.num_experts
+    if args.call == "route":
+        # the dispatch permutation of the batch from its routes' expert ids
+        off_h = g.offsets.cpu()
+        ids = (torch.searchsorted(off_h, g.dest_rows.cpu(), right=True) - 1).to(torch.int32)
+        ids = ids.cuda()
+        fn = lambda: mx.moe_route(ids, E)  # noqa: E731
+        fn()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.reps):
+            fn()
+        t1.record()
+        torch.cuda.synchronize()
+        print(json.dumps({"call": "route", "reps": args.reps,
+                          "us_per_call": round(t0.elapsed_time(t1) * 1e3 / args.reps, 2)}))
+        return 0
     codes = torch.empty((total, K // 2), dtype=torch.uint8, device="cuda")
     scales = torch.empty(mx.mxfp4_grouped_scale_bytes_bound(total, E, K), dtype=torch.uint8,
                          device="cuda")

@@ -504,6 +504,40 @@ int mxfp4_quantize_nvfp4_grouped_scatter_ws_f16(const void* x, int64_t num_token
                                                 uint8_t* scales, int32_t* scale_row_offsets,
                                                 int32_t* status, void* stream);
 
+/* mxfp4_moe_route — the dispatch permutation the grouped, scatter and
+ * gather calls take, from the router's choices ([PR43557] "Implementation
+ * breakdown" item 3: the experts quant takes the routed activations sorted
+ * by expert; this is that sort, on the device).
+ *
+ * topk_ids        DEVICE int32 [num_tokens, top_k]: the expert of route j of
+ *                 token t at t * top_k + j; -1: the route is not dispatched.
+ * num_tokens      >= 0; top_k >= 1; num_tokens * top_k <= INT32_MAX / 2.
+ * E               1 <= E <= MXFP4_ROUTE_MAX_EXPERTS.
+ * workspace       DEVICE, >= mxfp4_route_workspace_bytes(num_tokens, top_k, E)
+ *                 bytes, 16-byte aligned, contents on entry irrelevant
+ *                 (NULL allowed when num_tokens * top_k == 0).
+ * expert_offsets  DEVICE int32 [E+1], out: the first row of every expert and
+ *                 the number of rows (the expert_offsets of the grouped calls).
+ * dest_rows       DEVICE int32 [num_tokens, top_k], out: the row of every
+ *                 route, -1 when not dispatched (the scatter calls' dest_rows).
+ * row_index       DEVICE int32 [num_tokens * top_k] or NULL, out: the token of
+ *                 every row; entries from expert_offsets[E] on are not written
+ *                 (the gather calls' row_index).
+ * status          DEVICE int32 or NULL, out: MXFP4_OK, or MXFP4_EINDEX when
+ *                 an id is neither -1 nor in [0, E) (that route is dropped).
+ * Rows are the dispatched routes in order of expert, then of t * top_k + j:
+ * deterministic, and in token order within every expert.  Errors (returned
+ * before anything is enqueued): MXFP4_EINVAL for negative sizes, top_k < 1,
+ * E < 1, a NULL pointer or a small workspace; MXFP4_ESHAPE for E or the
+ * number of routes above the limits; MXFP4_EALIGN for an int32 array not
+ * 4-byte or a workspace not 16-byte aligned; MXFP4_EALIAS for overlapping
+ * buffers; MXFP4_ECUDA for a refused launch.  Asynchronous on `stream`. */
+#define MXFP4_ROUTE_MAX_EXPERTS 8192
+size_t mxfp4_route_workspace_bytes(int64_t num_tokens, int32_t top_k, int32_t E);
+int mxfp4_moe_route(const int32_t* topk_ids, int64_t num_tokens, int32_t top_k, int32_t E,
+                    void* workspace, size_t workspace_bytes, int32_t* expert_offsets,
+                    int32_t* dest_rows, int32_t* row_index, int32_t* status, void* stream);
+
 /* ---------------------------------------------------------------- NVFP4
  * The other branch of the same quantize kernel on [PR43557] ("Implementation
  * breakdown" item 1, the non-UE8M0 branch of the cvt_warp_fp16_to_fp4

@@ -44,6 +44,7 @@ __all__ = [
     "mxfp4_quantize_nvfp4_grouped_scatter", "mxfp4_quantize_nvfp4_grouped_scatter_f16",
     "quantize_nvfp4_grouped_scatter", "mxfp4_nvfp4_scatter_workspace_bytes",
     "mxfp4_quantize_nvfp4_grouped_scatter_ws", "mxfp4_quantize_nvfp4_grouped_scatter_ws_f16",
+    "MXFP4_ROUTE_MAX_EXPERTS", "mxfp4_route_workspace_bytes", "mxfp4_moe_route", "moe_route",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300.so")
@@ -52,6 +53,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb
 DEBUG_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300_debug.so")
 
 MXFP4_SCATTER_MAX_TOP_K = 32
+MXFP4_ROUTE_MAX_EXPERTS = 8192
 MXFP4_NOALLOC_SCRATCH_BYTES = 4 << 20
 MXFP4_OK = 0
 MXFP4_EINVAL = -1
@@ -146,6 +148,10 @@ def _load(path=LIB_PATH):
     L.mxfp4_nvfp4_scatter_workspace_bytes.argtypes = [i64, i32, i64]
     L.mxfp4_dequantize_nvfp4.restype = ctypes.c_int
     L.mxfp4_dequantize_nvfp4.argtypes = [vp, vp, vp, i64, i64, vp, vp]
+    L.mxfp4_route_workspace_bytes.restype = ctypes.c_size_t
+    L.mxfp4_route_workspace_bytes.argtypes = [i64, i32, i32]
+    L.mxfp4_moe_route.restype = ctypes.c_int
+    L.mxfp4_moe_route.argtypes = [vp, i64, i32, i32, vp, ctypes.c_size_t, vp, vp, vp, vp, vp]
     L.mxfp4_status_string.restype = ctypes.c_char_p
     L.mxfp4_status_string.argtypes = [ctypes.c_int]
     L.mxfp4_version.restype = ctypes.c_int
@@ -444,6 +450,36 @@ def mxfp4_quantize_grouped_scatter_ws_f16(x, dest_rows, expert_offsets, total_ro
              stream, True, workspace)
 
 
+def mxfp4_route_workspace_bytes(num_tokens: int, top_k: int, E: int) -> int:
+    return int(_lib.mxfp4_route_workspace_bytes(int(num_tokens), int(top_k), int(E)))
+
+
+def mxfp4_moe_route(topk_ids, num_experts: int, workspace, expert_offsets, dest_rows,
+                    row_index=None, status=None, stream=None) -> None:
+    """The dispatch permutation from the router's expert ids ``topk_ids``
+    [num_tokens, top_k] (int32, -1: not dispatched): ``expert_offsets``
+    [E+1], ``dest_rows`` [num_tokens, top_k] and, if given, ``row_index``
+    [num_tokens * top_k] (the token of every row), in order of expert, then
+    of entry.  ``workspace``: >= mxfp4_route_workspace_bytes bytes."""
+    for name, t in (("topk_ids", topk_ids), ("expert_offsets", expert_offsets),
+                    ("dest_rows", dest_rows), ("row_index", row_index), ("status", status)):
+        _need_cuda(name, t, torch.int32)
+    _need_cuda("workspace", workspace)
+    for name, t in (("topk_ids", topk_ids), ("dest_rows", dest_rows)):
+        if t.dim() != 2 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [num_tokens, top_k] tensor")
+    if dest_rows.shape != topk_ids.shape:
+        raise ValueError("dest_rows must have the shape of topk_ids")
+    T, top_k = topk_ids.shape
+    with torch.cuda.device(_device_of(topk_ids, workspace, expert_offsets, dest_rows,
+                                      row_index, status)):
+        _check(_lib.mxfp4_moe_route(_ptr(topk_ids), T, top_k, int(num_experts), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _ptr(expert_offsets), _ptr(dest_rows), _ptr(row_index),
+                                    _ptr(status), _stream(stream, topk_ids.device)),
+               "mxfp4_moe_route")
+
+
 def mxfp4_dequantize(codes, scales, M: int, K: int, y, stream=None) -> None:
     """``codes`` [M, K/2] + tiled ``scales`` -> BF16 ``y`` [M, K] (contiguous)."""
     _need_cuda("codes", codes, torch.uint8)
@@ -709,6 +745,23 @@ def quantize_grouped_scatter(x, dest_rows, expert_offsets, total_rows=None, stre
     _scatter(x, dest_rows, expert_offsets, total, codes, scales, sro, status, stream,
              x.dtype == torch.float16, ws)
     return codes, scales, sro, status
+
+
+def moe_route(topk_ids, num_experts: int, stream=None):
+    """Returns (expert_offsets, dest_rows, row_index, status) of the router's
+    expert ids ``topk_ids`` [num_tokens, top_k]: the inputs of the grouped,
+    scatter and gather calls (row_index holds expert_offsets[-1] valid rows;
+    the rest of it is not written)."""
+    dev = topk_ids.device
+    T, top_k = topk_ids.shape
+    off = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    dest = torch.empty((T, top_k), dtype=torch.int32, device=dev)
+    rows = torch.empty(max(T * top_k, 1), dtype=torch.int32, device=dev)
+    status = torch.empty(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(max(mxfp4_route_workspace_bytes(T, top_k, num_experts), 16),
+                     dtype=torch.uint8, device=dev)
+    mxfp4_moe_route(topk_ids, num_experts, ws, off, dest, rows, status, stream)
+    return off, dest, rows, status
 
 
 def dequantize(codes, scales, M: int, K: int, stream=None):

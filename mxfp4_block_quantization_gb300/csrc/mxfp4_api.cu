@@ -515,6 +515,42 @@ int mxfp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int
       mxfp4::launch_dequantize(codes, scales, M, K, y, static_cast<cudaStream_t>(stream)));
 }
 
+size_t mxfp4_route_workspace_bytes(int64_t num_tokens, int32_t top_k, int32_t E) {
+  if (num_tokens < 0 || top_k < 1 || E < 1 || E > MXFP4_ROUTE_MAX_EXPERTS) return 0;
+  if (num_tokens > (INT32_MAX / 2) / top_k) return 0;
+  return static_cast<size_t>(mxfp4::route_workspace_ints(num_tokens * top_k, E) * 4);
+}
+
+int mxfp4_moe_route(const int32_t* topk_ids, int64_t num_tokens, int32_t top_k, int32_t E,
+                    void* workspace, size_t workspace_bytes, int32_t* expert_offsets,
+                    int32_t* dest_rows, int32_t* row_index, int32_t* status, void* stream) {
+  if (num_tokens < 0 || top_k < 1 || E < 1) return MXFP4_EINVAL;
+  if (E > MXFP4_ROUTE_MAX_EXPERTS || num_tokens > (INT32_MAX / 2) / top_k) return MXFP4_ESHAPE;
+  const int64_t n = num_tokens * top_k;
+  if (!expert_offsets || (n > 0 && (!topk_ids || !dest_rows))) return MXFP4_EINVAL;
+  const int64_t ws_bytes = mxfp4::route_workspace_ints(n, E) * 4;
+  if (n > 0 && (!workspace || workspace_bytes < static_cast<size_t>(ws_bytes)))
+    return MXFP4_EINVAL;
+  const auto misaligned4 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 3u) != 0; };
+  if (misaligned4(topk_ids) || misaligned4(expert_offsets) || misaligned4(dest_rows) ||
+      misaligned4(row_index) || misaligned4(status) || (workspace && !aligned16(workspace)))
+    return MXFP4_EALIGN;
+  const Range in = range_of(topk_ids, n * 4);
+  const Range outs[5] = {range_of(expert_offsets, (static_cast<int64_t>(E) + 1) * 4),
+                         range_of(dest_rows, n * 4), range_of(row_index, row_index ? n * 4 : 0),
+                         range_of(status, status ? 4 : 0),
+                         range_of(workspace, n > 0 ? ws_bytes : 0)};
+  for (int i = 0; i < 5; ++i) {
+    if (overlap(outs[i], in)) return MXFP4_EALIAS;
+    for (int j = i + 1; j < 5; ++j)
+      if (overlap(outs[i], outs[j])) return MXFP4_EALIAS;
+  }
+  return from_cuda(mxfp4::launch_moe_route(topk_ids, num_tokens, top_k, E,
+                                           static_cast<int32_t*>(workspace), expert_offsets,
+                                           dest_rows, row_index, status,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 int mxfp4_swap_w13(const uint8_t* codes_in, const uint8_t* scales_in, const float* w13_bias_in,
                    int32_t E, int64_t two_n, int64_t K, int32_t scales_tiled, uint8_t* codes_out,
                    uint8_t* scales_out, void* w13_bias_out, const float* w2_bias_in,
@@ -861,7 +897,7 @@ int64_t mxfp4_debug_bounds_violations(void) {
   return static_cast<int64_t>(mxfp4::debug_violations_quantize()) +
          mxfp4::debug_violations_dispatch() +
          mxfp4::debug_violations_dequantize() + mxfp4::debug_violations_nvfp4() +
-         mxfp4::debug_violations_swap();
+         mxfp4::debug_violations_swap() + mxfp4::debug_violations_route();
 }
 #endif
 

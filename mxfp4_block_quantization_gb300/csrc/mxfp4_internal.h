@@ -131,6 +131,14 @@ struct SwapArgs {
 
 cudaError_t launch_swap_w13(const SwapArgs& a, cudaStream_t stream);
 
+// The dispatch permutation from [num_tokens, top_k] expert ids: offsets
+// [E+1], dest [num_tokens * top_k] (-1: not dispatched), row_index [rows] or
+// NULL, status or NULL; workspace of route_workspace_ints(n, E) int32.
+int64_t route_workspace_ints(int64_t n, int64_t E);
+cudaError_t launch_moe_route(const int32_t* ids, int64_t num_tokens, int32_t top_k, int32_t E,
+                             int32_t* workspace, int32_t* offsets, int32_t* dest,
+                             int32_t* row_index, int32_t* status, cudaStream_t stream);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
@@ -142,6 +150,7 @@ unsigned int debug_violations_dispatch();
 unsigned int debug_violations_dequantize();
 unsigned int debug_violations_nvfp4();
 unsigned int debug_violations_swap();
+unsigned int debug_violations_route();
 #endif
 
 // Launch with programmatic dependent launch allowed: the grid may be

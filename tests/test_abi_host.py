@@ -441,3 +441,38 @@ def test_gather_workspace_bytes_is_zero_beyond_the_call_limits(lib):
     assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 1 << 38) == 0
     assert lib.mxfp4_gather_workspace_bytes(50, 10, 2, 1 << 20) > 0
     assert lib.mxfp4_gather_workspace_bytes((1 << 31) // 4 + 1, 10, 2, 64) == 0
+
+
+def test_route_validation(lib):
+    """mxfp4_moe_route refuses bad arguments before any device work."""
+    f = lib._lib.mxfp4_moe_route
+    ws_need = lib.mxfp4_route_workspace_bytes(300, 4, 13)
+    # 1200 routes: 5 chunks of 256 x (E + 1) counts and flags, and a 16-byte ticket
+    assert ws_need == (5 * 14 + 4) * 4
+    assert lib.mxfp4_route_workspace_bytes(16384, 8, 384) == (512 * 385 + 4) * 4
+    assert lib.mxfp4_route_workspace_bytes(10, 8, lib.MXFP4_ROUTE_MAX_EXPERTS + 1) == 0
+    assert lib.mxfp4_route_workspace_bytes(10, 0, 4) == 0
+    # ids, T, top_k, E, ws, ws_bytes, offsets, dest, rows, status, stream
+    ok = [A, 300, 4, 13, 8 * A, ws_need, 2 * A, 3 * A, 4 * A, 5 * A, None]
+
+    def call(**kw):
+        names = ["ids", "T", "k", "E", "ws", "wsb", "off", "dest", "rows", "st", "strm"]
+        a = dict(zip(names, ok))
+        a.update(kw)
+        return f(*[a[n] for n in names])
+
+    assert call(T=-1) == lib.MXFP4_EINVAL
+    assert call(k=0) == lib.MXFP4_EINVAL
+    assert call(E=0) == lib.MXFP4_EINVAL
+    assert call(E=lib.MXFP4_ROUTE_MAX_EXPERTS + 1) == lib.MXFP4_ESHAPE
+    assert call(T=(1 << 30), k=2) == lib.MXFP4_ESHAPE
+    assert call(ids=None) == lib.MXFP4_EINVAL
+    assert call(off=None) == lib.MXFP4_EINVAL
+    assert call(dest=None) == lib.MXFP4_EINVAL
+    assert call(ws=None) == lib.MXFP4_EINVAL
+    assert call(wsb=ws_need - 4) == lib.MXFP4_EINVAL
+    assert call(ws=8 * A + 8) == lib.MXFP4_EALIGN
+    assert call(dest=3 * A + 2) == lib.MXFP4_EALIGN
+    assert call(dest=A + 16) == lib.MXFP4_EALIAS          # dest_rows overlaps the ids
+    assert call(rows=3 * A + 64) == lib.MXFP4_EALIAS      # row_index overlaps dest_rows
+    assert call(st=2 * A + 4) == lib.MXFP4_EALIAS         # status inside the offsets

@@ -182,6 +182,16 @@ def test_everything_in_bounds(libs):
         b2 = torch.randn(E, 33, device="cuda")
         cases.append(lambda c=codes, s=scales, b13=b13, b2=b2, t=tiled:
                      mx.swap_w13(c, s, b13, b2, scales_tiled=t))
+    # the dispatch permutation from router ids: chunk boundaries, dropped and
+    # invalid ids, many experts
+    def route_case(ids, E):
+        off, dest, rows, st = mx.moe_route(ids, E)
+        return off, dest, rows[:int(off[-1])], st       # rows past the total are not written
+
+    rng = np.random.default_rng(12)
+    for T, k, E in [(1025, 1, 7), (300, 8, 384), (40, 2, 5000)]:
+        ids = torch.from_numpy(rng.integers(-1, E + 1, (T, k)).astype(np.int32)).cuda()
+        cases.append(lambda ids=ids, E=E: route_case(ids, E))
     for fn in cases:
         r, d = both(libs, fn)
         same(r, d)
