@@ -599,7 +599,7 @@ def measure_rows(mx, W, stream, peak, l2_bytes, sweep):
 
 DISPATCH_CALLS = ("gather", "gather_ws", "scatter", "scatter_ws", "nvfp4_scatter",
                   "nvfp4_scatter_ws", "nvfp4_scatter_ws_own_g")
-SINGLE_CALLS = DISPATCH_CALLS + ("dense", "w13", "route")
+SINGLE_CALLS = DISPATCH_CALLS + ("dense", "w13", "route", "dequant", "nvfp4_dequant")
 
 
 def run_one_call(args):
@@ -608,11 +608,44 @@ def run_one_call(args):
     (ncu -k on this command sees only its kernels).  NAME is a dispatch call
     on the MoE batch (16384 tokens x top-8 over 384 experts, K = 7168;
     nvfp4_scatter_ws_own_g with a global scale of its own per expert), the
-    dense quantize of the 4096 x 7168 activation, or the dense quantize of the
-    w13 expert weights [128 x 1536, 2048]."""
+    dense quantize of the 4096 x 7168 activation, the dense quantize of the
+    w13 expert weights [128 x 1536, 2048], or the MXFP4 / NVFP4 dequantize of
+    the quantized 4096 x 7168 activation (5 rotating input/output sets, 372 MB,
+    so that no call finds its operands in the L2)."""
     import torch
     import mxfp4_block_quantization_gb300 as mx
     import workloads as W
+    if args.call in ("dequant", "nvfp4_dequant"):
+        M, K, R = M_DENSE, K_DENSE, 5
+        x = W.dense_activation(1, M, K, device="cuda")
+        if args.call == "dequant":
+            codes, scales = mx.quantize(x)
+            nbytes = dequant_bytes(M, K)
+        else:
+            g_nv = torch.tensor([448.0 * 6.0 / float(x.float().abs().max())], device="cuda")
+            codes, scales = mx.quantize_nvfp4(x, g_nv)
+            nbytes = M * K // 2 + scales.numel() + 2 * M * K
+        del x
+        cs = [codes.clone() for _ in range(R)]
+        ss = [scales.clone() for _ in range(R)]
+        ys = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+        if args.call == "dequant":
+            fn = lambda i: mx.mxfp4_dequantize(cs[i % R], ss[i % R], M, K, ys[i % R])  # noqa: E731
+        else:
+            fn = lambda i: mx.mxfp4_dequantize_nvfp4(cs[i % R], ss[i % R], g_nv, M, K,  # noqa: E731
+                                                     ys[i % R])
+        fn(0)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(args.reps):
+            fn(i + 1)
+        t1.record()
+        torch.cuda.synchronize()
+        us = t0.elapsed_time(t1) * 1e3 / args.reps
+        print(json.dumps({"call": args.call, "reps": args.reps, "us_per_call": round(us, 2),
+                          "bytes_per_call": nbytes}))
+        return 0
     if args.call in ("dense", "w13"):
         if args.call == "dense":
             x = W.dense_activation(1, M_DENSE, K_DENSE, device="cuda")
