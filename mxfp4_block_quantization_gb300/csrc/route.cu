@@ -8,8 +8,9 @@
 // entries with an expert in [0, E), in order of expert and, within an expert,
 // of entry index (a stable counting sort); -1 marks a route that is not
 // dispatched, any other id outside [0, E) is not dispatched either and is
-// reported.  Four kernels, each a fixed function of the previous one's
-// output, with no waiting between CTAs:
+// reported.  Three kernels, each a fixed function of the previous one's
+// output, with no waiting between CTAs (with no entries at all, a memset and
+// route_expert_scan_kernel write the zero offsets and the status instead):
 //   1. route_count_kernel: one CTA per chunk of kRouteChunk entries counts
 //      its entries per expert (shared-memory atomics; the order of the adds
 //      does not matter) and flags an invalid id;
