@@ -185,6 +185,21 @@ def _need_cuda(name, t, dtype=None):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _need_bytes(name, t, nbytes):
+    """``t`` (if given) must be contiguous and hold at least ``nbytes`` bytes:
+    the library sees only its pointer and reads or writes the whole extent
+    the call's sizes imply, so a short or strided buffer is refused here,
+    before anything is launched.  ``nbytes`` <= 0 (sizes the library itself
+    rejects) checks contiguity only."""
+    if t is None:
+        return
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name} holds {have} bytes; this call needs {nbytes}")
+
+
 def _check(rc, where):
     if rc != MXFP4_OK:
         raise MXFP4Error(rc, where)
@@ -225,6 +240,8 @@ def mxfp4_quantize(x, codes, scales, stream=None) -> None:
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with unit column stride")
     M, K = x.shape
+    _need_bytes("codes", codes, M * (K // 2))
+    _need_bytes("scales", scales, mxfp4_scale_bytes(M, K))
     with torch.cuda.device(_device_of(x, codes, scales)):
         _check(_lib.mxfp4_quantize(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales),
                                    _stream(stream, x.device)), "mxfp4_quantize")
@@ -239,9 +256,22 @@ def mxfp4_quantize_f16(x, codes, scales, stream=None) -> None:
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with unit column stride")
     M, K = x.shape
+    _need_bytes("codes", codes, M * (K // 2))
+    _need_bytes("scales", scales, mxfp4_scale_bytes(M, K))
     with torch.cuda.device(_device_of(x, codes, scales)):
         _check(_lib.mxfp4_quantize_f16(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales),
                                        _stream(stream, x.device)), "mxfp4_quantize_f16")
+
+
+def _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status, rows, K,
+                          scale_bound):
+    """The buffers of a grouped call over ``rows`` expert-sorted rows."""
+    E = expert_offsets.numel() - 1
+    _need_bytes("expert_offsets", expert_offsets, 4 * (E + 1))
+    _need_bytes("codes", codes, rows * (K // 2))
+    _need_bytes("scales", scales, scale_bound(rows, E, K) if E >= 0 and rows >= 0 else 0)
+    _need_bytes("scale_row_offsets", scale_row_offsets, 4 * (E + 1))
+    _need_bytes("status", status, 4)
 
 
 def _grouped(x, expert_offsets, codes, scales, scale_row_offsets, status, stream, f16):
@@ -256,6 +286,8 @@ def _grouped(x, expert_offsets, codes, scales, scale_row_offsets, status, stream
         raise ValueError("x must be a contiguous 2-D tensor")
     total, K = x.shape
     E = expert_offsets.numel() - 1
+    _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status, total, K,
+                          mxfp4_grouped_scale_bytes_bound)
     with torch.cuda.device(_device_of(x, expert_offsets, codes, scales, scale_row_offsets, status)):
         _check(getattr(_lib, name)(_ptr(x), total, K, _ptr(expert_offsets), E, _ptr(codes),
                                    _ptr(scales), _ptr(scale_row_offsets), _ptr(status),
@@ -290,6 +322,8 @@ def _gather(x, row_index, expert_offsets, codes, scales, scale_row_offsets, stat
         raise ValueError("row_index must be contiguous")
     n_src, K = x.shape
     E = expert_offsets.numel() - 1
+    _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status,
+                          row_index.numel(), K, mxfp4_grouped_scale_bytes_bound)
     with torch.cuda.device(_device_of(x, row_index, expert_offsets, codes, scales,
                                       scale_row_offsets, status)):
         _check(getattr(_lib, name)(
@@ -333,6 +367,8 @@ def _gather_ws(x, row_index, expert_offsets, workspace, codes, scales, scale_row
         raise ValueError("row_index and workspace must be contiguous")
     n_src, K = x.shape
     E = expert_offsets.numel() - 1
+    _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status,
+                          row_index.numel(), K, mxfp4_grouped_scale_bytes_bound)
     with torch.cuda.device(_device_of(x, row_index, expert_offsets, workspace, codes, scales,
                                       scale_row_offsets, status)):
         _check(getattr(_lib, name)(
@@ -367,6 +403,8 @@ def mxfp4_quantize_grouped_gather_noalloc(x, row_index, expert_offsets, codes, s
         raise ValueError("row_index must be contiguous")
     n_src, K = x.shape
     E = expert_offsets.numel() - 1
+    _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status,
+                          row_index.numel(), K, mxfp4_grouped_scale_bytes_bound)
     with torch.cuda.device(_device_of(x, row_index, expert_offsets, codes, scales,
                                       scale_row_offsets, status)):
         _check(_lib.mxfp4_quantize_grouped_gather_noalloc(
@@ -400,6 +438,9 @@ def _scatter(x, dest_rows, expert_offsets, total_rows, codes, scales, scale_row_
         raise ValueError("dest_rows must be a contiguous [num_tokens, top_k] tensor")
     T, K = x.shape
     E = expert_offsets.numel() - 1
+    _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status,
+                          int(total_rows), K, mxfp4_grouped_scale_bytes_bound)
+    _need_bytes("workspace", workspace, 0)
     ws = () if workspace is None else (_ptr(workspace), workspace.numel())
     with torch.cuda.device(_device_of(x, dest_rows, expert_offsets, codes, scales,
                                       scale_row_offsets, status, workspace)):
@@ -471,6 +512,10 @@ def mxfp4_moe_route(topk_ids, num_experts: int, workspace, expert_offsets, dest_
     if dest_rows.shape != topk_ids.shape:
         raise ValueError("dest_rows must have the shape of topk_ids")
     T, top_k = topk_ids.shape
+    _need_bytes("workspace", workspace, 0)
+    _need_bytes("expert_offsets", expert_offsets, 4 * (int(num_experts) + 1))
+    _need_bytes("row_index", row_index, 4 * T * top_k)
+    _need_bytes("status", status, 4)
     with torch.cuda.device(_device_of(topk_ids, workspace, expert_offsets, dest_rows,
                                       row_index, status)):
         _check(_lib.mxfp4_moe_route(_ptr(topk_ids), T, top_k, int(num_experts), _ptr(workspace),
@@ -485,8 +530,10 @@ def mxfp4_dequantize(codes, scales, M: int, K: int, y, stream=None) -> None:
     _need_cuda("codes", codes, torch.uint8)
     _need_cuda("scales", scales, torch.uint8)
     _need_cuda("y", y, torch.bfloat16)
-    if not y.is_contiguous():
-        raise ValueError("y must be contiguous")
+    M, K = int(M), int(K)
+    _need_bytes("codes", codes, M * (K // 2))
+    _need_bytes("scales", scales, mxfp4_scale_bytes(M, K))
+    _need_bytes("y", y, 2 * M * K)
     with torch.cuda.device(_device_of(codes, scales, y)):
         _check(_lib.mxfp4_dequantize(_ptr(codes), _ptr(scales), int(M), int(K), _ptr(y),
                                      _stream(stream, y.device)), "mxfp4_dequantize")
@@ -507,6 +554,19 @@ def mxfp4_swap_w13(codes_in, scales_in, w13_bias_in, E: int, two_n: int, K: int,
     dev = _device_of(codes_in, scales_in, codes_out, scales_out, w13_bias_in, w13_bias_out,
                      w2_bias_in, w2_bias_out)
     n2 = w2_bias_in.numel() if w2_bias_in is not None else 0
+    E, two_n, K = int(E), int(two_n), int(K)
+    code_bytes = E * two_n * (K // 2)
+    scale_bytes = (E * mxfp4_scale_bytes(two_n, K) if scales_tiled else E * two_n * (K // 32))
+    _need_bytes("codes_in", codes_in, code_bytes)
+    _need_bytes("codes_out", codes_out, code_bytes)
+    _need_bytes("scales_in", scales_in, scale_bytes)
+    _need_bytes("scales_out", scales_out, scale_bytes)
+    _need_bytes("w13_bias_in", w13_bias_in, 4 * E * two_n)
+    if w13_bias_in is not None:
+        _need_bytes("w13_bias_out", w13_bias_out, 2 * E * two_n)
+    _need_bytes("w2_bias_in", w2_bias_in, 4 * n2)
+    if w2_bias_in is not None:
+        _need_bytes("w2_bias_out", w2_bias_out, 2 * n2)
     with torch.cuda.device(dev):
         _check(_lib.mxfp4_swap_w13(_ptr(codes_in), _ptr(scales_in), _ptr(w13_bias_in), int(E),
                                    int(two_n), int(K), int(scales_tiled), _ptr(codes_out),
@@ -527,6 +587,9 @@ def _nvfp4(x, global_scale, codes, scales, stream, f16) -> None:
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with unit column stride")
     M, K = x.shape
+    _need_bytes("global_scale", global_scale, 4)
+    _need_bytes("codes", codes, M * (K // 2))
+    _need_bytes("scales", scales, mxfp4_nvfp4_scale_bytes(M, K))
     with torch.cuda.device(_device_of(x, global_scale, codes, scales)):
         _check(getattr(_lib, name)(_ptr(x), M, K, x.stride(0), _ptr(global_scale), _ptr(codes),
                                    _ptr(scales), _stream(stream, x.device)), name)
@@ -563,6 +626,9 @@ def _nvfp4_grouped(x, expert_offsets, global_scales, codes, scales, scale_row_of
     E = expert_offsets.numel() - 1
     if global_scales.numel() != E:
         raise ValueError("global_scales needs one entry per expert")
+    _need_bytes("global_scales", global_scales, 4 * E)
+    _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status, total, K,
+                          mxfp4_nvfp4_grouped_scale_bytes_bound)
     with torch.cuda.device(_device_of(x, expert_offsets, global_scales, codes, scales,
                                       scale_row_offsets, status)):
         _check(getattr(_lib, name)(
@@ -606,6 +672,10 @@ def _nvfp4_scatter(x, dest_rows, expert_offsets, total_rows, global_scales, code
     E = expert_offsets.numel() - 1
     if global_scales.numel() != E:
         raise ValueError("global_scales needs one entry per expert")
+    _need_bytes("global_scales", global_scales, 4 * E)
+    _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status,
+                          int(total_rows), K, mxfp4_nvfp4_grouped_scale_bytes_bound)
+    _need_bytes("workspace", workspace, 0)
     ws = () if workspace is None else (_ptr(workspace), workspace.numel())
     with torch.cuda.device(_device_of(x, dest_rows, expert_offsets, global_scales, codes, scales,
                                       scale_row_offsets, status, workspace)):
@@ -661,8 +731,11 @@ def mxfp4_dequantize_nvfp4(codes, scales, global_scale, M: int, K: int, y, strea
     _need_cuda("scales", scales, torch.uint8)
     _need_cuda("global_scale", global_scale, torch.float32)
     _need_cuda("y", y, torch.bfloat16)
-    if not y.is_contiguous():
-        raise ValueError("y must be contiguous")
+    M, K = int(M), int(K)
+    _need_bytes("global_scale", global_scale, 4)
+    _need_bytes("codes", codes, M * (K // 2))
+    _need_bytes("scales", scales, mxfp4_nvfp4_scale_bytes(M, K))
+    _need_bytes("y", y, 2 * M * K)
     with torch.cuda.device(_device_of(codes, scales, global_scale, y)):
         _check(_lib.mxfp4_dequantize_nvfp4(_ptr(codes), _ptr(scales), _ptr(global_scale), int(M),
                                            int(K), _ptr(y), _stream(stream, y.device)),
