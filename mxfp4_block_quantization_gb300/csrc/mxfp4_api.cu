@@ -121,19 +121,30 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int64_t padded_scale_cols(int64_t K) { return ceil_div(K / 32, 4) * 4; }
 
+// Byte count of `rows` rows of `cols` scale bytes for a size query, or 0 when
+// it does not fit in int64 (no call accepts such sizes).
+size_t rows_times_cols(int64_t rows, int64_t cols) {
+  int64_t r = 0;
+  return __builtin_mul_overflow(rows, cols, &r) ? 0 : static_cast<size_t>(r);
+}
+
+// Row counts above this are rejected by every call; the size queries return
+// 0 for them instead of wrapping around.
+constexpr int64_t kMaxRows = INT64_MAX / 4;
+
 }  // namespace
 
 extern "C" {
 
 size_t mxfp4_scale_bytes(int64_t M, int64_t K) {
-  if (M <= 0 || K <= 0 || K % 32 != 0) return 0;
-  return static_cast<size_t>(ceil_div(M, 128) * 128 * padded_scale_cols(K));
+  if (M <= 0 || K <= 0 || K % 32 != 0 || M > kMaxRows) return 0;
+  return rows_times_cols(ceil_div(M, 128) * 128, padded_scale_cols(K));
 }
 
 size_t mxfp4_grouped_scale_bytes_bound(int64_t total_rows, int32_t E, int64_t K) {
-  if (total_rows < 0 || E < 0 || K <= 0 || K % 32 != 0) return 0;
+  if (total_rows < 0 || E < 0 || K <= 0 || K % 32 != 0 || total_rows > kMaxRows) return 0;
   const int64_t tiles = (total_rows + 127 * static_cast<int64_t>(E)) / 128;
-  return static_cast<size_t>(tiles * 128 * padded_scale_cols(K));
+  return rows_times_cols(tiles * 128, padded_scale_cols(K));
 }
 
 }  // extern "C"
@@ -468,6 +479,8 @@ size_t mxfp4_scatter_workspace_bytes(int64_t num_tokens, int64_t total_rows, int
   if (num_tokens < 0 || total_rows < 0 || E < 0 || K < 0 || K % 32 != 0) return 0;
   if (num_tokens > INT32_MAX / 4 || total_rows + 127 * static_cast<int64_t>(E) > INT32_MAX)
     return 0;
+  // the k-tile bound the calls apply (the staged rows count k tiles in int)
+  if (ceil_div(K / 32, 4) > kMaxGrid) return 0;
   return static_cast<size_t>(mxfp4::scatter_workspace_ints(num_tokens, total_rows, E, K) * 4);
 }
 
@@ -612,8 +625,8 @@ int mxfp4_swap_w13(const uint8_t* codes_in, const uint8_t* scales_in, const floa
 }
 
 size_t mxfp4_nvfp4_scale_bytes(int64_t M, int64_t K) {
-  if (M <= 0 || K <= 0 || K % 16 != 0) return 0;
-  return static_cast<size_t>(ceil_div(M, 128) * 128 * ceil_div(K / 16, 4) * 4);
+  if (M <= 0 || K <= 0 || K % 16 != 0 || M > kMaxRows) return 0;
+  return rows_times_cols(ceil_div(M, 128) * 128, ceil_div(K / 16, 4) * 4);
 }
 
 }  // extern "C"
@@ -659,9 +672,9 @@ int mxfp4_quantize_nvfp4_f16(const void* x, int64_t M, int64_t K, int64_t ldx,
 }
 
 size_t mxfp4_nvfp4_grouped_scale_bytes_bound(int64_t total_rows, int32_t E, int64_t K) {
-  if (total_rows < 0 || E < 0 || K <= 0 || K % 16 != 0) return 0;
+  if (total_rows < 0 || E < 0 || K <= 0 || K % 16 != 0 || total_rows > kMaxRows) return 0;
   const int64_t tiles = (total_rows + 127 * static_cast<int64_t>(E)) / 128;
-  return static_cast<size_t>(tiles * 128 * ceil_div(K / 16, 4) * 4);
+  return rows_times_cols(tiles * 128, ceil_div(K / 16, 4) * 4);
 }
 
 }  // extern "C"
@@ -821,6 +834,7 @@ int mxfp4_quantize_nvfp4_grouped_scatter_f16(const void* x, int64_t num_tokens, 
 size_t mxfp4_nvfp4_scatter_workspace_bytes(int64_t total_rows, int32_t E, int64_t K) {
   if (total_rows < 0 || E < 0 || K < 0 || K % 16 != 0) return 0;
   if (total_rows + 127 * static_cast<int64_t>(E) > INT32_MAX) return 0;
+  if (ceil_div(K / 16, 4) > kMaxGrid) return 0;  // as the calls: k tiles counted in int
   return static_cast<size_t>(mxfp4::nvfp4_scatter_workspace_ints(total_rows, E, K) * 4);
 }
 

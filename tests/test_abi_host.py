@@ -476,3 +476,25 @@ def test_route_validation(lib):
     assert call(dest=A + 16) == lib.MXFP4_EALIAS          # dest_rows overlaps the ids
     assert call(rows=3 * A + 64) == lib.MXFP4_EALIAS      # row_index overlaps dest_rows
     assert call(st=2 * A + 4) == lib.MXFP4_EALIAS         # status inside the offsets
+
+
+def test_size_queries_return_zero_instead_of_wrapping(lib):
+    """Every size query answers 0 for sizes whose byte count would not fit in
+    int64, or whose k tiles the calls cannot count, instead of a wrapped or
+    truncated size; ordinary sizes are unchanged."""
+    big_rows, big_k = 1 << 62, 1 << 40
+    assert lib.mxfp4_scale_bytes(big_rows, 1024) == 0
+    assert lib.mxfp4_scale_bytes(1 << 40, 1 << 30) == 0            # rows x cols overflows
+    assert lib.mxfp4_grouped_scale_bytes_bound(big_rows, 4, 1024) == 0
+    assert lib.mxfp4_grouped_scale_bytes_bound(1 << 40, 4, 1 << 30) == 0
+    assert lib.mxfp4_nvfp4_scale_bytes(big_rows, 1024) == 0
+    assert lib.mxfp4_nvfp4_scale_bytes(1 << 40, 1 << 30) == 0
+    assert lib.mxfp4_nvfp4_grouped_scale_bytes_bound(1 << 40, 4, 1 << 30) == 0
+    assert lib.mxfp4_scatter_workspace_bytes(100, 400, 2, big_k) == 0
+    assert lib.mxfp4_nvfp4_scatter_workspace_bytes(400, 2, big_k) == 0
+    assert lib.mxfp4_gather_workspace_bytes(100, 400, 2, big_k) == 0
+    # ordinary sizes: 4096 x 7168 -> 4096 rows x 224 (MXFP4) / 448 (NVFP4) scale bytes
+    assert lib.mxfp4_scale_bytes(4096, 7168) == 4096 * 224
+    assert lib.mxfp4_nvfp4_scale_bytes(4096, 7168) == 4096 * 448
+    assert lib.mxfp4_grouped_scale_bytes_bound(131072, 384, 7168) == \
+        (131072 + 127 * 384) // 128 * 128 * 224
