@@ -148,6 +148,16 @@ class ClockSampler:
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
 
+    def wait_first(self, timeout=15.0):
+        """Until the first sample arrives (nvidia-smi can take a second or more
+        to start on a fresh box), at most `timeout` seconds: the settle period
+        that follows is then sampled from its start."""
+        t_end = time.time() + timeout
+        while self.proc is not None and not self.samples and time.time() < t_end:
+            if self.proc.poll() is not None:
+                return
+            time.sleep(0.02)
+
     def _read(self):
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
@@ -342,6 +352,35 @@ def time_batches(fn, stream, sweep, per_batch, batches, warmup=3):
     return sum(per) / len(per), statistics.median(per)
 
 
+def time_graph_batches(fn, stream, sweep, per_batch, batches, warmup=3):
+    """time_batches with each batch captured once as a CUDA graph of its
+    `per_batch` calls fn(i) on `stream` (not the default stream) and replayed
+    after an L2 sweep: the host's per-call cost (the binding's argument checks
+    and ctypes, 8-19 us a call) is then not in the time, which is the device
+    time of the calls alone.  Returns (mean, median) milliseconds per call."""
+    import torch
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(per_batch):
+            fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(batches)]
+    for s_, e_ in evs:
+        sweep()
+        s_.record(stream)
+        g.replay()
+        e_.record(stream)
+    torch.cuda.synchronize()
+    per = [s_.elapsed_time(e_) / per_batch for s_, e_ in evs]
+    del g
+    return sum(per) / len(per), statistics.median(per)
+
+
 def tiled_scale_index(M, K, device="cpu"):
     """[M, K/32] byte offsets of the scale bytes in the 128x4-tiled layout:
     chunk (r/128, c/4) of 512 bytes, byte (r%32)*16 + ((r%128)/32)*4 + c%4."""
@@ -405,9 +444,24 @@ ROW_FIELDS = ["GB/s", "frac of measured peak", "mean us", "median us"]
 def measure_rows(mx, W, stream, peak, l2_bytes, sweep):
     """Each remaining hot-path row on its own workload (device time, inputs
     resident in HBM, operands rotated or larger than L2, an L2 sweep before
-    each timed batch).  Every row is [GB/s, fraction of the peak, mean us,
-    median us] over the row's algorithmic bytes; `extra` holds the unfused
-    baselines the fused dispatch calls are compared with."""
+    each timed batch, each batch a CUDA graph of its calls).  Every row is
+    [GB/s, fraction of the peak, mean us, median us] over the row's
+    algorithmic bytes; `extra` holds the unfused baselines the fused dispatch
+    calls are compared with.  Runs on a stream of its own (graphs are not
+    captured on the default stream); `stream` is replaced by it."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    prev = torch.cuda.current_stream()
+    torch.cuda.set_stream(side)
+    try:
+        return _measure_rows(mx, W, side, peak, l2_bytes, sweep)
+    finally:
+        torch.cuda.synchronize()
+        torch.cuda.set_stream(prev)
+
+
+def _measure_rows(mx, W, stream, peak, l2_bytes, sweep):
     import torch
     rows, extra = {}, {}
 
@@ -418,7 +472,7 @@ def measure_rows(mx, W, stream, peak, l2_bytes, sweep):
                       round(med * 1e3, 2)]
 
     def tb(fn, per_batch, batches=5):
-        return time_batches(fn, stream, sweep, per_batch, batches)
+        return time_graph_batches(fn, stream, sweep, per_batch, batches)
 
     # dequantize 4096 x 7168 (rotate buffers beyond 2x L2)
     M, K = M_DENSE, K_DENSE
@@ -779,6 +833,7 @@ def run_ours(args):
     sweep = L2Sweep(l2_bytes, dev)
     clocks = ClockSampler(local)
     clocks.start()
+    clocks.wait_first()
     for i in range(args.warmup):
         sweep()                       # its first calls carry torch's one-time host work
         step(i)

@@ -19,6 +19,7 @@ conversion for FlashInfer CUTLASS" ([w1; w3] -> [w3; w1] swap, BF16 bias);
 PR #46915 "Fix the SM90 MXFP4 MoE test weight/scale interleave" (FP4 -> BF16
 table read back).
 """
+import contextlib
 import ctypes
 import os
 
@@ -214,6 +215,15 @@ def _device_of(*tensors):
     return devs.pop()
 
 
+def _switch(device):
+    """The library launches on the current device: make ``device`` current for
+    the call, or do nothing when it already is (the usual case, and a
+    measurable share of a call's host time)."""
+    if device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
 # ------------------------------------------------------- C entry points
 def mxfp4_scale_bytes(M: int, K: int) -> int:
     return int(_lib.mxfp4_scale_bytes(int(M), int(K)))
@@ -242,7 +252,7 @@ def mxfp4_quantize(x, codes, scales, stream=None) -> None:
     M, K = x.shape
     _need_bytes("codes", codes, M * (K // 2))
     _need_bytes("scales", scales, mxfp4_scale_bytes(M, K))
-    with torch.cuda.device(_device_of(x, codes, scales)):
+    with _switch(_device_of(x, codes, scales)):
         _check(_lib.mxfp4_quantize(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales),
                                    _stream(stream, x.device)), "mxfp4_quantize")
 
@@ -258,7 +268,7 @@ def mxfp4_quantize_f16(x, codes, scales, stream=None) -> None:
     M, K = x.shape
     _need_bytes("codes", codes, M * (K // 2))
     _need_bytes("scales", scales, mxfp4_scale_bytes(M, K))
-    with torch.cuda.device(_device_of(x, codes, scales)):
+    with _switch(_device_of(x, codes, scales)):
         _check(_lib.mxfp4_quantize_f16(_ptr(x), M, K, x.stride(0), _ptr(codes), _ptr(scales),
                                        _stream(stream, x.device)), "mxfp4_quantize_f16")
 
@@ -288,7 +298,7 @@ def _grouped(x, expert_offsets, codes, scales, scale_row_offsets, status, stream
     E = expert_offsets.numel() - 1
     _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status, total, K,
                           mxfp4_grouped_scale_bytes_bound)
-    with torch.cuda.device(_device_of(x, expert_offsets, codes, scales, scale_row_offsets, status)):
+    with _switch(_device_of(x, expert_offsets, codes, scales, scale_row_offsets, status)):
         _check(getattr(_lib, name)(_ptr(x), total, K, _ptr(expert_offsets), E, _ptr(codes),
                                    _ptr(scales), _ptr(scale_row_offsets), _ptr(status),
                                    _stream(stream, x.device)), name)
@@ -324,7 +334,7 @@ def _gather(x, row_index, expert_offsets, codes, scales, scale_row_offsets, stat
     E = expert_offsets.numel() - 1
     _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status,
                           row_index.numel(), K, mxfp4_grouped_scale_bytes_bound)
-    with torch.cuda.device(_device_of(x, row_index, expert_offsets, codes, scales,
+    with _switch(_device_of(x, row_index, expert_offsets, codes, scales,
                                       scale_row_offsets, status)):
         _check(getattr(_lib, name)(
             _ptr(x), n_src, K, x.stride(0), _ptr(row_index), row_index.numel(),
@@ -369,7 +379,7 @@ def _gather_ws(x, row_index, expert_offsets, workspace, codes, scales, scale_row
     E = expert_offsets.numel() - 1
     _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status,
                           row_index.numel(), K, mxfp4_grouped_scale_bytes_bound)
-    with torch.cuda.device(_device_of(x, row_index, expert_offsets, workspace, codes, scales,
+    with _switch(_device_of(x, row_index, expert_offsets, workspace, codes, scales,
                                       scale_row_offsets, status)):
         _check(getattr(_lib, name)(
             _ptr(x), n_src, K, x.stride(0), _ptr(row_index), row_index.numel(),
@@ -405,7 +415,7 @@ def mxfp4_quantize_grouped_gather_noalloc(x, row_index, expert_offsets, codes, s
     E = expert_offsets.numel() - 1
     _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status,
                           row_index.numel(), K, mxfp4_grouped_scale_bytes_bound)
-    with torch.cuda.device(_device_of(x, row_index, expert_offsets, codes, scales,
+    with _switch(_device_of(x, row_index, expert_offsets, codes, scales,
                                       scale_row_offsets, status)):
         _check(_lib.mxfp4_quantize_grouped_gather_noalloc(
             _ptr(x), n_src, K, x.stride(0), _ptr(row_index), row_index.numel(),
@@ -442,7 +452,7 @@ def _scatter(x, dest_rows, expert_offsets, total_rows, codes, scales, scale_row_
                           int(total_rows), K, mxfp4_grouped_scale_bytes_bound)
     _need_bytes("workspace", workspace, 0)
     ws = () if workspace is None else (_ptr(workspace), workspace.numel())
-    with torch.cuda.device(_device_of(x, dest_rows, expert_offsets, codes, scales,
+    with _switch(_device_of(x, dest_rows, expert_offsets, codes, scales,
                                       scale_row_offsets, status, workspace)):
         _check(getattr(_lib, name)(
             _ptr(x), T, K, x.stride(0), _ptr(dest_rows), dest_rows.shape[1], int(total_rows),
@@ -516,7 +526,7 @@ def mxfp4_moe_route(topk_ids, num_experts: int, workspace, expert_offsets, dest_
     _need_bytes("expert_offsets", expert_offsets, 4 * (int(num_experts) + 1))
     _need_bytes("row_index", row_index, 4 * T * top_k)
     _need_bytes("status", status, 4)
-    with torch.cuda.device(_device_of(topk_ids, workspace, expert_offsets, dest_rows,
+    with _switch(_device_of(topk_ids, workspace, expert_offsets, dest_rows,
                                       row_index, status)):
         _check(_lib.mxfp4_moe_route(_ptr(topk_ids), T, top_k, int(num_experts), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(),
@@ -534,7 +544,7 @@ def mxfp4_dequantize(codes, scales, M: int, K: int, y, stream=None) -> None:
     _need_bytes("codes", codes, M * (K // 2))
     _need_bytes("scales", scales, mxfp4_scale_bytes(M, K))
     _need_bytes("y", y, 2 * M * K)
-    with torch.cuda.device(_device_of(codes, scales, y)):
+    with _switch(_device_of(codes, scales, y)):
         _check(_lib.mxfp4_dequantize(_ptr(codes), _ptr(scales), int(M), int(K), _ptr(y),
                                      _stream(stream, y.device)), "mxfp4_dequantize")
 
@@ -567,7 +577,7 @@ def mxfp4_swap_w13(codes_in, scales_in, w13_bias_in, E: int, two_n: int, K: int,
     _need_bytes("w2_bias_in", w2_bias_in, 4 * n2)
     if w2_bias_in is not None:
         _need_bytes("w2_bias_out", w2_bias_out, 2 * n2)
-    with torch.cuda.device(dev):
+    with _switch(dev):
         _check(_lib.mxfp4_swap_w13(_ptr(codes_in), _ptr(scales_in), _ptr(w13_bias_in), int(E),
                                    int(two_n), int(K), int(scales_tiled), _ptr(codes_out),
                                    _ptr(scales_out), _ptr(w13_bias_out), _ptr(w2_bias_in), n2,
@@ -590,7 +600,7 @@ def _nvfp4(x, global_scale, codes, scales, stream, f16) -> None:
     _need_bytes("global_scale", global_scale, 4)
     _need_bytes("codes", codes, M * (K // 2))
     _need_bytes("scales", scales, mxfp4_nvfp4_scale_bytes(M, K))
-    with torch.cuda.device(_device_of(x, global_scale, codes, scales)):
+    with _switch(_device_of(x, global_scale, codes, scales)):
         _check(getattr(_lib, name)(_ptr(x), M, K, x.stride(0), _ptr(global_scale), _ptr(codes),
                                    _ptr(scales), _stream(stream, x.device)), name)
 
@@ -629,7 +639,7 @@ def _nvfp4_grouped(x, expert_offsets, global_scales, codes, scales, scale_row_of
     _need_bytes("global_scales", global_scales, 4 * E)
     _need_grouped_outputs(expert_offsets, codes, scales, scale_row_offsets, status, total, K,
                           mxfp4_nvfp4_grouped_scale_bytes_bound)
-    with torch.cuda.device(_device_of(x, expert_offsets, global_scales, codes, scales,
+    with _switch(_device_of(x, expert_offsets, global_scales, codes, scales,
                                       scale_row_offsets, status)):
         _check(getattr(_lib, name)(
             _ptr(x), total, K, _ptr(expert_offsets), E, _ptr(global_scales), _ptr(codes),
@@ -677,7 +687,7 @@ def _nvfp4_scatter(x, dest_rows, expert_offsets, total_rows, global_scales, code
                           int(total_rows), K, mxfp4_nvfp4_grouped_scale_bytes_bound)
     _need_bytes("workspace", workspace, 0)
     ws = () if workspace is None else (_ptr(workspace), workspace.numel())
-    with torch.cuda.device(_device_of(x, dest_rows, expert_offsets, global_scales, codes, scales,
+    with _switch(_device_of(x, dest_rows, expert_offsets, global_scales, codes, scales,
                                       scale_row_offsets, status, workspace)):
         _check(getattr(_lib, name)(
             _ptr(x), T, K, x.stride(0), _ptr(dest_rows), dest_rows.shape[1], int(total_rows),
@@ -736,7 +746,7 @@ def mxfp4_dequantize_nvfp4(codes, scales, global_scale, M: int, K: int, y, strea
     _need_bytes("codes", codes, M * (K // 2))
     _need_bytes("scales", scales, mxfp4_nvfp4_scale_bytes(M, K))
     _need_bytes("y", y, 2 * M * K)
-    with torch.cuda.device(_device_of(codes, scales, global_scale, y)):
+    with _switch(_device_of(codes, scales, global_scale, y)):
         _check(_lib.mxfp4_dequantize_nvfp4(_ptr(codes), _ptr(scales), _ptr(global_scale), int(M),
                                            int(K), _ptr(y), _stream(stream, y.device)),
                "mxfp4_dequantize_nvfp4")
