@@ -21,6 +21,7 @@ table read back).
 """
 import contextlib
 import ctypes
+import functools
 import os
 
 import torch
@@ -171,10 +172,17 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# The current stream's raw handle without building a torch Stream object (a
+# measurable share of a call's host time); the public path where torch lacks it.
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream, device):
-    if stream is None:
-        stream = torch.cuda.current_stream(device)
-    return ctypes.c_void_p(stream.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_current_stream is not None:
+        return ctypes.c_void_p(_raw_current_stream(device.index))
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
 def _need_cuda(name, t, dtype=None):
@@ -209,10 +217,18 @@ def _check(rc, where):
 def _device_of(*tensors):
     """The one CUDA device all given tensors live on (the library launches on
     the current device, so every call switches to it)."""
-    devs = {t.device for t in tensors if t is not None}
-    if len(devs) != 1:
-        raise ValueError(f"all tensors must be on the same CUDA device, got {sorted(map(str, devs))}")
-    return devs.pop()
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            devs = sorted({str(u.device) for u in tensors if u is not None})
+            raise ValueError(f"all tensors must be on the same CUDA device, got {devs}")
+    if dev is None:
+        raise ValueError("no tensor given")
+    return dev
 
 
 def _switch(device):
@@ -225,10 +241,12 @@ def _switch(device):
 
 
 # ------------------------------------------------------- C entry points
+@functools.lru_cache(maxsize=1024)
 def mxfp4_scale_bytes(M: int, K: int) -> int:
     return int(_lib.mxfp4_scale_bytes(int(M), int(K)))
 
 
+@functools.lru_cache(maxsize=1024)
 def mxfp4_grouped_scale_bytes_bound(total_rows: int, E: int, K: int) -> int:
     return int(_lib.mxfp4_grouped_scale_bytes_bound(int(total_rows), int(E), int(K)))
 
@@ -355,6 +373,7 @@ def mxfp4_quantize_grouped_gather_f16(x, row_index, expert_offsets, codes, scale
     _gather(x, row_index, expert_offsets, codes, scales, scale_row_offsets, status, stream, True)
 
 
+@functools.lru_cache(maxsize=1024)
 def mxfp4_gather_workspace_bytes(num_src_rows: int, total_rows: int, E: int, K: int) -> int:
     return int(_lib.mxfp4_gather_workspace_bytes(int(num_src_rows), int(total_rows), int(E),
                                                  int(K)))
@@ -478,6 +497,7 @@ def mxfp4_quantize_grouped_scatter_f16(x, dest_rows, expert_offsets, total_rows:
              stream, True)
 
 
+@functools.lru_cache(maxsize=1024)
 def mxfp4_scatter_workspace_bytes(num_tokens: int, total_rows: int, E: int, K: int) -> int:
     return int(_lib.mxfp4_scatter_workspace_bytes(int(num_tokens), int(total_rows), int(E),
                                                   int(K)))
@@ -501,6 +521,7 @@ def mxfp4_quantize_grouped_scatter_ws_f16(x, dest_rows, expert_offsets, total_ro
              stream, True, workspace)
 
 
+@functools.lru_cache(maxsize=1024)
 def mxfp4_route_workspace_bytes(num_tokens: int, top_k: int, E: int) -> int:
     return int(_lib.mxfp4_route_workspace_bytes(int(num_tokens), int(top_k), int(E)))
 
@@ -584,6 +605,7 @@ def mxfp4_swap_w13(codes_in, scales_in, w13_bias_in, E: int, two_n: int, K: int,
                                    _ptr(w2_bias_out), _stream(stream, dev)), "mxfp4_swap_w13")
 
 
+@functools.lru_cache(maxsize=1024)
 def mxfp4_nvfp4_scale_bytes(M: int, K: int) -> int:
     return int(_lib.mxfp4_nvfp4_scale_bytes(int(M), int(K)))
 
@@ -616,6 +638,7 @@ def mxfp4_quantize_nvfp4_f16(x, global_scale, codes, scales, stream=None) -> Non
     _nvfp4(x, global_scale, codes, scales, stream, True)
 
 
+@functools.lru_cache(maxsize=1024)
 def mxfp4_nvfp4_grouped_scale_bytes_bound(total_rows: int, E: int, K: int) -> int:
     return int(_lib.mxfp4_nvfp4_grouped_scale_bytes_bound(int(total_rows), int(E), int(K)))
 
@@ -713,6 +736,7 @@ def mxfp4_quantize_nvfp4_grouped_scatter_f16(x, dest_rows, expert_offsets, total
                    scale_row_offsets, status, stream, True)
 
 
+@functools.lru_cache(maxsize=1024)
 def mxfp4_nvfp4_scatter_workspace_bytes(total_rows: int, E: int, K: int) -> int:
     return int(_lib.mxfp4_nvfp4_scatter_workspace_bytes(int(total_rows), int(E), int(K)))
 
