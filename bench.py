@@ -653,7 +653,8 @@ def _measure_rows(mx, W, stream, peak, l2_bytes, sweep):
 
 DISPATCH_CALLS = ("gather", "gather_ws", "scatter", "scatter_ws", "nvfp4_scatter",
                   "nvfp4_scatter_ws", "nvfp4_scatter_ws_own_g")
-SINGLE_CALLS = DISPATCH_CALLS + ("dense", "w13", "route", "dequant", "nvfp4_dequant")
+SINGLE_CALLS = DISPATCH_CALLS + ("dense", "w13", "route", "dequant", "nvfp4_dequant", "grouped",
+                                  "swap")
 
 
 def run_one_call(args):
@@ -665,7 +666,10 @@ def run_one_call(args):
     dense quantize of the 4096 x 7168 activation, the dense quantize of the
     w13 expert weights [128 x 1536, 2048], or the MXFP4 / NVFP4 dequantize of
     the quantized 4096 x 7168 activation (5 rotating input/output sets, 372 MB,
-    so that no call finds its operands in the L2)."""
+    so that no call finds its operands in the L2), the grouped quantize of the
+    expert-sorted MoE batch (131072 x 7168, 384 experts), or the w13 swap of
+    the quantized expert weights (128 experts, 2N = 1536, K = 2048, tiled
+    scales and both biases)."""
     import torch
     import mxfp4_block_quantization_gb300 as mx
     import workloads as W
@@ -698,6 +702,28 @@ def run_one_call(args):
         torch.cuda.synchronize()
         us = t0.elapsed_time(t1) * 1e3 / args.reps
         print(json.dumps({"call": args.call, "reps": args.reps, "us_per_call": round(us, 2),
+                          "bytes_per_call": nbytes}))
+        return 0
+    if args.call == "swap":
+        w = W.expert_weights(3, device="cuda")
+        E, two_n, H = w.w13.shape
+        c13, s13 = mx.quantize(w.w13.view(E * two_n, H))
+        c_o, s_o = torch.empty_like(c13), torch.empty_like(s13)
+        b13 = torch.empty(w.w13_bias.shape, dtype=torch.bfloat16, device="cuda")
+        b2 = torch.empty(w.w2_bias.shape, dtype=torch.bfloat16, device="cuda")
+        nbytes = 2 * (c13.numel() + s13.numel()) + 6 * (w.w13_bias.numel() + w.w2_bias.numel())
+        fn = lambda: mx.mxfp4_swap_w13(c13, s13, w.w13_bias, E, two_n, H, 1, c_o, s_o,  # noqa: E731
+                                       b13, w.w2_bias, b2)
+        fn()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.reps):
+            fn()
+        t1.record()
+        torch.cuda.synchronize()
+        us = t0.elapsed_time(t1) * 1e3 / args.reps
+        print(json.dumps({"call": "swap", "reps": args.reps, "us_per_call": round(us, 2),
                           "bytes_per_call": nbytes}))
         return 0
     if args.call in ("dense", "w13"):
@@ -762,6 +788,7 @@ def run_one_call(args):
     ws = (torch.empty(ws_bytes[args.call](), dtype=torch.uint8, device="cuda")
           if args.call in ws_bytes else None)
     fn = {
+        "grouped": lambda: mx.mxfp4_quantize_grouped(g.x, g.offsets, codes, scales, sro, st),
         "gather": lambda: mx.mxfp4_quantize_grouped_gather(g.x_tokens, g.row_index, g.offsets,
                                                            codes, scales, sro, st),
         "gather_ws": lambda: mx.mxfp4_quantize_grouped_gather_ws(
