@@ -1,7 +1,10 @@
 """Seeded random cases across every quantize form, each compared with the
 oracle byte for byte: random row counts, K, row strides, 16- versus 32-byte
 alignment, BF16 / FP16, expert segment sizes (empty ones included), routings
-with dropped routes, top_k, and NVFP4 global scales."""
+with dropped routes, top_k, and NVFP4 global scales.  MXFP4_FUZZ_SCALE=n
+(default 1) runs n times as many seeds of each kind."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -10,6 +13,8 @@ import oracle
 import workloads as W
 
 pytestmark = pytest.mark.gpu
+
+SCALE = max(1, int(os.environ.get("MXFP4_FUZZ_SCALE", "1")))
 
 
 @pytest.fixture(scope="module")
@@ -41,7 +46,7 @@ def _random_x(rng, M, K, f16):
     return x.to(torch.float16 if f16 else torch.bfloat16).cuda()
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(12 * SCALE))
 def test_fuzz_dense(mx, seed):
     rng = np.random.default_rng(100 + seed)
     M, K = int(rng.integers(1, 700)), 32 * int(rng.integers(1, 100))
@@ -62,7 +67,7 @@ def _random_offsets(rng, E, total):
     return np.concatenate([[0], cuts, [total]]).astype(np.int32)
 
 
-@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("seed", range(8 * SCALE))
 def test_fuzz_grouped_gather_scatter(mx, seed):
     rng = np.random.default_rng(200 + seed)
     T, top_k = int(rng.integers(1, 400)), int(rng.integers(1, 13))
@@ -151,7 +156,7 @@ def test_fuzz_grouped_gather_scatter(mx, seed):
         assert np.array_equal(s[:used].cpu().numpy(), sg_o[:used]), via
 
 
-@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("seed", range(6 * SCALE))
 def test_fuzz_nvfp4(mx, seed):
     rng = np.random.default_rng(300 + seed)
     M, K = int(rng.integers(1, 500)), 16 * int(rng.integers(1, 120))
