@@ -178,3 +178,40 @@ def test_fuzz_nvfp4(mx, seed):
         used = int(sro_o[-1]) * ((K // 16 + 3) // 4 * 4)
         assert np.array_equal(cg.cpu().numpy(), cg_o)
         assert np.array_equal(sg[:used].cpu().numpy(), sg_o[:used])
+
+
+@pytest.mark.parametrize("seed", range(8 * SCALE))
+def test_fuzz_route(mx, seed):
+    """Random routings: token count, top_k, number of experts (up to the
+    largest the call accepts), skewed expert popularity, dropped routes and
+    ids outside [0, E); offsets, token -> rows, row -> token and the status
+    word against the oracle, guard words after every output untouched."""
+    rng = np.random.default_rng(900 + seed)
+    T = int(rng.integers(0, 3000))
+    k = int(rng.integers(1, 33))
+    E = int(rng.choice([1, 2, 7, 64, 384, 1000, mx.MXFP4_ROUTE_MAX_EXPERTS]))
+    popular = rng.zipf(1.5, (T, k)) - 1 if seed % 2 else rng.integers(0, E, (T, k))
+    ids = (np.asarray(popular) % E).astype(np.int32)
+    ids[rng.random((T, k)) < 0.05] = -1
+    if seed % 4 == 3 and ids.size:
+        ids.flat[int(rng.integers(0, ids.size))] = E + int(rng.integers(0, 5))  # invalid id
+    with_rows = seed % 3 != 2
+    g = torch.full((E + 1 + 64,), -5, dtype=torch.int32, device="cuda")
+    dest = torch.full((T * k + 64,), -5, dtype=torch.int32, device="cuda")
+    rows = torch.full((T * k + 64,), -5, dtype=torch.int32, device="cuda")
+    st = torch.full((1,), -5, dtype=torch.int32, device="cuda")
+    ws = torch.full((max(mx.mxfp4_route_workspace_bytes(T, k, E), 16),), 0x5A,
+                    dtype=torch.uint8, device="cuda")
+    mx.mxfp4_moe_route(torch.from_numpy(ids).cuda().view(T, k), E, ws, g[:E + 1],
+                       dest[:T * k].view(T, k), rows[:T * k] if with_rows else None, st)
+    torch.cuda.synchronize()
+    rc, off_o, dest_o, rows_o = oracle.moe_route(ids, E)
+    off_g, dest_g, rows_g = g.cpu().numpy(), dest.cpu().numpy(), rows.cpu().numpy()
+    assert int(st.item()) == rc, (T, k, E)
+    assert np.array_equal(off_g[:E + 1], off_o) and (off_g[E + 1:] == -5).all()
+    assert np.array_equal(dest_g[:T * k].reshape(T, k), dest_o) and (dest_g[T * k:] == -5).all()
+    n = int(off_o[-1])
+    if with_rows:
+        assert np.array_equal(rows_g[:n], rows_o) and (rows_g[n:] == -5).all()
+    else:
+        assert (rows_g == -5).all()
