@@ -215,3 +215,48 @@ def test_fuzz_route(mx, seed):
         assert np.array_equal(rows_g[:n], rows_o) and (rows_g[n:] == -5).all()
     else:
         assert (rows_g == -5).all()
+
+
+@pytest.mark.parametrize("seed", range(6 * SCALE))
+def test_fuzz_swap_w13(mx, seed):
+    """Random swaps: experts, 2N (even), K, flat or tiled scales, each bias
+    present or absent (the w13 bias with non-finite and tie-rounding values);
+    every output byte against the oracle, guard bytes after each output
+    untouched."""
+    rng = np.random.default_rng(1300 + seed)
+    E = int(rng.integers(1, 9))
+    two_n = 2 * int(rng.integers(1, 160))
+    K = 32 * int(rng.integers(1, 70))
+    tiled = int(seed % 2)
+    codes = rng.integers(0, 256, (E, two_n, K // 2), dtype=np.uint16).astype(np.uint8)
+    flat = rng.integers(0, 256, (E, two_n, K // 32), dtype=np.uint16).astype(np.uint8)
+    scales = np.concatenate([oracle.tile(flat[e]) for e in range(E)]) if tiled else flat
+    b13 = rng.standard_normal((E, two_n)).astype(np.float32) if seed % 3 != 1 else None
+    if b13 is not None:
+        b13.flat[0] = np.inf
+        b13.flat[-1] = np.float32(1.0 + 2.0 ** -8)          # a BF16 tie: rounds to even
+    b2 = rng.standard_normal(int(rng.integers(1, 3000))).astype(np.float32) if seed % 3 != 2 else None
+    want = oracle.swap_w13(codes, scales, b13, E, two_n, K, tiled, b2)
+    G = 64
+    c_out = torch.full((codes.size + G,), 0xA5, dtype=torch.uint8, device="cuda")
+    s_out = torch.full((scales.size + G,), 0xA5, dtype=torch.uint8, device="cuda")
+    b13_out = torch.full((E * two_n + G,), 0x7E7E, dtype=torch.int16, device="cuda")
+    b2_out = torch.full(((b2.size if b2 is not None else 0) + G,), 0x7E7E, dtype=torch.int16,
+                        device="cuda")
+    mx.mxfp4_swap_w13(torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda(),
+                      torch.from_numpy(b13).cuda() if b13 is not None else None,
+                      E, two_n, K, tiled, c_out[:codes.size], s_out[:scales.size],
+                      b13_out[:E * two_n].view(torch.bfloat16) if b13 is not None else None,
+                      torch.from_numpy(b2).cuda() if b2 is not None else None,
+                      b2_out[:b2.size].view(torch.bfloat16) if b2 is not None else None)
+    torch.cuda.synchronize()
+    c, s = c_out.cpu().numpy(), s_out.cpu().numpy()
+    assert np.array_equal(c[:codes.size], want[0].reshape(-1)) and (c[codes.size:] == 0xA5).all()
+    assert np.array_equal(s[:scales.size], want[1].reshape(-1)) and (s[scales.size:] == 0xA5).all()
+    b13g = b13_out.cpu().numpy().view(np.uint16)
+    if b13 is not None:
+        assert np.array_equal(b13g[:E * two_n], want[2].reshape(-1))
+    assert (b13g[E * two_n if b13 is not None else 0:] == 0x7E7E).all()
+    if b2 is not None:
+        b2g = b2_out.cpu().numpy().view(np.uint16)
+        assert np.array_equal(b2g[:b2.size], want[3].reshape(-1)) and (b2g[b2.size:] == 0x7E7E).all()
