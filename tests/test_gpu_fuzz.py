@@ -163,9 +163,16 @@ def test_fuzz_nvfp4(mx, seed):
     f16 = bool(seed % 2 == 1)
     x = _place(_random_x(rng, M, K, f16), rng)
     g = float(np.float32(448.0 * 6.0 / np.exp(rng.uniform(-3, 8))))
-    c, s = mx.quantize_nvfp4(x, torch.tensor([g], device="cuda"))
+    g_t = torch.tensor([g], device="cuda")
+    c, s = mx.quantize_nvfp4(x, g_t)
     c_o, s_o = oracle.nvfp4_quantize(_bits(x), g, f16=f16)
     assert np.array_equal(c.cpu().numpy(), c_o) and np.array_equal(s.cpu().numpy(), s_o)
+    # its dequantize, into a 32-byte (wide kernel) or a 16-byte aligned output
+    flat = torch.full((M * K + 16,), 7.0, dtype=torch.bfloat16, device="cuda")
+    y = flat[8 * (seed % 2):][:M * K].view(M, K)
+    mx.mxfp4_dequantize_nvfp4(c, s, g_t, M, K, y)
+    y_o = oracle.nvfp4_dequantize(c_o, s_o, M, K, g)
+    assert np.array_equal(_bits(y), y_o)
     if M > 1 and x.is_contiguous() and x.data_ptr() % 16 == 0:
         E = int(rng.integers(1, 9))
         off = _random_offsets(rng, E, M)
