@@ -56,7 +56,10 @@ def test_fuzz_dense(mx, seed):
     c_o, s_o = (oracle.quantize_f16 if f16 else oracle.quantize)(_bits(x))
     assert np.array_equal(c.cpu().numpy(), c_o) and np.array_equal(s.cpu().numpy(), s_o), (M, K)
     if not f16:
-        y = mx.dequantize(c, s, M, K)
+        # into a 32-byte (wide kernel) or a 16-byte aligned output (narrow kernel)
+        flat = torch.full((M * K + 16,), 7.0, dtype=torch.bfloat16, device="cuda")
+        y = flat[8 * (seed % 2):][:M * K].view(M, K)
+        mx.mxfp4_dequantize(c, s, M, K, y)
         assert np.array_equal(_bits(y), oracle.dequantize(c_o, s_o, M, K))
 
 
