@@ -942,6 +942,79 @@ def test_cuda_graph_capture_and_replay(mx):
         assert np.array_equal(bits(y), oracle.dequantize(c_o, s_o, M, K))
 
 
+
+def test_cuda_graph_of_the_moe_path(mx):
+    """Routing, the staged MXFP4 scatter, the gather through a workspace and
+    the staged NVFP4 scatter captured in one CUDA graph (memsets and
+    programmatic dependent launches included), then replayed on new token
+    values and new expert ids: every output against the oracle, so no
+    decision of the calls depends on the contents seen at capture time."""
+    T, k, E, K = 512, 4, 16, 512
+    total = T * k
+    ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    x = torch.empty((T, K), dtype=torch.bfloat16, device="cuda")
+    gs = torch.empty(E, dtype=torch.float32, device="cuda")
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    dest = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    rows = torch.empty(total, dtype=torch.int32, device="cuda")
+    st = [torch.empty(1, dtype=torch.int32, device="cuda") for _ in range(4)]
+    u8 = lambda n: torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")  # noqa: E731
+    r_ws = u8(mx.mxfp4_route_workspace_bytes(T, k, E))
+    s_ws = u8(mx.mxfp4_scatter_workspace_bytes(T, total, E, K))
+    g_ws = u8(mx.mxfp4_gather_workspace_bytes(T, total, E, K))
+    n_ws = u8(mx.mxfp4_nvfp4_scatter_workspace_bytes(total, E, K))
+    bound, nv_bound = (mx.mxfp4_grouped_scale_bytes_bound(total, E, K),
+                       mx.mxfp4_nvfp4_grouped_scale_bytes_bound(total, E, K))
+    c1, s1, c2, s2 = u8(total * K // 2).view(-1)[:total * K // 2], u8(bound), \
+        u8(total * K // 2).view(-1)[:total * K // 2], u8(bound)
+    c3, s3 = u8(total * K // 2).view(-1)[:total * K // 2], u8(nv_bound)
+    sro = [torch.empty(E + 1, dtype=torch.int32, device="cuda") for _ in range(3)]
+
+    def path():
+        mx.mxfp4_moe_route(ids, E, r_ws, off, dest, rows, st[0])
+        mx.mxfp4_quantize_grouped_scatter_ws(x, dest, off, total, s_ws, c1, s1, sro[0], st[1])
+        mx.mxfp4_quantize_grouped_gather_ws(x, rows, off, g_ws, c2, s2, sro[1], st[2])
+        mx.mxfp4_quantize_nvfp4_grouped_scatter_ws(x, dest, off, total, gs, n_ws, c3, s3, sro[2],
+                                                   st[3])
+
+    def fill(seed):
+        rng = np.random.default_rng(seed)
+        ids.copy_(torch.from_numpy(rng.integers(0, E, (T, k)).astype(np.int32)))
+        x.copy_(W.dense_activation(seed, T, K, device="cuda"))
+        gs.copy_(torch.from_numpy((448.0 * 6.0 / np.exp(rng.uniform(-2, 6, E))).astype(np.float32)))
+
+    fill(70)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):                    # warm-up outside the capture
+        path()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        path()
+    for seed in (71, 72):
+        fill(seed)
+        graph.replay()
+        torch.cuda.synchronize()
+        ids_h, xb, g_h = ids.cpu().numpy(), bits(x), gs.cpu().numpy()
+        rc, off_o, dest_o, rows_o = oracle.moe_route(ids_h, E)
+        assert rc == 0 and [int(t.item()) for t in st] == [0, 0, 0, 0]
+        assert np.array_equal(off.cpu().numpy(), off_o)
+        assert np.array_equal(dest.cpu().numpy(), dest_o)
+        assert np.array_equal(rows.cpu().numpy(), rows_o)
+        rc, c_o, s_o, sro_o = oracle.quantize_grouped_scatter(xb, dest_o, off_o, total)
+        used = int(sro_o[-1]) * ((K // 32 + 3) // 4 * 4)
+        assert rc == 0 and np.array_equal(sro[0].cpu().numpy(), sro_o)
+        for c, sc in ((c1, s1), (c2, s2)):           # the scatter and the gather
+            assert np.array_equal(c.cpu().numpy().reshape(c_o.shape), c_o)
+            assert np.array_equal(sc[:used].cpu().numpy(), s_o[:used])
+        rc, c_o, s_o, sro_o = oracle.nvfp4_quantize_grouped_scatter(xb, dest_o, off_o, total, g_h)
+        used = int(sro_o[-1]) * ((K // 16 + 3) // 4 * 4)
+        assert rc == 0 and np.array_equal(sro[2].cpu().numpy(), sro_o)
+        assert np.array_equal(c3.cpu().numpy().reshape(c_o.shape), c_o)
+        assert np.array_equal(s3[:used].cpu().numpy(), s_o[:used])
+
 def test_more_than_4gib_input(mx):
     """33000 x 65536 BF16 (4.3 GB): byte offsets beyond 2^32; the first and
     last 128-row tiles (and one in the middle) checked against the oracle."""
