@@ -1015,6 +1015,51 @@ def test_cuda_graph_of_the_moe_path(mx):
         assert np.array_equal(c3.cpu().numpy().reshape(c_o.shape), c_o)
         assert np.array_equal(s3[:used].cpu().numpy(), s_o[:used])
 
+
+def test_calls_on_concurrent_streams(mx):
+    """The library keeps no state between calls (the no-allocation gather's
+    fixed scratch excepted): the dense quantize and dequantize on one stream
+    and the routing plus staged scatter on another, enqueued interleaved and
+    running at the same time, give the oracle's bytes."""
+    M, K = 2048, 2048
+    T, k, E = 1024, 8, 32
+    total = T * k
+    xa = W.dense_activation(81, M, K, device="cuda")
+    xb = W.dense_activation(82, T, K, device="cuda")
+    rng = np.random.default_rng(83)
+    ids = torch.from_numpy(rng.integers(0, E, (T, k)).astype(np.int32)).cuda()
+    ca = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    sa = torch.empty(mx.mxfp4_scale_bytes(M, K), dtype=torch.uint8, device="cuda")
+    ya = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    ws_r = torch.empty(mx.mxfp4_route_workspace_bytes(T, k, E), dtype=torch.uint8, device="cuda")
+    ws_s = torch.empty(mx.mxfp4_scatter_workspace_bytes(T, total, E, K), dtype=torch.uint8,
+                       device="cuda")
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    dest = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    cb = torch.empty((total, K // 2), dtype=torch.uint8, device="cuda")
+    sb = torch.empty(mx.mxfp4_grouped_scale_bytes_bound(total, E, K), dtype=torch.uint8,
+                     device="cuda")
+    sro = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    st = torch.empty(1, dtype=torch.int32, device="cuda")
+    s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
+    s_a.wait_stream(torch.cuda.current_stream())
+    s_b.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):
+        mx.mxfp4_quantize(xa, ca, sa, s_a)
+        mx.mxfp4_moe_route(ids, E, ws_r, off, dest, None, None, s_b)
+        mx.mxfp4_dequantize(ca, sa, M, K, ya, s_a)
+        mx.mxfp4_quantize_grouped_scatter_ws(xb, dest, off, total, ws_s, cb, sb, sro, st, s_b)
+    torch.cuda.synchronize()
+    c_o, s_o = oracle.quantize(bits(xa))
+    assert np.array_equal(ca.cpu().numpy(), c_o) and np.array_equal(sa.cpu().numpy(), s_o)
+    assert np.array_equal(bits(ya), oracle.dequantize(c_o, s_o, M, K))
+    rc, off_o, dest_o, _ = oracle.moe_route(ids.cpu().numpy(), E)
+    assert rc == 0 and np.array_equal(dest.cpu().numpy(), dest_o)
+    rc, cq, sq, sro_o = oracle.quantize_grouped_scatter(bits(xb), dest_o, off_o, total)
+    used = int(sro_o[-1]) * ((K // 32 + 3) // 4 * 4)
+    assert rc == 0 and int(st.item()) == 0
+    assert np.array_equal(cb.cpu().numpy(), cq) and np.array_equal(sb[:used].cpu().numpy(), sq[:used])
+
 def test_more_than_4gib_input(mx):
     """33000 x 65536 BF16 (4.3 GB): byte offsets beyond 2^32; the first and
     last 128-row tiles (and one in the middle) checked against the oracle."""
