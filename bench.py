@@ -816,6 +816,46 @@ def run_one_call(args):
                       "us_per_call": round(t0.elapsed_time(t1) * 1e3 / args.reps, 2)}))
 
 
+def run_sweep(args):
+    """--sweep: the dense quantize (BF16, K = 7168 and K = 2048) over a range of
+    row counts, one JSON line per size: device time per call from CUDA-graph
+    batches of back-to-back calls after an L2 sweep, the inputs and outputs
+    rotated over enough sets that together they exceed twice the L2, so no
+    call finds its operands there.  Shows where the kernel leaves the launch
+    and latency regime and reaches the copy bandwidth."""
+    import torch
+    import mxfp4_block_quantization_gb300 as mx
+    import workloads as W
+    torch.cuda.set_device(0)
+    peak, _ = hbm_peak()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    sweep = L2Sweep(l2)
+    side = torch.cuda.Stream()
+    torch.cuda.set_stream(side)
+    for K in (7168, 2048):
+        for M in (128, 512, 1024, 2048, 4096, 8192, 16384, 65536):
+            nb = quant_bytes(M, K)
+            R = max(2, -(-2 * l2 // nb) + 1)
+            x = W.dense_activation(1, M, K, device="cuda")
+            xs = [x] + [x.clone() for _ in range(R - 1)]
+            cs = [torch.empty((M, K // 2), dtype=torch.uint8, device="cuda") for _ in range(R)]
+            ss = [torch.empty(mx.mxfp4_scale_bytes(M, K), dtype=torch.uint8, device="cuda")
+                  for _ in range(R)]
+            per = max(R, min(200, -(-(1 << 30) // nb)))
+            mean, med = time_graph_batches(
+                lambda i: mx.mxfp4_quantize(xs[i % R], cs[i % R], ss[i % R], side), side, sweep,
+                per, 5)
+            gbs = nb / (mean * 1e-3) / 1e9
+            print(json.dumps({"sweep": "dense quantize", "M": M, "K": K, "ctas":
+                              ((M + 127) // 128) * ((K // 32 + 3) // 4), "us": round(mean * 1e3, 2),
+                              "median_us": round(med * 1e3, 2), "GB_per_s": round(gbs, 1),
+                              "frac_of_peak": round(gbs / peak, 4), "rotating_sets": R}),
+                  flush=True)
+            del xs, cs, ss, x
+            torch.cuda.empty_cache()
+    return 0
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -1058,6 +1098,8 @@ def main(argv=None):
     ap.add_argument("--call", choices=SINGLE_CALLS,
                     help="only time this one call (for profiling)")
     ap.add_argument("--reps", type=int, default=5, help="repetitions of --call")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the dense quantize over a range of sizes, one JSON line each")
     ap.add_argument("--e2e-chunks", type=int, default=4, choices=(1, 2, 4, 8, 16, 32),
                     help="row chunks per step of the pipelined e2e measurement")
     ap.add_argument("--settle", type=float, default=1.0,
@@ -1069,6 +1111,8 @@ def main(argv=None):
         return run_reference(args)
     if args.call:
         return run_one_call(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 
