@@ -1081,6 +1081,50 @@ def test_more_than_4gib_input(mx):
     torch.cuda.empty_cache()
 
 
+
+def test_grouped_and_scatter_beyond_4gib(mx):
+    """The grouped quantize and the staged scatter over a 33000 x 65536 BF16
+    batch (4.3 GB; row byte offsets past 2^32) in five uneven segments, one
+    empty: the first and last 128-row tiles of the first and last segments
+    against the oracle (the scatter's rows through a random permutation of
+    the tokens)."""
+    M, K = 33000, 65536
+    x = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    for r0 in range(0, M, 4096):
+        r1 = min(M, r0 + 4096)
+        x[r0:r1] = W.normal_bf16((r1 - r0, K), seed=r0 + 7, device="cuda")
+    off_h = np.array([0, 7000, 7000, 20000, 26001, M], dtype=np.int32)
+    off = torch.from_numpy(off_h).cuda()
+    E = off_h.size - 1
+    per_tile = mx.mxfp4_scale_bytes(128, K)
+
+    def check(codes, scales, sro, rows_of):
+        for e in (0, E - 1):
+            n = int(off_h[e + 1] - off_h[e])
+            for t in (0, (n - 1) // 128):
+                r0 = int(off_h[e]) + 128 * t
+                r1 = min(int(off_h[e + 1]), r0 + 128)
+                c_o, s_o = oracle.quantize(bits(x[rows_of(r0, r1)]))
+                assert np.array_equal(codes[r0:r1].cpu().numpy(), c_o), (e, t)
+                c0 = (int(sro[e]) // 128 + t) * per_tile
+                assert np.array_equal(scales[c0:c0 + per_tile].cpu().numpy(), s_o), (e, t)
+
+    codes, scales, sro, st = mx.quantize_grouped(x, off)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    check(codes, scales, sro.cpu().numpy(), lambda r0, r1: slice(r0, r1))
+    del codes, scales
+    perm = torch.randperm(M, generator=torch.Generator().manual_seed(5)).to(torch.int32)
+    dest = perm.view(M, 1).cuda()                   # token t -> row perm[t]
+    inv = torch.empty_like(perm)
+    inv[perm.long()] = torch.arange(M, dtype=torch.int32)
+    codes, scales, sro, st = mx.quantize_grouped_scatter(x, dest, off)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    check(codes, scales, sro.cpu().numpy(), lambda r0, r1: inv[r0:r1].long().cuda())
+    del x, codes, scales
+    torch.cuda.empty_cache()
+
 def test_grouped_many_skewed_experts(mx):
     """3000 experts (the offsets scan spans three 1024-wide chunks) with
     Zipf-like segment sizes, many empty: the segment estimate misses and the
