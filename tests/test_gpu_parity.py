@@ -1083,11 +1083,12 @@ def test_more_than_4gib_input(mx):
 
 
 def test_grouped_and_scatter_beyond_4gib(mx):
-    """The grouped quantize and the staged scatter over a 33000 x 65536 BF16
-    batch (4.3 GB; row byte offsets past 2^32) in five uneven segments, one
-    empty: the first and last 128-row tiles of the first and last segments
-    against the oracle (the scatter's rows through a random permutation of
-    the tokens)."""
+    """The grouped quantize, the staged scatter, the gather and the NVFP4
+    experts quant over a 33000 x 65536 BF16 batch (4.3 GB; row byte offsets
+    past 2^32) in five uneven segments, one empty: the first and last 128-row
+    tiles of the first and last segments against the oracle (the scatter's
+    rows through a random permutation of the tokens; the gather of the same
+    rows equal to the scatter)."""
     M, K = 33000, 65536
     x = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
     for r0 in range(0, M, 4096):
@@ -1122,6 +1123,29 @@ def test_grouped_and_scatter_beyond_4gib(mx):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     check(codes, scales, sro.cpu().numpy(), lambda r0, r1: inv[r0:r1].long().cuda())
+    # the same rows as a gather (row -> token), which must equal the scatter
+    codes_g, scales_g, sro_g, st = mx.quantize_grouped_gather(x, inv.cuda(), off)
+    torch.cuda.synchronize()
+    used = int(sro[-1]) * ((K // 32 + 3) // 4 * 4)
+    assert int(st.item()) == 0 and torch.equal(sro_g, sro)
+    assert torch.equal(codes_g, codes) and torch.equal(scales_g[:used], scales[:used])
+    del codes, scales, codes_g, scales_g
+    # the NVFP4 experts quant, a global scale per expert
+    gs = torch.tensor([448.0 * 6.0 / v for v in (3.0, 5.0, 7.0, 4.0, 6.0)], device="cuda")
+    codes, scales, sro, st = mx.quantize_nvfp4_grouped(x, off, gs)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    per_tile = mx.mxfp4_nvfp4_scale_bytes(128, K)
+    sro_h = sro.cpu().numpy()
+    for e in (0, E - 1):
+        n = int(off_h[e + 1] - off_h[e])
+        for t in (0, (n - 1) // 128):
+            r0 = int(off_h[e]) + 128 * t
+            r1 = min(int(off_h[e + 1]), r0 + 128)
+            c_o, s_o = oracle.nvfp4_quantize(bits(x[r0:r1]), float(gs[e]))
+            assert np.array_equal(codes[r0:r1].cpu().numpy(), c_o), (e, t)
+            c0 = (int(sro_h[e]) // 128 + t) * per_tile
+            assert np.array_equal(scales[c0:c0 + per_tile].cpu().numpy(), s_o), (e, t)
     del x, codes, scales
     torch.cuda.empty_cache()
 
