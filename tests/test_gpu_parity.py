@@ -1062,7 +1062,8 @@ def test_calls_on_concurrent_streams(mx):
 
 def test_more_than_4gib_input(mx):
     """33000 x 65536 BF16 (4.3 GB): byte offsets beyond 2^32; the first and
-    last 128-row tiles (and one in the middle) checked against the oracle."""
+    last 128-row tiles (and one in the middle) checked against the oracle,
+    then the same tiles of its dequantize (a 4.3 GB output)."""
     M, K = 33000, 65536
     x = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
     for r0 in range(0, M, 4096):
@@ -1077,9 +1078,19 @@ def test_more_than_4gib_input(mx):
         c_o, s_o = oracle.quantize(bits(x[r0:r1]))
         assert np.array_equal(codes[r0:r1].cpu().numpy(), c_o), t
         assert np.array_equal(scales[t * per_tile:(t + 1) * per_tile].cpu().numpy(), s_o), t
-    del x, codes, scales
+    # and its dequantize: a 4.3 GB BF16 output, the same tiles against the oracle
+    del x
     torch.cuda.empty_cache()
-
+    y = mx.dequantize(codes, scales, M, K)
+    torch.cuda.synchronize()
+    for t in (0, 128, (M - 1) // 128):
+        r0 = t * 128
+        r1 = min(M, r0 + 128)
+        c_t = codes[r0:r1].cpu().numpy()
+        s_t = scales[t * per_tile:(t + 1) * per_tile].cpu().numpy()
+        assert np.array_equal(bits(y[r0:r1]), oracle.dequantize(c_t, s_t, r1 - r0, K)), t
+    del y, codes, scales
+    torch.cuda.empty_cache()
 
 
 def test_grouped_and_scatter_beyond_4gib(mx):
