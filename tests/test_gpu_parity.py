@@ -1094,8 +1094,8 @@ def test_more_than_4gib_input(mx):
 
 
 def test_grouped_and_scatter_beyond_4gib(mx):
-    """The grouped quantize, the staged scatter, the gather and the NVFP4
-    experts quant over a 33000 x 65536 BF16 batch (4.3 GB; row byte offsets
+    """The grouped quantize, the staged scatter, the gather, the NVFP4 experts
+    quant and its staged scatter over a 33000 x 65536 BF16 batch (4.3 GB; row byte offsets
     past 2^32) in five uneven segments, one empty: the first and last 128-row
     tiles of the first and last segments against the oracle (the scatter's
     rows through a random permutation of the tokens; the gather of the same
@@ -1154,6 +1154,21 @@ def test_grouped_and_scatter_beyond_4gib(mx):
             r0 = int(off_h[e]) + 128 * t
             r1 = min(int(off_h[e + 1]), r0 + 128)
             c_o, s_o = oracle.nvfp4_quantize(bits(x[r0:r1]), float(gs[e]))
+            assert np.array_equal(codes[r0:r1].cpu().numpy(), c_o), (e, t)
+            c0 = (int(sro_h[e]) // 128 + t) * per_tile
+            assert np.array_equal(scales[c0:c0 + per_tile].cpu().numpy(), s_o), (e, t)
+    del codes, scales
+    # and the staged NVFP4 scatter through the permutation
+    codes, scales, sro, st = mx.quantize_nvfp4_grouped_scatter(x, dest, off, gs)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    sro_h = sro.cpu().numpy()
+    for e in (0, E - 1):
+        n = int(off_h[e + 1] - off_h[e])
+        for t in (0, (n - 1) // 128):
+            r0 = int(off_h[e]) + 128 * t
+            r1 = min(int(off_h[e + 1]), r0 + 128)
+            c_o, s_o = oracle.nvfp4_quantize(bits(x[inv[r0:r1].long().cuda()]), float(gs[e]))
             assert np.array_equal(codes[r0:r1].cpu().numpy(), c_o), (e, t)
             c0 = (int(sro_h[e]) // 128 + t) * per_tile
             assert np.array_equal(scales[c0:c0 + per_tile].cpu().numpy(), s_o), (e, t)
