@@ -65,8 +65,10 @@ typedef enum {
 
 /* Bytes of the 128x4-tiled scale buffer of an [M, K] matrix:
  * ceil(M/128)*128 * ceil((K/32)/4)*4.  Every byte of that range is written by
- * the quantizers (pad bytes as 0x00).  Returns 0 when M <= 0, K <= 0 or
- * K % 32 != 0.  [PR43557] untile_cutlass_scale (padded_M x padded_sK). */
+ * the quantizers (pad bytes as 0x00).  Returns 0 when M <= 0, K <= 0,
+ * K % 32 != 0 or the byte count would not fit in int64 (sizes no call
+ * accepts).  [PR43557] untile_cutlass_scale (padded_M x padded_sK).  Every
+ * size query of this header answers 0 in that last case too. */
 size_t mxfp4_scale_bytes(int64_t M, int64_t K);
 
 /* Upper bound of the grouped scale buffer for `total_rows` rows split into E
