@@ -276,9 +276,7 @@ __global__ void __launch_bounds__(kScanThreads) grouped_offsets_kernel(const Off
   const int64_t total_rows = q.total_rows;
   int32_t* __restrict__ padded = q.padded;
   int32_t* __restrict__ status = q.status;
-  __shared__ int s_bad;
   __shared__ int64_t s_warp[kScanThreads / 32];
-  __shared__ int64_t s_carry;
   pdl_wait();
   pdl_release();
   // every index below lies in [0, E]
@@ -287,17 +285,16 @@ __global__ void __launch_bounds__(kScanThreads) grouped_offsets_kernel(const Off
       (status != nullptr && !MXFP4_IN_BOUNDS(q, kDbgStatus, status, 4)))
     return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    s_bad = (off[0] != 0) || (static_cast<int64_t>(off[E]) != total_rows);
-    s_carry = 0;
-  }
-  __syncthreads();
+  // every thread's loads are in flight at once: the first and last offsets
+  // are checked by the threads that load them anyway
+  bool bad = E == 0 && (off[0] != 0 || static_cast<int64_t>(off[0]) != total_rows);
+  int64_t carry = 0;  // the same in every thread
   for (int base = 0; base < E; base += kScanThreads) {
     const int e = base + tid;
     int64_t cnt = 0;
     if (e < E) {
       const int64_t a = off[e], b = off[e + 1];
-      if (b < a) atomicOr(&s_bad, 1);
+      if (b < a || (e == 0 && a != 0) || (e == E - 1 && b != total_rows)) bad = true;
       else cnt = (b - a + kTileRows - 1) / kTileRows * kTileRows;
     }
     int64_t inc = cnt;  // inclusive warp scan
@@ -318,18 +315,18 @@ __global__ void __launch_bounds__(kScanThreads) grouped_offsets_kernel(const Off
       s_warp[lane] = w;  // inclusive over warps
     }
     __syncthreads();
-    const int64_t before = s_carry + (warp > 0 ? s_warp[warp - 1] : 0) + inc - cnt;
+    const int64_t before = carry + (warp > 0 ? s_warp[warp - 1] : 0) + inc - cnt;
     if (e < E) padded[e] = static_cast<int32_t>(before);
-    __syncthreads();
-    if (tid == 0) s_carry += s_warp[kScanThreads / 32 - 1];
-    __syncthreads();
+    carry += s_warp[kScanThreads / 32 - 1];
+    __syncthreads();  // s_warp is rewritten by the next chunk
   }
-  if (tid == 0) padded[E] = static_cast<int32_t>(s_carry);
+  const bool any_bad = __syncthreads_or(bad) != 0;
+  if (tid == 0) padded[E] = static_cast<int32_t>(carry);
   __syncthreads();
-  if (s_bad) {
+  if (any_bad) {
     for (int e = tid; e <= E; e += kScanThreads) padded[e] = -1;
   }
-  if (tid == 0 && status != nullptr) *status = s_bad ? MXFP4_EOFFSETS : MXFP4_OK;
+  if (tid == 0 && status != nullptr) *status = any_bad ? MXFP4_EOFFSETS : MXFP4_OK;
 }
 
 
